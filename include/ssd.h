@@ -1,0 +1,179 @@
+/*
+ * ssd.h -- C ABI of libssd.so, the GB300 (sm_103a) Mamba-2 SSD chunked scan.
+ *
+ * The operation (Mamba-2 state-space duality; the recurrence of the Mamba-3-Lite
+ * "SSD Reference" page, section "Math: the recurrence both functions implement",
+ * with the dt factor on the input, a D skip, an optional silu(z) gate and
+ * initial/final states):
+ *
+ *   dt_t  = softplus(dt_raw_t + dt_bias_h)                     per token and head
+ *   h_t   = exp(dt_t * A_h) * h_{t-1} + dt_t * x_t (outer) B_t    state [P][N] per head
+ *   y_t   = (C_t . h_t + D_h * x_t) * silu(z_t)                 (gate only when z is given)
+ *
+ * Head h reads B/C group g = h / (H / G) (H must be a multiple of G).
+ * h_{-1} is the initial state (zero when absent); the final state is h after the
+ * last token of each sequence.
+ *
+ * The scan is evaluated in chunks (the chunkwise decomposition of that page's
+ * section "ssd_complex_chunkwise -- the production scan": in-chunk cumulative
+ * log-decay, intra-chunk segment-sum matrix, per-chunk states, carried chunk
+ * states).  The chunk length only changes the association of the arithmetic,
+ * never the function: the library uses its own internal chunk length (128 on
+ * the tensor-core path, 64 on the SIMT path) and accepts any power-of-two
+ * `chunk_size` in [16, 256] as a hint.
+ *
+ * ---------------------------------------------------------------------------
+ * Ownership and execution contract (all entry points)
+ *   - The caller owns every buffer: inputs, outputs and the workspace.  The
+ *     library never allocates, frees or synchronises (except ssd_query_status),
+ *     keeps no per-call state outside the workspace, and enqueues all work on
+ *     the given stream (a cudaStream_t passed as void*; NULL = legacy stream).
+ *   - Pointers in ssd_tensor are DEVICE pointers on the current device.
+ *   - Validation runs on the host before any launch; a non-OK return means
+ *     nothing was enqueued.  Errors found on the device (bad cu_seqlens
+ *     contents, a bounded wait that expired) are written to a status word in the
+ *     workspace and read back with ssd_query_status().
+ *   - Two calls may share a workspace only if they are ordered on one stream.
+ *
+ * Tensor conventions (element strides, outermost first, innermost stride 1):
+ *   x, z, y, dy, dx, dz : [batch, seqlen, nheads, headdim]        bf16 or f32
+ *   B, C, dB, dC        : [batch, seqlen, ngroups, dstate]        same dtype as x
+ *   dt, ddt             : [batch, seqlen, nheads]                 f32
+ *   A, D, dt_bias, dA, dD, ddt_bias : [nheads], contiguous        f32
+ *   initial_states, final_states, dfinal_states, dinitial_states :
+ *                         [nstate, nheads, headdim, dstate], contiguous, f32
+ *                         (nstate = batch, or nseqs with cu_seqlens)
+ *   cu_seqlens          : int32 [nseqs + 1] device array, batch must be 1;
+ *                         cu[0] = 0, non-decreasing, cu[nseqs] = seqlen.
+ *                         Sequence s is tokens [cu[s], cu[s+1]) of row 0; its
+ *                         scan starts from initial_states[s] and ends in
+ *                         final_states[s]; sequences never interact.
+ * ---------------------------------------------------------------------------
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_ABI_VERSION 1
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARGUMENT = 1,   /* bad shape, stride, dtype mix, NULL required pointer, bad cu_seqlens */
+    SSD_ERR_UNSUPPORTED = 2,        /* valid but outside the compiled set (headdim/dstate/chunk/algo) */
+    SSD_ERR_MISALIGNED = 3,         /* a pointer or stride breaks the 16-byte rule of the TMA path */
+    SSD_ERR_WORKSPACE_TOO_SMALL = 4,
+    SSD_ERR_CUDA = 5,               /* a CUDA runtime call or a launch failed */
+    SSD_ERR_DEVICE_TIMEOUT = 6      /* a bounded inter-CTA wait expired (device-side, via ssd_query_status) */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Which forward/backward pipeline to run.  AUTO takes the tensor-core path when
+ * the inputs are bf16 and headdim == 64, dstate == 128 (the compiled tile set),
+ * and the SIMT path otherwise (f32 inputs always take SIMT: fp32 inputs are
+ * computed in fp32 FMA, never in tf32). */
+typedef enum {
+    SSD_ALGO_AUTO = 0,
+    SSD_ALGO_STAGED = 1,   /* SIMT, one kernel per step: cumsum, chunk_state, state_passing, chunk_scan */
+    SSD_ALGO_FUSED = 2     /* tcgen05/TMA single-pass forward; tcgen05 backward */
+} ssd_algo;
+
+typedef struct {
+    void *ptr;          /* device pointer; NULL marks an absent optional tensor */
+    int32_t dtype;      /* ssd_dtype */
+    int32_t reserved;
+    int64_t stride[4];  /* element strides, outermost first; entries past the rank are ignored */
+} ssd_tensor;
+
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs;
+    int32_t algo;        /* ssd_algo */
+    int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..16 */
+} ssd_problem;
+
+typedef struct {
+    ssd_tensor x, dt, A, B, C, D, z, dt_bias, initial_states;   /* inputs; D, z, dt_bias, initial_states optional */
+    ssd_tensor y, final_states;                                 /* outputs; final_states optional */
+    const int32_t *cu_seqlens;                                  /* optional device array (see above) */
+} ssd_fwd_args;
+
+typedef struct {
+    ssd_fwd_args fwd;                 /* the forward's inputs (its y/final_states are ignored) */
+    ssd_tensor dy, dfinal_states;     /* upstream gradients; dfinal_states optional (zero) */
+    ssd_tensor dx, ddt, dA, dB, dC;   /* required outputs */
+    ssd_tensor dD, dz, ddt_bias, dinitial_states;   /* required iff the matching input is given */
+} ssd_bwd_args;
+
+/*
+ * ssd_fwd_workspace_size / ssd_fwd
+ * Forward scan: y and (optionally) final_states from the inputs.
+ * Defined by the recurrence above; steps: chunk cumsum of dt*A, intra-chunk
+ * C.B^T under the segment-sum decay mask, chunk states, inter-chunk state
+ * passing, chunk output (Mamba-3-Lite "SSD Reference", sections "Chunking and
+ * the discretized log-decay", "Intra-chunk outputs and per-chunk states",
+ * "Inter-chunk propagation -- the fixed contract", "Readout").
+ * Workspace: at least *bytes bytes of device memory, 256-byte aligned, contents
+ * need not be initialised; it is clobbered.
+ * Returns SSD_OK or the first validation error; nothing is enqueued on error.
+ */
+ssd_status ssd_fwd_workspace_size(const ssd_problem *prob, const ssd_fwd_args *args, size_t *bytes);
+ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *args, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * ssd_bwd_workspace_size / ssd_bwd
+ * Gradients of L = sum(dy * y) + sum(dfinal_states * final_states) with respect
+ * to x, dt (the raw input, through softplus), A, B, C, and D, z, dt_bias,
+ * initial_states when given.  dB/dC sum over the heads of each group.  All
+ * reductions run in a fixed order: results are bitwise reproducible.
+ * The forward is recomputed inside (no saved activations are needed).
+ * Same workspace rules as ssd_fwd.
+ */
+ssd_status ssd_bwd_workspace_size(const ssd_problem *prob, const ssd_bwd_args *args, size_t *bytes);
+ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *args, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * ssd_query_status
+ * Synchronises `stream`, then returns the device-side status word of the most
+ * recent ssd_fwd/ssd_bwd call that used `workspace` (SSD_OK,
+ * SSD_ERR_INVALID_ARGUMENT for bad cu_seqlens contents, SSD_ERR_DEVICE_TIMEOUT),
+ * or SSD_ERR_CUDA if the synchronisation or the read fails.
+ */
+ssd_status ssd_query_status(const void *workspace, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *ssd_status_string(ssd_status status);
+
+/* SSD_ABI_VERSION of the built library. */
+int32_t ssd_abi_version(void);
+
+/*
+ * ssd_fwd_debug_layout
+ * Byte offsets, inside an ssd_fwd workspace, of the intermediates the STAGED
+ * forward leaves behind after it completes (for stage-by-stage checks):
+ *   meta_counts : int32[4]  {n_chunks, n_units, n_seqs, status}
+ *   chunk_info  : int32[n_chunks][4] {seq, batch row, first token in row, length}
+ *   dt          : f32[n_chunks][nheads][qi]   softplus(dt_raw + dt_bias), 0 past the chunk's length
+ *   cs          : f32[n_chunks][nheads][qi]   inclusive in-chunk cumulative sum of dt*A
+ *   states      : f32[n_chunks][nheads][headdim][dstate]  carry-in state of each chunk
+ * where qi is the internal chunk length written to *qi.  Chunks are listed
+ * sequence by sequence, in order, each sequence cut into qi-token chunks from its
+ * first token (the last one ragged).  Offsets of -1 mean "not produced by algo".
+ */
+typedef struct {
+    int64_t meta_counts, chunk_info, dt, cs, states;
+    int64_t qi;
+} ssd_debug_layout;
+ssd_status ssd_fwd_debug_layout(const ssd_problem *prob, const ssd_fwd_args *args, ssd_debug_layout *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_GB300_H */

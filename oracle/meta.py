@@ -1,0 +1,42 @@
+"""Plain-Python builder of the chunk and work-unit lists -- TEST INFRASTRUCTURE ONLY.
+
+The bit-exact reference for the library's metadata kernel.  Definition (the
+reading of packed variable-length sequences used throughout: each sequence is
+an independent scan from its own initial state; the chunk grid restarts at every
+sequence's first token, so no chunk mixes two sequences):
+
+* sequence s = tokens [t0, t0+len) of batch row b  (fixed-length batch: s = b,
+  t0 = 0, len = L; packed: b = 0, t0 = cu[s], len = cu[s+1] - cu[s]);
+* its chunks are [t0 + c Q, t0 + min((c+1) Q, len)) for c = 0 .. ceil(len/Q)-1,
+  listed sequence by sequence -> rows (seq, b, first token, length);
+* its work units group R consecutive chunks: unit (s, j) covers chunks
+  j R .. min((j+1) R, nchunks)-1; units are listed by j, then s -> rows
+  (seq, b, first token, token count, chunk count, index of unit (s, j-1) or -1,
+  1 if last unit of s, index of its first chunk).
+"""
+
+
+def build(cu=None, batch=1, seqlen=0, Q=64, R=1):
+    if cu is None:
+        seqs = [(b, 0, seqlen) for b in range(batch)]
+    else:
+        cu = [int(c) for c in cu]
+        seqs = [(0, cu[s], cu[s + 1] - cu[s]) for s in range(len(cu) - 1)]
+    chunks, chunk0 = [], []
+    for s, (b, t0, n) in enumerate(seqs):
+        chunk0.append(len(chunks))
+        nch = -(-n // Q)
+        for c in range(nch):
+            chunks.append((s, b, t0 + c * Q, min(Q, n - c * Q)))
+    units = []
+    last = {}
+    nseg = [-(-(-(-n // Q)) // R) for (_, _, n) in seqs]
+    for j in range(max(nseg) if nseg else 0):
+        for s, (b, t0, n) in enumerate(seqs):
+            if nseg[s] <= j:
+                continue
+            nch = -(-n // Q)
+            units.append((s, b, t0 + j * R * Q, min(R * Q, n - j * R * Q), min(R, nch - j * R),
+                          last.get(s, -1) if j > 0 else -1, 1 if j == nseg[s] - 1 else 0, chunk0[s] + j * R))
+            last[s] = len(units) - 1
+    return dict(seqs=[(b, t0, n, chunk0[s]) for s, (b, t0, n) in enumerate(seqs)], chunks=chunks, units=units)

@@ -1,0 +1,186 @@
+"""ctypes binding of libssd.so (include/ssd.h).
+
+Argument marshalling only: every step of the scan runs in the library's CUDA
+kernels.  Torch is used to own device memory and to supply the current stream;
+nothing here computes any part of the scan.  If libssd.so is missing the calls
+raise -- there is no fallback.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssd.so")
+
+SSD_OK = 0
+STATUS_NAMES = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARGUMENT", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_MISALIGNED",
+                4: "SSD_ERR_WORKSPACE_TOO_SMALL", 5: "SSD_ERR_CUDA", 6: "SSD_ERR_DEVICE_TIMEOUT"}
+SSD_F32, SSD_BF16 = 0, 1
+ALGO = {"auto": 0, "staged": 1, "fused": 2}
+
+# Every symbol include/ssd.h declares.
+EXPORTS = ["ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
+           "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout"]
+
+
+class SSDError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = int(code)
+        super().__init__("%s: %s" % (where, STATUS_NAMES.get(int(code), str(code))))
+
+
+class Tensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("stride", ctypes.c_int64 * 4)]
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("dstate", ctypes.c_int64),
+                ("chunk_size", ctypes.c_int64), ("nseqs", ctypes.c_int64), ("algo", ctypes.c_int32),
+                ("seg_chunks", ctypes.c_int32)]
+
+
+_FWD_FIELDS = ["x", "dt", "A", "B", "C", "D", "z", "dt_bias", "initial_states", "y", "final_states"]
+
+
+class FwdArgs(ctypes.Structure):
+    _fields_ = [(n, Tensor) for n in _FWD_FIELDS] + [("cu_seqlens", ctypes.c_void_p)]
+
+
+_BWD_FIELDS = ["dy", "dfinal_states", "dx", "ddt", "dA", "dB", "dC", "dD", "dz", "ddt_bias", "dinitial_states"]
+
+
+class BwdArgs(ctypes.Structure):
+    _fields_ = [("fwd", FwdArgs)] + [(n, Tensor) for n in _BWD_FIELDS]
+
+
+class DebugLayout(ctypes.Structure):
+    _fields_ = [("meta_counts", ctypes.c_int64), ("chunk_info", ctypes.c_int64), ("dt", ctypes.c_int64),
+                ("cs", ctypes.c_int64), ("states", ctypes.c_int64), ("qi", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libssd.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libssd.so not found at %s: build it with state_space_model_scan_gb300.build.build()" % path)
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    lib.ssd_fwd_workspace_size.argtypes = [P(Problem), P(FwdArgs), P(ctypes.c_size_t)]
+    lib.ssd_fwd.argtypes = [P(Problem), P(FwdArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.ssd_bwd_workspace_size.argtypes = [P(Problem), P(BwdArgs), P(ctypes.c_size_t)]
+    lib.ssd_bwd.argtypes = [P(Problem), P(BwdArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.ssd_query_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.ssd_status_string.argtypes = [ctypes.c_int]
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    lib.ssd_abi_version.restype = ctypes.c_int32
+    lib.ssd_fwd_debug_layout.argtypes = [P(Problem), P(FwdArgs), P(DebugLayout)]
+    for f in ("ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
+              "ssd_fwd_debug_layout"):
+        getattr(lib, f).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def tensor(t, rank=None):
+    """An ssd_tensor for a torch tensor (or an absent one for None)."""
+    out = Tensor()
+    if t is None:
+        return out
+    if t.dtype == torch.bfloat16:
+        out.dtype = SSD_BF16
+    elif t.dtype == torch.float32:
+        out.dtype = SSD_F32
+    else:
+        out.dtype = -1
+    out.ptr = t.data_ptr()
+    st = list(t.stride())
+    for i, s in enumerate(st[:4]):
+        out.stride[i] = s
+    return out
+
+
+def problem(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs=0, algo="auto", seg_chunks=0):
+    return Problem(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs, ALGO[algo], seg_chunks)
+
+
+def fwd_args(x, dt, A, B, C, y, D=None, z=None, dt_bias=None, initial_states=None, final_states=None,
+             cu_seqlens=None):
+    a = FwdArgs()
+    for name, t in dict(x=x, dt=dt, A=A, B=B, C=C, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
+                        y=y, final_states=final_states).items():
+        setattr(a, name, tensor(t))
+    a.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
+    return a
+
+
+def bwd_args(fwd, dy, dx, ddt, dA, dB, dC, dD=None, dz=None, ddt_bias=None, dinitial_states=None,
+             dfinal_states=None):
+    b = BwdArgs()
+    b.fwd = fwd
+    for name, t in dict(dy=dy, dfinal_states=dfinal_states, dx=dx, ddt=ddt, dA=dA, dB=dB, dC=dC, dD=dD, dz=dz,
+                        ddt_bias=ddt_bias, dinitial_states=dinitial_states).items():
+        setattr(b, name, tensor(t))
+    return b
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def check(code, where):
+    if code != SSD_OK:
+        raise SSDError(code, where)
+
+
+def fwd_workspace_size(prob, args):
+    n = ctypes.c_size_t(0)
+    check(load().ssd_fwd_workspace_size(ctypes.byref(prob), ctypes.byref(args), ctypes.byref(n)),
+          "ssd_fwd_workspace_size")
+    return int(n.value)
+
+
+def bwd_workspace_size(prob, args):
+    n = ctypes.c_size_t(0)
+    check(load().ssd_bwd_workspace_size(ctypes.byref(prob), ctypes.byref(args), ctypes.byref(n)),
+          "ssd_bwd_workspace_size")
+    return int(n.value)
+
+
+def ssd_fwd(prob, args, workspace, stream=None):
+    """Raw call: returns the status code (no raise)."""
+    return load().ssd_fwd(ctypes.byref(prob), ctypes.byref(args), ctypes.c_void_p(workspace.data_ptr()),
+                          ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream))
+
+
+def ssd_bwd(prob, args, workspace, stream=None):
+    return load().ssd_bwd(ctypes.byref(prob), ctypes.byref(args), ctypes.c_void_p(workspace.data_ptr()),
+                          ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream))
+
+
+def query_status(workspace, stream=None):
+    return int(load().ssd_query_status(ctypes.c_void_p(workspace.data_ptr()), _stream_handle(stream)))
+
+
+def debug_layout(prob, args):
+    out = DebugLayout()
+    check(load().ssd_fwd_debug_layout(ctypes.byref(prob), ctypes.byref(args), ctypes.byref(out)),
+          "ssd_fwd_debug_layout")
+    return out
+
+
+def status_string(code):
+    return load().ssd_status_string(int(code)).decode()
+
+
+def abi_version():
+    return int(load().ssd_abi_version())

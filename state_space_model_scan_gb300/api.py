@@ -1,0 +1,107 @@
+"""Torch-facing wrappers around the C ABI.
+
+They allocate outputs and workspace with torch, marshal pointers/strides/stream
+into the ABI structs and raise on a non-OK status.  All arithmetic runs in
+libssd.so.
+"""
+import torch
+
+from . import _lib
+
+
+class Workspace:
+    """A reusable device workspace: grows to the largest size requested."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes):
+        nbytes = max(int(nbytes), 256)
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device or "cuda")
+        return self.buf
+
+
+def _nseqs(x, cu_seqlens):
+    return (cu_seqlens.numel() - 1) if cu_seqlens is not None else x.shape[0]
+
+
+def ssd_forward(x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_states=None, cu_seqlens=None,
+                chunk_size=128, return_final_states=True, algo="auto", seg_chunks=0, workspace=None,
+                y=None, final_states=None, stream=None):
+    """y, final_states = SSD scan (see include/ssd.h for the definition and layouts).
+
+    x, z: [B, L, H, P]; dt: [B, L, H] fp32; A, D, dt_bias: [H] fp32; B, C: [B, L, G, N];
+    initial_states: [S, H, P, N] fp32; cu_seqlens: int32 [S+1] (batch 1).
+    """
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    S = _nseqs(x, cu_seqlens)
+    if y is None:
+        y = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    if final_states is None and return_final_states:
+        final_states = torch.empty(S, H, P, N, dtype=torch.float32, device=x.device)
+    prob = _lib.problem(Bsz, L, H, P, G, N, chunk_size, S if cu_seqlens is not None else 0, algo, seg_chunks)
+    args = _lib.fwd_args(x, dt, A, B, C, y, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
+                         final_states=final_states, cu_seqlens=cu_seqlens)
+    nbytes = _lib.fwd_workspace_size(prob, args)
+    ws = workspace.get(nbytes) if workspace is not None else torch.empty(max(nbytes, 256), dtype=torch.uint8,
+                                                                          device=x.device)
+    _lib.check(_lib.ssd_fwd(prob, args, ws, stream), "ssd_fwd")
+    return y, final_states
+
+
+def ssd_backward(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, initial_states=None, dfinal_states=None,
+                 cu_seqlens=None, chunk_size=128, algo="auto", seg_chunks=0, workspace=None, stream=None):
+    """Gradients of sum(dy*y) + sum(dfinal_states*final_states).  Returns a dict with
+    dx, ddt, dA, dB, dC and, when the matching input is given, dD, dz, ddt_bias, dinitial_states."""
+    Bsz, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    S = _nseqs(x, cu_seqlens)
+    dev = x.device
+    g = dict(dx=torch.empty(x.shape, dtype=x.dtype, device=dev),
+             ddt=torch.empty(dt.shape, dtype=torch.float32, device=dev),
+             dA=torch.empty(H, dtype=torch.float32, device=dev),
+             dB=torch.empty(B.shape, dtype=B.dtype, device=dev),
+             dC=torch.empty(C.shape, dtype=C.dtype, device=dev))
+    if D is not None:
+        g["dD"] = torch.empty(H, dtype=torch.float32, device=dev)
+    if z is not None:
+        g["dz"] = torch.empty(z.shape, dtype=z.dtype, device=dev)
+    if dt_bias is not None:
+        g["ddt_bias"] = torch.empty(H, dtype=torch.float32, device=dev)
+    if initial_states is not None:
+        g["dinitial_states"] = torch.empty(S, H, P, N, dtype=torch.float32, device=dev)
+    prob = _lib.problem(Bsz, L, H, P, G, N, chunk_size, S if cu_seqlens is not None else 0, algo, seg_chunks)
+    fa = _lib.fwd_args(x, dt, A, B, C, None, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
+                       cu_seqlens=cu_seqlens)
+    ba = _lib.bwd_args(fa, dy, g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], dD=g.get("dD"), dz=g.get("dz"),
+                       ddt_bias=g.get("ddt_bias"), dinitial_states=g.get("dinitial_states"),
+                       dfinal_states=dfinal_states)
+    nbytes = _lib.bwd_workspace_size(prob, ba)
+    ws = workspace.get(nbytes) if workspace is not None else torch.empty(max(nbytes, 256), dtype=torch.uint8,
+                                                                          device=dev)
+    _lib.check(_lib.ssd_bwd(prob, ba, ws, stream), "ssd_bwd")
+    return g
+
+
+class SSDFunction(torch.autograd.Function):
+    """Autograd wrapper: forward and backward both run in libssd.so."""
+
+    @staticmethod
+    def forward(ctx, x, dt, A, B, C, D, z, dt_bias, initial_states, cu_seqlens, chunk_size):
+        y, fin = ssd_forward(x, dt, A, B, C, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
+                             cu_seqlens=cu_seqlens, chunk_size=chunk_size)
+        ctx.save_for_backward(x, dt, A, B, C, D, z, dt_bias, initial_states, cu_seqlens)
+        ctx.chunk_size = chunk_size
+        return y, fin
+
+    @staticmethod
+    def backward(ctx, dy, dfin):
+        x, dt, A, B, C, D, z, dt_bias, init, cu = ctx.saved_tensors
+        g = ssd_backward(x, dt, A, B, C, dy.contiguous(), D=D, z=z, dt_bias=dt_bias, initial_states=init,
+                         dfinal_states=None if dfin is None else dfin.contiguous(), cu_seqlens=cu,
+                         chunk_size=ctx.chunk_size)
+        return (g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], g.get("dD"), g.get("dz"), g.get("ddt_bias"),
+                g.get("dinitial_states"), None, None)

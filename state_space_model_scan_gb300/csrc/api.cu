@@ -1,0 +1,370 @@
+// api.cu -- the C ABI of libssd.so (declared in include/ssd.h): argument
+// validation, workspace planning and launch sequencing on the caller's stream.
+#include <string.h>
+
+#include "common.cuh"
+
+namespace ssd {
+// meta.cu
+cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int kmax, int umax, int32_t *hdr,
+                              SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units, int32_t *last_unit,
+                              uint32_t *zero_words, int64_t n_zero, cudaStream_t st);
+cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr, const float *init,
+                                   float *final_, cudaStream_t st);
+// simt_fwd.cu
+cudaError_t launch_chunk_cumsum(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const float *dt_raw,
+                                int64_t sdb, int64_t sdl, const float *A, const float *bias, float *dt_out,
+                                float *cs_out, cudaStream_t st);
+template <typename T>
+cudaError_t launch_chunk_state(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 x, View3 Bm,
+                               const float *dtw, const float *csw, float *states, cudaStream_t st);
+cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqInfo *seqs, const float *csw,
+                                 float *states, const float *init, float *final_, int reverse, cudaStream_t st);
+template <typename T>
+cudaError_t launch_chunk_scan(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 x, View3 Bm,
+                              View3 Cm, View3 z, const float *D, const float *dtw, const float *csw,
+                              const float *states, MView3 y, cudaStream_t st);
+// simt_bwd.cu
+template <typename T>
+cudaError_t launch_bwd_dstates(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 dy, View3 z,
+                               View3 Cm, const float *csw, float *dstates, cudaStream_t st);
+template <typename T>
+cudaError_t launch_bwd_chunk(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 x, View3 Bm,
+                             View3 Cm, View3 z, View3 dy, const float *dt_raw, int64_t sdb, int64_t sdl,
+                             const float *A, const float *D, const float *bias, const float *dtw, const float *csw,
+                             const float *states, const float *dstates, MView3 dx, MView3 dz, float *ddt,
+                             int64_t sddb, int64_t sddl, float *dBh, float *dCh, float *partials, cudaStream_t st);
+template <typename T>
+cudaError_t launch_reduce_group(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const float *src,
+                                MView3 dst, cudaStream_t st);
+cudaError_t launch_reduce_heads(const Shape &sh, const int32_t *hdr, const float *partials, float *dA, float *dD,
+                                float *dbias, cudaStream_t st);
+size_t bwd_chunk_smem(const Shape &sh);
+size_t chunk_scan_smem(const Shape &sh);
+}  // namespace ssd
+
+using namespace ssd;
+
+namespace {
+
+constexpr int kSimtQ = 64;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool pow2_in(int64_t v, int64_t lo, int64_t hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+struct Plan {
+    Shape sh;
+    bool bf16 = false;
+    bool varlen = false;
+    int algo = SSD_ALGO_STAGED;
+    size_t off_hdr = 0, off_seqs = 0, off_chunks = 0, off_lastunit = 0, off_units = 0;
+    size_t off_dt = 0, off_cs = 0, off_states = 0, off_dstates = 0, off_dBh = 0, off_dCh = 0, off_part = 0;
+    size_t total = 0;
+};
+
+struct Layout {
+    size_t cur = 0;
+    size_t take(size_t bytes) {
+        size_t o = cur;
+        cur = align_up(cur + bytes);
+        return o;
+    }
+};
+
+// Checks one tensor argument.  rank = number of meaningful strides; the
+// innermost stride must be 1 and all strides non-negative.
+ssd_status check_tensor(const ssd_tensor &t, int rank, int dtype_req, bool required) {
+    if (t.ptr == nullptr) return required ? SSD_ERR_INVALID_ARGUMENT : SSD_OK;
+    if (dtype_req >= 0 && t.dtype != dtype_req) return SSD_ERR_INVALID_ARGUMENT;
+    if (t.dtype != SSD_F32 && t.dtype != SSD_BF16) return SSD_ERR_INVALID_ARGUMENT;
+    if (rank > 0 && t.stride[rank - 1] != 1) return SSD_ERR_INVALID_ARGUMENT;
+    for (int i = 0; i < rank; ++i)
+        if (t.stride[i] < 0) return SSD_ERR_INVALID_ARGUMENT;
+    return SSD_OK;
+}
+
+// Contiguous [S, H, P, N] state tensors.
+ssd_status check_state(const ssd_tensor &t, int64_t H, int64_t P, int64_t N) {
+    if (t.ptr == nullptr) return SSD_OK;
+    if (t.dtype != SSD_F32) return SSD_ERR_INVALID_ARGUMENT;
+    if (t.stride[3] != 1 || t.stride[2] != N || t.stride[1] != P * N || t.stride[0] != H * P * N)
+        return SSD_ERR_INVALID_ARGUMENT;
+    return SSD_OK;
+}
+
+ssd_status check_vec(const ssd_tensor &t, bool required) {
+    if (t.ptr == nullptr) return required ? SSD_ERR_INVALID_ARGUMENT : SSD_OK;
+    if (t.dtype != SSD_F32 || t.stride[0] != 1) return SSD_ERR_INVALID_ARGUMENT;
+    return SSD_OK;
+}
+
+#define SSD_TRY(expr)                      \
+    do {                                   \
+        ssd_status _s = (expr);            \
+        if (_s != SSD_OK) return _s;       \
+    } while (0)
+
+ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Plan *out) {
+    if (p == nullptr || a == nullptr || out == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    const int64_t B = p->batch, L = p->seqlen, H = p->nheads, P = p->headdim, G = p->ngroups, N = p->dstate;
+    if (B < 1 || L < 0 || H < 1 || G < 1 || P < 1 || N < 1 || p->chunk_size < 1) return SSD_ERR_INVALID_ARGUMENT;
+    if (H % G != 0) return SSD_ERR_INVALID_ARGUMENT;
+    if (L > (int64_t)1 << 30 || B > (int64_t)1 << 20 || H > 65535) return SSD_ERR_UNSUPPORTED;
+    if (!pow2_in(p->chunk_size, 16, 256)) return SSD_ERR_UNSUPPORTED;
+    if (!pow2_in(P, 16, 128) || !pow2_in(N, 16, 128)) return SSD_ERR_UNSUPPORTED;
+    if (p->algo < SSD_ALGO_AUTO || p->algo > SSD_ALGO_FUSED) return SSD_ERR_INVALID_ARGUMENT;
+    if (p->seg_chunks < 0 || p->seg_chunks > 16) return SSD_ERR_INVALID_ARGUMENT;
+    const bool varlen = a->cu_seqlens != nullptr;
+    int64_t S = B;
+    if (varlen) {
+        if (B != 1 || p->nseqs < 1) return SSD_ERR_INVALID_ARGUMENT;
+        S = p->nseqs;
+        if (S > (int64_t)1 << 24) return SSD_ERR_UNSUPPORTED;
+    } else if (p->nseqs != 0 && p->nseqs != B) {
+        return SSD_ERR_INVALID_ARGUMENT;
+    }
+    // Token tensors of an empty sequence axis have no storage (NULL is allowed).
+    const bool tok = L > 0;
+    if (a->x.dtype != SSD_F32 && a->x.dtype != SSD_BF16) return SSD_ERR_INVALID_ARGUMENT;
+    SSD_TRY(check_tensor(a->x, 4, -1, tok));
+    const int dt_ = a->x.dtype;
+    SSD_TRY(check_tensor(a->B, 4, dt_, tok));
+    SSD_TRY(check_tensor(a->C, 4, dt_, tok));
+    SSD_TRY(check_tensor(a->z, 4, dt_, false));
+    SSD_TRY(check_tensor(a->dt, 3, SSD_F32, tok));
+    SSD_TRY(check_vec(a->A, true));
+    SSD_TRY(check_vec(a->D, false));
+    SSD_TRY(check_vec(a->dt_bias, false));
+    SSD_TRY(check_state(a->initial_states, H, P, N));
+    if (!bwd) {
+        SSD_TRY(check_tensor(a->y, 4, dt_, tok));
+        SSD_TRY(check_state(a->final_states, H, P, N));
+    }
+    Plan pl;
+    pl.bf16 = dt_ == SSD_BF16;
+    pl.varlen = varlen;
+    // Path choice: the tensor-core path is not part of this build's SIMT-only
+    // configuration; AUTO resolves to STAGED.
+    if (p->algo == SSD_ALGO_FUSED) return SSD_ERR_UNSUPPORTED;
+    pl.algo = SSD_ALGO_STAGED;
+    const int Q = kSimtQ;
+    int64_t kmax = varlen ? (L + Q - 1) / Q + S : B * ((L + Q - 1) / Q);
+    if (kmax > (int64_t)1 << 30) return SSD_ERR_UNSUPPORTED;
+    Shape sh;
+    sh.B = (int)B; sh.L = (int)L; sh.H = (int)H; sh.P = (int)P; sh.G = (int)G; sh.N = (int)N; sh.S = (int)S;
+    sh.Q = Q; sh.hpg = (int)(H / G); sh.kmax = (int)kmax; sh.umax = 0; sh.R = 1;
+    pl.sh = sh;
+    Layout lay;
+    pl.off_hdr = lay.take(HDR_WORDS * sizeof(int32_t));
+    pl.off_seqs = lay.take(sizeof(SeqInfo) * (size_t)S);
+    pl.off_chunks = lay.take(sizeof(ChunkInfo) * (size_t)kmax);
+    pl.off_lastunit = lay.take(sizeof(int32_t) * (size_t)S);
+    const size_t kh = (size_t)kmax * (size_t)H;
+    pl.off_dt = lay.take(sizeof(float) * kh * Q);
+    pl.off_cs = lay.take(sizeof(float) * kh * Q);
+    pl.off_states = lay.take(sizeof(float) * kh * (size_t)(P * N));
+    if (bwd) {
+        pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * N));
+        pl.off_dBh = lay.take(sizeof(float) * kh * Q * (size_t)N);
+        pl.off_dCh = lay.take(sizeof(float) * kh * Q * (size_t)N);
+        pl.off_part = lay.take(sizeof(float) * kh * 4);
+    }
+    pl.total = lay.cur;
+    *out = pl;
+    return SSD_OK;
+}
+
+ssd_status plan_bwd(const ssd_problem *p, const ssd_bwd_args *b, Plan *out) {
+    if (b == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    SSD_TRY(plan_common(p, &b->fwd, true, out));
+    const int dt_ = b->fwd.x.dtype;
+    const int64_t H = p->nheads, P = p->headdim, N = p->dstate;
+    const bool tok = p->seqlen > 0;
+    SSD_TRY(check_tensor(b->dy, 4, dt_, tok));
+    SSD_TRY(check_state(b->dfinal_states, H, P, N));
+    SSD_TRY(check_tensor(b->dx, 4, dt_, tok));
+    SSD_TRY(check_tensor(b->ddt, 3, SSD_F32, tok));
+    SSD_TRY(check_vec(b->dA, true));
+    SSD_TRY(check_tensor(b->dB, 4, dt_, tok));
+    SSD_TRY(check_tensor(b->dC, 4, dt_, tok));
+    SSD_TRY(check_vec(b->dD, b->fwd.D.ptr != nullptr));
+    SSD_TRY(check_tensor(b->dz, 4, dt_, tok && b->fwd.z.ptr != nullptr));
+    SSD_TRY(check_vec(b->ddt_bias, b->fwd.dt_bias.ptr != nullptr));
+    SSD_TRY(check_state(b->dinitial_states, H, P, N));
+    if (b->fwd.initial_states.ptr != nullptr && b->dinitial_states.ptr == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    return SSD_OK;
+}
+
+View3 view(const ssd_tensor &t) {
+    View3 v;
+    v.p = t.ptr; v.s0 = t.stride[0]; v.s1 = t.stride[1]; v.s2 = t.stride[2];
+    return v;
+}
+MView3 mview(const ssd_tensor &t) {
+    MView3 v;
+    v.p = t.ptr; v.s0 = t.stride[0]; v.s1 = t.stride[1]; v.s2 = t.stride[2];
+    return v;
+}
+
+template <typename Tp>
+Tp *at(void *ws, size_t off) { return reinterpret_cast<Tp *>(static_cast<char *>(ws) + off); }
+
+#define SSD_CUDA(expr)                               \
+    do {                                             \
+        if ((expr) != cudaSuccess) return SSD_ERR_CUDA; \
+    } while (0)
+
+// Metadata, dt/cs, carry-in states (and final states) -- shared by fwd and bwd.
+ssd_status run_forward_states(const Plan &pl, const ssd_fwd_args *a, void *ws, float *final_, cudaStream_t st) {
+    const Shape &sh = pl.sh;
+    int32_t *hdr = at<int32_t>(ws, pl.off_hdr);
+    SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
+    ChunkInfo *chunks = at<ChunkInfo>(ws, pl.off_chunks);
+    float *dtw = at<float>(ws, pl.off_dt), *csw = at<float>(ws, pl.off_cs), *states = at<float>(ws, pl.off_states);
+    SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, 1, sh.kmax, 0, hdr, seqs, chunks, nullptr,
+                               at<int32_t>(ws, pl.off_lastunit), nullptr, 0, st));
+    if (sh.kmax > 0) {
+        SSD_CUDA(launch_chunk_cumsum(sh, hdr, chunks, (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1],
+                                     (const float *)a->A.ptr, (const float *)a->dt_bias.ptr, dtw, csw, st));
+        if (pl.bf16)
+            SSD_CUDA(launch_chunk_state<__nv_bfloat16>(sh, hdr, chunks, view(a->x), view(a->B), dtw, csw, states, st));
+        else
+            SSD_CUDA(launch_chunk_state<float>(sh, hdr, chunks, view(a->x), view(a->B), dtw, csw, states, st));
+    }
+    SSD_CUDA(launch_state_passing(sh, hdr, seqs, csw, states, (const float *)a->initial_states.ptr, final_, 0, st));
+    return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ssd_status_string(ssd_status s) {
+    switch (s) {
+        case SSD_OK: return "SSD_OK";
+        case SSD_ERR_INVALID_ARGUMENT: return "SSD_ERR_INVALID_ARGUMENT";
+        case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED";
+        case SSD_ERR_MISALIGNED: return "SSD_ERR_MISALIGNED";
+        case SSD_ERR_WORKSPACE_TOO_SMALL: return "SSD_ERR_WORKSPACE_TOO_SMALL";
+        case SSD_ERR_CUDA: return "SSD_ERR_CUDA";
+        case SSD_ERR_DEVICE_TIMEOUT: return "SSD_ERR_DEVICE_TIMEOUT";
+    }
+    return "SSD_ERR_UNKNOWN";
+}
+
+int32_t ssd_abi_version(void) { return SSD_ABI_VERSION; }
+
+ssd_status ssd_fwd_workspace_size(const ssd_problem *prob, const ssd_fwd_args *args, size_t *bytes) {
+    if (bytes == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    Plan pl;
+    SSD_TRY(plan_common(prob, args, false, &pl));
+    *bytes = pl.total;
+    return SSD_OK;
+}
+
+ssd_status ssd_fwd_debug_layout(const ssd_problem *prob, const ssd_fwd_args *args, ssd_debug_layout *out) {
+    if (out == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    Plan pl;
+    SSD_TRY(plan_common(prob, args, false, &pl));
+    out->meta_counts = (int64_t)pl.off_hdr;
+    out->chunk_info = (int64_t)pl.off_chunks;
+    const bool staged = pl.algo == SSD_ALGO_STAGED;
+    out->dt = staged ? (int64_t)pl.off_dt : -1;
+    out->cs = staged ? (int64_t)pl.off_cs : -1;
+    out->states = staged ? (int64_t)pl.off_states : -1;
+    out->qi = pl.sh.Q;
+    return SSD_OK;
+}
+
+ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, size_t ws_bytes, void *stream) {
+    Plan pl;
+    SSD_TRY(plan_common(prob, a, false, &pl));
+    if (ws == nullptr || ws_bytes < pl.total) return SSD_ERR_WORKSPACE_TOO_SMALL;
+    if (((uintptr_t)ws) % kAlign != 0) return SSD_ERR_MISALIGNED;
+    cudaStream_t st = (cudaStream_t)stream;
+    const Shape &sh = pl.sh;
+    float *final_ = (float *)a->final_states.ptr;
+    SSD_TRY(run_forward_states(pl, a, ws, final_, st));
+    if (sh.kmax > 0) {
+        int32_t *hdr = at<int32_t>(ws, pl.off_hdr);
+        ChunkInfo *chunks = at<ChunkInfo>(ws, pl.off_chunks);
+        float *dtw = at<float>(ws, pl.off_dt), *csw = at<float>(ws, pl.off_cs), *states = at<float>(ws, pl.off_states);
+        if (pl.bf16)
+            SSD_CUDA(launch_chunk_scan<__nv_bfloat16>(sh, hdr, chunks, view(a->x), view(a->B), view(a->C), view(a->z),
+                                                      (const float *)a->D.ptr, dtw, csw, states, mview(a->y), st));
+        else
+            SSD_CUDA(launch_chunk_scan<float>(sh, hdr, chunks, view(a->x), view(a->B), view(a->C), view(a->z),
+                                              (const float *)a->D.ptr, dtw, csw, states, mview(a->y), st));
+    }
+    return SSD_OK;
+}
+
+ssd_status ssd_bwd_workspace_size(const ssd_problem *prob, const ssd_bwd_args *args, size_t *bytes) {
+    if (bytes == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    Plan pl;
+    SSD_TRY(plan_bwd(prob, args, &pl));
+    *bytes = pl.total;
+    return SSD_OK;
+}
+
+ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, size_t ws_bytes, void *stream) {
+    Plan pl;
+    SSD_TRY(plan_bwd(prob, b, &pl));
+    if (ws == nullptr || ws_bytes < pl.total) return SSD_ERR_WORKSPACE_TOO_SMALL;
+    if (((uintptr_t)ws) % kAlign != 0) return SSD_ERR_MISALIGNED;
+    cudaStream_t st = (cudaStream_t)stream;
+    const Shape &sh = pl.sh;
+    const ssd_fwd_args *a = &b->fwd;
+    SSD_TRY(run_forward_states(pl, a, ws, nullptr, st));
+    int32_t *hdr = at<int32_t>(ws, pl.off_hdr);
+    SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
+    ChunkInfo *chunks = at<ChunkInfo>(ws, pl.off_chunks);
+    float *dtw = at<float>(ws, pl.off_dt), *csw = at<float>(ws, pl.off_cs), *states = at<float>(ws, pl.off_states);
+    float *dstates = at<float>(ws, pl.off_dstates);
+    float *dBh = at<float>(ws, pl.off_dBh), *dCh = at<float>(ws, pl.off_dCh), *part = at<float>(ws, pl.off_part);
+    if (sh.kmax > 0) {
+        if (pl.bf16)
+            SSD_CUDA(launch_bwd_dstates<__nv_bfloat16>(sh, hdr, chunks, view(b->dy), view(a->z), view(a->C), csw,
+                                                       dstates, st));
+        else
+            SSD_CUDA(launch_bwd_dstates<float>(sh, hdr, chunks, view(b->dy), view(a->z), view(a->C), csw, dstates, st));
+    }
+    SSD_CUDA(launch_state_passing(sh, hdr, seqs, csw, dstates, (const float *)b->dfinal_states.ptr,
+                                  (float *)b->dinitial_states.ptr, 1, st));
+    if (sh.kmax > 0) {
+        if (pl.bf16) {
+            SSD_CUDA(launch_bwd_chunk<__nv_bfloat16>(
+                sh, hdr, chunks, view(a->x), view(a->B), view(a->C), view(a->z), view(b->dy), (const float *)a->dt.ptr,
+                a->dt.stride[0], a->dt.stride[1], (const float *)a->A.ptr, (const float *)a->D.ptr,
+                (const float *)a->dt_bias.ptr, dtw, csw, states, dstates, mview(b->dx), mview(b->dz),
+                (float *)b->ddt.ptr, b->ddt.stride[0], b->ddt.stride[1], dBh, dCh, part, st));
+            SSD_CUDA(launch_reduce_group<__nv_bfloat16>(sh, hdr, chunks, dBh, mview(b->dB), st));
+            SSD_CUDA(launch_reduce_group<__nv_bfloat16>(sh, hdr, chunks, dCh, mview(b->dC), st));
+        } else {
+            SSD_CUDA(launch_bwd_chunk<float>(
+                sh, hdr, chunks, view(a->x), view(a->B), view(a->C), view(a->z), view(b->dy), (const float *)a->dt.ptr,
+                a->dt.stride[0], a->dt.stride[1], (const float *)a->A.ptr, (const float *)a->D.ptr,
+                (const float *)a->dt_bias.ptr, dtw, csw, states, dstates, mview(b->dx), mview(b->dz),
+                (float *)b->ddt.ptr, b->ddt.stride[0], b->ddt.stride[1], dBh, dCh, part, st));
+            SSD_CUDA(launch_reduce_group<float>(sh, hdr, chunks, dBh, mview(b->dB), st));
+            SSD_CUDA(launch_reduce_group<float>(sh, hdr, chunks, dCh, mview(b->dC), st));
+        }
+    }
+    SSD_CUDA(launch_reduce_heads(sh, hdr, part, (float *)b->dA.ptr, (float *)b->dD.ptr, (float *)b->ddt_bias.ptr, st));
+    return SSD_OK;
+}
+
+ssd_status ssd_query_status(const void *ws, void *stream) {
+    if (ws == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, static_cast<const int32_t *>(ws) + HDR_STATUS, sizeof(v), cudaMemcpyDeviceToHost, st) !=
+        cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+    return (ssd_status)v;
+}
+
+}  // extern "C"

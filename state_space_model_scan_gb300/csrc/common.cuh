@@ -1,0 +1,91 @@
+// common.cuh -- types and device helpers shared by the libssd kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/ssd.h"
+
+namespace ssd {
+
+// ---------------------------------------------------------------------------
+// Workspace header: 64 int32 words at offset 0 of every workspace.
+enum HeaderWord {
+    HDR_NCHUNKS = 0,   // number of chunks in the chunk list
+    HDR_NUNITS = 1,    // number of work units (fused path)
+    HDR_NSEQS = 2,
+    HDR_STATUS = 3,    // device-side ssd_status (first error wins)
+    HDR_TICKET = 4,    // fused path: next unit ticket
+    HDR_MAXSEG = 5,    // fused path: largest number of units in one sequence
+    HDR_WORDS = 64
+};
+
+// One sequence: tokens [t0, t0 + len) of batch row b; its chunks start at chunk0.
+struct SeqInfo {
+    int32_t b, t0, len, chunk0;
+};
+// One chunk of one sequence: tokens [t0, t0 + len) of batch row b, len <= Q.
+struct ChunkInfo {
+    int32_t seq, b, t0, len;
+};
+// One work unit of the fused forward: `nchunk` consecutive chunks of one sequence.
+struct UnitInfo {
+    int32_t seq, b, t0, len;         // token range [t0, t0+len) of row b
+    int32_t nchunk, prev, last, first_chunk;  // prev: unit index of the same sequence's previous unit (-1 if none)
+};
+
+// Shape of one call, as the kernels see it.
+struct Shape {
+    int B, L, H, P, G, N, S;
+    int Q;            // internal chunk length
+    int hpg;          // H / G
+    int kmax;         // capacity of the chunk list
+    int umax;         // capacity of the unit list
+    int R;            // chunks per unit (fused path)
+};
+
+// Strided views (element strides of the three outer dims; innermost stride 1).
+struct View3 {
+    const void *p;
+    int64_t s0, s1, s2;
+};
+struct MView3 {
+    void *p;
+    int64_t s0, s1, s2;
+};
+
+__device__ __forceinline__ void set_status(int32_t *hdr, int32_t code) {
+    atomicCAS(&hdr[HDR_STATUS], 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// dtype helpers
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// softplus in fp32: log(1 + exp(v)); for v > 20 the exact value differs from v
+// by less than 2.1e-9 relative, so v is returned there.
+__device__ __forceinline__ float softplus_f(float v) { return v > 20.f ? v : log1pf(expf(v)); }
+__device__ __forceinline__ float sigmoid_f(float v) { return 1.f / (1.f + expf(-v)); }
+
+// Inclusive warp prefix sum.
+__device__ __forceinline__ float warp_incl_sum(float v) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        float t = __shfl_up_sync(0xffffffffu, v, o);
+        if ((threadIdx.x & 31) >= o) v += t;
+    }
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace ssd

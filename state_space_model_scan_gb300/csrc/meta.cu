@@ -1,0 +1,188 @@
+// meta.cu -- chunk and work-unit lists for fixed-length batches and packed
+// variable-length sequences (cu_seqlens).
+//
+// Each sequence is cut into Q-token chunks from its own first token (the last
+// chunk ragged), so no chunk ever holds two sequences; the carried state is
+// reset to the sequence's initial state at its first chunk.  Chunks are listed
+// sequence by sequence.  Work units of the fused forward group R consecutive
+// chunks of one sequence and are listed by (segment index j, sequence s), so a
+// unit only ever depends on units listed before it.
+#include "common.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr int kMetaThreads = 1024;
+
+__device__ int block_excl_scan(int v, int *total, int *sm) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += t;
+    }
+    if (lane == 31) sm[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int s = lane < nw ? sm[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int t = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += t;
+        }
+        sm[lane] = s;
+    }
+    __syncthreads();
+    int excl = x - v + (w > 0 ? sm[w - 1] : 0);
+    *total = sm[nw - 1];
+    __syncthreads();
+    return excl;
+}
+
+__device__ int block_max(int v, int *sm) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) sm[w] = v;
+    __syncthreads();
+    int m = 0;
+    for (int i = 0; i < nw; ++i) m = max(m, sm[i]);
+    __syncthreads();
+    return m;
+}
+
+__global__ void __launch_bounds__(kMetaThreads)
+k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, int kmax, int umax,
+             int32_t *hdr, SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units, int32_t *last_unit,
+             uint32_t *zero_words, int64_t n_zero) {
+    __shared__ int sm[32];
+    __shared__ int bad;
+    const int tid = threadIdx.x;
+    for (int64_t i = tid; i < n_zero; i += blockDim.x) zero_words[i] = 0u;
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    if (tid < HDR_WORDS) hdr[tid] = 0;
+    if (cu != nullptr) {
+        for (int s = tid; s <= S; s += blockDim.x) {
+            int c = cu[s];
+            if (s == 0 && c != 0) bad = 1;
+            if (s == S && c != L) bad = 1;
+            if (s < S && cu[s + 1] < c) bad = 1;
+        }
+    }
+    __syncthreads();
+    if (bad) {
+        if (tid == 0) hdr[HDR_STATUS] = SSD_ERR_INVALID_ARGUMENT;
+        return;
+    }
+    // pass 1: chunk offsets and the largest segment count
+    int carry = 0, maxseg = 0;
+    for (int base = 0; base < S; base += blockDim.x) {
+        int s = base + tid;
+        int len = 0, t0 = 0, b = 0;
+        if (s < S) {
+            if (cu) { t0 = cu[s]; len = cu[s + 1] - t0; }
+            else { b = s; len = L; }
+        }
+        int nch = (len + Q - 1) / Q;
+        int tot;
+        int off = block_excl_scan(s < S ? nch : 0, &tot, sm);
+        if (s < S) {
+            SeqInfo si;
+            si.b = b; si.t0 = t0; si.len = len; si.chunk0 = carry + off;
+            seqs[s] = si;
+        }
+        int nseg = (nch + R - 1) / R;
+        maxseg = max(maxseg, block_max(s < S ? nseg : 0, sm));
+        carry += tot;
+    }
+    const int nchunks = carry;
+    if (nchunks > kmax) {
+        if (tid == 0) hdr[HDR_STATUS] = SSD_ERR_INVALID_ARGUMENT;
+        return;
+    }
+    __syncthreads();
+    // pass 2: the chunk list, sequence by sequence
+    for (int s = tid; s < S; s += blockDim.x) {
+        SeqInfo si = seqs[s];
+        int nch = (si.len + Q - 1) / Q;
+        for (int c = 0; c < nch; ++c) {
+            ChunkInfo ci;
+            ci.seq = s; ci.b = si.b; ci.t0 = si.t0 + c * Q; ci.len = min(Q, si.len - c * Q);
+            chunks[si.chunk0 + c] = ci;
+        }
+    }
+    // pass 3: work units ordered by (segment j, sequence s)
+    int nunits = 0;
+    if (units != nullptr) {
+        for (int j = 0; j < maxseg; ++j) {
+            for (int base = 0; base < S; base += blockDim.x) {
+                int s = base + tid;
+                int on = 0, nch = 0;
+                SeqInfo si;
+                if (s < S) {
+                    si = seqs[s];
+                    nch = (si.len + Q - 1) / Q;
+                    on = ((nch + R - 1) / R) > j;
+                }
+                int tot;
+                int off = block_excl_scan(on, &tot, sm);
+                if (on) {
+                    int u = nunits + off;
+                    if (u < umax) {
+                        UnitInfo ui;
+                        ui.seq = s; ui.b = si.b;
+                        ui.t0 = si.t0 + j * R * Q;
+                        ui.len = min(R * Q, si.len - j * R * Q);
+                        ui.nchunk = min(R, nch - j * R);
+                        ui.prev = (j == 0) ? -1 : last_unit[s];
+                        ui.last = (j == (nch + R - 1) / R - 1) ? 1 : 0;
+                        ui.first_chunk = si.chunk0 + j * R;
+                        units[u] = ui;
+                        last_unit[s] = u;
+                    }
+                }
+                nunits += tot;
+            }
+            __syncthreads();
+        }
+        if (nunits > umax && tid == 0) hdr[HDR_STATUS] = SSD_ERR_INVALID_ARGUMENT;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        hdr[HDR_NCHUNKS] = nchunks;
+        hdr[HDR_NUNITS] = nunits > umax ? 0 : nunits;
+        hdr[HDR_NSEQS] = S;
+        hdr[HDR_MAXSEG] = maxseg;
+    }
+}
+
+// final_states[s] = initial_states[s] (or 0) for sequences with no tokens.
+__global__ void k_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr,
+                                  const float *init, float *final_) {
+    const int s = blockIdx.x, h = blockIdx.y;
+    if (hdr[HDR_STATUS] != 0 || s >= S || seqs[s].len != 0) return;
+    const int64_t base = ((int64_t)s * H + h) * PN;
+    for (int i = threadIdx.x; i < PN; i += blockDim.x) final_[base + i] = init ? init[base + i] : 0.f;
+}
+
+}  // namespace
+
+cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int kmax, int umax,
+                              int32_t *hdr, SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units,
+                              int32_t *last_unit, uint32_t *zero_words, int64_t n_zero, cudaStream_t st) {
+    k_build_meta<<<1, kMetaThreads, 0, st>>>(cu, B, L, S, Q, R, kmax, umax, hdr, seqs, chunks, units,
+                                             last_unit, zero_words, n_zero);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr,
+                                   const float *init, float *final_, cudaStream_t st) {
+    if (S <= 0) return cudaSuccess;
+    k_empty_seq_final<<<dim3(S, H), 256, 0, st>>>(S, H, PN, seqs, hdr, init, final_);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -1,0 +1,404 @@
+// simt_bwd.cu -- the staged SIMT backward of the chunked SSD scan.
+//
+// Recompute-based, as the Mamba-3-Lite "SSD Reference" page's section "6. The
+// autograd backward contract" prescribes for its kernel (re-run the forward math,
+// inject the true upstream gradients): the forward's dt, cs and carry-in states
+// are recomputed by the forward's own a1/a3/a4 kernels, then
+//   bwd_dstates      : dS_loc[c][p][n] = sum_l exp(cs[l]) dyp[l][p] C[l][n]
+//   state_passing    : reverse scan  dS_out[c] = exp(cs_{c+1}[Q-1]) dS_out[c+1] + dS_loc[c+1],
+//                      dS_out[last] = dfinal, dinit = exp(cs_0[Q-1]) dS_out[0] + dS_loc[0]
+//   bwd_chunk        : per chunk and head, every gradient of the chunk's closed form:
+//     with E[l][s] = exp(cs[l]-cs[s]) (s <= l), CB = C B^T, dM = dyp x^T, M = E dt_s CB,
+//     w_s = dt[s] exp(cs[Q-1]-cs[s]), u[s][p] = sum_n B[s][n] dS_out[p][n]:
+//       dx[s]   = sum_l M[l][s] dyp[l] + w_s u[s] + D dyp[s]
+//       dB[s]   = sum_l E dt_s dM[l][s] C[l]      + w_s x[s]^T dS_out
+//       dC[l]   = sum_s E dt_s dM[l][s] B[s]      + exp(cs[l]) dyp[l]^T S_in
+//       ddt[s] (direct) = sum_l E CB dM[l][s]     + exp(cs[Q-1]-cs[s]) x[s].u[s]
+//       dcs[i]  = sum_s T1[i][s] - sum_l T1[l][i] + T2[i] - T4[i] + [i = Q-1](T3 + sum_s T4[s])
+//         T1 = M o dM, T2[l] = dyp[l].Y_off[l], T4[s] = w_s x[s].u[s], T3 = exp(cs[Q-1]) <S_in, dS_out>
+//       da[u] = sum_{i>=u} dcs[i];  ddt = ddt_direct + A da;  dA += sum dt da
+//       ddt_raw = ddt * sigmoid(dt_raw + dt_bias);  dz = dy ypre silu'(z)
+//   reductions       : dB/dC over the heads of a group, dA/dD/ddt_bias over chunks, in a
+//                      fixed order (bitwise reproducible; no atomics).
+// SIMT internal chunk length is 64: one chunk row per 4 threads.
+#include "common.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr int QS = 64;   // SIMT chunk length
+
+__device__ __forceinline__ float sum4(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    return v;
+}
+
+// ------------------------------------------------------------------ bwd_dstates
+// grid (kmax, H), block 256; mapping as the forward chunk_state kernel.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_bwd_dstates(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restrict__ chunks,
+              View3 dy, View3 z, View3 Cm, const float *__restrict__ csw, float *__restrict__ dstates) {
+    constexpr int LT = 16;
+    __shared__ float ds[LT][129];
+    __shared__ float cs_[LT][129];
+    __shared__ float w[QS];
+    const int k = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    if (k >= hdr[HDR_NCHUNKS] || hdr[HDR_STATUS] != 0) return;
+    const ChunkInfo ci = chunks[k];
+    const int P = sh.P, N = sh.N, g = h / sh.hpg;
+    const float *csk = csw + ((int64_t)k * sh.H + h) * QS;
+    if (tid < QS) w[tid] = expf(csk[tid]);
+    const int np = 256 / N, n = tid % N, p0 = tid / N, J = P / np;
+    float acc[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+    const T *dyb = (const T *)dy.p + (int64_t)ci.b * dy.s0 + (int64_t)h * dy.s2;
+    const T *zb = z.p ? (const T *)z.p + (int64_t)ci.b * z.s0 + (int64_t)h * z.s2 : nullptr;
+    const T *cb = (const T *)Cm.p + (int64_t)ci.b * Cm.s0 + (int64_t)g * Cm.s2;
+    __syncthreads();
+    for (int l0 = 0; l0 < ci.len; l0 += LT) {
+        for (int i = tid; i < LT * P; i += 256) {
+            int r = i / P, c = i % P, l = l0 + r;
+            float v = 0.f;
+            if (l < ci.len) {
+                int64_t tok = ci.t0 + l;
+                v = to_f(dyb[tok * dy.s1 + c]);
+                if (zb) { float zz = to_f(zb[tok * z.s1 + c]); v *= zz * sigmoid_f(zz); }
+                v *= w[l];
+            }
+            ds[r][c] = v;
+        }
+        for (int i = tid; i < LT * N; i += 256) {
+            int r = i / N, c = i % N, l = l0 + r;
+            cs_[r][c] = (l < ci.len) ? to_f(cb[(int64_t)(ci.t0 + l) * Cm.s1 + c]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int r = 0; r < LT; ++r) {
+            const float cv = cs_[r][n];
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+                if (j < J) acc[j] += ds[r][p0 + np * j] * cv;
+        }
+        __syncthreads();
+    }
+    float *out = dstates + ((int64_t)k * sh.H + h) * P * N;
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+        if (j < J) out[(int64_t)(p0 + np * j) * N + n] = acc[j];
+}
+
+// ------------------------------------------------------------------ bwd_chunk
+// grid (kmax, H), block 256 = 64 rows x 4 threads.  Dynamic shared memory.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restrict__ chunks,
+            View3 x, View3 Bm, View3 Cm, View3 z, View3 dy, const float *__restrict__ dt_raw, int64_t sdb,
+            int64_t sdl, const float *__restrict__ A, const float *__restrict__ D, const float *__restrict__ bias,
+            const float *__restrict__ dtw, const float *__restrict__ csw, const float *__restrict__ states,
+            const float *__restrict__ dstates, MView3 dx, MView3 dz, float *__restrict__ ddt, int64_t sddb,
+            int64_t sddl, float *__restrict__ dBh, float *__restrict__ dCh, float *__restrict__ partials) {
+    extern __shared__ float sm[];
+    const int k = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    if (k >= hdr[HDR_NCHUNKS] || hdr[HDR_STATUS] != 0) return;
+    const ChunkInfo ci = chunks[k];
+    const int P = sh.P, N = sh.N, g = h / sh.hpg;
+    const int P1 = P + 1, N1 = N + 1, Q1 = QS + 1;
+    float *cs = sm;                  // QS
+    float *dt = cs + QS;             // QS
+    float *wst = dt + QS;            // QS
+    float *vec = wst + QS;           // 8 x QS per-row scalars
+    float *xs = vec + 8 * QS;        // QS x P1
+    float *dys = xs + QS * P1;       // QS x P1  (dyp = dy * silu(z))
+    float *Bs = dys + QS * P1;       // QS x N1
+    float *Cs = Bs + QS * N1;        // QS x N1
+    float *Mm = Cs + QS * N1;        // QS x Q1  CB, then M
+    float *Em = Mm + QS * Q1;        // QS x Q1  dM, then E dt dM
+    float *Tm = Em + QS * Q1;        // QS x Q1  E CB dM
+    float *rowXU = vec, *rowT2 = vec + QS, *rowD = vec + 2 * QS;
+
+    const float *dtk = dtw + ((int64_t)k * sh.H + h) * QS;
+    const float *csk = csw + ((int64_t)k * sh.H + h) * QS;
+    if (tid < QS) { cs[tid] = csk[tid]; dt[tid] = dtk[tid]; }
+    __syncthreads();
+    const float clast = cs[QS - 1];
+    if (tid < QS) wst[tid] = dt[tid] * expf(clast - cs[tid]);
+    const T *xb = (const T *)x.p + (int64_t)ci.b * x.s0 + (int64_t)h * x.s2;
+    const T *bb = (const T *)Bm.p + (int64_t)ci.b * Bm.s0 + (int64_t)g * Bm.s2;
+    const T *cb = (const T *)Cm.p + (int64_t)ci.b * Cm.s0 + (int64_t)g * Cm.s2;
+    const T *zb = z.p ? (const T *)z.p + (int64_t)ci.b * z.s0 + (int64_t)h * z.s2 : nullptr;
+    const T *dyb = (const T *)dy.p + (int64_t)ci.b * dy.s0 + (int64_t)h * dy.s2;
+    for (int i = tid; i < QS * P; i += 256) {
+        int r = i / P, c = i % P;
+        float xv = 0.f, dv = 0.f;
+        if (r < ci.len) {
+            int64_t tok = ci.t0 + r;
+            xv = to_f(xb[tok * x.s1 + c]);
+            dv = to_f(dyb[tok * dy.s1 + c]);
+            if (zb) { float zz = to_f(zb[tok * z.s1 + c]); dv *= zz * sigmoid_f(zz); }
+        }
+        xs[r * P1 + c] = xv;
+        dys[r * P1 + c] = dv;
+    }
+    for (int i = tid; i < QS * N; i += 256) {
+        int r = i / N, c = i % N;
+        bool in = r < ci.len;
+        Bs[r * N1 + c] = in ? to_f(bb[(int64_t)(ci.t0 + r) * Bm.s1 + c]) : 0.f;
+        Cs[r * N1 + c] = in ? to_f(cb[(int64_t)(ci.t0 + r) * Cm.s1 + c]) : 0.f;
+    }
+    __syncthreads();
+    // CB[l][s], dM[l][s]
+    for (int i = tid; i < QS * QS; i += 256) {
+        int l = i / QS, s = i % QS;
+        float a = 0.f, b = 0.f;
+        if (s <= l) {
+            for (int n = 0; n < N; ++n) a += Cs[l * N1 + n] * Bs[s * N1 + n];
+            for (int p = 0; p < P; ++p) b += dys[l * P1 + p] * xs[s * P1 + p];
+        }
+        const float E = (s <= l) ? expf(cs[l] - cs[s]) : 0.f;
+        Mm[l * Q1 + s] = E * dt[s] * a;
+        Em[l * Q1 + s] = E * dt[s] * b;
+        Tm[l * Q1 + s] = E * a * b;
+    }
+    __syncthreads();
+
+    const int r = tid >> 2, part = tid & 3;     // row r, quarter `part`
+    const float *dso = dstates + ((int64_t)k * sh.H + h) * P * N;
+    const float *sin = states + ((int64_t)k * sh.H + h) * P * N;
+    const float Dh = D ? D[h] : 0.f;
+    const bool live = r < ci.len;
+    const int64_t tok = (int64_t)ci.t0 + r;
+    // dx[r][p] and x.u row sums
+    {
+        float xu = 0.f;
+        for (int p = part; p < P; p += 4) {
+            float a = 0.f;
+            for (int l = r; l < QS; ++l) a += Mm[l * Q1 + r] * dys[l * P1 + p];
+            float u = 0.f;
+            const float *drow = dso + (int64_t)p * N;
+            for (int n = 0; n < N; ++n) u += Bs[r * N1 + n] * drow[n];
+            xu += xs[r * P1 + p] * u;
+            if (live) {
+                T *o = (T *)dx.p + (int64_t)ci.b * dx.s0 + tok * dx.s1 + (int64_t)h * dx.s2;
+                o[p] = from_f<T>(a + wst[r] * u + Dh * dys[r * P1 + p]);
+            }
+        }
+        xu = sum4(xu);
+        if (part == 0) rowXU[r] = xu;
+    }
+    // dB (this head) [r][n]
+    {
+        float *o = dBh + (((int64_t)k * sh.H + h) * QS + r) * N;
+        for (int n = part; n < N; n += 4) {
+            float a = 0.f;
+            for (int l = r; l < QS; ++l) a += Em[l * Q1 + r] * Cs[l * N1 + n];
+            float b = 0.f;
+            for (int p = 0; p < P; ++p) b += xs[r * P1 + p] * dso[(int64_t)p * N + n];
+            o[n] = a + wst[r] * b;
+        }
+    }
+    // dC (this head) [r][n]
+    {
+        float *o = dCh + (((int64_t)k * sh.H + h) * QS + r) * N;
+        const float er = expf(cs[r]);
+        for (int n = part; n < N; n += 4) {
+            float a = 0.f;
+            for (int s = 0; s <= r; ++s) a += Em[r * Q1 + s] * Bs[s * N1 + n];
+            float b = 0.f;
+            for (int p = 0; p < P; ++p) b += dys[r * P1 + p] * sin[(int64_t)p * N + n];
+            o[n] = a + er * b;
+        }
+    }
+    // ypre, dz, T2, dD row sums
+    {
+        const float er = expf(cs[r]);
+        float t2 = 0.f, dd = 0.f;
+        for (int p = part; p < P; p += 4) {
+            float yd = 0.f;
+            for (int s = 0; s <= r; ++s) yd += Mm[r * Q1 + s] * xs[s * P1 + p];
+            float yb = 0.f;
+            const float *srow = sin + (int64_t)p * N;
+            for (int n = 0; n < N; ++n) yb += Cs[r * N1 + n] * srow[n];
+            const float yo = er * yb;
+            t2 += dys[r * P1 + p] * yo;
+            dd += dys[r * P1 + p] * xs[r * P1 + p];
+            if (zb && live) {
+                const float ypre = yd + yo + Dh * xs[r * P1 + p];
+                const float zz = to_f(zb[tok * z.s1 + p]);
+                const float sg = sigmoid_f(zz);
+                const float dyv = to_f(dyb[tok * dy.s1 + p]);
+                T *o = (T *)dz.p + (int64_t)ci.b * dz.s0 + tok * dz.s1 + (int64_t)h * dz.s2;
+                o[p] = from_f<T>(dyv * ypre * sg * (1.f + zz * (1.f - sg)));
+            }
+        }
+        t2 = sum4(t2);
+        dd = sum4(dd);
+        if (part == 0) { rowT2[r] = t2; rowD[r] = dd; }
+    }
+    __syncthreads();
+    // T3 = exp(cs[Q-1]) <S_in, dS_out>: fixed-order block reduction
+    float t3p = 0.f;
+    for (int i = tid; i < P * N; i += 256) t3p += sin[i] * dso[i];
+    t3p = warp_sum(t3p);
+    float *red = vec + 3 * QS;    // 8 warp partials
+    if ((tid & 31) == 0) red[tid >> 5] = t3p;
+    __syncthreads();
+    if (tid < 32) {
+        // per-position scalars: thread i handles positions i and i + 32
+        float T3 = 0.f;
+        for (int w = 0; w < 8; ++w) T3 += red[w];
+        T3 *= expf(clast);
+        float dcs[2], t4[2], ddir[2];
+        float t4sum_part = 0.f;
+        for (int q = 0; q < 2; ++q) {
+            const int i = tid + 32 * q;
+            float rowT1 = 0.f, colT1 = 0.f, colTm = 0.f;
+            for (int s = 0; s <= i; ++s) rowT1 += dt[s] * Tm[i * Q1 + s];
+            for (int l = i; l < QS; ++l) { colTm += Tm[l * Q1 + i]; }
+            colT1 = dt[i] * colTm;
+            t4[q] = wst[i] * rowXU[i];
+            ddir[q] = colTm + expf(clast - cs[i]) * rowXU[i];
+            dcs[q] = rowT1 - colT1 + rowT2[i] - t4[q];
+            t4sum_part += t4[q];
+        }
+        const float t4sum = warp_sum(t4sum_part);
+        if (tid == 31) dcs[1] += T3 + t4sum;        // position QS-1
+        // da[u] = sum_{i >= u} dcs[i]: reverse inclusive scan over 64 positions
+        float hi = dcs[1], lo = dcs[0];
+        // suffix sums within each half via reversed warp scan
+        float hs = hi, ls = lo;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            float th = __shfl_down_sync(0xffffffffu, hs, o);
+            float tl = __shfl_down_sync(0xffffffffu, ls, o);
+            if (tid + o < 32) { hs += th; ls += tl; }
+        }
+        const float hi_total = __shfl_sync(0xffffffffu, hs, 0);
+        const float da[2] = {ls + hi_total, hs};
+        const float Ah = A[h];
+        float pa = 0.f, pb = 0.f;
+        for (int q = 0; q < 2; ++q) {
+            const int i = tid + 32 * q;
+            if (i < ci.len) {
+                const float v = dt_raw[(int64_t)ci.b * sdb + (int64_t)(ci.t0 + i) * sdl + h] + (bias ? bias[h] : 0.f);
+                const float g_ = (ddir[q] + Ah * da[q]) * sigmoid_f(v);
+                ddt[(int64_t)ci.b * sddb + (int64_t)(ci.t0 + i) * sddl + h] = g_;
+                pa += dt[i] * da[q];
+                pb += g_;
+            }
+        }
+        pa = warp_sum(pa);
+        pb = warp_sum(pb);
+        float pd = rowD[tid] + rowD[tid + 32];
+        pd = warp_sum(pd);
+        if (tid == 0) {
+            float *pp = partials + ((int64_t)k * sh.H + h) * 4;
+            pp[0] = pa; pp[1] = pd; pp[2] = pb; pp[3] = 0.f;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ reductions
+// dB/dC: sum the per-head rows of each group in head order.  grid (kmax, G), block 256.
+template <typename T>
+__global__ void k_reduce_group(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restrict__ chunks,
+                               const float *__restrict__ src, MView3 dst) {
+    const int k = blockIdx.x, g = blockIdx.y;
+    if (k >= hdr[HDR_NCHUNKS] || hdr[HDR_STATUS] != 0) return;
+    const ChunkInfo ci = chunks[k];
+    const int N = sh.N;
+    for (int i = threadIdx.x; i < ci.len * N; i += blockDim.x) {
+        const int l = i / N, n = i % N;
+        float a = 0.f;
+        for (int j = 0; j < sh.hpg; ++j) {
+            const int h = g * sh.hpg + j;
+            a += src[(((int64_t)k * sh.H + h) * QS + l) * N + n];
+        }
+        T *o = (T *)dst.p + (int64_t)ci.b * dst.s0 + (int64_t)(ci.t0 + l) * dst.s1 + (int64_t)g * dst.s2;
+        o[n] = from_f<T>(a);
+    }
+}
+
+// dA, dD, ddt_bias: sum chunk partials in a fixed order.  grid H, block 256.
+__global__ void k_reduce_heads(Shape sh, const int32_t *__restrict__ hdr, const float *__restrict__ partials,
+                               float *dA, float *dD, float *dbias) {
+    __shared__ float red[3][8];
+    const int h = blockIdx.x, tid = threadIdx.x;
+    const int nk = hdr[HDR_STATUS] != 0 ? 0 : hdr[HDR_NCHUNKS];
+    float a = 0.f, d = 0.f, b = 0.f;
+    for (int k = tid; k < nk; k += 256) {
+        const float *pp = partials + ((int64_t)k * sh.H + h) * 4;
+        a += pp[0]; d += pp[1]; b += pp[2];
+    }
+    a = warp_sum(a); d = warp_sum(d); b = warp_sum(b);
+    if ((tid & 31) == 0) { red[0][tid >> 5] = a; red[1][tid >> 5] = d; red[2][tid >> 5] = b; }
+    __syncthreads();
+    if (tid == 0) {
+        float ta = 0.f, td = 0.f, tb = 0.f;
+        for (int w = 0; w < 8; ++w) { ta += red[0][w]; td += red[1][w]; tb += red[2][w]; }
+        dA[h] = ta;
+        if (dD) dD[h] = td;
+        if (dbias) dbias[h] = tb;
+    }
+}
+
+}  // namespace
+
+size_t bwd_chunk_smem(const Shape &sh) {
+    const int P1 = sh.P + 1, N1 = sh.N + 1, Q1 = QS + 1;
+    return sizeof(float) * (size_t)(11 * QS + 2 * QS * P1 + 2 * QS * N1 + 3 * QS * Q1);
+}
+
+template <typename T>
+cudaError_t launch_bwd_dstates(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 dy, View3 z,
+                               View3 Cm, const float *csw, float *dstates, cudaStream_t st) {
+    k_bwd_dstates<T><<<dim3(sh.kmax, sh.H), 256, 0, st>>>(sh, hdr, chunks, dy, z, Cm, csw, dstates);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_bwd_chunk(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 x, View3 Bm,
+                             View3 Cm, View3 z, View3 dy, const float *dt_raw, int64_t sdb, int64_t sdl,
+                             const float *A, const float *D, const float *bias, const float *dtw, const float *csw,
+                             const float *states, const float *dstates, MView3 dx, MView3 dz, float *ddt,
+                             int64_t sddb, int64_t sddl, float *dBh, float *dCh, float *partials, cudaStream_t st) {
+    const size_t smem = bwd_chunk_smem(sh);
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_chunk<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_bwd_chunk<T><<<dim3(sh.kmax, sh.H), 256, smem, st>>>(sh, hdr, chunks, x, Bm, Cm, z, dy, dt_raw, sdb, sdl, A, D,
+                                                           bias, dtw, csw, states, dstates, dx, dz, ddt, sddb, sddl,
+                                                           dBh, dCh, partials);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_reduce_group(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const float *src,
+                                MView3 dst, cudaStream_t st) {
+    k_reduce_group<T><<<dim3(sh.kmax, sh.G), 256, 0, st>>>(sh, hdr, chunks, src, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_heads(const Shape &sh, const int32_t *hdr, const float *partials, float *dA, float *dD,
+                                float *dbias, cudaStream_t st) {
+    k_reduce_heads<<<sh.H, 256, 0, st>>>(sh, hdr, partials, dA, dD, dbias);
+    return cudaGetLastError();
+}
+
+#define SSD_INST(T)                                                                                              \
+    template cudaError_t launch_bwd_dstates<T>(const Shape &, const int32_t *, const ChunkInfo *, View3, View3,  \
+                                               View3, const float *, float *, cudaStream_t);                     \
+    template cudaError_t launch_bwd_chunk<T>(const Shape &, const int32_t *, const ChunkInfo *, View3, View3,    \
+                                             View3, View3, View3, const float *, int64_t, int64_t, const float *, \
+                                             const float *, const float *, const float *, const float *,          \
+                                             const float *, const float *, MView3, MView3, float *, int64_t,      \
+                                             int64_t, float *, float *, float *, cudaStream_t);                   \
+    template cudaError_t launch_reduce_group<T>(const Shape &, const int32_t *, const ChunkInfo *, const float *, \
+                                                MView3, cudaStream_t);
+SSD_INST(float)
+SSD_INST(__nv_bfloat16)
+#undef SSD_INST
+
+}  // namespace ssd

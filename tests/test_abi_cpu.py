@@ -1,0 +1,155 @@
+"""The C ABI on the CPU: the library loads, exports every declared symbol, and
+host-side validation returns the documented status codes (no GPU needed: every
+call here fails validation before anything is enqueued)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from state_space_model_scan_gb300 import build, _lib
+    build.build()
+    return _lib
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_[a-z_0-9]+)\s*\(", txt)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    L = lib.load()
+    names = declared_functions()
+    assert set(names) == set(lib.EXPORTS), names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.abi_version() == 1
+    for code, name in lib.STATUS_NAMES.items():
+        assert lib.status_string(code) == name
+    assert lib.status_string(99) == "SSD_ERR_UNKNOWN"
+
+
+def _fake(dtype, strides, ptr=0x100000):
+    t = lib_mod().Tensor()
+    t.ptr = ptr
+    t.dtype = dtype
+    for i, s in enumerate(strides):
+        t.stride[i] = s
+    return t
+
+
+def lib_mod():
+    from state_space_model_scan_gb300 import _lib
+    return _lib
+
+
+def good_case(Bsz=2, L=100, H=4, P=16, G=2, N=16, bf16=True):
+    m = lib_mod()
+    dt_ = m.SSD_BF16 if bf16 else m.SSD_F32
+    xs = [L * H * P, H * P, P, 1]
+    bs = [L * G * N, G * N, N, 1]
+    a = m.FwdArgs()
+    a.x = _fake(dt_, xs)
+    a.y = _fake(dt_, xs)
+    a.z = _fake(dt_, xs)
+    a.B = _fake(dt_, bs)
+    a.C = _fake(dt_, bs)
+    a.dt = _fake(m.SSD_F32, [L * H, H, 1])
+    a.A = _fake(m.SSD_F32, [1])
+    a.D = _fake(m.SSD_F32, [1])
+    a.dt_bias = _fake(m.SSD_F32, [1])
+    a.final_states = _fake(m.SSD_F32, [H * P * N, P * N, N, 1])
+    p = m.problem(Bsz, L, H, P, G, N, 64)
+    return p, a
+
+
+def ws_size(p, a):
+    m = lib_mod()
+    n = ctypes.c_size_t(0)
+    rc = m.load().ssd_fwd_workspace_size(ctypes.byref(p), ctypes.byref(a), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_valid_problem_has_workspace(lib):
+    p, a = good_case()
+    rc, n = ws_size(p, a)
+    assert rc == 0 and n > 0
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (lambda p, a: setattr(p, "ngroups", 3), 1),                  # H % G != 0
+    (lambda p, a: setattr(p, "headdim", 48), 2),                 # P outside the compiled set
+    (lambda p, a: setattr(p, "dstate", 256), 2),                 # N outside the compiled set
+    (lambda p, a: setattr(p, "chunk_size", 100), 2),             # not a power of two
+    (lambda p, a: setattr(p, "chunk_size", 0), 1),
+    (lambda p, a: setattr(p, "batch", 0), 1),
+    (lambda p, a: setattr(a.x, "ptr", None), 1),                 # missing required input
+    (lambda p, a: setattr(a.y, "ptr", None), 1),                 # missing required output
+    (lambda p, a: setattr(a.B, "dtype", 0), 1),                  # dtype mix
+    (lambda p, a: setattr(a.dt, "dtype", 1), 1),                 # dt must be f32
+    (lambda p, a: a.x.stride.__setitem__(3, 2), 1),              # innermost stride must be 1
+    (lambda p, a: a.final_states.stride.__setitem__(0, 7), 1),   # states must be contiguous
+    (lambda p, a: setattr(p, "nseqs", 5), 1),                    # nseqs without cu_seqlens must match batch
+    (lambda p, a: setattr(a, "cu_seqlens", 0x2000), 1),          # cu_seqlens needs batch 1
+    (lambda p, a: setattr(p, "algo", 7), 1),
+])
+def test_validation_codes(lib, mutate, code):
+    p, a = good_case()
+    mutate(p, a)
+    rc, _ = ws_size(p, a)
+    assert rc == code
+    # the call itself fails the same way before touching the device
+    m = lib_mod()
+    rc2 = m.load().ssd_fwd(ctypes.byref(p), ctypes.byref(a), ctypes.c_void_p(0x100000), ctypes.c_size_t(1 << 40),
+                           None)
+    assert rc2 == code
+
+
+def test_workspace_checks(lib):
+    m = lib_mod()
+    p, a = good_case()
+    rc, n = ws_size(p, a)
+    assert m.load().ssd_fwd(ctypes.byref(p), ctypes.byref(a), ctypes.c_void_p(0x100000), ctypes.c_size_t(n - 1),
+                            None) == 4
+    assert m.load().ssd_fwd(ctypes.byref(p), ctypes.byref(a), None, ctypes.c_size_t(n), None) == 4
+    assert m.load().ssd_fwd(ctypes.byref(p), ctypes.byref(a), ctypes.c_void_p(0x100010), ctypes.c_size_t(n),
+                            None) == 3
+
+
+def test_bwd_requires_matching_gradients(lib):
+    m = lib_mod()
+    p, a = good_case()
+    b = m.BwdArgs()
+    b.fwd = a
+    xs = [a.x.stride[i] for i in range(4)]
+    for f in ("dy", "dx", "dz"):
+        setattr(b, f, _fake(a.x.dtype, xs))
+    for f in ("dB", "dC"):
+        setattr(b, f, _fake(a.x.dtype, [a.B.stride[i] for i in range(4)]))
+    b.ddt = _fake(m.SSD_F32, [a.dt.stride[i] for i in range(3)])
+    for f in ("dA", "dD", "ddt_bias"):
+        setattr(b, f, _fake(m.SSD_F32, [1]))
+    n = ctypes.c_size_t(0)
+    assert m.load().ssd_bwd_workspace_size(ctypes.byref(p), ctypes.byref(b), ctypes.byref(n)) == 0
+    b.dz = m.Tensor()      # z given but dz missing
+    assert m.load().ssd_bwd_workspace_size(ctypes.byref(p), ctypes.byref(b), ctypes.byref(n)) == 1
+
+
+def test_metadata_reference_builder():
+    from oracle import meta
+    m = meta.build(cu=[0, 5, 5, 300], Q=64, R=2)
+    assert m["chunks"] == [(0, 0, 0, 5), (2, 0, 5, 64), (2, 0, 69, 64), (2, 0, 133, 64), (2, 0, 197, 64),
+                           (2, 0, 261, 39)]
+    assert [u[:5] for u in m["units"]] == [(0, 0, 0, 5, 1), (2, 0, 5, 128, 2), (2, 0, 133, 128, 2), (2, 0, 261, 39, 1)]
+    assert [u[5] for u in m["units"]] == [-1, -1, 1, 2]
+    assert [u[6] for u in m["units"]] == [1, 0, 0, 1]

@@ -1,0 +1,75 @@
+"""Backward parity of the CUDA path against the oracle's adjoint (GPU).
+
+The oracle's gradients are pinned on CPU by central differences and by torch
+autograd of the quadratic form (tests/test_oracle_grad.py).
+"""
+import numpy as np
+import pytest
+import torch
+
+from state_space_model_scan_gb300 import inputs as I
+from helpers import TOL, rel_l2, gpu_backward, oracle_backward, flat
+
+pytestmark = pytest.mark.gpu
+
+NAMES = [("dx", "dx"), ("ddt", "ddt_raw"), ("dA", "dA"), ("dB", "dB"), ("dC", "dC"), ("dD", "dD"), ("dz", "dz"),
+         ("ddt_bias", "ddt_bias"), ("dinitial_states", "dinit")]
+
+
+def W(name="t", B=1, L=256, H=4, P=16, G=1, N=16, Q=64, dtype="f32", **kw):
+    return I.Workload(name, B, L, H, P, G, N, Q, dtype, **kw)
+
+
+def check_bwd(w, algo="auto", with_dfinal=True, tol=None):
+    inp = I.make_inputs(w, with_grad_inputs=True, with_dfinal=with_dfinal)
+    g = gpu_backward(w, inp, algo=algo)
+    o = oracle_backward(w, inp)
+    T = w.batch * w.seqlen
+    tol = tol or TOL[w.dtype]
+    errs = {}
+    for gn, on in NAMES:
+        if gn not in g:
+            assert on not in o
+            continue
+        t = g[gn]
+        a = flat(t, T) if t.dim() >= 3 and t.shape[0] == w.batch and gn not in ("dinitial_states",) else \
+            t.detach().double().cpu().numpy()
+        b = o[on]
+        a = a.reshape(b.shape)
+        assert np.isfinite(a).all(), gn
+        errs[gn] = rel_l2(a, b)
+    bad = {k: v for k, v in errs.items() if v > tol}
+    assert not bad, (w, errs)
+    return errs
+
+
+@pytest.mark.parametrize("case", [
+    dict(),
+    dict(L=1), dict(L=70), dict(L=129, H=6, G=2, has_z=True, has_init=True),
+    dict(B=2, L=100, H=6, G=3, P=32, N=32, has_z=True, has_init=True),
+    dict(P=128, N=128, L=90, H=2, has_z=True),
+    dict(has_D=False, has_dt_bias=False, L=77),
+])
+def test_bwd_fp32(case):
+    check_bwd(W(**case))
+
+
+@pytest.mark.parametrize("case", [
+    dict(L=600, H=8, P=64, G=2, N=128, Q=128, has_z=True, has_init=True),
+])
+def test_bwd_bf16(case):
+    check_bwd(W(dtype="bf16", **case))
+
+
+def test_bwd_varlen():
+    w = I.Workload("v", 1, 241, 4, 16, 2, 16, 64, "f32", has_z=True, has_init=True, seqlens=[40, 0, 130, 1, 70])
+    check_bwd(w)
+
+
+def test_bwd_deterministic():
+    w = W(L=300, H=4, P=32, G=2, N=32, dtype="bf16", has_z=True, has_init=True)
+    inp = I.make_inputs(w, with_grad_inputs=True, with_dfinal=True)
+    g1 = gpu_backward(w, inp)
+    g2 = gpu_backward(w, inp)
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k

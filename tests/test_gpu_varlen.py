@@ -1,0 +1,105 @@
+"""Packed variable-length sequences (cu_seqlens) on the GPU: bit-exact metadata,
+parity with the oracle, packed == separate runs, empty sequences, and bad
+cu_seqlens contents reported through the device status word."""
+import numpy as np
+import pytest
+import torch
+
+from state_space_model_scan_gb300 import inputs as I
+from state_space_model_scan_gb300 import _lib
+from helpers import TOL, rel_l2, gpu_forward, oracle_forward, flat, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def VW(lens, H=4, P=16, G=2, N=16, dtype="f32", **kw):
+    return I.Workload("v", 1, sum(lens), H, P, G, N, 64, dtype, has_init=True, seqlens=list(lens), **kw)
+
+
+def run_staged_meta(w, inp):
+    d = to_dev(inp)
+    y = torch.empty_like(d["x"])
+    S = w.nseqs
+    fin = torch.empty(S, w.nheads, w.headdim, w.dstate, device="cuda")
+    prob = _lib.problem(1, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, 64, S, "staged")
+    args = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                         initial_states=d["initial_states"], final_states=fin, cu_seqlens=d["cu_seqlens"])
+    n = _lib.fwd_workspace_size(prob, args)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    _lib.check(_lib.ssd_fwd(prob, args, ws), "ssd_fwd")
+    torch.cuda.synchronize()
+    return ws, _lib.debug_layout(prob, args), y, fin, prob, args
+
+
+def test_chunk_metadata_bit_exact():
+    from oracle import meta
+    lens = [5, 0, 300, 64, 1, 128, 0, 77]
+    w = VW(lens)
+    inp = I.make_inputs(w)
+    ws, lay, *_ = run_staged_meta(w, inp)
+    raw = ws.cpu().numpy()
+    counts = raw[lay.meta_counts:lay.meta_counts + 16].view(np.int32)
+    ref = meta.build(cu=inp["cu_seqlens"].tolist(), Q=lay.qi)
+    assert counts[0] == len(ref["chunks"]) and counts[3] == 0
+    got = raw[lay.chunk_info:lay.chunk_info + 16 * counts[0]].view(np.int32).reshape(-1, 4)
+    assert np.array_equal(got, np.array(ref["chunks"], dtype=np.int32))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_varlen_matches_oracle(dtype):
+    w = VW([40, 0, 130, 1, 70, 64, 129], dtype=dtype, has_z=True)
+    inp = I.make_inputs(w)
+    y, fin = gpu_forward(w, inp)
+    yo, fo = oracle_forward(w, inp)
+    assert rel_l2(flat(y, w.seqlen), yo) <= TOL[dtype]
+    assert rel_l2(fin.double().cpu().numpy(), fo) <= TOL[dtype]
+
+
+def test_packed_equals_separate_runs():
+    lens = [50, 130, 7]
+    w = VW(lens, dtype="bf16")
+    inp = I.make_inputs(w)
+    y, fin = gpu_forward(w, inp)
+    cu = inp["cu_seqlens"].tolist()
+    for s in range(3):
+        a = dict(inp)
+        for k in ("x", "dt_raw", "B", "C"):
+            a[k] = inp[k][:, cu[s]:cu[s + 1]].contiguous()
+        a["z"] = None
+        a["initial_states"] = inp["initial_states"][s:s + 1]
+        a["cu_seqlens"] = None
+        ws = I.Workload("s", 1, lens[s], w.nheads, w.headdim, w.ngroups, w.dstate, 64, "bf16", has_init=True)
+        ys, fs = gpu_forward(ws, a)
+        assert torch.equal(ys, y[:, cu[s]:cu[s + 1]])
+        assert torch.equal(fs[0], fin[s])
+
+
+def test_empty_sequences_return_initial_state():
+    w = VW([0, 10, 0])
+    inp = I.make_inputs(w)
+    y, fin = gpu_forward(w, inp)
+    assert torch.equal(fin[0].cpu(), inp["initial_states"][0])
+    assert torch.equal(fin[2].cpu(), inp["initial_states"][2])
+
+
+@pytest.mark.parametrize("bad", [[0, 10, 5, 20], [1, 10, 20], [0, 10, 19]])
+def test_bad_cu_seqlens_reported_on_device(bad):
+    """Contents of cu_seqlens live on the device: the metadata kernel validates them,
+    writes SSD_ERR_INVALID_ARGUMENT to the workspace status word and no other
+    kernel touches the outputs."""
+    L = 20
+    w = I.Workload("bad", 1, L, 2, 16, 1, 16, 64, "f32", has_init=True, seqlens=[L])
+    inp = I.make_inputs(w)
+    d = to_dev(inp)
+    S = len(bad) - 1
+    cu = torch.tensor(bad, dtype=torch.int32, device="cuda")
+    y = torch.full_like(d["x"], 7.0)
+    fin = torch.full((S, 2, 16, 16), 7.0, device="cuda")
+    init = torch.zeros(S, 2, 16, 16, device="cuda")
+    prob = _lib.problem(1, L, 2, 16, 1, 16, 64, S, "staged")
+    args = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], dt_bias=d["dt_bias"],
+                         initial_states=init, final_states=fin, cu_seqlens=cu)
+    ws = torch.empty(_lib.fwd_workspace_size(prob, args), dtype=torch.uint8, device="cuda")
+    assert _lib.ssd_fwd(prob, args, ws) == 0
+    assert _lib.query_status(ws) == 1
+    assert (y == 7.0).all() and (fin == 7.0).all()
