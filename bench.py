@@ -1,0 +1,380 @@
+"""Benchmark of the SSD scan hot path on GB300.
+
+One step = one forward (metadata + fused tensor-core forward) and one backward
+of the Nemotron-Nano-shaped workload (batch 1, L=8192, 64 heads x 64, 8 groups,
+dstate 128, chunk 128, z gate and D skip, bf16 x/B/C/z, fp32 dt/A/D/states),
+each replayed from a CUDA graph, with L2 flushed (256 MB write) before each step.
+`value` is forward tokens/s from CUDA events around the forward; `ms_per_step`
+is forward + backward device time.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the float64 CPU oracle (the reference arm of this build)
+on a bounded sample of the same workload on the host cores.  With N > 1 (under
+torchrun) every rank runs an independent replica (the scan does not shard:
+replicas only) and rank 0 reports the aggregate over ranks.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ssd_fwd_tokens_per_s"
+WORKLOAD = "nemotron_nano"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def workload_desc(w):
+    return ("Mamba-2 SSD fwd+bwd, batch %d, L=%d, %d heads x %d, %d groups, dstate %d, chunk %d, z gate + D skip, "
+            "bf16 x/B/C/z, fp32 dt/A/D/states" % (w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate,
+                                                  w.chunk_size))
+
+
+def algorithmic_bytes(w, fwd=True):
+    """Compulsory HBM bytes of one forward (or backward) of workload w."""
+    b_x = 2 if w.dtype == "bf16" else 4
+    T = w.batch * w.seqlen
+    per_tok_heads = w.nheads * w.headdim * b_x
+    bc = 2 * w.ngroups * w.dstate * b_x
+    st = w.nseqs * w.nheads * w.headdim * w.dstate * 4
+    if fwd:
+        n = T * ((3 if w.has_z else 2) * per_tok_heads + bc + 4 * w.nheads) + st   # x, z, y, B, C, dt, final
+        if w.has_init:
+            n += st
+        return n
+    # backward: read x, z, B, C, dt, dy; write dx, dz, dB, dC, ddt
+    nz = 2 if w.has_z else 0
+    return T * ((4 + nz) * per_tok_heads + 2 * bc + 2 * 4 * w.nheads)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), "measured"
+    return 6800.0, "fallback"
+
+
+def profile_traffic(kernel_src):
+    """Per-launch DRAM bytes of the fused forward from the committed ncu summary,
+    or None when the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "fused_fwd_nemotron_nano.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", txt)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m or not t:
+        return None
+    cur = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return float(t.group(1)) if m.group(1) == cur else None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(w, seconds_budget=20.0):
+    """Time the float64 oracle forward on a bounded sample of the workload:
+    all tokens of a few heads (heads are independent), scaled to tokens/s of the
+    full workload.  Uses every host core (OpenMP over heads)."""
+    import numpy as np
+    from state_space_model_scan_gb300 import inputs as I
+    from oracle import sequential
+    inp = I.make_inputs(w)
+    o = I.to_oracle(inp, w)
+    cores = os.cpu_count() or 1
+    # all heads when that stays within the bound, else as many as there are cores
+    nheads = w.nheads if w.nheads <= 4 * cores else max(1, min(w.nheads, cores))
+    heads = list(range(nheads))
+    t0 = time.perf_counter()
+    sequential.forward(o["x"], o["dt_raw"], o["A"], o["B"], o["C"], D=o["D"], z=o["z"], dt_bias=o["dt_bias"],
+                       init=o["init"], cu=o["cu"], heads=heads, threads=cores)
+    dt = time.perf_counter() - t0
+    tok_per_s = (w.batch * w.seqlen) * (nheads / w.nheads) / dt
+    return {"value": tok_per_s, "unit": "tokens/s", "cores": min(cores, nheads), "kind": "oracle",
+            "sample": "float64 sequential oracle forward, all %d tokens of %d of %d heads (%.2f s), scaled by "
+                      "heads" % (w.batch * w.seqlen, nheads, w.nheads, dt),
+            "threads": sequential.num_threads()}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from state_space_model_scan_gb300 import inputs as I
+    w = I.named(WORKLOAD)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_sample(w)
+        if i >= args.warmup:
+            vals.append(r)
+    v = sum(r["value"] for r in vals) / len(vals)
+    toks = w.batch * w.seqlen
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * toks / v, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w) + " (forward only on the oracle)", "global_batch": w.batch,
+                       "seq_len": w.seqlen},
+            "cpu_baseline": dict(vals[-1], value=v),
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device() if world == 1 else local)
+    from state_space_model_scan_gb300 import inputs as I
+    from state_space_model_scan_gb300 import _lib
+    from state_space_model_scan_gb300.api import Workspace
+    w = I.named(WORKLOAD)
+    inp = I.make_inputs(w, with_grad_inputs=True)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    Bsz, L, H, P, G, N = w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate
+    y = torch.empty_like(d["x"])
+    fin = torch.empty(Bsz, H, P, N, dtype=torch.float32, device=dev)
+    prob = _lib.problem(Bsz, L, H, P, G, N, w.chunk_size)
+    fargs = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                          final_states=fin)
+    g = dict(dx=torch.empty_like(d["x"]), ddt=torch.empty_like(d["dt_raw"]),
+             dA=torch.empty(H, device=dev), dB=torch.empty_like(d["B"]), dC=torch.empty_like(d["C"]),
+             dD=torch.empty(H, device=dev), dz=torch.empty_like(d["z"]), ddt_bias=torch.empty(H, device=dev))
+    bfa = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], None, D=d["D"], z=d["z"], dt_bias=d["dt_bias"])
+    bargs = _lib.bwd_args(bfa, d["dy"], g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], dD=g["dD"], dz=g["dz"],
+                          ddt_bias=g["ddt_bias"])
+    wsf = torch.empty(_lib.fwd_workspace_size(prob, fargs), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(_lib.bwd_workspace_size(prob, bargs), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    s = torch.cuda.Stream(device=dev)
+    # warm the calls once outside capture (module load, attributes)
+    with torch.cuda.stream(s):
+        _lib.check(_lib.ssd_fwd(prob, fargs, wsf, s), "ssd_fwd")
+        _lib.check(_lib.ssd_bwd(prob, bargs, wsb, s), "ssd_bwd")
+    s.synchronize()
+    gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gf, stream=s):
+        _lib.check(_lib.ssd_fwd(prob, fargs, wsf, torch.cuda.current_stream()), "ssd_fwd")
+    with torch.cuda.graph(gb, stream=s):
+        _lib.check(_lib.ssd_bwd(prob, bargs, wsb, torch.cuda.current_stream()), "ssd_bwd")
+    launches_fwd, launches_bwd = 2, 10   # metadata + fused forward; staged backward pipeline
+
+    def step(ev=None):
+        with torch.cuda.stream(s):
+            flush.fill_(float(rank + 1))
+            if ev is not None:
+                ev[0].record(s)
+            gf.replay()
+            if ev is not None:
+                ev[1].record(s)
+            gb.replay()
+            if ev is not None:
+                ev[2].record(s)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    fwd_mean = sum(fwd_ms) / len(fwd_ms)
+    step_mean = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / len(fwd_ms)
+    if world > 1:
+        t = torch.tensor([fwd_mean, step_mean], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        fwd_mean, step_mean = float(t[0]), float(t[1])
+    toks = w.batch * w.seqlen
+    value = world * toks / (fwd_mean * 1e-3)
+
+    # end to end through the C ABI with host buffers: pinned H2D of the inputs, forward, D2H of y
+    host = {k: d[k].cpu().pin_memory() for k in ("x", "dt_raw", "B", "C", "z")}
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y_host.numel() * y_host.element_size()
+
+    def e2e_step():
+        with torch.cuda.stream(s):
+            for k, t in host.items():
+                d[k].copy_(t, non_blocking=True)
+            _lib.check(_lib.ssd_fwd(prob, fargs, wsf, s), "ssd_fwd")
+            y_host.copy_(y, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_val = world * toks / (e2e_ms * 1e-3)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = measured_peaks()
+    alg = algorithmic_bytes(w, fwd=True)
+    achieved = alg / (fwd_mean * 1e-3) / 1e9
+    traffic = profile_traffic(os.path.join(ROOT, "state_space_model_scan_gb300", "csrc", "fused_fwd.cu"))
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_mean, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "global_batch": w.batch * world, "seq_len": w.seqlen,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed before every step (256 MB write)", "timing": "CUDA graph replay, CUDA events"},
+        "fwd_ms": fwd_mean, "fwd_bwd_ms": step_mean, "bwd_ms": step_mean - fwd_mean,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "ssd_fwd (metadata + fused tensor-core forward)",
+                     "algorithmic_bytes_per_launch": alg, "peak_source": peak_kind},
+        "bwd_roofline": {"bound": "hbm", "achieved": algorithmic_bytes(w, fwd=False) / ((step_mean - fwd_mean) * 1e-3)
+                         / 1e9, "peak": peak, "unit": "GB/s",
+                         "algorithmic_bytes_per_launch": algorithmic_bytes(w, fwd=False)},
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (launches_fwd + launches_bwd),
+        "clocks": clk.summary(),
+        "wall_s": wall,
+    }
+    line["roofline"]["frac"] = achieved / peak
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w)
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_fwd_only(args):
+    """Forward only, plain calls (no graph, no backward): the command the ncu captures run."""
+    import torch
+    from state_space_model_scan_gb300 import inputs as I
+    from state_space_model_scan_gb300.api import ssd_forward, Workspace
+    w = I.named(WORKLOAD)
+    inp = I.make_inputs(w)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    ws = Workspace()
+    y = torch.empty_like(d["x"])
+    fin = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for i in range(args.warmup + args.steps):
+        e0.record()
+        ssd_forward(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                    chunk_size=w.chunk_size, workspace=ws, y=y, final_states=fin, seg_chunks=args.seg_chunks)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    print(json.dumps({"mode": "fwd", "workload": WORKLOAD, "fwd_ms": times,
+                      "tokens_per_s": w.batch * w.seqlen / (sum(times) / len(times) * 1e-3)}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="bench", choices=["bench", "fwd"])
+    ap.add_argument("--seg-chunks", type=int, default=0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.mode == "fwd":
+        run_fwd_only(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -94,7 +94,7 @@ typedef struct {
 typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs;
     int32_t algo;        /* ssd_algo */
-    int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..16 */
+    int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..8 */
 } ssd_problem;
 
 typedef struct {
@@ -163,12 +163,17 @@ int32_t ssd_abi_version(void);
  *   dt          : f32[n_chunks][nheads][qi]   softplus(dt_raw + dt_bias), 0 past the chunk's length
  *   cs          : f32[n_chunks][nheads][qi]   inclusive in-chunk cumulative sum of dt*A
  *   states      : f32[n_chunks][nheads][headdim][dstate]  carry-in state of each chunk
+ *   units       : int32[n_units][8] (fused path) {seq, batch row, first token, token count,
+ *                 chunk count, index of the sequence's previous unit or -1, 1 if last unit
+ *                 of its sequence, segment index j}; segment j of a sequence is its chunks
+ *                 [j*R, (j+1)*R); segments are grouped in blocks of 8 and units are listed
+ *                 by (block, sequence, segment)
  * where qi is the internal chunk length written to *qi.  Chunks are listed
  * sequence by sequence, in order, each sequence cut into qi-token chunks from its
  * first token (the last one ragged).  Offsets of -1 mean "not produced by algo".
  */
 typedef struct {
-    int64_t meta_counts, chunk_info, dt, cs, states;
+    int64_t meta_counts, chunk_info, dt, cs, states, units;
     int64_t qi;
 } ssd_debug_layout;
 ssd_status ssd_fwd_debug_layout(const ssd_problem *prob, const ssd_fwd_args *args, ssd_debug_layout *out);

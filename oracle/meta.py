@@ -10,13 +10,13 @@ sequence's first token, so no chunk mixes two sequences):
 * its chunks are [t0 + c Q, t0 + min((c+1) Q, len)) for c = 0 .. ceil(len/Q)-1,
   listed sequence by sequence -> rows (seq, b, first token, length);
 * its work units group R consecutive chunks: unit (s, j) covers chunks
-  j R .. min((j+1) R, nchunks)-1; units are listed by j, then s -> rows
-  (seq, b, first token, token count, chunk count, index of unit (s, j-1) or -1,
-  1 if last unit of s, index of its first chunk).
+  j R .. min((j+1) R, nchunks)-1; segments j are grouped in blocks of KB;
+  units are listed by (block, s, j) -> rows (seq, b, first token, token count,
+  chunk count, index of unit (s, j-1) or -1, 1 if last unit of s, j).
 """
 
 
-def build(cu=None, batch=1, seqlen=0, Q=64, R=1):
+def build(cu=None, batch=1, seqlen=0, Q=64, R=1, KB=8):
     if cu is None:
         seqs = [(b, 0, seqlen) for b in range(batch)]
     else:
@@ -31,12 +31,12 @@ def build(cu=None, batch=1, seqlen=0, Q=64, R=1):
     units = []
     last = {}
     nseg = [-(-(-(-n // Q)) // R) for (_, _, n) in seqs]
-    for j in range(max(nseg) if nseg else 0):
+    maxseg = max(nseg) if nseg else 0
+    for blk in range(-(-maxseg // KB)):
         for s, (b, t0, n) in enumerate(seqs):
-            if nseg[s] <= j:
-                continue
             nch = -(-n // Q)
-            units.append((s, b, t0 + j * R * Q, min(R * Q, n - j * R * Q), min(R, nch - j * R),
-                          last.get(s, -1) if j > 0 else -1, 1 if j == nseg[s] - 1 else 0, chunk0[s] + j * R))
-            last[s] = len(units) - 1
+            for j in range(blk * KB, min((blk + 1) * KB, nseg[s])):
+                units.append((s, b, t0 + j * R * Q, min(R * Q, n - j * R * Q), min(R, nch - j * R),
+                              last.get(s, -1) if j > 0 else -1, 1 if j == nseg[s] - 1 else 0, j))
+                last[s] = len(units) - 1
     return dict(seqs=[(b, t0, n, chunk0[s]) for s, (b, t0, n) in enumerate(seqs)], chunks=chunks, units=units)

@@ -127,11 +127,11 @@ int ssd_oracle_fwd(const ssd_oracle_in *in, double *y, double *final_states, int
 }
 
 /*
- * Adjoint.  Work is split by (sequence, group) so that dB/dC rows of a
- * (sequence, group) are owned by one task; the heads of the group run in
- * ascending order inside the task.  Per-head scalars (dA, dD, ddt_bias) are
- * accumulated per (sequence, head) and summed over sequences in order at the
- * end, so the result does not depend on the thread count.
+ * Adjoint.  Work is split by (sequence, head).  Each task writes its head's dB/dC
+ * contributions into a private buffer; afterwards the buffers of the heads of
+ * each group are summed in ascending head order, and the per-head scalars
+ * (dA, dD, ddt_bias) are summed over sequences in order -- so the result does
+ * not depend on the thread count.
  */
 int ssd_oracle_bwd(const ssd_oracle_in *in, const double *dy, const double *dfinal,
                    double *dx, double *ddt_raw, double *dA, double *dB, double *dC,
@@ -151,14 +151,18 @@ int ssd_oracle_bwd(const ssd_oracle_in *in, const double *dy, const double *dfin
     double *pA = (double *)calloc((size_t)(S * H), sizeof(double));
     double *pD = (double *)calloc((size_t)(S * H), sizeof(double));
     double *pBias = (double *)calloc((size_t)(S * H), sizeof(double));
-    if (!pA || !pD || !pBias) { free(pA); free(pD); free(pBias); return 2; }
-    /* dB/dC are accumulated over heads: clear the rows of every sequence. */
-    memset(dB, 0, sizeof(double) * (size_t)(T * G * N));
-    memset(dC, 0, sizeof(double) * (size_t)(T * G * N));
+    /* per-head dB/dC rows: [H][T][N], only touched for computed heads */
+    double *hB = (double *)calloc((size_t)(H * T * N) + 1, sizeof(double));
+    double *hC = (double *)calloc((size_t)(H * T * N) + 1, sizeof(double));
+    if (!pA || !pD || !pBias || !hB || !hC) {
+        free(pA); free(pD); free(pBias); free(hB); free(hC);
+        return 2;
+    }
     int err = 0;
 #pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t sg = 0; sg < S * G; ++sg) {
-        const int64_t s = sg / G, g = sg % G;
+    for (int64_t sh = 0; sh < S * H; ++sh) {
+        const int64_t s = sh / H, h = sh % H, g = h / hpg;
+        if (!head_on(in, h)) continue;
         const int64_t t0 = in->cu[s], t1 = in->cu[s + 1], len = t1 - t0;
         const int64_t nck = len / ckpt + 1;
         double *ck = (double *)malloc(sizeof(double) * PN * (size_t)nck);
@@ -171,102 +175,114 @@ int ssd_oracle_bwd(const ssd_oracle_in *in, const double *dy, const double *dfin
             err = 2;
             continue;
         }
-        for (int64_t h = g * hpg; h < (g + 1) * hpg; ++h) {
-            if (!head_on(in, h)) continue;
-            const double Ah = in->A[h];
-            const double Dh = in->D ? in->D[h] : 0.0;
-            /* forward: checkpoints ck[k] = state before token t0 + k*ckpt */
-            double *st = seg; /* scratch */
-            if (in->init) memcpy(st, in->init + (s * H + h) * PN, sizeof(double) * PN);
-            else memset(st, 0, sizeof(double) * PN);
-            for (int64_t k = 0; k < len; ++k) {
-                if (k % ckpt == 0) memcpy(ck + (size_t)(k / ckpt) * PN, st, sizeof(double) * PN);
-                fwd_step(in, t0 + k, h, g, st, ypre, NULL, NULL, NULL);
-            }
-            /* reverse sweep */
-            if (dfinal) memcpy(Gs, dfinal + (s * H + h) * PN, sizeof(double) * PN);
-            else memset(Gs, 0, sizeof(double) * PN);
-            double accA = 0.0, accD = 0.0, accBias = 0.0;
-            for (int64_t sgi = (len > 0 ? (len - 1) / ckpt : -1); sgi >= 0; --sgi) {
-                const int64_t k0 = sgi * ckpt;
-                const int64_t k1 = (k0 + ckpt < len) ? k0 + ckpt : len;
-                /* seg[j] = state before token k0+j, j = 0..k1-k0 */
-                memcpy(seg, ck + (size_t)sgi * PN, sizeof(double) * PN);
-                for (int64_t k = k0; k < k1; ++k) {
-                    double *nx = seg + (size_t)(k - k0 + 1) * PN;
-                    memcpy(nx, seg + (size_t)(k - k0) * PN, sizeof(double) * PN);
-                    fwd_step(in, t0 + k, h, g, nx, ypre, NULL, NULL, NULL);
-                }
-                for (int64_t k = k1 - 1; k >= k0; --k) {
-                    const int64_t t = t0 + k;
-                    const double *hprev = seg + (size_t)(k - k0) * PN;
-                    const double *hcur = seg + (size_t)(k - k0 + 1) * PN;
-                    double v = in->dt_raw[t * H + h] + (in->dt_bias ? in->dt_bias[h] : 0.0);
-                    double dt = softplus(v);
-                    double a = exp(dt * Ah);
-                    const double *xr = in->x + (t * H + h) * P;
-                    const double *br = in->Bm + (t * G + g) * N;
-                    const double *cr = in->Cm + (t * G + g) * N;
-                    const double *dyr = dy + (t * H + h) * P;
-                    /* ypre recomputed from h_t */
-                    for (int64_t p = 0; p < P; ++p) {
-                        double acc = 0.0;
-                        for (int64_t n = 0; n < N; ++n) acc += cr[n] * hcur[p * N + n];
-                        ypre[p] = acc + Dh * xr[p];
-                    }
-                    if (in->z) {
-                        const double *zr = in->z + (t * H + h) * P;
-                        double *dzr = dz + (t * H + h) * P;
-                        for (int64_t p = 0; p < P; ++p) {
-                            double sg_ = sigmoid(zr[p]);
-                            dyp[p] = dyr[p] * zr[p] * sg_;
-                            dzr[p] = dyr[p] * ypre[p] * sg_ * (1.0 + zr[p] * (1.0 - sg_));
-                        }
-                    } else {
-                        for (int64_t p = 0; p < P; ++p) dyp[p] = dyr[p];
-                    }
-                    /* dL/dh_t += C_t (outer) dypre ; dC_t += dypre . h_t */
-                    double *dcr = dC + (t * G + g) * N;
-                    for (int64_t p = 0; p < P; ++p) {
-                        double *grow = Gs + p * N;
-                        const double *hrow = hcur + p * N;
-                        for (int64_t n = 0; n < N; ++n) {
-                            grow[n] += cr[n] * dyp[p];
-                            dcr[n] += dyp[p] * hrow[n];
-                        }
-                        accD += dyp[p] * xr[p];
-                    }
-                    /* through h_t = a h_{t-1} + dt x (outer) B */
-                    double *dxr = dx + (t * H + h) * P;
-                    double *dbr = dB + (t * G + g) * N;
-                    double ddt = 0.0, dAa = 0.0;
-                    for (int64_t p = 0; p < P; ++p) {
-                        const double *grow = Gs + p * N;
-                        const double *hrow = hprev + p * N;
-                        double gb = 0.0;
-                        for (int64_t n = 0; n < N; ++n) {
-                            gb += grow[n] * br[n];
-                            dbr[n] += dt * grow[n] * xr[p];
-                            dAa += grow[n] * hrow[n];
-                        }
-                        dxr[p] = Dh * dyp[p] + dt * gb;
-                        ddt += xr[p] * gb;
-                    }
-                    /* dAa = <G, h_{t-1}>; d a_t contributes via a = exp(dt*A) */
-                    ddt += dAa * a * Ah;
-                    accA += dAa * a * dt;
-                    double dv = ddt * sigmoid(v);
-                    ddt_raw[t * H + h] = dv;
-                    accBias += dv;
-                    for (size_t i = 0; i < PN; ++i) Gs[i] *= a;
-                }
-            }
-            if (dinit) memcpy(dinit + (s * H + h) * PN, Gs, sizeof(double) * PN);
-            pA[s * H + h] = accA;
-            pD[s * H + h] = accD;
-            pBias[s * H + h] = accBias;
+        const double Ah = in->A[h];
+        const double Dh = in->D ? in->D[h] : 0.0;
+        /* forward: checkpoints ck[k] = state before token t0 + k*ckpt */
+        double *st = seg; /* scratch */
+        if (in->init) memcpy(st, in->init + (s * H + h) * PN, sizeof(double) * PN);
+        else memset(st, 0, sizeof(double) * PN);
+        for (int64_t k = 0; k < len; ++k) {
+            if (k % ckpt == 0) memcpy(ck + (size_t)(k / ckpt) * PN, st, sizeof(double) * PN);
+            fwd_step(in, t0 + k, h, g, st, ypre, NULL, NULL, NULL);
         }
+        /* reverse sweep */
+        if (dfinal) memcpy(Gs, dfinal + (s * H + h) * PN, sizeof(double) * PN);
+        else memset(Gs, 0, sizeof(double) * PN);
+        double accA = 0.0, accD = 0.0, accBias = 0.0;
+        for (int64_t sgi = (len > 0 ? (len - 1) / ckpt : -1); sgi >= 0; --sgi) {
+            const int64_t k0 = sgi * ckpt;
+            const int64_t k1 = (k0 + ckpt < len) ? k0 + ckpt : len;
+            /* seg[j] = state before token k0+j, j = 0..k1-k0 */
+            memcpy(seg, ck + (size_t)sgi * PN, sizeof(double) * PN);
+            for (int64_t k = k0; k < k1; ++k) {
+                double *nx = seg + (size_t)(k - k0 + 1) * PN;
+                memcpy(nx, seg + (size_t)(k - k0) * PN, sizeof(double) * PN);
+                fwd_step(in, t0 + k, h, g, nx, ypre, NULL, NULL, NULL);
+            }
+            for (int64_t k = k1 - 1; k >= k0; --k) {
+                const int64_t t = t0 + k;
+                const double *hprev = seg + (size_t)(k - k0) * PN;
+                const double *hcur = seg + (size_t)(k - k0 + 1) * PN;
+                double v = in->dt_raw[t * H + h] + (in->dt_bias ? in->dt_bias[h] : 0.0);
+                double dt = softplus(v);
+                double a = exp(dt * Ah);
+                const double *xr = in->x + (t * H + h) * P;
+                const double *br = in->Bm + (t * G + g) * N;
+                const double *cr = in->Cm + (t * G + g) * N;
+                const double *dyr = dy + (t * H + h) * P;
+                /* ypre recomputed from h_t */
+                for (int64_t p = 0; p < P; ++p) {
+                    double acc = 0.0;
+                    for (int64_t n = 0; n < N; ++n) acc += cr[n] * hcur[p * N + n];
+                    ypre[p] = acc + Dh * xr[p];
+                }
+                if (in->z) {
+                    const double *zr = in->z + (t * H + h) * P;
+                    double *dzr = dz + (t * H + h) * P;
+                    for (int64_t p = 0; p < P; ++p) {
+                        double sg_ = sigmoid(zr[p]);
+                        dyp[p] = dyr[p] * zr[p] * sg_;
+                        dzr[p] = dyr[p] * ypre[p] * sg_ * (1.0 + zr[p] * (1.0 - sg_));
+                    }
+                } else {
+                    for (int64_t p = 0; p < P; ++p) dyp[p] = dyr[p];
+                }
+                /* dL/dh_t += C_t (outer) dypre ; dC_t += dypre . h_t */
+                double *dcr = hC + ((size_t)h * (size_t)T + (size_t)t) * (size_t)N;
+                for (int64_t p = 0; p < P; ++p) {
+                    double *grow = Gs + p * N;
+                    const double *hrow = hcur + p * N;
+                    for (int64_t n = 0; n < N; ++n) {
+                        grow[n] += cr[n] * dyp[p];
+                        dcr[n] += dyp[p] * hrow[n];
+                    }
+                    accD += dyp[p] * xr[p];
+                }
+                /* through h_t = a h_{t-1} + dt x (outer) B */
+                double *dxr = dx + (t * H + h) * P;
+                double *dbr = hB + ((size_t)h * (size_t)T + (size_t)t) * (size_t)N;
+                double ddt = 0.0, dAa = 0.0;
+                for (int64_t p = 0; p < P; ++p) {
+                    const double *grow = Gs + p * N;
+                    const double *hrow = hprev + p * N;
+                    double gb = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        gb += grow[n] * br[n];
+                        dbr[n] += dt * grow[n] * xr[p];
+                        dAa += grow[n] * hrow[n];
+                    }
+                    dxr[p] = Dh * dyp[p] + dt * gb;
+                    ddt += xr[p] * gb;
+                }
+                /* dAa = <G, h_{t-1}>; d a_t contributes via a = exp(dt*A) */
+                ddt += dAa * a * Ah;
+                accA += dAa * a * dt;
+                double dv = ddt * sigmoid(v);
+                ddt_raw[t * H + h] = dv;
+                accBias += dv;
+                for (size_t i = 0; i < PN; ++i) Gs[i] *= a;
+            }
+        }
+        if (dinit) memcpy(dinit + (s * H + h) * PN, Gs, sizeof(double) * PN);
+        pA[s * H + h] = accA;
+        pD[s * H + h] = accD;
+        pBias[s * H + h] = accBias;
         free(ck); free(seg); free(Gs); free(ypre); free(dyp);
+    }
+    /* dB/dC: heads of each group summed in ascending order */
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t g = 0; g < G; ++g) {
+            double *ob = dB + (t * G + g) * N;
+            double *oc = dC + (t * G + g) * N;
+            for (int64_t n = 0; n < N; ++n) { ob[n] = 0.0; oc[n] = 0.0; }
+            for (int64_t h = g * hpg; h < (g + 1) * hpg; ++h) {
+                if (!head_on(in, h)) continue;
+                const double *sb = hB + ((size_t)h * (size_t)T + (size_t)t) * (size_t)N;
+                const double *sc = hC + ((size_t)h * (size_t)T + (size_t)t) * (size_t)N;
+                for (int64_t n = 0; n < N; ++n) { ob[n] += sb[n]; oc[n] += sc[n]; }
+            }
+        }
     }
     for (int64_t h = 0; h < H; ++h) {
         double a = 0.0, d = 0.0, b = 0.0;
@@ -279,7 +295,7 @@ int ssd_oracle_bwd(const ssd_oracle_in *in, const double *dy, const double *dfin
         if (dD) dD[h] = d;
         if (ddt_bias) ddt_bias[h] = b;
     }
-    free(pA); free(pD); free(pBias);
+    free(pA); free(pD); free(pBias); free(hB); free(hC);
     return err;
 }
 

@@ -58,7 +58,8 @@ class BwdArgs(ctypes.Structure):
 
 class DebugLayout(ctypes.Structure):
     _fields_ = [("meta_counts", ctypes.c_int64), ("chunk_info", ctypes.c_int64), ("dt", ctypes.c_int64),
-                ("cs", ctypes.c_int64), ("states", ctypes.c_int64), ("qi", ctypes.c_int64)]
+                ("cs", ctypes.c_int64), ("states", ctypes.c_int64), ("units", ctypes.c_int64),
+                ("qi", ctypes.c_int64)]
 
 
 _lib = None

@@ -6,7 +6,7 @@
 
 namespace ssd {
 // meta.cu
-cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int kmax, int umax, int32_t *hdr,
+cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int KB, int kmax, int umax, int32_t *hdr,
                               SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units, int32_t *last_unit,
                               uint32_t *zero_words, int64_t n_zero, cudaStream_t st);
 cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr, const float *init,
@@ -41,6 +41,15 @@ cudaError_t launch_reduce_heads(const Shape &sh, const int32_t *hdr, const float
                                 float *dbias, cudaStream_t st);
 size_t bwd_chunk_smem(const Shape &sh);
 size_t chunk_scan_smem(const Shape &sh);
+// fused_fwd.cu
+int fused_rmax();
+int fused_block_units();
+cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *units, const void *x, const int64_t *sx,
+                             const void *Bp, const int64_t *sb, const void *Cp, const int64_t *sc, const float *dt_raw,
+                             int64_t sdb, int64_t sdl, const float *A, const float *D, const float *bias,
+                             const void *z, const int64_t *sz, void *y, const int64_t *sy, const float *init,
+                             float *final_, float *agg, float *incl, float *lam, uint32_t *flags, int grid,
+                             cudaStream_t st);
 }  // namespace ssd
 
 using namespace ssd;
@@ -48,7 +57,15 @@ using namespace ssd;
 namespace {
 
 constexpr int kSimtQ = 64;
+constexpr int kTcQ = 128;
 constexpr size_t kAlign = 256;
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -61,6 +78,7 @@ struct Plan {
     int algo = SSD_ALGO_STAGED;
     size_t off_hdr = 0, off_seqs = 0, off_chunks = 0, off_lastunit = 0, off_units = 0;
     size_t off_dt = 0, off_cs = 0, off_states = 0, off_dstates = 0, off_dBh = 0, off_dCh = 0, off_part = 0;
+    size_t off_agg = 0, off_incl = 0, off_lam = 0, off_flags = 0;
     size_t total = 0;
 };
 
@@ -115,7 +133,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     if (!pow2_in(p->chunk_size, 16, 256)) return SSD_ERR_UNSUPPORTED;
     if (!pow2_in(P, 16, 128) || !pow2_in(N, 16, 128)) return SSD_ERR_UNSUPPORTED;
     if (p->algo < SSD_ALGO_AUTO || p->algo > SSD_ALGO_FUSED) return SSD_ERR_INVALID_ARGUMENT;
-    if (p->seg_chunks < 0 || p->seg_chunks > 16) return SSD_ERR_INVALID_ARGUMENT;
+    if (p->seg_chunks < 0 || p->seg_chunks > 8) return SSD_ERR_INVALID_ARGUMENT;
     const bool varlen = a->cu_seqlens != nullptr;
     int64_t S = B;
     if (varlen) {
@@ -145,16 +163,47 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     Plan pl;
     pl.bf16 = dt_ == SSD_BF16;
     pl.varlen = varlen;
-    // Path choice: the tensor-core path is not part of this build's SIMT-only
-    // configuration; AUTO resolves to STAGED.
-    if (p->algo == SSD_ALGO_FUSED) return SSD_ERR_UNSUPPORTED;
-    pl.algo = SSD_ALGO_STAGED;
-    const int Q = kSimtQ;
+    // Path choice.  The tensor-core forward covers bf16 inputs with headdim 64 and
+    // dstate 128 whose x/B/C/z/y obey the 16-byte rule of TMA and vector access;
+    // everything else (fp32 inputs in particular) runs the SIMT pipeline.  The
+    // backward always runs the staged pipeline.
+    bool tc_ok = !bwd && pl.bf16 && P == 64 && N == 128;
+    bool aligned = true;
+    {
+        const ssd_tensor *ts[5] = {&a->x, &a->B, &a->C, &a->z, &a->y};
+        for (const ssd_tensor *t : ts) {
+            if (t->ptr == nullptr) continue;
+            if (((uintptr_t)t->ptr) % 16 != 0) aligned = false;
+            for (int i = 0; i < 3; ++i)
+                if (t->stride[i] % 8 != 0) aligned = false;
+        }
+    }
+    if (p->algo == SSD_ALGO_FUSED) {
+        if (!tc_ok) return SSD_ERR_UNSUPPORTED;
+        if (!aligned) return SSD_ERR_MISALIGNED;
+    }
+    pl.algo = (p->algo == SSD_ALGO_FUSED || (p->algo == SSD_ALGO_AUTO && tc_ok && aligned)) ? SSD_ALGO_FUSED
+                                                                                           : SSD_ALGO_STAGED;
+    const bool fused = pl.algo == SSD_ALGO_FUSED;
+    const int Q = fused ? kTcQ : kSimtQ;
     int64_t kmax = varlen ? (L + Q - 1) / Q + S : B * ((L + Q - 1) / Q);
     if (kmax > (int64_t)1 << 30) return SSD_ERR_UNSUPPORTED;
+    int R = 1;
+    int64_t umax = 0;
+    if (fused) {
+        R = p->seg_chunks;
+        if (R == 0) {
+            // enough units for about eight tickets per SM, chunks of a unit at most the compiled maximum
+            const int64_t target = 8LL * num_sms();
+            int64_t r = (kmax * H + target - 1) / target;
+            R = (int)(r < 1 ? 1 : (r > 4 ? 4 : r));
+        }
+        if (R > fused_rmax()) return SSD_ERR_UNSUPPORTED;
+        umax = varlen ? kmax / R + S : B * (((L + Q - 1) / Q + R - 1) / R);
+    }
     Shape sh;
     sh.B = (int)B; sh.L = (int)L; sh.H = (int)H; sh.P = (int)P; sh.G = (int)G; sh.N = (int)N; sh.S = (int)S;
-    sh.Q = Q; sh.hpg = (int)(H / G); sh.kmax = (int)kmax; sh.umax = 0; sh.R = 1;
+    sh.Q = Q; sh.hpg = (int)(H / G); sh.kmax = (int)kmax; sh.umax = (int)umax; sh.R = R;
     pl.sh = sh;
     Layout lay;
     pl.off_hdr = lay.take(HDR_WORDS * sizeof(int32_t));
@@ -162,9 +211,18 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     pl.off_chunks = lay.take(sizeof(ChunkInfo) * (size_t)kmax);
     pl.off_lastunit = lay.take(sizeof(int32_t) * (size_t)S);
     const size_t kh = (size_t)kmax * (size_t)H;
-    pl.off_dt = lay.take(sizeof(float) * kh * Q);
-    pl.off_cs = lay.take(sizeof(float) * kh * Q);
-    pl.off_states = lay.take(sizeof(float) * kh * (size_t)(P * N));
+    if (fused) {
+        const size_t uh = (size_t)umax * (size_t)H;
+        pl.off_units = lay.take(sizeof(UnitInfo) * (size_t)umax);
+        pl.off_agg = lay.take(sizeof(float) * uh * (size_t)(P * N));
+        pl.off_incl = lay.take(sizeof(float) * uh * (size_t)(P * N));
+        pl.off_lam = lay.take(sizeof(float) * uh);
+        pl.off_flags = lay.take(sizeof(uint32_t) * uh);
+    } else {
+        pl.off_dt = lay.take(sizeof(float) * kh * Q);
+        pl.off_cs = lay.take(sizeof(float) * kh * Q);
+        pl.off_states = lay.take(sizeof(float) * kh * (size_t)(P * N));
+    }
     if (bwd) {
         pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * N));
         pl.off_dBh = lay.take(sizeof(float) * kh * Q * (size_t)N);
@@ -223,7 +281,7 @@ ssd_status run_forward_states(const Plan &pl, const ssd_fwd_args *a, void *ws, f
     SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
     ChunkInfo *chunks = at<ChunkInfo>(ws, pl.off_chunks);
     float *dtw = at<float>(ws, pl.off_dt), *csw = at<float>(ws, pl.off_cs), *states = at<float>(ws, pl.off_states);
-    SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, 1, sh.kmax, 0, hdr, seqs, chunks, nullptr,
+    SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, 1, 1, sh.kmax, 0, hdr, seqs, chunks, nullptr,
                                at<int32_t>(ws, pl.off_lastunit), nullptr, 0, st));
     if (sh.kmax > 0) {
         SSD_CUDA(launch_chunk_cumsum(sh, hdr, chunks, (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1],
@@ -274,6 +332,7 @@ ssd_status ssd_fwd_debug_layout(const ssd_problem *prob, const ssd_fwd_args *arg
     out->dt = staged ? (int64_t)pl.off_dt : -1;
     out->cs = staged ? (int64_t)pl.off_cs : -1;
     out->states = staged ? (int64_t)pl.off_states : -1;
+    out->units = staged ? -1 : (int64_t)pl.off_units;
     out->qi = pl.sh.Q;
     return SSD_OK;
 }
@@ -286,6 +345,30 @@ ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, siz
     cudaStream_t st = (cudaStream_t)stream;
     const Shape &sh = pl.sh;
     float *final_ = (float *)a->final_states.ptr;
+    if (pl.algo == SSD_ALGO_FUSED) {
+        int32_t *hdr = at<int32_t>(ws, pl.off_hdr);
+        SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
+        UnitInfo *units = at<UnitInfo>(ws, pl.off_units);
+        uint32_t *flags = at<uint32_t>(ws, pl.off_flags);
+        SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, sh.R, fused_block_units(), sh.kmax,
+                                   sh.umax, hdr, seqs,
+                                   at<ChunkInfo>(ws, pl.off_chunks), units, at<int32_t>(ws, pl.off_lastunit), flags,
+                                   (int64_t)sh.umax * sh.H, st));
+        const int64_t tickets = (int64_t)sh.umax * sh.H;
+        if (tickets > 0) {
+            const int grid = (int)(tickets < num_sms() ? tickets : num_sms());
+            SSD_CUDA(launch_fused_fwd(sh, hdr, units, a->x.ptr, a->x.stride, a->B.ptr, a->B.stride, a->C.ptr,
+                                      a->C.stride, (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1],
+                                      (const float *)a->A.ptr, (const float *)a->D.ptr, (const float *)a->dt_bias.ptr,
+                                      a->z.ptr, a->z.ptr ? a->z.stride : nullptr, a->y.ptr, a->y.stride,
+                                      (const float *)a->initial_states.ptr, final_, at<float>(ws, pl.off_agg),
+                                      at<float>(ws, pl.off_incl), at<float>(ws, pl.off_lam), flags, grid, st));
+        }
+        if (final_ != nullptr && (pl.varlen || sh.L == 0))
+            SSD_CUDA(launch_empty_seq_final(sh.S, sh.H, sh.P * sh.N, seqs, hdr,
+                                            (const float *)a->initial_states.ptr, final_, st));
+        return SSD_OK;
+    }
     SSD_TRY(run_forward_states(pl, a, ws, final_, st));
     if (sh.kmax > 0) {
         int32_t *hdr = at<int32_t>(ws, pl.off_hdr);

@@ -29,10 +29,10 @@ struct SeqInfo {
 struct ChunkInfo {
     int32_t seq, b, t0, len;
 };
-// One work unit of the fused forward: `nchunk` consecutive chunks of one sequence.
+// One work unit of the fused forward: segment j (`nchunk` consecutive chunks) of one sequence.
 struct UnitInfo {
-    int32_t seq, b, t0, len;         // token range [t0, t0+len) of row b
-    int32_t nchunk, prev, last, first_chunk;  // prev: unit index of the same sequence's previous unit (-1 if none)
+    int32_t seq, b, t0, len;          // token range [t0, t0+len) of row b
+    int32_t nchunk, prev, last, j;    // prev: index of unit (seq, j-1) or -1; last: j is the final segment
 };
 
 // Shape of one call, as the kernels see it.
@@ -54,6 +54,20 @@ struct MView3 {
     void *p;
     int64_t s0, s1, s2;
 };
+
+// Raises a kernel's dynamic shared memory limit once per device (the flag word
+// holds one bit per device ordinal < 64).
+template <typename K>
+inline cudaError_t ensure_smem_attr(K kernel, int bytes, unsigned long long *done_mask) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (*done_mask & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) *done_mask |= bit;
+    return e;
+}
 
 __device__ __forceinline__ void set_status(int32_t *hdr, int32_t code) {
     atomicCAS(&hdr[HDR_STATUS], 0, code);

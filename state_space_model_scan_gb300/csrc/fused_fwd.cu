@@ -1,0 +1,627 @@
+// fused_fwd.cu -- single-pass tensor-core forward of the SSD chunked scan (bf16
+// inputs, fp32 state and accumulation), headdim 64, dstate 128, chunk 128.
+//
+// Work decomposition.  A work unit is (sequence, head, R consecutive 128-token
+// chunks).  Units are handed out in list order through an atomic ticket (the
+// metadata kernel lists them by segment index, then sequence; tickets put the
+// heads of one unit next to each other so the heads of a group share B/C tiles
+// in L2).  For one unit a CTA:
+//   phase 1  loads x, B per chunk (TMA) and accumulates, on the tensor cores, the
+//            unit's end-state contribution from a zero start,
+//              agg[n][p] = sum_l B[l][n] * dt[l] exp(cs_u[end] - cs_u[l]) * x[l][p],
+//            then publishes agg and the unit's total log-decay;
+//   carry-in folds, in a fixed order, the aggregates of the unit's predecessors
+//            inside its block of KB segments and the end state published by the
+//            previous block's last unit (or the initial state) -- the inter-chunk
+//            propagation of the Mamba-3-Lite "SSD Reference" page ("Inter-chunk
+//            propagation -- the fixed contract"), telescoped per unit, plus the
+//            initial-state term.  The last unit of a block publishes its end state.
+//            The association never depends on timing, so results are bitwise
+//            reproducible;
+//   phase 2  walks its chunks again (x, B now L2-resident) with the state in
+//            registers and, per chunk on the tensor cores,
+//              CB   = C B^T                           (segment-sum mask applied on chip)
+//              S_c^T = B^T (w o x)                     (chunk state, w = dt exp(cs[Q-1]-cs))
+//              Y_off = C S_in^T                        (carried state readout)
+//              Y_diag = M x,  M = CB o exp(cs[l]-cs[s]) dt[s] 1[s<=l]
+//            y = (Y_diag + exp(cs) Y_off + D x) silu(z) is written once (bf16).
+// dt, cs, CB, M, chunk states and carried states never reach global memory;
+// only the per-unit aggregates / end states (fp32, small) are exchanged.
+//
+// Every wait (TMA, MMA completion, predecessor flags) is bounded; on expiry the
+// kernel records SSD_ERR_DEVICE_TIMEOUT, stops taking work, frees its TMEM and
+// exits.
+#include <cudaTypedefs.h>
+
+#include "tc_common.cuh"
+
+namespace ssd {
+
+namespace {
+
+using namespace tc;
+
+constexpr int QT = 128;   // chunk length
+constexpr int PT = 64;    // head dim
+constexpr int NT = 128;   // state dim
+constexpr int RMAX = 8;   // max chunks per unit
+constexpr int KB = 8;     // segments per block of the carry-in fold
+constexpr int NTHR = 128;
+
+constexpr uint32_t X_BYTES = QT * PT * 2;    // 16 KB
+constexpr uint32_t BC_BYTES = QT * NT * 2;   // 32 KB
+constexpr uint32_t S_BYTES = PT * NT * 2;    // 16 KB
+constexpr uint32_t STAGE_BYTES = X_BYTES + 2 * BC_BYTES;
+
+// shared memory map (offsets from a 1024-aligned base)
+constexpr uint32_t OFF_STAGE0 = 0;
+constexpr uint32_t OFF_STAGE1 = STAGE_BYTES;            // 81920
+constexpr uint32_t OFF_WX = 2 * STAGE_BYTES;            // 163840
+constexpr uint32_t OFF_SS = OFF_WX + X_BYTES;           // 180224
+constexpr uint32_t OFF_DTU = OFF_SS + S_BYTES;          // 196608
+constexpr uint32_t OFF_WU = OFF_DTU + RMAX * QT * 4;    // 200704
+constexpr uint32_t OFF_CS2 = OFF_WU + RMAX * QT * 4;    // 204800
+constexpr uint32_t OFF_DTC = OFF_CS2 + QT * 4;          // 205312
+constexpr uint32_t OFF_MISC = OFF_DTC + QT * 4;         // 205824
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 256 + 1024;  // + alignment slack
+
+// TMEM columns
+constexpr uint32_t TM_CB = 0;     // [0,128) CB, then [0,64) Y_diag
+constexpr uint32_t TM_SC = 128;   // [128,192) chunk state^T
+constexpr uint32_t TM_YO = 192;   // [192,256) Y_off
+constexpr uint32_t TM_AGG = 256;  // [256,320) unit aggregate^T
+constexpr uint32_t TM_COLS = 512;
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct FusedParams {
+    Shape sh;
+    int32_t *hdr;
+    const UnitInfo *units;
+    const float *dt_raw;
+    int64_t sdb, sdl;
+    const float *A, *D, *bias;
+    const __nv_bfloat16 *z;
+    int64_t szb, szl, szh;
+    __nv_bfloat16 *y;
+    int64_t syb, syl, syh;
+    const float *init;
+    float *final_;
+    float *agg, *incl, *lam;
+    uint32_t *flags;
+};
+
+struct Misc {
+    uint64_t bar_tma[2];
+    uint64_t bar_mma;
+    uint32_t tmem_base;
+    int ticket;
+    int abort_;
+    uint32_t flag;
+    float wsum[4];
+};
+
+__device__ __forceinline__ float block_scan128(float v, float *wsum, float *total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    float x = warp_incl_sum(v);
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    float off = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (i < w) off += wsum[i];
+    *total = wsum[0] + wsum[1] + wsum[2] + wsum[3];
+    __syncthreads();
+    return x + off;
+}
+
+// K-major SW128 operand: rows of 64 bf16 (128 B), atom columns of `col_bytes`.
+__device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t col_bytes) {
+    return sdesc(base + (uint32_t)(k >> 2) * col_bytes + (uint32_t)(k & 3) * 32u, 16u, 1024u);
+}
+// MN-major SW128 operand: K rows of 128 B; 16-row K step = 2048 B; MN atoms 16 KB apart.
+__device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k) {
+    return sdesc(base + (uint32_t)k * 2048u, 16384u, 1024u);
+}
+
+__global__ void __launch_bounds__(NTHR, 1)
+k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
+            const __grid_constant__ CUtensorMap tmC, const FusedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    Misc *ms = reinterpret_cast<Misc *>(sm + OFF_MISC);
+    float *dtu = reinterpret_cast<float *>(sm + OFF_DTU);
+    float *wu = reinterpret_cast<float *>(sm + OFF_WU);
+    float *cs2 = reinterpret_cast<float *>(sm + OFF_CS2);
+    float *dtc = reinterpret_cast<float *>(sm + OFF_DTC);
+    uint8_t *Wx = sm + OFF_WX;
+    uint8_t *Ss = sm + OFF_SS;
+    const Shape sh = p.sh;
+
+    if (tid == 0) {
+        mbar_init(&ms->bar_tma[0], 1);
+        mbar_init(&ms->bar_tma[1], 1);
+        mbar_init(&ms->bar_mma, 1);
+        fence_mbar_init();
+        ms->abort_ = 0;
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
+    }
+    if (warp == 0) tmem_alloc(&ms->tmem_base, TM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ms->tmem_base;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+    uint32_t load_seq = 0;   // sequence number of the next chunk load (stage = seq & 1)
+    uint32_t mma_seq = 0;    // MMA commits waited for
+    // Issue/wait counters kept identically by every thread (issue decisions are
+    // uniform): what is still in flight when the kernel stops early gets drained.
+    uint32_t ld_issued = 0, ld_waited = 0, mma_issued = 0;
+    const int total = (p.hdr[HDR_STATUS] != 0) ? 0 : p.hdr[HDR_NUNITS] * sh.H;
+
+    auto stage_ptr = [&](uint32_t seq) { return sm + ((seq & 1) ? OFF_STAGE1 : OFF_STAGE0); };
+    // one thread: issue the loads of chunk (row b, first token t) into stage seq&1
+    auto issue_load = [&](uint32_t seq, int h, int g, int t, int b, bool withC) {
+        uint8_t *st = stage_ptr(seq);
+        uint64_t *bar = &ms->bar_tma[seq & 1];
+        mbar_expect_tx(bar, X_BYTES + BC_BYTES + (withC ? BC_BYTES : 0));
+        tma_load_4d(st, &tmX, bar, 0, h, t, b);
+        tma_load_4d(st + X_BYTES, &tmB, bar, 0, g, t, b);
+        tma_load_4d(st + X_BYTES + BC_BYTES / 2, &tmB, bar, 64, g, t, b);
+        if (withC) {
+            tma_load_4d(st + X_BYTES + BC_BYTES, &tmC, bar, 0, g, t, b);
+            tma_load_4d(st + X_BYTES + BC_BYTES + BC_BYTES / 2, &tmC, bar, 64, g, t, b);
+        }
+    };
+    // all threads: wait for load `seq`
+    auto wait_load = [&](uint32_t seq) {
+        if (!mbar_wait(&ms->bar_tma[seq & 1], (seq >> 1) & 1)) {
+            ms->abort_ = 1;
+            set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+        }
+        ++ld_waited;
+    };
+    auto wait_mma = [&]() {
+        if (!mbar_wait(&ms->bar_mma, mma_seq & 1)) {
+            ms->abort_ = 1;
+            set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+        }
+        ++mma_seq;
+        tc_fence_after();
+    };
+
+    const uint32_t idesc_cb = idesc_bf16(128, 128, 0, 0);
+    const uint32_t idesc_sc = idesc_bf16(128, 64, 1, 1);
+    const uint32_t idesc_yo = idesc_bf16(128, 64, 0, 0);
+    const uint32_t idesc_yd = idesc_bf16(128, 64, 0, 1);
+    const uint32_t sWx = smem_u32(Wx), sSs = smem_u32(Ss);
+    const int64_t unit_stride = (int64_t)NT * PT;   // floats per (unit, head) aggregate
+
+    for (;;) {
+        if (tid == 0) ms->ticket = atomicAdd(&p.hdr[HDR_TICKET], 1);
+        __syncthreads();
+        const int ticket = ms->ticket;
+        if (ticket >= total || ms->abort_) break;
+        const int u = ticket / sh.H, h = ticket % sh.H, g = h / sh.hpg;
+        const UnitInfo ui = p.units[u];
+        const float Ah = p.A[h];
+        const int ntok = ui.nchunk * QT;
+
+        // ---- dt over the unit, unit-level cumulative log-decay, phase-1 weights
+        for (int i = tid; i < ntok; i += NTHR) {
+            float dt = 0.f;
+            if (i < ui.len) {
+                float v = p.dt_raw[(int64_t)ui.b * p.sdb + (int64_t)(ui.t0 + i) * p.sdl + h] + (p.bias ? p.bias[h] : 0.f);
+                dt = softplus_f(v);
+            }
+            dtu[i] = dt;
+        }
+        __syncthreads();
+        float carry = 0.f;
+        for (int c = 0; c < ui.nchunk; ++c) {
+            float tot;
+            float v = block_scan128(dtu[c * QT + tid] * Ah, ms->wsum, &tot);
+            wu[c * QT + tid] = carry + v;
+            carry += tot;
+        }
+        const float lam_u = carry;
+        for (int i = tid; i < ntok; i += NTHR) wu[i] = dtu[i] * ex2((lam_u - wu[i]) * LOG2E);
+        __syncthreads();
+
+        // ---- phase 1: unit aggregate on the tensor cores
+        const uint32_t seq0 = load_seq;
+        if (tid == 0) issue_load(seq0, h, g, ui.t0, ui.b, false);
+        ++ld_issued;
+        for (int c = 0; c < ui.nchunk; ++c) {
+            const uint32_t seq = seq0 + c;
+            if (c > 0) wait_mma();   // MMA(c-1) done: Wx and stage (c+1)&1 free
+            if (c + 1 < ui.nchunk) {
+                if (tid == 0) issue_load(seq + 1, h, g, ui.t0 + (c + 1) * QT, ui.b, false);
+                ++ld_issued;
+            }
+            wait_load(seq);
+            {   // Wx row tid = w[tid] * x row tid (same swizzled positions)
+                const uint8_t *xs = stage_ptr(seq);
+                const float wl = wu[c * QT + tid];
+                const uint4 *src = reinterpret_cast<const uint4 *>(xs + tid * 128);
+                uint4 *dst = reinterpret_cast<uint4 *>(Wx + tid * 128);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint4 v = src[q];
+                    __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float2 f = __bfloat1622float2(e[i]);
+                        e[i] = __floats2bfloat162_rn(f.x * wl, f.y * wl);
+                    }
+                    dst[q] = v;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (ms->abort_) break;
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t sB = smem_u32(stage_ptr(seq) + X_BYTES);
+#pragma unroll
+                for (int k = 0; k < QT / 16; ++k)
+                    umma_bf16(tmem + TM_AGG, mnmaj(sB, k), mnmaj(sWx, k), idesc_sc, (c > 0 || k > 0) ? 1u : 0u);
+                umma_commit(&ms->bar_mma);
+            }
+            ++mma_issued;
+        }
+        load_seq = seq0 + ui.nchunk;
+        if (ms->abort_) break;
+        wait_mma();
+        float a_reg[64];
+        {
+            float t32[32];
+            tmem_ld32(tmem + lane_base + TM_AGG, t32);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a_reg[i] = t32[i];
+            tmem_ld32(tmem + lane_base + TM_AGG + 32, t32);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a_reg[32 + i] = t32[i];
+            tmem_wait_ld();
+        }
+        const int64_t my = (int64_t)u * sh.H + h;
+        {
+            float4 *dst = reinterpret_cast<float4 *>(p.agg + my * unit_stride + (int64_t)tid * PT);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                __stcg(dst + i, make_float4(a_reg[4 * i], a_reg[4 * i + 1], a_reg[4 * i + 2], a_reg[4 * i + 3]));
+            if (tid == 0) __stcg(p.lam + my, lam_u);
+        }
+        __threadfence();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) st_release_u32(p.flags + my, 1u);
+
+        // prefetch phase-2 chunk 0 while looking back
+        if (tid == 0) issue_load(load_seq, h, g, ui.t0, ui.b, true);
+        ++ld_issued;
+
+        // ---- carry-in state of the unit (row n = tid, 64 columns p)
+        // P_j = sum_{i=b0}^{j-1} exp(lam_{i+1} + .. + lam_{j-1}) agg_i + exp(lam_{b0} + .. + lam_{j-1}) E,
+        // E = end state of unit b0-1 (published by it) or the initial state when b0 = 0.
+        float s_run[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s_run[i] = 0.f;
+        const int b0 = ui.j - (ui.j % KB);
+        const int nfold = ui.j - b0;     // in-block predecessors: units u-1 .. u-nfold
+        const int uprev_blk = (b0 > 0) ? (nfold > 0 ? p.units[u - nfold].prev : ui.prev) : -1;
+        {   // wait for the flags: thread i < nfold polls unit u-1-i (aggregate), thread nfold the block end
+            int need = 0;
+            int64_t fi = 0;
+            if (tid < nfold) { need = 1; fi = (int64_t)(u - 1 - tid) * sh.H + h; }
+            else if (tid == nfold && uprev_blk >= 0) { need = 2; fi = (int64_t)uprev_blk * sh.H + h; }
+            if (need) {
+                uint32_t fl = ld_acquire_u32(p.flags + fi);
+                if (fl < (uint32_t)need) {
+                    const uint64_t t0 = globaltimer();
+                    while ((fl = ld_acquire_u32(p.flags + fi)) < (uint32_t)need) {
+                        if (globaltimer() - t0 > kWaitLimitNs) break;
+                        __nanosleep(64);
+                    }
+                }
+                if (fl < (uint32_t)need) {
+                    ms->abort_ = 1;
+                    set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+                }
+            }
+            __threadfence();
+            __syncthreads();
+            if (ms->abort_) break;
+        }
+        float logm = 0.f;
+        for (int i = 1; i <= nfold; ++i) {   // units u-1, u-2, .. in that order
+            const int64_t pi = (int64_t)(u - i) * sh.H + h;
+            const float sc = ex2(logm * LOG2E);
+            const float4 *src = reinterpret_cast<const float4 *>(p.agg + pi * unit_stride + (int64_t)tid * PT);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                float4 v = __ldcg(src + q);
+                s_run[4 * q] += sc * v.x;
+                s_run[4 * q + 1] += sc * v.y;
+                s_run[4 * q + 2] += sc * v.z;
+                s_run[4 * q + 3] += sc * v.w;
+            }
+            logm += __ldcg(p.lam + pi);
+        }
+        if (uprev_blk >= 0) {
+            const float sc = ex2(logm * LOG2E);
+            const int64_t pi = (int64_t)uprev_blk * sh.H + h;
+            const float4 *src = reinterpret_cast<const float4 *>(p.incl + pi * unit_stride + (int64_t)tid * PT);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                float4 v = __ldcg(src + q);
+                s_run[4 * q] += sc * v.x;
+                s_run[4 * q + 1] += sc * v.y;
+                s_run[4 * q + 2] += sc * v.z;
+                s_run[4 * q + 3] += sc * v.w;
+            }
+        } else if (p.init) {
+            const float sc = ex2(logm * LOG2E);
+            const float *src = p.init + ((int64_t)ui.seq * sh.H + h) * PT * NT + tid;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) s_run[i] += sc * src[(int64_t)i * NT];
+        }
+        if ((ui.j % KB) == KB - 1 && !ui.last) {   // block end: publish the unit's end state
+            const float dec = ex2(lam_u * LOG2E);
+            float4 *dst = reinterpret_cast<float4 *>(p.incl + my * unit_stride + (int64_t)tid * PT);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                __stcg(dst + i, make_float4(a_reg[4 * i] + dec * s_run[4 * i], a_reg[4 * i + 1] + dec * s_run[4 * i + 1],
+                                            a_reg[4 * i + 2] + dec * s_run[4 * i + 2],
+                                            a_reg[4 * i + 3] + dec * s_run[4 * i + 3]));
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) st_release_u32(p.flags + my, 2u);
+        }
+
+        // ---- phase 2: outputs
+        for (int c = 0; c < ui.nchunk; ++c) {
+            const uint32_t seq = load_seq + c;
+            const int tc0 = ui.t0 + c * QT;
+            const int clen = min(QT, ui.len - c * QT);
+            if (c + 1 < ui.nchunk) {
+                if (tid == 0) issue_load(seq + 1, h, g, tc0 + QT, ui.b, true);
+                ++ld_issued;
+            }
+            // chunk-local cumulative log-decay
+            const float dtl = dtu[c * QT + tid];
+            float ctot;
+            const float csl = block_scan128(dtl * Ah, ms->wsum, &ctot);
+            cs2[tid] = csl * LOG2E;
+            dtc[tid] = dtl;
+            const float a_c = ex2(ctot * LOG2E);
+            // carried state S_in (bf16, K-major [p][n]) for Y_off
+            {
+                const int n = tid, ac = n >> 6, cn = (n & 63) >> 3;
+                uint8_t *base = Ss + ac * (S_BYTES / 2) + (n & 7) * 2;
+#pragma unroll
+                for (int pp = 0; pp < 64; ++pp) {
+                    *reinterpret_cast<__nv_bfloat16 *>(base + pp * 128 + ((cn ^ (pp & 7)) << 4)) =
+                        __float2bfloat16_rn(s_run[pp]);
+                }
+            }
+            wait_load(seq);
+            __syncthreads();   // cs2/dtc visible
+            const uint8_t *st = stage_ptr(seq);
+            {   // Wx = w o x, w[l] = dt[l] exp(cs[Q-1] - cs[l])
+                const float wl = dtc[tid] * ex2(cs2[QT - 1] - cs2[tid]);
+                const uint4 *src = reinterpret_cast<const uint4 *>(st + tid * 128);
+                uint4 *dst = reinterpret_cast<uint4 *>(Wx + tid * 128);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint4 v = src[q];
+                    __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float2 f = __bfloat1622float2(e[i]);
+                        e[i] = __floats2bfloat162_rn(f.x * wl, f.y * wl);
+                    }
+                    dst[q] = v;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (ms->abort_) break;
+            const uint32_t sX = smem_u32(st), sB = sX + X_BYTES, sC = sB + BC_BYTES;
+            if (tid == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < NT / 16; ++k)   // CB = C B^T (K = state dim)
+                    umma_bf16(tmem + TM_CB, kmaj(sC, k, BC_BYTES / 2), kmaj(sB, k, BC_BYTES / 2), idesc_cb, k > 0);
+#pragma unroll
+                for (int k = 0; k < QT / 16; ++k)   // S_c^T = B^T (w o x) (K = tokens)
+                    umma_bf16(tmem + TM_SC, mnmaj(sB, k), mnmaj(sWx, k), idesc_sc, k > 0);
+#pragma unroll
+                for (int k = 0; k < NT / 16; ++k)   // Y_off = C S_in^T (K = state dim)
+                    umma_bf16(tmem + TM_YO, kmaj(sC, k, BC_BYTES / 2), kmaj(sSs, k, S_BYTES / 2), idesc_yo, k > 0);
+                umma_commit(&ms->bar_mma);
+            }
+            ++mma_issued;
+            wait_mma();
+            // M (bf16, K-major [l][s]) into the B buffer, which the MMAs above are done with
+            {
+                uint8_t *Ms = const_cast<uint8_t *>(st) + X_BYTES;
+                const int l = tid;
+                const float cl = cs2[l];
+#pragma unroll
+                for (int sb = 0; sb < 4; ++sb) {
+                    uint32_t pk[16];
+                    if (sb <= warp) {
+                        float cb[32];
+                        tmem_ld32(tmem + lane_base + TM_CB + sb * 32, cb);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const int s0 = sb * 32 + i;
+                            float m0 = (s0 <= l) ? cb[i] * ex2(cl - cs2[s0]) * dtc[s0] : 0.f;
+                            float m1 = (s0 + 1 <= l) ? cb[i + 1] * ex2(cl - cs2[s0 + 1]) * dtc[s0 + 1] : 0.f;
+                            pk[i >> 1] = pack_bf16(m0, m1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                    }
+                    uint8_t *rowp = Ms + (sb >> 1) * (BC_BYTES / 2) + l * 128;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int cidx = ((sb & 1) << 2) + q;
+                        *reinterpret_cast<uint4 *>(rowp + ((cidx ^ (l & 7)) << 4)) =
+                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    }
+                }
+                // carried state update: S_in[c+1] = a_c S_in[c] + S_c (row n = tid)
+                float sc[32];
+                tmem_ld32(tmem + lane_base + TM_SC, sc);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s_run[i] = a_c * s_run[i] + sc[i];
+                tmem_ld32(tmem + lane_base + TM_SC + 32, sc);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s_run[32 + i] = a_c * s_run[32 + i] + sc[i];
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t sM = sB;
+#pragma unroll
+                for (int k = 0; k < QT / 16; ++k)   // Y_diag = M x (K = source tokens)
+                    umma_bf16(tmem + TM_CB, kmaj(sM, k, BC_BYTES / 2), mnmaj(sX, k), idesc_yd, k > 0);
+                umma_commit(&ms->bar_mma);
+            }
+            ++mma_issued;
+            wait_mma();
+            {   // epilogue: row l = tid
+                const int l = tid;
+                float yd[32], yo[32];
+                const float el = ex2(cs2[l]);
+                const float Dh = p.D ? p.D[h] : 0.f;
+                const int64_t tok = (int64_t)tc0 + l;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    tmem_ld32(tmem + lane_base + TM_CB + half * 32, yd);
+                    tmem_ld32(tmem + lane_base + TM_YO + half * 32, yo);
+                    tmem_wait_ld();
+                    if (l < clen) {
+                        const uint8_t *xrow = st + l * 128;
+                        __nv_bfloat16 *yrow = p.y + (int64_t)ui.b * p.syb + tok * p.syl + (int64_t)h * p.syh + half * 32;
+                        const __nv_bfloat16 *zrow =
+                            p.z ? p.z + (int64_t)ui.b * p.szb + tok * p.szl + (int64_t)h * p.szh + half * 32 : nullptr;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int cidx = half * 4 + q;
+                            uint4 xv = *reinterpret_cast<const uint4 *>(xrow + ((cidx ^ (l & 7)) << 4));
+                            const __nv_bfloat162 *xe = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                            uint4 zv;
+                            if (zrow) zv = *reinterpret_cast<const uint4 *>(zrow + q * 8);
+                            const __nv_bfloat162 *ze = reinterpret_cast<const __nv_bfloat162 *>(&zv);
+                            uint32_t o[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 xf = __bfloat1622float2(xe[i]);
+                                const int j = q * 8 + 2 * i;
+                                float v0 = yd[j] + el * yo[j] + Dh * xf.x;
+                                float v1 = yd[j + 1] + el * yo[j + 1] + Dh * xf.y;
+                                if (zrow) {
+                                    const float2 zf = __bfloat1622float2(ze[i]);
+                                    v0 *= zf.x * rcp(1.f + ex2(-zf.x * LOG2E));
+                                    v1 *= zf.y * rcp(1.f + ex2(-zf.y * LOG2E));
+                                }
+                                o[i] = pack_bf16(v0, v1);
+                            }
+                            *reinterpret_cast<uint4 *>(yrow + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncthreads();
+        }
+        load_seq += ui.nchunk;
+        if (ms->abort_) break;
+        if (ui.last && p.final_) {
+            float *dst = p.final_ + ((int64_t)ui.seq * sh.H + h) * PT * NT + tid;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = s_run[i];
+        }
+    }
+    // Drain (only non-empty after an early stop): bounded waits for loads and
+    // MMAs still in flight, so nothing lands in shared memory or TMEM after exit.
+    for (uint32_t q = ld_waited; q < ld_issued; ++q) mbar_wait(&ms->bar_tma[q & 1], (q >> 1) & 1);
+    if (mma_issued > mma_seq) mbar_wait(&ms->bar_mma, (mma_issued - 1) & 1);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 4-D bf16 map over [B][L][H or G][64*k] with box {64, 1, 128, 1}, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t inner, int64_t d1, int64_t L, int64_t B, int64_t s1,
+              int64_t sL, int64_t sB) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)d1, (cuuint64_t)L, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)(s1 * 2), (cuuint64_t)(sL * 2), (cuuint64_t)(sB * 2)};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)QT, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int fused_rmax() { return RMAX; }
+int fused_block_units() { return KB; }
+
+cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *units, const void *x, const int64_t *sx,
+                             const void *Bp, const int64_t *sb, const void *Cp, const int64_t *sc, const float *dt_raw,
+                             int64_t sdb, int64_t sdl, const float *A, const float *D, const float *bias,
+                             const void *z, const int64_t *sz, void *y, const int64_t *sy, const float *init,
+                             float *final_, float *agg, float *incl, float *lam, uint32_t *flags, int grid,
+                             cudaStream_t st) {
+    CUtensorMap mx, mb, mc;
+    if (!make_map(&mx, x, PT, sh.H, sh.L, sh.B, sx[2], sx[1], sx[0])) return cudaErrorInvalidValue;
+    if (!make_map(&mb, Bp, NT, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
+    if (!make_map(&mc, Cp, NT, sh.G, sh.L, sh.B, sc[2], sc[1], sc[0])) return cudaErrorInvalidValue;
+    FusedParams fp;
+    fp.sh = sh; fp.hdr = hdr; fp.units = units; fp.dt_raw = dt_raw; fp.sdb = sdb; fp.sdl = sdl;
+    fp.A = A; fp.D = D; fp.bias = bias;
+    fp.z = (const __nv_bfloat16 *)z;
+    fp.szb = sz ? sz[0] : 0; fp.szl = sz ? sz[1] : 0; fp.szh = sz ? sz[2] : 0;
+    fp.y = (__nv_bfloat16 *)y; fp.syb = sy[0]; fp.syl = sy[1]; fp.syh = sy[2];
+    fp.init = init; fp.final_ = final_; fp.agg = agg; fp.incl = incl; fp.lam = lam; fp.flags = flags;
+    static unsigned long long attr_done = 0;
+    cudaError_t e = ensure_smem_attr(k_fused_fwd, (int)SMEM_BYTES, &attr_done);
+    if (e != cudaSuccess) return e;
+    k_fused_fwd<<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, fp);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -5,8 +5,10 @@
 // chunk ragged), so no chunk ever holds two sequences; the carried state is
 // reset to the sequence's initial state at its first chunk.  Chunks are listed
 // sequence by sequence.  Work units of the fused forward group R consecutive
-// chunks of one sequence and are listed by (segment index j, sequence s), so a
-// unit only ever depends on units listed before it.
+// chunks of one sequence (segment j of the sequence); segments are grouped in
+// blocks of KB.  Units are listed by (block, sequence, segment), so a unit only
+// ever depends on units listed before it and the units of one sequence inside
+// one block are consecutive in the list.
 #include "common.cuh"
 
 namespace ssd {
@@ -54,7 +56,7 @@ __device__ int block_max(int v, int *sm) {
 }
 
 __global__ void __launch_bounds__(kMetaThreads)
-k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, int kmax, int umax,
+k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, int KB, int kmax, int umax,
              int32_t *hdr, SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units, int32_t *last_unit,
              uint32_t *zero_words, int64_t n_zero) {
     __shared__ int sm[32];
@@ -114,34 +116,37 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
             chunks[si.chunk0 + c] = ci;
         }
     }
-    // pass 3: work units ordered by (segment j, sequence s)
+    // pass 3: work units ordered by (block of KB segments, sequence, segment)
     int nunits = 0;
     if (units != nullptr) {
-        for (int j = 0; j < maxseg; ++j) {
+        const int maxblk = (maxseg + KB - 1) / KB;
+        for (int blk = 0; blk < maxblk; ++blk) {
             for (int base = 0; base < S; base += blockDim.x) {
                 int s = base + tid;
-                int on = 0, nch = 0;
+                int cnt = 0, nch = 0, nseg = 0;
                 SeqInfo si;
                 if (s < S) {
                     si = seqs[s];
                     nch = (si.len + Q - 1) / Q;
-                    on = ((nch + R - 1) / R) > j;
+                    nseg = (nch + R - 1) / R;
+                    cnt = max(0, min(KB, nseg - blk * KB));
                 }
                 int tot;
-                int off = block_excl_scan(on, &tot, sm);
-                if (on) {
-                    int u = nunits + off;
+                int off = block_excl_scan(cnt, &tot, sm);
+                for (int i = 0; i < cnt; ++i) {
+                    const int j = blk * KB + i;
+                    const int u = nunits + off + i;
                     if (u < umax) {
                         UnitInfo ui;
                         ui.seq = s; ui.b = si.b;
                         ui.t0 = si.t0 + j * R * Q;
                         ui.len = min(R * Q, si.len - j * R * Q);
                         ui.nchunk = min(R, nch - j * R);
-                        ui.prev = (j == 0) ? -1 : last_unit[s];
-                        ui.last = (j == (nch + R - 1) / R - 1) ? 1 : 0;
-                        ui.first_chunk = si.chunk0 + j * R;
+                        ui.prev = (j == 0) ? -1 : (i > 0 ? u - 1 : last_unit[s]);
+                        ui.last = (j == nseg - 1) ? 1 : 0;
+                        ui.j = j;
                         units[u] = ui;
-                        last_unit[s] = u;
+                        if (i == cnt - 1) last_unit[s] = u;
                     }
                 }
                 nunits += tot;
@@ -170,10 +175,10 @@ __global__ void k_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, con
 
 }  // namespace
 
-cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int kmax, int umax,
+cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int KB, int kmax, int umax,
                               int32_t *hdr, SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units,
                               int32_t *last_unit, uint32_t *zero_words, int64_t n_zero, cudaStream_t st) {
-    k_build_meta<<<1, kMetaThreads, 0, st>>>(cu, B, L, S, Q, R, kmax, umax, hdr, seqs, chunks, units,
+    k_build_meta<<<1, kMetaThreads, 0, st>>>(cu, B, L, S, Q, R, KB, kmax, umax, hdr, seqs, chunks, units,
                                              last_unit, zero_words, n_zero);
     return cudaGetLastError();
 }

@@ -147,9 +147,15 @@ def test_bwd_requires_matching_gradients(lib):
 
 def test_metadata_reference_builder():
     from oracle import meta
-    m = meta.build(cu=[0, 5, 5, 300], Q=64, R=2)
+    m = meta.build(cu=[0, 5, 5, 300], Q=64, R=2, KB=8)
     assert m["chunks"] == [(0, 0, 0, 5), (2, 0, 5, 64), (2, 0, 69, 64), (2, 0, 133, 64), (2, 0, 197, 64),
                            (2, 0, 261, 39)]
     assert [u[:5] for u in m["units"]] == [(0, 0, 0, 5, 1), (2, 0, 5, 128, 2), (2, 0, 133, 128, 2), (2, 0, 261, 39, 1)]
     assert [u[5] for u in m["units"]] == [-1, -1, 1, 2]
     assert [u[6] for u in m["units"]] == [1, 0, 0, 1]
+    assert [u[7] for u in m["units"]] == [0, 0, 1, 2]
+    # blocks of two segments: sequence 1's first block (j=0,1) is contiguous, then block 2
+    m = meta.build(cu=[0, 300, 600], Q=64, R=1, KB=2)
+    assert [(u[0], u[7]) for u in m["units"]] == [(0, 0), (0, 1), (1, 0), (1, 1), (0, 2), (0, 3), (1, 2), (1, 3),
+                                                  (0, 4), (1, 4)]
+    assert [u[5] for u in m["units"]] == [-1, 0, -1, 2, 1, 4, 3, 6, 5, 7]

@@ -1,0 +1,63 @@
+"""Parity at the full sizes of the benchmarked workloads, in the launch
+configuration bench.py times (AUTO path, default work units).  The float64
+oracle computes a sample of heads (heads are independent, so each sampled head
+is an exact reference for that head's outputs and final state)."""
+import numpy as np
+import pytest
+import torch
+
+from state_space_model_scan_gb300 import inputs as I
+from helpers import TOL, rel_l2, gpu_forward, gpu_backward, oracle_forward, oracle_backward, flat
+
+pytestmark = pytest.mark.gpu
+
+
+def check_sampled(w, heads):
+    inp = I.make_inputs(w)
+    y, fin = gpu_forward(w, inp)
+    yo, fo = oracle_forward(w, inp, heads=heads)
+    T = w.batch * w.seqlen
+    yg = flat(y, T)[:, heads]
+    fg = fin.double().cpu().numpy()[:, heads]
+    assert np.isfinite(yg).all() and np.isfinite(fg).all()
+    ey, ef = rel_l2(yg, yo[:, heads]), rel_l2(fg, fo[:, heads])
+    assert ey <= TOL[w.dtype] and ef <= TOL[w.dtype], (w.name, ey, ef)
+    return ey, ef
+
+
+def test_nemotron_nano_fwd_full_size():
+    """L=8192, 64 heads x 64, 8 groups, N=128, z + D, bf16."""
+    check_sampled(I.named("nemotron_nano"), [0, 13, 37, 63])
+
+
+@pytest.mark.parametrize("L", [1024, 8192, 32768])
+def test_long_sequence_fwd_full_size(L):
+    """128 heads x 64, 1 group, N=128, random initial states, final states returned."""
+    check_sampled(I.named("long_seq", L), [0, 77, 127])
+
+
+def test_varlen_fwd_full_size():
+    """16 packed sequences, lengths U{512..8192}, 80 heads x 64, 1 group, own initial states."""
+    check_sampled(I.named("varlen"), [0, 41, 79])
+
+
+def test_nemotron_nano_bwd_full_size():
+    """fwd+bwd workload: gradients of one whole group (dB/dC sum over its 8 heads)."""
+    w = I.named("nemotron_nano")
+    inp = I.make_inputs(w, with_grad_inputs=True)
+    g = gpu_backward(w, inp)
+    heads = list(range(8, 16))          # group 1
+    o = oracle_backward(w, inp, heads=heads)
+    T = w.seqlen
+    errs = dict(
+        dx=rel_l2(flat(g["dx"], T)[:, heads], o["dx"][:, heads]),
+        dz=rel_l2(flat(g["dz"], T)[:, heads], o["dz"][:, heads]),
+        ddt=rel_l2(flat(g["ddt"], T)[:, heads], o["ddt_raw"][:, heads]),
+        dB=rel_l2(flat(g["dB"], T)[:, 1], o["dB"][:, 1]),
+        dC=rel_l2(flat(g["dC"], T)[:, 1], o["dC"][:, 1]),
+        dA=rel_l2(g["dA"].double().cpu().numpy()[heads], o["dA"][heads]),
+        dD=rel_l2(g["dD"].double().cpu().numpy()[heads], o["dD"][heads]),
+        ddt_bias=rel_l2(g["ddt_bias"].double().cpu().numpy()[heads], o["ddt_bias"][heads]),
+    )
+    bad = {k: v for k, v in errs.items() if not v <= TOL["bf16"]}
+    assert not bad, errs

@@ -45,27 +45,28 @@ def test_chunk_metadata_bit_exact():
     assert np.array_equal(got, np.array(ref["chunks"], dtype=np.int32))
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_varlen_matches_oracle(dtype):
-    w = VW([40, 0, 130, 1, 70, 64, 129], dtype=dtype, has_z=True)
+@pytest.mark.parametrize("dtype,P,N,algo", [("f32", 16, 16, "staged"), ("bf16", 16, 16, "staged"),
+                                             ("bf16", 64, 128, "fused"), ("bf16", 64, 128, "staged")])
+def test_varlen_matches_oracle(dtype, P, N, algo):
+    w = VW([40, 0, 130, 1, 70, 64, 129, 300], dtype=dtype, P=P, N=N, has_z=True)
     inp = I.make_inputs(w)
-    y, fin = gpu_forward(w, inp)
+    y, fin = gpu_forward(w, inp, algo=algo, seg_chunks=1 if algo == "fused" else 0)
     yo, fo = oracle_forward(w, inp)
     assert rel_l2(flat(y, w.seqlen), yo) <= TOL[dtype]
     assert rel_l2(fin.double().cpu().numpy(), fo) <= TOL[dtype]
 
 
-def test_packed_equals_separate_runs():
-    lens = [50, 130, 7]
-    w = VW(lens, dtype="bf16")
+@pytest.mark.parametrize("P,N", [(16, 16), (64, 128)])
+def test_packed_equals_separate_runs(P, N):
+    lens = [50, 130, 7, 260]
+    w = VW(lens, dtype="bf16", P=P, N=N)
     inp = I.make_inputs(w)
     y, fin = gpu_forward(w, inp)
     cu = inp["cu_seqlens"].tolist()
-    for s in range(3):
+    for s in range(len(lens)):
         a = dict(inp)
-        for k in ("x", "dt_raw", "B", "C"):
+        for k in ("x", "dt_raw", "B", "C", "z"):
             a[k] = inp[k][:, cu[s]:cu[s + 1]].contiguous()
-        a["z"] = None
         a["initial_states"] = inp["initial_states"][s:s + 1]
         a["cu_seqlens"] = None
         ws = I.Workload("s", 1, lens[s], w.nheads, w.headdim, w.ngroups, w.dstate, 64, "bf16", has_init=True)
@@ -74,12 +75,39 @@ def test_packed_equals_separate_runs():
         assert torch.equal(fs[0], fin[s])
 
 
-def test_empty_sequences_return_initial_state():
-    w = VW([0, 10, 0])
+@pytest.mark.parametrize("P,N", [(16, 16), (64, 128)])
+def test_empty_sequences_return_initial_state(P, N):
+    w = VW([0, 10, 0], P=P, N=N, dtype="bf16")
     inp = I.make_inputs(w)
     y, fin = gpu_forward(w, inp)
     assert torch.equal(fin[0].cpu(), inp["initial_states"][0])
     assert torch.equal(fin[2].cpu(), inp["initial_states"][2])
+
+
+def test_fused_unit_metadata_bit_exact():
+    """The work-unit list of the fused path equals the CPU builder's."""
+    from oracle import meta
+    lens = [5, 0, 300, 640, 1, 1280, 0, 77]
+    w = VW(lens, P=64, N=128, dtype="bf16")
+    inp = I.make_inputs(w)
+    d = to_dev(inp)
+    S = len(lens)
+    y = torch.empty_like(d["x"])
+    prob = _lib.problem(1, w.seqlen, w.nheads, 64, w.ngroups, 128, 128, S, "fused", 2)
+    args = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], dt_bias=d["dt_bias"],
+                         initial_states=d["initial_states"], cu_seqlens=d["cu_seqlens"])
+    ws = torch.empty(_lib.fwd_workspace_size(prob, args), dtype=torch.uint8, device="cuda")
+    _lib.check(_lib.ssd_fwd(prob, args, ws), "ssd_fwd")
+    torch.cuda.synchronize()
+    lay = _lib.debug_layout(prob, args)
+    raw = ws.cpu().numpy()
+    counts = raw[lay.meta_counts:lay.meta_counts + 16].view(np.int32)
+    ref = meta.build(cu=inp["cu_seqlens"].tolist(), Q=128, R=2, KB=8)
+    assert lay.units >= 0 and counts[1] == len(ref["units"]) and counts[3] == 0
+    got = raw[lay.units:lay.units + 32 * counts[1]].view(np.int32).reshape(-1, 8)
+    assert np.array_equal(got, np.array(ref["units"], dtype=np.int32))
+    got_c = raw[lay.chunk_info:lay.chunk_info + 16 * counts[0]].view(np.int32).reshape(-1, 4)
+    assert np.array_equal(got_c, np.array(ref["chunks"], dtype=np.int32))
 
 
 @pytest.mark.parametrize("bad", [[0, 10, 5, 20], [1, 10, 20], [0, 10, 19]])
