@@ -55,17 +55,16 @@ struct MView3 {
     int64_t s0, s1, s2;
 };
 
-// Raises a kernel's dynamic shared memory limit once per device (the flag word
-// holds one bit per device ordinal < 64).
+// Raises a kernel's dynamic shared memory limit when a launch needs more than
+// was set before on this device (state: the largest limit set per device < 64).
 template <typename K>
-inline cudaError_t ensure_smem_attr(K kernel, int bytes, unsigned long long *done_mask) {
+inline cudaError_t ensure_smem_attr(K kernel, int bytes, int *set_bytes /* [64] */) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (*done_mask & bit) return cudaSuccess;
+    if (set_bytes[dev & 63] >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) *done_mask |= bit;
+    if (e == cudaSuccess) set_bytes[dev & 63] = bytes;
     return e;
 }
 

@@ -46,7 +46,7 @@ constexpr int PT = 64;    // head dim
 constexpr int NT = 128;   // state dim
 constexpr int RMAX = 8;   // max chunks per unit
 constexpr int KB = 8;     // segments per block of the carry-in fold
-constexpr int NTHR = 128;
+constexpr int NTHR = 256;
 
 constexpr uint32_t X_BYTES = QT * PT * 2;    // 16 KB
 constexpr uint32_t BC_BYTES = QT * NT * 2;   // 32 KB
@@ -97,20 +97,22 @@ struct Misc {
     uint32_t tmem_base;
     int ticket;
     int abort_;
-    uint32_t flag;
-    float wsum[4];
+    float wsum[8];
 };
 
-__device__ __forceinline__ float block_scan128(float v, float *wsum, float *total) {
+// Inclusive scan of one value per thread over the block (8 warps; threads >= 128 pass 0).
+__device__ __forceinline__ float block_scan(float v, float *wsum, float *total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     float x = warp_incl_sum(v);
     if (lane == 31) wsum[w] = x;
     __syncthreads();
-    float off = 0.f;
+    float off = 0.f, tot = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < NTHR / 32; ++i) {
         if (i < w) off += wsum[i];
-    *total = wsum[0] + wsum[1] + wsum[2] + wsum[3];
+        tot += wsum[i];
+    }
+    *total = tot;
     __syncthreads();
     return x + off;
 }
@@ -124,12 +126,46 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k) {
     return sdesc(base + (uint32_t)k * 2048u, 16384u, 1024u);
 }
 
+// dst row = src row * w, for 4 of the 8 16-byte chunks of one 128-byte row (the
+// scale is uniform along the row).  Chunk slots are visited XOR-ed with row % 8, so
+// eight consecutive rows touch eight different bank groups.
+__device__ __forceinline__ void scale_row_half(const uint8_t *src_row, uint8_t *dst_row, int row, int hf, float wl) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(src_row);
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+        const int q = (4 * hf + qq) ^ (row & 7);
+        uint4 v = src[q];
+        __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(e[i]);
+            e[i] = __floats2bfloat162_rn(f.x * wl, f.y * wl);
+        }
+        dst[q] = v;
+    }
+}
+
+// acc[i] += sc * src[i * NT] for the 32 state columns of this thread's half
+// (a [P][N] state: for each column p the warp reads one contiguous 128-byte line).
+__device__ __forceinline__ void fma_col32(float *acc, const float *src, float sc) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __ldcg(src + (int64_t)i * NT);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] += sc * v[i];
+}
+
+// Thread layout: 8 warps.  row = tid & 127 is the tile row / TMEM lane (warp w
+// reaches lanes 32 (w & 3) .. +31), hf = tid >> 7 picks a half of the 64-wide
+// columns (state columns p, output columns, x chunks).
 __global__ void __launch_bounds__(NTHR, 1)
 k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int row = tid & 127, hf = tid >> 7, quad = warp & 3;
     Misc *ms = reinterpret_cast<Misc *>(sm + OFF_MISC);
     float *dtu = reinterpret_cast<float *>(sm + OFF_DTU);
     float *wu = reinterpret_cast<float *>(sm + OFF_WU);
@@ -154,7 +190,8 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t col_half = (uint32_t)(32 * hf);
 
     uint32_t load_seq = 0;   // sequence number of the next chunk load (stage = seq & 1)
     uint32_t mma_seq = 0;    // MMA commits waited for
@@ -211,6 +248,11 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         const float Ah = p.A[h];
         const int ntok = ui.nchunk * QT;
 
+        // first phase-1 load goes out before anything else
+        const uint32_t seq0 = load_seq;
+        if (tid == 0) issue_load(seq0, h, g, ui.t0, ui.b, false);
+        ++ld_issued;
+
         // ---- dt over the unit, unit-level cumulative log-decay, phase-1 weights
         for (int i = tid; i < ntok; i += NTHR) {
             float dt = 0.f;
@@ -224,18 +266,16 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         float carry = 0.f;
         for (int c = 0; c < ui.nchunk; ++c) {
             float tot;
-            float v = block_scan128(dtu[c * QT + tid] * Ah, ms->wsum, &tot);
-            wu[c * QT + tid] = carry + v;
+            float v = block_scan(tid < QT ? dtu[c * QT + tid] * Ah : 0.f, ms->wsum, &tot);
+            if (tid < QT) wu[c * QT + tid] = carry + v;
             carry += tot;
         }
         const float lam_u = carry;
+        __syncthreads();
         for (int i = tid; i < ntok; i += NTHR) wu[i] = dtu[i] * ex2((lam_u - wu[i]) * LOG2E);
         __syncthreads();
 
         // ---- phase 1: unit aggregate on the tensor cores
-        const uint32_t seq0 = load_seq;
-        if (tid == 0) issue_load(seq0, h, g, ui.t0, ui.b, false);
-        ++ld_issued;
         for (int c = 0; c < ui.nchunk; ++c) {
             const uint32_t seq = seq0 + c;
             if (c > 0) wait_mma();   // MMA(c-1) done: Wx and stage (c+1)&1 free
@@ -244,23 +284,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 ++ld_issued;
             }
             wait_load(seq);
-            {   // Wx row tid = w[tid] * x row tid (same swizzled positions)
-                const uint8_t *xs = stage_ptr(seq);
-                const float wl = wu[c * QT + tid];
-                const uint4 *src = reinterpret_cast<const uint4 *>(xs + tid * 128);
-                uint4 *dst = reinterpret_cast<uint4 *>(Wx + tid * 128);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    uint4 v = src[q];
-                    __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&v);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float2 f = __bfloat1622float2(e[i]);
-                        e[i] = __floats2bfloat162_rn(f.x * wl, f.y * wl);
-                    }
-                    dst[q] = v;
-                }
-            }
+            scale_row_half(stage_ptr(seq) + row * 128, Wx + row * 128, row, hf, wu[c * QT + row]);
             fence_proxy_async_smem();
             __syncthreads();
             if (ms->abort_) break;
@@ -277,23 +301,14 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         load_seq = seq0 + ui.nchunk;
         if (ms->abort_) break;
         wait_mma();
-        float a_reg[64];
-        {
-            float t32[32];
-            tmem_ld32(tmem + lane_base + TM_AGG, t32);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a_reg[i] = t32[i];
-            tmem_ld32(tmem + lane_base + TM_AGG + 32, t32);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a_reg[32 + i] = t32[i];
-            tmem_wait_ld();
-        }
+        float a_reg[32];
+        tmem_ld32(tmem + lane_base + TM_AGG + col_half, a_reg);
+        tmem_wait_ld();
         const int64_t my = (int64_t)u * sh.H + h;
-        {
-            float4 *dst = reinterpret_cast<float4 *>(p.agg + my * unit_stride + (int64_t)tid * PT);
+        {   // aggregate^T row n -> agg[p][n]
+            float *dst = p.agg + my * unit_stride + (int64_t)col_half * NT + row;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                __stcg(dst + i, make_float4(a_reg[4 * i], a_reg[4 * i + 1], a_reg[4 * i + 2], a_reg[4 * i + 3]));
+            for (int i = 0; i < 32; ++i) __stcg(dst + (int64_t)i * NT, a_reg[i]);
             if (tid == 0) __stcg(p.lam + my, lam_u);
         }
         __threadfence();
@@ -301,16 +316,16 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         __syncthreads();
         if (tid == 0) st_release_u32(p.flags + my, 1u);
 
-        // prefetch phase-2 chunk 0 while looking back
+        // prefetch phase-2 chunk 0 while folding the carry-in
         if (tid == 0) issue_load(load_seq, h, g, ui.t0, ui.b, true);
         ++ld_issued;
 
-        // ---- carry-in state of the unit (row n = tid, 64 columns p)
+        // ---- carry-in state of the unit (row n, columns p of this thread's half)
         // P_j = sum_{i=b0}^{j-1} exp(lam_{i+1} + .. + lam_{j-1}) agg_i + exp(lam_{b0} + .. + lam_{j-1}) E,
         // E = end state of unit b0-1 (published by it) or the initial state when b0 = 0.
-        float s_run[64];
+        float s_run[32];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) s_run[i] = 0.f;
+        for (int i = 0; i < 32; ++i) s_run[i] = 0.f;
         const int b0 = ui.j - (ui.j % KB);
         const int nfold = ui.j - b0;     // in-block predecessors: units u-1 .. u-nfold
         const int uprev_blk = (b0 > 0) ? (nfold > 0 ? p.units[u - nfold].prev : ui.prev) : -1;
@@ -340,50 +355,31 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         float logm = 0.f;
         for (int i = 1; i <= nfold; ++i) {   // units u-1, u-2, .. in that order
             const int64_t pi = (int64_t)(u - i) * sh.H + h;
-            const float sc = ex2(logm * LOG2E);
-            const float4 *src = reinterpret_cast<const float4 *>(p.agg + pi * unit_stride + (int64_t)tid * PT);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                float4 v = __ldcg(src + q);
-                s_run[4 * q] += sc * v.x;
-                s_run[4 * q + 1] += sc * v.y;
-                s_run[4 * q + 2] += sc * v.z;
-                s_run[4 * q + 3] += sc * v.w;
-            }
-            logm += __ldcg(p.lam + pi);
+            const float lam_i = __ldcg(p.lam + pi);
+            fma_col32(s_run, p.agg + pi * unit_stride + (int64_t)col_half * NT + row, ex2(logm * LOG2E));
+            logm += lam_i;
         }
         if (uprev_blk >= 0) {
-            const float sc = ex2(logm * LOG2E);
             const int64_t pi = (int64_t)uprev_blk * sh.H + h;
-            const float4 *src = reinterpret_cast<const float4 *>(p.incl + pi * unit_stride + (int64_t)tid * PT);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                float4 v = __ldcg(src + q);
-                s_run[4 * q] += sc * v.x;
-                s_run[4 * q + 1] += sc * v.y;
-                s_run[4 * q + 2] += sc * v.z;
-                s_run[4 * q + 3] += sc * v.w;
-            }
+            fma_col32(s_run, p.incl + pi * unit_stride + (int64_t)col_half * NT + row, ex2(logm * LOG2E));
         } else if (p.init) {
             const float sc = ex2(logm * LOG2E);
-            const float *src = p.init + ((int64_t)ui.seq * sh.H + h) * PT * NT + tid;
+            const float *src = p.init + ((int64_t)ui.seq * sh.H + h) * PT * NT + (int64_t)col_half * NT + row;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) s_run[i] += sc * src[(int64_t)i * NT];
+            for (int i = 0; i < 32; ++i) s_run[i] += sc * src[(int64_t)i * NT];
         }
         if ((ui.j % KB) == KB - 1 && !ui.last) {   // block end: publish the unit's end state
             const float dec = ex2(lam_u * LOG2E);
-            float4 *dst = reinterpret_cast<float4 *>(p.incl + my * unit_stride + (int64_t)tid * PT);
+            float *dst = p.incl + my * unit_stride + (int64_t)col_half * NT + row;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                __stcg(dst + i, make_float4(a_reg[4 * i] + dec * s_run[4 * i], a_reg[4 * i + 1] + dec * s_run[4 * i + 1],
-                                            a_reg[4 * i + 2] + dec * s_run[4 * i + 2],
-                                            a_reg[4 * i + 3] + dec * s_run[4 * i + 3]));
+            for (int i = 0; i < 32; ++i) __stcg(dst + (int64_t)i * NT, a_reg[i] + dec * s_run[i]);
             __threadfence();
             __syncthreads();
             if (tid == 0) st_release_u32(p.flags + my, 2u);
         }
 
         // ---- phase 2: outputs
+        const float Dh = p.D ? p.D[h] : 0.f;
         for (int c = 0; c < ui.nchunk; ++c) {
             const uint32_t seq = load_seq + c;
             const int tc0 = ui.t0 + c * QT;
@@ -392,42 +388,41 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 if (tid == 0) issue_load(seq + 1, h, g, tc0 + QT, ui.b, true);
                 ++ld_issued;
             }
+            // gate values of this thread's output row/half, fetched early
+            const int64_t tok = (int64_t)tc0 + row;
+            uint4 zv[4];
+            const bool has_z = p.z != nullptr && row < clen;
+            if (has_z) {
+                const uint4 *zp = reinterpret_cast<const uint4 *>(p.z + (int64_t)ui.b * p.szb + tok * p.szl +
+                                                                  (int64_t)h * p.szh + col_half);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) zv[q] = __ldcs(zp + q);
+            }
             // chunk-local cumulative log-decay
-            const float dtl = dtu[c * QT + tid];
+            const float dtl = (tid < QT) ? dtu[c * QT + tid] : 0.f;
             float ctot;
-            const float csl = block_scan128(dtl * Ah, ms->wsum, &ctot);
-            cs2[tid] = csl * LOG2E;
-            dtc[tid] = dtl;
+            const float csl = block_scan(dtl * Ah, ms->wsum, &ctot);
+            if (tid < QT) {
+                cs2[tid] = csl * LOG2E;
+                dtc[tid] = dtl;
+            }
             const float a_c = ex2(ctot * LOG2E);
             // carried state S_in (bf16, K-major [p][n]) for Y_off
             {
-                const int n = tid, ac = n >> 6, cn = (n & 63) >> 3;
+                const int n = row, ac = n >> 6, cn = (n & 63) >> 3;
                 uint8_t *base = Ss + ac * (S_BYTES / 2) + (n & 7) * 2;
 #pragma unroll
-                for (int pp = 0; pp < 64; ++pp) {
+                for (int i = 0; i < 32; ++i) {
+                    const int pp = (int)col_half + i;
                     *reinterpret_cast<__nv_bfloat16 *>(base + pp * 128 + ((cn ^ (pp & 7)) << 4)) =
-                        __float2bfloat16_rn(s_run[pp]);
+                        __float2bfloat16_rn(s_run[i]);
                 }
             }
             wait_load(seq);
             __syncthreads();   // cs2/dtc visible
             const uint8_t *st = stage_ptr(seq);
-            {   // Wx = w o x, w[l] = dt[l] exp(cs[Q-1] - cs[l])
-                const float wl = dtc[tid] * ex2(cs2[QT - 1] - cs2[tid]);
-                const uint4 *src = reinterpret_cast<const uint4 *>(st + tid * 128);
-                uint4 *dst = reinterpret_cast<uint4 *>(Wx + tid * 128);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    uint4 v = src[q];
-                    __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&v);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float2 f = __bfloat1622float2(e[i]);
-                        e[i] = __floats2bfloat162_rn(f.x * wl, f.y * wl);
-                    }
-                    dst[q] = v;
-                }
-            }
+            // Wx = w o x, w[l] = dt[l] exp(cs[Q-1] - cs[l])
+            scale_row_half(st + row * 128, Wx + row * 128, row, hf, dtc[row] * ex2(cs2[QT - 1] - cs2[row]));
             fence_proxy_async_smem();
             __syncthreads();
             if (ms->abort_) break;
@@ -447,15 +442,17 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             }
             ++mma_issued;
             wait_mma();
-            // M (bf16, K-major [l][s]) into the B buffer, which the MMAs above are done with
+            // M (bf16, K-major [l][s]) into the B buffer, which the MMAs above are done with.
+            // Half 0 builds s-blocks {0, 3}, half 1 {1, 2}; blocks above the diagonal are zero.
             {
                 uint8_t *Ms = const_cast<uint8_t *>(st) + X_BYTES;
-                const int l = tid;
+                const int l = row;
                 const float cl = cs2[l];
 #pragma unroll
-                for (int sb = 0; sb < 4; ++sb) {
+                for (int bi = 0; bi < 2; ++bi) {
+                    const int sb = hf == 0 ? (bi == 0 ? 0 : 3) : (bi == 0 ? 1 : 2);
                     uint32_t pk[16];
-                    if (sb <= warp) {
+                    if (sb <= quad) {
                         float cb[32];
                         tmem_ld32(tmem + lane_base + TM_CB + sb * 32, cb);
                         tmem_wait_ld();
@@ -478,70 +475,56 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                             make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                     }
                 }
-                // carried state update: S_in[c+1] = a_c S_in[c] + S_c (row n = tid)
+                // carried state update: S_in[c+1] = a_c S_in[c] + S_c (row n, this half's columns)
                 float sc[32];
-                tmem_ld32(tmem + lane_base + TM_SC, sc);
+                tmem_ld32(tmem + lane_base + TM_SC + col_half, sc);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s_run[i] = a_c * s_run[i] + sc[i];
-                tmem_ld32(tmem + lane_base + TM_SC + 32, sc);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s_run[32 + i] = a_c * s_run[32 + i] + sc[i];
             }
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
             if (tid == 0) {
                 tc_fence_after();
-                const uint32_t sM = sB;
 #pragma unroll
                 for (int k = 0; k < QT / 16; ++k)   // Y_diag = M x (K = source tokens)
-                    umma_bf16(tmem + TM_CB, kmaj(sM, k, BC_BYTES / 2), mnmaj(sX, k), idesc_yd, k > 0);
+                    umma_bf16(tmem + TM_CB, kmaj(sB, k, BC_BYTES / 2), mnmaj(sX, k), idesc_yd, k > 0);
                 umma_commit(&ms->bar_mma);
             }
             ++mma_issued;
             wait_mma();
-            {   // epilogue: row l = tid
-                const int l = tid;
+            {   // epilogue: row l, this thread's half of the 64 output columns
+                const int l = row;
                 float yd[32], yo[32];
-                const float el = ex2(cs2[l]);
-                const float Dh = p.D ? p.D[h] : 0.f;
-                const int64_t tok = (int64_t)tc0 + l;
+                tmem_ld32(tmem + lane_base + TM_CB + col_half, yd);
+                tmem_ld32(tmem + lane_base + TM_YO + col_half, yo);
+                tmem_wait_ld();
+                if (l < clen) {
+                    const float el = ex2(cs2[l]);
+                    const uint8_t *xrow = st + l * 128;
+                    __nv_bfloat16 *yrow = p.y + (int64_t)ui.b * p.syb + tok * p.syl + (int64_t)h * p.syh + col_half;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_base + TM_CB + half * 32, yd);
-                    tmem_ld32(tmem + lane_base + TM_YO + half * 32, yo);
-                    tmem_wait_ld();
-                    if (l < clen) {
-                        const uint8_t *xrow = st + l * 128;
-                        __nv_bfloat16 *yrow = p.y + (int64_t)ui.b * p.syb + tok * p.syl + (int64_t)h * p.syh + half * 32;
-                        const __nv_bfloat16 *zrow =
-                            p.z ? p.z + (int64_t)ui.b * p.szb + tok * p.szl + (int64_t)h * p.szh + half * 32 : nullptr;
+                    for (int q = 0; q < 4; ++q) {
+                        const int cidx = hf * 4 + q;
+                        uint4 xv = *reinterpret_cast<const uint4 *>(xrow + ((cidx ^ (l & 7)) << 4));
+                        const __nv_bfloat162 *xe = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+                        const __nv_bfloat162 *ze = reinterpret_cast<const __nv_bfloat162 *>(&zv[q]);
+                        uint32_t o[4];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int cidx = half * 4 + q;
-                            uint4 xv = *reinterpret_cast<const uint4 *>(xrow + ((cidx ^ (l & 7)) << 4));
-                            const __nv_bfloat162 *xe = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-                            uint4 zv;
-                            if (zrow) zv = *reinterpret_cast<const uint4 *>(zrow + q * 8);
-                            const __nv_bfloat162 *ze = reinterpret_cast<const __nv_bfloat162 *>(&zv);
-                            uint32_t o[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 xf = __bfloat1622float2(xe[i]);
-                                const int j = q * 8 + 2 * i;
-                                float v0 = yd[j] + el * yo[j] + Dh * xf.x;
-                                float v1 = yd[j + 1] + el * yo[j + 1] + Dh * xf.y;
-                                if (zrow) {
-                                    const float2 zf = __bfloat1622float2(ze[i]);
-                                    v0 *= zf.x * rcp(1.f + ex2(-zf.x * LOG2E));
-                                    v1 *= zf.y * rcp(1.f + ex2(-zf.y * LOG2E));
-                                }
-                                o[i] = pack_bf16(v0, v1);
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 xf = __bfloat1622float2(xe[i]);
+                            const int j = q * 8 + 2 * i;
+                            float v0 = yd[j] + el * yo[j] + Dh * xf.x;
+                            float v1 = yd[j + 1] + el * yo[j + 1] + Dh * xf.y;
+                            if (has_z) {
+                                const float2 zf = __bfloat1622float2(ze[i]);
+                                v0 *= zf.x * rcp(1.f + ex2(-zf.x * LOG2E));
+                                v1 *= zf.y * rcp(1.f + ex2(-zf.y * LOG2E));
                             }
-                            *reinterpret_cast<uint4 *>(yrow + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+                            o[i] = pack_bf16(v0, v1);
                         }
+                        *reinterpret_cast<uint4 *>(yrow + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
             }
@@ -551,9 +534,9 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         load_seq += ui.nchunk;
         if (ms->abort_) break;
         if (ui.last && p.final_) {
-            float *dst = p.final_ + ((int64_t)ui.seq * sh.H + h) * PT * NT + tid;
+            float *dst = p.final_ + ((int64_t)ui.seq * sh.H + h) * PT * NT + (int64_t)col_half * NT + row;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = s_run[i];
+            for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = s_run[i];
         }
     }
     // Drain (only non-empty after an early stop): bounded waits for loads and
@@ -617,8 +600,8 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
     fp.szb = sz ? sz[0] : 0; fp.szl = sz ? sz[1] : 0; fp.szh = sz ? sz[2] : 0;
     fp.y = (__nv_bfloat16 *)y; fp.syb = sy[0]; fp.syl = sy[1]; fp.syh = sy[2];
     fp.init = init; fp.final_ = final_; fp.agg = agg; fp.incl = incl; fp.lam = lam; fp.flags = flags;
-    static unsigned long long attr_done = 0;
-    cudaError_t e = ensure_smem_attr(k_fused_fwd, (int)SMEM_BYTES, &attr_done);
+    static int attr_done[64] = {0};
+    cudaError_t e = ensure_smem_attr(k_fused_fwd, (int)SMEM_BYTES, attr_done);
     if (e != cudaSuccess) return e;
     k_fused_fwd<<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, fp);
     return cudaGetLastError();

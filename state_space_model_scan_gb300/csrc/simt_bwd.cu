@@ -366,8 +366,8 @@ cudaError_t launch_bwd_chunk(const Shape &sh, const int32_t *hdr, const ChunkInf
                              const float *states, const float *dstates, MView3 dx, MView3 dz, float *ddt,
                              int64_t sddb, int64_t sddl, float *dBh, float *dCh, float *partials, cudaStream_t st) {
     const size_t smem = bwd_chunk_smem(sh);
-    static unsigned long long attr_done = 0;
-    cudaError_t e = ensure_smem_attr(k_bwd_chunk<T>, (int)smem, &attr_done);
+    static int attr_done[64] = {0};
+    cudaError_t e = ensure_smem_attr(k_bwd_chunk<T>, (int)smem, attr_done);
     if (e != cudaSuccess) return e;
     k_bwd_chunk<T><<<dim3(sh.kmax, sh.H), 256, smem, st>>>(sh, hdr, chunks, x, Bm, Cm, z, dy, dt_raw, sdb, sdl, A, D,
                                                            bias, dtw, csw, states, dstates, dx, dz, ddt, sddb, sddl,

@@ -286,8 +286,8 @@ cudaError_t launch_chunk_scan(const Shape &sh, const int32_t *hdr, const ChunkIn
                               View3 Cm, View3 z, const float *D, const float *dtw, const float *csw,
                               const float *states, MView3 y, cudaStream_t st) {
     const size_t smem = chunk_scan_smem(sh);
-    static unsigned long long attr_done = 0;
-    cudaError_t e = ensure_smem_attr(k_chunk_scan<T>, (int)smem, &attr_done);
+    static int attr_done[64] = {0};
+    cudaError_t e = ensure_smem_attr(k_chunk_scan<T>, (int)smem, attr_done);
     if (e != cudaSuccess) return e;
     k_chunk_scan<T><<<dim3(sh.kmax, sh.H, sh.Q / 32), 256, smem, st>>>(sh, hdr, chunks, x, Bm, Cm, z, D, dtw, csw,
                                                                         states, y);
