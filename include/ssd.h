@@ -148,6 +148,27 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *args, void *work
  */
 ssd_status ssd_query_status(const void *workspace, void *stream);
 
+/*
+ * ssd_fwd_noalloc
+ * The forward scan (same operation, arguments and results as ssd_fwd) for
+ * callers that cannot allocate device memory where they run it: code running
+ * while a CUDA graph is captured (allocation is not a capturable operation),
+ * serving runtimes that reserve all device memory in their own pools, and
+ * real-time loops that must not call the allocator.  There is no counterpart on
+ * the source pages: it is a deployment variant of ssd_fwd.
+ * The scratch memory is a library-owned static device array of
+ * SSD_NOALLOC_SCRATCH_BYTES bytes; a problem whose ssd_fwd workspace would be
+ * larger is rejected with SSD_ERR_WORKSPACE_TOO_SMALL before any launch.  The
+ * array is loaded on the first call on a device, which also looks up its device
+ * address once (make that first call before any stream capture); it stays
+ * allocated until the process exits.  Nothing is allocated or freed per call.
+ * All calls share the one array (each call re-initialises the parts that must
+ * start at zero), so calls whose work overlaps on the GPU -- on different
+ * streams or host threads without ordering -- race and must not be issued.
+ */
+#define SSD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+ssd_status ssd_fwd_noalloc(const ssd_problem *prob, const ssd_fwd_args *args, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *ssd_status_string(ssd_status status);
 

@@ -21,7 +21,8 @@ ALGO = {"auto": 0, "staged": 1, "fused": 2}
 
 # Every symbol include/ssd.h declares.
 EXPORTS = ["ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
-           "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout"]
+           "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout", "ssd_fwd_noalloc"]
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class SSDError(RuntimeError):
@@ -83,8 +84,9 @@ def load(path: str = LIB_PATH):
     lib.ssd_status_string.restype = ctypes.c_char_p
     lib.ssd_abi_version.restype = ctypes.c_int32
     lib.ssd_fwd_debug_layout.argtypes = [P(Problem), P(FwdArgs), P(DebugLayout)]
+    lib.ssd_fwd_noalloc.argtypes = [P(Problem), P(FwdArgs), ctypes.c_void_p]
     for f in ("ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
-              "ssd_fwd_debug_layout"):
+              "ssd_fwd_debug_layout", "ssd_fwd_noalloc"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -166,6 +168,11 @@ def ssd_fwd(prob, args, workspace, stream=None):
 def ssd_bwd(prob, args, workspace, stream=None):
     return load().ssd_bwd(ctypes.byref(prob), ctypes.byref(args), ctypes.c_void_p(workspace.data_ptr()),
                           ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream))
+
+
+def ssd_fwd_noalloc(prob, args, stream=None):
+    """Raw call of the forward that uses the library's static scratch (no workspace)."""
+    return load().ssd_fwd_noalloc(ctypes.byref(prob), ctypes.byref(args), _stream_handle(stream))
 
 
 def query_status(workspace, stream=None):

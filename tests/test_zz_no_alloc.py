@@ -1,0 +1,68 @@
+"""ssd_fwd_noalloc: the forward for callers that cannot allocate device memory.
+
+Runs through the C ABI and must give the same results as ssd_fwd with a
+caller-supplied workspace, on two calls in a row (the shared static scratch keeps
+the previous call's contents; each call must re-initialise what it needs).  This
+file is collected last on purpose.
+"""
+import numpy as np
+import pytest
+import torch
+
+from state_space_model_scan_gb300 import inputs as I
+from state_space_model_scan_gb300 import _lib
+from helpers import TOL, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _args(w, inp):
+    d = to_dev(inp)
+    y = torch.full_like(d["x"], float("nan"))
+    fin = torch.full((w.nseqs, w.nheads, w.headdim, w.dstate), float("nan"), device="cuda")
+    prob = _lib.problem(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk_size,
+                        w.nseqs if inp["cu_seqlens"] is not None else 0)
+    args = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                         initial_states=d["initial_states"], final_states=fin, cu_seqlens=d["cu_seqlens"])
+    return prob, args, y, fin, d
+
+
+@pytest.mark.parametrize("w", [
+    I.Workload("fused", 2, 1500, 8, 64, 2, 128, 128, "bf16", has_z=True, has_init=True),
+    I.Workload("staged", 1, 300, 4, 32, 2, 64, 64, "f32", has_z=True, has_init=True),
+    I.Workload("packed", 1, 600, 8, 64, 1, 128, 128, "bf16", has_init=True, seqlens=[100, 0, 373, 127]),
+], ids=lambda w: w.name)
+def test_noalloc_matches_workspace_forward_twice(w):
+    inp = I.make_inputs(w)
+    prob, args, y_ref, fin_ref, _ = _args(w, inp)
+    ws = torch.empty(_lib.fwd_workspace_size(prob, args), dtype=torch.uint8, device="cuda")
+    assert ws.numel() <= _lib.NOALLOC_SCRATCH_BYTES
+    _lib.check(_lib.ssd_fwd(prob, args, ws), "ssd_fwd")
+    torch.cuda.synchronize()
+    tol = TOL[w.dtype]
+    for _ in range(2):
+        prob2, args2, y, fin, _ = _args(w, inp)
+        _lib.check(_lib.ssd_fwd_noalloc(prob2, args2), "ssd_fwd_noalloc")
+        torch.cuda.synchronize()
+        assert torch.isfinite(y.float()).all() and torch.isfinite(fin).all()
+        assert rel_l2(y.double().cpu(), y_ref.double().cpu()) <= tol
+        assert rel_l2(fin.double().cpu(), fin_ref.double().cpu()) <= tol
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    w = I.Workload("big", 4, 8192, 64, 64, 8, 128, 128, "bf16", has_z=False)
+    # metadata only: the pointers are never dereferenced because the call is rejected first
+    prob = _lib.problem(w.batch, w.seqlen, w.nheads, 64, 8, 128, 128, 0, "staged")
+    x = torch.empty(1, dtype=torch.bfloat16, device="cuda")
+    f = torch.empty(1, device="cuda")
+    args = _lib.FwdArgs()
+    for name, t, strides in (("x", x, [8192 * 64 * 64, 64 * 64, 64, 1]), ("y", x, [8192 * 64 * 64, 64 * 64, 64, 1]),
+                             ("B", x, [8192 * 8 * 128, 8 * 128, 128, 1]), ("C", x, [8192 * 8 * 128, 8 * 128, 128, 1]),
+                             ("dt", f, [8192 * 64, 64, 1]), ("A", f, [1])):
+        tt = _lib.tensor(t)
+        for i, s in enumerate(strides):
+            tt.stride[i] = s
+        setattr(args, name, tt)
+    need = _lib.fwd_workspace_size(prob, args)
+    assert need > _lib.NOALLOC_SCRATCH_BYTES
+    assert _lib.ssd_fwd_noalloc(prob, args) == 4
