@@ -18,8 +18,9 @@ cudaError_t launch_chunk_cumsum(const Shape &sh, const int32_t *hdr, const Chunk
 template <typename T>
 cudaError_t launch_chunk_state(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 x, View3 Bm,
                                const float *dtw, const float *csw, float *states, cudaStream_t st);
-cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqInfo *seqs, const float *csw,
-                                 float *states, const float *init, float *final_, int reverse, cudaStream_t st);
+cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqInfo *seqs, const float *lamw,
+                                 int lam_stride, float *states, const float *init, float *final_, int reverse,
+                                 cudaStream_t st);
 template <typename T>
 cudaError_t launch_chunk_scan(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 x, View3 Bm,
                               View3 Cm, View3 z, const float *D, const float *dtw, const float *csw,
@@ -44,12 +45,17 @@ size_t chunk_scan_smem(const Shape &sh);
 // fused_fwd.cu
 int fused_rmax();
 int fused_block_units();
+// bwd_tc.cu
+cudaError_t launch_bwd_dstates_tc(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const BwdTcArgs &a,
+                                  cudaStream_t st);
+cudaError_t launch_bwd_chunk_tc(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const BwdTcArgs &a,
+                                cudaStream_t st);
 cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *units, const void *x, const int64_t *sx,
                              const void *Bp, const int64_t *sb, const void *Cp, const int64_t *sc, const float *dt_raw,
                              int64_t sdb, int64_t sdl, const float *A, const float *D, const float *bias,
                              const void *z, const int64_t *sz, void *y, const int64_t *sy, const float *init,
                              float *final_, float *agg, float *incl, float *lam, uint32_t *flags, int grid,
-                             cudaStream_t st);
+                             __nv_bfloat16 *states_out, const SeqInfo *seqs, cudaStream_t st);
 }  // namespace ssd
 
 using namespace ssd;
@@ -124,7 +130,8 @@ ssd_status check_vec(const ssd_tensor &t, bool required) {
         if (_s != SSD_OK) return _s;       \
     } while (0)
 
-ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Plan *out) {
+ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Plan *out,
+                       const ssd_bwd_args *b = nullptr) {
     if (p == nullptr || a == nullptr || out == nullptr) return SSD_ERR_INVALID_ARGUMENT;
     const int64_t B = p->batch, L = p->seqlen, H = p->nheads, P = p->headdim, G = p->ngroups, N = p->dstate;
     if (B < 1 || L < 0 || H < 1 || G < 1 || P < 1 || N < 1 || p->chunk_size < 1) return SSD_ERR_INVALID_ARGUMENT;
@@ -167,11 +174,13 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     // dstate 128 whose x/B/C/z/y obey the 16-byte rule of TMA and vector access;
     // everything else (fp32 inputs in particular) runs the SIMT pipeline.  The
     // backward always runs the staged pipeline.
-    bool tc_ok = !bwd && pl.bf16 && P == 64 && N == 128;
+    bool tc_ok = pl.bf16 && P == 64 && N == 128;
     bool aligned = true;
     {
-        const ssd_tensor *ts[5] = {&a->x, &a->B, &a->C, &a->z, &a->y};
+        const ssd_tensor *ts[8] = {&a->x, &a->B, &a->C, &a->z, bwd ? nullptr : &a->y, b ? &b->dy : nullptr,
+                                   b ? &b->dx : nullptr, b ? &b->dz : nullptr};
         for (const ssd_tensor *t : ts) {
+            if (t == nullptr) continue;
             if (t->ptr == nullptr) continue;
             if (((uintptr_t)t->ptr) % 16 != 0) aligned = false;
             for (int i = 0; i < 3; ++i)
@@ -186,6 +195,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
                                                                                            : SSD_ALGO_STAGED;
     const bool fused = pl.algo == SSD_ALGO_FUSED;
     const int Q = fused ? kTcQ : kSimtQ;
+    if (fused && bwd && b == nullptr) return SSD_ERR_INVALID_ARGUMENT;
     int64_t kmax = varlen ? (L + Q - 1) / Q + S : B * ((L + Q - 1) / Q);
     if (kmax > (int64_t)1 << 30) return SSD_ERR_UNSUPPORTED;
     int R = 1;
@@ -218,12 +228,20 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         pl.off_incl = lay.take(sizeof(float) * uh * (size_t)(P * N));
         pl.off_lam = lay.take(sizeof(float) * uh);
         pl.off_flags = lay.take(sizeof(uint32_t) * uh);
+        if (bwd) {
+            pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * N));   // carried states, bf16
+            pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * N));
+            pl.off_cs = lay.take(sizeof(float) * kh);                                // chunk total log-decay
+            pl.off_dBh = lay.take(sizeof(float) * kh * Q * (size_t)N);
+            pl.off_dCh = lay.take(sizeof(float) * kh * Q * (size_t)N);
+            pl.off_part = lay.take(sizeof(float) * kh * 4);
+        }
     } else {
         pl.off_dt = lay.take(sizeof(float) * kh * Q);
         pl.off_cs = lay.take(sizeof(float) * kh * Q);
         pl.off_states = lay.take(sizeof(float) * kh * (size_t)(P * N));
     }
-    if (bwd) {
+    if (bwd && !fused) {
         pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * N));
         pl.off_dBh = lay.take(sizeof(float) * kh * Q * (size_t)N);
         pl.off_dCh = lay.take(sizeof(float) * kh * Q * (size_t)N);
@@ -236,7 +254,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
 
 ssd_status plan_bwd(const ssd_problem *p, const ssd_bwd_args *b, Plan *out) {
     if (b == nullptr) return SSD_ERR_INVALID_ARGUMENT;
-    SSD_TRY(plan_common(p, &b->fwd, true, out));
+    SSD_TRY(plan_common(p, &b->fwd, true, out, b));
     const int dt_ = b->fwd.x.dtype;
     const int64_t H = p->nheads, P = p->headdim, N = p->dstate;
     const bool tok = p->seqlen > 0;
@@ -291,7 +309,8 @@ ssd_status run_forward_states(const Plan &pl, const ssd_fwd_args *a, void *ws, f
         else
             SSD_CUDA(launch_chunk_state<float>(sh, hdr, chunks, view(a->x), view(a->B), dtw, csw, states, st));
     }
-    SSD_CUDA(launch_state_passing(sh, hdr, seqs, csw, states, (const float *)a->initial_states.ptr, final_, 0, st));
+    SSD_CUDA(launch_state_passing(sh, hdr, seqs, csw + (sh.Q - 1), sh.Q, states, (const float *)a->initial_states.ptr,
+                                  final_, 0, st));
     return SSD_OK;
 }
 
@@ -362,7 +381,8 @@ ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, siz
                                       (const float *)a->A.ptr, (const float *)a->D.ptr, (const float *)a->dt_bias.ptr,
                                       a->z.ptr, a->z.ptr ? a->z.stride : nullptr, a->y.ptr, a->y.stride,
                                       (const float *)a->initial_states.ptr, final_, at<float>(ws, pl.off_agg),
-                                      at<float>(ws, pl.off_incl), at<float>(ws, pl.off_lam), flags, grid, st));
+                                      at<float>(ws, pl.off_incl), at<float>(ws, pl.off_lam), flags, grid, nullptr,
+                                      seqs, st));
         }
         if (final_ != nullptr && (pl.varlen || sh.L == 0))
             SSD_CUDA(launch_empty_seq_final(sh.S, sh.H, sh.P * sh.N, seqs, hdr,
@@ -400,6 +420,50 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
     cudaStream_t st = (cudaStream_t)stream;
     const Shape &sh = pl.sh;
     const ssd_fwd_args *a = &b->fwd;
+    if (pl.algo == SSD_ALGO_FUSED) {
+        int32_t *hdr = at<int32_t>(ws, pl.off_hdr);
+        SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
+        ChunkInfo *chunks = at<ChunkInfo>(ws, pl.off_chunks);
+        UnitInfo *units = at<UnitInfo>(ws, pl.off_units);
+        uint32_t *flags = at<uint32_t>(ws, pl.off_flags);
+        __nv_bfloat16 *states = at<__nv_bfloat16>(ws, pl.off_states);
+        float *dS = at<float>(ws, pl.off_dstates), *clam = at<float>(ws, pl.off_cs);
+        float *dBh = at<float>(ws, pl.off_dBh), *dCh = at<float>(ws, pl.off_dCh), *part = at<float>(ws, pl.off_part);
+        SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, sh.R, fused_block_units(), sh.kmax,
+                                   sh.umax, hdr, seqs, chunks, units, at<int32_t>(ws, pl.off_lastunit), flags,
+                                   (int64_t)sh.umax * sh.H, st));
+        const int64_t tickets = (int64_t)sh.umax * sh.H;
+        if (tickets > 0) {
+            // carried state entering every chunk (forward recomputed in states-only mode)
+            const int grid = (int)(tickets < num_sms() ? tickets : num_sms());
+            SSD_CUDA(launch_fused_fwd(sh, hdr, units, a->x.ptr, a->x.stride, a->B.ptr, a->B.stride, a->C.ptr,
+                                      a->C.stride, (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1],
+                                      (const float *)a->A.ptr, (const float *)a->D.ptr, (const float *)a->dt_bias.ptr,
+                                      nullptr, nullptr, nullptr, a->x.stride, (const float *)a->initial_states.ptr,
+                                      nullptr, at<float>(ws, pl.off_agg), at<float>(ws, pl.off_incl),
+                                      at<float>(ws, pl.off_lam), flags, grid, states, seqs, st));
+        }
+        BwdTcArgs ta;
+        ta.x = a->x.ptr; ta.Bp = a->B.ptr; ta.Cp = a->C.ptr;
+        ta.sx = a->x.stride; ta.sb = a->B.stride; ta.sc = a->C.stride;
+        ta.dt_raw = (const float *)a->dt.ptr; ta.sdb = a->dt.stride[0]; ta.sdl = a->dt.stride[1];
+        ta.A = (const float *)a->A.ptr; ta.D = (const float *)a->D.ptr; ta.bias = (const float *)a->dt_bias.ptr;
+        ta.dy = b->dy.ptr; ta.z = a->z.ptr; ta.sdy = b->dy.stride; ta.sz = a->z.ptr ? a->z.stride : nullptr;
+        ta.dx = b->dx.ptr; ta.dz = b->dz.ptr; ta.sdx = b->dx.stride; ta.sdz = b->dz.ptr ? b->dz.stride : nullptr;
+        ta.ddt = (float *)b->ddt.ptr; ta.sddb = b->ddt.stride[0]; ta.sddl = b->ddt.stride[1];
+        ta.states = states; ta.dS = dS; ta.chunk_lam = clam; ta.dBh = dBh; ta.dCh = dCh; ta.partials = part;
+        if (sh.kmax > 0) SSD_CUDA(launch_bwd_dstates_tc(sh, hdr, chunks, ta, st));
+        SSD_CUDA(launch_state_passing(sh, hdr, seqs, clam, 1, dS, (const float *)b->dfinal_states.ptr,
+                                      (float *)b->dinitial_states.ptr, 1, st));
+        if (sh.kmax > 0) {
+            SSD_CUDA(launch_bwd_chunk_tc(sh, hdr, chunks, ta, st));
+            SSD_CUDA(launch_reduce_group<__nv_bfloat16>(sh, hdr, chunks, dBh, mview(b->dB), st));
+            SSD_CUDA(launch_reduce_group<__nv_bfloat16>(sh, hdr, chunks, dCh, mview(b->dC), st));
+        }
+        SSD_CUDA(launch_reduce_heads(sh, hdr, part, (float *)b->dA.ptr, (float *)b->dD.ptr,
+                                     (float *)b->ddt_bias.ptr, st));
+        return SSD_OK;
+    }
     SSD_TRY(run_forward_states(pl, a, ws, nullptr, st));
     int32_t *hdr = at<int32_t>(ws, pl.off_hdr);
     SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
@@ -414,7 +478,7 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         else
             SSD_CUDA(launch_bwd_dstates<float>(sh, hdr, chunks, view(b->dy), view(a->z), view(a->C), csw, dstates, st));
     }
-    SSD_CUDA(launch_state_passing(sh, hdr, seqs, csw, dstates, (const float *)b->dfinal_states.ptr,
+    SSD_CUDA(launch_state_passing(sh, hdr, seqs, csw + (sh.Q - 1), sh.Q, dstates, (const float *)b->dfinal_states.ptr,
                                   (float *)b->dinitial_states.ptr, 1, st));
     if (sh.kmax > 0) {
         if (pl.bf16) {

@@ -45,6 +45,23 @@ struct Shape {
     int R;            // chunks per unit (fused path)
 };
 
+// Arguments of the tensor-core backward kernels (bwd_tc.cu).
+struct BwdTcArgs {
+    const void *x, *Bp, *Cp;
+    const int64_t *sx, *sb, *sc;
+    const float *dt_raw;
+    int64_t sdb, sdl;
+    const float *A, *D, *bias;
+    const void *dy, *z;
+    const int64_t *sdy, *sz;
+    void *dx, *dz;
+    const int64_t *sdx, *sdz;
+    float *ddt;
+    int64_t sddb, sddl;
+    const __nv_bfloat16 *states;   // [chunk][H][P][N] bf16 carried states
+    float *dS, *chunk_lam, *dBh, *dCh, *partials;
+};
+
 // Strided views (element strides of the three outer dims; innermost stride 1).
 struct View3 {
     const void *p;

@@ -89,6 +89,11 @@ struct FusedParams {
     float *final_;
     float *agg, *incl, *lam;
     uint32_t *flags;
+    // States-only mode (used by the backward): when set, the carried state at the
+    // start of every chunk is written here (bf16 [chunk][head][P][N]) and no output
+    // is computed (no CB, M, Y_off, Y_diag, y).  Chunk index = seqs[seq].chunk0 + j*R + c.
+    __nv_bfloat16 *states_out;
+    const SeqInfo *seqs;
 };
 
 struct Misc {
@@ -378,8 +383,10 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             if (tid == 0) st_release_u32(p.flags + my, 2u);
         }
 
-        // ---- phase 2: outputs
+        // ---- phase 2: outputs (or, in states-only mode, the carried state of every chunk)
         const float Dh = p.D ? p.D[h] : 0.f;
+        const bool full = p.states_out == nullptr;
+        const int64_t kfirst = full ? 0 : (int64_t)p.seqs[ui.seq].chunk0 + (int64_t)ui.j * sh.R;
         for (int c = 0; c < ui.nchunk; ++c) {
             const uint32_t seq = load_seq + c;
             const int tc0 = ui.t0 + c * QT;
@@ -391,7 +398,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             // gate values of this thread's output row/half, fetched early
             const int64_t tok = (int64_t)tc0 + row;
             uint4 zv[4];
-            const bool has_z = p.z != nullptr && row < clen;
+            const bool has_z = full && p.z != nullptr && row < clen;
             if (has_z) {
                 const uint4 *zp = reinterpret_cast<const uint4 *>(p.z + (int64_t)ui.b * p.szb + tok * p.szl +
                                                                   (int64_t)h * p.szh + col_half);
@@ -407,8 +414,12 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 dtc[tid] = dtl;
             }
             const float a_c = ex2(ctot * LOG2E);
-            // carried state S_in (bf16, K-major [p][n]) for Y_off
-            {
+            if (!full) {   // states-only: S_in[chunk] -> global bf16 [p][n] (row n, this half's p)
+                __nv_bfloat16 *dst = p.states_out + ((kfirst + c) * sh.H + h) * (int64_t)(PT * NT) +
+                                     (int64_t)col_half * NT + row;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(s_run[i]);
+            } else {   // carried state S_in (bf16, K-major [p][n]) for Y_off
                 const int n = row, ac = n >> 6, cn = (n & 63) >> 3;
                 uint8_t *base = Ss + ac * (S_BYTES / 2) + (n & 7) * 2;
 #pragma unroll
@@ -429,15 +440,20 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             const uint32_t sX = smem_u32(st), sB = sX + X_BYTES, sC = sB + BC_BYTES;
             if (tid == 0) {
                 tc_fence_after();
+                if (full) {
 #pragma unroll
-                for (int k = 0; k < NT / 16; ++k)   // CB = C B^T (K = state dim)
-                    umma_bf16(tmem + TM_CB, kmaj(sC, k, BC_BYTES / 2), kmaj(sB, k, BC_BYTES / 2), idesc_cb, k > 0);
+                    for (int k = 0; k < NT / 16; ++k)   // CB = C B^T (K = state dim)
+                        umma_bf16(tmem + TM_CB, kmaj(sC, k, BC_BYTES / 2), kmaj(sB, k, BC_BYTES / 2), idesc_cb, k > 0);
+                }
 #pragma unroll
                 for (int k = 0; k < QT / 16; ++k)   // S_c^T = B^T (w o x) (K = tokens)
                     umma_bf16(tmem + TM_SC, mnmaj(sB, k), mnmaj(sWx, k), idesc_sc, k > 0);
+                if (full) {
 #pragma unroll
-                for (int k = 0; k < NT / 16; ++k)   // Y_off = C S_in^T (K = state dim)
-                    umma_bf16(tmem + TM_YO, kmaj(sC, k, BC_BYTES / 2), kmaj(sSs, k, S_BYTES / 2), idesc_yo, k > 0);
+                    for (int k = 0; k < NT / 16; ++k)   // Y_off = C S_in^T (K = state dim)
+                        umma_bf16(tmem + TM_YO, kmaj(sC, k, BC_BYTES / 2), kmaj(sSs, k, S_BYTES / 2), idesc_yo,
+                                  k > 0);
+                }
                 umma_commit(&ms->bar_mma);
             }
             ++mma_issued;
@@ -452,7 +468,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 for (int bi = 0; bi < 2; ++bi) {
                     const int sb = hf == 0 ? (bi == 0 ? 0 : 3) : (bi == 0 ? 1 : 2);
                     uint32_t pk[16];
-                    if (sb <= quad) {
+                    if (full && sb <= quad) {
                         float cb[32];
                         tmem_ld32(tmem + lane_base + TM_CB + sb * 32, cb);
                         tmem_wait_ld();
@@ -485,6 +501,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
+            if (!full) continue;   // states-only: no outputs (uniform across the CTA)
             if (tid == 0) {
                 tc_fence_after();
 #pragma unroll
@@ -533,7 +550,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         }
         load_seq += ui.nchunk;
         if (ms->abort_) break;
-        if (ui.last && p.final_) {
+        if (ui.last && p.final_ && full) {
             float *dst = p.final_ + ((int64_t)ui.seq * sh.H + h) * PT * NT + (int64_t)col_half * NT + row;
 #pragma unroll
             for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = s_run[i];
@@ -588,7 +605,7 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
                              int64_t sdb, int64_t sdl, const float *A, const float *D, const float *bias,
                              const void *z, const int64_t *sz, void *y, const int64_t *sy, const float *init,
                              float *final_, float *agg, float *incl, float *lam, uint32_t *flags, int grid,
-                             cudaStream_t st) {
+                             __nv_bfloat16 *states_out, const SeqInfo *seqs, cudaStream_t st) {
     CUtensorMap mx, mb, mc;
     if (!make_map(&mx, x, PT, sh.H, sh.L, sh.B, sx[2], sx[1], sx[0])) return cudaErrorInvalidValue;
     if (!make_map(&mb, Bp, NT, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
@@ -600,6 +617,7 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
     fp.szb = sz ? sz[0] : 0; fp.szl = sz ? sz[1] : 0; fp.szh = sz ? sz[2] : 0;
     fp.y = (__nv_bfloat16 *)y; fp.syb = sy[0]; fp.syl = sy[1]; fp.syh = sy[2];
     fp.init = init; fp.final_ = final_; fp.agg = agg; fp.incl = incl; fp.lam = lam; fp.flags = flags;
+    fp.states_out = states_out; fp.seqs = seqs;
     static int attr_done[64] = {0};
     cudaError_t e = ensure_smem_attr(k_fused_fwd, (int)SMEM_BYTES, attr_done);
     if (e != cudaSuccess) return e;

@@ -315,7 +315,7 @@ __global__ void k_reduce_group(Shape sh, const int32_t *__restrict__ hdr, const 
         float a = 0.f;
         for (int j = 0; j < sh.hpg; ++j) {
             const int h = g * sh.hpg + j;
-            a += src[(((int64_t)k * sh.H + h) * QS + l) * N + n];
+            a += src[(((int64_t)k * sh.H + h) * sh.Q + l) * N + n];
         }
         T *o = (T *)dst.p + (int64_t)ci.b * dst.s0 + (int64_t)(ci.t0 + l) * dst.s1 + (int64_t)g * dst.s2;
         o[n] = from_f<T>(a);

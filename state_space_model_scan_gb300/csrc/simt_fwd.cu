@@ -105,12 +105,13 @@ k_chunk_state(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__rest
 // affine maps s -> a_j s + S_j across lanes (lane = chunk), composing
 // (a1, b1) then (a2, b2) into (a1 a2, a2 b1 + b2).  In place: S_c is replaced by
 // the chunk's carry-in state.  The carry after the last chunk is the final state.
+// The chunk's total log-decay is lamw[(chunk * H + h) * lam_stride].
 // With reverse = 1 the chunks are visited last to first: that is the backward
 // recursion dS_out[c] = exp(cs_{c+1}[Q-1]) dS_out[c+1] + dS_loc[c+1] (same affine
 // form, the chunk's own decay), with `init` = dfinal and `final_` = dinit.
 __global__ void __launch_bounds__(256)
 k_state_passing(Shape sh, const int32_t *__restrict__ hdr, const SeqInfo *__restrict__ seqs,
-                const float *__restrict__ csw, float *__restrict__ states,
+                const float *__restrict__ lamw, int lam_stride, float *__restrict__ states,
                 const float *__restrict__ init, float *__restrict__ final_, int reverse) {
     __shared__ float tile[8][32][33];
     if (hdr[HDR_STATUS] != 0) return;
@@ -132,7 +133,7 @@ k_state_passing(Shape sh, const int32_t *__restrict__ hdr, const SeqInfo *__rest
         for (int r = 0; r < nc; ++r)
             tl[r][lane] = states[((int64_t)chunk_of(c0 + r) * sh.H + h) * PN + e0 + lane];
         const float dec = (lane < nc)
-            ? expf(csw[((int64_t)chunk_of(c0 + lane) * sh.H + h) * sh.Q + sh.Q - 1]) : 1.f;
+            ? expf(lamw[((int64_t)chunk_of(c0 + lane) * sh.H + h) * lam_stride]) : 1.f;
         __syncwarp();
         for (int col = 0; col < 32; ++col) {
             float a = dec, b = (lane < nc) ? tl[lane][col] : 0.f;
@@ -268,12 +269,13 @@ cudaError_t launch_chunk_state(const Shape &sh, const int32_t *hdr, const ChunkI
     return cudaGetLastError();
 }
 
-cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqInfo *seqs, const float *csw,
-                                 float *states, const float *init, float *final_, int reverse, cudaStream_t st) {
+cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqInfo *seqs, const float *lamw,
+                                 int lam_stride, float *states, const float *init, float *final_, int reverse,
+                                 cudaStream_t st) {
     const int PN = sh.P * sh.N;
     if (sh.S * sh.H == 0) return cudaSuccess;
-    k_state_passing<<<dim3(sh.S * sh.H, (PN + 255) / 256), 256, 0, st>>>(sh, hdr, seqs, csw, states, init, final_,
-                                                                          reverse);
+    k_state_passing<<<dim3(sh.S * sh.H, (PN + 255) / 256), 256, 0, st>>>(sh, hdr, seqs, lamw, lam_stride, states,
+                                                                          init, final_, reverse);
     return cudaGetLastError();
 }
 

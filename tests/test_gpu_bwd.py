@@ -54,11 +54,30 @@ def test_bwd_fp32(case):
     check_bwd(W(**case))
 
 
+@pytest.mark.parametrize("algo", ["staged", "fused"])
 @pytest.mark.parametrize("case", [
     dict(L=600, H=8, P=64, G=2, N=128, Q=128, has_z=True, has_init=True),
+    dict(L=1, H=2, P=64, G=1, N=128, Q=128, has_init=True),
+    dict(L=127, H=6, P=64, G=2, N=128, Q=128, has_z=True),
+    dict(B=2, L=300, H=3, P=64, G=3, N=128, Q=128, has_D=False, has_dt_bias=False),
+    dict(L=1000, H=4, P=64, G=1, N=128, Q=128, has_z=True, has_init=True),
 ])
-def test_bwd_bf16(case):
-    check_bwd(W(dtype="bf16", **case))
+def test_bwd_bf16(case, algo):
+    check_bwd(W(dtype="bf16", **case), algo=algo)
+
+
+@pytest.mark.parametrize("seg", [1, 3])
+def test_bwd_fused_multi_unit(seg):
+    w = W(B=2, L=1300, H=4, P=64, G=2, N=128, Q=128, dtype="bf16", has_z=True, has_init=True)
+    inp = I.make_inputs(w, with_grad_inputs=True, with_dfinal=True)
+    from helpers import gpu_backward as gb
+    g = gb(w, inp, algo="fused", seg_chunks=seg)
+    o = oracle_backward(w, inp)
+    T = w.batch * w.seqlen
+    for gn, on in NAMES:
+        t = g[gn]
+        a = flat(t, T) if t.dim() >= 3 and gn != "dinitial_states" else t.detach().double().cpu().numpy()
+        assert rel_l2(a.reshape(o[on].shape), o[on]) <= TOL["bf16"], gn
 
 
 def test_bwd_varlen():
@@ -66,8 +85,15 @@ def test_bwd_varlen():
     check_bwd(w)
 
 
-def test_bwd_deterministic():
-    w = W(L=300, H=4, P=32, G=2, N=32, dtype="bf16", has_z=True, has_init=True)
+def test_bwd_varlen_fused():
+    lens = [40, 0, 130, 1, 270, 128]
+    w = I.Workload("v", 1, sum(lens), 4, 64, 2, 128, 128, "bf16", has_z=True, has_init=True, seqlens=lens)
+    check_bwd(w, algo="fused")
+
+
+@pytest.mark.parametrize("P,N", [(32, 32), (64, 128)])
+def test_bwd_deterministic(P, N):
+    w = W(L=700, H=4, P=P, G=2, N=N, dtype="bf16", has_z=True, has_init=True)
     inp = I.make_inputs(w, with_grad_inputs=True, with_dfinal=True)
     g1 = gpu_backward(w, inp)
     g2 = gpu_backward(w, inp)
