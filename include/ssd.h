@@ -94,7 +94,7 @@ typedef struct {
 typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs;
     int32_t algo;        /* ssd_algo */
-    int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..8 */
+    int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..4 */
 } ssd_problem;
 
 typedef struct {

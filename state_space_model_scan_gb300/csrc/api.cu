@@ -375,7 +375,8 @@ ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, siz
                                    (int64_t)sh.umax * sh.H, st));
         const int64_t tickets = (int64_t)sh.umax * sh.H;
         if (tickets > 0) {
-            const int grid = (int)(tickets < num_sms() ? tickets : num_sms());
+            const int64_t slots = 2LL * num_sms();   // two CTAs per SM
+            const int grid = (int)(tickets < slots ? tickets : slots);
             SSD_CUDA(launch_fused_fwd(sh, hdr, units, a->x.ptr, a->x.stride, a->B.ptr, a->B.stride, a->C.ptr,
                                       a->C.stride, (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1],
                                       (const float *)a->A.ptr, (const float *)a->D.ptr, (const float *)a->dt_bias.ptr,
@@ -435,7 +436,8 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         const int64_t tickets = (int64_t)sh.umax * sh.H;
         if (tickets > 0) {
             // carried state entering every chunk (forward recomputed in states-only mode)
-            const int grid = (int)(tickets < num_sms() ? tickets : num_sms());
+            const int64_t slots = 2LL * num_sms();   // two CTAs per SM
+            const int grid = (int)(tickets < slots ? tickets : slots);
             SSD_CUDA(launch_fused_fwd(sh, hdr, units, a->x.ptr, a->x.stride, a->B.ptr, a->B.stride, a->C.ptr,
                                       a->C.stride, (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1],
                                       (const float *)a->A.ptr, (const float *)a->D.ptr, (const float *)a->dt_bias.ptr,

@@ -6,7 +6,7 @@
 // metadata kernel lists them by segment index, then sequence; tickets put the
 // heads of one unit next to each other so the heads of a group share B/C tiles
 // in L2).  For one unit a CTA:
-//   phase 1  loads x, B per chunk (TMA) and accumulates, on the tensor cores, the
+//   phase 1  loads x, B per chunk (TMA, two stages) and accumulates, on the tensor cores, the
 //            unit's end-state contribution from a zero start,
 //              agg[n][p] = sum_l B[l][n] * dt[l] exp(cs_u[end] - cs_u[l]) * x[l][p],
 //            then publishes agg and the unit's total log-decay;
@@ -44,33 +44,36 @@ using namespace tc;
 constexpr int QT = 128;   // chunk length
 constexpr int PT = 64;    // head dim
 constexpr int NT = 128;   // state dim
-constexpr int RMAX = 8;   // max chunks per unit
+constexpr int RMAX = 4;   // max chunks per unit
 constexpr int KB = 8;     // segments per block of the carry-in fold
-constexpr int NTHR = 256;
+constexpr int NTHR = 128; // one thread per tile row / TMEM lane
 
 constexpr uint32_t X_BYTES = QT * PT * 2;    // 16 KB
 constexpr uint32_t BC_BYTES = QT * NT * 2;   // 32 KB
 constexpr uint32_t S_BYTES = PT * NT * 2;    // 16 KB
-constexpr uint32_t STAGE_BYTES = X_BYTES + 2 * BC_BYTES;
 
-// shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t OFF_STAGE0 = 0;
-constexpr uint32_t OFF_STAGE1 = STAGE_BYTES;            // 81920
-constexpr uint32_t OFF_WX = 2 * STAGE_BYTES;            // 163840
-constexpr uint32_t OFF_SS = OFF_WX + X_BYTES;           // 180224
-constexpr uint32_t OFF_DTU = OFF_SS + S_BYTES;          // 196608
-constexpr uint32_t OFF_WU = OFF_DTU + RMAX * QT * 4;    // 200704
-constexpr uint32_t OFF_CS2 = OFF_WU + RMAX * QT * 4;    // 204800
-constexpr uint32_t OFF_DTC = OFF_CS2 + QT * 4;          // 205312
-constexpr uint32_t OFF_MISC = OFF_DTC + QT * 4;         // 205824
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 256 + 1024;  // + alignment slack
+// Shared memory (offsets from a 1024-aligned base), about 102 KB so that two CTAs
+// share an SM and fill each other's load / tensor-core waits.
+//   X  : x tile                     phase 1: stage-0 x (scaled in place to w o x)
+//   B  : B tile, then M             phase 1: stage-0 B
+//   C  : C tile                     phase 1: stage-1 B
+//   W  : w o x, then S_in (bf16)    phase 1: stage-1 x (scaled in place)
+constexpr uint32_t OFF_X = 0;
+constexpr uint32_t OFF_B = OFF_X + X_BYTES;        // 16384
+constexpr uint32_t OFF_C = OFF_B + BC_BYTES;       // 49152
+constexpr uint32_t OFF_W = OFF_C + BC_BYTES;       // 81920
+constexpr uint32_t OFF_DTU = OFF_W + X_BYTES;      // 98304
+constexpr uint32_t OFF_WU = OFF_DTU + RMAX * QT * 4;
+constexpr uint32_t OFF_CS2 = OFF_WU + RMAX * QT * 4;
+constexpr uint32_t OFF_DTC = OFF_CS2 + QT * 4;
+constexpr uint32_t OFF_MISC = OFF_DTC + QT * 4;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 256 + 1024;   // + alignment slack
 
-// TMEM columns
-constexpr uint32_t TM_CB = 0;     // [0,128) CB, then [0,64) Y_diag
-constexpr uint32_t TM_SC = 128;   // [128,192) chunk state^T
-constexpr uint32_t TM_YO = 192;   // [192,256) Y_off
-constexpr uint32_t TM_AGG = 256;  // [256,320) unit aggregate^T
-constexpr uint32_t TM_COLS = 512;
+// TMEM columns (256 per CTA)
+constexpr uint32_t TM_CB = 0;     // [0,128) CB, then [0,64) Y_diag (+ D x)
+constexpr uint32_t TM_SC = 128;   // [128,192) chunk state^T (phase 1: unit aggregate^T)
+constexpr uint32_t TM_YO = 192;   // [192,256) C S_in^T
+constexpr uint32_t TM_COLS = 256;
 
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -96,16 +99,18 @@ struct FusedParams {
     const SeqInfo *seqs;
 };
 
+// Barriers: x (phase-1 stage 0 / phase-2 x), b (phase-2 B), c (phase-1 stage 1 / phase-2 C),
+// mma (tensor-core completion).  Each counts its own completed phases.
+enum { BAR_X = 0, BAR_B = 1, BAR_C = 2, BAR_MMA = 3 };
+
 struct Misc {
-    uint64_t bar_tma[2];
-    uint64_t bar_mma;
+    uint64_t bar[4];
     uint32_t tmem_base;
     int ticket;
     int abort_;
-    float wsum[8];
+    float wsum[4];
 };
 
-// Inclusive scan of one value per thread over the block (8 warps; threads >= 128 pass 0).
 __device__ __forceinline__ float block_scan(float v, float *wsum, float *total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     float x = warp_incl_sum(v);
@@ -131,15 +136,14 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k) {
     return sdesc(base + (uint32_t)k * 2048u, 16384u, 1024u);
 }
 
-// dst row = src row * w, for 4 of the 8 16-byte chunks of one 128-byte row (the
-// scale is uniform along the row).  Chunk slots are visited XOR-ed with row % 8, so
-// eight consecutive rows touch eight different bank groups.
-__device__ __forceinline__ void scale_row_half(const uint8_t *src_row, uint8_t *dst_row, int row, int hf, float wl) {
+// dst row = src row * w (a full 128-byte row; the 16-byte chunks are visited in
+// swizzled order so eight consecutive rows hit eight different bank groups).
+__device__ __forceinline__ void scale_row(const uint8_t *src_row, uint8_t *dst_row, int row, float wl) {
     const uint4 *src = reinterpret_cast<const uint4 *>(src_row);
     uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-        const int q = (4 * hf + qq) ^ (row & 7);
+    for (int qq = 0; qq < 8; ++qq) {
+        const int q = qq ^ (row & 7);
         uint4 v = src[q];
         __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&v);
 #pragma unroll
@@ -151,39 +155,36 @@ __device__ __forceinline__ void scale_row_half(const uint8_t *src_row, uint8_t *
     }
 }
 
-// acc[i] += sc * src[i * NT] for the 32 state columns of this thread's half
-// (a [P][N] state: for each column p the warp reads one contiguous 128-byte line).
-__device__ __forceinline__ void fma_col32(float *acc, const float *src, float sc) {
-    float v[32];
+// acc[i] += sc * src[i * NT] for the 64 state columns p (a [P][N] state: for each
+// column p the warp reads one contiguous 128-byte line).
+__device__ __forceinline__ void fma_col64(float *acc, const float *src, float sc) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __ldcg(src + (int64_t)i * NT);
+    for (int h = 0; h < 2; ++h) {
+        float v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] += sc * v[i];
+        for (int i = 0; i < 32; ++i) v[i] = __ldcg(src + (int64_t)(32 * h + i) * NT);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[32 * h + i] += sc * v[i];
+    }
 }
 
-// Thread layout: 8 warps.  row = tid & 127 is the tile row / TMEM lane (warp w
-// reaches lanes 32 (w & 3) .. +31), hf = tid >> 7 picks a half of the 64-wide
-// columns (state columns p, output columns, x chunks).
-__global__ void __launch_bounds__(NTHR, 1)
+__global__ void __launch_bounds__(NTHR, 2)
 k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = tid & 127, hf = tid >> 7, quad = warp & 3;
+    const int row = tid;
     Misc *ms = reinterpret_cast<Misc *>(sm + OFF_MISC);
     float *dtu = reinterpret_cast<float *>(sm + OFF_DTU);
     float *wu = reinterpret_cast<float *>(sm + OFF_WU);
     float *cs2 = reinterpret_cast<float *>(sm + OFF_CS2);
     float *dtc = reinterpret_cast<float *>(sm + OFF_DTC);
-    uint8_t *Wx = sm + OFF_WX;
-    uint8_t *Ss = sm + OFF_SS;
+    uint8_t *Xs = sm + OFF_X, *Bs = sm + OFF_B, *Cs = sm + OFF_C, *Ws = sm + OFF_W;
     const Shape sh = p.sh;
 
     if (tid == 0) {
-        mbar_init(&ms->bar_tma[0], 1);
-        mbar_init(&ms->bar_tma[1], 1);
-        mbar_init(&ms->bar_mma, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&ms->bar[i], 1);
         fence_mbar_init();
         ms->abort_ = 0;
         prefetch_tmap(&tmX);
@@ -195,52 +196,60 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
-    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t col_half = (uint32_t)(32 * hf);
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 
-    uint32_t load_seq = 0;   // sequence number of the next chunk load (stage = seq & 1)
-    uint32_t mma_seq = 0;    // MMA commits waited for
-    // Issue/wait counters kept identically by every thread (issue decisions are
-    // uniform): what is still in flight when the kernel stops early gets drained.
-    uint32_t ld_issued = 0, ld_waited = 0, mma_issued = 0;
+    // Completed-phase counters, kept identically by every thread (all issue
+    // decisions are uniform), and the count of issued-but-unwaited operations per
+    // barrier for the drain after an early stop.
+    uint32_t done[4] = {0, 0, 0, 0};
+    uint32_t issued[4] = {0, 0, 0, 0};
     const int total = (p.hdr[HDR_STATUS] != 0) ? 0 : p.hdr[HDR_NUNITS] * sh.H;
 
-    auto stage_ptr = [&](uint32_t seq) { return sm + ((seq & 1) ? OFF_STAGE1 : OFF_STAGE0); };
-    // one thread: issue the loads of chunk (row b, first token t) into stage seq&1
-    auto issue_load = [&](uint32_t seq, int h, int g, int t, int b, bool withC) {
-        uint8_t *st = stage_ptr(seq);
-        uint64_t *bar = &ms->bar_tma[seq & 1];
-        mbar_expect_tx(bar, X_BYTES + BC_BYTES + (withC ? BC_BYTES : 0));
-        tma_load_4d(st, &tmX, bar, 0, h, t, b);
-        tma_load_4d(st + X_BYTES, &tmB, bar, 0, g, t, b);
-        tma_load_4d(st + X_BYTES + BC_BYTES / 2, &tmB, bar, 64, g, t, b);
-        if (withC) {
-            tma_load_4d(st + X_BYTES + BC_BYTES, &tmC, bar, 0, g, t, b);
-            tma_load_4d(st + X_BYTES + BC_BYTES + BC_BYTES / 2, &tmC, bar, 64, g, t, b);
-        }
+    auto fail = [&]() {
+        ms->abort_ = 1;
+        set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
     };
-    // all threads: wait for load `seq`
-    auto wait_load = [&](uint32_t seq) {
-        if (!mbar_wait(&ms->bar_tma[seq & 1], (seq >> 1) & 1)) {
-            ms->abort_ = 1;
-            set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
-        }
-        ++ld_waited;
+    auto wait_bar = [&](int b) {
+        if (!mbar_wait(&ms->bar[b], done[b] & 1)) fail();
+        ++done[b];
+        if (b == BAR_MMA) tc_fence_after();
     };
-    auto wait_mma = [&]() {
-        if (!mbar_wait(&ms->bar_mma, mma_seq & 1)) {
-            ms->abort_ = 1;
-            set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+    // TMA issue helpers (one thread issues; every thread counts)
+    auto load_xb = [&](int b_, uint8_t *xd, uint8_t *bd, int h, int g, int t, int bb) {
+        if (tid == 0) {
+            uint64_t *bar = &ms->bar[b_];
+            mbar_expect_tx(bar, X_BYTES + BC_BYTES);
+            tma_load_4d(xd, &tmX, bar, 0, h, t, bb);
+            tma_load_4d(bd, &tmB, bar, 0, g, t, bb);
+            tma_load_4d(bd + BC_BYTES / 2, &tmB, bar, 64, g, t, bb);
         }
-        ++mma_seq;
-        tc_fence_after();
+        ++issued[b_];
+    };
+    auto load_x = [&](int h, int t, int bb) {
+        if (tid == 0) {
+            mbar_expect_tx(&ms->bar[BAR_X], X_BYTES);
+            tma_load_4d(Xs, &tmX, &ms->bar[BAR_X], 0, h, t, bb);
+        }
+        ++issued[BAR_X];
+    };
+    auto load_bc = [&](int b_, const CUtensorMap *map, uint8_t *dst, int g, int t, int bb) {
+        if (tid == 0) {
+            mbar_expect_tx(&ms->bar[b_], BC_BYTES);
+            tma_load_4d(dst, map, &ms->bar[b_], 0, g, t, bb);
+            tma_load_4d(dst + BC_BYTES / 2, map, &ms->bar[b_], 64, g, t, bb);
+        }
+        ++issued[b_];
+    };
+    auto commit = [&]() {
+        if (tid == 0) umma_commit(&ms->bar[BAR_MMA]);
+        ++issued[BAR_MMA];
     };
 
     const uint32_t idesc_cb = idesc_bf16(128, 128, 0, 0);
     const uint32_t idesc_sc = idesc_bf16(128, 64, 1, 1);
     const uint32_t idesc_yo = idesc_bf16(128, 64, 0, 0);
     const uint32_t idesc_yd = idesc_bf16(128, 64, 0, 1);
-    const uint32_t sWx = smem_u32(Wx), sSs = smem_u32(Ss);
+    const uint32_t sX = smem_u32(Xs), sB = smem_u32(Bs), sC = smem_u32(Cs), sW = smem_u32(Ws);
     const int64_t unit_stride = (int64_t)NT * PT;   // floats per (unit, head) aggregate
 
     for (;;) {
@@ -253,10 +262,9 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         const float Ah = p.A[h];
         const int ntok = ui.nchunk * QT;
 
-        // first phase-1 load goes out before anything else
-        const uint32_t seq0 = load_seq;
-        if (tid == 0) issue_load(seq0, h, g, ui.t0, ui.b, false);
-        ++ld_issued;
+        // phase-1 loads of the first two chunks go out first: stage 0 = (X, B), stage 1 = (W, C)
+        load_xb(BAR_X, Xs, Bs, h, g, ui.t0, ui.b);
+        if (ui.nchunk > 1) load_xb(BAR_C, Ws, Cs, h, g, ui.t0 + QT, ui.b);
 
         // ---- dt over the unit, unit-level cumulative log-decay, phase-1 weights
         for (int i = tid; i < ntok; i += NTHR) {
@@ -271,49 +279,52 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         float carry = 0.f;
         for (int c = 0; c < ui.nchunk; ++c) {
             float tot;
-            float v = block_scan(tid < QT ? dtu[c * QT + tid] * Ah : 0.f, ms->wsum, &tot);
-            if (tid < QT) wu[c * QT + tid] = carry + v;
+            const float v = block_scan(dtu[c * QT + tid] * Ah, ms->wsum, &tot);
+            wu[c * QT + tid] = carry + v;
             carry += tot;
         }
         const float lam_u = carry;
-        __syncthreads();
         for (int i = tid; i < ntok; i += NTHR) wu[i] = dtu[i] * ex2((lam_u - wu[i]) * LOG2E);
         __syncthreads();
 
-        // ---- phase 1: unit aggregate on the tensor cores
+        // ---- phase 1: unit aggregate^T[n][p] = sum_l B[l][n] (w o x)[l][p], double-buffered
         for (int c = 0; c < ui.nchunk; ++c) {
-            const uint32_t seq = seq0 + c;
-            if (c > 0) wait_mma();   // MMA(c-1) done: Wx and stage (c+1)&1 free
-            if (c + 1 < ui.nchunk) {
-                if (tid == 0) issue_load(seq + 1, h, g, ui.t0 + (c + 1) * QT, ui.b, false);
-                ++ld_issued;
-            }
-            wait_load(seq);
-            scale_row_half(stage_ptr(seq) + row * 128, Wx + row * 128, row, hf, wu[c * QT + row]);
+            const int st = c & 1;
+            uint8_t *xs = st ? Ws : Xs;
+            wait_bar(st ? BAR_C : BAR_X);
+            scale_row(xs + row * 128, xs + row * 128, row, wu[c * QT + row]);   // x -> w o x in place
             fence_proxy_async_smem();
             __syncthreads();
             if (ms->abort_) break;
             if (tid == 0) {
                 tc_fence_after();
-                const uint32_t sB = smem_u32(stage_ptr(seq) + X_BYTES);
+                const uint32_t sb_ = smem_u32(st ? Cs : Bs), sx_ = smem_u32(xs);
 #pragma unroll
                 for (int k = 0; k < QT / 16; ++k)
-                    umma_bf16(tmem + TM_AGG, mnmaj(sB, k), mnmaj(sWx, k), idesc_sc, (c > 0 || k > 0) ? 1u : 0u);
-                umma_commit(&ms->bar_mma);
+                    umma_bf16(tmem + TM_SC, mnmaj(sb_, k), mnmaj(sx_, k), idesc_sc, (c > 0 || k > 0) ? 1u : 0u);
             }
-            ++mma_issued;
+            commit();
+            wait_bar(BAR_MMA);   // stage st free again
+            if (c + 2 < ui.nchunk)
+                load_xb(st ? BAR_C : BAR_X, xs, st ? Cs : Bs, h, g, ui.t0 + (c + 2) * QT, ui.b);
         }
-        load_seq = seq0 + ui.nchunk;
         if (ms->abort_) break;
-        wait_mma();
-        float a_reg[32];
-        tmem_ld32(tmem + lane_base + TM_AGG + col_half, a_reg);
-        tmem_wait_ld();
+        float s_run[64];   // row n = tid: aggregate, then carried state, columns p
+        {
+            float t32[32];
+            tmem_ld32(tmem + lane_base + TM_SC, t32);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s_run[i] = t32[i];
+            tmem_ld32(tmem + lane_base + TM_SC + 32, t32);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s_run[32 + i] = t32[i];
+            tmem_wait_ld();
+        }
         const int64_t my = (int64_t)u * sh.H + h;
         {   // aggregate^T row n -> agg[p][n]
-            float *dst = p.agg + my * unit_stride + (int64_t)col_half * NT + row;
+            float *dst = p.agg + my * unit_stride + row;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) __stcg(dst + (int64_t)i * NT, a_reg[i]);
+            for (int i = 0; i < 64; ++i) __stcg(dst + (int64_t)i * NT, s_run[i]);
             if (tid == 0) __stcg(p.lam + my, lam_u);
         }
         __threadfence();
@@ -321,16 +332,18 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         __syncthreads();
         if (tid == 0) st_release_u32(p.flags + my, 1u);
 
-        // prefetch phase-2 chunk 0 while folding the carry-in
-        if (tid == 0) issue_load(load_seq, h, g, ui.t0, ui.b, true);
-        ++ld_issued;
+        const bool full = p.states_out == nullptr;
+        // prefetch phase-2 chunk 0 while folding the carry-in (all phase-1 MMAs are done)
+        load_x(h, ui.t0, ui.b);
+        load_bc(BAR_B, &tmB, Bs, g, ui.t0, ui.b);
+        if (full) load_bc(BAR_C, &tmC, Cs, g, ui.t0, ui.b);
 
-        // ---- carry-in state of the unit (row n, columns p of this thread's half)
+        // ---- carry-in state of the unit (row n, all 64 columns p)
         // P_j = sum_{i=b0}^{j-1} exp(lam_{i+1} + .. + lam_{j-1}) agg_i + exp(lam_{b0} + .. + lam_{j-1}) E,
         // E = end state of unit b0-1 (published by it) or the initial state when b0 = 0.
-        float s_run[32];
+        float agg_keep[64];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s_run[i] = 0.f;
+        for (int i = 0; i < 64; ++i) { agg_keep[i] = s_run[i]; s_run[i] = 0.f; }
         const int b0 = ui.j - (ui.j % KB);
         const int nfold = ui.j - b0;     // in-block predecessors: units u-1 .. u-nfold
         const int uprev_blk = (b0 > 0) ? (nfold > 0 ? p.units[u - nfold].prev : ui.prev) : -1;
@@ -348,10 +361,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                         __nanosleep(64);
                     }
                 }
-                if (fl < (uint32_t)need) {
-                    ms->abort_ = 1;
-                    set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
-                }
+                if (fl < (uint32_t)need) fail();
             }
             __threadfence();
             __syncthreads();
@@ -361,23 +371,23 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         for (int i = 1; i <= nfold; ++i) {   // units u-1, u-2, .. in that order
             const int64_t pi = (int64_t)(u - i) * sh.H + h;
             const float lam_i = __ldcg(p.lam + pi);
-            fma_col32(s_run, p.agg + pi * unit_stride + (int64_t)col_half * NT + row, ex2(logm * LOG2E));
+            fma_col64(s_run, p.agg + pi * unit_stride + row, ex2(logm * LOG2E));
             logm += lam_i;
         }
         if (uprev_blk >= 0) {
             const int64_t pi = (int64_t)uprev_blk * sh.H + h;
-            fma_col32(s_run, p.incl + pi * unit_stride + (int64_t)col_half * NT + row, ex2(logm * LOG2E));
+            fma_col64(s_run, p.incl + pi * unit_stride + row, ex2(logm * LOG2E));
         } else if (p.init) {
             const float sc = ex2(logm * LOG2E);
-            const float *src = p.init + ((int64_t)ui.seq * sh.H + h) * PT * NT + (int64_t)col_half * NT + row;
+            const float *src = p.init + ((int64_t)ui.seq * sh.H + h) * PT * NT + row;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) s_run[i] += sc * src[(int64_t)i * NT];
+            for (int i = 0; i < 64; ++i) s_run[i] += sc * src[(int64_t)i * NT];
         }
         if ((ui.j % KB) == KB - 1 && !ui.last) {   // block end: publish the unit's end state
             const float dec = ex2(lam_u * LOG2E);
-            float *dst = p.incl + my * unit_stride + (int64_t)col_half * NT + row;
+            float *dst = p.incl + my * unit_stride + row;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) __stcg(dst + (int64_t)i * NT, a_reg[i] + dec * s_run[i]);
+            for (int i = 0; i < 64; ++i) __stcg(dst + (int64_t)i * NT, agg_keep[i] + dec * s_run[i]);
             __threadfence();
             __syncthreads();
             if (tid == 0) st_release_u32(p.flags + my, 2u);
@@ -385,59 +395,42 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 
         // ---- phase 2: outputs (or, in states-only mode, the carried state of every chunk)
         const float Dh = p.D ? p.D[h] : 0.f;
-        const bool full = p.states_out == nullptr;
         const int64_t kfirst = full ? 0 : (int64_t)p.seqs[ui.seq].chunk0 + (int64_t)ui.j * sh.R;
         for (int c = 0; c < ui.nchunk; ++c) {
-            const uint32_t seq = load_seq + c;
             const int tc0 = ui.t0 + c * QT;
             const int clen = min(QT, ui.len - c * QT);
-            if (c + 1 < ui.nchunk) {
-                if (tid == 0) issue_load(seq + 1, h, g, tc0 + QT, ui.b, true);
-                ++ld_issued;
-            }
-            // gate values of this thread's output row/half, fetched early
+            const bool more = c + 1 < ui.nchunk;
+            // gate values of this thread's output row, fetched early
             const int64_t tok = (int64_t)tc0 + row;
-            uint4 zv[4];
+            uint4 zv[8];
             const bool has_z = full && p.z != nullptr && row < clen;
             if (has_z) {
                 const uint4 *zp = reinterpret_cast<const uint4 *>(p.z + (int64_t)ui.b * p.szb + tok * p.szl +
-                                                                  (int64_t)h * p.szh + col_half);
+                                                                  (int64_t)h * p.szh);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) zv[q] = __ldcs(zp + q);
+                for (int q = 0; q < 8; ++q) zv[q] = __ldcs(zp + q);
             }
             // chunk-local cumulative log-decay
-            const float dtl = (tid < QT) ? dtu[c * QT + tid] : 0.f;
+            const float dtl = dtu[c * QT + tid];
             float ctot;
             const float csl = block_scan(dtl * Ah, ms->wsum, &ctot);
-            if (tid < QT) {
-                cs2[tid] = csl * LOG2E;
-                dtc[tid] = dtl;
-            }
+            cs2[tid] = csl * LOG2E;
+            dtc[tid] = dtl;
             const float a_c = ex2(ctot * LOG2E);
-            if (!full) {   // states-only: S_in[chunk] -> global bf16 [p][n] (row n, this half's p)
-                __nv_bfloat16 *dst = p.states_out + ((kfirst + c) * sh.H + h) * (int64_t)(PT * NT) +
-                                     (int64_t)col_half * NT + row;
+            if (!full) {   // states-only: S_in[chunk] -> global bf16 [p][n] (row n)
+                __nv_bfloat16 *dst = p.states_out + ((kfirst + c) * sh.H + h) * (int64_t)(PT * NT) + row;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(s_run[i]);
-            } else {   // carried state S_in (bf16, K-major [p][n]) for Y_off
-                const int n = row, ac = n >> 6, cn = (n & 63) >> 3;
-                uint8_t *base = Ss + ac * (S_BYTES / 2) + (n & 7) * 2;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int pp = (int)col_half + i;
-                    *reinterpret_cast<__nv_bfloat16 *>(base + pp * 128 + ((cn ^ (pp & 7)) << 4)) =
-                        __float2bfloat16_rn(s_run[i]);
-                }
+                for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(s_run[i]);
             }
-            wait_load(seq);
-            __syncthreads();   // cs2/dtc visible
-            const uint8_t *st = stage_ptr(seq);
-            // Wx = w o x, w[l] = dt[l] exp(cs[Q-1] - cs[l])
-            scale_row_half(st + row * 128, Wx + row * 128, row, hf, dtc[row] * ex2(cs2[QT - 1] - cs2[row]));
+            wait_bar(BAR_X);
+            wait_bar(BAR_B);
+            if (full) wait_bar(BAR_C);
+            __syncthreads();   // cs2 / dtc visible; tiles landed
+            // W = w o x, w[l] = dt[l] exp(cs[Q-1] - cs[l])
+            scale_row(Xs + row * 128, Ws + row * 128, row, dtc[row] * ex2(cs2[QT - 1] - cs2[row]));
             fence_proxy_async_smem();
             __syncthreads();
             if (ms->abort_) break;
-            const uint32_t sX = smem_u32(st), sB = sX + X_BYTES, sC = sB + BC_BYTES;
             if (tid == 0) {
                 tc_fence_after();
                 if (full) {
@@ -447,28 +440,36 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 }
 #pragma unroll
                 for (int k = 0; k < QT / 16; ++k)   // S_c^T = B^T (w o x) (K = tokens)
-                    umma_bf16(tmem + TM_SC, mnmaj(sB, k), mnmaj(sWx, k), idesc_sc, k > 0);
-                if (full) {
+                    umma_bf16(tmem + TM_SC, mnmaj(sB, k), mnmaj(sW, k), idesc_sc, k > 0);
+            }
+            commit();
+            wait_bar(BAR_MMA);
+            if (full) {
+                // S_in (bf16, K-major [p][n]) over the w o x buffer, then Y_off = C S_in^T
+                {
+                    const int n = row, ac = n >> 6, cn = (n & 63) >> 3;
+                    uint8_t *base = Ws + ac * (S_BYTES / 2) + (n & 7) * 2;
+#pragma unroll
+                    for (int pp = 0; pp < 64; ++pp)
+                        *reinterpret_cast<__nv_bfloat16 *>(base + pp * 128 + ((cn ^ (pp & 7)) << 4)) =
+                            __float2bfloat16_rn(s_run[pp]);
+                }
+                fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < NT / 16; ++k)   // Y_off = C S_in^T (K = state dim)
-                        umma_bf16(tmem + TM_YO, kmaj(sC, k, BC_BYTES / 2), kmaj(sSs, k, S_BYTES / 2), idesc_yo,
-                                  k > 0);
+                        umma_bf16(tmem + TM_YO, kmaj(sC, k, BC_BYTES / 2), kmaj(sW, k, S_BYTES / 2), idesc_yo, k > 0);
                 }
-                umma_commit(&ms->bar_mma);
-            }
-            ++mma_issued;
-            wait_mma();
-            // M (bf16, K-major [l][s]) into the B buffer, which the MMAs above are done with.
-            // Half 0 builds s-blocks {0, 3}, half 1 {1, 2}; blocks above the diagonal are zero.
-            {
-                uint8_t *Ms = const_cast<uint8_t *>(st) + X_BYTES;
+                commit();
+                // M (bf16, K-major [l][s], D on the diagonal) into the B buffer while Y_off runs
                 const int l = row;
                 const float cl = cs2[l];
 #pragma unroll
-                for (int bi = 0; bi < 2; ++bi) {
-                    const int sb = hf == 0 ? (bi == 0 ? 0 : 3) : (bi == 0 ? 1 : 2);
+                for (int sb = 0; sb < 4; ++sb) {
                     uint32_t pk[16];
-                    if (full && sb <= quad) {
+                    if (sb <= warp) {
                         float cb[32];
                         tmem_ld32(tmem + lane_base + TM_CB + sb * 32, cb);
                         tmem_wait_ld();
@@ -477,13 +478,15 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                             const int s0 = sb * 32 + i;
                             float m0 = (s0 <= l) ? cb[i] * ex2(cl - cs2[s0]) * dtc[s0] : 0.f;
                             float m1 = (s0 + 1 <= l) ? cb[i + 1] * ex2(cl - cs2[s0 + 1]) * dtc[s0 + 1] : 0.f;
+                            if (s0 == l) m0 += Dh;
+                            if (s0 + 1 == l) m1 += Dh;
                             pk[i >> 1] = pack_bf16(m0, m1);
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) pk[i] = 0u;
                     }
-                    uint8_t *rowp = Ms + (sb >> 1) * (BC_BYTES / 2) + l * 128;
+                    uint8_t *rowp = Bs + (sb >> 1) * (BC_BYTES / 2) + l * 128;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int cidx = ((sb & 1) << 2) + q;
@@ -491,75 +494,90 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                             make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                     }
                 }
-                // carried state update: S_in[c+1] = a_c S_in[c] + S_c (row n, this half's columns)
+            }
+            {   // carried state update: S_in[c+1] = a_c S_in[c] + S_c (row n)
                 float sc[32];
-                tmem_ld32(tmem + lane_base + TM_SC + col_half, sc);
+                tmem_ld32(tmem + lane_base + TM_SC, sc);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s_run[i] = a_c * s_run[i] + sc[i];
+                tmem_ld32(tmem + lane_base + TM_SC + 32, sc);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s_run[32 + i] = a_c * s_run[32 + i] + sc[i];
             }
+            if (!full) {
+                tc_fence_before();
+                __syncthreads();   // x, B, W free: next chunk's loads
+                if (more) {
+                    load_x(h, tc0 + QT, ui.b);
+                    load_bc(BAR_B, &tmB, Bs, g, tc0 + QT, ui.b);
+                }
+                continue;
+            }
+            wait_bar(BAR_MMA);   // Y_off done: C free
+            if (more) load_bc(BAR_C, &tmC, Cs, g, tc0 + QT, ui.b);
             fence_proxy_async_smem();
             tc_fence_before();
-            __syncthreads();
-            if (!full) continue;   // states-only: no outputs (uniform across the CTA)
+            __syncthreads();   // M visible
             if (tid == 0) {
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < QT / 16; ++k)   // Y_diag = M x (K = source tokens)
+                for (int k = 0; k < QT / 16; ++k)   // Y_diag + D x = M x (K = source tokens)
                     umma_bf16(tmem + TM_CB, kmaj(sB, k, BC_BYTES / 2), mnmaj(sX, k), idesc_yd, k > 0);
-                umma_commit(&ms->bar_mma);
             }
-            ++mma_issued;
-            wait_mma();
-            {   // epilogue: row l, this thread's half of the 64 output columns
+            commit();
+            wait_bar(BAR_MMA);   // x, B free: next chunk's loads
+            if (more) {
+                load_x(h, tc0 + QT, ui.b);
+                load_bc(BAR_B, &tmB, Bs, g, tc0 + QT, ui.b);
+            }
+            {   // epilogue: row l
                 const int l = row;
-                float yd[32], yo[32];
-                tmem_ld32(tmem + lane_base + TM_CB + col_half, yd);
-                tmem_ld32(tmem + lane_base + TM_YO + col_half, yo);
-                tmem_wait_ld();
-                if (l < clen) {
-                    const float el = ex2(cs2[l]);
-                    const uint8_t *xrow = st + l * 128;
-                    __nv_bfloat16 *yrow = p.y + (int64_t)ui.b * p.syb + tok * p.syl + (int64_t)h * p.syh + col_half;
+                const float el = ex2(cs2[l]);
+                __nv_bfloat16 *yrow = p.y + (int64_t)ui.b * p.syb + tok * p.syl + (int64_t)h * p.syh;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int cidx = hf * 4 + q;
-                        uint4 xv = *reinterpret_cast<const uint4 *>(xrow + ((cidx ^ (l & 7)) << 4));
-                        const __nv_bfloat162 *xe = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-                        const __nv_bfloat162 *ze = reinterpret_cast<const __nv_bfloat162 *>(&zv[q]);
-                        uint32_t o[4];
+                for (int half = 0; half < 2; ++half) {
+                    float yd[32], yo[32];
+                    tmem_ld32(tmem + lane_base + TM_CB + 32 * half, yd);
+                    tmem_ld32(tmem + lane_base + TM_YO + 32 * half, yo);
+                    tmem_wait_ld();
+                    if (l < clen) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 xf = __bfloat1622float2(xe[i]);
-                            const int j = q * 8 + 2 * i;
-                            float v0 = yd[j] + el * yo[j] + Dh * xf.x;
-                            float v1 = yd[j + 1] + el * yo[j + 1] + Dh * xf.y;
-                            if (has_z) {
-                                const float2 zf = __bfloat1622float2(ze[i]);
-                                v0 *= zf.x * rcp(1.f + ex2(-zf.x * LOG2E));
-                                v1 *= zf.y * rcp(1.f + ex2(-zf.y * LOG2E));
+                        for (int q = 0; q < 4; ++q) {
+                            const __nv_bfloat162 *ze = reinterpret_cast<const __nv_bfloat162 *>(&zv[half * 4 + q]);
+                            uint32_t o[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int j = q * 8 + 2 * i;
+                                float v0 = yd[j] + el * yo[j];
+                                float v1 = yd[j + 1] + el * yo[j + 1];
+                                if (has_z) {
+                                    const float2 zf = __bfloat1622float2(ze[i]);
+                                    v0 *= zf.x * rcp(1.f + ex2(-zf.x * LOG2E));
+                                    v1 *= zf.y * rcp(1.f + ex2(-zf.y * LOG2E));
+                                }
+                                o[i] = pack_bf16(v0, v1);
                             }
-                            o[i] = pack_bf16(v0, v1);
+                            *reinterpret_cast<uint4 *>(yrow + half * 32 + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
                         }
-                        *reinterpret_cast<uint4 *>(yrow + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
             }
             tc_fence_before();
             __syncthreads();
         }
-        load_seq += ui.nchunk;
         if (ms->abort_) break;
         if (ui.last && p.final_ && full) {
-            float *dst = p.final_ + ((int64_t)ui.seq * sh.H + h) * PT * NT + (int64_t)col_half * NT + row;
+            float *dst = p.final_ + ((int64_t)ui.seq * sh.H + h) * PT * NT + row;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = s_run[i];
+            for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = s_run[i];
         }
     }
     // Drain (only non-empty after an early stop): bounded waits for loads and
     // MMAs still in flight, so nothing lands in shared memory or TMEM after exit.
-    for (uint32_t q = ld_waited; q < ld_issued; ++q) mbar_wait(&ms->bar_tma[q & 1], (q >> 1) & 1);
-    if (mma_issued > mma_seq) mbar_wait(&ms->bar_mma, (mma_issued - 1) & 1);
+    for (int b_ = 0; b_ < 4; ++b_)
+        for (uint32_t q = done[b_]; q < issued[b_]; ++q) mbar_wait(&ms->bar[b_], q & 1);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
