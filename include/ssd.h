@@ -187,7 +187,7 @@ int32_t ssd_abi_version(void);
  *   units       : int32[n_units][8] (fused path) {seq, batch row, first token, token count,
  *                 chunk count, index of the sequence's previous unit or -1, 1 if last unit
  *                 of its sequence, segment index j}; segment j of a sequence is its chunks
- *                 [j*R, (j+1)*R); segments are grouped in blocks of 8 and units are listed
+ *                 [j*R, (j+1)*R); segments are grouped in blocks of 4 and units are listed
  *                 by (block, sequence, segment)
  * where qi is the internal chunk length written to *qi.  Chunks are listed
  * sequence by sequence, in order, each sequence cut into qi-token chunks from its

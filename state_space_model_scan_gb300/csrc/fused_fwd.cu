@@ -45,7 +45,7 @@ constexpr int QT = 128;   // chunk length
 constexpr int PT = 64;    // head dim
 constexpr int NT = 128;   // state dim
 constexpr int RMAX = 4;   // max chunks per unit
-constexpr int KB = 8;     // segments per block of the carry-in fold
+constexpr int KB = 4;     // segments per block of the carry-in fold
 constexpr int NTHR = 128; // one thread per tile row / TMEM lane
 
 constexpr uint32_t X_BYTES = QT * PT * 2;    // 16 KB
@@ -57,16 +57,16 @@ constexpr uint32_t S_BYTES = PT * NT * 2;    // 16 KB
 //   X  : x tile                     phase 1: stage-0 x (scaled in place to w o x)
 //   B  : B tile, then M             phase 1: stage-0 B
 //   C  : C tile                     phase 1: stage-1 B
-//   W  : w o x, then S_in (bf16)    phase 1: stage-1 x (scaled in place)
+//   W  : w o x, then S_in (bf16), then z (TMA)     phase 1: stage-1 x (scaled in place)
 constexpr uint32_t OFF_X = 0;
 constexpr uint32_t OFF_B = OFF_X + X_BYTES;        // 16384
 constexpr uint32_t OFF_C = OFF_B + BC_BYTES;       // 49152
 constexpr uint32_t OFF_W = OFF_C + BC_BYTES;       // 81920
 constexpr uint32_t OFF_DTU = OFF_W + X_BYTES;      // 98304
 constexpr uint32_t OFF_WU = OFF_DTU + RMAX * QT * 4;
-constexpr uint32_t OFF_CS2 = OFF_WU + RMAX * QT * 4;
-constexpr uint32_t OFF_DTC = OFF_CS2 + QT * 4;
-constexpr uint32_t OFF_MISC = OFF_DTC + QT * 4;
+constexpr uint32_t OFF_CS2 = OFF_WU + RMAX * QT * 4;    // chunk-local cumsum * log2 e, every chunk of the unit
+constexpr uint32_t OFF_CF = OFF_CS2 + RMAX * QT * 4;     // per-column decay factors of the M build, every chunk
+constexpr uint32_t OFF_MISC = OFF_CF + RMAX * QT * 4;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 256 + 1024;   // + alignment slack
 
 // TMEM columns (256 per CTA)
@@ -100,11 +100,11 @@ struct FusedParams {
 };
 
 // Barriers: x (phase-1 stage 0 / phase-2 x), b (phase-2 B), c (phase-1 stage 1 / phase-2 C),
-// mma (tensor-core completion).  Each counts its own completed phases.
-enum { BAR_X = 0, BAR_B = 1, BAR_C = 2, BAR_MMA = 3 };
+// mma (tensor-core completion), z (phase-2 gate tile).  Each counts its own completed phases.
+enum { BAR_X = 0, BAR_B = 1, BAR_C = 2, BAR_MMA = 3, BAR_Z = 4, NBAR = 5 };
 
 struct Misc {
-    uint64_t bar[4];
+    uint64_t bar[NBAR];
     uint32_t tmem_base;
     int ticket;
     int abort_;
@@ -125,6 +125,13 @@ __device__ __forceinline__ float block_scan(float v, float *wsum, float *total) 
     *total = tot;
     __syncthreads();
     return x + off;
+}
+
+// silu(z) = z sigmoid(z), sigmoid(z) = (1 + tanh(z/2)) / 2 (one tanh.approx).
+__device__ __forceinline__ float silu_tanh(float z) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+    return 0.5f * z * (1.f + t);
 }
 
 // K-major SW128 operand: rows of 64 bf16 (128 B), atom columns of `col_bytes`.
@@ -170,7 +177,7 @@ __device__ __forceinline__ void fma_col64(float *acc, const float *src, float sc
 
 __global__ void __launch_bounds__(NTHR, 2)
 k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
-            const __grid_constant__ CUtensorMap tmC, const FusedParams p) {
+            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmZ, const FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -178,18 +185,19 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     Misc *ms = reinterpret_cast<Misc *>(sm + OFF_MISC);
     float *dtu = reinterpret_cast<float *>(sm + OFF_DTU);
     float *wu = reinterpret_cast<float *>(sm + OFF_WU);
-    float *cs2 = reinterpret_cast<float *>(sm + OFF_CS2);
-    float *dtc = reinterpret_cast<float *>(sm + OFF_DTC);
+    float *cs2u = reinterpret_cast<float *>(sm + OFF_CS2);
+    float *cfu = reinterpret_cast<float *>(sm + OFF_CF);
     uint8_t *Xs = sm + OFF_X, *Bs = sm + OFF_B, *Cs = sm + OFF_C, *Ws = sm + OFF_W;
     const Shape sh = p.sh;
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&ms->bar[i], 1);
+        for (int i = 0; i < NBAR; ++i) mbar_init(&ms->bar[i], 1);
         fence_mbar_init();
         ms->abort_ = 0;
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmC);
+        if (p.z) prefetch_tmap(&tmZ);
     }
     if (warp == 0) tmem_alloc(&ms->tmem_base, TM_COLS);
     tc_fence_before();
@@ -201,8 +209,8 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     // Completed-phase counters, kept identically by every thread (all issue
     // decisions are uniform), and the count of issued-but-unwaited operations per
     // barrier for the drain after an early stop.
-    uint32_t done[4] = {0, 0, 0, 0};
-    uint32_t issued[4] = {0, 0, 0, 0};
+    uint32_t done[NBAR] = {0, 0, 0, 0, 0};
+    uint32_t issued[NBAR] = {0, 0, 0, 0, 0};
     const int total = (p.hdr[HDR_STATUS] != 0) ? 0 : p.hdr[HDR_NUNITS] * sh.H;
 
     auto fail = [&]() {
@@ -239,6 +247,13 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             tma_load_4d(dst + BC_BYTES / 2, map, &ms->bar[b_], 64, g, t, bb);
         }
         ++issued[b_];
+    };
+    auto load_z = [&](int h, int t, int bb) {
+        if (tid == 0) {
+            mbar_expect_tx(&ms->bar[BAR_Z], X_BYTES);
+            tma_load_4d(Ws, &tmZ, &ms->bar[BAR_Z], 0, h, t, bb);
+        }
+        ++issued[BAR_Z];
     };
     auto commit = [&]() {
         if (tid == 0) umma_commit(&ms->bar[BAR_MMA]);
@@ -281,11 +296,14 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             float tot;
             const float v = block_scan(dtu[c * QT + tid] * Ah, ms->wsum, &tot);
             wu[c * QT + tid] = carry + v;
+            cs2u[c * QT + tid] = v * LOG2E;   // chunk-local inclusive cumsum (phase 2)
             carry += tot;
         }
         const float lam_u = carry;
         for (int i = tid; i < ntok; i += NTHR) wu[i] = dtu[i] * ex2((lam_u - wu[i]) * LOG2E);
         __syncthreads();
+        // column factors of the M build: cf[s] = dt[s] exp(cs[end of s's 32-block] - cs[s]) <= dt[s]
+        for (int i = tid; i < ntok; i += NTHR) cfu[i] = dtu[i] * ex2(cs2u[i | 31] - cs2u[i]);
 
         // ---- phase 1: unit aggregate^T[n][p] = sum_l B[l][n] (w o x)[l][p], double-buffered
         for (int c = 0; c < ui.nchunk; ++c) {
@@ -400,23 +418,13 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             const int tc0 = ui.t0 + c * QT;
             const int clen = min(QT, ui.len - c * QT);
             const bool more = c + 1 < ui.nchunk;
-            // gate values of this thread's output row, fetched early
             const int64_t tok = (int64_t)tc0 + row;
-            uint4 zv[8];
-            const bool has_z = full && p.z != nullptr && row < clen;
-            if (has_z) {
-                const uint4 *zp = reinterpret_cast<const uint4 *>(p.z + (int64_t)ui.b * p.szb + tok * p.szl +
-                                                                  (int64_t)h * p.szh);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) zv[q] = __ldcs(zp + q);
-            }
-            // chunk-local cumulative log-decay
-            const float dtl = dtu[c * QT + tid];
-            float ctot;
-            const float csl = block_scan(dtl * Ah, ms->wsum, &ctot);
-            cs2[tid] = csl * LOG2E;
-            dtc[tid] = dtl;
-            const float a_c = ex2(ctot * LOG2E);
+            const bool has_z = full && p.z != nullptr;
+            // chunk-local cumulative log-decay (computed at unit start)
+            const float *cs2 = cs2u + c * QT;
+            const float *dtc = dtu + c * QT;
+            const float *cf = cfu + c * QT;
+            const float a_c = ex2(cs2[QT - 1]);
             if (!full) {   // states-only: S_in[chunk] -> global bf16 [p][n] (row n)
                 __nv_bfloat16 *dst = p.states_out + ((kfirst + c) * sh.H + h) * (int64_t)(PT * NT) + row;
 #pragma unroll
@@ -425,7 +433,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             wait_bar(BAR_X);
             wait_bar(BAR_B);
             if (full) wait_bar(BAR_C);
-            __syncthreads();   // cs2 / dtc visible; tiles landed
+            __syncthreads();   // tiles landed
             // W = w o x, w[l] = dt[l] exp(cs[Q-1] - cs[l])
             scale_row(Xs + row * 128, Ws + row * 128, row, dtc[row] * ex2(cs2[QT - 1] - cs2[row]));
             fence_proxy_async_smem();
@@ -469,7 +477,17 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                 for (int sb = 0; sb < 4; ++sb) {
                     uint32_t pk[16];
-                    if (sb <= warp) {
+                    if (sb < warp) {
+                        // strictly below the diagonal: exp(cs[l]-cs[s]) = exp(cs[l]-cs[e]) exp(cs[e]-cs[s]),
+                        // e = last token of the block; both factors <= 1, so neither overflows
+                        float cb[32];
+                        tmem_ld32(tmem + lane_base + TM_CB + sb * 32, cb);
+                        const float rl = ex2(cl - cs2[sb * 32 + 31]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            pk[i >> 1] = pack_bf16(cb[i] * rl * cf[sb * 32 + i], cb[i + 1] * rl * cf[sb * 32 + i + 1]);
+                    } else if (sb == warp) {   // diagonal block: causal mask, D on the diagonal
                         float cb[32];
                         tmem_ld32(tmem + lane_base + TM_CB + sb * 32, cb);
                         tmem_wait_ld();
@@ -515,7 +533,8 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 }
                 continue;
             }
-            wait_bar(BAR_MMA);   // Y_off done: C free
+            wait_bar(BAR_MMA);   // Y_off done: C and W free
+            if (has_z) load_z(h, tc0, ui.b);
             if (more) load_bc(BAR_C, &tmC, Cs, g, tc0 + QT, ui.b);
             fence_proxy_async_smem();
             tc_fence_before();
@@ -532,10 +551,12 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 load_x(h, tc0 + QT, ui.b);
                 load_bc(BAR_B, &tmB, Bs, g, tc0 + QT, ui.b);
             }
+            if (has_z) wait_bar(BAR_Z);
             {   // epilogue: row l
                 const int l = row;
                 const float el = ex2(cs2[l]);
                 __nv_bfloat16 *yrow = p.y + (int64_t)ui.b * p.syb + tok * p.syl + (int64_t)h * p.syh;
+                const uint8_t *zrow = Ws + l * 128;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float yd[32], yo[32];
@@ -545,7 +566,9 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     if (l < clen) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const __nv_bfloat162 *ze = reinterpret_cast<const __nv_bfloat162 *>(&zv[half * 4 + q]);
+                            uint4 zq = make_uint4(0u, 0u, 0u, 0u);
+                            if (has_z) zq = *reinterpret_cast<const uint4 *>(zrow + (((half * 4 + q) ^ (l & 7)) << 4));
+                            const __nv_bfloat162 *ze = reinterpret_cast<const __nv_bfloat162 *>(&zq);
                             uint32_t o[4];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
@@ -554,8 +577,8 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                                 float v1 = yd[j + 1] + el * yo[j + 1];
                                 if (has_z) {
                                     const float2 zf = __bfloat1622float2(ze[i]);
-                                    v0 *= zf.x * rcp(1.f + ex2(-zf.x * LOG2E));
-                                    v1 *= zf.y * rcp(1.f + ex2(-zf.y * LOG2E));
+                                    v0 *= silu_tanh(zf.x);
+                                    v1 *= silu_tanh(zf.y);
                                 }
                                 o[i] = pack_bf16(v0, v1);
                             }
@@ -576,7 +599,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     }
     // Drain (only non-empty after an early stop): bounded waits for loads and
     // MMAs still in flight, so nothing lands in shared memory or TMEM after exit.
-    for (int b_ = 0; b_ < 4; ++b_)
+    for (int b_ = 0; b_ < NBAR; ++b_)
         for (uint32_t q = done[b_]; q < issued[b_]; ++q) mbar_wait(&ms->bar[b_], q & 1);
     tc_fence_before();
     __syncthreads();
@@ -624,8 +647,13 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
                              const void *z, const int64_t *sz, void *y, const int64_t *sy, const float *init,
                              float *final_, float *agg, float *incl, float *lam, uint32_t *flags, int grid,
                              __nv_bfloat16 *states_out, const SeqInfo *seqs, cudaStream_t st) {
-    CUtensorMap mx, mb, mc;
+    CUtensorMap mx, mb, mc, mz;
     if (!make_map(&mx, x, PT, sh.H, sh.L, sh.B, sx[2], sx[1], sx[0])) return cudaErrorInvalidValue;
+    if (z != nullptr) {
+        if (!make_map(&mz, z, PT, sh.H, sh.L, sh.B, sz[2], sz[1], sz[0])) return cudaErrorInvalidValue;
+    } else {
+        mz = mx;
+    }
     if (!make_map(&mb, Bp, NT, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
     if (!make_map(&mc, Cp, NT, sh.G, sh.L, sh.B, sc[2], sc[1], sc[0])) return cudaErrorInvalidValue;
     FusedParams fp;
@@ -639,7 +667,7 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
     static int attr_done[64] = {0};
     cudaError_t e = ensure_smem_attr(k_fused_fwd, (int)SMEM_BYTES, attr_done);
     if (e != cudaSuccess) return e;
-    k_fused_fwd<<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, fp);
+    k_fused_fwd<<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, mz, fp);
     return cudaGetLastError();
 }
 

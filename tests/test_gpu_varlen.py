@@ -102,7 +102,7 @@ def test_fused_unit_metadata_bit_exact():
     lay = _lib.debug_layout(prob, args)
     raw = ws.cpu().numpy()
     counts = raw[lay.meta_counts:lay.meta_counts + 16].view(np.int32)
-    ref = meta.build(cu=inp["cu_seqlens"].tolist(), Q=128, R=2, KB=8)
+    ref = meta.build(cu=inp["cu_seqlens"].tolist(), Q=128, R=2, KB=4)
     assert lay.units >= 0 and counts[1] == len(ref["units"]) and counts[3] == 0
     got = raw[lay.units:lay.units + 32 * counts[1]].view(np.int32).reshape(-1, 8)
     assert np.array_equal(got, np.array(ref["units"], dtype=np.int32))
