@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 1
+#define SSD_ABI_VERSION 2
 
 typedef enum {
     SSD_OK = 0,
@@ -95,6 +95,9 @@ typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs;
     int32_t algo;        /* ssd_algo */
     int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..4 */
+    int32_t bwd_heads;   /* tensor-core backward: heads per CTA, 0 = library choice, else a divisor
+                            of nheads/ngroups no larger than 32 */
+    int32_t reserved0;   /* must be 0 */
 } ssd_problem;
 
 typedef struct {

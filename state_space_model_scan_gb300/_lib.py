@@ -40,7 +40,7 @@ class Problem(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
                 ("headdim", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("dstate", ctypes.c_int64),
                 ("chunk_size", ctypes.c_int64), ("nseqs", ctypes.c_int64), ("algo", ctypes.c_int32),
-                ("seg_chunks", ctypes.c_int32)]
+                ("seg_chunks", ctypes.c_int32), ("bwd_heads", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
 
 
 _FWD_FIELDS = ["x", "dt", "A", "B", "C", "D", "z", "dt_bias", "initial_states", "y", "final_states"]
@@ -110,8 +110,10 @@ def tensor(t, rank=None):
     return out
 
 
-def problem(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs=0, algo="auto", seg_chunks=0):
-    return Problem(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs, ALGO[algo], seg_chunks)
+def problem(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs=0, algo="auto", seg_chunks=0,
+            bwd_heads=0):
+    return Problem(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs, ALGO[algo], seg_chunks,
+                   bwd_heads, 0)
 
 
 def fwd_args(x, dt, A, B, C, y, D=None, z=None, dt_bias=None, initial_states=None, final_states=None,

@@ -53,9 +53,11 @@ def ssd_forward(x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_states=Non
 
 
 def ssd_backward(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, initial_states=None, dfinal_states=None,
-                 cu_seqlens=None, chunk_size=128, algo="auto", seg_chunks=0, workspace=None, stream=None):
+                 cu_seqlens=None, chunk_size=128, algo="auto", seg_chunks=0, bwd_heads=0, workspace=None,
+                 stream=None):
     """Gradients of sum(dy*y) + sum(dfinal_states*final_states).  Returns a dict with
-    dx, ddt, dA, dB, dC and, when the matching input is given, dD, dz, ddt_bias, dinitial_states."""
+    dx, ddt, dA, dB, dC and, when the matching input is given, dD, dz, ddt_bias, dinitial_states.
+    bwd_heads: heads per CTA of the tensor-core gradient kernel (0 = library choice)."""
     Bsz, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     S = _nseqs(x, cu_seqlens)
@@ -73,7 +75,8 @@ def ssd_backward(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, initial_state
         g["ddt_bias"] = torch.empty(H, dtype=torch.float32, device=dev)
     if initial_states is not None:
         g["dinitial_states"] = torch.empty(S, H, P, N, dtype=torch.float32, device=dev)
-    prob = _lib.problem(Bsz, L, H, P, G, N, chunk_size, S if cu_seqlens is not None else 0, algo, seg_chunks)
+    prob = _lib.problem(Bsz, L, H, P, G, N, chunk_size, S if cu_seqlens is not None else 0, algo, seg_chunks,
+                        bwd_heads)
     fa = _lib.fwd_args(x, dt, A, B, C, None, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
                        cu_seqlens=cu_seqlens)
     ba = _lib.bwd_args(fa, dy, g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], dD=g.get("dD"), dz=g.get("dz"),

@@ -36,8 +36,8 @@ cudaError_t launch_bwd_chunk(const Shape &sh, const int32_t *hdr, const ChunkInf
                              const float *states, const float *dstates, MView3 dx, MView3 dz, float *ddt,
                              int64_t sddb, int64_t sddl, float *dBh, float *dCh, float *partials, cudaStream_t st);
 template <typename T>
-cudaError_t launch_reduce_group(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const float *src,
-                                MView3 dst, cudaStream_t st);
+cudaError_t launch_reduce_group(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const float *srcB,
+                                MView3 dstB, const float *srcC, MView3 dstC, cudaStream_t st);
 cudaError_t launch_reduce_heads(const Shape &sh, const int32_t *hdr, const float *partials, float *dA, float *dD,
                                 float *dbias, cudaStream_t st);
 size_t bwd_chunk_smem(const Shape &sh);
@@ -82,11 +82,36 @@ struct Plan {
     bool bf16 = false;
     bool varlen = false;
     int algo = SSD_ALGO_STAGED;
+    int hs = 1;   // heads per CTA of the tensor-core gradient kernel
     size_t off_hdr = 0, off_seqs = 0, off_chunks = 0, off_lastunit = 0, off_units = 0;
     size_t off_dt = 0, off_cs = 0, off_states = 0, off_dstates = 0, off_dBh = 0, off_dCh = 0, off_part = 0;
     size_t off_agg = 0, off_incl = 0, off_lam = 0, off_flags = 0;
     size_t total = 0;
 };
+
+// Heads per CTA of the tensor-core gradient kernel: a divisor of H/G up to 32.  A
+// CTA (one per SM, by its shared memory) loads B and C of its chunk once for all its
+// heads and writes final dB/dC when it covers the whole group; otherwise a reduction
+// reads back fp32 shares of dB and dC for every head subset.  The choice minimises
+// the estimated time: whole waves of CTAs, each a head iteration of about 8 us per
+// head, plus that reduction's traffic at about 5 TB/s.
+int bwd_heads_per_cta(int64_t kmax, int64_t H, int hpg) {
+    const int64_t sms = num_sms();
+    int best = 1;
+    double best_us = 1e300;
+    for (int d = 1; d <= 32 && d <= hpg; ++d) {
+        if (hpg % d != 0) continue;
+        const int64_t ctas = kmax * (H / d);
+        const int64_t waves = (ctas + sms - 1) / sms;
+        double us = 8.0 * (double)(waves * d);
+        if (d < hpg) us += (double)ctas * 128.0 * 128.0 * 4.0 * 3.0 / 5.0e6;   // 2 reads + 1 write per subset tile
+        if (us <= best_us) {   // ties go to more heads per CTA
+            best_us = us;
+            best = d;
+        }
+    }
+    return best;
+}
 
 struct Layout {
     size_t cur = 0;
@@ -141,6 +166,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     if (!pow2_in(P, 16, 128) || !pow2_in(N, 16, 128)) return SSD_ERR_UNSUPPORTED;
     if (p->algo < SSD_ALGO_AUTO || p->algo > SSD_ALGO_FUSED) return SSD_ERR_INVALID_ARGUMENT;
     if (p->seg_chunks < 0 || p->seg_chunks > 8) return SSD_ERR_INVALID_ARGUMENT;
+    if (p->bwd_heads < 0 || p->bwd_heads > 32 || p->reserved0 != 0) return SSD_ERR_INVALID_ARGUMENT;
     const bool varlen = a->cu_seqlens != nullptr;
     int64_t S = B;
     if (varlen) {
@@ -173,12 +199,13 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     // Path choice.  The tensor-core forward covers bf16 inputs with headdim 64 and
     // dstate 128 whose x/B/C/z/y obey the 16-byte rule of TMA and vector access;
     // everything else (fp32 inputs in particular) runs the SIMT pipeline.  The
-    // backward always runs the staged pipeline.
+    // backward follows the same choice, with dy/dx/dz/dB/dC under the same rule.
     bool tc_ok = pl.bf16 && P == 64 && N == 128;
     bool aligned = true;
     {
-        const ssd_tensor *ts[8] = {&a->x, &a->B, &a->C, &a->z, bwd ? nullptr : &a->y, b ? &b->dy : nullptr,
-                                   b ? &b->dx : nullptr, b ? &b->dz : nullptr};
+        const ssd_tensor *ts[10] = {&a->x, &a->B, &a->C, &a->z, bwd ? nullptr : &a->y, b ? &b->dy : nullptr,
+                                    b ? &b->dx : nullptr, b ? &b->dz : nullptr, b ? &b->dB : nullptr,
+                                    b ? &b->dC : nullptr};
         for (const ssd_tensor *t : ts) {
             if (t == nullptr) continue;
             if (t->ptr == nullptr) continue;
@@ -229,11 +256,15 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         pl.off_lam = lay.take(sizeof(float) * uh);
         pl.off_flags = lay.take(sizeof(uint32_t) * uh);
         if (bwd) {
+            pl.hs = p->bwd_heads > 0 ? p->bwd_heads : bwd_heads_per_cta(kmax, H, sh.hpg);
+            if (sh.hpg % pl.hs != 0) return SSD_ERR_INVALID_ARGUMENT;
+            // dB/dC shares of head subsets, only when a CTA covers part of a group
+            const size_t ksub = pl.hs < sh.hpg ? (size_t)kmax * (size_t)(H / pl.hs) : 0;
             pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * N));   // carried states, bf16
             pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * N));
             pl.off_cs = lay.take(sizeof(float) * kh);                                // chunk total log-decay
-            pl.off_dBh = lay.take(sizeof(float) * kh * Q * (size_t)N);
-            pl.off_dCh = lay.take(sizeof(float) * kh * Q * (size_t)N);
+            pl.off_dBh = lay.take(sizeof(float) * ksub * Q * (size_t)N);
+            pl.off_dCh = lay.take(sizeof(float) * ksub * Q * (size_t)N);
             pl.off_part = lay.take(sizeof(float) * kh * 4);
         }
     } else {
@@ -454,13 +485,19 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         ta.dx = b->dx.ptr; ta.dz = b->dz.ptr; ta.sdx = b->dx.stride; ta.sdz = b->dz.ptr ? b->dz.stride : nullptr;
         ta.ddt = (float *)b->ddt.ptr; ta.sddb = b->ddt.stride[0]; ta.sddl = b->ddt.stride[1];
         ta.states = states; ta.dS = dS; ta.chunk_lam = clam; ta.dBh = dBh; ta.dCh = dCh; ta.partials = part;
+        ta.hs = pl.hs; ta.dB = b->dB.ptr; ta.dC = b->dC.ptr; ta.sdB = b->dB.stride; ta.sdC = b->dC.stride;
         if (sh.kmax > 0) SSD_CUDA(launch_bwd_dstates_tc(sh, hdr, chunks, ta, st));
         SSD_CUDA(launch_state_passing(sh, hdr, seqs, clam, 1, dS, (const float *)b->dfinal_states.ptr,
                                       (float *)b->dinitial_states.ptr, 1, st));
         if (sh.kmax > 0) {
             SSD_CUDA(launch_bwd_chunk_tc(sh, hdr, chunks, ta, st));
-            SSD_CUDA(launch_reduce_group<__nv_bfloat16>(sh, hdr, chunks, dBh, mview(b->dB), st));
-            SSD_CUDA(launch_reduce_group<__nv_bfloat16>(sh, hdr, chunks, dCh, mview(b->dC), st));
+            if (pl.hs < sh.hpg) {
+                // sum the head subsets' shares: the same reduction over H/hs "heads", hpg/hs per group
+                Shape ss = sh;
+                ss.H = sh.H / pl.hs;
+                ss.hpg = sh.hpg / pl.hs;
+                SSD_CUDA(launch_reduce_group<__nv_bfloat16>(ss, hdr, chunks, dBh, mview(b->dB), dCh, mview(b->dC), st));
+            }
         }
         SSD_CUDA(launch_reduce_heads(sh, hdr, part, (float *)b->dA.ptr, (float *)b->dD.ptr,
                                      (float *)b->ddt_bias.ptr, st));
@@ -489,16 +526,14 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
                 a->dt.stride[0], a->dt.stride[1], (const float *)a->A.ptr, (const float *)a->D.ptr,
                 (const float *)a->dt_bias.ptr, dtw, csw, states, dstates, mview(b->dx), mview(b->dz),
                 (float *)b->ddt.ptr, b->ddt.stride[0], b->ddt.stride[1], dBh, dCh, part, st));
-            SSD_CUDA(launch_reduce_group<__nv_bfloat16>(sh, hdr, chunks, dBh, mview(b->dB), st));
-            SSD_CUDA(launch_reduce_group<__nv_bfloat16>(sh, hdr, chunks, dCh, mview(b->dC), st));
+            SSD_CUDA(launch_reduce_group<__nv_bfloat16>(sh, hdr, chunks, dBh, mview(b->dB), dCh, mview(b->dC), st));
         } else {
             SSD_CUDA(launch_bwd_chunk<float>(
                 sh, hdr, chunks, view(a->x), view(a->B), view(a->C), view(a->z), view(b->dy), (const float *)a->dt.ptr,
                 a->dt.stride[0], a->dt.stride[1], (const float *)a->A.ptr, (const float *)a->D.ptr,
                 (const float *)a->dt_bias.ptr, dtw, csw, states, dstates, mview(b->dx), mview(b->dz),
                 (float *)b->ddt.ptr, b->ddt.stride[0], b->ddt.stride[1], dBh, dCh, part, st));
-            SSD_CUDA(launch_reduce_group<float>(sh, hdr, chunks, dBh, mview(b->dB), st));
-            SSD_CUDA(launch_reduce_group<float>(sh, hdr, chunks, dCh, mview(b->dC), st));
+            SSD_CUDA(launch_reduce_group<float>(sh, hdr, chunks, dBh, mview(b->dB), dCh, mview(b->dC), st));
         }
     }
     SSD_CUDA(launch_reduce_heads(sh, hdr, part, (float *)b->dA.ptr, (float *)b->dD.ptr, (float *)b->ddt_bias.ptr, st));

@@ -18,6 +18,8 @@
 // k_bwd_dstates computes the per-chunk state gradient source
 //     dS_loc[p][n] = sum_l e_l dyp[l][p] C[l][n]
 // which the reverse warp-shuffle scan turns into dS for every chunk.
+// The row sums of M o dM and the dt-weighted column sums of E CB dM cancel along the
+// suffix sums of dcs, so both come from the same fp32 products (never from bf16 tiles).
 // All contractions run as tcgen05.mma chains on 128-byte-swizzled shared-memory
 // tiles (TMA for x, B, C and the bf16 carried states); reductions are fixed-order.
 #include <cudaTypedefs.h>
@@ -52,8 +54,11 @@ struct BwdParams {
     const float *dS;         // [chunk][H][P][N] fp32: gradient of the state leaving the chunk
     float *dS_loc;           // [chunk][H][P][N] fp32 (dstates kernel output)
     float *chunk_lam;        // [chunk][H] total log-decay of the chunk (dstates kernel output)
-    float *dBh, *dCh;        // [chunk][H][Q][N] fp32 per-head shares
+    float *dBh, *dCh;        // [chunk][H/hs][Q][N] fp32 shares of head subsets (when hs < H/G)
     float *partials;         // [chunk][H][4]: dA, dD, ddt_bias shares
+    int hs;                  // heads per CTA of the gradient kernel
+    __nv_bfloat16 *dB, *dC;  // final outputs when hs == H/G
+    int64_t sdBb, sdBl, sdBg, sdCb, sdCl, sdCg;
 };
 
 __device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t col_bytes) {
@@ -134,6 +139,28 @@ __device__ __forceinline__ float block_scan256(float v, float *wsum, float *tota
         tot += wsum[i];
     }
     *total = tot;
+    __syncthreads();
+    return x + off;
+}
+
+// Inclusive block scan of v with the block total (*total), plus the block sum of u
+// (*usum), in one pass; fixed order.  wsum holds 16 floats.
+__device__ __forceinline__ float block_scan_sum(float v, float u, float *wsum, float *total, float *usum) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const float x = warp_incl_sum(v);
+    const float us = warp_sum(u);
+    if (lane == 31) wsum[w] = x;
+    if (lane == 0) wsum[8 + w] = us;
+    __syncthreads();
+    float off = 0.f, tot = 0.f, ut = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i < w) off += wsum[i];
+        tot += wsum[i];
+        ut += wsum[8 + i];
+    }
+    *total = tot;
+    *usum = ut;
     __syncthreads();
     return x + off;
 }
@@ -248,382 +275,527 @@ constexpr uint32_t O_B = O_X + X_BYTES;            // B      [s][n]   32 KB (TMA
 constexpr uint32_t O_C = O_B + BC_BYTES;           // C      [l][n]   32 KB (TMA)
 constexpr uint32_t O_SI = O_C + BC_BYTES;          // S_in   [p][n]   16 KB (TMA, bf16)
 constexpr uint32_t O_DY = O_SI + S_BYTES;          // dyp, then e o dyp [l][p] 16 KB
-constexpr uint32_t O_WX = O_DY + X_BYTES;          // w o x  [s][p]   16 KB
-constexpr uint32_t O_M = O_WX + X_BYTES;           // M      [l][s]   32 KB
-constexpr uint32_t O_E = O_M + BC_BYTES;           // E'     [l][s]   32 KB
-constexpr uint32_t O_SD = O_E + BC_BYTES;          // dS     [p][n]   16 KB (bf16)
+constexpr uint32_t O_M = O_DY + X_BYTES;           // M      [l][s]   32 KB
+constexpr uint32_t O_E = O_M + BC_BYTES;           // E'     [l][s]   32 KB; before: dy, z of the head (TMA)
+constexpr uint32_t O_WX = O_E + BC_BYTES;          // w o x  [s][p]   16 KB } before: dS of the head,
+constexpr uint32_t O_SD = O_WX + X_BYTES;          // dS     [p][n]   16 KB }   fp32 [p][n] (bulk copy)
 constexpr uint32_t O_MISC = O_SD + S_BYTES;
 // misc floats
 constexpr int F_CS2 = 0, F_DT = 128, F_W = 256, F_ROWT1 = 384, F_ROWXU = 640, F_ROWT2 = 896, F_ROWD = 1152,
-              F_COLP = 1408, F_RED = 1920, F_WSUM = 1936, F_END = 1952;
+              F_COLP = 1408, F_GD = 1920, F_RED = 2176, F_WSUM = 2192, F_PB = 2208, F_END = 2216;
+// F_GD: per position s, {exp(cs[a] - cs[s]), dt[s]} with a the last position of s's 32-block
 constexpr uint32_t BWD_SMEM = O_MISC + F_END * 4 + 64 + 1024;
 
-// TMEM columns
-constexpr uint32_t T_CB = 0, T_DM = 128;                       // group 1
-constexpr uint32_t T_DXD = 0, T_DXS = 64, T_DB = 128, T_DC = 256;  // group 2 (+ dC part 2 in group 3)
-constexpr uint32_t T_YD = 384, T_YO = 448;                     // group 3
+// TMEM columns: dB and dC accumulate over the CTA's heads and C B^T (shared by the
+// group's heads) is computed once; columns 384.. serve each head's three MMA groups.
+constexpr uint32_t T_DB = 0, T_DC = 128, T_CB = 256;      // whole CTA
+constexpr uint32_t T_DM = 384;                            // group 1
+constexpr uint32_t T_DXD = 384, T_DXS = 448;              // group 2 (+ dB, dC)
+constexpr uint32_t T_YD = 384, T_YO = 448;                // group 3 (+ dC)
 
+// grid (kmax, H / HS): one chunk and HS heads of one group per CTA (HS divides H/G).
+// B and C are loaded once.  Every per-head input arrives one head ahead: dy, z and
+// dS land in the E', w o x and dS tiles as soon as the previous head's second MMA
+// group has consumed them, x and S_in as soon as its third has, and dt is read into
+// a register, so no head waits on global memory.  dB and dC accumulate over the
+// CTA's heads in TMEM and are written once: as bf16 outputs when the CTA covers the
+// whole group, else as fp32 shares summed later in head order.
 __global__ void __launch_bounds__(256, 1)
 k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
+               const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmZ, const BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, hf = tid >> 7, quad = warp & 3;
     const int lane = tid & 31;
-    const int k = blockIdx.x, h = blockIdx.y;
+    const int k = blockIdx.x, jsub = blockIdx.y;
     if (k >= p.hdr[HDR_NCHUNKS] || p.hdr[HDR_STATUS] != 0) return;
     const ChunkInfo ci = p.chunks[k];
-    const int g = h / p.sh.hpg;
-    const int H = p.sh.H;
+    const int H = p.sh.H, HS = p.hs;
+    const int h0 = jsub * HS, g = h0 / p.sh.hpg;
+    const bool has_z = p.z != nullptr;
     float *fm = reinterpret_cast<float *>(sm + O_MISC);
     float *cs2 = fm + F_CS2, *dtc = fm + F_DT, *wst = fm + F_W;
+    // 0: B/C, 1: x/S_in, 2: MMA (dx and y tiles), 3: dy/z/dS, 4: MMA (dB/dC chains of group 2)
     uint64_t *bar = reinterpret_cast<uint64_t *>(fm + F_END);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
-    __shared__ int s_abort;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
+    auto load_head = [&](int h) {   // one thread: x and S_in
+        const int slab = k * H + h;
+        mbar_expect_tx(&bar[1], X_BYTES + S_BYTES);
+        tma_load_4d(sm + O_X, &tmX, &bar[1], 0, h, ci.t0, ci.b);
+        tma_load_4d(sm + O_SI, &tmS, &bar[1], 0, 0, slab * PT, 0);
+        tma_load_4d(sm + O_SI + S_BYTES / 2, &tmS, &bar[1], 64, 0, slab * PT, 0);
+    };
+    auto stage_head = [&](int h) {   // one thread: dy, z and fp32 dS
+        const float *src = p.dS + ((int64_t)k * H + h) * (PT * NT);
+        mbar_expect_tx(&bar[3], X_BYTES * (has_z ? 2u : 1u) + 2u * S_BYTES);   // dS fp32 = 2 x S_BYTES
+        tma_load_4d(sm + O_E, &tmDY, &bar[3], 0, h, ci.t0, ci.b);
+        if (has_z) tma_load_4d(sm + O_E + X_BYTES, &tmZ, &bar[3], 0, h, ci.t0, ci.b);
+        bulk_load(sm + O_WX, src, S_BYTES, &bar[3]);
+        bulk_load(sm + O_WX + S_BYTES, src + PT * NT / 2, S_BYTES, &bar[3]);
+    };
     if (tid == 0) {
-        s_abort = 0;
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
-        mbar_expect_tx(&bar[0], X_BYTES + 2 * BC_BYTES + S_BYTES);
-        tma_load_4d(sm + O_X, &tmX, &bar[0], 0, h, ci.t0, ci.b);
+        mbar_expect_tx(&bar[0], 2 * BC_BYTES);
         tma_load_4d(sm + O_B, &tmB, &bar[0], 0, g, ci.t0, ci.b);
         tma_load_4d(sm + O_B + BC_BYTES / 2, &tmB, &bar[0], 64, g, ci.t0, ci.b);
         tma_load_4d(sm + O_C, &tmC, &bar[0], 0, g, ci.t0, ci.b);
         tma_load_4d(sm + O_C + BC_BYTES / 2, &tmC, &bar[0], 64, g, ci.t0, ci.b);
-        // S_in (bf16 [p][n]) of (chunk, head): rows p of the [chunk*H + h] slab
-        const int slab = k * H + h;
-        tma_load_4d(sm + O_SI, &tmS, &bar[0], 0, 0, slab * PT, 0);
-        tma_load_4d(sm + O_SI + S_BYTES / 2, &tmS, &bar[0], 64, 0, slab * PT, 0);
+        stage_head(h0);
+        load_head(h0);
     }
+    // dt_raw + bias of position tid for a head (0 past the chunk's end)
+    auto load_dtv = [&](int h) -> float {
+        return tid < ci.len ? p.dt_raw[(int64_t)ci.b * p.sdb + (int64_t)(ci.t0 + tid) * p.sdl + h] +
+                                  (p.bias ? p.bias[h] : 0.f)
+                            : 0.f;
+    };
+    float dt_next = load_dtv(h0), A_next = p.A[h0], D_next = p.D ? p.D[h0] : 0.f;
     if (warp == 0) tmem_alloc(tslot, 512);
     tc_fence_before();
-    const float lam = chunk_scan_dt(p, ci, h, dtc, cs2, fm + F_WSUM);   // syncs
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lb = (uint32_t)(quad * 32) << 16;
-    const float cl2 = cs2[QT - 1];
-    if (tid < QT) wst[tid] = dtc[tid] * ex2(cl2 - cs2[tid]);
-    __syncthreads();
-    const float Dh = p.D ? p.D[h] : 0.f;
-    const float Ah = p.A[h];
     const int64_t tok = (int64_t)ci.t0 + row;
     const bool live = row < ci.len;
-    uint32_t mma_phase = 0;
+    uint32_t mma_phase = 0, mma2_phase = 0, ld_done = 0, ld_issued = 1, st_done = 0, st_issued = 1, bc_done = 0;
+    int bad = 0;          // this thread saw a wait run out
+    bool aborted = false; // uniform: some thread did (checked once per head)
+    auto fail = [&]() {
+        bad = 1;
+        set_status(const_cast<int32_t *>(p.hdr), SSD_ERR_DEVICE_TIMEOUT);
+    };
     auto wait_mma = [&]() {
-        if (!mbar_wait(&bar[1], mma_phase & 1)) {
-            s_abort = 1;
-            set_status(const_cast<int32_t *>(p.hdr), SSD_ERR_DEVICE_TIMEOUT);
-        }
+        if (!mbar_wait(&bar[2], mma_phase & 1)) fail();
         ++mma_phase;
         tc_fence_after();
     };
-    // dyp rows -> smem; dS (fp32 -> bf16 [p][n]) -> smem; T3 partial
-    float dyp[32];
-    {
-        if (live) {
-            float zz[32];
-            load_row32(p.dy + (int64_t)ci.b * p.sdyb + tok * p.sdyl + (int64_t)h * p.sdyh + 32 * hf, dyp);
-            if (p.z) {
-                load_row32(p.z + (int64_t)ci.b * p.szb + tok * p.szl + (int64_t)h * p.szh + 32 * hf, zz);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dyp[i] *= silu_f(zz[i]);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) dyp[i] = 0.f;
-        }
-        store_row32_swz(sm + O_DY + row * 128, row, hf, dyp);
-    }
-    float t3p = 0.f;
-    {
-        const float *src = p.dS + ((int64_t)k * H + h) * (PT * NT) + (int64_t)(32 * hf) * NT + row;
-        const int n = row, ac = n >> 6, cn = (n & 63) >> 3;
-        uint8_t *base = sm + O_SD + ac * (S_BYTES / 2) + (n & 7) * 2;
-        const uint8_t *sib = sm + O_SI + ac * (S_BYTES / 2) + (n & 7) * 2;
-        float dsv[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) dsv[i] = __ldg(src + (int64_t)i * NT);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int pp = 32 * hf + i;
-            *reinterpret_cast<__nv_bfloat16 *>(base + pp * 128 + ((cn ^ (pp & 7)) << 4)) = __float2bfloat16_rn(dsv[i]);
-        }
-        const bool okS = mbar_wait(&bar[0], 0);   // S_in (and x, B, C) landed
-        if (!okS) {
-            s_abort = 1;
-            set_status(const_cast<int32_t *>(p.hdr), SSD_ERR_DEVICE_TIMEOUT);
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int pp = 32 * hf + i;
-            t3p += __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sib + pp * 128 + ((cn ^ (pp & 7)) << 4))) *
-                   dsv[i];
-        }
-    }
-    // w o x
-    {
-        float xv[32];
-        load_row32_swz(sm + O_X + row * 128, row, hf, xv);
-        const float wl = wst[row];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) xv[i] *= wl;
-        store_row32_swz(sm + O_WX + row * 128, row, hf, xv);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
+    auto wait_mma2 = [&]() {
+        if (!mbar_wait(&bar[4], mma2_phase & 1)) fail();
+        ++mma2_phase;
+        tc_fence_after();
+    };
     const uint32_t sX = smem_u32(sm + O_X), sB = smem_u32(sm + O_B), sC = smem_u32(sm + O_C);
     const uint32_t sSI = smem_u32(sm + O_SI), sDY = smem_u32(sm + O_DY), sWX = smem_u32(sm + O_WX);
     const uint32_t sM = smem_u32(sm + O_M), sE = smem_u32(sm + O_E), sSD = smem_u32(sm + O_SD);
-    if (!s_abort && tid == 0) {   // group 1: CB = C B^T, dM = dyp x^T
-        tc_fence_after();
+
+    for (int hi = 0; hi < HS; ++hi) {
+        const int h = h0 + hi;
+        const float Dh = D_next, Ah = A_next;
+        const float vcur = dt_next;   // dt_raw + bias at position tid
+        {   // dt and the in-chunk cumulative log-decay (cs2 = cs log2 e)
+            const float dt = tid < ci.len ? softplus_f(vcur) : 0.f;
+            float tot;
+            const float cs = block_scan256(tid < QT ? dt * Ah : 0.f, fm + F_WSUM, &tot);
+            if (tid < QT) {
+                dtc[tid] = dt;
+                cs2[tid] = cs * LOG2E;
+            }
+            __syncthreads();
+        }
+        const float cl2 = cs2[QT - 1];
+        if (tid < QT) {
+            wst[tid] = dtc[tid] * ex2(cl2 - cs2[tid]);
+            reinterpret_cast<float2 *>(fm + F_GD)[tid] = make_float2(ex2(cs2[tid | 31] - cs2[tid]), dtc[tid]);
+        }
+        if (!mbar_wait(&bar[3], st_done & 1)) fail();   // dy, z, dS of this head landed
+        ++st_done;
+        if (!mbar_wait(&bar[1], ld_done & 1)) fail();   // x and S_in of this head landed
+        ++ld_done;
+        if (hi == 0) {
+            if (!mbar_wait(&bar[0], bc_done & 1)) fail();
+            ++bc_done;
+        }
+        __syncthreads();
+        float fz[32];   // dy silu'(z): dz = fz o ypre
+        float t3p = 0.f;
+        {
+            float xv[32];
+            {   // dyp = dy silu(z) -> dyp tile; dD row sums dyp . x
+                float dyp[32];
+                load_row32_swz(sm + O_E + row * 128, row, hf, dyp);
+                if (has_z) {
+                    float zz[32];
+                    load_row32_swz(sm + O_E + X_BYTES + row * 128, row, hf, zz);
 #pragma unroll
-        for (int kk = 0; kk < NT / 16; ++kk)
-            umma_bf16(tmem + T_CB, kmaj(sC, kk, BC_BYTES / 2), kmaj(sB, kk, BC_BYTES / 2), idesc_bf16(128, 128, 0, 0),
-                      kk > 0);
+                    for (int i = 0; i < 32; ++i) {
+                        const float sg = sig_f(zz[i]);
+                        fz[i] = dyp[i] * sg * (1.f + zz[i] * (1.f - sg));
+                        dyp[i] *= zz[i] * sg;
+                    }
+                } else {
 #pragma unroll
-        for (int kk = 0; kk < PT / 16; ++kk)
-            umma_bf16(tmem + T_DM, kmaj(sDY, kk, X_BYTES), kmaj(sX, kk, X_BYTES), idesc_bf16(128, 128, 0, 0), kk > 0);
-        umma_commit(&bar[1]);
-    }
-    if (!s_abort) wait_mma();
-    // ---- M, E' (bf16) rows; row sums of M o dM; column sums of E CB dM (fixed order)
-    float rowt1 = 0.f;
-    {
-        const int l = row;
-        const float c2l = cs2[l];
-        float *colp = fm + F_COLP;   // [8 warps][64]
+                    for (int i = 0; i < 32; ++i) fz[i] = 0.f;
+                }
+                if (!live) {
 #pragma unroll
-        for (int bi = 0; bi < 2; ++bi) {
-            const int sb = hf == 0 ? (bi == 0 ? 0 : 3) : (bi == 0 ? 1 : 2);
-            uint32_t pm[16], pe[16];
-            float tmv[32];
-            if (sb <= quad && !s_abort) {
+                    for (int i = 0; i < 32; ++i) dyp[i] = 0.f;
+                }
+                store_row32_swz(sm + O_DY + row * 128, row, hf, dyp);
+                load_row32_swz(sm + O_X + row * 128, row, hf, xv);
+                float dd = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dd += dyp[i] * xv[i];
+                fm[F_ROWD + hf * 128 + row] = dd;
+            }
+            const float wl = wst[row];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xv[i] *= wl;
+            // dS (fp32 [p][n], staged over the w o x and dS tiles): T3 partial and a bf16 copy.
+            // Thread: 4 runs of 8 consecutive n (run c = tid + 256 j: p = c / 16, n0 = 8 (c % 16)).
+            float dsv[4][8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = tid + 256 * j, pp = c >> 4, nc = c & 15;
+                const float4 *s4 = reinterpret_cast<const float4 *>(sm + O_WX) + pp * (NT / 4) + nc * 2;
+                const float4 a = s4[0], b = s4[1];
+                dsv[j][0] = a.x; dsv[j][1] = a.y; dsv[j][2] = a.z; dsv[j][3] = a.w;
+                dsv[j][4] = b.x; dsv[j][5] = b.y; dsv[j][6] = b.z; dsv[j][7] = b.w;
+                const uint4 si = *reinterpret_cast<const uint4 *>(sm + O_SI + (nc >> 3) * (S_BYTES / 2) + pp * 128 +
+                                                                  (((nc & 7) ^ (pp & 7)) << 4));
+                const __nv_bfloat162 *e2 = reinterpret_cast<const __nv_bfloat162 *>(&si);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 sv = __bfloat1622float2(e2[i]);
+                    t3p = fmaf(sv.x, dsv[j][2 * i], t3p);
+                    t3p = fmaf(sv.y, dsv[j][2 * i + 1], t3p);
+                }
+            }
+            __syncthreads();   // the staged dS is read: its space becomes the w o x and dS tiles
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = tid + 256 * j, pp = c >> 4, nc = c & 15;
+                *reinterpret_cast<uint4 *>(sm + O_SD + (nc >> 3) * (S_BYTES / 2) + pp * 128 + (((nc & 7) ^ (pp & 7)) << 4)) =
+                    make_uint4(pack_bf16(dsv[j][0], dsv[j][1]), pack_bf16(dsv[j][2], dsv[j][3]),
+                               pack_bf16(dsv[j][4], dsv[j][5]), pack_bf16(dsv[j][6], dsv[j][7]));
+            }
+            store_row32_swz(sm + O_WX + row * 128, row, hf, xv);
+        }
+        fence_proxy_async_smem();
+        if (__syncthreads_or(bad)) {
+            aborted = true;
+            break;
+        }
+        if (tid == 0) {   // group 1: CB = C B^T (first head only), dM = dyp x^T
+            tc_fence_after();
+            if (hi == 0) {
+#pragma unroll
+                for (int kk = 0; kk < NT / 16; ++kk)
+                    umma_bf16(tmem + T_CB, kmaj(sC, kk, BC_BYTES / 2), kmaj(sB, kk, BC_BYTES / 2),
+                              idesc_bf16(128, 128, 0, 0), kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < PT / 16; ++kk)
+                umma_bf16(tmem + T_DM, kmaj(sDY, kk, X_BYTES), kmaj(sX, kk, X_BYTES), idesc_bf16(128, 128, 0, 0), kk > 0);
+            umma_commit(&bar[2]);
+        }
+        wait_mma();
+        // ---- M = E dt_s CB and E' = E dt_s dM (bf16) rows; row sums of M o dM; column sums of
+        // E CB dM (fixed order).  Blocks of 32 columns below the diagonal take
+        // E = exp(cs[l] - cs[a]) exp(cs[a] - cs[s]) (a = the block's last column; both factors
+        // <= 1), the diagonal block exp per element.
+        {
+            float rowt1 = 0.f;
+            const int l = row;
+            const float c2l = cs2[l];
+            const float2 *gd = reinterpret_cast<const float2 *>(fm + F_GD);
+            float *colp = fm + F_COLP;   // [8 warps][64]
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi) {
+                const int sb = hf == 0 ? (bi == 0 ? 0 : 3) : (bi == 0 ? 1 : 2);   // warp-uniform
+                uint8_t *rm = sm + O_M + (sb >> 1) * (BC_BYTES / 2) + l * 128;
+                uint8_t *re = sm + O_E + (sb >> 1) * (BC_BYTES / 2) + l * 128;
+                if (sb > quad) {   // above the diagonal: zeros (no column sums are read for it)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int cidx = (((sb & 1) << 2) + q) ^ (l & 7);
+                        *reinterpret_cast<uint4 *>(rm + (cidx << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(re + (cidx << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    continue;
+                }
+                uint32_t pm[16], pe[16];
                 float cb[32], dm[32];
                 tmem_ld32(tmem + lb + T_CB + sb * 32, cb);
                 tmem_ld32(tmem + lb + T_DM + sb * 32, dm);
                 tmem_wait_ld();
+                if (sb < quad) {
+                    const float r = ex2(c2l - cs2[sb * 32 + 31]);
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float mv[2], ev[2];
+                    for (int i = 0; i < 32; i += 2) {
+                        float mv[2], ev[2];
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int s = sb * 32 + i + j;
-                        float m = 0.f, e = 0.f, t = 0.f;
-                        if (s <= l) {
-                            const float E = ex2(c2l - cs2[s]);
-                            const float ec = E * cb[i + j];
-                            m = ec * dtc[s];
-                            e = E * dtc[s] * dm[i + j];
-                            t = ec * dm[i + j];
-                            rowt1 += m * dm[i + j];
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const float2 g = gd[sb * 32 + i + jj];
+                            const float E = r * g.x;
+                            const float ec = E * cb[i + jj], ed = E * g.y;
+                            mv[jj] = ed * cb[i + jj];
+                            ev[jj] = ed * dm[i + jj];
+                            rowt1 = fmaf(mv[jj], dm[i + jj], rowt1);
+                            cb[i + jj] = ec * dm[i + jj];   // E CB dM, for the column sums
                         }
-                        mv[j] = m;
-                        ev[j] = e;
-                        tmv[i + j] = t;
+                        pm[i >> 1] = pack_bf16(mv[0], mv[1]);
+                        pe[i >> 1] = pack_bf16(ev[0], ev[1]);
                     }
-                    pm[i >> 1] = pack_bf16(mv[0], mv[1]);
-                    pe[i >> 1] = pack_bf16(ev[0], ev[1]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float mv[2], ev[2];
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int s = sb * 32 + i + jj;
+                            float m = 0.f, e = 0.f, t = 0.f;
+                            if (s <= l) {
+                                const float E = ex2(c2l - cs2[s]);
+                                const float ec = E * cb[i + jj], ed = E * dtc[s];
+                                m = ed * cb[i + jj];
+                                e = ed * dm[i + jj];
+                                t = ec * dm[i + jj];
+                                rowt1 = fmaf(m, dm[i + jj], rowt1);
+                            }
+                            mv[jj] = m;
+                            ev[jj] = e;
+                            cb[i + jj] = t;
+                        }
+                        pm[i >> 1] = pack_bf16(mv[0], mv[1]);
+                        pe[i >> 1] = pack_bf16(ev[0], ev[1]);
+                    }
                 }
-            } else {
+                colp[warp * 64 + bi * 32 + lane] = colsum32(cb);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) { pm[i] = 0u; pe[i] = 0u; }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) tmv[i] = 0.f;
+                for (int q = 0; q < 4; ++q) {
+                    const int cidx = (((sb & 1) << 2) + q) ^ (l & 7);
+                    *reinterpret_cast<uint4 *>(rm + (cidx << 4)) = make_uint4(pm[4 * q], pm[4 * q + 1], pm[4 * q + 2], pm[4 * q + 3]);
+                    *reinterpret_cast<uint4 *>(re + (cidx << 4)) = make_uint4(pe[4 * q], pe[4 * q + 1], pe[4 * q + 2], pe[4 * q + 3]);
+                }
             }
-            const float cs_ = colsum32(tmv);
-            colp[warp * 64 + bi * 32 + lane] = cs_;
-            uint8_t *rm = sm + O_M + (sb >> 1) * (BC_BYTES / 2) + l * 128;
-            uint8_t *re = sm + O_E + (sb >> 1) * (BC_BYTES / 2) + l * 128;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int cidx = (((sb & 1) << 2) + q) ^ (l & 7);
-                *reinterpret_cast<uint4 *>(rm + (cidx << 4)) = make_uint4(pm[4 * q], pm[4 * q + 1], pm[4 * q + 2], pm[4 * q + 3]);
-                *reinterpret_cast<uint4 *>(re + (cidx << 4)) = make_uint4(pe[4 * q], pe[4 * q + 1], pe[4 * q + 2], pe[4 * q + 3]);
-            }
+            fm[F_ROWT1 + hf * 128 + l] = rowt1;
         }
-        fm[F_ROWT1 + hf * 128 + l] = rowt1;
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (!s_abort && tid == 0) {   // group 2
-        tc_fence_after();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {   // group 2
+            tc_fence_after();
+            const uint32_t first = hi == 0 ? 0u : 1u;
 #pragma unroll
-        for (int kk = 0; kk < QT / 16; ++kk)   // dx_diag[s][p] = sum_l M[l][s] dyp[l][p]
-            umma_bf16(tmem + T_DXD, mnmaj(sM, kk, BC_BYTES / 2), mnmaj(sDY, kk, 16384u), idesc_bf16(128, 64, 1, 1),
-                      kk > 0);
+            for (int kk = 0; kk < QT / 16; ++kk)   // dx_diag[s][p] = sum_l M[l][s] dyp[l][p]
+                umma_bf16(tmem + T_DXD, mnmaj(sM, kk, BC_BYTES / 2), mnmaj(sDY, kk, 16384u), idesc_bf16(128, 64, 1, 1),
+                          kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < NT / 16; ++kk)   // u[s][p] = sum_n B[s][n] dS[p][n]
-            umma_bf16(tmem + T_DXS, kmaj(sB, kk, BC_BYTES / 2), kmaj(sSD, kk, S_BYTES / 2), idesc_bf16(128, 64, 0, 0),
-                      kk > 0);
+            for (int kk = 0; kk < NT / 16; ++kk)   // u[s][p] = sum_n B[s][n] dS[p][n]
+                umma_bf16(tmem + T_DXS, kmaj(sB, kk, BC_BYTES / 2), kmaj(sSD, kk, S_BYTES / 2), idesc_bf16(128, 64, 0, 0),
+                          kk > 0);
+            umma_commit(&bar[2]);   // the dx tiles; the dB/dC chains below run on during the dx epilogue
 #pragma unroll
-        for (int kk = 0; kk < QT / 16; ++kk)   // dB[s][n] = sum_l E'[l][s] C[l][n]
-            umma_bf16(tmem + T_DB, mnmaj(sE, kk, BC_BYTES / 2), mnmaj(sC, kk, BC_BYTES / 2),
-                      idesc_bf16(128, 128, 1, 1), kk > 0);
+            for (int kk = 0; kk < QT / 16; ++kk)   // dB[s][n] (+)= sum_l E'[l][s] C[l][n]
+                umma_bf16(tmem + T_DB, mnmaj(sE, kk, BC_BYTES / 2), mnmaj(sC, kk, BC_BYTES / 2),
+                          idesc_bf16(128, 128, 1, 1), (kk > 0) ? 1u : first);
 #pragma unroll
-        for (int kk = 0; kk < PT / 16; ++kk)   // dB[s][n] += sum_p (w o x)[s][p] dS[p][n]
-            umma_bf16(tmem + T_DB, kmaj(sWX, kk, X_BYTES), mnmaj(sSD, kk, S_BYTES / 2),
-                      idesc_bf16(128, 128, 0, 1), 1);
+            for (int kk = 0; kk < PT / 16; ++kk)   // dB[s][n] += sum_p (w o x)[s][p] dS[p][n]
+                umma_bf16(tmem + T_DB, kmaj(sWX, kk, X_BYTES), mnmaj(sSD, kk, S_BYTES / 2), idesc_bf16(128, 128, 0, 1), 1);
 #pragma unroll
-        for (int kk = 0; kk < QT / 16; ++kk)   // dC[l][n] = sum_s E'[l][s] B[s][n]
-            umma_bf16(tmem + T_DC, kmaj(sE, kk, BC_BYTES / 2), mnmaj(sB, kk, BC_BYTES / 2),
-                      idesc_bf16(128, 128, 0, 1), kk > 0);
-        umma_commit(&bar[1]);
-    }
-    if (!s_abort) wait_mma();
-    // ---- dx = dx_diag + w o u + D dyp; x.u row sums
-    {
-        float dxd[32], u[32], xv[32];
-        tmem_ld32(tmem + lb + T_DXD + 32 * hf, dxd);
-        tmem_ld32(tmem + lb + T_DXS + 32 * hf, u);
-        tmem_wait_ld();
-        load_row32_swz(sm + O_X + row * 128, row, hf, xv);
-        const float ws = wst[row];
-        float xu = 0.f;
-        float o[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            xu += xv[i] * u[i];
-            o[i] = dxd[i] + ws * u[i] + Dh * dyp[i];
+            for (int kk = 0; kk < QT / 16; ++kk)   // dC[l][n] (+)= sum_s E'[l][s] B[s][n]
+                umma_bf16(tmem + T_DC, kmaj(sE, kk, BC_BYTES / 2), mnmaj(sB, kk, BC_BYTES / 2),
+                          idesc_bf16(128, 128, 0, 1), (kk > 0) ? 1u : first);
+            umma_commit(&bar[4]);
         }
-        fm[F_ROWXU + hf * 128 + row] = xu;
-        if (live) {
-            uint4 *dst = reinterpret_cast<uint4 *>(p.dx + (int64_t)ci.b * p.sdxb + tok * p.sdxl + (int64_t)h * p.sdxh + 32 * hf);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                                    pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+        wait_mma();
+        if (hi + 1 < HS) {
+            dt_next = load_dtv(h + 1);
+            A_next = p.A[h + 1];
+            D_next = p.D ? p.D[h + 1] : 0.f;
         }
-        // e o dyp over the dyp tile (row-uniform scale)
-        const float el = ex2(cs2[row]);
-        float ev[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ev[i] = dyp[i] * el;
-        store_row32_swz(sm + O_DY + row * 128, row, hf, ev);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (!s_abort && tid == 0) {   // group 3
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < PT / 16; ++kk)   // dC[l][n] += sum_p (e o dyp)[l][p] S_in[p][n]
-            umma_bf16(tmem + T_DC, kmaj(sDY, kk, X_BYTES), mnmaj(sSI, kk, S_BYTES / 2), idesc_bf16(128, 128, 0, 1), 1);
-#pragma unroll
-        for (int kk = 0; kk < QT / 16; ++kk)   // Y_diag[l][p] = sum_s M[l][s] x[s][p]
-            umma_bf16(tmem + T_YD, kmaj(sM, kk, BC_BYTES / 2), mnmaj(sX, kk, 16384u), idesc_bf16(128, 64, 0, 1), kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < NT / 16; ++kk)   // Ybar[l][p] = sum_n C[l][n] S_in[p][n]
-            umma_bf16(tmem + T_YO, kmaj(sC, kk, BC_BYTES / 2), kmaj(sSI, kk, S_BYTES / 2), idesc_bf16(128, 64, 0, 0),
-                      kk > 0);
-        umma_commit(&bar[1]);
-    }
-    if (!s_abort) wait_mma();
-    // ---- dB, dC shares; ypre -> dz; T2, dD row sums
-    {
-        const int64_t base = ((int64_t)k * H + h) * QT * NT + (int64_t)row * NT + 64 * hf;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float v[32];
-            tmem_ld32(tmem + lb + T_DB + 64 * hf + 32 * half, v);
+        {   // dx = dx_diag + w o u + D dyp; x.u row sums; then e o dyp over the dyp tile
+            float dxd[32], u[32], xv[32], dyp[32];
+            tmem_ld32(tmem + lb + T_DXD + 32 * hf, dxd);
+            tmem_ld32(tmem + lb + T_DXS + 32 * hf, u);
+            load_row32_swz(sm + O_X + row * 128, row, hf, xv);
+            load_row32_swz(sm + O_DY + row * 128, row, hf, dyp);
             tmem_wait_ld();
-            float4 *d = reinterpret_cast<float4 *>(p.dBh + base + 32 * half);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            tmem_ld32(tmem + lb + T_DC + 64 * hf + 32 * half, v);
-            tmem_wait_ld();
-            d = reinterpret_cast<float4 *>(p.dCh + base + 32 * half);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
-        float yd[32], yb[32], xv[32];
-        tmem_ld32(tmem + lb + T_YD + 32 * hf, yd);
-        tmem_ld32(tmem + lb + T_YO + 32 * hf, yb);
-        tmem_wait_ld();
-        load_row32_swz(sm + O_X + row * 128, row, hf, xv);
-        const float el = ex2(cs2[row]);
-        float t2 = 0.f, dd = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            t2 += dyp[i] * el * yb[i];
-            dd += dyp[i] * xv[i];
-        }
-        fm[F_ROWT2 + hf * 128 + row] = t2;
-        fm[F_ROWD + hf * 128 + row] = dd;
-        if (live && p.z) {
-            float dyv[32], zz[32], o[32];
-            load_row32(p.dy + (int64_t)ci.b * p.sdyb + tok * p.sdyl + (int64_t)h * p.sdyh + 32 * hf, dyv);
-            load_row32(p.z + (int64_t)ci.b * p.szb + tok * p.szl + (int64_t)h * p.szh + 32 * hf, zz);
+            const float ws = wst[row];
+            float xu = 0.f;
+            float o[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float ypre = yd[i] + el * yb[i] + Dh * xv[i];
-                const float sg = sig_f(zz[i]);
-                o[i] = dyv[i] * ypre * sg * (1.f + zz[i] * (1.f - sg));
+                xu = fmaf(xv[i], u[i], xu);
+                o[i] = dxd[i] + ws * u[i] + Dh * dyp[i];
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(p.dz + (int64_t)ci.b * p.sdzb + tok * p.sdzl + (int64_t)h * p.sdzh + 32 * hf);
+            fm[F_ROWXU + hf * 128 + row] = xu;
+            if (live) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.dx + (int64_t)ci.b * p.sdxb + tok * p.sdxl + (int64_t)h * p.sdxh + 32 * hf);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                                    pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
-        }
-    }
-    // T3 = exp(cs[Q-1]) <S_in, dS>: fixed-order block reduction
-    {
-        const float w = warp_sum(t3p);
-        if (lane == 0) fm[F_RED + warp] = w;
-    }
-    __syncthreads();
-    // ---- per-position scalars (threads 0..127 = position i)
-    {
-        const int i = tid;
-        float dcs = 0.f, ddir = 0.f, t4 = 0.f;
-        if (i < QT) {
-            // column sums of E CB dM for column i: warps with the half that built block i/32, quads >= i/32
-            const int sb = i >> 5, j = i & 31;
-            const int hsel = (sb == 0 || sb == 3) ? 0 : 1;
-            const int bi = (sb == 0 || sb == 1) ? 0 : 1;
-            float colTm = 0.f;
-            for (int q = sb; q < 4; ++q) colTm += fm[F_COLP + (hsel * 4 + q) * 64 + bi * 32 + j];
-            const float xu = fm[F_ROWXU + i] + fm[F_ROWXU + 128 + i];
-            const float r1 = fm[F_ROWT1 + i] + fm[F_ROWT1 + 128 + i];
-            const float r2 = fm[F_ROWT2 + i] + fm[F_ROWT2 + 128 + i];
-            t4 = wst[i] * xu;
-            ddir = colTm + ex2(cl2 - cs2[i]) * xu;
-            dcs = r1 - dtc[i] * colTm + r2 - t4;
-        }
-        float t4tot;
-        (void)block_scan256(t4, fm + F_WSUM, &t4tot);   // total of T4 (positions >= len contribute 0)
-        float T3 = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) T3 += fm[F_RED + w];
-        T3 *= ex2(cl2);
-        if (i == QT - 1) dcs += T3 + t4tot;
-        // da[u] = sum_{i >= u} dcs[i] = total - (inclusive prefix up to u) + dcs[u]
-        float dtot;
-        const float inc = block_scan256(i < QT ? dcs : 0.f, fm + F_WSUM, &dtot);
-        float pa = 0.f, pb = 0.f, pd = 0.f;
-        if (i < QT) {
-            const float da = dtot - inc + dcs;
-            if (i < ci.len) {
-                const float v = p.dt_raw[(int64_t)ci.b * p.sdb + (int64_t)(ci.t0 + i) * p.sdl + h] + (p.bias ? p.bias[h] : 0.f);
-                const float gv = (ddir + Ah * da) * sigmoid_f(v);
-                p.ddt[(int64_t)ci.b * p.sddb + (int64_t)(ci.t0 + i) * p.sddl + h] = gv;
-                pa = dtc[i] * da;
-                pb = gv;
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                                        pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
             }
-            pd = fm[F_ROWD + i] + fm[F_ROWD + 128 + i];
+            const float el = ex2(cs2[row]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dyp[i] *= el;
+            store_row32_swz(sm + O_DY + row * 128, row, hf, dyp);
         }
-        float ta, tb, td;
-        (void)block_scan256(pa, fm + F_WSUM, &ta);
-        (void)block_scan256(pb, fm + F_WSUM, &tb);
-        (void)block_scan256(pd, fm + F_WSUM, &td);
-        if (tid == 0) {
-            float *pp = p.partials + ((int64_t)k * H + h) * 4;
-            pp[0] = ta; pp[1] = td; pp[2] = tb; pp[3] = 0.f;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {   // group 3
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < PT / 16; ++kk)   // dC[l][n] += sum_p (e o dyp)[l][p] S_in[p][n]
+                umma_bf16(tmem + T_DC, kmaj(sDY, kk, X_BYTES), mnmaj(sSI, kk, S_BYTES / 2), idesc_bf16(128, 128, 0, 1), 1);
+#pragma unroll
+            for (int kk = 0; kk < QT / 16; ++kk)   // Y_diag[l][p] = sum_s M[l][s] x[s][p]
+                umma_bf16(tmem + T_YD, kmaj(sM, kk, BC_BYTES / 2), mnmaj(sX, kk, 16384u), idesc_bf16(128, 64, 0, 1), kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < NT / 16; ++kk)   // Ybar[l][p] = sum_n C[l][n] S_in[p][n]
+                umma_bf16(tmem + T_YO, kmaj(sC, kk, BC_BYTES / 2), kmaj(sSI, kk, S_BYTES / 2), idesc_bf16(128, 64, 0, 0),
+                          kk > 0);
+            umma_commit(&bar[2]);
+        }
+        wait_mma();
+        wait_mma2();   // done with the group above: no MMA reads smem now
+        // this head's x row, then E', w o x, dS, x and S_in are free: fetch the next head's inputs
+        float xv[32];
+        load_row32_swz(sm + O_X + row * 128, row, hf, xv);
+        __syncthreads();
+        if (hi + 1 < HS) {
+            if (tid == 0) {
+                stage_head(h + 1);
+                load_head(h + 1);
+            }
+            ++st_issued;
+            ++ld_issued;
+        }
+        {   // ypre -> dz; T2 row sums
+            float yd[32], yb[32], ev[32];
+            tmem_ld32(tmem + lb + T_YD + 32 * hf, yd);
+            tmem_ld32(tmem + lb + T_YO + 32 * hf, yb);
+            load_row32_swz(sm + O_DY + row * 128, row, hf, ev);
+            tmem_wait_ld();
+            const float el = ex2(cs2[row]);
+            float t2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) t2 += ev[i] * yb[i];
+            fm[F_ROWT2 + hf * 128 + row] = t2;
+            if (live && has_z) {
+                float o[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = fz[i] * (yd[i] + el * yb[i] + Dh * xv[i]);
+                uint4 *dst = reinterpret_cast<uint4 *>(p.dz + (int64_t)ci.b * p.sdzb + tok * p.sdzl + (int64_t)h * p.sdzh + 32 * hf);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                                        pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+            }
+        }
+        {   // T3 = exp(cs[Q-1]) <S_in, dS>: fixed-order block reduction
+            const float w = warp_sum(t3p);
+            if (lane == 0) fm[F_RED + warp] = w;
+        }
+        __syncthreads();
+        {   // ---- per-position scalars (threads 0..127 = position i)
+            const int i = tid;
+            float dcs = 0.f, ddir = 0.f, t4 = 0.f;
+            if (i < QT) {
+                const int sb = i >> 5, jj = i & 31;
+                const int hsel = (sb == 0 || sb == 3) ? 0 : 1;
+                const int bi = (sb == 0 || sb == 1) ? 0 : 1;
+                float colTm = 0.f;   // sum_l (E CB dM)[l][i], rows in quads >= sb, in quad order
+                for (int q = sb; q < 4; ++q) colTm += fm[F_COLP + (hsel * 4 + q) * 64 + bi * 32 + jj];
+                const float xu = fm[F_ROWXU + i] + fm[F_ROWXU + 128 + i];
+                const float r1 = fm[F_ROWT1 + i] + fm[F_ROWT1 + 128 + i];
+                const float r2 = fm[F_ROWT2 + i] + fm[F_ROWT2 + 128 + i];
+                t4 = wst[i] * xu;
+                ddir = colTm + ex2(cl2 - cs2[i]) * xu;
+                dcs = r1 - dtc[i] * colTm + r2 - t4;
+            }
+            float T3 = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) T3 += fm[F_RED + w];
+            T3 *= ex2(cl2);
+            // da[u] = sum_{i>=u} dcs[i] + T3 + sum_s T4[s]: one pass gives the scan of dcs and the sum of T4
+            float dtot, t4tot;
+            const float inc = block_scan_sum(dcs, t4, fm + F_WSUM, &dtot, &t4tot);
+            float pa = 0.f, pb = 0.f, pd = 0.f;
+            if (i < QT) {
+                const float da = dtot - inc + dcs + T3 + t4tot;
+                if (i < ci.len) {
+                    const float gv = (ddir + Ah * da) * sigmoid_f(vcur);
+                    p.ddt[(int64_t)ci.b * p.sddb + (int64_t)(ci.t0 + i) * p.sddl + h] = gv;
+                    pa = dtc[i] * da;
+                    pb = gv;
+                }
+                pd = fm[F_ROWD + i] + fm[F_ROWD + 128 + i];
+            }
+            // dA, ddt_bias, dD shares: fixed-order block sums of pa, pb, pd
+            pa = warp_sum(pa);
+            pb = warp_sum(pb);
+            pd = warp_sum(pd);
+            if (lane == 0) {
+                fm[F_RED + warp] = pa;
+                fm[F_PB + warp] = pb;
+                fm[F_RED + 8 + warp] = pd;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                float ta = 0.f, tb = 0.f, td = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    ta += fm[F_RED + w];
+                    tb += fm[F_PB + w];
+                    td += fm[F_RED + 8 + w];
+                }
+                float *pp = p.partials + ((int64_t)k * H + h) * 4;
+                pp[0] = ta; pp[1] = td; pp[2] = tb; pp[3] = 0.f;
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    // ---- dB, dC of the CTA's heads: final bf16 rows when the CTA covers the group, else fp32 shares
+    if (!aborted && !__syncthreads_or(bad)) {
+        const bool whole = p.hs == p.sh.hpg;
+        const int NSUB = H / HS;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const uint32_t col0 = (which == 0 ? T_DB : T_DC) + 64 * hf;
+            float v[64];
+            {
+                float t[32];
+                tmem_ld32(tmem + lb + col0, t);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = t[i];
+                tmem_ld32(tmem + lb + col0 + 32, t);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[32 + i] = t[i];
+            }
+            if (whole) {
+                if (live) {
+                    __nv_bfloat16 *dst = (which == 0 ? p.dB : p.dC) +
+                                         (int64_t)ci.b * (which == 0 ? p.sdBb : p.sdCb) +
+                                         tok * (which == 0 ? p.sdBl : p.sdCl) + (int64_t)g * (which == 0 ? p.sdBg : p.sdCg) +
+                                         64 * hf;
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        d4[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                                           pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+                }
+            } else {
+                float *dst = (which == 0 ? p.dBh : p.dCh) + (((int64_t)k * NSUB + jsub) * QT + row) * NT + 64 * hf;
+                float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
         }
     }
-    (void)lam;
+    // drain (only after an early stop) and free TMEM
+    for (uint32_t q = ld_done; q < ld_issued; ++q) mbar_wait(&bar[1], q & 1);
+    for (uint32_t q = st_done; q < st_issued; ++q) mbar_wait(&bar[3], q & 1);
+    if (bc_done == 0) mbar_wait(&bar[0], 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -670,6 +842,10 @@ static BwdParams make_params(const Shape &sh, const int32_t *hdr, const ChunkInf
     p.sdzb = a.sdz ? a.sdz[0] : 0; p.sdzl = a.sdz ? a.sdz[1] : 0; p.sdzh = a.sdz ? a.sdz[2] : 0;
     p.ddt = a.ddt; p.sddb = a.sddb; p.sddl = a.sddl;
     p.dS = a.dS; p.dS_loc = a.dS; p.chunk_lam = a.chunk_lam; p.dBh = a.dBh; p.dCh = a.dCh; p.partials = a.partials;
+    p.hs = a.hs;
+    p.dB = (__nv_bfloat16 *)a.dB; p.dC = (__nv_bfloat16 *)a.dC;
+    p.sdBb = a.sdB ? a.sdB[0] : 0; p.sdBl = a.sdB ? a.sdB[1] : 0; p.sdBg = a.sdB ? a.sdB[2] : 0;
+    p.sdCb = a.sdC ? a.sdC[0] : 0; p.sdCl = a.sdC ? a.sdC[1] : 0; p.sdCg = a.sdC ? a.sdC[2] : 0;
     return p;
 }
 
@@ -687,8 +863,14 @@ cudaError_t launch_bwd_dstates_tc(const Shape &sh, const int32_t *hdr, const Chu
 
 cudaError_t launch_bwd_chunk_tc(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const BwdTcArgs &a,
                                 cudaStream_t st) {
-    CUtensorMap mx, mb, mc, ms;
+    CUtensorMap mx, mb, mc, ms, mdy, mz;
     if (!map4(&mx, a.x, PT, sh.H, sh.L, sh.B, a.sx[2], a.sx[1], a.sx[0], QT)) return cudaErrorInvalidValue;
+    if (!map4(&mdy, a.dy, PT, sh.H, sh.L, sh.B, a.sdy[2], a.sdy[1], a.sdy[0], QT)) return cudaErrorInvalidValue;
+    if (a.z != nullptr) {
+        if (!map4(&mz, a.z, PT, sh.H, sh.L, sh.B, a.sz[2], a.sz[1], a.sz[0], QT)) return cudaErrorInvalidValue;
+    } else {
+        mz = mdy;   // not read
+    }
     if (!map4(&mb, a.Bp, NT, sh.G, sh.L, sh.B, a.sb[2], a.sb[1], a.sb[0], QT)) return cudaErrorInvalidValue;
     if (!map4(&mc, a.Cp, NT, sh.G, sh.L, sh.B, a.sc[2], a.sc[1], a.sc[0], QT)) return cudaErrorInvalidValue;
     // carried states as a [rows = chunk*H*P][N] matrix, box {64, 64 rows}
@@ -698,7 +880,7 @@ cudaError_t launch_bwd_chunk_tc(const Shape &sh, const int32_t *hdr, const Chunk
     static int attr_done[64] = {0};
     cudaError_t e = ensure_smem_attr(k_bwd_chunk_tc, (int)BWD_SMEM, attr_done);
     if (e != cudaSuccess) return e;
-    k_bwd_chunk_tc<<<dim3(sh.kmax, sh.H), 256, BWD_SMEM, st>>>(mx, mb, mc, ms, p);
+    k_bwd_chunk_tc<<<dim3(sh.kmax, sh.H / a.hs), 256, BWD_SMEM, st>>>(mx, mb, mc, ms, mdy, mz, p);
     return cudaGetLastError();
 }
 

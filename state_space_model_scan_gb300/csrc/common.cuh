@@ -60,6 +60,9 @@ struct BwdTcArgs {
     int64_t sddb, sddl;
     const __nv_bfloat16 *states;   // [chunk][H][P][N] bf16 carried states
     float *dS, *chunk_lam, *dBh, *dCh, *partials;
+    int hs;                         // heads per CTA of the gradient kernel (divides H/G)
+    void *dB, *dC;                  // final dB/dC (written directly when hs == H/G)
+    const int64_t *sdB, *sdC;
 };
 
 // Strided views (element strides of the three outer dims; innermost stride 1).

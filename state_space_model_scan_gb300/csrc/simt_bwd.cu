@@ -302,21 +302,26 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
 }
 
 // ------------------------------------------------------------------ reductions
-// dB/dC: sum the per-head rows of each group in head order.  grid (kmax, G), block 256.
+// dB and dC: sum the per-head rows of each group in head order.  grid (kmax, G,
+// 2 * ceil(Q/16)): z picks dB or dC and a slab of 16 rows of the chunk; block 256.
 template <typename T>
 __global__ void k_reduce_group(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restrict__ chunks,
-                               const float *__restrict__ src, MView3 dst) {
+                               const float *__restrict__ srcB, MView3 dstB, const float *__restrict__ srcC,
+                               MView3 dstC) {
     const int k = blockIdx.x, g = blockIdx.y;
+    const int nslab = (sh.Q + 15) / 16;
+    const int which = blockIdx.z / nslab, l0 = (blockIdx.z % nslab) * 16;
     if (k >= hdr[HDR_NCHUNKS] || hdr[HDR_STATUS] != 0) return;
     const ChunkInfo ci = chunks[k];
+    const float *src = which == 0 ? srcB : srcC;
+    const MView3 dst = which == 0 ? dstB : dstC;
     const int N = sh.N;
-    for (int i = threadIdx.x; i < ci.len * N; i += blockDim.x) {
-        const int l = i / N, n = i % N;
+    const int rows = min(16, ci.len - l0);
+    for (int i = threadIdx.x; i < rows * N; i += blockDim.x) {
+        const int l = l0 + i / N, n = i % N;
         float a = 0.f;
-        for (int j = 0; j < sh.hpg; ++j) {
-            const int h = g * sh.hpg + j;
-            a += src[(((int64_t)k * sh.H + h) * sh.Q + l) * N + n];
-        }
+        const float *s = src + (((int64_t)k * sh.H + (int64_t)g * sh.hpg) * sh.Q + l) * N + n;
+        for (int j = 0; j < sh.hpg; ++j) a += s[(int64_t)j * sh.Q * N];
         T *o = (T *)dst.p + (int64_t)ci.b * dst.s0 + (int64_t)(ci.t0 + l) * dst.s1 + (int64_t)g * dst.s2;
         o[n] = from_f<T>(a);
     }
@@ -376,9 +381,10 @@ cudaError_t launch_bwd_chunk(const Shape &sh, const int32_t *hdr, const ChunkInf
 }
 
 template <typename T>
-cudaError_t launch_reduce_group(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const float *src,
-                                MView3 dst, cudaStream_t st) {
-    k_reduce_group<T><<<dim3(sh.kmax, sh.G), 256, 0, st>>>(sh, hdr, chunks, src, dst);
+cudaError_t launch_reduce_group(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const float *srcB,
+                                MView3 dstB, const float *srcC, MView3 dstC, cudaStream_t st) {
+    const int nslab = (sh.Q + 15) / 16;
+    k_reduce_group<T><<<dim3(sh.kmax, sh.G, 2 * nslab), 256, 0, st>>>(sh, hdr, chunks, srcB, dstB, srcC, dstC);
     return cudaGetLastError();
 }
 
@@ -397,7 +403,7 @@ cudaError_t launch_reduce_heads(const Shape &sh, const int32_t *hdr, const float
                                              const float *, const float *, MView3, MView3, float *, int64_t,      \
                                              int64_t, float *, float *, float *, cudaStream_t);                   \
     template cudaError_t launch_reduce_group<T>(const Shape &, const int32_t *, const ChunkInfo *, const float *, \
-                                                MView3, cudaStream_t);
+                                                MView3, const float *, MView3, cudaStream_t);
 SSD_INST(float)
 SSD_INST(__nv_bfloat16)
 #undef SSD_INST

@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.abi_version() == 1
+    assert lib.abi_version() == 2
     for code, name in lib.STATUS_NAMES.items():
         assert lib.status_string(code) == name
     assert lib.status_string(99) == "SSD_ERR_UNKNOWN"

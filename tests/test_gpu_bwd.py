@@ -99,3 +99,37 @@ def test_bwd_deterministic(P, N):
     g2 = gpu_backward(w, inp)
     for k in g1:
         assert torch.equal(g1[k], g2[k]), k
+
+
+@pytest.mark.parametrize("H,G", [(24, 2), (16, 1)])
+def test_bwd_heads_per_cta(H, G):
+    """The gradient kernel's heads-per-CTA choice (whole group in one CTA, or subsets
+    of it summed afterwards) changes only the summation order of dB and dC."""
+    w = W(L=300, H=H, P=64, G=G, N=128, Q=128, dtype="bf16", has_z=True, has_init=True)
+    inp = I.make_inputs(w, with_grad_inputs=True, with_dfinal=True)
+    o = oracle_backward(w, inp)
+    T = w.batch * w.seqlen
+    hpg = H // G
+    choices = [0] + [d for d in range(1, 33) if hpg % d == 0]
+    ref = None
+    for hs in choices:
+        g = gpu_backward(w, inp, algo="fused", bwd_heads=hs)
+        for gn, on in NAMES:
+            t = g[gn]
+            a = flat(t, T) if t.dim() >= 3 and gn != "dinitial_states" else t.detach().double().cpu().numpy()
+            assert rel_l2(a.reshape(o[on].shape), o[on]) <= TOL["bf16"], (hs, gn)
+        if ref is None:
+            ref = g
+        else:
+            for k in g:
+                if k not in ("dB", "dC"):
+                    assert torch.equal(g[k], ref[k]), (hs, k)
+
+
+def test_bwd_heads_invalid():
+    from state_space_model_scan_gb300._lib import SSDError
+    w = W(L=200, H=12, P=64, G=1, N=128, Q=128, dtype="bf16")
+    inp = I.make_inputs(w, with_grad_inputs=True)
+    for hs in (5, 33, -1):
+        with pytest.raises(SSDError):
+            gpu_backward(w, inp, algo="fused", bwd_heads=hs)
