@@ -113,6 +113,15 @@ int bwd_heads_per_cta(int64_t kmax, int64_t H, int hpg) {
     return best;
 }
 
+// Heads per CTA of the tensor-core dstates kernel (two CTAs per SM): the largest
+// divisor of H/G up to 8 that still gives two full waves of CTAs, else 1.
+int dstates_heads_per_cta(int64_t kmax, int64_t H, int hpg) {
+    const int64_t slots = 2LL * num_sms();
+    for (int d = 8; d > 1; --d)
+        if (hpg % d == 0 && kmax * (H / d) >= 2 * slots) return d;
+    return 1;
+}
+
 struct Layout {
     size_t cur = 0;
     size_t take(size_t bytes) {
@@ -485,7 +494,7 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         ta.dx = b->dx.ptr; ta.dz = b->dz.ptr; ta.sdx = b->dx.stride; ta.sdz = b->dz.ptr ? b->dz.stride : nullptr;
         ta.ddt = (float *)b->ddt.ptr; ta.sddb = b->ddt.stride[0]; ta.sddl = b->ddt.stride[1];
         ta.states = states; ta.dS = dS; ta.chunk_lam = clam; ta.dBh = dBh; ta.dCh = dCh; ta.partials = part;
-        ta.hs = pl.hs; ta.dB = b->dB.ptr; ta.dC = b->dC.ptr; ta.sdB = b->dB.stride; ta.sdC = b->dC.stride;
+        ta.hs = pl.hs; ta.hs_ds = dstates_heads_per_cta(sh.kmax, sh.H, sh.hpg); ta.dB = b->dB.ptr; ta.dC = b->dC.ptr; ta.sdB = b->dB.stride; ta.sdC = b->dC.stride;
         if (sh.kmax > 0) SSD_CUDA(launch_bwd_dstates_tc(sh, hdr, chunks, ta, st));
         SSD_CUDA(launch_state_passing(sh, hdr, seqs, clam, 1, dS, (const float *)b->dfinal_states.ptr,
                                       (float *)b->dinitial_states.ptr, 1, st));

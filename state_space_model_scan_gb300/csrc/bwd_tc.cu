@@ -15,7 +15,7 @@
 //     dcs[i] = sum_s (M o dM)[i][s] - sum_l (M o dM)[l][i] + dyp[i].(e_i C S_in^T)[i] - T4[i]
 //              + [i = Q-1](exp(cs[Q-1]) <S_in, dS> + sum_s T4[s]),  T4[s] = w_s x[s].(B dS^T)[s]
 //     dz = dy ypre silu'(z),  ypre = M x + e o (C S_in^T) + D x
-// k_bwd_dstates computes the per-chunk state gradient source
+// k_bwd_dstates_tc computes the per-chunk state gradient source
 //     dS_loc[p][n] = sum_l e_l dyp[l][p] C[l][n]
 // which the reverse warp-shuffle scan turns into dS for every chunk.
 // The row sums of M o dM and the dt-weighted column sums of E CB dM cancel along the
@@ -57,6 +57,7 @@ struct BwdParams {
     float *dBh, *dCh;        // [chunk][H/hs][Q][N] fp32 shares of head subsets (when hs < H/G)
     float *partials;         // [chunk][H][4]: dA, dD, ddt_bias shares
     int hs;                  // heads per CTA of the gradient kernel
+    int hs_ds;               // heads per CTA of the dstates kernel
     __nv_bfloat16 *dB, *dC;  // final outputs when hs == H/G
     int64_t sdBb, sdBl, sdBg, sdCb, sdCl, sdCg;
 };
@@ -165,103 +166,126 @@ __device__ __forceinline__ float block_scan_sum(float v, float u, float *wsum, f
     return x + off;
 }
 
-// dt and the in-chunk cumulative log-decay of (chunk, head) into smem (cs2 = cs*log2 e).
-__device__ __forceinline__ float chunk_scan_dt(const BwdParams &p, const ChunkInfo &ci, int h, float *dtc,
-                                               float *cs2, float *wsum) {
-    const int tid = threadIdx.x;
-    float dt = 0.f;
-    if (tid < ci.len) {
-        const float v = p.dt_raw[(int64_t)ci.b * p.sdb + (int64_t)(ci.t0 + tid) * p.sdl + h] + (p.bias ? p.bias[h] : 0.f);
-        dt = softplus_f(v);
-    }
-    float tot;
-    const float cs = block_scan256(tid < QT ? dt * p.A[h] : 0.f, wsum, &tot);
-    if (tid < QT) {
-        dtc[tid] = dt;
-        cs2[tid] = cs * LOG2E;
-    }
-    __syncthreads();
-    return tot;
-}
-
 // ------------------------------------------------------------------ dstates
-// grid (kmax, H), 256 threads.  dS_loc^T[n][p] = sum_l C[l][n] (e o dyp)[l][p] on the
-// tensor cores (A = C^T, M-major; B = e o dyp, N-major), written as fp32 [p][n].
-constexpr uint32_t DS_OFF_C = 0, DS_OFF_Y = BC_BYTES, DS_OFF_MISC = BC_BYTES + X_BYTES;
+// grid (kmax, H / hs_ds), 256 threads, two CTAs per SM: one chunk and hs_ds heads of one
+// group per CTA.  Per head, dS_loc^T[n][p] = sum_l C[l][n] (e o dyp)[l][p] on the tensor
+// cores (A = C^T, M-major; B = e o dyp, N-major), written as fp32 [p][n].  C is loaded
+// once; each head's dy and z tiles arrive by TMA while the previous head computes.
+constexpr uint32_t DS_OFF_C = 0, DS_OFF_ST = BC_BYTES, DS_OFF_Y = BC_BYTES + 2 * X_BYTES,
+                   DS_OFF_MISC = DS_OFF_Y + X_BYTES;
 constexpr uint32_t DS_SMEM = DS_OFF_MISC + 2048 + 1024;
 
-__global__ void __launch_bounds__(256)
-k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const BwdParams p) {
+__global__ void __launch_bounds__(256, 2)
+k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmDY,
+                 const __grid_constant__ CUtensorMap tmZ, const BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, hf = tid >> 7;
-    const int k = blockIdx.x, h = blockIdx.y;
+    const int k = blockIdx.x, HS = p.hs_ds, h0 = blockIdx.y * HS;
     if (k >= p.hdr[HDR_NCHUNKS] || p.hdr[HDR_STATUS] != 0) return;
     const ChunkInfo ci = p.chunks[k];
-    const int g = h / p.sh.hpg;
+    const int g = h0 / p.sh.hpg;
+    const bool has_z = p.z != nullptr;
     float *dtc = reinterpret_cast<float *>(sm + DS_OFF_MISC);
     float *cs2 = dtc + QT;
-    float *wsum = cs2 + QT;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(wsum + 8);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
+    float *wsum = cs2 + QT;                                        // 16
+    uint64_t *bar = reinterpret_cast<uint64_t *>(wsum + 16);       // 0: C, 1: dy/z, 2: MMA
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
+    auto stage_head = [&](int h) {   // one thread
+        mbar_expect_tx(&bar[1], X_BYTES * (has_z ? 2u : 1u));
+        tma_load_4d(sm + DS_OFF_ST, &tmDY, &bar[1], 0, h, ci.t0, ci.b);
+        if (has_z) tma_load_4d(sm + DS_OFF_ST + X_BYTES, &tmZ, &bar[1], 0, h, ci.t0, ci.b);
+    };
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
         mbar_expect_tx(&bar[0], BC_BYTES);
         tma_load_4d(sm + DS_OFF_C, &tmC, &bar[0], 0, g, ci.t0, ci.b);
         tma_load_4d(sm + DS_OFF_C + BC_BYTES / 2, &tmC, &bar[0], 64, g, ci.t0, ci.b);
+        stage_head(h0);
     }
+    auto load_dtv = [&](int h) -> float {
+        return tid < ci.len ? p.dt_raw[(int64_t)ci.b * p.sdb + (int64_t)(ci.t0 + tid) * p.sdl + h] +
+                                  (p.bias ? p.bias[h] : 0.f)
+                            : 0.f;
+    };
+    float dt_next = load_dtv(h0), A_next = p.A[h0];
     if (warp == 0) tmem_alloc(tslot, 64);
     tc_fence_before();
-    const float lam = chunk_scan_dt(p, ci, h, dtc, cs2, wsum);   // contains __syncthreads
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    if (tid == 0) p.chunk_lam[(int64_t)k * p.sh.H + h] = lam;
-    // (e o dyp) row `row`, half hf -> swizzled [l][p] tile
-    {
-        float v[32];
-        if (row < ci.len) {
-            const int64_t tok = (int64_t)ci.t0 + row;
-            float zz[32];
-            load_row32(p.dy + (int64_t)ci.b * p.sdyb + tok * p.sdyl + (int64_t)h * p.sdyh + 32 * hf, v);
-            const float el = ex2(cs2[row]);
-            if (p.z) {
-                load_row32(p.z + (int64_t)ci.b * p.szb + tok * p.szl + (int64_t)h * p.szh + 32 * hf, zz);
+    uint32_t st_done = 0, st_issued = 1, mma_phase = 0, c_done = 0;
+    int bad = 0;
+    const uint32_t sC = smem_u32(sm + DS_OFF_C), sY = smem_u32(sm + DS_OFF_Y);
+    for (int hi = 0; hi < HS; ++hi) {
+        const int h = h0 + hi;
+        const float vcur = dt_next, Ah = A_next;
+        {   // dt and the in-chunk cumulative log-decay (cs2 = cs log2 e); chunk total -> chunk_lam
+            const float dt = tid < ci.len ? softplus_f(vcur) : 0.f;
+            float tot;
+            const float cs = block_scan256(tid < QT ? dt * Ah : 0.f, wsum, &tot);
+            if (tid < QT) {
+                dtc[tid] = dt;
+                cs2[tid] = cs * LOG2E;
+            }
+            if (tid == 0) p.chunk_lam[(int64_t)k * p.sh.H + h] = tot;
+            __syncthreads();
+        }
+        if (!mbar_wait(&bar[1], st_done & 1)) bad = 1;
+        ++st_done;
+        {   // (e o dyp) row `row`, half hf -> swizzled [l][p] tile
+            float v[32];
+            load_row32_swz(sm + DS_OFF_ST + row * 128, row, hf, v);
+            const float el = row < ci.len ? ex2(cs2[row]) : 0.f;
+            if (has_z) {
+                float zz[32];
+                load_row32_swz(sm + DS_OFF_ST + X_BYTES + row * 128, row, hf, zz);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] *= silu_f(zz[i]) * el;
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] *= el;
             }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            store_row32_swz(sm + DS_OFF_Y + row * 128, row, hf, v);
         }
-        store_row32_swz(sm + DS_OFF_Y + row * 128, row, hf, v);
-    }
-    fence_proxy_async_smem();
-    const bool ok = mbar_wait(&bar[0], 0);
-    __syncthreads();
-    if (ok && tid == 0) {
+        fence_proxy_async_smem();
+        if (__syncthreads_or(bad)) break;
+        if (tid == 0) {
+            if (hi + 1 < HS) stage_head(h + 1);   // the staged tiles are read
+            if (hi == 0) {
+                if (!mbar_wait(&bar[0], 0)) bad = 1;
+                ++c_done;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < QT / 16; ++kk)
+                umma_bf16(tmem, mnmaj(sC, kk, BC_BYTES / 2), mnmaj(sY, kk, 16384u), idesc_bf16(128, 64, 1, 1), kk > 0);
+            umma_commit(&bar[2]);
+        }
+        if (hi + 1 < HS) {
+            ++st_issued;
+            dt_next = load_dtv(h + 1);
+            A_next = p.A[h + 1];
+        }
+        if (!mbar_wait(&bar[2], mma_phase & 1)) bad = 1;
+        ++mma_phase;
         tc_fence_after();
-        const uint32_t sC = smem_u32(sm + DS_OFF_C), sY = smem_u32(sm + DS_OFF_Y);
+        {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + 32 * hf, v);
+            tmem_wait_ld();
+            float *dst = p.dS_loc + ((int64_t)k * p.sh.H + h) * (PT * NT) + (int64_t)(32 * hf) * NT + row;
 #pragma unroll
-        for (int kk = 0; kk < QT / 16; ++kk)
-            umma_bf16(tmem, mnmaj(sC, kk, BC_BYTES / 2), mnmaj(sY, kk, 16384u), idesc_bf16(128, 64, 1, 1), kk > 0);
-        umma_commit(&bar[1]);
+            for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = v[i];
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     }
-    bool ok2 = ok && mbar_wait(&bar[1], 0);
-    if (!ok || !ok2) set_status(const_cast<int32_t *>(p.hdr), SSD_ERR_DEVICE_TIMEOUT);
-    tc_fence_after();
-    if (ok2) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + 32 * hf, v);
-        tmem_wait_ld();
-        float *dst = p.dS_loc + ((int64_t)k * p.sh.H + h) * (PT * NT) + (int64_t)(32 * hf) * NT + row;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = v[i];
-    }
+    if (bad) set_status(const_cast<int32_t *>(p.hdr), SSD_ERR_DEVICE_TIMEOUT);
+    for (uint32_t q = st_done; q < st_issued; ++q) mbar_wait(&bar[1], q & 1);
+    if (tid == 0 && c_done == 0) mbar_wait(&bar[0], 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -843,6 +867,7 @@ static BwdParams make_params(const Shape &sh, const int32_t *hdr, const ChunkInf
     p.ddt = a.ddt; p.sddb = a.sddb; p.sddl = a.sddl;
     p.dS = a.dS; p.dS_loc = a.dS; p.chunk_lam = a.chunk_lam; p.dBh = a.dBh; p.dCh = a.dCh; p.partials = a.partials;
     p.hs = a.hs;
+    p.hs_ds = a.hs_ds;
     p.dB = (__nv_bfloat16 *)a.dB; p.dC = (__nv_bfloat16 *)a.dC;
     p.sdBb = a.sdB ? a.sdB[0] : 0; p.sdBl = a.sdB ? a.sdB[1] : 0; p.sdBg = a.sdB ? a.sdB[2] : 0;
     p.sdCb = a.sdC ? a.sdC[0] : 0; p.sdCl = a.sdC ? a.sdC[1] : 0; p.sdCg = a.sdC ? a.sdC[2] : 0;
@@ -851,13 +876,19 @@ static BwdParams make_params(const Shape &sh, const int32_t *hdr, const ChunkInf
 
 cudaError_t launch_bwd_dstates_tc(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const BwdTcArgs &a,
                                   cudaStream_t st) {
-    CUtensorMap mc;
+    CUtensorMap mc, mdy, mz;
     if (!map4(&mc, a.Cp, NT, sh.G, sh.L, sh.B, a.sc[2], a.sc[1], a.sc[0], QT)) return cudaErrorInvalidValue;
+    if (!map4(&mdy, a.dy, PT, sh.H, sh.L, sh.B, a.sdy[2], a.sdy[1], a.sdy[0], QT)) return cudaErrorInvalidValue;
+    if (a.z != nullptr) {
+        if (!map4(&mz, a.z, PT, sh.H, sh.L, sh.B, a.sz[2], a.sz[1], a.sz[0], QT)) return cudaErrorInvalidValue;
+    } else {
+        mz = mdy;   // not read
+    }
     BwdParams p = make_params(sh, hdr, chunks, a);
     static int attr_done[64] = {0};
     cudaError_t e = ensure_smem_attr(k_bwd_dstates_tc, (int)DS_SMEM, attr_done);
     if (e != cudaSuccess) return e;
-    k_bwd_dstates_tc<<<dim3(sh.kmax, sh.H), 256, DS_SMEM, st>>>(mc, p);
+    k_bwd_dstates_tc<<<dim3(sh.kmax, sh.H / a.hs_ds), 256, DS_SMEM, st>>>(mc, mdy, mz, p);
     return cudaGetLastError();
 }
 

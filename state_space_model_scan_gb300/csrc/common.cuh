@@ -61,6 +61,7 @@ struct BwdTcArgs {
     const __nv_bfloat16 *states;   // [chunk][H][P][N] bf16 carried states
     float *dS, *chunk_lam, *dBh, *dCh, *partials;
     int hs;                         // heads per CTA of the gradient kernel (divides H/G)
+    int hs_ds;                      // heads per CTA of the dstates kernel (divides H/G)
     void *dB, *dC;                  // final dB/dC (written directly when hs == H/G)
     const int64_t *sdB, *sdC;
 };

@@ -99,64 +99,52 @@ k_chunk_state(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__rest
 }
 
 // ---------------------------------------------------------------------------- a4
-// Inter-chunk scan with warp shuffles.  grid (S*H, ceil(P*N/256)), block 256.
-// Warp w owns 32 consecutive state elements; it stages 32 chunks x 32 elements
-// through shared memory (coalesced rows), then for each element scans the 32
-// affine maps s -> a_j s + S_j across lanes (lane = chunk), composing
-// (a1, b1) then (a2, b2) into (a1 a2, a2 b1 + b2).  In place: S_c is replaced by
-// the chunk's carry-in state.  The carry after the last chunk is the final state.
-// The chunk's total log-decay is lamw[(chunk * H + h) * lam_stride].
-// With reverse = 1 the chunks are visited last to first: that is the backward
-// recursion dS_out[c] = exp(cs_{c+1}[Q-1]) dS_out[c+1] + dS_loc[c+1] (same affine
-// form, the chunk's own decay), with `init` = dfinal and `final_` = dinit.
+// Inter-chunk scan: sequential over the chunks of a sequence, parallel over the
+// state elements.  grid (S*H, ceil(P*N/256)), block 256; thread = one element
+// (p, n) of (sequence, head), its running carry in a register.  In place: the
+// chunk's local state S_c is replaced by the carry entering the chunk, and
+//   carry <- exp(lam_c) carry + S_c
+// passes the chunk; the carry after the last chunk is the final state.  Per batch
+// of 32 chunks each lane holds one chunk's decay exp(lam_c) in a register and the
+// warp broadcasts it with a shuffle at every step; the batch's 32 loads of S_c are
+// issued ahead of the recurrence (they do not depend on the carry), so a warp keeps
+// 32 coalesced 128-byte rows in flight.  The chunk's total log-decay is
+// lamw[(chunk * H + h) * lam_stride].  With reverse = 1 the chunks are visited last
+// to first: that is the backward recursion dS_out[c] = exp(cs_{c+1}[Q-1]) dS_out[c+1]
+// + dS_loc[c+1] (same affine form, the chunk's own decay), with `init` = dfinal and
+// `final_` = dinit.
 __global__ void __launch_bounds__(256)
 k_state_passing(Shape sh, const int32_t *__restrict__ hdr, const SeqInfo *__restrict__ seqs,
                 const float *__restrict__ lamw, int lam_stride, float *__restrict__ states,
                 const float *__restrict__ init, float *__restrict__ final_, int reverse) {
-    __shared__ float tile[8][32][33];
     if (hdr[HDR_STATUS] != 0) return;
-    const int sh_idx = blockIdx.x;
-    const int s = sh_idx / sh.H, h = sh_idx % sh.H;
-    const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+    const int s = blockIdx.x / sh.H, h = blockIdx.x % sh.H;
     const int PN = sh.P * sh.N;
-    const int e0 = (blockIdx.y * 8 + wp) * 32;
-    if (e0 >= PN) return;
+    const int e = blockIdx.y * 256 + threadIdx.x, lane = threadIdx.x & 31;
+    if (blockIdx.y * 256 + (threadIdx.x & ~31) >= PN) return;   // whole warp past the end
     const SeqInfo si = seqs[s];
     const int nch = (si.len + sh.Q - 1) / sh.Q;
     const int64_t sbase = ((int64_t)s * sh.H + h) * PN;
-    // lane c keeps the running carry of element e0 + c
-    float carry = init ? init[sbase + e0 + lane] : 0.f;
-    float (*tl)[33] = tile[wp];
+    const bool act = e < PN;
+    float carry = (init != nullptr && act) ? init[sbase + e] : 0.f;
     auto chunk_of = [&](int pos) { return reverse ? si.chunk0 + nch - 1 - pos : si.chunk0 + pos; };
+    auto slot = [&](int pos) { return ((int64_t)chunk_of(pos) * sh.H + h) * PN + e; };
     for (int c0 = 0; c0 < nch; c0 += 32) {
         const int nc = min(32, nch - c0);
-        for (int r = 0; r < nc; ++r)
-            tl[r][lane] = states[((int64_t)chunk_of(c0 + r) * sh.H + h) * PN + e0 + lane];
-        const float dec = (lane < nc)
-            ? expf(lamw[((int64_t)chunk_of(c0 + lane) * sh.H + h) * lam_stride]) : 1.f;
-        __syncwarp();
-        for (int col = 0; col < 32; ++col) {
-            float a = dec, b = (lane < nc) ? tl[lane][col] : 0.f;
+        const float mydec = lane < nc ? expf(lamw[((int64_t)chunk_of(c0 + lane) * sh.H + h) * lam_stride]) : 0.f;
+        float v[32];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                float ap = __shfl_up_sync(0xffffffffu, a, o);
-                float bp = __shfl_up_sync(0xffffffffu, b, o);
-                if (lane >= o) { b = a * bp + b; a = a * ap; }
+        for (int j = 0; j < 32; ++j) v[j] = (act && j < nc) ? states[slot(c0 + j)] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float d = __shfl_sync(0xffffffffu, mydec, j);
+            if (j < nc) {
+                if (act) states[slot(c0 + j)] = carry;   // carry entering the chunk
+                carry = fmaf(d, carry, v[j]);
             }
-            const float cin = __shfl_sync(0xffffffffu, carry, col);
-            float ae = __shfl_up_sync(0xffffffffu, a, 1);
-            float be = __shfl_up_sync(0xffffffffu, b, 1);
-            if (lane == 0) { ae = 1.f; be = 0.f; }
-            if (lane < nc) tl[lane][col] = ae * cin + be;        // carry-in of chunk c0 + lane
-            const float a31 = __shfl_sync(0xffffffffu, a, 31), b31 = __shfl_sync(0xffffffffu, b, 31);
-            if (lane == col) carry = a31 * cin + b31;
         }
-        __syncwarp();
-        for (int r = 0; r < nc; ++r)
-            states[((int64_t)chunk_of(c0 + r) * sh.H + h) * PN + e0 + lane] = tl[r][lane];
-        __syncwarp();
     }
-    if (final_) final_[sbase + e0 + lane] = carry;
+    if (final_ != nullptr && act) final_[sbase + e] = carry;
 }
 
 // ---------------------------------------------------------------------------- a5
