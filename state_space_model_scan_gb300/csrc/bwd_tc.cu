@@ -72,21 +72,6 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k, uint32_t mn_atom
 __device__ __forceinline__ float silu_f(float z) { return z * rcp(1.f + ex2(-z * LOG2E)); }
 __device__ __forceinline__ float sig_f(float z) { return rcp(1.f + ex2(-z * LOG2E)); }
 
-// Loads 32 bf16 (64 bytes) of a row into floats.
-__device__ __forceinline__ void load_row32(const __nv_bfloat16 *src, float *v) {
-    const uint4 *s = reinterpret_cast<const uint4 *>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u = __ldg(s + q);
-        const __nv_bfloat162 *e = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 f = __bfloat1622float2(e[i]);
-            v[q * 8 + 2 * i] = f.x;
-            v[q * 8 + 2 * i + 1] = f.y;
-        }
-    }
-}
 // Writes 32 floats as bf16 into the 4 chunks (4*hf .. 4*hf+3) of a 128-byte swizzled row.
 __device__ __forceinline__ void store_row32_swz(uint8_t *row_base, int row, int hf, const float *v) {
 #pragma unroll

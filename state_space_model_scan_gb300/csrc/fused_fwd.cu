@@ -50,7 +50,6 @@ constexpr int NTHR = 128; // one thread per tile row / TMEM lane
 
 constexpr uint32_t X_BYTES = QT * PT * 2;    // 16 KB
 constexpr uint32_t BC_BYTES = QT * NT * 2;   // 32 KB
-constexpr uint32_t S_BYTES = PT * NT * 2;    // 16 KB
 
 // Shared memory (offsets from a 1024-aligned base), about 102 KB so that two CTAs
 // share an SM and fill each other's load / tensor-core waits.
@@ -66,7 +65,8 @@ constexpr uint32_t OFF_DTU = OFF_W + X_BYTES;      // 98304
 constexpr uint32_t OFF_WU = OFF_DTU + RMAX * QT * 4;
 constexpr uint32_t OFF_CS2 = OFF_WU + RMAX * QT * 4;    // chunk-local cumsum * log2 e, every chunk of the unit
 constexpr uint32_t OFF_CF = OFF_CS2 + RMAX * QT * 4;     // per-column decay factors of the M build, every chunk
-constexpr uint32_t OFF_MISC = OFF_CF + RMAX * QT * 4;
+constexpr uint32_t OFF_DTN = OFF_CF + RMAX * QT * 4;     // raw dt of the next unit (cp.async during the fold)
+constexpr uint32_t OFF_MISC = OFF_DTN + RMAX * QT * 4;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 256 + 1024;   // + alignment slack
 
 // TMEM columns (256 per CTA)
@@ -106,26 +106,12 @@ enum { BAR_X = 0, BAR_B = 1, BAR_C = 2, BAR_MMA = 3, BAR_Z = 4, NBAR = 5 };
 struct Misc {
     uint64_t bar[NBAR];
     uint32_t tmem_base;
-    int ticket;
+    int tnext;        // ticket of the next unit (taken at the start of the current one)
     int abort_;
     float wsum[4];
+    float A_next, bias_next;   // A and dt_bias of the next unit's head (cp.async)
+    UnitInfo ui_next;
 };
-
-__device__ __forceinline__ float block_scan(float v, float *wsum, float *total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    float x = warp_incl_sum(v);
-    if (lane == 31) wsum[w] = x;
-    __syncthreads();
-    float off = 0.f, tot = 0.f;
-#pragma unroll
-    for (int i = 0; i < NTHR / 32; ++i) {
-        if (i < w) off += wsum[i];
-        tot += wsum[i];
-    }
-    *total = tot;
-    __syncthreads();
-    return x + off;
-}
 
 // silu(z) = z sigmoid(z), sigmoid(z) = (1 + tanh(z/2)) / 2 (one tanh.approx).
 __device__ __forceinline__ float silu_tanh(float z) {
@@ -133,6 +119,12 @@ __device__ __forceinline__ float silu_tanh(float z) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
     return 0.5f * z * (1.f + t);
 }
+
+// 4-byte asynchronous global -> shared copy (completion: cp_async_wait_all by the issuing thread).
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // K-major SW128 operand: rows of 64 bf16 (128 B), atom columns of `col_bytes`.
 __device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t col_bytes) {
@@ -187,6 +179,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     float *wu = reinterpret_cast<float *>(sm + OFF_WU);
     float *cs2u = reinterpret_cast<float *>(sm + OFF_CS2);
     float *cfu = reinterpret_cast<float *>(sm + OFF_CF);
+    float *dtn = reinterpret_cast<float *>(sm + OFF_DTN);
     uint8_t *Xs = sm + OFF_X, *Bs = sm + OFF_B, *Cs = sm + OFF_C, *Ws = sm + OFF_W;
     const Shape sh = p.sh;
 
@@ -262,48 +255,96 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 
     const uint32_t idesc_cb = idesc_bf16(128, 128, 0, 0);
     const uint32_t idesc_sc = idesc_bf16(128, 64, 1, 1);
-    const uint32_t idesc_yo = idesc_bf16(128, 64, 0, 0);
+    const uint32_t idesc_yo = idesc_bf16(128, 64, 0, 1);
     const uint32_t idesc_yd = idesc_bf16(128, 64, 0, 1);
     const uint32_t sX = smem_u32(Xs), sB = smem_u32(Bs), sC = smem_u32(Cs), sW = smem_u32(Ws);
     const int64_t unit_stride = (int64_t)NT * PT;   // floats per (unit, head) aggregate
 
+    // Inputs of a unit's dt prologue, fetched ahead by cp.async: thread (warp w, lane j)
+    // copies raw dt of chunk w, positions 4j..4j+3 (the values it scans), thread 0 A and dt_bias.
+    const int lane = tid & 31;
+    auto fetch_unit_inputs = [&](const UnitInfo &un, int hn) {
+        if (warp < un.nchunk) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int pos = warp * QT + 4 * lane + i;
+                if (pos < un.len)
+                    cp_async4(dtn + pos, p.dt_raw + (int64_t)un.b * p.sdb + (int64_t)(un.t0 + pos) * p.sdl + hn);
+            }
+        }
+        if (tid == 0) {
+            cp_async4(&ms->A_next, p.A + hn);
+            if (p.bias) cp_async4(&ms->bias_next, p.bias + hn);
+        }
+    };
+    if (tid == 0) {
+        ms->tnext = atomicAdd(&p.hdr[HDR_TICKET], 1);
+        if (ms->tnext < total) ms->ui_next = p.units[ms->tnext / sh.H];
+    }
+    __syncthreads();
+    int ticket = ms->tnext;
+    if (ticket < total) fetch_unit_inputs(ms->ui_next, ticket % sh.H);
+
     for (;;) {
-        if (tid == 0) ms->ticket = atomicAdd(&p.hdr[HDR_TICKET], 1);
         __syncthreads();
-        const int ticket = ms->ticket;
         if (ticket >= total || ms->abort_) break;
         const int u = ticket / sh.H, h = ticket % sh.H, g = h / sh.hpg;
-        const UnitInfo ui = p.units[u];
-        const float Ah = p.A[h];
-        const int ntok = ui.nchunk * QT;
+        const UnitInfo ui = ms->ui_next;
+        __syncthreads();   // ui_next and tnext read: the next unit's may be written
+        if (tid == 0) ms->tnext = atomicAdd(&p.hdr[HDR_TICKET], 1);   // fetched during the fold
 
         // phase-1 loads of the first two chunks go out first: stage 0 = (X, B), stage 1 = (W, C)
         load_xb(BAR_X, Xs, Bs, h, g, ui.t0, ui.b);
         if (ui.nchunk > 1) load_xb(BAR_C, Ws, Cs, h, g, ui.t0 + QT, ui.b);
 
-        // ---- dt over the unit, unit-level cumulative log-decay, phase-1 weights
-        for (int i = tid; i < ntok; i += NTHR) {
-            float dt = 0.f;
-            if (i < ui.len) {
-                float v = p.dt_raw[(int64_t)ui.b * p.sdb + (int64_t)(ui.t0 + i) * p.sdl + h] + (p.bias ? p.bias[h] : 0.f);
-                dt = softplus_f(v);
+        // ---- dt over the unit, chunk-local and unit-level cumulative log-decay, phase-1 weights.
+        // Warp w scans chunk w (four positions per lane); chunk totals meet in smem.
+        cp_async_wait_all();
+        __syncthreads();
+        const float Ah = ms->A_next;
+        float lam_u;
+        {
+            const float bias = p.bias ? ms->bias_next : 0.f;
+            const bool wact = warp < ui.nchunk;
+            float dt4[4], loc[4], run = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int pos = warp * QT + 4 * lane + i;
+                dt4[i] = (wact && pos < ui.len) ? softplus_f(dtn[pos] + bias) : 0.f;
+                run += dt4[i] * Ah;
+                loc[i] = run;
             }
-            dtu[i] = dt;
+            const float incl = warp_incl_sum(run);
+            const float excl = incl - run;
+            const float ctot = __shfl_sync(0xffffffffu, incl, 31);
+            if (lane == 0) ms->wsum[warp] = wact ? ctot : 0.f;
+            __syncthreads();
+            float off = 0.f, tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < NTHR / 32; ++w) {
+                const float t = ms->wsum[w];
+                if (w < warp) off += t;
+                tot += t;
+            }
+            lam_u = tot;
+            const float last = __shfl_sync(0xffffffffu, excl + loc[3], lane | 7);   // cs at the 32-block's end
+            if (wact) {
+                float pc[4], pw[4], pf[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float cs = excl + loc[i];
+                    pc[i] = cs * LOG2E;
+                    pw[i] = dt4[i] * ex2((lam_u - (off + cs)) * LOG2E);
+                    pf[i] = dt4[i] * ex2((last - cs) * LOG2E);
+                }
+                const int b4 = warp * QT + 4 * lane;
+                *reinterpret_cast<float4 *>(dtu + b4) = make_float4(dt4[0], dt4[1], dt4[2], dt4[3]);
+                *reinterpret_cast<float4 *>(cs2u + b4) = make_float4(pc[0], pc[1], pc[2], pc[3]);
+                *reinterpret_cast<float4 *>(wu + b4) = make_float4(pw[0], pw[1], pw[2], pw[3]);
+                *reinterpret_cast<float4 *>(cfu + b4) = make_float4(pf[0], pf[1], pf[2], pf[3]);
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        float carry = 0.f;
-        for (int c = 0; c < ui.nchunk; ++c) {
-            float tot;
-            const float v = block_scan(dtu[c * QT + tid] * Ah, ms->wsum, &tot);
-            wu[c * QT + tid] = carry + v;
-            cs2u[c * QT + tid] = v * LOG2E;   // chunk-local inclusive cumsum (phase 2)
-            carry += tot;
-        }
-        const float lam_u = carry;
-        for (int i = tid; i < ntok; i += NTHR) wu[i] = dtu[i] * ex2((lam_u - wu[i]) * LOG2E);
-        __syncthreads();
-        // column factors of the M build: cf[s] = dt[s] exp(cs[end of s's 32-block] - cs[s]) <= dt[s]
-        for (int i = tid; i < ntok; i += NTHR) cfu[i] = dtu[i] * ex2(cs2u[i | 31] - cs2u[i]);
 
         // ---- phase 1: unit aggregate^T[n][p] = sum_l B[l][n] (w o x)[l][p], double-buffered
         for (int c = 0; c < ui.nchunk; ++c) {
@@ -356,6 +397,15 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         load_bc(BAR_B, &tmB, Bs, g, ui.t0, ui.b);
         if (full) load_bc(BAR_C, &tmC, Cs, g, ui.t0, ui.b);
 
+        {   // the next unit: its UnitInfo and dt inputs travel while this one folds and runs phase 2
+            const int tn = ms->tnext;
+            if (tn < total) {
+                const UnitInfo un = p.units[tn / sh.H];
+                if (tid == 0) ms->ui_next = un;
+                fetch_unit_inputs(un, tn % sh.H);
+            }
+            ticket = tn;
+        }
         // ---- carry-in state of the unit (row n, all 64 columns p)
         // P_j = sum_{i=b0}^{j-1} exp(lam_{i+1} + .. + lam_{j-1}) agg_i + exp(lam_{b0} + .. + lam_{j-1}) E,
         // E = end state of unit b0-1 (published by it) or the initial state when b0 = 0.
@@ -430,37 +480,43 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                 for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(s_run[i]);
             }
-            wait_bar(BAR_X);
             wait_bar(BAR_B);
-            if (full) wait_bar(BAR_C);
-            __syncthreads();   // tiles landed
+            if (full) {   // CB = C B^T (K = state dim) runs while x is scaled; committed with S_c below
+                wait_bar(BAR_C);
+                if (tid == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < NT / 16; ++k)
+                        umma_bf16(tmem + TM_CB, kmaj(sC, k, BC_BYTES / 2), kmaj(sB, k, BC_BYTES / 2), idesc_cb, k > 0);
+                }
+            }
+            wait_bar(BAR_X);
             // W = w o x, w[l] = dt[l] exp(cs[Q-1] - cs[l])
             scale_row(Xs + row * 128, Ws + row * 128, row, dtc[row] * ex2(cs2[QT - 1] - cs2[row]));
             fence_proxy_async_smem();
             __syncthreads();
-            if (ms->abort_) break;
+            if (ms->abort_) {
+                if (full) commit();   // the CB MMAs are in flight: the drain waits for them
+                break;
+            }
             if (tid == 0) {
                 tc_fence_after();
-                if (full) {
-#pragma unroll
-                    for (int k = 0; k < NT / 16; ++k)   // CB = C B^T (K = state dim)
-                        umma_bf16(tmem + TM_CB, kmaj(sC, k, BC_BYTES / 2), kmaj(sB, k, BC_BYTES / 2), idesc_cb, k > 0);
-                }
 #pragma unroll
                 for (int k = 0; k < QT / 16; ++k)   // S_c^T = B^T (w o x) (K = tokens)
                     umma_bf16(tmem + TM_SC, mnmaj(sB, k), mnmaj(sW, k), idesc_sc, k > 0);
             }
-            commit();
-            wait_bar(BAR_MMA);
+            commit();   // one barrier phase per commit, waited before the next commit: a parity
+            wait_bar(BAR_MMA);   // wait cannot tell a barrier two phases ahead from one behind
             if (full) {
-                // S_in (bf16, K-major [p][n]) over the w o x buffer, then Y_off = C S_in^T
+                // S_in (bf16, MN-major [n][p]: row n = this thread's 64 columns) over the w o x
+                // buffer, then Y_off = C S_in^T
                 {
-                    const int n = row, ac = n >> 6, cn = (n & 63) >> 3;
-                    uint8_t *base = Ws + ac * (S_BYTES / 2) + (n & 7) * 2;
+                    uint8_t *rowp = Ws + row * 128;
 #pragma unroll
-                    for (int pp = 0; pp < 64; ++pp)
-                        *reinterpret_cast<__nv_bfloat16 *>(base + pp * 128 + ((cn ^ (pp & 7)) << 4)) =
-                            __float2bfloat16_rn(s_run[pp]);
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<uint4 *>(rowp + ((q ^ (row & 7)) << 4)) =
+                            make_uint4(pack_bf16(s_run[8 * q], s_run[8 * q + 1]), pack_bf16(s_run[8 * q + 2], s_run[8 * q + 3]),
+                                       pack_bf16(s_run[8 * q + 4], s_run[8 * q + 5]), pack_bf16(s_run[8 * q + 6], s_run[8 * q + 7]));
                 }
                 fence_proxy_async_smem();
                 __syncthreads();
@@ -468,7 +524,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < NT / 16; ++k)   // Y_off = C S_in^T (K = state dim)
-                        umma_bf16(tmem + TM_YO, kmaj(sC, k, BC_BYTES / 2), kmaj(sW, k, S_BYTES / 2), idesc_yo, k > 0);
+                        umma_bf16(tmem + TM_YO, kmaj(sC, k, BC_BYTES / 2), mnmaj(sW, k), idesc_yo, k > 0);
                 }
                 commit();
                 // M (bf16, K-major [l][s], D on the diagonal) into the B buffer while Y_off runs
@@ -599,6 +655,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     }
     // Drain (only non-empty after an early stop): bounded waits for loads and
     // MMAs still in flight, so nothing lands in shared memory or TMEM after exit.
+    cp_async_wait_all();
     for (int b_ = 0; b_ < NBAR; ++b_)
         for (uint32_t q = done[b_]; q < issued[b_]; ++q) mbar_wait(&ms->bar[b_], q & 1);
     tc_fence_before();
