@@ -299,8 +299,8 @@ constexpr uint32_t BWD_SMEM = O_MISC + F_END * 4 + 64 + 1024;
 // group's heads) is computed once; columns 384.. serve each head's three MMA groups.
 constexpr uint32_t T_DB = 0, T_DC = 128, T_CB = 256;      // whole CTA
 constexpr uint32_t T_DM = 384;                            // group 1
-constexpr uint32_t T_DXD = 384, T_DXS = 448;              // group 2 (+ dB, dC)
-constexpr uint32_t T_YD = 384, T_YO = 448;                // group 3 (+ dC)
+constexpr uint32_t T_DXD = 384, T_DXS = 448;              // group 2
+constexpr uint32_t T_YD = 384, T_YO = 448;                // group 3 (+ dB, dC)
 
 // grid (kmax, H / HS): one chunk and HS heads of one group per CTA (HS divides H/G).
 // B and C are loaded once.  Every per-head input arrives one head ahead: dy, z and
@@ -325,7 +325,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     const bool has_z = p.z != nullptr;
     float *fm = reinterpret_cast<float *>(sm + O_MISC);
     float *cs2 = fm + F_CS2, *dtc = fm + F_DT, *wst = fm + F_W;
-    // 0: B/C, 1: x/S_in, 2: MMA (dx and y tiles), 3: dy/z/dS, 4: MMA (dB/dC chains of group 2)
+    // 0: B/C, 1: x/S_in, 2: MMA (dx and y tiles), 3: dy/z/dS, 4: MMA (dB/dC chains)
     uint64_t *bar = reinterpret_cast<uint64_t *>(fm + F_END);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
     auto load_head = [&](int h) {   // one thread: x and S_in
@@ -587,7 +587,6 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         __syncthreads();
         if (tid == 0) {   // group 2
             tc_fence_after();
-            const uint32_t first = hi == 0 ? 0u : 1u;
 #pragma unroll
             for (int kk = 0; kk < QT / 16; ++kk)   // dx_diag[s][p] = sum_l M[l][s] dyp[l][p]
                 umma_bf16(tmem + T_DXD, mnmaj(sM, kk, BC_BYTES / 2), mnmaj(sDY, kk, 16384u), idesc_bf16(128, 64, 1, 1),
@@ -596,19 +595,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             for (int kk = 0; kk < NT / 16; ++kk)   // u[s][p] = sum_n B[s][n] dS[p][n]
                 umma_bf16(tmem + T_DXS, kmaj(sB, kk, BC_BYTES / 2), kmaj(sSD, kk, S_BYTES / 2), idesc_bf16(128, 64, 0, 0),
                           kk > 0);
-            umma_commit(&bar[2]);   // the dx tiles; the dB/dC chains below run on during the dx epilogue
-#pragma unroll
-            for (int kk = 0; kk < QT / 16; ++kk)   // dB[s][n] (+)= sum_l E'[l][s] C[l][n]
-                umma_bf16(tmem + T_DB, mnmaj(sE, kk, BC_BYTES / 2), mnmaj(sC, kk, BC_BYTES / 2),
-                          idesc_bf16(128, 128, 1, 1), (kk > 0) ? 1u : first);
-#pragma unroll
-            for (int kk = 0; kk < PT / 16; ++kk)   // dB[s][n] += sum_p (w o x)[s][p] dS[p][n]
-                umma_bf16(tmem + T_DB, kmaj(sWX, kk, X_BYTES), mnmaj(sSD, kk, S_BYTES / 2), idesc_bf16(128, 128, 0, 1), 1);
-#pragma unroll
-            for (int kk = 0; kk < QT / 16; ++kk)   // dC[l][n] (+)= sum_s E'[l][s] B[s][n]
-                umma_bf16(tmem + T_DC, kmaj(sE, kk, BC_BYTES / 2), mnmaj(sB, kk, BC_BYTES / 2),
-                          idesc_bf16(128, 128, 0, 1), (kk > 0) ? 1u : first);
-            umma_commit(&bar[4]);
+            umma_commit(&bar[2]);
         }
         wait_mma();
         if (hi + 1 < HS) {
@@ -650,31 +637,33 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         if (tid == 0) {   // group 3
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < PT / 16; ++kk)   // dC[l][n] += sum_p (e o dyp)[l][p] S_in[p][n]
-                umma_bf16(tmem + T_DC, kmaj(sDY, kk, X_BYTES), mnmaj(sSI, kk, S_BYTES / 2), idesc_bf16(128, 128, 0, 1), 1);
-#pragma unroll
             for (int kk = 0; kk < QT / 16; ++kk)   // Y_diag[l][p] = sum_s M[l][s] x[s][p]
                 umma_bf16(tmem + T_YD, kmaj(sM, kk, BC_BYTES / 2), mnmaj(sX, kk, 16384u), idesc_bf16(128, 64, 0, 1), kk > 0);
 #pragma unroll
             for (int kk = 0; kk < NT / 16; ++kk)   // Ybar[l][p] = sum_n C[l][n] S_in[p][n]
                 umma_bf16(tmem + T_YO, kmaj(sC, kk, BC_BYTES / 2), kmaj(sSI, kk, S_BYTES / 2), idesc_bf16(128, 64, 0, 0),
                           kk > 0);
-            umma_commit(&bar[2]);
+            umma_commit(&bar[2]);   // the y tiles; the dB/dC chains below run on during the dz epilogue
+            const uint32_t first = hi == 0 ? 0u : 1u;   // dB, dC start at the CTA's first head
+#pragma unroll
+            for (int kk = 0; kk < QT / 16; ++kk)   // dB[s][n] (+)= sum_l E'[l][s] C[l][n]
+                umma_bf16(tmem + T_DB, mnmaj(sE, kk, BC_BYTES / 2), mnmaj(sC, kk, BC_BYTES / 2),
+                          idesc_bf16(128, 128, 1, 1), (kk > 0) ? 1u : first);
+#pragma unroll
+            for (int kk = 0; kk < PT / 16; ++kk)   // dB[s][n] += sum_p (w o x)[s][p] dS[p][n]
+                umma_bf16(tmem + T_DB, kmaj(sWX, kk, X_BYTES), mnmaj(sSD, kk, S_BYTES / 2), idesc_bf16(128, 128, 0, 1), 1);
+#pragma unroll
+            for (int kk = 0; kk < QT / 16; ++kk)   // dC[l][n] (+)= sum_s E'[l][s] B[s][n]
+                umma_bf16(tmem + T_DC, kmaj(sE, kk, BC_BYTES / 2), mnmaj(sB, kk, BC_BYTES / 2),
+                          idesc_bf16(128, 128, 0, 1), (kk > 0) ? 1u : first);
+#pragma unroll
+            for (int kk = 0; kk < PT / 16; ++kk)   // dC[l][n] += sum_p (e o dyp)[l][p] S_in[p][n]
+                umma_bf16(tmem + T_DC, kmaj(sDY, kk, X_BYTES), mnmaj(sSI, kk, S_BYTES / 2), idesc_bf16(128, 128, 0, 1), 1);
+            umma_commit(&bar[4]);
         }
         wait_mma();
-        wait_mma2();   // done with the group above: no MMA reads smem now
-        // this head's x row, then E', w o x, dS, x and S_in are free: fetch the next head's inputs
         float xv[32];
         load_row32_swz(sm + O_X + row * 128, row, hf, xv);
-        __syncthreads();
-        if (hi + 1 < HS) {
-            if (tid == 0) {
-                stage_head(h + 1);
-                load_head(h + 1);
-            }
-            ++st_issued;
-            ++ld_issued;
-        }
         {   // ypre -> dz; T2 row sums
             float yd[32], yb[32], ev[32];
             tmem_ld32(tmem + lb + T_YD + 32 * hf, yd);
@@ -701,7 +690,17 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             const float w = warp_sum(t3p);
             if (lane == 0) fm[F_RED + warp] = w;
         }
+        wait_mma2();   // the dB/dC chains are done: no MMA reads smem now
         __syncthreads();
+        // E', w o x, dS, x and S_in are free: fetch the next head's inputs
+        if (hi + 1 < HS) {
+            if (tid == 0) {
+                stage_head(h + 1);
+                load_head(h + 1);
+            }
+            ++st_issued;
+            ++ld_issued;
+        }
         {   // ---- per-position scalars (threads 0..127 = position i)
             const int i = tid;
             float dcs = 0.f, ddir = 0.f, t4 = 0.f;
