@@ -9,14 +9,24 @@ sequence's first token, so no chunk mixes two sequences):
   t0 = 0, len = L; packed: b = 0, t0 = cu[s], len = cu[s+1] - cu[s]);
 * its chunks are [t0 + c Q, t0 + min((c+1) Q, len)) for c = 0 .. ceil(len/Q)-1,
   listed sequence by sequence -> rows (seq, b, first token, length);
-* its work units group R consecutive chunks: unit (s, j) covers chunks
-  j R .. min((j+1) R, nchunks)-1; segments j are grouped in blocks of KB;
+* its work units group consecutive chunks: a sequence of n chunks has
+  m = max(ceil(n/R), min(n, ceil(n num/den))) units (num/den = 1/R unless given),
+  unit j holding floor(n/m) chunks plus one more for j < n mod m, so unit j starts
+  at chunk j floor(n/m) + min(j, n mod m); segments j are grouped in blocks of KB;
   units are listed by (block, s, j) -> rows (seq, b, first token, token count,
   chunk count, index of unit (s, j-1) or -1, 1 if last unit of s, j).
 """
 
 
-def build(cu=None, batch=1, seqlen=0, Q=64, R=1, KB=8):
+def seg_count(n, R, num, den):
+    if n <= 0:
+        return 0
+    return max(-(-n // R), min(n, -(-(n * num) // den)))
+
+
+def build(cu=None, batch=1, seqlen=0, Q=64, R=1, KB=8, num=None, den=None):
+    if num is None:
+        num, den = 1, R
     if cu is None:
         seqs = [(b, 0, seqlen) for b in range(batch)]
     else:
@@ -30,13 +40,16 @@ def build(cu=None, batch=1, seqlen=0, Q=64, R=1, KB=8):
             chunks.append((s, b, t0 + c * Q, min(Q, n - c * Q)))
     units = []
     last = {}
-    nseg = [-(-(-(-n // Q)) // R) for (_, _, n) in seqs]
+    nseg = [seg_count(-(-n // Q), R, num, den) for (_, _, n) in seqs]
     maxseg = max(nseg) if nseg else 0
     for blk in range(-(-maxseg // KB)):
         for s, (b, t0, n) in enumerate(seqs):
             nch = -(-n // Q)
             for j in range(blk * KB, min((blk + 1) * KB, nseg[s])):
-                units.append((s, b, t0 + j * R * Q, min(R * Q, n - j * R * Q), min(R, nch - j * R),
+                base, rem = divmod(nch, nseg[s])
+                c0 = j * base + min(j, rem)
+                nc = base + (1 if j < rem else 0)
+                units.append((s, b, t0 + c0 * Q, min(nc * Q, n - c0 * Q), nc,
                               last.get(s, -1) if j > 0 else -1, 1 if j == nseg[s] - 1 else 0, j))
                 last[s] = len(units) - 1
     return dict(seqs=[(b, t0, n, chunk0[s]) for s, (b, t0, n) in enumerate(seqs)], chunks=chunks, units=units)

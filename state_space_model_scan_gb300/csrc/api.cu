@@ -6,7 +6,8 @@
 
 namespace ssd {
 // meta.cu
-cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int KB, int kmax, int umax, int32_t *hdr,
+cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int num, int den, int KB, int kmax,
+                              int umax, int32_t *hdr,
                               SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units, int32_t *last_unit,
                               uint32_t *zero_words, int64_t n_zero, cudaStream_t st);
 cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr, const float *init,
@@ -234,7 +235,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     if (fused && bwd && b == nullptr) return SSD_ERR_INVALID_ARGUMENT;
     int64_t kmax = varlen ? (L + Q - 1) / Q + S : B * ((L + Q - 1) / Q);
     if (kmax > (int64_t)1 << 30) return SSD_ERR_UNSUPPORTED;
-    int R = 1;
+    int R = 1, num = 1, den = 1;
     int64_t umax = 0;
     if (fused) {
         R = p->seg_chunks;
@@ -245,11 +246,15 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
             R = (int)(r < 1 ? 1 : (r > 4 ? 4 : r));
         }
         if (R > fused_rmax()) return SSD_ERR_UNSUPPORTED;
-        umax = varlen ? kmax / R + S : B * (((L + Q - 1) / Q + R - 1) / R);
+        num = 1;   // units per chunk: 1/R (the metadata kernel also accepts a larger ratio)
+        den = R;
+        // units: sum over sequences of max(ceil(n/R), ceil(n num/den)) <= kmax max(1/R, num/den) + S
+        const int64_t per = (int64_t)num * R > den ? (kmax * num + den - 1) / den : (kmax + R - 1) / R;
+        umax = per + S;
     }
     Shape sh;
     sh.B = (int)B; sh.L = (int)L; sh.H = (int)H; sh.P = (int)P; sh.G = (int)G; sh.N = (int)N; sh.S = (int)S;
-    sh.Q = Q; sh.hpg = (int)(H / G); sh.kmax = (int)kmax; sh.umax = (int)umax; sh.R = R;
+    sh.Q = Q; sh.hpg = (int)(H / G); sh.kmax = (int)kmax; sh.umax = (int)umax; sh.R = R; sh.useg_num = num; sh.useg_den = den;
     pl.sh = sh;
     Layout lay;
     pl.off_hdr = lay.take(HDR_WORDS * sizeof(int32_t));
@@ -339,7 +344,7 @@ ssd_status run_forward_states(const Plan &pl, const ssd_fwd_args *a, void *ws, f
     SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
     ChunkInfo *chunks = at<ChunkInfo>(ws, pl.off_chunks);
     float *dtw = at<float>(ws, pl.off_dt), *csw = at<float>(ws, pl.off_cs), *states = at<float>(ws, pl.off_states);
-    SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, 1, 1, sh.kmax, 0, hdr, seqs, chunks, nullptr,
+    SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, 1, 1, 1, 1, sh.kmax, 0, hdr, seqs, chunks, nullptr,
                                at<int32_t>(ws, pl.off_lastunit), nullptr, 0, st));
     if (sh.kmax > 0) {
         SSD_CUDA(launch_chunk_cumsum(sh, hdr, chunks, (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1],
@@ -409,7 +414,7 @@ ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, siz
         SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
         UnitInfo *units = at<UnitInfo>(ws, pl.off_units);
         uint32_t *flags = at<uint32_t>(ws, pl.off_flags);
-        SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, sh.R, fused_block_units(), sh.kmax,
+        SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, sh.R, sh.useg_num, sh.useg_den, fused_block_units(), sh.kmax,
                                    sh.umax, hdr, seqs,
                                    at<ChunkInfo>(ws, pl.off_chunks), units, at<int32_t>(ws, pl.off_lastunit), flags,
                                    (int64_t)sh.umax * sh.H, st));
@@ -470,7 +475,7 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         __nv_bfloat16 *states = at<__nv_bfloat16>(ws, pl.off_states);
         float *dS = at<float>(ws, pl.off_dstates), *clam = at<float>(ws, pl.off_cs);
         float *dBh = at<float>(ws, pl.off_dBh), *dCh = at<float>(ws, pl.off_dCh), *part = at<float>(ws, pl.off_part);
-        SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, sh.R, fused_block_units(), sh.kmax,
+        SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, sh.R, sh.useg_num, sh.useg_den, fused_block_units(), sh.kmax,
                                    sh.umax, hdr, seqs, chunks, units, at<int32_t>(ws, pl.off_lastunit), flags,
                                    (int64_t)sh.umax * sh.H, st));
         const int64_t tickets = (int64_t)sh.umax * sh.H;

@@ -42,7 +42,8 @@ struct Shape {
     int hpg;          // H / G
     int kmax;         // capacity of the chunk list
     int umax;         // capacity of the unit list
-    int R;            // chunks per unit (fused path)
+    int R;            // most chunks per unit (fused path)
+    int useg_num, useg_den;   // units per chunk of a sequence (>= 1/R): see the metadata kernel
 };
 
 // Arguments of the tensor-core backward kernels (bwd_tc.cu).

@@ -94,7 +94,7 @@ struct FusedParams {
     uint32_t *flags;
     // States-only mode (used by the backward): when set, the carried state at the
     // start of every chunk is written here (bf16 [chunk][head][P][N]) and no output
-    // is computed (no CB, M, Y_off, Y_diag, y).  Chunk index = seqs[seq].chunk0 + j*R + c.
+    // is computed (no CB, M, Y_off, Y_diag, y).  Chunk index = seqs[seq].chunk0 + (t0 - seqs[seq].t0)/Q + c.
     __nv_bfloat16 *states_out;
     const SeqInfo *seqs;
 };
@@ -463,7 +463,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 
         // ---- phase 2: outputs (or, in states-only mode, the carried state of every chunk)
         const float Dh = p.D ? p.D[h] : 0.f;
-        const int64_t kfirst = full ? 0 : (int64_t)p.seqs[ui.seq].chunk0 + (int64_t)ui.j * sh.R;
+        const int64_t kfirst = full ? 0 : (int64_t)p.seqs[ui.seq].chunk0 + (ui.t0 - p.seqs[ui.seq].t0) / QT;
         for (int c = 0; c < ui.nchunk; ++c) {
             const int tc0 = ui.t0 + c * QT;
             const int clen = min(QT, ui.len - c * QT);

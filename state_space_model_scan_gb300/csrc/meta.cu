@@ -4,8 +4,11 @@
 // Each sequence is cut into Q-token chunks from its own first token (the last
 // chunk ragged), so no chunk ever holds two sequences; the carried state is
 // reset to the sequence's initial state at its first chunk.  Chunks are listed
-// sequence by sequence.  Work units of the fused forward group R consecutive
-// chunks of one sequence (segment j of the sequence); segments are grouped in
+// sequence by sequence.  Work units of the fused forward group consecutive
+// chunks of one sequence (segment j of the sequence): a sequence of n chunks has
+// m = max(ceil(n / R), min(n, ceil(n * num / den))) segments of floor(n/m) or
+// ceil(n/m) chunks, the larger ones first (the planner raises m above ceil(n/R)
+// so that the units fill whole rounds of the resident CTAs); segments are grouped in
 // blocks of KB.  Units are listed by (block, sequence, segment), so a unit only
 // ever depends on units listed before it and the units of one sequence inside
 // one block are consecutive in the list.
@@ -43,6 +46,15 @@ __device__ int block_excl_scan(int v, int *total, int *sm) {
     return excl;
 }
 
+// Segment count of a sequence of n chunks (see the file comment).
+__device__ __forceinline__ int seg_count(int n, int R, int num, int den) {
+    if (n <= 0) return 0;
+    const int lo = (n + R - 1) / R;
+    const int64_t want = ((int64_t)n * num + den - 1) / den;
+    const int m = (int)(want < n ? want : n);
+    return m > lo ? m : lo;
+}
+
 __device__ int block_max(int v, int *sm) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
@@ -56,7 +68,8 @@ __device__ int block_max(int v, int *sm) {
 }
 
 __global__ void __launch_bounds__(kMetaThreads)
-k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, int KB, int kmax, int umax,
+k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, int num, int den, int KB, int kmax,
+             int umax,
              int32_t *hdr, SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units, int32_t *last_unit,
              uint32_t *zero_words, int64_t n_zero) {
     __shared__ int sm[32];
@@ -96,7 +109,7 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
             si.b = b; si.t0 = t0; si.len = len; si.chunk0 = carry + off;
             seqs[s] = si;
         }
-        int nseg = (nch + R - 1) / R;
+        int nseg = seg_count(nch, R, num, den);
         maxseg = max(maxseg, block_max(s < S ? nseg : 0, sm));
         carry += tot;
     }
@@ -128,7 +141,7 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
                 if (s < S) {
                     si = seqs[s];
                     nch = (si.len + Q - 1) / Q;
-                    nseg = (nch + R - 1) / R;
+                    nseg = seg_count(nch, R, num, den);
                     cnt = max(0, min(KB, nseg - blk * KB));
                 }
                 int tot;
@@ -139,9 +152,11 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
                     if (u < umax) {
                         UnitInfo ui;
                         ui.seq = s; ui.b = si.b;
-                        ui.t0 = si.t0 + j * R * Q;
-                        ui.len = min(R * Q, si.len - j * R * Q);
-                        ui.nchunk = min(R, nch - j * R);
+                        const int base = nch / nseg, rem = nch % nseg;
+                        const int c0 = j * base + min(j, rem);
+                        ui.t0 = si.t0 + c0 * Q;
+                        ui.nchunk = base + (j < rem ? 1 : 0);
+                        ui.len = min(ui.nchunk * Q, si.len - c0 * Q);
                         ui.prev = (j == 0) ? -1 : (i > 0 ? u - 1 : last_unit[s]);
                         ui.last = (j == nseg - 1) ? 1 : 0;
                         ui.j = j;
@@ -175,10 +190,10 @@ __global__ void k_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, con
 
 }  // namespace
 
-cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int KB, int kmax, int umax,
-                              int32_t *hdr, SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units,
+cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int num, int den, int KB,
+                              int kmax, int umax, int32_t *hdr, SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units,
                               int32_t *last_unit, uint32_t *zero_words, int64_t n_zero, cudaStream_t st) {
-    k_build_meta<<<1, kMetaThreads, 0, st>>>(cu, B, L, S, Q, R, KB, kmax, umax, hdr, seqs, chunks, units,
+    k_build_meta<<<1, kMetaThreads, 0, st>>>(cu, B, L, S, Q, R, num, den, KB, kmax, umax, hdr, seqs, chunks, units,
                                              last_unit, zero_words, n_zero);
     return cudaGetLastError();
 }

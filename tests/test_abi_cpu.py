@@ -159,3 +159,22 @@ def test_metadata_reference_builder():
     assert [(u[0], u[7]) for u in m["units"]] == [(0, 0), (0, 1), (1, 0), (1, 1), (0, 2), (0, 3), (1, 2), (1, 3),
                                                   (0, 4), (1, 4)]
     assert [u[5] for u in m["units"]] == [-1, 0, -1, 2, 1, 4, 3, 6, 5, 7]
+
+
+def test_metadata_balanced_units():
+    """Units of one sequence differ by at most one chunk, the larger ones first, and
+    tile its chunks exactly; a units-per-chunk ratio above 1/R raises the count."""
+    from oracle import meta
+    m = meta.build(batch=2, seqlen=64 * 9, Q=64, R=4, KB=4)
+    assert [u[4] for u in m["units"] if u[0] == 0] == [3, 3, 3]
+    m = meta.build(batch=1, seqlen=128 * 64 - 5, Q=128, R=4, KB=4, num=19, den=64)
+    sizes = [u[4] for u in m["units"]]
+    assert sizes == [4] * 7 + [3] * 12
+    pos = 0
+    for u in sorted(m["units"], key=lambda r: r[7]):
+        assert u[2] == pos and u[3] == min(u[4] * 128, 128 * 64 - 5 - pos)
+        pos += u[3]
+    assert pos == 128 * 64 - 5
+    # never fewer units than ceil(n/R), never more than n
+    assert len(meta.build(batch=1, seqlen=640, Q=64, R=4, num=1, den=100)["units"]) == 3
+    assert len(meta.build(batch=1, seqlen=640, Q=64, R=4, num=5, den=1)["units"]) == 10
