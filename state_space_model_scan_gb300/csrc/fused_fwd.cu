@@ -94,7 +94,8 @@ struct FusedParams {
     uint32_t *flags;
     // States-only mode (used by the backward): when set, the carried state at the
     // start of every chunk is written here (bf16 [chunk][head][P][N]) and no output
-    // is computed (no CB, M, Y_off, Y_diag, y).  Chunk index = seqs[seq].chunk0 + (t0 - seqs[seq].t0)/Q + c.
+    // is computed (no CB, M, Y_off, Y_diag, y).  Phase 1 then keeps each chunk's own
+    // state in TMEM, so phase 2 needs neither loads nor tensor-core work.  Chunk index = seqs[seq].chunk0 + (t0 - seqs[seq].t0)/Q + c.
     __nv_bfloat16 *states_out;
     const SeqInfo *seqs;
 };
@@ -167,6 +168,9 @@ __device__ __forceinline__ void fma_col64(float *acc, const float *src, float sc
     }
 }
 
+// kStatesOnly: the states-only mode (FusedParams::states_out set), compiled separately so
+// that neither mode's code shapes the other's register allocation.
+template <bool kStatesOnly>
 __global__ void __launch_bounds__(NTHR, 2)
 k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmZ, const FusedParams p) {
@@ -346,21 +350,28 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             __syncthreads();
         }
 
-        // ---- phase 1: unit aggregate^T[n][p] = sum_l B[l][n] (w o x)[l][p], double-buffered
+        // ---- phase 1: unit aggregate^T[n][p] = sum_l B[l][n] (w o x)[l][p], double-buffered.
+        // States-only mode keeps every chunk's own state S_c^T (chunk-local weights) in TMEM
+        // columns [64c, 64c+64) instead, and forms the aggregate from them.
+        constexpr bool full = !kStatesOnly;
         for (int c = 0; c < ui.nchunk; ++c) {
             const int st = c & 1;
             uint8_t *xs = st ? Ws : Xs;
             wait_bar(st ? BAR_C : BAR_X);
-            scale_row(xs + row * 128, xs + row * 128, row, wu[c * QT + row]);   // x -> w o x in place
+            const float wl = full ? wu[c * QT + row]
+                                  : dtu[c * QT + row] * ex2(cs2u[c * QT + QT - 1] - cs2u[c * QT + row]);
+            scale_row(xs + row * 128, xs + row * 128, row, wl);   // x -> w o x in place
             fence_proxy_async_smem();
             __syncthreads();
             if (ms->abort_) break;
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t sb_ = smem_u32(st ? Cs : Bs), sx_ = smem_u32(xs);
+                const uint32_t dcol = full ? TM_SC : 64u * (uint32_t)c;
 #pragma unroll
                 for (int k = 0; k < QT / 16; ++k)
-                    umma_bf16(tmem + TM_SC, mnmaj(sb_, k), mnmaj(sx_, k), idesc_sc, (c > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16(tmem + dcol, mnmaj(sb_, k), mnmaj(sx_, k), idesc_sc,
+                              (k > 0 || (full && c > 0)) ? 1u : 0u);
             }
             commit();
             wait_bar(BAR_MMA);   // stage st free again
@@ -369,7 +380,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         }
         if (ms->abort_) break;
         float s_run[64];   // row n = tid: aggregate, then carried state, columns p
-        {
+        if (full) {
             float t32[32];
             tmem_ld32(tmem + lane_base + TM_SC, t32);
 #pragma unroll
@@ -378,6 +389,20 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
             for (int i = 0; i < 32; ++i) s_run[32 + i] = t32[i];
             tmem_wait_ld();
+        } else {   // aggregate = (..(S_0 a_1 + S_1) a_2 + ..) + S_last, a_c = the chunk's decay
+#pragma unroll
+            for (int i = 0; i < 64; ++i) s_run[i] = 0.f;
+            for (int c = 0; c < ui.nchunk; ++c) {
+                const float a_c = ex2(cs2u[c * QT + QT - 1]);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float t32[32];
+                    tmem_ld32(tmem + lane_base + 64u * (uint32_t)c + 32 * hh, t32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s_run[32 * hh + i] = fmaf(a_c, s_run[32 * hh + i], t32[i]);
+                }
+            }
         }
         const int64_t my = (int64_t)u * sh.H + h;
         {   // aggregate^T row n -> agg[p][n]
@@ -391,11 +416,11 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         __syncthreads();
         if (tid == 0) st_release_u32(p.flags + my, 1u);
 
-        const bool full = p.states_out == nullptr;
-        // prefetch phase-2 chunk 0 while folding the carry-in (all phase-1 MMAs are done)
-        load_x(h, ui.t0, ui.b);
-        load_bc(BAR_B, &tmB, Bs, g, ui.t0, ui.b);
-        if (full) load_bc(BAR_C, &tmC, Cs, g, ui.t0, ui.b);
+        if (full) {   // prefetch phase-2 chunk 0 while folding the carry-in (all phase-1 MMAs are done)
+            load_x(h, ui.t0, ui.b);
+            load_bc(BAR_B, &tmB, Bs, g, ui.t0, ui.b);
+            load_bc(BAR_C, &tmC, Cs, g, ui.t0, ui.b);
+        }
 
         {   // the next unit: its UnitInfo and dt inputs travel while this one folds and runs phase 2
             const int tn = ms->tnext;
@@ -461,27 +486,43 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             if (tid == 0) st_release_u32(p.flags + my, 2u);
         }
 
-        // ---- phase 2: outputs (or, in states-only mode, the carried state of every chunk)
+        // ---- phase 2, states-only mode: the carried state entering every chunk, from the chunk
+        // states kept in TMEM (no loads, no MMAs)
+        if (!full) {
+            const int64_t kfirst = (int64_t)p.seqs[ui.seq].chunk0 + (ui.t0 - p.seqs[ui.seq].t0) / QT;
+            for (int c = 0; c < ui.nchunk; ++c) {
+                __nv_bfloat16 *dst = p.states_out + ((kfirst + c) * sh.H + h) * (int64_t)(PT * NT) + row;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(s_run[i]);
+                const float a_c = ex2(cs2u[c * QT + QT - 1]);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float t32[32];
+                    tmem_ld32(tmem + lane_base + 64u * (uint32_t)c + 32 * hh, t32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s_run[32 * hh + i] = fmaf(a_c, s_run[32 * hh + i], t32[i]);
+                }
+            }
+            tc_fence_before();
+            __syncthreads();   // TMEM read: the next unit's phase 1 may overwrite it
+            continue;
+        }
+        // ---- phase 2: outputs
         const float Dh = p.D ? p.D[h] : 0.f;
-        const int64_t kfirst = full ? 0 : (int64_t)p.seqs[ui.seq].chunk0 + (ui.t0 - p.seqs[ui.seq].t0) / QT;
         for (int c = 0; c < ui.nchunk; ++c) {
             const int tc0 = ui.t0 + c * QT;
             const int clen = min(QT, ui.len - c * QT);
             const bool more = c + 1 < ui.nchunk;
             const int64_t tok = (int64_t)tc0 + row;
-            const bool has_z = full && p.z != nullptr;
+            const bool has_z = p.z != nullptr;
             // chunk-local cumulative log-decay (computed at unit start)
             const float *cs2 = cs2u + c * QT;
             const float *dtc = dtu + c * QT;
             const float *cf = cfu + c * QT;
             const float a_c = ex2(cs2[QT - 1]);
-            if (!full) {   // states-only: S_in[chunk] -> global bf16 [p][n] (row n)
-                __nv_bfloat16 *dst = p.states_out + ((kfirst + c) * sh.H + h) * (int64_t)(PT * NT) + row;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(s_run[i]);
-            }
             wait_bar(BAR_B);
-            if (full) {   // CB = C B^T (K = state dim) runs while x is scaled; committed with S_c below
+            {   // CB = C B^T (K = state dim) runs while x is scaled; committed with S_c below
                 wait_bar(BAR_C);
                 if (tid == 0) {
                     tc_fence_after();
@@ -496,7 +537,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             fence_proxy_async_smem();
             __syncthreads();
             if (ms->abort_) {
-                if (full) commit();   // the CB MMAs are in flight: the drain waits for them
+                commit();   // the CB MMAs are in flight: the drain waits for them
                 break;
             }
             if (tid == 0) {
@@ -580,15 +621,6 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s_run[32 + i] = a_c * s_run[32 + i] + sc[i];
             }
-            if (!full) {
-                tc_fence_before();
-                __syncthreads();   // x, B, W free: next chunk's loads
-                if (more) {
-                    load_x(h, tc0 + QT, ui.b);
-                    load_bc(BAR_B, &tmB, Bs, g, tc0 + QT, ui.b);
-                }
-                continue;
-            }
             wait_bar(BAR_MMA);   // Y_off done: C and W free
             if (has_z) load_z(h, tc0, ui.b);
             if (more) load_bc(BAR_C, &tmC, Cs, g, tc0 + QT, ui.b);
@@ -647,7 +679,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             __syncthreads();
         }
         if (ms->abort_) break;
-        if (ui.last && p.final_ && full) {
+        if (ui.last && p.final_) {
             float *dst = p.final_ + ((int64_t)ui.seq * sh.H + h) * PT * NT + row;
 #pragma unroll
             for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = s_run[i];
@@ -721,10 +753,17 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
     fp.y = (__nv_bfloat16 *)y; fp.syb = sy[0]; fp.syl = sy[1]; fp.syh = sy[2];
     fp.init = init; fp.final_ = final_; fp.agg = agg; fp.incl = incl; fp.lam = lam; fp.flags = flags;
     fp.states_out = states_out; fp.seqs = seqs;
-    static int attr_done[64] = {0};
-    cudaError_t e = ensure_smem_attr(k_fused_fwd, (int)SMEM_BYTES, attr_done);
-    if (e != cudaSuccess) return e;
-    k_fused_fwd<<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, mz, fp);
+    if (states_out != nullptr) {
+        static int attr_done_s[64] = {0};
+        cudaError_t e = ensure_smem_attr(k_fused_fwd<true>, (int)SMEM_BYTES, attr_done_s);
+        if (e != cudaSuccess) return e;
+        k_fused_fwd<true><<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, mz, fp);
+    } else {
+        static int attr_done[64] = {0};
+        cudaError_t e = ensure_smem_attr(k_fused_fwd<false>, (int)SMEM_BYTES, attr_done);
+        if (e != cudaSuccess) return e;
+        k_fused_fwd<false><<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, mz, fp);
+    }
     return cudaGetLastError();
 }
 
