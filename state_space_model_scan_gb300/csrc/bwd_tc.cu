@@ -449,6 +449,25 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 for (int i = 0; i < 32; ++i) dd += dyp[i] * xv[i];
                 fm[F_ROWD + hf * 128 + row] = dd;
             }
+            fence_proxy_async_smem();
+            if (__syncthreads_or(bad)) {
+                aborted = true;
+                break;
+            }
+            if (tid == 0) {   // group 1 (runs during the dS work below): CB = C B^T (first head), dM = dyp x^T
+                tc_fence_after();
+                if (hi == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < NT / 16; ++kk)
+                        umma_bf16(tmem + T_CB, kmaj(sC, kk, BC_BYTES / 2), kmaj(sB, kk, BC_BYTES / 2),
+                                  idesc_bf16(128, 128, 0, 0), kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < PT / 16; ++kk)
+                    umma_bf16(tmem + T_DM, kmaj(sDY, kk, X_BYTES), kmaj(sX, kk, X_BYTES), idesc_bf16(128, 128, 0, 0),
+                              kk > 0);
+                umma_commit(&bar[2]);
+            }
             const float wl = wst[row];
 #pragma unroll
             for (int i = 0; i < 32; ++i) xv[i] *= wl;
@@ -483,24 +502,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             store_row32_swz(sm + O_WX + row * 128, row, hf, xv);
         }
         fence_proxy_async_smem();
-        if (__syncthreads_or(bad)) {
-            aborted = true;
-            break;
-        }
-        if (tid == 0) {   // group 1: CB = C B^T (first head only), dM = dyp x^T
-            tc_fence_after();
-            if (hi == 0) {
-#pragma unroll
-                for (int kk = 0; kk < NT / 16; ++kk)
-                    umma_bf16(tmem + T_CB, kmaj(sC, kk, BC_BYTES / 2), kmaj(sB, kk, BC_BYTES / 2),
-                              idesc_bf16(128, 128, 0, 0), kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < PT / 16; ++kk)
-                umma_bf16(tmem + T_DM, kmaj(sDY, kk, X_BYTES), kmaj(sX, kk, X_BYTES), idesc_bf16(128, 128, 0, 0), kk > 0);
-            umma_commit(&bar[2]);
-        }
-        wait_mma();
+        wait_mma();   // group 1
         // ---- M = E dt_s CB and E' = E dt_s dM (bf16) rows; row sums of M o dM; column sums of
         // E CB dM (fixed order).  Blocks of 32 columns below the diagonal take
         // E = exp(cs[l] - cs[a]) exp(cs[a] - cs[s]) (a = the block's last column; both factors
