@@ -83,7 +83,9 @@ struct Plan {
     bool bf16 = false;
     bool varlen = false;
     int algo = SSD_ALGO_STAGED;
-    int hs = 1;   // heads per CTA of the tensor-core gradient kernel
+    int hs = 1;   // heads per work item of the tensor-core gradient kernel
+    int k_pairs = 0, nsub_tail = 1, n_items = 0;   // its work items (see BwdTcArgs)
+    size_t off_tpart = 0;
     size_t off_hdr = 0, off_seqs = 0, off_chunks = 0, off_lastunit = 0, off_units = 0;
     size_t off_dt = 0, off_cs = 0, off_states = 0, off_dstates = 0, off_dBh = 0, off_dCh = 0, off_part = 0;
     size_t off_agg = 0, off_incl = 0, off_lam = 0, off_flags = 0;
@@ -272,6 +274,27 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         if (bwd) {
             pl.hs = p->bwd_heads > 0 ? p->bwd_heads : bwd_heads_per_cta(kmax, H, sh.hpg);
             if (sh.hpg % pl.hs != 0) return SSD_ERR_INVALID_ARGUMENT;
+            // Work items of the persistent gradient kernel (one CTA per SM).  With whole-group
+            // items, the pairs (chunk, group) that would form a last partial wave are split into
+            // subsets of >= 2 heads, so the last wave is filled with small items; their dB/dC
+            // shares are summed, in subset order, by a small kernel afterwards.
+            const int64_t pairs = kmax * G;
+            const int nsub_main = sh.hpg / pl.hs;
+            pl.k_pairs = (int)pairs;
+            pl.nsub_tail = nsub_main;
+            if (p->bwd_heads == 0 && nsub_main == 1) {
+                const int64_t sms = num_sms(), r = pairs % sms;
+                int f = 1;
+                for (int d = 4; d >= 2; --d)
+                    if (pl.hs % d == 0 && pl.hs / d >= 2) { f = d; break; }
+                if (r > 0 && f > 1 && pairs > sms) {
+                    pl.k_pairs = (int)(pairs - r);
+                    pl.nsub_tail = f;
+                }
+            }
+            pl.n_items = pl.k_pairs * nsub_main + (int)(pairs - pl.k_pairs) * pl.nsub_tail;
+            const int64_t tail_items = nsub_main == 1 && pl.nsub_tail > 1 ? (pairs - pl.k_pairs) * pl.nsub_tail : 0;
+            pl.off_tpart = lay.take(sizeof(float) * (size_t)tail_items * 2 * Q * (size_t)N);
             // dB/dC shares of head subsets, only when a CTA covers part of a group
             const size_t ksub = pl.hs < sh.hpg ? (size_t)kmax * (size_t)(H / pl.hs) : 0;
             pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * N));   // carried states, bf16
@@ -475,9 +498,10 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         __nv_bfloat16 *states = at<__nv_bfloat16>(ws, pl.off_states);
         float *dS = at<float>(ws, pl.off_dstates), *clam = at<float>(ws, pl.off_cs);
         float *dBh = at<float>(ws, pl.off_dBh), *dCh = at<float>(ws, pl.off_dCh), *part = at<float>(ws, pl.off_part);
-        SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, sh.R, sh.useg_num, sh.useg_den, fused_block_units(), sh.kmax,
-                                   sh.umax, hdr, seqs, chunks, units, at<int32_t>(ws, pl.off_lastunit), flags,
-                                   (int64_t)sh.umax * sh.H, st));
+        const int64_t n_zero = (int64_t)sh.umax * sh.H;   // the unit flags
+        SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, sh.R, sh.useg_num, sh.useg_den,
+                                   fused_block_units(), sh.kmax, sh.umax, hdr, seqs, chunks, units,
+                                   at<int32_t>(ws, pl.off_lastunit), flags, n_zero, st));
         const int64_t tickets = (int64_t)sh.umax * sh.H;
         if (tickets > 0) {
             // carried state entering every chunk (forward recomputed in states-only mode)
@@ -499,7 +523,11 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         ta.dx = b->dx.ptr; ta.dz = b->dz.ptr; ta.sdx = b->dx.stride; ta.sdz = b->dz.ptr ? b->dz.stride : nullptr;
         ta.ddt = (float *)b->ddt.ptr; ta.sddb = b->ddt.stride[0]; ta.sddl = b->ddt.stride[1];
         ta.states = states; ta.dS = dS; ta.chunk_lam = clam; ta.dBh = dBh; ta.dCh = dCh; ta.partials = part;
-        ta.hs = pl.hs; ta.hs_ds = dstates_heads_per_cta(sh.kmax, sh.H, sh.hpg); ta.dB = b->dB.ptr; ta.dC = b->dC.ptr; ta.sdB = b->dB.stride; ta.sdC = b->dC.stride;
+        ta.hs = pl.hs; ta.hs_ds = dstates_heads_per_cta(sh.kmax, sh.H, sh.hpg);
+        ta.dB = b->dB.ptr; ta.dC = b->dC.ptr; ta.sdB = b->dB.stride; ta.sdC = b->dC.stride;
+        ta.k_pairs = pl.k_pairs; ta.nsub_tail = pl.nsub_tail; ta.n_items = pl.n_items;
+        ta.grid = pl.n_items < num_sms() ? pl.n_items : num_sms();
+        ta.tpart = at<float>(ws, pl.off_tpart);
         if (sh.kmax > 0) SSD_CUDA(launch_bwd_dstates_tc(sh, hdr, chunks, ta, st));
         SSD_CUDA(launch_state_passing(sh, hdr, seqs, clam, 1, dS, (const float *)b->dfinal_states.ptr,
                                       (float *)b->dinitial_states.ptr, 1, st));

@@ -60,6 +60,8 @@ struct BwdParams {
     int hs_ds;               // heads per CTA of the dstates kernel
     __nv_bfloat16 *dB, *dC;  // final outputs when hs == H/G
     int64_t sdBb, sdBl, sdBg, sdCb, sdCl, sdCg;
+    int k_pairs, nsub_tail, n_items;   // gradient kernel work items
+    float *tpart;
 };
 
 __device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t col_bytes) {
@@ -317,59 +319,26 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, hf = tid >> 7, quad = warp & 3;
     const int lane = tid & 31;
-    const int k = blockIdx.x, jsub = blockIdx.y;
-    if (k >= p.hdr[HDR_NCHUNKS] || p.hdr[HDR_STATUS] != 0) return;
-    const ChunkInfo ci = p.chunks[k];
-    const int H = p.sh.H, HS = p.hs;
-    const int h0 = jsub * HS, g = h0 / p.sh.hpg;
+    const int H = p.sh.H, G = p.sh.G, hpg = p.sh.hpg, nsub_main = hpg / p.hs;
     const bool has_z = p.z != nullptr;
     float *fm = reinterpret_cast<float *>(sm + O_MISC);
     float *cs2 = fm + F_CS2, *dtc = fm + F_DT, *wst = fm + F_W;
     // 0: B/C, 1: x/S_in, 2: MMA (dx and y tiles), 3: dy/z/dS, 4: MMA (dB/dC chains)
     uint64_t *bar = reinterpret_cast<uint64_t *>(fm + F_END);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
-    auto load_head = [&](int h) {   // one thread: x and S_in
-        const int slab = k * H + h;
-        mbar_expect_tx(&bar[1], X_BYTES + S_BYTES);
-        tma_load_4d(sm + O_X, &tmX, &bar[1], 0, h, ci.t0, ci.b);
-        tma_load_4d(sm + O_SI, &tmS, &bar[1], 0, 0, slab * PT, 0);
-        tma_load_4d(sm + O_SI + S_BYTES / 2, &tmS, &bar[1], 64, 0, slab * PT, 0);
-    };
-    auto stage_head = [&](int h) {   // one thread: dy, z and fp32 dS
-        const float *src = p.dS + ((int64_t)k * H + h) * (PT * NT);
-        mbar_expect_tx(&bar[3], X_BYTES * (has_z ? 2u : 1u) + 2u * S_BYTES);   // dS fp32 = 2 x S_BYTES
-        tma_load_4d(sm + O_E, &tmDY, &bar[3], 0, h, ci.t0, ci.b);
-        if (has_z) tma_load_4d(sm + O_E + X_BYTES, &tmZ, &bar[3], 0, h, ci.t0, ci.b);
-        bulk_load(sm + O_WX, src, S_BYTES, &bar[3]);
-        bulk_load(sm + O_WX + S_BYTES, src + PT * NT / 2, S_BYTES, &bar[3]);
-    };
+    int *s_item = reinterpret_cast<int *>(tslot + 1);   // [0] item, [1] finished-subset count
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
-        mbar_expect_tx(&bar[0], 2 * BC_BYTES);
-        tma_load_4d(sm + O_B, &tmB, &bar[0], 0, g, ci.t0, ci.b);
-        tma_load_4d(sm + O_B + BC_BYTES / 2, &tmB, &bar[0], 64, g, ci.t0, ci.b);
-        tma_load_4d(sm + O_C, &tmC, &bar[0], 0, g, ci.t0, ci.b);
-        tma_load_4d(sm + O_C + BC_BYTES / 2, &tmC, &bar[0], 64, g, ci.t0, ci.b);
-        stage_head(h0);
-        load_head(h0);
     }
-    // dt_raw + bias of position tid for a head (0 past the chunk's end)
-    auto load_dtv = [&](int h) -> float {
-        return tid < ci.len ? p.dt_raw[(int64_t)ci.b * p.sdb + (int64_t)(ci.t0 + tid) * p.sdl + h] +
-                                  (p.bias ? p.bias[h] : 0.f)
-                            : 0.f;
-    };
-    float dt_next = load_dtv(h0), A_next = p.A[h0], D_next = p.D ? p.D[h0] : 0.f;
     if (warp == 0) tmem_alloc(tslot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lb = (uint32_t)(quad * 32) << 16;
-    const int64_t tok = (int64_t)ci.t0 + row;
-    const bool live = row < ci.len;
-    uint32_t mma_phase = 0, mma2_phase = 0, ld_done = 0, ld_issued = 1, st_done = 0, st_issued = 1, bc_done = 0;
+    uint32_t mma_phase = 0, mma2_phase = 0, ld_done = 0, ld_issued = 0, st_done = 0, st_issued = 0, bc_done = 0,
+             bc_issued = 0;
     int bad = 0;          // this thread saw a wait run out
     bool aborted = false; // uniform: some thread did (checked once per head)
     auto fail = [&]() {
@@ -390,8 +359,97 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     const uint32_t sSI = smem_u32(sm + O_SI), sDY = smem_u32(sm + O_DY), sWX = smem_u32(sm + O_WX);
     const uint32_t sM = smem_u32(sm + O_M), sE = smem_u32(sm + O_E), sSD = smem_u32(sm + O_SD);
 
+    // ---- work items: (chunk k, group g, subset of HS heads), in ticket order.  The next
+    // item is taken during the current item's last head, and its B/C tiles and first-head
+    // inputs are loaded while the current item finishes.
+    struct Item {
+        int item, pair, nsub, k, g, HS, h0;
+        bool tail;
+        ChunkInfo ci;
+    };
+    const int n_main = p.k_pairs * nsub_main;
+    auto pair_of = [&](int it) { return it >= n_main ? p.k_pairs + (it - n_main) / p.nsub_tail : it / nsub_main; };
+    auto decode = [&](int it, Item &w) {
+        w.item = it;
+        w.tail = it >= n_main;
+        w.pair = pair_of(it);
+        const int sub = w.tail ? (it - n_main) % p.nsub_tail : it % nsub_main;
+        w.nsub = w.tail ? p.nsub_tail : nsub_main;
+        w.k = w.pair / G;
+        w.g = w.pair % G;
+        w.HS = hpg / w.nsub;
+        w.h0 = w.g * hpg + sub * w.HS;
+        w.ci = p.chunks[w.k];
+    };
+    auto take = [&]() -> int {   // one thread: the next item whose chunk exists, else n_items
+        const int nch = p.hdr[HDR_NCHUNKS];
+        for (;;) {
+            if (p.hdr[HDR_STATUS] != 0) return p.n_items;   // an error anywhere ends the work
+            const int it = atomicAdd(const_cast<int32_t *>(p.hdr) + HDR_TICKET2, 1);
+            if (it >= p.n_items) return p.n_items;
+            if (pair_of(it) / G < nch) return it;
+        }
+    };
+    auto load_head = [&](const Item &w, int h) {   // one thread: x and S_in
+        const int slab = w.k * H + h;
+        mbar_expect_tx(&bar[1], X_BYTES + S_BYTES);
+        tma_load_4d(sm + O_X, &tmX, &bar[1], 0, h, w.ci.t0, w.ci.b);
+        tma_load_4d(sm + O_SI, &tmS, &bar[1], 0, 0, slab * PT, 0);
+        tma_load_4d(sm + O_SI + S_BYTES / 2, &tmS, &bar[1], 64, 0, slab * PT, 0);
+    };
+    auto stage_head = [&](const Item &w, int h) {   // one thread: dy, z and fp32 dS
+        const float *src = p.dS + ((int64_t)w.k * H + h) * (PT * NT);
+        mbar_expect_tx(&bar[3], X_BYTES * (has_z ? 2u : 1u) + 2u * S_BYTES);   // dS fp32 = 2 x S_BYTES
+        tma_load_4d(sm + O_E, &tmDY, &bar[3], 0, h, w.ci.t0, w.ci.b);
+        if (has_z) tma_load_4d(sm + O_E + X_BYTES, &tmZ, &bar[3], 0, h, w.ci.t0, w.ci.b);
+        bulk_load(sm + O_WX, src, S_BYTES, &bar[3]);
+        bulk_load(sm + O_WX + S_BYTES, src + PT * NT / 2, S_BYTES, &bar[3]);
+    };
+    auto issue_first = [&](const Item &w) {   // B/C and the first head's inputs (one thread issues)
+        if (tid == 0) {
+            mbar_expect_tx(&bar[0], 2 * BC_BYTES);
+            tma_load_4d(sm + O_B, &tmB, &bar[0], 0, w.g, w.ci.t0, w.ci.b);
+            tma_load_4d(sm + O_B + BC_BYTES / 2, &tmB, &bar[0], 64, w.g, w.ci.t0, w.ci.b);
+            tma_load_4d(sm + O_C, &tmC, &bar[0], 0, w.g, w.ci.t0, w.ci.b);
+            tma_load_4d(sm + O_C + BC_BYTES / 2, &tmC, &bar[0], 64, w.g, w.ci.t0, w.ci.b);
+            stage_head(w, w.h0);
+            load_head(w, w.h0);
+        }
+        ++bc_issued;
+        ++st_issued;
+        ++ld_issued;
+    };
+    // dt_raw + bias of position tid for a head (0 past the chunk's end)
+    auto load_dtv = [&](const ChunkInfo &c, int h) -> float {
+        return tid < c.len ? p.dt_raw[(int64_t)c.b * p.sdb + (int64_t)(c.t0 + tid) * p.sdl + h] +
+                                 (p.bias ? p.bias[h] : 0.f)
+                           : 0.f;
+    };
+    if (tid == 0) s_item[0] = take();
+    __syncthreads();
+    Item cur;
+    bool have = s_item[0] < p.n_items;
+    float dt_next = 0.f, A_next = 0.f, D_next = 0.f;
+    if (have) {
+        decode(s_item[0], cur);
+        issue_first(cur);
+        dt_next = load_dtv(cur.ci, cur.h0);
+        A_next = p.A[cur.h0];
+        D_next = p.D ? p.D[cur.h0] : 0.f;
+    }
+
+    while (have) {   // work items
+    const int item = cur.item, nsub = cur.nsub, k = cur.k, g = cur.g, HS = cur.HS, h0 = cur.h0;
+    const bool tail = cur.tail;
+    const ChunkInfo ci = cur.ci;
+    Item nxt;
+    bool have_next = false;
+    const int64_t tok = (int64_t)ci.t0 + row;
+    const bool live = row < ci.len;
+
     for (int hi = 0; hi < HS; ++hi) {
         const int h = h0 + hi;
+        if (hi + 1 == HS && tid == 0) s_item[0] = take();   // the item after this one (read after the head's syncs)
         const float Dh = D_next, Ah = A_next;
         const float vcur = dt_next;   // dt_raw + bias at position tid
         {   // dt and the in-chunk cumulative log-decay (cs2 = cs log2 e)
@@ -601,7 +659,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         }
         wait_mma();
         if (hi + 1 < HS) {
-            dt_next = load_dtv(h + 1);
+            dt_next = load_dtv(ci, h + 1);
             A_next = p.A[h + 1];
             D_next = p.D ? p.D[h + 1] : 0.f;
         }
@@ -694,14 +752,22 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         }
         wait_mma2();   // the dB/dC chains are done: no MMA reads smem now
         __syncthreads();
-        // E', w o x, dS, x and S_in are free: fetch the next head's inputs
+        // B, C, E', w o x, dS, x and S_in are free: fetch the next head's inputs (or the next
+        // item's B/C and first-head inputs)
         if (hi + 1 < HS) {
             if (tid == 0) {
-                stage_head(h + 1);
-                load_head(h + 1);
+                stage_head(cur, h + 1);
+                load_head(cur, h + 1);
             }
             ++st_issued;
             ++ld_issued;
+        } else if (s_item[0] < p.n_items) {
+            decode(s_item[0], nxt);
+            have_next = true;
+            issue_first(nxt);
+            dt_next = load_dtv(nxt.ci, nxt.h0);
+            A_next = p.A[nxt.h0];
+            D_next = p.D ? p.D[nxt.h0] : 0.f;
         }
         {   // ---- per-position scalars (threads 0..127 = position i)
             const int i = tid;
@@ -763,10 +829,25 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         __syncthreads();
         tc_fence_after();
     }
-    // ---- dB, dC of the CTA's heads: final bf16 rows when the CTA covers the group, else fp32 shares
-    if (!aborted && !__syncthreads_or(bad)) {
-        const bool whole = p.hs == p.sh.hpg;
-        const int NSUB = H / HS;
+    // ---- dB, dC of the item's heads: final bf16 rows when the item covers the group; else
+    // fp32 shares, summed in subset order afterwards by k_reduce_group (main items) or
+    // k_reduce_tail (the split pairs of the tail)
+    if (aborted || __syncthreads_or(bad)) {
+        aborted = true;
+        break;
+    }
+    {
+        auto store_bf16 = [&](int which, const float *v) {
+            if (!live) return;
+            __nv_bfloat16 *dst = (which == 0 ? p.dB : p.dC) + (int64_t)ci.b * (which == 0 ? p.sdBb : p.sdCb) +
+                                 tok * (which == 0 ? p.sdBl : p.sdCl) + (int64_t)g * (which == 0 ? p.sdBg : p.sdCg) +
+                                 64 * hf;
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                d4[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                                   pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+        };
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
             const uint32_t col0 = (which == 0 ? T_DB : T_DC) + 64 * hf;
@@ -782,34 +863,57 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[32 + i] = t[i];
             }
-            if (whole) {
-                if (live) {
-                    __nv_bfloat16 *dst = (which == 0 ? p.dB : p.dC) +
-                                         (int64_t)ci.b * (which == 0 ? p.sdBb : p.sdCb) +
-                                         tok * (which == 0 ? p.sdBl : p.sdCl) + (int64_t)g * (which == 0 ? p.sdBg : p.sdCg) +
-                                         64 * hf;
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        d4[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
-                                           pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
-                }
+            if (nsub == 1) {
+                store_bf16(which, v);
             } else {
-                float *dst = (which == 0 ? p.dBh : p.dCh) + (((int64_t)k * NSUB + jsub) * QT + row) * NT + 64 * hf;
+                float *dst = tail ? p.tpart + (((int64_t)(item - n_main) * 2 + which) * QT + row) * NT + 64 * hf
+                                  : (which == 0 ? p.dBh : p.dCh) +
+                                        (((int64_t)k * (H / p.hs) + h0 / p.hs) * QT + row) * NT + 64 * hf;
                 float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
                 for (int q = 0; q < 16; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         }
     }
+    tc_fence_before();
+    __syncthreads();   // dB/dC read from TMEM: the next item may start its chains
+    tc_fence_after();
+    have = have_next;
+    if (have) cur = nxt;
+    }   // work items
     // drain (only after an early stop) and free TMEM
     for (uint32_t q = ld_done; q < ld_issued; ++q) mbar_wait(&bar[1], q & 1);
     for (uint32_t q = st_done; q < st_issued; ++q) mbar_wait(&bar[3], q & 1);
-    if (bc_done == 0) mbar_wait(&bar[0], 0);
+    for (uint32_t q = bc_done; q < bc_issued; ++q) mbar_wait(&bar[0], q & 1);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// dB/dC of the pairs (chunk, group) split into subsets at the tail of the gradient kernel:
+// the subsets' fp32 shares summed in subset order.  grid (tail pairs, 2 (dB, dC), Q/16), 256
+// threads: 16 rows x 128 columns of one pair, 8 values a thread.
+__global__ void __launch_bounds__(256)
+k_reduce_tail(const BwdParams p) {
+    const int tp = blockIdx.x, which = blockIdx.y, l0 = blockIdx.z * 16;
+    const int pair = p.k_pairs + tp, k = pair / p.sh.G, g = pair % p.sh.G;
+    if (p.hdr[HDR_STATUS] != 0 || k >= p.hdr[HDR_NCHUNKS]) return;
+    const ChunkInfo ci = p.chunks[k];
+    const int l = l0 + (threadIdx.x >> 4), n0 = (threadIdx.x & 15) * 8;
+    if (l >= ci.len) return;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < p.nsub_tail; ++j) {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            p.tpart + ((((int64_t)tp * p.nsub_tail + j) * 2 + which) * QT + l) * NT + n0);
+        const float4 a = src[0], b = src[1];
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    __nv_bfloat16 *dst = (which == 0 ? p.dB : p.dC) + (int64_t)ci.b * (which == 0 ? p.sdBb : p.sdCb) +
+                         (int64_t)(ci.t0 + l) * (which == 0 ? p.sdBl : p.sdCl) + (int64_t)g * (which == 0 ? p.sdBg : p.sdCg) + n0;
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
+                                                 pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_b() {
@@ -857,6 +961,7 @@ static BwdParams make_params(const Shape &sh, const int32_t *hdr, const ChunkInf
     p.dB = (__nv_bfloat16 *)a.dB; p.dC = (__nv_bfloat16 *)a.dC;
     p.sdBb = a.sdB ? a.sdB[0] : 0; p.sdBl = a.sdB ? a.sdB[1] : 0; p.sdBg = a.sdB ? a.sdB[2] : 0;
     p.sdCb = a.sdC ? a.sdC[0] : 0; p.sdCl = a.sdC ? a.sdC[1] : 0; p.sdCg = a.sdC ? a.sdC[2] : 0;
+    p.k_pairs = a.k_pairs; p.nsub_tail = a.nsub_tail; p.n_items = a.n_items; p.tpart = a.tpart;
     return p;
 }
 
@@ -897,7 +1002,13 @@ cudaError_t launch_bwd_chunk_tc(const Shape &sh, const int32_t *hdr, const Chunk
     static int attr_done[64] = {0};
     cudaError_t e = ensure_smem_attr(k_bwd_chunk_tc, (int)BWD_SMEM, attr_done);
     if (e != cudaSuccess) return e;
-    k_bwd_chunk_tc<<<dim3(sh.kmax, sh.H / a.hs), 256, BWD_SMEM, st>>>(mx, mb, mc, ms, mdy, mz, p);
+    if (a.grid > 0) k_bwd_chunk_tc<<<a.grid, 256, BWD_SMEM, st>>>(mx, mb, mc, ms, mdy, mz, p);   // persistent
+    const int tail_pairs = sh.kmax * sh.G - a.k_pairs;
+    if (a.grid > 0 && tail_pairs > 0 && a.nsub_tail > 1 && a.hs == sh.hpg) {
+        cudaError_t e2 = cudaGetLastError();
+        if (e2 != cudaSuccess) return e2;
+        k_reduce_tail<<<dim3(tail_pairs, 2, QT / 16), 256, 0, st>>>(p);
+    }
     return cudaGetLastError();
 }
 

@@ -18,6 +18,7 @@ enum HeaderWord {
     HDR_STATUS = 3,    // device-side ssd_status (first error wins)
     HDR_TICKET = 4,    // fused path: next unit ticket
     HDR_MAXSEG = 5,    // fused path: largest number of units in one sequence
+    HDR_TICKET2 = 6,   // tensor-core backward: next work item of the gradient kernel
     HDR_WORDS = 64
 };
 
@@ -63,6 +64,10 @@ struct BwdTcArgs {
     float *dS, *chunk_lam, *dBh, *dCh, *partials;
     int hs;                         // heads per CTA of the gradient kernel (divides H/G)
     int hs_ds;                      // heads per CTA of the dstates kernel (divides H/G)
+    // gradient kernel work items: pairs (chunk, group) below k_pairs in H/G/hs subsets of hs
+    // heads, the rest in nsub_tail subsets whose dB/dC shares (tpart) are summed afterwards
+    int k_pairs, nsub_tail, n_items, grid;   // grid: persistent CTAs (one per SM at most)
+    float *tpart;                   // [tail item][2][Q][N] fp32
     void *dB, *dC;                  // final dB/dC (written directly when hs == H/G)
     const int64_t *sdB, *sdC;
 };
