@@ -94,7 +94,8 @@ typedef struct {
 typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs;
     int32_t algo;        /* ssd_algo */
-    int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..4 */
+    int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..5
+                            (1..4 for the backward) */
     int32_t bwd_heads;   /* tensor-core backward: heads per CTA, 0 = library choice, else a divisor
                             of nheads/ngroups no larger than 32 */
     int32_t reserved0;   /* must be 0 */

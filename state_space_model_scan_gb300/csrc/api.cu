@@ -45,6 +45,7 @@ size_t bwd_chunk_smem(const Shape &sh);
 size_t chunk_scan_smem(const Shape &sh);
 // fused_fwd.cu
 int fused_rmax();
+int fused_rmax_states();
 int fused_block_units();
 // bwd_tc.cu
 cudaError_t launch_bwd_dstates_tc(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const BwdTcArgs &a,
@@ -241,13 +242,26 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     int64_t umax = 0;
     if (fused) {
         R = p->seg_chunks;
+        const int rmax = bwd ? fused_rmax_states() : fused_rmax();
         if (R == 0) {
-            // enough units for about eight tickets per SM, chunks of a unit at most the compiled maximum
-            const int64_t target = 8LL * num_sms();
-            int64_t r = (kmax * H + target - 1) / target;
-            R = (int)(r < 1 ? 1 : (r > 4 ? 4 : r));
+            // Chunks per unit from a model of the persistent kernel: rounds of resident CTAs
+            // (two per SM) times one unit's time, R chunks plus a fixed part (unit prologue and
+            // carry-in fold).  Per-chunk cost: full forward about 9.3 us, states-only (the
+            // backward's recompute) about 2.3 us; fixed part about 8 us.
+            const int64_t slots = 2LL * num_sms();
+            const double c_chunk = bwd ? 2.3 : 9.3, c_unit = 8.0;
+            double best = 1e300;
+            for (int r = 1; r <= rmax; ++r) {
+                const int64_t units = varlen ? (kmax + r - 1) / r + S : B * (((L + Q - 1) / Q + r - 1) / r);
+                const int64_t rounds = (units * H + slots - 1) / slots;
+                const double cost = (double)rounds * (r * c_chunk + c_unit);
+                if (cost < best) {
+                    best = cost;
+                    R = r;
+                }
+            }
         }
-        if (R > fused_rmax()) return SSD_ERR_UNSUPPORTED;
+        if (R > rmax) return SSD_ERR_UNSUPPORTED;
         num = 1;   // units per chunk: 1/R (the metadata kernel also accepts a larger ratio)
         den = R;
         // units: sum over sequences of max(ceil(n/R), ceil(n num/den)) <= kmax max(1/R, num/den) + S

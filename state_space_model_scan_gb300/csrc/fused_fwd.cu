@@ -44,7 +44,8 @@ using namespace tc;
 constexpr int QT = 128;   // chunk length
 constexpr int PT = 64;    // head dim
 constexpr int NT = 128;   // state dim
-constexpr int RMAX = 4;   // max chunks per unit
+constexpr int RMAX = 5;   // max chunks per unit (states-only mode: 4, one 64-column TMEM slice each)
+constexpr int RMAX_STATES = 4;
 constexpr int KB = 4;     // segments per block of the carry-in fold
 constexpr int NTHR = 128; // one thread per tile row / TMEM lane
 
@@ -109,7 +110,7 @@ struct Misc {
     uint32_t tmem_base;
     int tnext;        // ticket of the next unit (taken at the start of the current one)
     int abort_;
-    float wsum[4];
+    float wsum[8];      // chunk totals of the unit prologue
     float A_next, bias_next;   // A and dt_bias of the next unit's head (cp.async)
     UnitInfo ui_next;
 };
@@ -265,13 +266,14 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     const int64_t unit_stride = (int64_t)NT * PT;   // floats per (unit, head) aggregate
 
     // Inputs of a unit's dt prologue, fetched ahead by cp.async: thread (warp w, lane j)
-    // copies raw dt of chunk w, positions 4j..4j+3 (the values it scans), thread 0 A and dt_bias.
+    // copies raw dt of chunks w and w+4, positions 4j..4j+3 (the values it scans), thread 0
+    // A and dt_bias.
     const int lane = tid & 31;
     auto fetch_unit_inputs = [&](const UnitInfo &un, int hn) {
-        if (warp < un.nchunk) {
+        for (int c = warp; c < un.nchunk; c += NTHR / 32) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int pos = warp * QT + 4 * lane + i;
+                const int pos = c * QT + 4 * lane + i;
                 if (pos < un.len)
                     cp_async4(dtn + pos, p.dt_raw + (int64_t)un.b * p.sdb + (int64_t)(un.t0 + pos) * p.sdl + hn);
             }
@@ -302,47 +304,54 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         if (ui.nchunk > 1) load_xb(BAR_C, Ws, Cs, h, g, ui.t0 + QT, ui.b);
 
         // ---- dt over the unit, chunk-local and unit-level cumulative log-decay, phase-1 weights.
-        // Warp w scans chunk w (four positions per lane); chunk totals meet in smem.
         cp_async_wait_all();
         __syncthreads();
         const float Ah = ms->A_next;
         float lam_u;
-        {
+        {   // warp w scans chunks w and w + 4 (four positions per lane); chunk totals meet in smem
+            constexpr int NR = (RMAX + NTHR / 32 - 1) / (NTHR / 32);
             const float bias = p.bias ? ms->bias_next : 0.f;
-            const bool wact = warp < ui.nchunk;
-            float dt4[4], loc[4], run = 0.f;
+            float dt4[NR][4], cs4[NR][4], last[NR];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int pos = warp * QT + 4 * lane + i;
-                dt4[i] = (wact && pos < ui.len) ? softplus_f(dtn[pos] + bias) : 0.f;
-                run += dt4[i] * Ah;
-                loc[i] = run;
+            for (int r = 0; r < NR; ++r) {
+                const int c = warp + r * (NTHR / 32);
+                const bool wact = c < ui.nchunk;
+                float run = 0.f, loc[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int pos = c * QT + 4 * lane + i;
+                    dt4[r][i] = (wact && pos < ui.len) ? softplus_f(dtn[pos] + bias) : 0.f;
+                    run += dt4[r][i] * Ah;
+                    loc[i] = run;
+                }
+                const float incl = warp_incl_sum(run);
+                const float excl = incl - run;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cs4[r][i] = excl + loc[i];
+                last[r] = __shfl_sync(0xffffffffu, cs4[r][3], lane | 7);   // cs at the 32-block's end
+                const float ctot = __shfl_sync(0xffffffffu, incl, 31);
+                if (lane == 0 && c < 8) ms->wsum[c] = wact ? ctot : 0.f;
             }
-            const float incl = warp_incl_sum(run);
-            const float excl = incl - run;
-            const float ctot = __shfl_sync(0xffffffffu, incl, 31);
-            if (lane == 0) ms->wsum[warp] = wact ? ctot : 0.f;
             __syncthreads();
-            float off = 0.f, tot = 0.f;
-#pragma unroll
-            for (int w = 0; w < NTHR / 32; ++w) {
-                const float t = ms->wsum[w];
-                if (w < warp) off += t;
-                tot += t;
-            }
+            float tot = 0.f;
+            for (int c = 0; c < ui.nchunk; ++c) tot += ms->wsum[c];
             lam_u = tot;
-            const float last = __shfl_sync(0xffffffffu, excl + loc[3], lane | 7);   // cs at the 32-block's end
-            if (wact) {
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const int c = warp + r * (NTHR / 32);
+                if (c >= ui.nchunk) continue;
+                float off = 0.f;
+                for (int c2 = 0; c2 < c; ++c2) off += ms->wsum[c2];
                 float pc[4], pw[4], pf[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float cs = excl + loc[i];
+                    const float cs = cs4[r][i];
                     pc[i] = cs * LOG2E;
-                    pw[i] = dt4[i] * ex2((lam_u - (off + cs)) * LOG2E);
-                    pf[i] = dt4[i] * ex2((last - cs) * LOG2E);
+                    pw[i] = dt4[r][i] * ex2((lam_u - (off + cs)) * LOG2E);
+                    pf[i] = dt4[r][i] * ex2((last[r] - cs) * LOG2E);
                 }
-                const int b4 = warp * QT + 4 * lane;
-                *reinterpret_cast<float4 *>(dtu + b4) = make_float4(dt4[0], dt4[1], dt4[2], dt4[3]);
+                const int b4 = c * QT + 4 * lane;
+                *reinterpret_cast<float4 *>(dtu + b4) = make_float4(dt4[r][0], dt4[r][1], dt4[r][2], dt4[r][3]);
                 *reinterpret_cast<float4 *>(cs2u + b4) = make_float4(pc[0], pc[1], pc[2], pc[3]);
                 *reinterpret_cast<float4 *>(wu + b4) = make_float4(pw[0], pw[1], pw[2], pw[3]);
                 *reinterpret_cast<float4 *>(cfu + b4) = make_float4(pf[0], pf[1], pf[2], pf[3]);
@@ -728,6 +737,7 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t inner, int64_t d1, int64_
 }  // namespace
 
 int fused_rmax() { return RMAX; }
+int fused_rmax_states() { return RMAX_STATES; }
 int fused_block_units() { return KB; }
 
 cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *units, const void *x, const int64_t *sx,

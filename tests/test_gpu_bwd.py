@@ -133,3 +133,13 @@ def test_bwd_heads_invalid():
     for hs in (5, 33, -1):
         with pytest.raises(SSDError):
             gpu_backward(w, inp, algo="fused", bwd_heads=hs)
+
+
+def test_bwd_rejects_five_chunk_units():
+    """The backward's state recompute keeps each chunk of a unit in its own TMEM slice, four at
+    most: five-chunk units are refused (the forward accepts them)."""
+    from state_space_model_scan_gb300._lib import SSDError
+    w = W(L=700, H=4, P=64, G=2, N=128, Q=128, dtype="bf16")
+    inp = I.make_inputs(w, with_grad_inputs=True)
+    with pytest.raises(SSDError):
+        gpu_backward(w, inp, algo="fused", seg_chunks=5)

@@ -71,7 +71,7 @@ def test_bf16_cases(algo, case):
     check_fwd(W(dtype="bf16", **case), algo=algo)
 
 
-@pytest.mark.parametrize("seg", [1, 2, 3, 4])
+@pytest.mark.parametrize("seg", [1, 2, 3, 4, 5])
 def test_fused_units_and_lookback(seg):
     """Several work units per sequence: every unit's carry-in comes from the
     predecessors' published aggregates / end states."""
