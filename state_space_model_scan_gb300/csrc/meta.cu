@@ -119,15 +119,19 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
         return;
     }
     __syncthreads();
-    // pass 2: the chunk list, sequence by sequence
-    for (int s = tid; s < S; s += blockDim.x) {
-        SeqInfo si = seqs[s];
-        int nch = (si.len + Q - 1) / Q;
-        for (int c = 0; c < nch; ++c) {
-            ChunkInfo ci;
-            ci.seq = s; ci.b = si.b; ci.t0 = si.t0 + c * Q; ci.len = min(Q, si.len - c * Q);
-            chunks[si.chunk0 + c] = ci;
+    // pass 2: the chunk list, one thread per chunk; its sequence is the last one whose first
+    // chunk is not after it (empty sequences share their successor's first chunk)
+    for (int c = tid; c < nchunks; c += blockDim.x) {
+        int lo = 0, hi = S - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (seqs[mid].chunk0 <= c) lo = mid; else hi = mid - 1;
         }
+        const SeqInfo si = seqs[lo];
+        const int j = c - si.chunk0;
+        ChunkInfo ci;
+        ci.seq = lo; ci.b = si.b; ci.t0 = si.t0 + j * Q; ci.len = min(Q, si.len - j * Q);
+        chunks[c] = ci;
     }
     // pass 3: work units ordered by (block of KB segments, sequence, segment)
     int nunits = 0;
