@@ -93,13 +93,16 @@ struct Plan {
     size_t total = 0;
 };
 
-// Heads per CTA of the tensor-core gradient kernel: a divisor of H/G up to 32.  A
-// CTA (one per SM, by its shared memory) loads B and C of its chunk once for all its
-// heads and writes final dB/dC when it covers the whole group; otherwise a reduction
-// reads back fp32 shares of dB and dC for every head subset.  The choice minimises
-// the estimated time: whole waves of CTAs, each a head iteration of about 8 us per
+// Heads per work item of the tensor-core gradient kernel: a divisor of H/G up to 32.  An
+// item loads B and C of its chunk once for all its heads and writes final dB/dC when it
+// covers the whole group; otherwise a reduction reads back fp32 shares of dB and dC for
+// every head subset.  Groups of at most 8 heads are whole items; for larger groups the
+// choice minimises the estimated time: whole rounds of items over the SMs, about 8 us per
 // head, plus that reduction's traffic at about 5 TB/s.
 int bwd_heads_per_cta(int64_t kmax, int64_t H, int hpg) {
+    // groups of at most 8 heads: whole-group items (no dB/dC reduction; the persistent kernel
+    // splits the pairs of its last partial wave itself)
+    if (hpg <= 8) return hpg;
     const int64_t sms = num_sms();
     int best = 1;
     double best_us = 1e300;

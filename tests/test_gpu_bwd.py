@@ -143,3 +143,15 @@ def test_bwd_rejects_five_chunk_units():
     inp = I.make_inputs(w, with_grad_inputs=True)
     with pytest.raises(SSDError):
         gpu_backward(w, inp, algo="fused", seg_chunks=5)
+
+
+@pytest.mark.parametrize("lens", [None, [1000, 3000, 1120]])
+def test_bwd_tail_split(lens):
+    """More (chunk, group) pairs than SMs: the gradient kernel's last partial wave is split into
+    2-head items whose dB/dC shares are summed afterwards; packed sequences also leave work items
+    past the real chunk count, which are skipped."""
+    if lens is None:
+        w = W(L=128 * 40, H=32, P=64, G=4, N=128, Q=128, dtype="bf16", has_z=True, has_init=True)
+    else:
+        w = I.Workload("v", 1, sum(lens), 32, 64, 4, 128, 128, "bf16", has_z=True, has_init=True, seqlens=lens)
+    check_bwd(w, algo="fused")
