@@ -143,6 +143,19 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(vals, device="cpu"):
+    """Each value's maximum over the ranks of the default process group (unchanged without
+    one).  The bench reports whole-job throughput as the units of all ranks over the slowest
+    rank's time."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 _ORACLE_INPUTS = {}
 
 
@@ -273,10 +286,7 @@ def run_gpu(args):
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     fwd_mean = sum(fwd_ms) / len(fwd_ms)
     step_mean = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / len(fwd_ms)
-    if world > 1:
-        t = torch.tensor([fwd_mean, step_mean], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        fwd_mean, step_mean = float(t[0]), float(t[1])
+    fwd_mean, step_mean = max_over_ranks([fwd_mean, step_mean], device=dev)
     toks = w.batch * w.seqlen
     value = world * toks / (fwd_mean * 1e-3)
 
@@ -334,7 +344,7 @@ def run_gpu(args):
     s_out.wait_event(ev_c[(args.steps - 1) % nset])
     e1.record(s_out)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / args.steps], device=dev)[0]
     e2e_val = world * toks / (e2e_ms * 1e-3)
 
     if rank != 0:
