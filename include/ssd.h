@@ -153,6 +153,20 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *args, void *work
 ssd_status ssd_query_status(const void *workspace, void *stream);
 
 /*
+ * ssd_selftest_bounded_wait
+ * Self-test of the device-side failure path (no counterpart on the source pages):
+ * enqueues on `stream` one thread block that clears the workspace's status word and
+ * then waits for a flag in the workspace header that nothing sets, polling exactly as
+ * the kernels' inter-CTA waits do but giving up after `wait_ms` milliseconds (1..2000),
+ * when it records SSD_ERR_DEVICE_TIMEOUT as a kernel whose peer never arrives would.
+ * Read the result with ssd_query_status; the context stays usable.  The workspace must
+ * be device memory of at least 256 bytes (the header); it is scratch for later calls.
+ * Returns SSD_ERR_INVALID_ARGUMENT for a NULL or short workspace or a limit out of
+ * range, SSD_ERR_CUDA if the launch fails.
+ */
+ssd_status ssd_selftest_bounded_wait(void *workspace, size_t workspace_bytes, int32_t wait_ms, void *stream);
+
+/*
  * ssd_fwd_noalloc
  * The forward scan (same operation, arguments and results as ssd_fwd) for
  * callers that cannot allocate device memory where they run it: code running

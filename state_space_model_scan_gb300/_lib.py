@@ -21,7 +21,8 @@ ALGO = {"auto": 0, "staged": 1, "fused": 2}
 
 # Every symbol include/ssd.h declares.
 EXPORTS = ["ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
-           "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout", "ssd_fwd_noalloc"]
+           "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout", "ssd_fwd_noalloc",
+           "ssd_selftest_bounded_wait"]
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -85,8 +86,9 @@ def load(path: str = LIB_PATH):
     lib.ssd_abi_version.restype = ctypes.c_int32
     lib.ssd_fwd_debug_layout.argtypes = [P(Problem), P(FwdArgs), P(DebugLayout)]
     lib.ssd_fwd_noalloc.argtypes = [P(Problem), P(FwdArgs), ctypes.c_void_p]
+    lib.ssd_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p]
     for f in ("ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
-              "ssd_fwd_debug_layout", "ssd_fwd_noalloc"):
+              "ssd_fwd_debug_layout", "ssd_fwd_noalloc", "ssd_selftest_bounded_wait"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -175,6 +177,13 @@ def ssd_bwd(prob, args, workspace, stream=None):
 def ssd_fwd_noalloc(prob, args, stream=None):
     """Raw call of the forward that uses the library's static scratch (no workspace)."""
     return load().ssd_fwd_noalloc(ctypes.byref(prob), ctypes.byref(args), _stream_handle(stream))
+
+
+def selftest_bounded_wait(workspace, wait_ms, stream=None):
+    """Enqueue the bounded-wait self-test (see include/ssd.h); read the result with query_status."""
+    return int(load().ssd_selftest_bounded_wait(ctypes.c_void_p(workspace.data_ptr()),
+                                                ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                                ctypes.c_int32(wait_ms), _stream_handle(stream)))
 
 
 def query_status(workspace, stream=None):

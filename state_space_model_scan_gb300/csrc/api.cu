@@ -10,6 +10,7 @@ cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int
                               int umax, int32_t *hdr,
                               SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units, int32_t *last_unit,
                               uint32_t *zero_words, int64_t n_zero, cudaStream_t st);
+cudaError_t launch_wait_probe(int32_t *hdr, int wait_ms, cudaStream_t st);
 cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr, const float *init,
                                    float *final_, cudaStream_t st);
 // simt_fwd.cu
@@ -596,6 +597,13 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         }
     }
     SSD_CUDA(launch_reduce_heads(sh, hdr, part, (float *)b->dA.ptr, (float *)b->dD.ptr, (float *)b->ddt_bias.ptr, st));
+    return SSD_OK;
+}
+
+ssd_status ssd_selftest_bounded_wait(void *ws, size_t ws_bytes, int32_t wait_ms, void *stream) {
+    if (ws == nullptr || ws_bytes < HDR_WORDS * sizeof(int32_t) || wait_ms < 1 || wait_ms > 2000)
+        return SSD_ERR_INVALID_ARGUMENT;
+    if (launch_wait_probe(static_cast<int32_t *>(ws), wait_ms, (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
     return SSD_OK;
 }
 

@@ -19,6 +19,7 @@ enum HeaderWord {
     HDR_TICKET = 4,    // fused path: next unit ticket
     HDR_MAXSEG = 5,    // fused path: largest number of units in one sequence
     HDR_TICKET2 = 6,   // tensor-core backward: next work item of the gradient kernel
+    HDR_PROBE = 7,     // ssd_selftest_bounded_wait: the flag nothing sets
     HDR_WORDS = 64
 };
 

@@ -192,7 +192,31 @@ __global__ void k_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, con
     for (int i = threadIdx.x; i < PN; i += blockDim.x) final_[base + i] = init ? init[base + i] : 0.f;
 }
 
+// One block: clear the status word, then wait (bounded) for a header flag nothing sets.
+__global__ void k_wait_probe(int32_t *hdr, uint64_t limit_ns) {
+    if (threadIdx.x != 0) return;
+    hdr[HDR_STATUS] = 0;
+    hdr[HDR_PROBE] = 0;
+    __threadfence();
+    volatile int32_t *flag = hdr + HDR_PROBE;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (;;) {
+        if (*flag != 0) return;
+        uint64_t t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 > limit_ns) break;
+        __nanosleep(1000);
+    }
+    set_status(hdr, SSD_ERR_DEVICE_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(int32_t *hdr, int wait_ms, cudaStream_t st) {
+    k_wait_probe<<<1, 32, 0, st>>>(hdr, (uint64_t)wait_ms * 1000000ull);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int num, int den, int KB,
                               int kmax, int umax, int32_t *hdr, SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units,

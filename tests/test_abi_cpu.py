@@ -178,3 +178,10 @@ def test_metadata_balanced_units():
     # never fewer units than ceil(n/R), never more than n
     assert len(meta.build(batch=1, seqlen=640, Q=64, R=4, num=1, den=100)["units"]) == 3
     assert len(meta.build(batch=1, seqlen=640, Q=64, R=4, num=5, den=1)["units"]) == 10
+
+
+def test_selftest_bounded_wait_validates_on_host(lib):
+    """Argument checks happen before any launch (no GPU needed)."""
+    import ctypes
+    m = lib.load()
+    assert m.ssd_selftest_bounded_wait(None, ctypes.c_size_t(4096), 10, None) == 1
