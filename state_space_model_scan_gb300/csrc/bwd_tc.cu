@@ -304,13 +304,14 @@ constexpr uint32_t T_DM = 384;                            // group 1
 constexpr uint32_t T_DXD = 384, T_DXS = 448;              // group 2
 constexpr uint32_t T_YD = 384, T_YO = 448;                // group 3 (+ dB, dC)
 
-// grid (kmax, H / HS): one chunk and HS heads of one group per CTA (HS divides H/G).
-// B and C are loaded once.  Every per-head input arrives one head ahead: dy, z and
-// dS land in the E', w o x and dS tiles as soon as the previous head's second MMA
-// group has consumed them, x and S_in as soon as its third has, and dt is read into
-// a register, so no head waits on global memory.  dB and dC accumulate over the
-// CTA's heads in TMEM and are written once: as bf16 outputs when the CTA covers the
-// whole group, else as fp32 shares summed later in head order.
+// Persistent: at most one CTA per SM, taking work items (chunk, group, subset of HS
+// heads; HS divides H/G) from a ticket.  An item loads B and C once and computes C B^T
+// once for its heads.  Every per-head input arrives one head ahead: dy, z and dS land in
+// the E', w o x and dS tiles once the previous head's MMAs have consumed them, x and S_in
+// likewise, and dt is read into a register, so no head waits on global memory; the next
+// item's B/C and first-head inputs are loaded during the current item's last head.  dB and
+// dC accumulate over the item's heads in TMEM and are written once: as bf16 outputs when
+// the item covers the whole group, else as fp32 shares summed afterwards in subset order.
 __global__ void __launch_bounds__(256, 1)
 k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
