@@ -96,8 +96,10 @@ typedef struct {
     int32_t algo;        /* ssd_algo */
     int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..5
                             (1..4 for the backward) */
-    int32_t bwd_heads;   /* tensor-core backward: heads per CTA, 0 = library choice, else a divisor
-                            of nheads/ngroups no larger than 32 */
+    int32_t bwd_heads;   /* tensor-core backward: heads per work item of the gradient kernel,
+                            0 = library choice (whole groups of up to 8 heads, with the last
+                            partial wave split into 2-head items), else a divisor of
+                            nheads/ngroups no larger than 32 (no split) */
     int32_t reserved0;   /* must be 0 */
 } ssd_problem;
 
