@@ -71,7 +71,8 @@ constexpr uint32_t OFF_MISC = OFF_DTN + RMAX * QT * 4;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 256 + 1024;   // + alignment slack
 
 // TMEM columns (256 per CTA)
-constexpr uint32_t TM_CB = 0;     // [0,128) CB, then [0,64) Y_diag (+ D x)
+constexpr uint32_t TM_CB = 0;     // [0,128) CB; then [0,64) M (bf16 pairs, the Y_diag A operand), [64,128) Y_diag
+constexpr uint32_t TM_M = 0, TM_YD = 64;
 constexpr uint32_t TM_SC = 128;   // [128,192) chunk state^T (phase 1: unit aggregate^T)
 constexpr uint32_t TM_YO = 192;   // [192,256) C S_in^T
 constexpr uint32_t TM_COLS = 256;
@@ -557,6 +558,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             }
             commit();   // one barrier phase per commit, waited before the next commit: a parity
             wait_bar(BAR_MMA);   // wait cannot tell a barrier two phases ahead from one behind
+            if (full && more) load_bc(BAR_B, &tmB, Bs, g, tc0 + QT, ui.b);   // B is read by CB and S_c only
             if (full) {
                 // S_in (bf16, MN-major [n][p]: row n = this thread's 64 columns) over the w o x
                 // buffer, then Y_off = C S_in^T
@@ -610,13 +612,9 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                         for (int i = 0; i < 16; ++i) pk[i] = 0u;
                     }
-                    uint8_t *rowp = Bs + (sb >> 1) * (BC_BYTES / 2) + l * 128;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int cidx = ((sb & 1) << 2) + q;
-                        *reinterpret_cast<uint4 *>(rowp + ((cidx ^ (l & 7)) << 4)) =
-                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                    }
+                    // row l of M, columns [32 sb, 32 sb + 32): 16 packed pairs into this lane's TMEM
+                    // (a thread only ever touches its own lane, and this block's CB is already read)
+                    tmem_st16(tmem + lane_base + TM_M + 16 * sb, pk);
                 }
             }
             {   // carried state update: S_in[c+1] = a_c S_in[c] + S_c (row n)
@@ -633,21 +631,18 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             wait_bar(BAR_MMA);   // Y_off done: C and W free
             if (has_z) load_z(h, tc0, ui.b);
             if (more) load_bc(BAR_C, &tmC, Cs, g, tc0 + QT, ui.b);
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
-            __syncthreads();   // M visible
+            __syncthreads();   // M in TMEM
             if (tid == 0) {
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < QT / 16; ++k)   // Y_diag + D x = M x (K = source tokens)
-                    umma_bf16(tmem + TM_CB, kmaj(sB, k, BC_BYTES / 2), mnmaj(sX, k), idesc_yd, k > 0);
+                for (int k = 0; k < QT / 16; ++k)   // Y_diag + D x = M x (K = source tokens), M from TMEM
+                    umma_bf16_ta(tmem + TM_YD, tmem + TM_M + 8 * k, mnmaj(sX, k), idesc_yd, k > 0);
             }
             commit();
-            wait_bar(BAR_MMA);   // x, B free: next chunk's loads
-            if (more) {
-                load_x(h, tc0 + QT, ui.b);
-                load_bc(BAR_B, &tmB, Bs, g, tc0 + QT, ui.b);
-            }
+            wait_bar(BAR_MMA);   // x free: next chunk's x
+            if (more) load_x(h, tc0 + QT, ui.b);
             if (has_z) wait_bar(BAR_Z);
             {   // epilogue: row l
                 const int l = row;
@@ -657,7 +652,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float yd[32], yo[32];
-                    tmem_ld32(tmem + lane_base + TM_CB + 32 * half, yd);
+                    tmem_ld32(tmem + lane_base + TM_YD + 32 * half, yd);
                     tmem_ld32(tmem + lane_base + TM_YO + 32 * half, yo);
                     tmem_wait_ld();
                     if (l < clen) {
