@@ -1,13 +1,16 @@
 """Benchmark of the SSD scan hot path on GB300.
 
-One step = one forward (metadata + fused tensor-core forward) and one backward
-of the Nemotron-Nano-shaped workload (batch 1, L=8192, 64 heads x 64, 8 groups,
-dstate 128, chunk 128, z gate and D skip, bf16 x/B/C/z, fp32 dt/A/D/states),
-each replayed from a CUDA graph, with L2 flushed (256 MB write) before each step.
-`value` is forward tokens/s from CUDA events around the forward; `ms_per_step`
-is forward + backward device time; `e2e` is forward tokens/s with every step's inputs
-copied from pinned host memory and its y copied back inside the timed region, two
-independent steps in flight (copy-in, compute and copy-out streams).  Prints ONE JSON line.
+One step, on the Nemotron-Nano-shaped workload (batch 1, L=8192, 64 heads x 64,
+8 groups, dstate 128, chunk 128, z gate and D skip, bf16 x/B/C/z, fp32
+dt/A/D/states), each call replayed from a CUDA graph:
+  L2 flush (256 MB write), inference forward (metadata + fused tensor-core forward),
+  L2 flush, training step = forward that also keeps the carried chunk states +
+  backward that reads them (no states recompute).
+`value` is inference-forward tokens/s from CUDA events around that forward;
+`ms_per_step` is the training step's device time (forward + backward); `e2e` is
+forward tokens/s with every step's inputs copied from pinned host memory and its y
+copied back inside the timed region, two independent steps in flight (copy-in,
+compute and copy-out streams).  Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -231,7 +234,12 @@ def run_gpu(args):
     g = dict(dx=torch.empty_like(d["x"]), ddt=torch.empty_like(d["dt_raw"]),
              dA=torch.empty(H, device=dev), dB=torch.empty_like(d["B"]), dC=torch.empty_like(d["C"]),
              dD=torch.empty(H, device=dev), dz=torch.empty_like(d["z"]), ddt_bias=torch.empty(H, device=dev))
-    bfa = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], None, D=d["D"], z=d["z"], dt_bias=d["dt_bias"])
+    # the training step's forward keeps the carried chunk states; its backward reads them
+    cstates = torch.empty(_lib.chunk_states_size(prob, fargs), dtype=torch.uint8, device=dev)
+    fargs_t = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], z=d["z"],
+                            dt_bias=d["dt_bias"], final_states=fin, chunk_states=cstates)
+    bfa = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], None, D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                        chunk_states=cstates)
     bargs = _lib.bwd_args(bfa, d["dy"], g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], dD=g["dD"], dz=g["dz"],
                           ddt_bias=g["ddt_bias"])
     wsf = torch.empty(_lib.fwd_workspace_size(prob, fargs), dtype=torch.uint8, device=dev)
@@ -242,34 +250,43 @@ def run_gpu(args):
     # warm the calls once outside capture (module load, attributes)
     with torch.cuda.stream(s):
         _lib.check(_lib.ssd_fwd(prob, fargs, wsf, s), "ssd_fwd")
+        _lib.check(_lib.ssd_fwd(prob, fargs_t, wsf, s), "ssd_fwd")
         _lib.check(_lib.ssd_bwd(prob, bargs, wsb, s), "ssd_bwd")
     s.synchronize()
-    gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    gf, gft, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(gf, stream=s):
         _lib.check(_lib.ssd_fwd(prob, fargs, wsf, torch.cuda.current_stream()), "ssd_fwd")
+    with torch.cuda.graph(gft, stream=s):
+        _lib.check(_lib.ssd_fwd(prob, fargs_t, wsf, torch.cuda.current_stream()), "ssd_fwd")
     with torch.cuda.graph(gb, stream=s):
         _lib.check(_lib.ssd_bwd(prob, bargs, wsb, torch.cuda.current_stream()), "ssd_bwd")
-    # kernels per call: forward = metadata + fused forward; backward = metadata, forward in
-    # states-only mode, dstates, reverse state scan, gradient kernel, the tail pairs' dB/dC
+    # kernels per call: forward = metadata + fused forward; backward (chunk states kept by the
+    # forward) = metadata, dstates, reverse state scan, gradient kernel, the tail pairs' dB/dC
     # reduction, head reduction (the ncu launch list in profiles/ shows the same set)
-    launches_fwd, launches_bwd = 2, 7
+    launches_fwd, launches_bwd = 2, 6
 
     def step(ev=None):
         with torch.cuda.stream(s):
             flush.fill_(float(rank + 1))
             if ev is not None:
                 ev[0].record(s)
-            gf.replay()
+            gf.replay()                    # inference forward
             if ev is not None:
                 ev[1].record(s)
-            gb.replay()
+            flush.fill_(float(rank + 2))
             if ev is not None:
                 ev[2].record(s)
+            gft.replay()                   # training step: forward keeping the chunk states ...
+            if ev is not None:
+                ev[3].record(s)
+            gb.replay()                    # ... and the backward
+            if ev is not None:
+                ev[4].record(s)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -283,10 +300,12 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    fwdt_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    bwd_ms = [e[3].elapsed_time(e[4]) for e in evs]
     fwd_mean = sum(fwd_ms) / len(fwd_ms)
-    step_mean = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / len(fwd_ms)
-    fwd_mean, step_mean = max_over_ranks([fwd_mean, step_mean], device=dev)
+    fwdt_mean = sum(fwdt_ms) / len(fwdt_ms)
+    step_mean = sum(f + b for f, b in zip(fwdt_ms, bwd_ms)) / len(fwdt_ms)
+    fwd_mean, fwdt_mean, step_mean = max_over_ranks([fwd_mean, fwdt_mean, step_mean], device=dev)
     toks = w.batch * w.seqlen
     value = world * toks / (fwd_mean * 1e-3)
 
@@ -362,16 +381,17 @@ def run_gpu(args):
         "config": {"workload": workload_desc(w), "global_batch": w.batch * world, "seq_len": w.seqlen,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed before every step (256 MB write)", "timing": "CUDA graph replay, CUDA events"},
-        "fwd_ms": fwd_mean, "fwd_bwd_ms": step_mean, "bwd_ms": step_mean - fwd_mean,
+        "fwd_ms": fwd_mean, "fwd_bwd_ms": step_mean, "fwd_train_ms": fwdt_mean, "bwd_ms": step_mean - fwdt_mean,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "ssd_fwd (metadata + fused tensor-core forward)",
                      "algorithmic_bytes_per_launch": alg, "peak_source": peak_kind},
-        "bwd_roofline": {"bound": "hbm", "achieved": algorithmic_bytes(w, fwd=False) / ((step_mean - fwd_mean) * 1e-3)
+        "bwd_roofline": {"bound": "hbm", "achieved": algorithmic_bytes(w, fwd=False) / ((step_mean - fwdt_mean) * 1e-3)
                          / 1e9, "peak": peak, "unit": "GB/s",
                          "algorithmic_bytes_per_launch": algorithmic_bytes(w, fwd=False)},
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (launches_fwd + launches_bwd),
+        # library kernels in the two timed regions: the step loop and the end-to-end loop
+        "gpu_launches": args.steps * (2 * launches_fwd + launches_bwd) + args.steps * launches_fwd,
         "clocks": clk.summary(),
         "wall_s": wall,
     }

@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 2
+#define SSD_ABI_VERSION 3
 
 typedef enum {
     SSD_OK = 0,
@@ -107,6 +107,10 @@ typedef struct {
     ssd_tensor x, dt, A, B, C, D, z, dt_bias, initial_states;   /* inputs; D, z, dt_bias, initial_states optional */
     ssd_tensor y, final_states;                                 /* outputs; final_states optional */
     const int32_t *cu_seqlens;                                  /* optional device array (see above) */
+    void *chunk_states;   /* optional device buffer of ssd_chunk_states_size bytes, 16-byte aligned
+                             (tensor-core path only): ssd_fwd writes the carried state entering
+                             every chunk into it; ssd_bwd, given the same pointer in its `fwd`
+                             arguments, reads them instead of recomputing them */
 } ssd_fwd_args;
 
 typedef struct {
@@ -118,7 +122,9 @@ typedef struct {
 
 /*
  * ssd_fwd_workspace_size / ssd_fwd
- * Forward scan: y and (optionally) final_states from the inputs.
+ * Forward scan: y and (optionally) final_states from the inputs; with
+ * args->chunk_states set, also the carried state entering every chunk (for a
+ * later ssd_bwd; see ssd_chunk_states_size).
  * Defined by the recurrence above; steps: chunk cumsum of dt*A, intra-chunk
  * C.B^T under the segment-sum decay mask, chunk states, inter-chunk state
  * passing, chunk output (Mamba-3-Lite "SSD Reference", sections "Chunking and
@@ -133,12 +139,29 @@ ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *args, void *work
                    size_t workspace_bytes, void *stream);
 
 /*
+ * ssd_chunk_states_size
+ * Size of the chunk-state buffer (ssd_fwd_args.chunk_states) for a problem that
+ * takes the tensor-core path: one 16 KB tile per (chunk, head) of the library's
+ * 128-token chunk grid (the carried state entering the chunk, bf16 -- the value the
+ * scan's readout C . h of that chunk starts from; Mamba-3-Lite "SSD Reference",
+ * section "Inter-chunk propagation -- the fixed contract"), for the largest chunk
+ * count the problem can have.  The tile layout is internal to the library (it is
+ * the operand layout of the backward's tensor-core kernel); its only use is to be
+ * handed from ssd_fwd to ssd_bwd of the same problem, inputs and cu_seqlens
+ * contents, in stream order.  Returns SSD_ERR_UNSUPPORTED for a problem that takes
+ * the SIMT path (which recomputes its states in the backward).
+ */
+ssd_status ssd_chunk_states_size(const ssd_problem *prob, const ssd_fwd_args *args, size_t *bytes);
+
+/*
  * ssd_bwd_workspace_size / ssd_bwd
  * Gradients of L = sum(dy * y) + sum(dfinal_states * final_states) with respect
  * to x, dt (the raw input, through softplus), A, B, C, and D, z, dt_bias,
  * initial_states when given.  dB/dC sum over the heads of each group.  All
  * reductions run in a fixed order: results are bitwise reproducible.
- * The forward is recomputed inside (no saved activations are needed).
+ * The carried chunk states are recomputed inside (no saved activations are
+ * needed) unless args->fwd.chunk_states holds the ones an ssd_fwd call of the same
+ * problem and inputs wrote; then the recompute is skipped.
  * Same workspace rules as ssd_fwd.
  */
 ssd_status ssd_bwd_workspace_size(const ssd_problem *prob, const ssd_bwd_args *args, size_t *bytes);

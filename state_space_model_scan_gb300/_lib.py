@@ -22,7 +22,7 @@ ALGO = {"auto": 0, "staged": 1, "fused": 2}
 # Every symbol include/ssd.h declares.
 EXPORTS = ["ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
            "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout", "ssd_fwd_noalloc",
-           "ssd_selftest_bounded_wait"]
+           "ssd_selftest_bounded_wait", "ssd_chunk_states_size"]
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -48,7 +48,7 @@ _FWD_FIELDS = ["x", "dt", "A", "B", "C", "D", "z", "dt_bias", "initial_states", 
 
 
 class FwdArgs(ctypes.Structure):
-    _fields_ = [(n, Tensor) for n in _FWD_FIELDS] + [("cu_seqlens", ctypes.c_void_p)]
+    _fields_ = [(n, Tensor) for n in _FWD_FIELDS] + [("cu_seqlens", ctypes.c_void_p), ("chunk_states", ctypes.c_void_p)]
 
 
 _BWD_FIELDS = ["dy", "dfinal_states", "dx", "ddt", "dA", "dB", "dC", "dD", "dz", "ddt_bias", "dinitial_states"]
@@ -87,8 +87,9 @@ def load(path: str = LIB_PATH):
     lib.ssd_fwd_debug_layout.argtypes = [P(Problem), P(FwdArgs), P(DebugLayout)]
     lib.ssd_fwd_noalloc.argtypes = [P(Problem), P(FwdArgs), ctypes.c_void_p]
     lib.ssd_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p]
+    lib.ssd_chunk_states_size.argtypes = [P(Problem), P(FwdArgs), P(ctypes.c_size_t)]
     for f in ("ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
-              "ssd_fwd_debug_layout", "ssd_fwd_noalloc", "ssd_selftest_bounded_wait"):
+              "ssd_fwd_debug_layout", "ssd_fwd_noalloc", "ssd_selftest_bounded_wait", "ssd_chunk_states_size"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -119,12 +120,14 @@ def problem(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs=0
 
 
 def fwd_args(x, dt, A, B, C, y, D=None, z=None, dt_bias=None, initial_states=None, final_states=None,
-             cu_seqlens=None):
+             cu_seqlens=None, chunk_states=None):
+    """chunk_states: a device buffer (any dtype) of chunk_states_size bytes, or None."""
     a = FwdArgs()
     for name, t in dict(x=x, dt=dt, A=A, B=B, C=C, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
                         y=y, final_states=final_states).items():
         setattr(a, name, tensor(t))
     a.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
+    a.chunk_states = None if chunk_states is None else chunk_states.data_ptr()
     return a
 
 
@@ -153,6 +156,14 @@ def fwd_workspace_size(prob, args):
     n = ctypes.c_size_t(0)
     check(load().ssd_fwd_workspace_size(ctypes.byref(prob), ctypes.byref(args), ctypes.byref(n)),
           "ssd_fwd_workspace_size")
+    return int(n.value)
+
+
+def chunk_states_size(prob, args):
+    """Bytes of the chunk-state buffer the forward can keep for the backward (tensor-core path)."""
+    n = ctypes.c_size_t(0)
+    check(load().ssd_chunk_states_size(ctypes.byref(prob), ctypes.byref(args), ctypes.byref(n)),
+          "ssd_chunk_states_size")
     return int(n.value)
 
 

@@ -29,11 +29,14 @@ def _nseqs(x, cu_seqlens):
 
 def ssd_forward(x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_states=None, cu_seqlens=None,
                 chunk_size=128, return_final_states=True, algo="auto", seg_chunks=0, workspace=None,
-                y=None, final_states=None, stream=None):
+                y=None, final_states=None, stream=None, keep_chunk_states=False, chunk_states=None):
     """y, final_states = SSD scan (see include/ssd.h for the definition and layouts).
 
     x, z: [B, L, H, P]; dt: [B, L, H] fp32; A, D, dt_bias: [H] fp32; B, C: [B, L, G, N];
     initial_states: [S, H, P, N] fp32; cu_seqlens: int32 [S+1] (batch 1).
+    keep_chunk_states: also return the carried chunk states (a uint8 device buffer, tensor-core
+    path only; raises SSDError(SSD_ERR_UNSUPPORTED) otherwise) for ssd_backward(chunk_states=...),
+    which then skips their recompute.  chunk_states: a caller-owned buffer to fill instead.
     """
     Bsz, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
@@ -45,19 +48,29 @@ def ssd_forward(x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_states=Non
     prob = _lib.problem(Bsz, L, H, P, G, N, chunk_size, S if cu_seqlens is not None else 0, algo, seg_chunks)
     args = _lib.fwd_args(x, dt, A, B, C, y, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
                          final_states=final_states, cu_seqlens=cu_seqlens)
+    if keep_chunk_states or chunk_states is not None:
+        need = _lib.chunk_states_size(prob, args)
+        if chunk_states is None:
+            chunk_states = torch.empty(need, dtype=torch.uint8, device=x.device)
+        if chunk_states.numel() * chunk_states.element_size() < need:
+            raise ValueError("chunk_states holds %d bytes, %d needed" % (chunk_states.numel() * chunk_states.element_size(), need))
+        args.chunk_states = chunk_states.data_ptr()
     nbytes = _lib.fwd_workspace_size(prob, args)
     ws = workspace.get(nbytes) if workspace is not None else torch.empty(max(nbytes, 256), dtype=torch.uint8,
                                                                           device=x.device)
     _lib.check(_lib.ssd_fwd(prob, args, ws, stream), "ssd_fwd")
+    if keep_chunk_states:
+        return y, final_states, chunk_states
     return y, final_states
 
 
 def ssd_backward(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, initial_states=None, dfinal_states=None,
                  cu_seqlens=None, chunk_size=128, algo="auto", seg_chunks=0, bwd_heads=0, workspace=None,
-                 stream=None):
+                 stream=None, chunk_states=None):
     """Gradients of sum(dy*y) + sum(dfinal_states*final_states).  Returns a dict with
     dx, ddt, dA, dB, dC and, when the matching input is given, dD, dz, ddt_bias, dinitial_states.
-    bwd_heads: heads per CTA of the tensor-core gradient kernel (0 = library choice)."""
+    bwd_heads: heads per CTA of the tensor-core gradient kernel (0 = library choice).
+    chunk_states: the buffer ssd_forward(keep_chunk_states=True) returned for the same inputs."""
     Bsz, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     S = _nseqs(x, cu_seqlens)
@@ -78,7 +91,7 @@ def ssd_backward(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, initial_state
     prob = _lib.problem(Bsz, L, H, P, G, N, chunk_size, S if cu_seqlens is not None else 0, algo, seg_chunks,
                         bwd_heads)
     fa = _lib.fwd_args(x, dt, A, B, C, None, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
-                       cu_seqlens=cu_seqlens)
+                       cu_seqlens=cu_seqlens, chunk_states=chunk_states)
     ba = _lib.bwd_args(fa, dy, g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], dD=g.get("dD"), dz=g.get("dz"),
                        ddt_bias=g.get("ddt_bias"), dinitial_states=g.get("dinitial_states"),
                        dfinal_states=dfinal_states)
@@ -90,13 +103,22 @@ def ssd_backward(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, initial_state
 
 
 class SSDFunction(torch.autograd.Function):
-    """Autograd wrapper: forward and backward both run in libssd.so."""
+    """Autograd wrapper: forward and backward both run in libssd.so.  On the tensor-core
+    path the forward keeps its carried chunk states for the backward."""
 
     @staticmethod
     def forward(ctx, x, dt, A, B, C, D, z, dt_bias, initial_states, cu_seqlens, chunk_size):
-        y, fin = ssd_forward(x, dt, A, B, C, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
-                             cu_seqlens=cu_seqlens, chunk_size=chunk_size)
+        kw = dict(D=D, z=z, dt_bias=dt_bias, initial_states=initial_states, cu_seqlens=cu_seqlens,
+                  chunk_size=chunk_size)
+        try:
+            y, fin, cs = ssd_forward(x, dt, A, B, C, keep_chunk_states=True, **kw)
+        except _lib.SSDError as e:   # the SIMT path recomputes its states
+            if e.code != 2:
+                raise
+            y, fin = ssd_forward(x, dt, A, B, C, **kw)
+            cs = None
         ctx.save_for_backward(x, dt, A, B, C, D, z, dt_bias, initial_states, cu_seqlens)
+        ctx.chunk_states = cs
         ctx.chunk_size = chunk_size
         return y, fin
 
@@ -105,6 +127,6 @@ class SSDFunction(torch.autograd.Function):
         x, dt, A, B, C, D, z, dt_bias, init, cu = ctx.saved_tensors
         g = ssd_backward(x, dt, A, B, C, dy.contiguous(), D=D, z=z, dt_bias=dt_bias, initial_states=init,
                          dfinal_states=None if dfin is None else dfin.contiguous(), cu_seqlens=cu,
-                         chunk_size=ctx.chunk_size)
+                         chunk_size=ctx.chunk_size, chunk_states=ctx.chunk_states)
         return (g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], g.get("dD"), g.get("dz"), g.get("ddt_bias"),
                 g.get("dinitial_states"), None, None)

@@ -58,7 +58,7 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
                              int64_t sdb, int64_t sdl, const float *A, const float *D, const float *bias,
                              const void *z, const int64_t *sz, void *y, const int64_t *sy, const float *init,
                              float *final_, float *agg, float *incl, float *lam, uint32_t *flags, int grid,
-                             __nv_bfloat16 *states_out, const SeqInfo *seqs, cudaStream_t st);
+                             __nv_bfloat16 *states_out, bool states_only, const SeqInfo *seqs, cudaStream_t st);
 }  // namespace ssd
 
 using namespace ssd;
@@ -91,6 +91,7 @@ struct Plan {
     size_t off_hdr = 0, off_seqs = 0, off_chunks = 0, off_lastunit = 0, off_units = 0;
     size_t off_dt = 0, off_cs = 0, off_states = 0, off_dstates = 0, off_dBh = 0, off_dCh = 0, off_part = 0;
     size_t off_agg = 0, off_incl = 0, off_lam = 0, off_flags = 0;
+    size_t chunk_state_bytes = 0;   // tensor-core path: one bf16 [P][N] tile per (chunk, head)
     size_t total = 0;
 };
 
@@ -238,6 +239,10 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     pl.algo = (p->algo == SSD_ALGO_FUSED || (p->algo == SSD_ALGO_AUTO && tc_ok && aligned)) ? SSD_ALGO_FUSED
                                                                                            : SSD_ALGO_STAGED;
     const bool fused = pl.algo == SSD_ALGO_FUSED;
+    if (a->chunk_states != nullptr) {   // kept chunk states: the tensor-core path's tile format only
+        if (!fused) return SSD_ERR_UNSUPPORTED;
+        if (((uintptr_t)a->chunk_states) % 16 != 0) return SSD_ERR_MISALIGNED;
+    }
     const int Q = fused ? kTcQ : kSimtQ;
     if (fused && bwd && b == nullptr) return SSD_ERR_INVALID_ARGUMENT;
     int64_t kmax = varlen ? (L + Q - 1) / Q + S : B * ((L + Q - 1) / Q);
@@ -315,7 +320,8 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
             pl.off_tpart = lay.take(sizeof(float) * (size_t)tail_items * 2 * Q * (size_t)N);
             // dB/dC shares of head subsets, only when a CTA covers part of a group
             const size_t ksub = pl.hs < sh.hpg ? (size_t)kmax * (size_t)(H / pl.hs) : 0;
-            pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * N));   // carried states, bf16
+            if (a->chunk_states == nullptr)   // carried states, bf16, unless the forward kept them
+                pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * N));
             pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * N));
             pl.off_cs = lay.take(sizeof(float) * kh);                                // chunk total log-decay
             pl.off_dBh = lay.take(sizeof(float) * ksub * Q * (size_t)N);
@@ -333,6 +339,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         pl.off_dCh = lay.take(sizeof(float) * kh * Q * (size_t)N);
         pl.off_part = lay.take(sizeof(float) * kh * 4);
     }
+    if (fused) pl.chunk_state_bytes = sizeof(__nv_bfloat16) * kh * (size_t)(P * N);
     pl.total = lay.cur;
     *out = pl;
     return SSD_OK;
@@ -468,8 +475,8 @@ ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, siz
                                       (const float *)a->A.ptr, (const float *)a->D.ptr, (const float *)a->dt_bias.ptr,
                                       a->z.ptr, a->z.ptr ? a->z.stride : nullptr, a->y.ptr, a->y.stride,
                                       (const float *)a->initial_states.ptr, final_, at<float>(ws, pl.off_agg),
-                                      at<float>(ws, pl.off_incl), at<float>(ws, pl.off_lam), flags, grid, nullptr,
-                                      seqs, st));
+                                      at<float>(ws, pl.off_incl), at<float>(ws, pl.off_lam), flags, grid,
+                                      static_cast<__nv_bfloat16 *>(a->chunk_states), false, seqs, st));
         }
         if (final_ != nullptr && (pl.varlen || sh.L == 0))
             SSD_CUDA(launch_empty_seq_final(sh.S, sh.H, sh.P * sh.N, seqs, hdr,
@@ -488,6 +495,15 @@ ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, siz
             SSD_CUDA(launch_chunk_scan<float>(sh, hdr, chunks, view(a->x), view(a->B), view(a->C), view(a->z),
                                               (const float *)a->D.ptr, dtw, csw, states, mview(a->y), st));
     }
+    return SSD_OK;
+}
+
+ssd_status ssd_chunk_states_size(const ssd_problem *prob, const ssd_fwd_args *args, size_t *bytes) {
+    if (bytes == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    Plan pl;
+    SSD_TRY(plan_common(prob, args, false, &pl));
+    if (pl.algo != SSD_ALGO_FUSED) return SSD_ERR_UNSUPPORTED;
+    *bytes = pl.chunk_state_bytes;
     return SSD_OK;
 }
 
@@ -513,7 +529,8 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         ChunkInfo *chunks = at<ChunkInfo>(ws, pl.off_chunks);
         UnitInfo *units = at<UnitInfo>(ws, pl.off_units);
         uint32_t *flags = at<uint32_t>(ws, pl.off_flags);
-        __nv_bfloat16 *states = at<__nv_bfloat16>(ws, pl.off_states);
+        const bool kept = a->chunk_states != nullptr;   // the forward's chunk states, else recomputed
+        __nv_bfloat16 *states = kept ? static_cast<__nv_bfloat16 *>(a->chunk_states) : at<__nv_bfloat16>(ws, pl.off_states);
         float *dS = at<float>(ws, pl.off_dstates), *clam = at<float>(ws, pl.off_cs);
         float *dBh = at<float>(ws, pl.off_dBh), *dCh = at<float>(ws, pl.off_dCh), *part = at<float>(ws, pl.off_part);
         const int64_t n_zero = (int64_t)sh.umax * sh.H;   // the unit flags
@@ -521,7 +538,7 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
                                    fused_block_units(), sh.kmax, sh.umax, hdr, seqs, chunks, units,
                                    at<int32_t>(ws, pl.off_lastunit), flags, n_zero, st));
         const int64_t tickets = (int64_t)sh.umax * sh.H;
-        if (tickets > 0) {
+        if (tickets > 0 && !kept) {
             // carried state entering every chunk (forward recomputed in states-only mode)
             const int64_t slots = 2LL * num_sms();   // two CTAs per SM
             const int grid = (int)(tickets < slots ? tickets : slots);
@@ -530,7 +547,7 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
                                       (const float *)a->A.ptr, (const float *)a->D.ptr, (const float *)a->dt_bias.ptr,
                                       nullptr, nullptr, nullptr, a->x.stride, (const float *)a->initial_states.ptr,
                                       nullptr, at<float>(ws, pl.off_agg), at<float>(ws, pl.off_incl),
-                                      at<float>(ws, pl.off_lam), flags, grid, states, seqs, st));
+                                      at<float>(ws, pl.off_lam), flags, grid, states, true, seqs, st));
         }
         BwdTcArgs ta;
         ta.x = a->x.ptr; ta.Bp = a->B.ptr; ta.Cp = a->C.ptr;

@@ -21,7 +21,9 @@
 // The row sums of M o dM and the dt-weighted column sums of E CB dM cancel along the
 // suffix sums of dcs, so both come from the same fp32 products (never from bf16 tiles).
 // All contractions run as tcgen05.mma chains on 128-byte-swizzled shared-memory
-// tiles (TMA for x, B, C and the bf16 carried states); reductions are fixed-order.
+// tiles (TMA for x, B, C, dy, z; one bulk copy for the carried state of a (chunk, head),
+// stored by the forward as the image of its swizzled [n][p] tile); reductions are
+// fixed-order.
 #include <cudaTypedefs.h>
 
 #include "tc_common.cuh"
@@ -52,6 +54,7 @@ struct BwdParams {
     float *ddt;
     int64_t sddb, sddl;
     const float *dS;         // [chunk][H][P][N] fp32: gradient of the state leaving the chunk
+    const __nv_bfloat16 *states;   // 16 KB tile per (chunk, head): row n = S_in[0..63][n], 128-byte swizzle
     float *dS_loc;           // [chunk][H][P][N] fp32 (dstates kernel output)
     float *chunk_lam;        // [chunk][H] total log-decay of the chunk (dstates kernel output)
     float *dBh, *dCh;        // [chunk][H/hs][Q][N] fp32 shares of head subsets (when hs < H/G)
@@ -284,7 +287,7 @@ k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
 constexpr uint32_t O_X = 0;                        // x      [s][p]   16 KB (TMA)
 constexpr uint32_t O_B = O_X + X_BYTES;            // B      [s][n]   32 KB (TMA)
 constexpr uint32_t O_C = O_B + BC_BYTES;           // C      [l][n]   32 KB (TMA)
-constexpr uint32_t O_SI = O_C + BC_BYTES;          // S_in   [p][n]   16 KB (TMA, bf16)
+constexpr uint32_t O_SI = O_C + BC_BYTES;          // S_in   [n][p]   16 KB (bulk copy, bf16)
 constexpr uint32_t O_DY = O_SI + S_BYTES;          // dyp, then e o dyp [l][p] 16 KB
 constexpr uint32_t O_M = O_DY + X_BYTES;           // M      [l][s]   32 KB
 constexpr uint32_t O_E = O_M + BC_BYTES;           // E'     [l][s]   32 KB; before: dy, z of the head (TMA)
@@ -314,8 +317,8 @@ constexpr uint32_t T_YD = 384, T_YO = 448;                // group 3 (+ dB, dC)
 // the item covers the whole group, else as fp32 shares summed afterwards in subset order.
 __global__ void __launch_bounds__(256, 1)
 k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
-               const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmZ, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmDY,
+               const __grid_constant__ CUtensorMap tmZ, const BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, row = tid & 127, hf = tid >> 7, quad = warp & 3;
@@ -395,8 +398,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int slab = w.k * H + h;
         mbar_expect_tx(&bar[1], X_BYTES + S_BYTES);
         tma_load_4d(sm + O_X, &tmX, &bar[1], 0, h, w.ci.t0, w.ci.b);
-        tma_load_4d(sm + O_SI, &tmS, &bar[1], 0, 0, slab * PT, 0);
-        tma_load_4d(sm + O_SI + S_BYTES / 2, &tmS, &bar[1], 64, 0, slab * PT, 0);
+        bulk_load(sm + O_SI, p.states + (int64_t)slab * (PT * NT), S_BYTES, &bar[1]);
     };
     auto stage_head = [&](const Item &w, int h) {   // one thread: dy, z and fp32 dS
         const float *src = p.dS + ((int64_t)w.k * H + h) * (PT * NT);
@@ -540,14 +542,20 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 const float4 a = s4[0], b = s4[1];
                 dsv[j][0] = a.x; dsv[j][1] = a.y; dsv[j][2] = a.z; dsv[j][3] = a.w;
                 dsv[j][4] = b.x; dsv[j][5] = b.y; dsv[j][6] = b.z; dsv[j][7] = b.w;
-                const uint4 si = *reinterpret_cast<const uint4 *>(sm + O_SI + (nc >> 3) * (S_BYTES / 2) + pp * 128 +
-                                                                  (((nc & 7) ^ (pp & 7)) << 4));
+            }
+            // <S_in, dS> partial: thread takes 8 consecutive p at one n (run r = tid + 256 j:
+            // n = r % 128, p = 8 (r / 128) ..), one 16-byte piece of the S_in tile's row n
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = tid + 256 * j, n = r & 127, q = r >> 7;
+                const uint4 si = *reinterpret_cast<const uint4 *>(sm + O_SI + n * 128 + ((q ^ (n & 7)) << 4));
                 const __nv_bfloat162 *e2 = reinterpret_cast<const __nv_bfloat162 *>(&si);
+                const float *dsn = reinterpret_cast<const float *>(sm + O_WX) + 8 * q * NT + n;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 sv = __bfloat1622float2(e2[i]);
-                    t3p = fmaf(sv.x, dsv[j][2 * i], t3p);
-                    t3p = fmaf(sv.y, dsv[j][2 * i + 1], t3p);
+                    t3p = fmaf(sv.x, dsn[(2 * i) * NT], t3p);
+                    t3p = fmaf(sv.y, dsn[(2 * i + 1) * NT], t3p);
                 }
             }
             __syncthreads();   // the staged dS is read: its space becomes the w o x and dS tiles
@@ -702,7 +710,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 umma_bf16(tmem + T_YD, kmaj(sM, kk, BC_BYTES / 2), mnmaj(sX, kk, 16384u), idesc_bf16(128, 64, 0, 1), kk > 0);
 #pragma unroll
             for (int kk = 0; kk < NT / 16; ++kk)   // Ybar[l][p] = sum_n C[l][n] S_in[p][n]
-                umma_bf16(tmem + T_YO, kmaj(sC, kk, BC_BYTES / 2), kmaj(sSI, kk, S_BYTES / 2), idesc_bf16(128, 64, 0, 0),
+                umma_bf16(tmem + T_YO, kmaj(sC, kk, BC_BYTES / 2), mnmaj(sSI, kk, 16384u), idesc_bf16(128, 64, 0, 1),
                           kk > 0);
             umma_commit(&bar[2]);   // the y tiles; the dB/dC chains below run on during the dz epilogue
             const uint32_t first = hi == 0 ? 0u : 1u;   // dB, dC start at the CTA's first head
@@ -719,7 +727,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                           idesc_bf16(128, 128, 0, 1), (kk > 0) ? 1u : first);
 #pragma unroll
             for (int kk = 0; kk < PT / 16; ++kk)   // dC[l][n] += sum_p (e o dyp)[l][p] S_in[p][n]
-                umma_bf16(tmem + T_DC, kmaj(sDY, kk, X_BYTES), mnmaj(sSI, kk, S_BYTES / 2), idesc_bf16(128, 128, 0, 1), 1);
+                umma_bf16(tmem + T_DC, kmaj(sDY, kk, X_BYTES), kmaj(sSI, kk, S_BYTES), idesc_bf16(128, 128, 0, 0), 1);
             umma_commit(&bar[4]);
         }
         wait_mma();
@@ -956,6 +964,7 @@ static BwdParams make_params(const Shape &sh, const int32_t *hdr, const ChunkInf
     p.dz = (__nv_bfloat16 *)a.dz;
     p.sdzb = a.sdz ? a.sdz[0] : 0; p.sdzl = a.sdz ? a.sdz[1] : 0; p.sdzh = a.sdz ? a.sdz[2] : 0;
     p.ddt = a.ddt; p.sddb = a.sddb; p.sddl = a.sddl;
+    p.states = a.states;
     p.dS = a.dS; p.dS_loc = a.dS; p.chunk_lam = a.chunk_lam; p.dBh = a.dBh; p.dCh = a.dCh; p.partials = a.partials;
     p.hs = a.hs;
     p.hs_ds = a.hs_ds;
@@ -986,7 +995,7 @@ cudaError_t launch_bwd_dstates_tc(const Shape &sh, const int32_t *hdr, const Chu
 
 cudaError_t launch_bwd_chunk_tc(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const BwdTcArgs &a,
                                 cudaStream_t st) {
-    CUtensorMap mx, mb, mc, ms, mdy, mz;
+    CUtensorMap mx, mb, mc, mdy, mz;
     if (!map4(&mx, a.x, PT, sh.H, sh.L, sh.B, a.sx[2], a.sx[1], a.sx[0], QT)) return cudaErrorInvalidValue;
     if (!map4(&mdy, a.dy, PT, sh.H, sh.L, sh.B, a.sdy[2], a.sdy[1], a.sdy[0], QT)) return cudaErrorInvalidValue;
     if (a.z != nullptr) {
@@ -996,14 +1005,11 @@ cudaError_t launch_bwd_chunk_tc(const Shape &sh, const int32_t *hdr, const Chunk
     }
     if (!map4(&mb, a.Bp, NT, sh.G, sh.L, sh.B, a.sb[2], a.sb[1], a.sb[0], QT)) return cudaErrorInvalidValue;
     if (!map4(&mc, a.Cp, NT, sh.G, sh.L, sh.B, a.sc[2], a.sc[1], a.sc[0], QT)) return cudaErrorInvalidValue;
-    // carried states as a [rows = chunk*H*P][N] matrix, box {64, 64 rows}
-    const int64_t rows = (int64_t)sh.kmax * sh.H * PT;
-    if (!map4(&ms, a.states, NT, 1, rows, 1, NT, NT, rows * NT, PT)) return cudaErrorInvalidValue;
     BwdParams p = make_params(sh, hdr, chunks, a);
     static int attr_done[64] = {0};
     cudaError_t e = ensure_smem_attr(k_bwd_chunk_tc, (int)BWD_SMEM, attr_done);
     if (e != cudaSuccess) return e;
-    if (a.grid > 0) k_bwd_chunk_tc<<<a.grid, 256, BWD_SMEM, st>>>(mx, mb, mc, ms, mdy, mz, p);   // persistent
+    if (a.grid > 0) k_bwd_chunk_tc<<<a.grid, 256, BWD_SMEM, st>>>(mx, mb, mc, mdy, mz, p);   // persistent
     const int tail_pairs = sh.kmax * sh.G - a.k_pairs;
     if (a.grid > 0 && tail_pairs > 0 && a.nsub_tail > 1 && a.hs == sh.hpg) {
         cudaError_t e2 = cudaGetLastError();

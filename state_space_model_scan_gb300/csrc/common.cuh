@@ -61,7 +61,7 @@ struct BwdTcArgs {
     const int64_t *sdx, *sdz;
     float *ddt;
     int64_t sddb, sddl;
-    const __nv_bfloat16 *states;   // [chunk][H][P][N] bf16 carried states
+    const __nv_bfloat16 *states;   // carried state entering each chunk: 16 KB swizzled tile per (chunk, head)
     float *dS, *chunk_lam, *dBh, *dCh, *partials;
     int hs;                         // heads per CTA of the gradient kernel (divides H/G)
     int hs_ds;                      // heads per CTA of the dstates kernel (divides H/G)

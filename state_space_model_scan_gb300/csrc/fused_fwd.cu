@@ -55,7 +55,7 @@ constexpr uint32_t BC_BYTES = QT * NT * 2;   // 32 KB
 // Shared memory (offsets from a 1024-aligned base), about 102 KB so that two CTAs
 // share an SM and fill each other's load / tensor-core waits.
 //   X  : x tile                     phase 1: stage-0 x (scaled in place to w o x)
-//   B  : B tile, then M             phase 1: stage-0 B
+//   B  : B tile                     phase 1: stage-0 B
 //   C  : C tile                     phase 1: stage-1 B
 //   W  : w o x, then S_in (bf16), then z (TMA)     phase 1: stage-1 x (scaled in place)
 constexpr uint32_t OFF_X = 0;
@@ -94,10 +94,14 @@ struct FusedParams {
     float *final_;
     float *agg, *incl, *lam;
     uint32_t *flags;
-    // States-only mode (used by the backward): when set, the carried state at the
-    // start of every chunk is written here (bf16 [chunk][head][P][N]) and no output
-    // is computed (no CB, M, Y_off, Y_diag, y).  Phase 1 then keeps each chunk's own
-    // state in TMEM, so phase 2 needs neither loads nor tensor-core work.  Chunk index = seqs[seq].chunk0 + (t0 - seqs[seq].t0)/Q + c.
+    // Optional: the carried state entering every chunk, one 16 KB tile per (chunk, head)
+    // at tile index chunk * H + head (chunk = seqs[seq].chunk0 + (t0 - seqs[seq].t0)/Q + c):
+    // bf16, 128-byte row n = S[0..63][n], its 16-byte pieces q (p = 8q..8q+7) stored at
+    // position q ^ (n & 7) -- the image of a 128-byte-swizzled shared-memory tile, so a
+    // plain bulk copy into 1024-aligned shared memory gives the backward's MMA operand.
+    // The states-only mode (template argument; used by the backward when the forward did
+    // not keep them) computes nothing else: no CB, M, Y_off, Y_diag or y; phase 1 then
+    // keeps each chunk's own state in TMEM, so phase 2 needs neither loads nor MMAs.
     __nv_bfloat16 *states_out;
     const SeqInfo *seqs;
 };
@@ -128,6 +132,11 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Row n of the carried-state tile of (chunk k, head h) in FusedParams::states_out.
+__device__ __forceinline__ uint8_t *state_tile_row(__nv_bfloat16 *base, int64_t k, int H, int h, int n) {
+    return reinterpret_cast<uint8_t *>(base) + ((k * H + h) * (int64_t)(PT * NT) + (int64_t)n * PT) * 2;
+}
 
 // K-major SW128 operand: rows of 64 bf16 (128 B), atom columns of `col_bytes`.
 __device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t col_bytes) {
@@ -170,8 +179,8 @@ __device__ __forceinline__ void fma_col64(float *acc, const float *src, float sc
     }
 }
 
-// kStatesOnly: the states-only mode (FusedParams::states_out set), compiled separately so
-// that neither mode's code shapes the other's register allocation.
+// kStatesOnly: the states-only mode (only FusedParams::states_out is written), compiled
+// separately so that neither mode's code shapes the other's register allocation.
 template <bool kStatesOnly>
 __global__ void __launch_bounds__(NTHR, 2)
 k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
@@ -501,9 +510,12 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         if (!full) {
             const int64_t kfirst = (int64_t)p.seqs[ui.seq].chunk0 + (ui.t0 - p.seqs[ui.seq].t0) / QT;
             for (int c = 0; c < ui.nchunk; ++c) {
-                __nv_bfloat16 *dst = p.states_out + ((kfirst + c) * sh.H + h) * (int64_t)(PT * NT) + row;
+                uint8_t *dst = state_tile_row(p.states_out, kfirst + c, sh.H, h, row);
 #pragma unroll
-                for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(s_run[i]);
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<uint4 *>(dst + ((q ^ (row & 7)) << 4)) =
+                        make_uint4(pack_bf16(s_run[8 * q], s_run[8 * q + 1]), pack_bf16(s_run[8 * q + 2], s_run[8 * q + 3]),
+                                   pack_bf16(s_run[8 * q + 4], s_run[8 * q + 5]), pack_bf16(s_run[8 * q + 6], s_run[8 * q + 7]));
                 const float a_c = ex2(cs2u[c * QT + QT - 1]);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -520,6 +532,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         }
         // ---- phase 2: outputs
         const float Dh = p.D ? p.D[h] : 0.f;
+        const int64_t kfirst = (int64_t)p.seqs[ui.seq].chunk0 + (ui.t0 - p.seqs[ui.seq].t0) / QT;
         for (int c = 0; c < ui.nchunk; ++c) {
             const int tc0 = ui.t0 + c * QT;
             const int clen = min(QT, ui.len - c * QT);
@@ -562,13 +575,17 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             if (full) {
                 // S_in (bf16, MN-major [n][p]: row n = this thread's 64 columns) over the w o x
                 // buffer, then Y_off = C S_in^T
-                {
+                {   // (and the same bytes to the chunk-state tile when the caller keeps them)
                     uint8_t *rowp = Ws + row * 128;
+                    uint8_t *grow = p.states_out ? state_tile_row(p.states_out, kfirst + c, sh.H, h, row) : nullptr;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        *reinterpret_cast<uint4 *>(rowp + ((q ^ (row & 7)) << 4)) =
+                    for (int q = 0; q < 8; ++q) {
+                        const uint4 v =
                             make_uint4(pack_bf16(s_run[8 * q], s_run[8 * q + 1]), pack_bf16(s_run[8 * q + 2], s_run[8 * q + 3]),
                                        pack_bf16(s_run[8 * q + 4], s_run[8 * q + 5]), pack_bf16(s_run[8 * q + 6], s_run[8 * q + 7]));
+                        *reinterpret_cast<uint4 *>(rowp + ((q ^ (row & 7)) << 4)) = v;
+                        if (grow) *reinterpret_cast<uint4 *>(grow + ((q ^ (row & 7)) << 4)) = v;
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncthreads();
@@ -740,7 +757,7 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
                              int64_t sdb, int64_t sdl, const float *A, const float *D, const float *bias,
                              const void *z, const int64_t *sz, void *y, const int64_t *sy, const float *init,
                              float *final_, float *agg, float *incl, float *lam, uint32_t *flags, int grid,
-                             __nv_bfloat16 *states_out, const SeqInfo *seqs, cudaStream_t st) {
+                             __nv_bfloat16 *states_out, bool states_only, const SeqInfo *seqs, cudaStream_t st) {
     CUtensorMap mx, mb, mc, mz;
     if (!make_map(&mx, x, PT, sh.H, sh.L, sh.B, sx[2], sx[1], sx[0])) return cudaErrorInvalidValue;
     if (z != nullptr) {
@@ -758,7 +775,8 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
     fp.y = (__nv_bfloat16 *)y; fp.syb = sy[0]; fp.syl = sy[1]; fp.syh = sy[2];
     fp.init = init; fp.final_ = final_; fp.agg = agg; fp.incl = incl; fp.lam = lam; fp.flags = flags;
     fp.states_out = states_out; fp.seqs = seqs;
-    if (states_out != nullptr) {
+    if (states_only) {
+        if (states_out == nullptr) return cudaErrorInvalidValue;
         static int attr_done_s[64] = {0};
         cudaError_t e = ensure_smem_attr(k_fused_fwd<true>, (int)SMEM_BYTES, attr_done_s);
         if (e != cudaSuccess) return e;

@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.abi_version() == 2
+    assert lib.abi_version() == 3
     for code, name in lib.STATUS_NAMES.items():
         assert lib.status_string(code) == name
     assert lib.status_string(99) == "SSD_ERR_UNKNOWN"
@@ -185,3 +185,68 @@ def test_selftest_bounded_wait_validates_on_host(lib):
     import ctypes
     m = lib.load()
     assert m.ssd_selftest_bounded_wait(None, ctypes.c_size_t(4096), 10, None) == 1
+
+
+def _tc_case(Bsz=2, L=1000, H=8, G=2, cu=None):
+    """A problem on the tensor-core path (bf16, headdim 64, dstate 128), fake 16-byte-aligned pointers."""
+    m = lib_mod()
+    p, a = good_case(Bsz=Bsz, L=L, H=H, P=64, G=G, N=128)
+    if cu is not None:
+        p.batch = 1
+        p.nseqs = cu
+        a.cu_seqlens = 0x300000
+        for t in ("x", "y", "z", "B", "C", "dt"):
+            getattr(a, t).stride[0] = 0
+        a.final_states = m.Tensor()
+    return p, a
+
+
+def _chunk_states_size(p, a):
+    m = lib_mod()
+    n = ctypes.c_size_t(0)
+    rc = m.load().ssd_chunk_states_size(ctypes.byref(p), ctypes.byref(a), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_chunk_states_size(lib):
+    """One bf16 64 x 128 tile per (chunk of 128 tokens, head), for the largest chunk count."""
+    p, a = _tc_case(Bsz=2, L=1000, H=8)
+    assert _chunk_states_size(p, a) == (0, 2 * 8 * 8 * 64 * 128 * 2)
+    p, a = _tc_case(L=1000, H=8, cu=5)   # packed: ceil(L / 128) + nseqs chunks at most
+    assert _chunk_states_size(p, a) == (0, (8 + 5) * 8 * 64 * 128 * 2)
+    p, a = good_case()                   # SIMT path: no chunk-state buffer
+    assert _chunk_states_size(p, a)[0] == 2
+
+
+def test_chunk_states_argument_checks(lib):
+    m = lib_mod()
+    p, a = good_case()
+    a.chunk_states = 0x400000            # SIMT path does not take kept states
+    assert ws_size(p, a)[0] == 2
+    p, a = _tc_case()
+    a.chunk_states = 0x400008            # not 16-byte aligned
+    assert ws_size(p, a)[0] == 3
+    a.chunk_states = 0x400000
+    assert ws_size(p, a)[0] == 0
+
+
+def test_bwd_workspace_drops_states_when_kept(lib):
+    """Given the forward's chunk states, the backward reserves no workspace copy of them."""
+    m = lib_mod()
+    p, a = _tc_case(Bsz=1, L=4096, H=8)
+    b = m.BwdArgs()
+    xs = [a.x.stride[i] for i in range(4)]
+    for f in ("dy", "dx", "dz"):
+        setattr(b, f, _fake(a.x.dtype, xs))
+    for f in ("dB", "dC"):
+        setattr(b, f, _fake(a.x.dtype, [a.B.stride[i] for i in range(4)]))
+    b.ddt = _fake(m.SSD_F32, [a.dt.stride[i] for i in range(3)])
+    for f in ("dA", "dD", "ddt_bias"):
+        setattr(b, f, _fake(m.SSD_F32, [1]))
+    n0, n1 = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    b.fwd = a
+    assert m.load().ssd_bwd_workspace_size(ctypes.byref(p), ctypes.byref(b), ctypes.byref(n0)) == 0
+    a.chunk_states = 0x400000
+    b.fwd = a
+    assert m.load().ssd_bwd_workspace_size(ctypes.byref(p), ctypes.byref(b), ctypes.byref(n1)) == 0
+    assert n0.value - n1.value >= 32 * 8 * 64 * 128 * 2
