@@ -100,51 +100,63 @@ k_chunk_state(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__rest
 
 // ---------------------------------------------------------------------------- a4
 // Inter-chunk scan: sequential over the chunks of a sequence, parallel over the
-// state elements.  grid (S*H, ceil(P*N/256)), block 256; thread = one element
-// (p, n) of (sequence, head), its running carry in a register.  In place: the
-// chunk's local state S_c is replaced by the carry entering the chunk, and
+// state elements.  grid (S*H, ceil(P*N/1024)), block 256; thread = four consecutive
+// elements (p, n) of (sequence, head) (one float4), their running carries in
+// registers.  In place: the chunk's local state S_c is replaced by the carry entering
+// the chunk, and
 //   carry <- exp(lam_c) carry + S_c
-// passes the chunk; the carry after the last chunk is the final state.  Per batch
-// of 32 chunks each lane holds one chunk's decay exp(lam_c) in a register and the
-// warp broadcasts it with a shuffle at every step; the batch's 32 loads of S_c are
-// issued ahead of the recurrence (they do not depend on the carry), so a warp keeps
-// 32 coalesced 128-byte rows in flight.  The chunk's total log-decay is
-// lamw[(chunk * H + h) * lam_stride].  With reverse = 1 the chunks are visited last
-// to first: that is the backward recursion dS_out[c] = exp(cs_{c+1}[Q-1]) dS_out[c+1]
-// + dS_loc[c+1] (same affine form, the chunk's own decay), with `init` = dfinal and
-// `final_` = dinit.
+// passes the chunk; the carry after the last chunk is the final state.  Per batch of
+// 8 chunks, lane j < 8 holds chunk j's decay exp(lam_c) and the warp broadcasts it
+// with a shuffle at each step; the batch's 8 loads of S_c are issued ahead of the
+// recurrence (they do not depend on the carry), so a warp keeps 8 contiguous
+// 512-byte pieces in flight, and all blocks are resident at once.  The chunk's total
+// log-decay is lamw[(chunk * H + h) * lam_stride].  With reverse = 1 the chunks are
+// visited last to first: that is the backward recursion dS_out[c] = exp(cs_{c+1}[Q-1])
+// dS_out[c+1] + dS_loc[c+1] (same affine form, the chunk's own decay), with `init` =
+// dfinal and `final_` = dinit (caller tensors: read and written per element, since
+// their 16-byte alignment is not guaranteed).  P*N is a multiple of 256.
 __global__ void __launch_bounds__(256)
 k_state_passing(Shape sh, const int32_t *__restrict__ hdr, const SeqInfo *__restrict__ seqs,
                 const float *__restrict__ lamw, int lam_stride, float *__restrict__ states,
                 const float *__restrict__ init, float *__restrict__ final_, int reverse) {
+    constexpr int CB = 8;   // chunks per batch
     if (hdr[HDR_STATUS] != 0) return;
     const int s = blockIdx.x / sh.H, h = blockIdx.x % sh.H;
     const int PN = sh.P * sh.N;
-    const int e = blockIdx.y * 256 + threadIdx.x, lane = threadIdx.x & 31;
-    if (blockIdx.y * 256 + (threadIdx.x & ~31) >= PN) return;   // whole warp past the end
+    const int e = (blockIdx.y * 256 + threadIdx.x) * 4, lane = threadIdx.x & 31;
+    if ((blockIdx.y * 256 + (threadIdx.x & ~31)) * 4 >= PN) return;   // whole warp past the end
     const SeqInfo si = seqs[s];
     const int nch = (si.len + sh.Q - 1) / sh.Q;
     const int64_t sbase = ((int64_t)s * sh.H + h) * PN;
     const bool act = e < PN;
-    float carry = (init != nullptr && act) ? init[sbase + e] : 0.f;
+    float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (init != nullptr && act) carry = make_float4(init[sbase + e], init[sbase + e + 1], init[sbase + e + 2], init[sbase + e + 3]);
     auto chunk_of = [&](int pos) { return reverse ? si.chunk0 + nch - 1 - pos : si.chunk0 + pos; };
-    auto slot = [&](int pos) { return ((int64_t)chunk_of(pos) * sh.H + h) * PN + e; };
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-        const int nc = min(32, nch - c0);
+    auto slot = [&](int pos) { return reinterpret_cast<float4 *>(states + ((int64_t)chunk_of(pos) * sh.H + h) * PN + e); };
+    for (int c0 = 0; c0 < nch; c0 += CB) {
+        const int nc = min(CB, nch - c0);
         const float mydec = lane < nc ? expf(lamw[((int64_t)chunk_of(c0 + lane) * sh.H + h) * lam_stride]) : 0.f;
-        float v[32];
+        float4 v[CB];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = (act && j < nc) ? states[slot(c0 + j)] : 0.f;
+        for (int j = 0; j < CB; ++j) v[j] = (act && j < nc) ? *slot(c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < CB; ++j) {
             const float d = __shfl_sync(0xffffffffu, mydec, j);
             if (j < nc) {
-                if (act) states[slot(c0 + j)] = carry;   // carry entering the chunk
-                carry = fmaf(d, carry, v[j]);
+                if (act) *slot(c0 + j) = carry;   // carry entering the chunk
+                carry.x = fmaf(d, carry.x, v[j].x);
+                carry.y = fmaf(d, carry.y, v[j].y);
+                carry.z = fmaf(d, carry.z, v[j].z);
+                carry.w = fmaf(d, carry.w, v[j].w);
             }
         }
     }
-    if (final_ != nullptr && act) final_[sbase + e] = carry;
+    if (final_ != nullptr && act) {
+        final_[sbase + e] = carry.x;
+        final_[sbase + e + 1] = carry.y;
+        final_[sbase + e + 2] = carry.z;
+        final_[sbase + e + 3] = carry.w;
+    }
 }
 
 // ---------------------------------------------------------------------------- a5
@@ -262,8 +274,9 @@ cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqI
                                  cudaStream_t st) {
     const int PN = sh.P * sh.N;
     if (sh.S * sh.H == 0) return cudaSuccess;
-    k_state_passing<<<dim3(sh.S * sh.H, (PN + 255) / 256), 256, 0, st>>>(sh, hdr, seqs, lamw, lam_stride, states,
-                                                                          init, final_, reverse);
+    if (PN % 256 != 0) return cudaErrorInvalidValue;   // float4 per thread, whole warps
+    k_state_passing<<<dim3(sh.S * sh.H, (PN + 1023) / 1024), 256, 0, st>>>(sh, hdr, seqs, lamw, lam_stride, states,
+                                                                           init, final_, reverse);
     return cudaGetLastError();
 }
 
