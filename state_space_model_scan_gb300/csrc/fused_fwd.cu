@@ -57,7 +57,7 @@ constexpr uint32_t BC_BYTES = QT * NT * 2;   // 32 KB
 //   X  : x tile                     phase 1: stage-0 x (scaled in place to w o x)
 //   B  : B tile                     phase 1: stage-0 B
 //   C  : C tile                     phase 1: stage-1 B
-//   W  : w o x, then S_in (bf16), then z (TMA)     phase 1: stage-1 x (scaled in place)
+//   W  : w o x, then S_in (bf16), then z (TMA), then y (TMA store)   phase 1: stage-1 x (scaled in place)
 constexpr uint32_t OFF_X = 0;
 constexpr uint32_t OFF_B = OFF_X + X_BYTES;        // 16384
 constexpr uint32_t OFF_C = OFF_B + BC_BYTES;       // 49152
@@ -184,7 +184,8 @@ __device__ __forceinline__ void fma_col64(float *acc, const float *src, float sc
 template <bool kStatesOnly>
 __global__ void __launch_bounds__(NTHR, 2)
 k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
-            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmZ, const FusedParams p) {
+            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmZ,
+            const __grid_constant__ CUtensorMap tmY, const FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -206,6 +207,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmC);
         if (p.z) prefetch_tmap(&tmZ);
+        if (p.y) prefetch_tmap(&tmY);
     }
     if (warp == 0) tmem_alloc(&ms->tmem_base, TM_COLS);
     tc_fence_before();
@@ -301,8 +303,11 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     int ticket = ms->tnext;
     if (ticket < total) fetch_unit_inputs(ms->ui_next, ticket % sh.H);
 
+    bool y_inflight = false;   // a y tile is being stored out of W (uniform)
     for (;;) {
         __syncthreads();
+        if (tid == 0) bulk_wait_read0();   // W is refilled below (phase-1 loads)
+        y_inflight = false;
         if (ticket >= total || ms->abort_) break;
         const int u = ticket / sh.H, h = ticket % sh.H, g = h / sh.hpg;
         const UnitInfo ui = ms->ui_next;
@@ -555,6 +560,11 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 }
             }
             wait_bar(BAR_X);
+            if (y_inflight) {   // the previous chunk's y tile is still being read out of W
+                if (tid == 0) bulk_wait_read0();
+                __syncthreads();
+                y_inflight = false;
+            }
             // W = w o x, w[l] = dt[l] exp(cs[Q-1] - cs[l])
             scale_row(Xs + row * 128, Ws + row * 128, row, dtc[row] * ex2(cs2[QT - 1] - cs2[row]));
             fence_proxy_async_smem();
@@ -661,6 +671,10 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             wait_bar(BAR_MMA);   // x free: next chunk's x
             if (more) load_x(h, tc0 + QT, ui.b);
             if (has_z) wait_bar(BAR_Z);
+            // full chunks: y rows go into W (in place of the gate rows just read) and leave as
+            // one TMA store; a ragged chunk stores its rows directly (rows past it may belong
+            // to the next packed sequence)
+            const bool tile_out = clen == QT;
             {   // epilogue: row l
                 const int l = row;
                 const float el = ex2(cs2[l]);
@@ -691,13 +705,25 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                                 }
                                 o[i] = pack_bf16(v0, v1);
                             }
-                            *reinterpret_cast<uint4 *>(yrow + half * 32 + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+                            const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+                            if (tile_out)
+                                *reinterpret_cast<uint4 *>(Ws + l * 128 + (((half * 4 + q) ^ (l & 7)) << 4)) = ov;
+                            else
+                                *reinterpret_cast<uint4 *>(yrow + half * 32 + q * 8) = ov;
                         }
                     }
                 }
             }
+            if (tile_out) fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
+            if (tile_out) {
+                if (tid == 0) {
+                    tma_store_4d(&tmY, Ws, 0, h, tc0, ui.b);
+                    bulk_commit();
+                }
+                y_inflight = true;
+            }
         }
         if (ms->abort_) break;
         if (ui.last && p.final_) {
@@ -709,6 +735,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     // Drain (only non-empty after an early stop): bounded waits for loads and
     // MMAs still in flight, so nothing lands in shared memory or TMEM after exit.
     cp_async_wait_all();
+    if (tid == 0) bulk_wait0();   // y stores
     for (int b_ = 0; b_ < NBAR; ++b_)
         for (uint32_t q = done[b_]; q < issued[b_]; ++q) mbar_wait(&ms->bar[b_], q & 1);
     tc_fence_before();
@@ -758,7 +785,7 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
                              const void *z, const int64_t *sz, void *y, const int64_t *sy, const float *init,
                              float *final_, float *agg, float *incl, float *lam, uint32_t *flags, int grid,
                              __nv_bfloat16 *states_out, bool states_only, const SeqInfo *seqs, cudaStream_t st) {
-    CUtensorMap mx, mb, mc, mz;
+    CUtensorMap mx, mb, mc, mz, my;
     if (!make_map(&mx, x, PT, sh.H, sh.L, sh.B, sx[2], sx[1], sx[0])) return cudaErrorInvalidValue;
     if (z != nullptr) {
         if (!make_map(&mz, z, PT, sh.H, sh.L, sh.B, sz[2], sz[1], sz[0])) return cudaErrorInvalidValue;
@@ -766,6 +793,11 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
         mz = mx;
     }
     if (!make_map(&mb, Bp, NT, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
+    if (y != nullptr) {
+        if (!make_map(&my, y, PT, sh.H, sh.L, sh.B, sy[2], sy[1], sy[0])) return cudaErrorInvalidValue;
+    } else {
+        my = mx;   // not written (states-only mode)
+    }
     if (!make_map(&mc, Cp, NT, sh.G, sh.L, sh.B, sc[2], sc[1], sc[0])) return cudaErrorInvalidValue;
     FusedParams fp;
     fp.sh = sh; fp.hdr = hdr; fp.units = units; fp.dt_raw = dt_raw; fp.sdb = sdb; fp.sdl = sdl;
@@ -780,12 +812,12 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
         static int attr_done_s[64] = {0};
         cudaError_t e = ensure_smem_attr(k_fused_fwd<true>, (int)SMEM_BYTES, attr_done_s);
         if (e != cudaSuccess) return e;
-        k_fused_fwd<true><<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, mz, fp);
+        k_fused_fwd<true><<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, mz, my, fp);
     } else {
         static int attr_done[64] = {0};
         cudaError_t e = ensure_smem_attr(k_fused_fwd<false>, (int)SMEM_BYTES, attr_done);
         if (e != cudaSuccess) return e;
-        k_fused_fwd<false><<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, mz, fp);
+        k_fused_fwd<false><<<grid, NTHR, SMEM_BYTES, st>>>(mx, mb, mc, mz, my, fp);
     }
     return cudaGetLastError();
 }
