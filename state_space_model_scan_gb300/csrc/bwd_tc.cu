@@ -64,6 +64,7 @@ struct BwdParams {
     __nv_bfloat16 *dB, *dC;  // final outputs when hs == H/G
     int64_t sdBb, sdBl, sdBg, sdCb, sdCl, sdCg;
     int k_pairs, nsub_tail, n_items;   // gradient kernel work items
+    int st32;                // dx and dz rows are 32-byte aligned: stored with 256-bit stores
     float *tpart;
 };
 
@@ -76,6 +77,27 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k, uint32_t mn_atom
 }
 __device__ __forceinline__ float silu_f(float z) { return z * rcp(1.f + ex2(-z * LOG2E)); }
 __device__ __forceinline__ float sig_f(float z) { return rcp(1.f + ex2(-z * LOG2E)); }
+
+// 32 floats as bf16 to 64 contiguous bytes of global memory: two 256-bit stores when the
+// address is 32-byte aligned (`st32`, checked on the host for base and strides), else four
+// 128-bit stores.
+__device__ __forceinline__ void store_row32_global(__nv_bfloat16 *dst, const float *o, bool st32) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(o[2 * i], o[2 * i + 1]);
+    if (st32) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * j),
+                         "r"(w[8 * j]), "r"(w[8 * j + 1]), "r"(w[8 * j + 2]), "r"(w[8 * j + 3]), "r"(w[8 * j + 4]),
+                         "r"(w[8 * j + 5]), "r"(w[8 * j + 6]), "r"(w[8 * j + 7])
+                         : "memory");
+    } else {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+}
 
 // Writes 32 floats as bf16 into the 4 chunks (4*hf .. 4*hf+3) of a 128-byte swizzled row.
 __device__ __forceinline__ void store_row32_swz(uint8_t *row_base, int row, int hf, const float *v) {
@@ -671,6 +693,11 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             dt_next = load_dtv(ci, h + 1);
             A_next = p.A[h + 1];
             D_next = p.D ? p.D[h + 1] : 0.f;
+        } else if (s_item[0] < p.n_items) {   // last head: the next item's first head (taken at this head's start)
+            decode(s_item[0], nxt);
+            dt_next = load_dtv(nxt.ci, nxt.h0);
+            A_next = p.A[nxt.h0];
+            D_next = p.D ? p.D[nxt.h0] : 0.f;
         }
         {   // dx = dx_diag + w o u + D dyp; x.u row sums; then e o dyp over the dyp tile
             float dxd[32], u[32], xv[32], dyp[32];
@@ -688,13 +715,9 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 o[i] = dxd[i] + ws * u[i] + Dh * dyp[i];
             }
             fm[F_ROWXU + hf * 128 + row] = xu;
-            if (live) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.dx + (int64_t)ci.b * p.sdxb + tok * p.sdxl + (int64_t)h * p.sdxh + 32 * hf);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                                        pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
-            }
+            if (live)
+                store_row32_global(p.dx + (int64_t)ci.b * p.sdxb + tok * p.sdxl + (int64_t)h * p.sdxh + 32 * hf, o,
+                                   p.st32 != 0);
             const float el = ex2(cs2[row]);
 #pragma unroll
             for (int i = 0; i < 32; ++i) dyp[i] *= el;
@@ -748,11 +771,8 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 float o[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = fz[i] * (yd[i] + el * yb[i] + Dh * xv[i]);
-                uint4 *dst = reinterpret_cast<uint4 *>(p.dz + (int64_t)ci.b * p.sdzb + tok * p.sdzl + (int64_t)h * p.sdzh + 32 * hf);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                                        pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+                store_row32_global(p.dz + (int64_t)ci.b * p.sdzb + tok * p.sdzl + (int64_t)h * p.sdzh + 32 * hf, o,
+                                   p.st32 != 0);
             }
         }
         {   // T3 = exp(cs[Q-1]) <S_in, dS>: fixed-order block reduction
@@ -770,13 +790,9 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             }
             ++st_issued;
             ++ld_issued;
-        } else if (s_item[0] < p.n_items) {
-            decode(s_item[0], nxt);
+        } else if (s_item[0] < p.n_items) {   // nxt and its dt were read after group 2
             have_next = true;
             issue_first(nxt);
-            dt_next = load_dtv(nxt.ci, nxt.h0);
-            A_next = p.A[nxt.h0];
-            D_next = p.D ? p.D[nxt.h0] : 0.f;
         }
         {   // ---- per-position scalars (threads 0..127 = position i)
             const int i = tid;
@@ -972,6 +988,11 @@ static BwdParams make_params(const Shape &sh, const int32_t *hdr, const ChunkInf
     p.sdBb = a.sdB ? a.sdB[0] : 0; p.sdBl = a.sdB ? a.sdB[1] : 0; p.sdBg = a.sdB ? a.sdB[2] : 0;
     p.sdCb = a.sdC ? a.sdC[0] : 0; p.sdCl = a.sdC ? a.sdC[1] : 0; p.sdCg = a.sdC ? a.sdC[2] : 0;
     p.k_pairs = a.k_pairs; p.nsub_tail = a.nsub_tail; p.n_items = a.n_items; p.tpart = a.tpart;
+    // 256-bit row stores need every dx / dz row piece 32-byte aligned: base and all strides
+    auto a32 = [](const void *ptr, const int64_t *st) {
+        return ptr == nullptr || ((uintptr_t)ptr % 32 == 0 && st[0] % 16 == 0 && st[1] % 16 == 0 && st[2] % 16 == 0);
+    };
+    p.st32 = (a32(a.dx, a.sdx) && a32(a.dz, a.sdz)) ? 1 : 0;
     return p;
 }
 

@@ -155,3 +155,40 @@ def test_bwd_tail_split(lens):
     else:
         w = I.Workload("v", 1, sum(lens), 32, 64, 4, 128, 128, "bf16", has_z=True, has_init=True, seqlens=lens)
     check_bwd(w, algo="fused")
+
+
+def test_bwd_row_store_alignment_paths_agree():
+    """dx / dz rows go out as 256-bit stores when base and strides are 32-byte aligned, as
+    128-bit stores otherwise (16-byte aligned views): both give the same bits."""
+    from state_space_model_scan_gb300 import _lib
+    from helpers import to_dev
+    w = W(L=700, H=8, P=64, G=2, N=128, Q=128, dtype="bf16", has_z=True, has_init=True)
+    inp = I.make_inputs(w, with_grad_inputs=True, with_dfinal=True)
+    d = to_dev(inp)
+    H = w.nheads
+
+    def run(offset):
+        n = d["x"].numel()
+        bx = torch.zeros(n + 16, dtype=torch.bfloat16, device="cuda")
+        bz = torch.zeros(n + 16, dtype=torch.bfloat16, device="cuda")
+        dx = bx[offset:offset + n].view(d["x"].shape)
+        dz = bz[offset:offset + n].view(d["x"].shape)
+        g = dict(ddt=torch.empty_like(d["dt_raw"]), dA=torch.empty(H, device="cuda"), dB=torch.empty_like(d["B"]),
+                 dC=torch.empty_like(d["C"]), dD=torch.empty(H, device="cuda"), ddt_bias=torch.empty(H, device="cuda"),
+                 dinit=torch.empty_like(d["initial_states"]))
+        prob = _lib.problem(w.batch, w.seqlen, H, 64, w.ngroups, 128, 128)
+        fa = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], None, D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                           initial_states=d["initial_states"])
+        ba = _lib.bwd_args(fa, d["dy"], dx, g["ddt"], g["dA"], g["dB"], g["dC"], dD=g["dD"], dz=dz,
+                           ddt_bias=g["ddt_bias"], dinitial_states=g["dinit"], dfinal_states=d["dfinal_states"])
+        ws = torch.empty(_lib.bwd_workspace_size(prob, ba), dtype=torch.uint8, device="cuda")
+        _lib.check(_lib.ssd_bwd(prob, ba, ws), "ssd_bwd")
+        torch.cuda.synchronize()
+        return dx.clone(), dz.clone(), g
+
+    dx0, dz0, g0 = run(0)      # 32-byte aligned base
+    dx1, dz1, g1 = run(8)      # 16 bytes off
+    assert dx0.data_ptr() % 32 == 0
+    assert torch.equal(dx0, dx1) and torch.equal(dz0, dz1)
+    for k in g0:
+        assert torch.equal(g0[k], g1[k]), k
