@@ -317,9 +317,12 @@ constexpr uint32_t O_WX = O_E + BC_BYTES;          // w o x  [s][p]   16 KB } be
 constexpr uint32_t O_SD = O_WX + X_BYTES;          // dS     [p][n]   16 KB }   fp32 [p][n] (bulk copy)
 constexpr uint32_t O_MISC = O_SD + S_BYTES;
 // misc floats
-constexpr int F_CS2 = 0, F_DT = 128, F_W = 256, F_ROWT1 = 384, F_ROWXU = 640, F_ROWT2 = 896, F_ROWD = 1152,
-              F_COLP = 1408, F_GD = 1920, F_RED = 2176, F_WSUM = 2192, F_PB = 2208, F_END = 2216;
-// F_GD: per position s, {exp(cs[a] - cs[s]), dt[s]} with a the last position of s's 32-block
+constexpr int F_ROWT1 = 0, F_ROWXU = 256, F_ROWT2 = 512, F_ROWD = 768, F_COLP = 1024, F_RED = 1536,
+              F_WSUM = 1552, F_PB = 1568, F_TSUM = 1576, F_TAB = 1584, F_END = 3120;
+// Per-head position tables, two sets (the next head's is built while this head runs):
+// T_CS2 cs log2 e, T_DT dt, T_W w = dt exp(cs[Q-1] - cs), T_GD {exp(cs[a] - cs[s]), dt[s]}
+// with a the last position of s's 32-block, T_VR dt_raw + dt_bias.
+constexpr int T_CS2 = 0, T_DT = 128, T_W = 256, T_GD = 384, T_VR = 640, TAB_STRIDE = 768;
 constexpr uint32_t BWD_SMEM = O_MISC + F_END * 4 + 64 + 1024;
 
 // TMEM columns: dB and dC accumulate over the CTA's heads and C B^T (shared by the
@@ -348,7 +351,9 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     const int H = p.sh.H, G = p.sh.G, hpg = p.sh.hpg, nsub_main = hpg / p.hs;
     const bool has_z = p.z != nullptr;
     float *fm = reinterpret_cast<float *>(sm + O_MISC);
-    float *cs2 = fm + F_CS2, *dtc = fm + F_DT, *wst = fm + F_W;
+    int tb = 0;   // table set of the current head
+    float *cs2 = fm + F_TAB + T_CS2, *dtc = fm + F_TAB + T_DT, *wst = fm + F_TAB + T_W, *vrt = fm + F_TAB + T_VR;
+    const float2 *gdt = reinterpret_cast<const float2 *>(fm + F_TAB + T_GD);
     // 0: B/C, 1: x/S_in, 2: MMA (dx and y tiles), 3: dy/z/dS, 4: MMA (dB/dC chains)
     uint64_t *bar = reinterpret_cast<uint64_t *>(fm + F_END);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 5);
@@ -445,23 +450,50 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         ++ld_issued;
     };
     // dt_raw + bias of position tid for a head (0 past the chunk's end)
+    // dt_raw + bias at position tid - 128 (warps 4..7; 0 past the chunk's end)
     auto load_dtv = [&](const ChunkInfo &c, int h) -> float {
-        return tid < c.len ? p.dt_raw[(int64_t)c.b * p.sdb + (int64_t)(c.t0 + tid) * p.sdl + h] +
+        const int pos = tid - 128;
+        return pos < c.len ? p.dt_raw[(int64_t)c.b * p.sdb + (int64_t)(c.t0 + pos) * p.sdl + h] +
                                  (p.bias ? p.bias[h] : 0.f)
                            : 0.f;
+    };
+    // Warps 4..7 (position tid - 128): a head's tables into set `set` (dt, the in-chunk cumulative
+    // log-decay by a fixed-order scan over the four warps' partial sums, w, the block factors)
+    auto build_tables = [&](int set, float vraw, float Aval, int clen) {
+        const int pos = tid - 128, wl = warp - 4;
+        float *T = fm + F_TAB + set * TAB_STRIDE;
+        const float dt = pos < clen ? softplus_f(vraw) : 0.f;
+        const float x = warp_incl_sum(dt * Aval);
+        if (lane == 31) fm[F_TSUM + wl] = x;
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        float off = 0.f, tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (i < wl) off += fm[F_TSUM + i];
+            tot += fm[F_TSUM + i];
+        }
+        const float c2 = (x + off) * LOG2E, cl = tot * LOG2E;
+        const float c31 = __shfl_sync(0xffffffffu, c2, 31);   // position pos | 31
+        T[T_CS2 + pos] = c2;
+        T[T_DT + pos] = dt;
+        T[T_W + pos] = dt * ex2(cl - c2);
+        reinterpret_cast<float2 *>(T + T_GD)[pos] = make_float2(ex2(c31 - c2), dt);
+        T[T_VR + pos] = vraw;
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // F_TSUM read before a later build rewrites it
     };
     if (tid == 0) s_item[0] = take();
     __syncthreads();
     Item cur;
     bool have = s_item[0] < p.n_items;
-    float dt_next = 0.f, A_next = 0.f, D_next = 0.f;
+    float A_next = 0.f, D_next = 0.f;
     if (have) {
         decode(s_item[0], cur);
         issue_first(cur);
-        dt_next = load_dtv(cur.ci, cur.h0);
         A_next = p.A[cur.h0];
         D_next = p.D ? p.D[cur.h0] : 0.f;
+        if (tid >= 128) build_tables(0, load_dtv(cur.ci, cur.h0), A_next, cur.ci.len);
     }
+    __syncthreads();
 
     while (have) {   // work items
     const int item = cur.item, nsub = cur.nsub, k = cur.k, g = cur.g, HS = cur.HS, h0 = cur.h0;
@@ -476,22 +508,12 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int h = h0 + hi;
         if (hi + 1 == HS && tid == 0) s_item[0] = take();   // the item after this one (read after the head's syncs)
         const float Dh = D_next, Ah = A_next;
-        const float vcur = dt_next;   // dt_raw + bias at position tid
-        {   // dt and the in-chunk cumulative log-decay (cs2 = cs log2 e)
-            const float dt = tid < ci.len ? softplus_f(vcur) : 0.f;
-            float tot;
-            const float cs = block_scan256(tid < QT ? dt * Ah : 0.f, fm + F_WSUM, &tot);
-            if (tid < QT) {
-                dtc[tid] = dt;
-                cs2[tid] = cs * LOG2E;
-            }
-            __syncthreads();
+        {   // this head's tables (built during the previous head, or before the first)
+            float *T = fm + F_TAB + tb * TAB_STRIDE;
+            cs2 = T + T_CS2; dtc = T + T_DT; wst = T + T_W; vrt = T + T_VR;
+            gdt = reinterpret_cast<const float2 *>(T + T_GD);
         }
         const float cl2 = cs2[QT - 1];
-        if (tid < QT) {
-            wst[tid] = dtc[tid] * ex2(cl2 - cs2[tid]);
-            reinterpret_cast<float2 *>(fm + F_GD)[tid] = make_float2(ex2(cs2[tid | 31] - cs2[tid]), dtc[tid]);
-        }
         if (!mbar_wait(&bar[3], st_done & 1)) fail();   // dy, z, dS of this head landed
         ++st_done;
         if (!mbar_wait(&bar[1], ld_done & 1)) fail();   // x and S_in of this head landed
@@ -501,6 +523,22 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             ++bc_done;
         }
         __syncthreads();
+        // the next head (this item's, or the first of the item taken at this head's start): its
+        // dt (warps 4..7), A and D are read now; warps 4..7 build its tables during group 2
+        bool nh_has = false;
+        int nh = 0, nh_len = 0;
+        if (hi + 1 < HS) {
+            nh_has = true; nh = h + 1; nh_len = ci.len;
+        } else if (s_item[0] < p.n_items) {
+            decode(s_item[0], nxt);
+            nh_has = true; nh = nxt.h0; nh_len = nxt.ci.len;
+        }
+        float v_next = 0.f;
+        if (nh_has) {
+            if (tid >= 128) v_next = load_dtv(hi + 1 < HS ? ci : nxt.ci, nh);
+            A_next = p.A[nh];
+            D_next = p.D ? p.D[nh] : 0.f;
+        }
         float fz[32];   // dy silu'(z): dz = fz o ypre
         float t3p = 0.f;
         {
@@ -600,7 +638,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             float rowt1 = 0.f;
             const int l = row;
             const float c2l = cs2[l];
-            const float2 *gd = reinterpret_cast<const float2 *>(fm + F_GD);
+            const float2 *gd = gdt;
             float *colp = fm + F_COLP;   // [8 warps][64]
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
@@ -688,17 +726,8 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                           kk > 0);
             umma_commit(&bar[2]);
         }
+        if (nh_has && tid >= 128) build_tables(tb ^ 1, v_next, A_next, nh_len);   // while group 2 runs
         wait_mma();
-        if (hi + 1 < HS) {
-            dt_next = load_dtv(ci, h + 1);
-            A_next = p.A[h + 1];
-            D_next = p.D ? p.D[h + 1] : 0.f;
-        } else if (s_item[0] < p.n_items) {   // last head: the next item's first head (taken at this head's start)
-            decode(s_item[0], nxt);
-            dt_next = load_dtv(nxt.ci, nxt.h0);
-            A_next = p.A[nxt.h0];
-            D_next = p.D ? p.D[nxt.h0] : 0.f;
-        }
         {   // dx = dx_diag + w o u + D dyp; x.u row sums; then e o dyp over the dyp tile
             float dxd[32], u[32], xv[32], dyp[32];
             tmem_ld32(tmem + lb + T_DXD + 32 * hf, dxd);
@@ -790,7 +819,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             }
             ++st_issued;
             ++ld_issued;
-        } else if (s_item[0] < p.n_items) {   // nxt and its dt were read after group 2
+        } else if (s_item[0] < p.n_items) {   // nxt was decoded, its tables built, during this head
             have_next = true;
             issue_first(nxt);
         }
@@ -821,7 +850,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             if (i < QT) {
                 const float da = dtot - inc + dcs + T3 + t4tot;
                 if (i < ci.len) {
-                    const float gv = (ddir + Ah * da) * sigmoid_f(vcur);
+                    const float gv = (ddir + Ah * da) * sigmoid_f(vrt[i]);
                     p.ddt[(int64_t)ci.b * p.sddb + (int64_t)(ci.t0 + i) * p.sddl + h] = gv;
                     pa = dtc[i] * da;
                     pb = gv;
@@ -850,6 +879,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 pp[0] = ta; pp[1] = td; pp[2] = tb; pp[3] = 0.f;
             }
         }
+        tb ^= 1;
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
