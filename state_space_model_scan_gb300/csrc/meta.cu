@@ -12,6 +12,8 @@
 // blocks of KB.  Units are listed by (block, sequence, segment), so a unit only
 // ever depends on units listed before it and the units of one sequence inside
 // one block are consecutive in the list.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace ssd {
@@ -183,6 +185,61 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
     }
 }
 
+// Fixed-length batch (no cu_seqlens): every sequence has the same chunk and segment
+// counts, so each list entry has a closed form -- the lists the general kernel builds,
+// entry for entry, with one thread per entry and no block-wide steps.  Sequence s = row s;
+// chunk c = (s, c mod nch); units of block blk (KB segments, cnt in the last) are listed
+// sequence by sequence, so unit (s, j = blk KB + i) sits at B blk KB + s cnt + i.
+__global__ void __launch_bounds__(kMetaThreads)
+k_build_meta_fixed(int B, int L, int Q, int R, int num, int den, int KB, int kmax, int umax, int32_t *hdr,
+                   SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units, uint32_t *zero_words, int64_t n_zero) {
+    const int nch = (L + Q - 1) / Q;
+    const int nseg = seg_count(nch, R, num, den);
+    const int64_t nchunks = (int64_t)B * nch, nunits = units != nullptr ? (int64_t)B * nseg : 0;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool fits = nchunks <= kmax && nunits <= umax;
+    if (t0 == 0) {
+        for (int i = 0; i < HDR_WORDS; ++i) hdr[i] = 0;
+        if (!fits) hdr[HDR_STATUS] = SSD_ERR_INVALID_ARGUMENT;
+        hdr[HDR_NCHUNKS] = fits ? (int)nchunks : 0;
+        hdr[HDR_NUNITS] = fits ? (int)nunits : 0;
+        hdr[HDR_NSEQS] = B;
+        hdr[HDR_MAXSEG] = nseg;
+    }
+    for (int64_t i = t0; i < n_zero; i += stride) zero_words[i] = 0u;
+    if (!fits) return;
+    for (int64_t s = t0; s < B; s += stride) {
+        SeqInfo si;
+        si.b = (int)s; si.t0 = 0; si.len = L; si.chunk0 = (int)(s * nch);
+        seqs[s] = si;
+    }
+    for (int64_t c = t0; c < nchunks; c += stride) {
+        const int s = (int)(c / nch), j = (int)(c % nch);
+        ChunkInfo ci;
+        ci.seq = s; ci.b = s; ci.t0 = j * Q; ci.len = min(Q, L - j * Q);
+        chunks[c] = ci;
+    }
+    const int base = nseg > 0 ? nch / nseg : 0, rem = nseg > 0 ? nch % nseg : 0;
+    for (int64_t u = t0; u < nunits; u += stride) {
+        const int64_t blk = u / ((int64_t)B * KB);          // full blocks before hold B KB units each
+        const int cnt = min(KB, nseg - (int)blk * KB);
+        const int64_t r = u - blk * B * KB;
+        const int s = (int)(r / cnt), i = (int)(r % cnt);
+        const int j = (int)blk * KB + i;
+        UnitInfo ui;
+        ui.seq = s; ui.b = s;
+        const int c0 = j * base + min(j, rem);
+        ui.t0 = c0 * Q;
+        ui.nchunk = base + (j < rem ? 1 : 0);
+        ui.len = min(ui.nchunk * Q, L - c0 * Q);
+        ui.prev = j == 0 ? -1 : (i > 0 ? (int)u - 1 : (int)((blk - 1) * B * KB + (int64_t)s * KB + KB - 1));
+        ui.last = j == nseg - 1 ? 1 : 0;
+        ui.j = j;
+        units[u] = ui;
+    }
+}
+
 // final_states[s] = initial_states[s] (or 0) for sequences with no tokens.
 __global__ void k_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr,
                                   const float *init, float *final_) {
@@ -221,8 +278,15 @@ cudaError_t launch_wait_probe(int32_t *hdr, int wait_ms, cudaStream_t st) {
 cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int R, int num, int den, int KB,
                               int kmax, int umax, int32_t *hdr, SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units,
                               int32_t *last_unit, uint32_t *zero_words, int64_t n_zero, cudaStream_t st) {
-    k_build_meta<<<1, kMetaThreads, 0, st>>>(cu, B, L, S, Q, R, num, den, KB, kmax, umax, hdr, seqs, chunks, units,
-                                             last_unit, zero_words, n_zero);
+    if (cu == nullptr) {
+        const int64_t work = std::max<int64_t>({(int64_t)B * ((L + Q - 1) / Q), n_zero, (int64_t)B, 1});
+        const int blocks = (int)std::min<int64_t>((work + kMetaThreads - 1) / kMetaThreads, 256);
+        k_build_meta_fixed<<<blocks, kMetaThreads, 0, st>>>(B, L, Q, R, num, den, KB, kmax, umax, hdr, seqs, chunks,
+                                                            units, zero_words, n_zero);
+    } else {
+        k_build_meta<<<1, kMetaThreads, 0, st>>>(cu, B, L, S, Q, R, num, den, KB, kmax, umax, hdr, seqs, chunks, units,
+                                                 last_unit, zero_words, n_zero);
+    }
     return cudaGetLastError();
 }
 

@@ -131,3 +131,39 @@ def test_bad_cu_seqlens_reported_on_device(bad):
     assert _lib.ssd_fwd(prob, args, ws) == 0
     assert _lib.query_status(ws) == 1
     assert (y == 7.0).all() and (fin == 7.0).all()
+
+
+@pytest.mark.parametrize("B,L,seg,algo", [(3, 1000, 2, "fused"), (2, 8192, 0, "fused"), (1, 129, 1, "fused"),
+                                          (3, 700, 0, "staged"), (2, 1, 0, "staged")])
+def test_fixed_batch_metadata_bit_exact(B, L, seg, algo):
+    """Without cu_seqlens the lists have a closed form (one thread per entry): still the CPU
+    builder's lists, entry for entry."""
+    from oracle import meta
+    fused = algo == "fused"
+    P, N, Q = (64, 128, 128) if fused else (16, 16, 64)
+    w = I.Workload("fb", B, L, 4, P, 2, N, Q, "bf16")
+    inp = I.make_inputs(w)
+    d = to_dev(inp)
+    y = torch.empty_like(d["x"])
+    prob = _lib.problem(B, L, 4, P, 2, N, Q, 0, algo, seg)
+    args = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], dt_bias=d["dt_bias"])
+    ws = torch.empty(_lib.fwd_workspace_size(prob, args), dtype=torch.uint8, device="cuda")
+    _lib.check(_lib.ssd_fwd(prob, args, ws), "ssd_fwd")
+    torch.cuda.synchronize()
+    lay = _lib.debug_layout(prob, args)
+    raw = ws.cpu().numpy()
+    counts = raw[lay.meta_counts:lay.meta_counts + 16].view(np.int32)
+    if fused:
+        R = int(prob.seg_chunks) or None
+        nch = -(-L // 128)
+        # the library's own unit size when seg = 0: read it back from the unit list's first entry
+        got = raw[lay.units:lay.units + 32 * counts[1]].view(np.int32).reshape(-1, 8)
+        R = R or int(got[0][4])
+        ref = meta.build(batch=B, seqlen=L, Q=128, R=R, KB=4)
+        assert counts[1] == len(ref["units"]) and counts[3] == 0
+        assert np.array_equal(got, np.array(ref["units"], dtype=np.int32))
+    else:
+        ref = meta.build(batch=B, seqlen=L, Q=lay.qi)
+    assert counts[0] == len(ref["chunks"]) and counts[3] == 0
+    got_c = raw[lay.chunk_info:lay.chunk_info + 16 * counts[0]].view(np.int32).reshape(-1, 4)
+    assert np.array_equal(got_c, np.array(ref["chunks"], dtype=np.int32))
