@@ -261,9 +261,9 @@ def run_gpu(args):
     with torch.cuda.graph(gb, stream=s):
         _lib.check(_lib.ssd_bwd(prob, bargs, wsb, torch.cuda.current_stream()), "ssd_bwd")
     # kernels per call: forward = metadata + fused forward; backward (chunk states kept by the
-    # forward) = metadata, dstates, reverse state scan, gradient kernel, the tail pairs' dB/dC
-    # reduction, head reduction (the ncu launch list in profiles/ shows the same set)
-    launches_fwd, launches_bwd = 2, 6
+    # forward) = metadata, dstates, reverse state scan, gradient kernel, the finishing sums
+    # (tail pairs' dB/dC, per-head dA/dD/ddt_bias) (the ncu launch list in profiles/ shows the same set)
+    launches_fwd, launches_bwd = 2, 5
 
     def step(ev=None):
         with torch.cuda.stream(s):

@@ -563,6 +563,7 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         ta.k_pairs = pl.k_pairs; ta.nsub_tail = pl.nsub_tail; ta.n_items = pl.n_items;
         ta.grid = pl.n_items < num_sms() ? pl.n_items : num_sms();
         ta.tpart = at<float>(ws, pl.off_tpart);
+        ta.dA = (float *)b->dA.ptr; ta.dD = (float *)b->dD.ptr; ta.dbias = (float *)b->ddt_bias.ptr;
         if (sh.kmax > 0) SSD_CUDA(launch_bwd_dstates_tc(sh, hdr, chunks, ta, st));
         SSD_CUDA(launch_state_passing(sh, hdr, seqs, clam, 1, dS, (const float *)b->dfinal_states.ptr,
                                       (float *)b->dinitial_states.ptr, 1, st));
@@ -575,9 +576,10 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
                 ss.hpg = sh.hpg / pl.hs;
                 SSD_CUDA(launch_reduce_group<__nv_bfloat16>(ss, hdr, chunks, dBh, mview(b->dB), dCh, mview(b->dC), st));
             }
+        } else {   // no chunks: the per-head sums (zero) without the gradient kernel's finishing launch
+            SSD_CUDA(launch_reduce_heads(sh, hdr, part, (float *)b->dA.ptr, (float *)b->dD.ptr,
+                                         (float *)b->ddt_bias.ptr, st));
         }
-        SSD_CUDA(launch_reduce_heads(sh, hdr, part, (float *)b->dA.ptr, (float *)b->dD.ptr,
-                                     (float *)b->ddt_bias.ptr, st));
         return SSD_OK;
     }
     SSD_TRY(run_forward_states(pl, a, ws, nullptr, st));

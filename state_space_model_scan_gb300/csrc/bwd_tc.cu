@@ -66,6 +66,7 @@ struct BwdParams {
     int k_pairs, nsub_tail, n_items;   // gradient kernel work items
     int st32;                // dx and dz rows are 32-byte aligned: stored with 256-bit stores
     float *tpart;
+    float *dA, *dD, *dbias;
 };
 
 __device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t col_bytes) {
@@ -886,7 +887,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
     // ---- dB, dC of the item's heads: final bf16 rows when the item covers the group; else
     // fp32 shares, summed in subset order afterwards by k_reduce_group (main items) or
-    // k_reduce_tail (the split pairs of the tail)
+    // k_bwd_finish (the split pairs of the tail)
     if (aborted || __syncthreads_or(bad)) {
         aborted = true;
         break;
@@ -946,12 +947,37 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// dB/dC of the pairs (chunk, group) split into subsets at the tail of the gradient kernel:
-// the subsets' fp32 shares summed in subset order.  grid (tail pairs, 2 (dB, dC), Q/16), 256
-// threads: 16 rows x 128 columns of one pair, 8 values a thread.
+// The two sums after the gradient kernel, one launch (their outputs are disjoint):
+//  - blocks [0, tail_blocks): dB/dC of the pairs (chunk, group) split into subsets at the tail
+//    of the gradient kernel, the subsets' fp32 shares summed in subset order; block =
+//    (tail pair, dB or dC, 16 rows), 256 threads: 16 rows x 128 columns, 8 values a thread;
+//  - the next H blocks: dA, dD, ddt_bias of a head, its per-chunk partials summed in a fixed
+//    order.
 __global__ void __launch_bounds__(256)
-k_reduce_tail(const BwdParams p) {
-    const int tp = blockIdx.x, which = blockIdx.y, l0 = blockIdx.z * 16;
+k_bwd_finish(const BwdParams p, int tail_blocks) {
+    if ((int)blockIdx.x >= tail_blocks) {
+        __shared__ float red[3][8];
+        const int h = blockIdx.x - tail_blocks, tid = threadIdx.x;
+        const int nk = p.hdr[HDR_STATUS] != 0 ? 0 : p.hdr[HDR_NCHUNKS];
+        float a = 0.f, d = 0.f, b = 0.f;
+        for (int k = tid; k < nk; k += 256) {
+            const float *pp = p.partials + ((int64_t)k * p.sh.H + h) * 4;
+            a += pp[0]; d += pp[1]; b += pp[2];
+        }
+        a = warp_sum(a); d = warp_sum(d); b = warp_sum(b);
+        if ((tid & 31) == 0) { red[0][tid >> 5] = a; red[1][tid >> 5] = d; red[2][tid >> 5] = b; }
+        __syncthreads();
+        if (tid == 0) {
+            float ta = 0.f, td = 0.f, tb = 0.f;
+            for (int w = 0; w < 8; ++w) { ta += red[0][w]; td += red[1][w]; tb += red[2][w]; }
+            p.dA[h] = ta;
+            if (p.dD) p.dD[h] = td;
+            if (p.dbias) p.dbias[h] = tb;
+        }
+        return;
+    }
+    const int per = 2 * (QT / 16);
+    const int tp = blockIdx.x / per, which = (blockIdx.x % per) / (QT / 16), l0 = (blockIdx.x % (QT / 16)) * 16;
     const int pair = p.k_pairs + tp, k = pair / p.sh.G, g = pair % p.sh.G;
     if (p.hdr[HDR_STATUS] != 0 || k >= p.hdr[HDR_NCHUNKS]) return;
     const ChunkInfo ci = p.chunks[k];
@@ -1018,6 +1044,7 @@ static BwdParams make_params(const Shape &sh, const int32_t *hdr, const ChunkInf
     p.sdBb = a.sdB ? a.sdB[0] : 0; p.sdBl = a.sdB ? a.sdB[1] : 0; p.sdBg = a.sdB ? a.sdB[2] : 0;
     p.sdCb = a.sdC ? a.sdC[0] : 0; p.sdCl = a.sdC ? a.sdC[1] : 0; p.sdCg = a.sdC ? a.sdC[2] : 0;
     p.k_pairs = a.k_pairs; p.nsub_tail = a.nsub_tail; p.n_items = a.n_items; p.tpart = a.tpart;
+    p.dA = a.dA; p.dD = a.dD; p.dbias = a.dbias;
     // 256-bit row stores need every dx / dz row piece 32-byte aligned: base and all strides
     auto a32 = [](const void *ptr, const int64_t *st) {
         return ptr == nullptr || ((uintptr_t)ptr % 32 == 0 && st[0] % 16 == 0 && st[1] % 16 == 0 && st[2] % 16 == 0);
@@ -1062,11 +1089,10 @@ cudaError_t launch_bwd_chunk_tc(const Shape &sh, const int32_t *hdr, const Chunk
     if (e != cudaSuccess) return e;
     if (a.grid > 0) k_bwd_chunk_tc<<<a.grid, 256, BWD_SMEM, st>>>(mx, mb, mc, mdy, mz, p);   // persistent
     const int tail_pairs = sh.kmax * sh.G - a.k_pairs;
-    if (a.grid > 0 && tail_pairs > 0 && a.nsub_tail > 1 && a.hs == sh.hpg) {
-        cudaError_t e2 = cudaGetLastError();
-        if (e2 != cudaSuccess) return e2;
-        k_reduce_tail<<<dim3(tail_pairs, 2, QT / 16), 256, 0, st>>>(p);
-    }
+    const int tail_blocks = (a.grid > 0 && tail_pairs > 0 && a.nsub_tail > 1 && a.hs == sh.hpg) ? tail_pairs * 2 * (QT / 16) : 0;
+    cudaError_t e2 = cudaGetLastError();
+    if (e2 != cudaSuccess) return e2;
+    k_bwd_finish<<<tail_blocks + sh.H, 256, 0, st>>>(p, tail_blocks);
     return cudaGetLastError();
 }
 

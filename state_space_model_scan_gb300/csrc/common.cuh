@@ -70,6 +70,7 @@ struct BwdTcArgs {
     int k_pairs, nsub_tail, n_items, grid;   // grid: persistent CTAs (one per SM at most)
     float *tpart;                   // [tail item][2][Q][N] fp32
     void *dB, *dC;                  // final dB/dC (written directly when hs == H/G)
+    float *dA, *dD, *dbias;         // per-head gradients (sums of the per-(chunk, head) partials)
     const int64_t *sdB, *sdC;
 };
 

@@ -41,11 +41,20 @@ def test_varlen_fwd_full_size():
     check_sampled(I.named("varlen"), [0, 41, 79])
 
 
-def test_nemotron_nano_bwd_full_size():
-    """fwd+bwd workload: gradients of one whole group (dB/dC sum over its 8 heads)."""
+@pytest.mark.parametrize("kept", [False, True])
+def test_nemotron_nano_bwd_full_size(kept):
+    """fwd+bwd workload: gradients of one whole group (dB/dC sum over its 8 heads); with the
+    chunk states recomputed, and kept by the forward as bench.py's training step runs it."""
     w = I.named("nemotron_nano")
     inp = I.make_inputs(w, with_grad_inputs=True)
-    g = gpu_backward(w, inp)
+    kw = {}
+    if kept:
+        from helpers import to_dev
+        from state_space_model_scan_gb300.api import ssd_forward
+        d = to_dev(inp)
+        _, _, kw["chunk_states"] = ssd_forward(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"],
+                                               dt_bias=d["dt_bias"], chunk_size=w.chunk_size, keep_chunk_states=True)
+    g = gpu_backward(w, inp, **kw)
     heads = list(range(8, 16))          # group 1
     o = oracle_backward(w, inp, heads=heads)
     T = w.seqlen
