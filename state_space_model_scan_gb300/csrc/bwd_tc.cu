@@ -1,9 +1,11 @@
 // bwd_tc.cu -- tensor-core backward of the SSD chunked scan (bf16 inputs, fp32
 // accumulation), headdim 64, dstate 128, chunk 128.
 //
-// Recompute-based, as the Mamba-3-Lite "SSD Reference" page's section "6. The
-// autograd backward contract" prescribes (re-run the forward math, inject the true
-// upstream gradients).  Per chunk c of a sequence and head h, with
+// The forward math is re-run per chunk with the true upstream gradients injected, as the
+// Mamba-3-Lite "SSD Reference" page's section "6. The autograd backward contract"
+// describes; the carried states S_in are the ones the forward kept (ssd_fwd_args.chunk_states)
+// or, when it did not, recomputed by the fused forward in states-only mode.  Per chunk c
+// of a sequence and head h, with
 //   E[l][s] = exp(cs[l] - cs[s]) 1[s<=l], CB = C B^T, dyp = dy silu(z), dM = dyp x^T,
 //   M = E dt_s CB, E' = E dt_s dM, w_s = dt_s exp(cs[Q-1] - cs[s]), e_l = exp(cs[l]),
 //   S_in = carried state entering the chunk, dS = gradient of the state leaving it:
