@@ -34,14 +34,14 @@ def _args(w, inp):
 ], ids=lambda w: w.name)
 def test_noalloc_matches_workspace_forward_twice(w):
     inp = I.make_inputs(w)
-    prob, args, y_ref, fin_ref, _ = _args(w, inp)
+    prob, args, y_ref, fin_ref, d_ref = _args(w, inp)   # d_ref: the device inputs stay alive
     ws = torch.empty(_lib.fwd_workspace_size(prob, args), dtype=torch.uint8, device="cuda")
     assert ws.numel() <= _lib.NOALLOC_SCRATCH_BYTES
     _lib.check(_lib.ssd_fwd(prob, args, ws), "ssd_fwd")
     torch.cuda.synchronize()
     tol = TOL[w.dtype]
     for _ in range(2):
-        prob2, args2, y, fin, _ = _args(w, inp)
+        prob2, args2, y, fin, d2 = _args(w, inp)
         _lib.check(_lib.ssd_fwd_noalloc(prob2, args2), "ssd_fwd_noalloc")
         torch.cuda.synchronize()
         assert torch.isfinite(y.float()).all() and torch.isfinite(fin).all()
@@ -66,3 +66,22 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     need = _lib.fwd_workspace_size(prob, args)
     assert need > _lib.NOALLOC_SCRATCH_BYTES
     assert _lib.ssd_fwd_noalloc(prob, args) == 4
+
+
+def test_noalloc_forward_keeps_the_same_chunk_states():
+    """The allocation-free forward writes the caller's chunk-state buffer like ssd_fwd does."""
+    w = I.Workload("keep", 2, 900, 8, 64, 2, 128, 128, "bf16", has_z=True, has_init=True)
+    inp = I.make_inputs(w)
+    prob, args, y1, fin1, d1 = _args(w, inp)   # every tensor stays alive: args holds raw pointers
+    n = _lib.chunk_states_size(prob, args)
+    cs_ref = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    cs = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")
+    args.chunk_states = cs_ref.data_ptr()
+    ws = torch.empty(_lib.fwd_workspace_size(prob, args), dtype=torch.uint8, device="cuda")
+    _lib.check(_lib.ssd_fwd(prob, args, ws), "ssd_fwd")
+    prob2, args2, y2, fin2, d2 = _args(w, inp)
+    args2.chunk_states = cs.data_ptr()
+    _lib.check(_lib.ssd_fwd_noalloc(prob2, args2), "ssd_fwd_noalloc")
+    torch.cuda.synchronize()
+    used = 2 * 8 * 8 * 16384   # batch rows x chunks per row x heads x tile bytes
+    assert torch.equal(cs[:used], cs_ref[:used])
