@@ -70,3 +70,25 @@ def test_nemotron_nano_bwd_full_size(kept):
     )
     bad = {k: v for k, v in errs.items() if not v <= TOL["bf16"]}
     assert not bad, errs
+
+
+def test_long_sequence_bwd_one_group_of_128_heads():
+    """The long-sequence shape (128 heads in one B/C group) through the backward, with the
+    forward's kept chunk states: the gradient kernel covers the group in head subsets whose
+    dB/dC shares are summed afterwards."""
+    from helpers import to_dev
+    from state_space_model_scan_gb300.api import ssd_forward
+    w = I.Workload("long_bwd", 1, 1024, 128, 64, 1, 128, 128, "bf16", has_z=False, has_init=True)
+    inp = I.make_inputs(w, with_grad_inputs=True, with_dfinal=True)
+    d = to_dev(inp)
+    _, _, cs = ssd_forward(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], D=d["D"], dt_bias=d["dt_bias"],
+                           initial_states=d["initial_states"], chunk_size=128, keep_chunk_states=True)
+    g = gpu_backward(w, inp, chunk_states=cs)
+    o = oracle_backward(w, inp)
+    T = w.seqlen
+    errs = dict(dx=rel_l2(flat(g["dx"], T), o["dx"]), ddt=rel_l2(flat(g["ddt"], T), o["ddt_raw"]),
+                dB=rel_l2(flat(g["dB"], T), o["dB"]), dC=rel_l2(flat(g["dC"], T), o["dC"]),
+                dA=rel_l2(g["dA"].double().cpu().numpy(), o["dA"]), dD=rel_l2(g["dD"].double().cpu().numpy(), o["dD"]),
+                dinit=rel_l2(g["dinitial_states"].double().cpu().numpy(), o["dinit"]))
+    bad = {k: v for k, v in errs.items() if not v <= TOL["bf16"]}
+    assert not bad, errs
