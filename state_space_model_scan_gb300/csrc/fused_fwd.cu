@@ -25,7 +25,8 @@
 //              Y_off = C S_in^T                        (carried state readout)
 //              Y_diag = M x,  M = CB o exp(cs[l]-cs[s]) dt[s] 1[s<=l]
 //            y = (Y_diag + exp(cs) Y_off + D x) silu(z) is written once (bf16).
-// dt, cs, CB, M, chunk states and carried states never reach global memory;
+// dt, cs, CB, M and chunk states never reach global memory, nor do the carried
+// states unless the caller keeps them for the backward (FusedParams::states_out);
 // only the per-unit aggregates / end states (fp32, small) are exchanged.
 //
 // Every wait (TMA, MMA completion, predecessor flags) is bounded; on expiry the

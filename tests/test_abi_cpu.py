@@ -250,3 +250,46 @@ def test_bwd_workspace_drops_states_when_kept(lib):
     b.fwd = a
     assert m.load().ssd_bwd_workspace_size(ctypes.byref(p), ctypes.byref(b), ctypes.byref(n1)) == 0
     assert n0.value - n1.value >= 32 * 8 * 64 * 128 * 2
+
+
+def _tc_bwd_args(p, a):
+    m = lib_mod()
+    b = m.BwdArgs()
+    b.fwd = a
+    xs = [a.x.stride[i] for i in range(4)]
+    for f in ("dy", "dx", "dz"):
+        setattr(b, f, _fake(a.x.dtype, xs))
+    for f in ("dB", "dC"):
+        setattr(b, f, _fake(a.x.dtype, [a.B.stride[i] for i in range(4)]))
+    b.ddt = _fake(m.SSD_F32, [a.dt.stride[i] for i in range(3)])
+    for f in ("dA", "dD", "ddt_bias"):
+        setattr(b, f, _fake(m.SSD_F32, [1]))
+    return b
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("bwd_heads", 0, 0), ("bwd_heads", 2, 0), ("bwd_heads", 12, 0),   # 12 heads per group
+    ("bwd_heads", 5, 1),                                                # not a divisor of 12
+    ("bwd_heads", 33, 1), ("bwd_heads", -1, 1),
+    ("seg_chunks", 4, 0), ("seg_chunks", 5, 2),                         # the backward's recompute: 4 at most
+    ("seg_chunks", 9, 1),
+    ("reserved0", 1, 1),
+])
+def test_bwd_planner_validation(lib, field, value, code):
+    """The tensor-core backward's planning choices are checked on the host (no GPU)."""
+    m = lib_mod()
+    p, a = _tc_case(Bsz=1, L=1000, H=12, G=1)
+    p.algo = 2   # fused
+    setattr(p, field, value)
+    b = _tc_bwd_args(p, a)
+    n = ctypes.c_size_t(0)
+    assert m.load().ssd_bwd_workspace_size(ctypes.byref(p), ctypes.byref(b), ctypes.byref(n)) == code
+
+
+def test_fwd_accepts_five_chunk_units(lib):
+    p, a = _tc_case(Bsz=1, L=1000, H=12, G=1)
+    p.algo = 2
+    p.seg_chunks = 5
+    assert ws_size(p, a)[0] == 0
+    p.seg_chunks = 6
+    assert ws_size(p, a)[0] == 2
