@@ -162,6 +162,17 @@ def max_over_ranks(vals, device="cpu"):
 _ORACLE_INPUTS = {}
 
 
+def _cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_oracle_sample(w, seconds_budget=20.0):
     """Time the float64 oracle forward on a bounded sample of the workload:
     all tokens of a few heads (heads are independent), scaled to tokens/s of the
@@ -183,9 +194,19 @@ def cpu_oracle_sample(w, seconds_budget=20.0):
                        init=o["init"], cu=o["cu"], heads=heads, threads=cores)
     dt = time.perf_counter() - t0
     tok_per_s = (w.batch * w.seqlen) * (nheads / w.nheads) / dt
+    # the same oracle on one host thread: all tokens of a few heads, scaled by heads
+    n1 = min(4, w.nheads)
+    t1 = time.perf_counter()
+    sequential.forward(o["x"], o["dt_raw"], o["A"], o["B"], o["C"], D=o["D"], z=o["z"], dt_bias=o["dt_bias"],
+                       init=o["init"], cu=o["cu"], heads=list(range(n1)), threads=1)
+    dt1 = time.perf_counter() - t1
     return {"value": tok_per_s, "unit": "tokens/s", "cores": min(cores, nheads), "kind": "oracle",
             "sample": "float64 sequential oracle forward over %s (%d tokens, %.2f s)" % (what, w.batch * w.seqlen, dt),
-            "threads": sequential.num_threads()}
+            "threads": sequential.num_threads(),
+            "value_1thread": (w.batch * w.seqlen) * (n1 / w.nheads) / dt1,
+            "sample_1thread": "one host thread, all tokens of %d of %d heads, scaled by heads (%.2f s)" % (
+                n1, w.nheads, dt1),
+            "cpu": _cpu_model()}
 
 
 def run_reference(args):
