@@ -189,20 +189,22 @@ def cpu_oracle_sample(w, seconds_budget=20.0):
     heads = list(range(nheads))
     what = "the full workload" if nheads == w.nheads else "all tokens of %d of %d heads, scaled by heads" % (
         nheads, w.nheads)
-    t0 = time.perf_counter()
-    sequential.forward(o["x"], o["dt_raw"], o["A"], o["B"], o["C"], D=o["D"], z=o["z"], dt_bias=o["dt_bias"],
-                       init=o["init"], cu=o["cu"], heads=heads, threads=cores)
-    dt = time.perf_counter() - t0
-    tok_per_s = (w.batch * w.seqlen) * (nheads / w.nheads) / dt
-    # the same oracle on one host thread: all tokens of a few heads, scaled by heads
+    # the oracle on one host thread: all tokens of a few heads, scaled by heads
     n1 = min(4, w.nheads)
     t1 = time.perf_counter()
     sequential.forward(o["x"], o["dt_raw"], o["A"], o["B"], o["C"], D=o["D"], z=o["z"], dt_bias=o["dt_bias"],
                        init=o["init"], cu=o["cu"], heads=list(range(n1)), threads=1)
     dt1 = time.perf_counter() - t1
+    # and on every host core
+    t0 = time.perf_counter()
+    sequential.forward(o["x"], o["dt_raw"], o["A"], o["B"], o["C"], D=o["D"], z=o["z"], dt_bias=o["dt_bias"],
+                       init=o["init"], cu=o["cu"], heads=heads, threads=cores)
+    dt = time.perf_counter() - t0
+    threads = sequential.num_threads()
+    tok_per_s = (w.batch * w.seqlen) * (nheads / w.nheads) / dt
     return {"value": tok_per_s, "unit": "tokens/s", "cores": min(cores, nheads), "kind": "oracle",
             "sample": "float64 sequential oracle forward over %s (%d tokens, %.2f s)" % (what, w.batch * w.seqlen, dt),
-            "threads": sequential.num_threads(),
+            "threads": threads,
             "value_1thread": (w.batch * w.seqlen) * (n1 / w.nheads) / dt1,
             "sample_1thread": "one host thread, all tokens of %d of %d heads, scaled by heads (%.2f s)" % (
                 n1, w.nheads, dt1),
