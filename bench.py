@@ -451,6 +451,54 @@ def run_fwd_only(args):
                       "tokens_per_s": w.batch * w.seqlen / (sum(times) / len(times) * 1e-3)}))
 
 
+def run_sweep(args):
+    """Forward throughput of the other forward workloads (long-sequence sweep, packed varlen):
+    CUDA graph replay, L2 flushed before each run, median of --steps runs; one JSON line each."""
+    import torch
+    from state_space_model_scan_gb300 import inputs as I
+    from state_space_model_scan_gb300 import _lib
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    cases = [I.named("long_seq", L=L) for L in (1024, 2048, 4096, 8192, 16384, 32768)] + [I.named("varlen")]
+    for w in cases:
+        inp = I.make_inputs(w)
+        d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        S = w.nseqs
+        y = torch.empty_like(d["x"])
+        fin = torch.empty(S, w.nheads, w.headdim, w.dstate, device="cuda")
+        prob = _lib.problem(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk_size,
+                            S if d["cu_seqlens"] is not None else 0)
+        args_ = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], z=d["z"],
+                              dt_bias=d["dt_bias"], initial_states=d["initial_states"], final_states=fin,
+                              cu_seqlens=d["cu_seqlens"])
+        ws = torch.empty(_lib.fwd_workspace_size(prob, args_), dtype=torch.uint8, device="cuda")
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            _lib.check(_lib.ssd_fwd(prob, args_, ws, s), "ssd_fwd")
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            _lib.check(_lib.ssd_fwd(prob, args_, ws, torch.cuda.current_stream()), "ssd_fwd")
+        ts = []
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(s):
+                flush.fill_(1.0)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                g.replay()
+                e1.record(s)
+            s.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1))
+        ts.sort()
+        ms = ts[len(ts) // 2]
+        toks = w.batch * w.seqlen
+        per_tok = 2 * w.nheads * w.headdim * (3 if w.has_z else 2) + 2 * 2 * w.ngroups * w.dstate + 4 * w.nheads
+        alg = toks * per_tok + 4 * w.nheads * w.headdim * w.dstate * S * (2 if w.has_init else 1)
+        print(json.dumps({"mode": "sweep", "workload": w.name, "seqlen": w.seqlen, "nseqs": S, "nheads": w.nheads,
+                          "fwd_ms_median": ms, "tokens_per_s": toks / (ms * 1e-3),
+                          "algorithmic_bytes": alg, "algorithmic_gbs": alg / (ms * 1e-3) / 1e9}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,13 +506,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="bench", choices=["bench", "fwd"])
+    ap.add_argument("--mode", default="bench", choices=["bench", "fwd", "sweep"])
     ap.add_argument("--seg-chunks", type=int, default=0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.mode == "fwd":
         run_fwd_only(args)
+    elif args.mode == "sweep":
+        run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
