@@ -145,26 +145,32 @@ def test_bwd_requires_matching_gradients(lib):
     assert m.load().ssd_bwd_workspace_size(ctypes.byref(p), ctypes.byref(b), ctypes.byref(n)) == 1
 
 
-def test_metadata_reference_builder():
-    from oracle import meta
+def test_unit_schedule_restatement():
+    """The Python restatement of the library's tile and unit lists (a scheduler
+    self-consistency check, built on the oracle's segments) on two hand-worked cases."""
+    import unit_schedule as meta
     m = meta.build(cu=[0, 5, 5, 300], Q=64, R=2, KB=8)
-    assert m["chunks"] == [(0, 0, 0, 5), (2, 0, 5, 64), (2, 0, 69, 64), (2, 0, 133, 64), (2, 0, 197, 64),
-                           (2, 0, 261, 39)]
-    assert [u[:5] for u in m["units"]] == [(0, 0, 0, 5, 1), (2, 0, 5, 128, 2), (2, 0, 133, 128, 2), (2, 0, 261, 39, 1)]
+    # tiles: (seq, row, t0 of the physical chunk, end - t0, first - t0)
+    assert m["chunks"] == [(0, 0, 0, 5, 0), (2, 0, 0, 64, 5), (2, 0, 64, 64, 0), (2, 0, 128, 64, 0),
+                           (2, 0, 192, 64, 0), (2, 0, 256, 44, 0)]
+    assert [u[:5] for u in m["units"]] == [(0, 0, 0, 5, 1), (2, 0, 0, 128, 2), (2, 0, 128, 128, 2),
+                                           (2, 0, 256, 44, 1)]
     assert [u[5] for u in m["units"]] == [-1, -1, 1, 2]
     assert [u[6] for u in m["units"]] == [1, 0, 0, 1]
     assert [u[7] for u in m["units"]] == [0, 0, 1, 2]
-    # blocks of two segments: sequence 1's first block (j=0,1) is contiguous, then block 2
+    assert [u[8] for u in m["units"]] == [0, 5, 0, 0]
+    # blocks of two units; sequence 1 starts inside physical chunk 4 and has 6 tiles
     m = meta.build(cu=[0, 300, 600], Q=64, R=1, KB=2)
     assert [(u[0], u[7]) for u in m["units"]] == [(0, 0), (0, 1), (1, 0), (1, 1), (0, 2), (0, 3), (1, 2), (1, 3),
-                                                  (0, 4), (1, 4)]
-    assert [u[5] for u in m["units"]] == [-1, 0, -1, 2, 1, 4, 3, 6, 5, 7]
+                                                  (0, 4), (1, 4), (1, 5)]
+    assert [u[5] for u in m["units"]] == [-1, 0, -1, 2, 1, 4, 3, 6, 5, 7, 9]
+    assert [(u[2], u[3], u[8]) for u in m["units"] if u[0] == 1][:2] == [(256, 64, 44), (320, 64, 0)]
 
 
-def test_metadata_balanced_units():
-    """Units of one sequence differ by at most one chunk, the larger ones first, and
-    tile its chunks exactly; a units-per-chunk ratio above 1/R raises the count."""
-    from oracle import meta
+def test_unit_schedule_balanced_units():
+    """Units of one sequence differ by at most one tile, the larger ones first, and
+    cover its tiles exactly; a units-per-tile ratio above 1/R raises the count."""
+    import unit_schedule as meta
     m = meta.build(batch=2, seqlen=64 * 9, Q=64, R=4, KB=4)
     assert [u[4] for u in m["units"] if u[0] == 0] == [3, 3, 3]
     m = meta.build(batch=1, seqlen=128 * 64 - 5, Q=128, R=4, KB=4, num=19, den=64)
