@@ -14,13 +14,22 @@
  * h_{-1} is the initial state (zero when absent); the final state is h after the
  * last token of each sequence.
  *
- * The scan is evaluated in chunks (the chunkwise decomposition of that page's
- * section "ssd_complex_chunkwise -- the production scan": in-chunk cumulative
- * log-decay, intra-chunk segment-sum matrix, per-chunk states, carried chunk
- * states).  The chunk length only changes the association of the arithmetic,
- * never the function: the library uses its own internal chunk length (128 on
- * the tensor-core path, 64 on the SIMT path) and accepts any power-of-two
- * `chunk_size` in [16, 256] as a hint.
+ * The scan is evaluated in chunks of `chunk_size` tokens (the chunkwise
+ * decomposition of that page's section "ssd_complex_chunkwise -- the production
+ * scan": in-chunk cumulative log-decay, intra-chunk segment-sum matrix, per-chunk
+ * states, carried chunk states).  The chunk length only changes the association of
+ * the arithmetic, never the function, and the library computes with exactly the
+ * chunk length the caller passes: 128 on the tensor-core path (one M = 128 tcgen05
+ * tile per chunk), 64 on the SIMT path.  Any other value, or a value the chosen path
+ * does not compute, returns SSD_ERR_UNSUPPORTED; nothing is re-chunked silently.
+ *
+ * The chunk grid runs over each batch row's token axis: chunk c holds tokens
+ * [c*Q, (c+1)*Q).  With packed sequences (cu_seqlens) chunk boundaries need not meet
+ * sequence starts, and a chunk may hold parts (segments) of several sequences; the
+ * intra-chunk matrix then couples only tokens of one sequence, the carried state is
+ * reset to a sequence's initial state where it starts, mid-chunk or not, and its
+ * final state is the state after its last token.  ssd_varlen_metadata returns that
+ * grid's metadata.
  *
  * ---------------------------------------------------------------------------
  * Ownership and execution contract (all entry points)
@@ -60,7 +69,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 3
+#define SSD_ABI_VERSION 4
 
 typedef enum {
     SSD_OK = 0,
@@ -75,9 +84,11 @@ typedef enum {
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
 /* Which forward/backward pipeline to run.  AUTO takes the tensor-core path when
- * the inputs are bf16 and headdim == 64, dstate == 128 (the compiled tile set),
- * and the SIMT path otherwise (f32 inputs always take SIMT: fp32 inputs are
- * computed in fp32 FMA, never in tf32). */
+ * chunk_size == 128 and the inputs are bf16 with headdim == 64, dstate == 128 (the
+ * compiled tile set; tensors that break its 16-byte rule then return
+ * SSD_ERR_MISALIGNED), and the SIMT path when chunk_size == 64 (f32 inputs always
+ * take SIMT: fp32 inputs are computed in fp32 FMA, never in tf32); any other
+ * combination returns SSD_ERR_UNSUPPORTED. */
 typedef enum {
     SSD_ALGO_AUTO = 0,
     SSD_ALGO_STAGED = 1,   /* SIMT, one kernel per step: cumsum, chunk_state, state_passing, chunk_scan */
@@ -157,8 +168,14 @@ ssd_status ssd_chunk_states_size(const ssd_problem *prob, const ssd_fwd_args *ar
  * ssd_bwd_workspace_size / ssd_bwd
  * Gradients of L = sum(dy * y) + sum(dfinal_states * final_states) with respect
  * to x, dt (the raw input, through softplus), A, B, C, and D, z, dt_bias,
- * initial_states when given.  dB/dC sum over the heads of each group.  All
- * reductions run in a fixed order: results are bitwise reproducible.
+ * initial_states when given (Mamba-3-Lite "SSD Reference", section "6. The
+ * autograd backward contract": the backward recomputes what the forward did not
+ * keep; the stages are those the Helion pull request for the Mamba-2 SSD path times
+ * in "Measurements": chunk_scan_bwd_dstates, the reverse state passing,
+ * chunk_scan_chunk_state_bwd_dx, chunk_scan_bwd_dC, the dA/dt cumulative-sum
+ * gradients).  dB/dC sum over the heads of each group.  All reductions run in a
+ * fixed order: results are bitwise reproducible (that page's "Limitations":
+ * atomics make its backward nondeterministic; this one uses none).
  * The carried chunk states are recomputed inside (no saved activations are
  * needed) unless args->fwd.chunk_states holds the ones an ssd_fwd call of the same
  * problem and inputs wrote; then the recompute is skipped.
@@ -173,7 +190,10 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *args, void *work
  * Synchronises `stream`, then returns the device-side status word of the most
  * recent ssd_fwd/ssd_bwd call that used `workspace` (SSD_OK,
  * SSD_ERR_INVALID_ARGUMENT for bad cu_seqlens contents, SSD_ERR_DEVICE_TIMEOUT),
- * or SSD_ERR_CUDA if the synchronisation or the read fails.
+ * or SSD_ERR_CUDA if the synchronisation or the read fails.  The status lives in
+ * the caller-owned workspace, as the cuDNN frontend's Mamba-2 SSD engine keeps all
+ * scratch caller-owned and its calls allocation-free (that pull request's review
+ * notes); this is the one call here that synchronises.
  */
 ssd_status ssd_query_status(const void *workspace, void *stream);
 
@@ -203,14 +223,57 @@ ssd_status ssd_selftest_bounded_wait(void *workspace, size_t workspace_bytes, in
  * SSD_NOALLOC_SCRATCH_BYTES bytes; a problem whose ssd_fwd workspace would be
  * larger is rejected with SSD_ERR_WORKSPACE_TOO_SMALL before any launch.  The
  * array is loaded on the first call on a device, which also looks up its device
- * address once (make that first call before any stream capture); it stays
- * allocated until the process exits.  Nothing is allocated or freed per call.
+ * address (once per device and context: make that first call before any stream
+ * capture); it stays allocated until the process exits.  Nothing is allocated or
+ * freed per call.  Errors found on the device are read with
+ * ssd_noalloc_query_status.  Device ordinals from 64 up return SSD_ERR_CUDA.
  * All calls share the one array (each call re-initialises the parts that must
  * start at zero), so calls whose work overlaps on the GPU -- on different
  * streams or host threads without ordering -- race and must not be issued.
  */
 #define SSD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 ssd_status ssd_fwd_noalloc(const ssd_problem *prob, const ssd_fwd_args *args, void *stream);
+
+/*
+ * ssd_noalloc_query_status
+ * Synchronises `stream`, then returns the device-side status word that the most
+ * recent ssd_fwd_noalloc call on the current device left in the library's scratch
+ * array (SSD_OK, SSD_ERR_INVALID_ARGUMENT for bad cu_seqlens contents,
+ * SSD_ERR_DEVICE_TIMEOUT), or SSD_ERR_CUDA if the lookup, the synchronisation or the
+ * read fails.  The noalloc caller has no workspace to hand to ssd_query_status, so
+ * this reader is its only way to see errors found on the device.  No counterpart on
+ * the source pages.
+ */
+ssd_status ssd_noalloc_query_status(void *stream);
+
+/*
+ * ssd_varlen_metadata
+ * The integer metadata of packed sequences on the chunk grid: for cu_seqlens
+ * (int32 [nseqs + 1], device; cu[0] = 0, non-decreasing, cu[nseqs] = seqlen) and
+ * chunk length Q = chunk_size (1 .. 65536), with n_chunks = ceil(seqlen / Q):
+ *   seq_idx     int32 [seqlen]            the s with cu[s] <= t < cu[s+1], per token t
+ *                                         (may be NULL: not written)
+ *   chunk_begin int32 [n_chunks + 1]      index of chunk c's first segment; the last
+ *                                         entry is the number of segments
+ *   segments    int32 [n_chunks + nseqs][3] (seq, first token, end token) of every
+ *                                         maximal run of one chunk's tokens (tokens
+ *                                         [c*Q, min((c+1)*Q, seqlen))) that belongs to
+ *                                         one sequence, chunk by chunk, in token order
+ *   status      int32 [1]                 SSD_OK, or SSD_ERR_INVALID_ARGUMENT when the
+ *                                         contents of cu_seqlens break the rules above
+ *                                         (then nothing else is written)
+ * All pointers are device memory owned by the caller; work is enqueued on `stream`.
+ * The forward and backward build the same segments internally (one chunk tile per
+ * segment).  Definition: the packed (THD) path of the Helion pull request for the
+ * Mamba-2 SSD path ("Testing") and the vLLM fused-SSD pull request's cont-batch
+ * tests ("Test Plan"), sequences packed on one token axis with the chunk grid over
+ * that axis.  Returns SSD_ERR_INVALID_ARGUMENT for NULL required pointers or sizes
+ * out of range, SSD_ERR_UNSUPPORTED above 2^24 sequences or 2^30 tokens, SSD_ERR_CUDA
+ * if a launch fails.
+ */
+ssd_status ssd_varlen_metadata(const int32_t *cu_seqlens, int64_t nseqs, int64_t seqlen, int64_t chunk_size,
+                               int32_t *seq_idx, int32_t *chunk_begin, int32_t *segments, int32_t *status,
+                               void *stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *ssd_status_string(ssd_status status);
@@ -223,18 +286,22 @@ int32_t ssd_abi_version(void);
  * Byte offsets, inside an ssd_fwd workspace, of the intermediates the STAGED
  * forward leaves behind after it completes (for stage-by-stage checks):
  *   meta_counts : int32[4]  {n_chunks, n_units, n_seqs, status}
- *   chunk_info  : int32[n_chunks][4] {seq, batch row, first token in row, length}
+ *   chunk_info  : int32[n_chunks][8] {seq, batch row, first token t0 of the physical
+ *                 chunk in the row, end - t0, first - t0, 0, 0, 0}: one chunk tile per
+ *                 segment of a physical chunk; tile rows [first - t0, end - t0) are the
+ *                 sequence's
  *   dt          : f32[n_chunks][nheads][qi]   softplus(dt_raw + dt_bias), 0 past the chunk's length
  *   cs          : f32[n_chunks][nheads][qi]   inclusive in-chunk cumulative sum of dt*A
  *   states      : f32[n_chunks][nheads][headdim][dstate]  carry-in state of each chunk
- *   units       : int32[n_units][8] (fused path) {seq, batch row, first token, token count,
- *                 chunk count, index of the sequence's previous unit or -1, 1 if last unit
- *                 of its sequence, segment index j}; segment j of a sequence is its chunks
- *                 [j*R, (j+1)*R); segments are grouped in blocks of 4 and units are listed
- *                 by (block, sequence, segment)
- * where qi is the internal chunk length written to *qi.  Chunks are listed
- * sequence by sequence, in order, each sequence cut into qi-token chunks from its
- * first token (the last one ragged).  Offsets of -1 mean "not produced by algo".
+ *   units       : int32[n_units][12] (fused path) {seq, batch row, t0 of its first tile,
+ *                 end of the sequence's rows from t0 (capped at its tiles), tile count,
+ *                 index of the sequence's previous unit or -1, 1 if last unit of its
+ *                 sequence, unit index j within the sequence, first row of its first tile,
+ *                 0, 0, 0}; units are grouped in blocks of 4 and listed by (block,
+ *                 sequence, j)
+ * where qi is the chunk length (chunk_size) written to *qi.  Tiles are listed sequence
+ * by sequence, in order (the same order as chunk by chunk).  Offsets of -1 mean "not
+ * produced by algo".
  */
 typedef struct {
     int64_t meta_counts, chunk_info, dt, cs, states, units;

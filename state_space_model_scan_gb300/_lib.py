@@ -22,7 +22,7 @@ ALGO = {"auto": 0, "staged": 1, "fused": 2}
 # Every symbol include/ssd.h declares.
 EXPORTS = ["ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
            "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout", "ssd_fwd_noalloc",
-           "ssd_selftest_bounded_wait", "ssd_chunk_states_size"]
+           "ssd_selftest_bounded_wait", "ssd_chunk_states_size", "ssd_noalloc_query_status", "ssd_varlen_metadata"]
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -88,8 +88,13 @@ def load(path: str = LIB_PATH):
     lib.ssd_fwd_noalloc.argtypes = [P(Problem), P(FwdArgs), ctypes.c_void_p]
     lib.ssd_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p]
     lib.ssd_chunk_states_size.argtypes = [P(Problem), P(FwdArgs), P(ctypes.c_size_t)]
+    lib.ssd_noalloc_query_status.argtypes = [ctypes.c_void_p]
+    lib.ssd_varlen_metadata.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p]
     for f in ("ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
-              "ssd_fwd_debug_layout", "ssd_fwd_noalloc", "ssd_selftest_bounded_wait", "ssd_chunk_states_size"):
+              "ssd_fwd_debug_layout", "ssd_fwd_noalloc", "ssd_selftest_bounded_wait", "ssd_chunk_states_size",
+              "ssd_noalloc_query_status", "ssd_varlen_metadata"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -188,6 +193,30 @@ def ssd_bwd(prob, args, workspace, stream=None):
 def ssd_fwd_noalloc(prob, args, stream=None):
     """Raw call of the forward that uses the library's static scratch (no workspace)."""
     return load().ssd_fwd_noalloc(ctypes.byref(prob), ctypes.byref(args), _stream_handle(stream))
+
+
+def noalloc_query_status(stream=None):
+    """Status word the last ssd_fwd_noalloc call left on the current device (synchronises)."""
+    return int(load().ssd_noalloc_query_status(_stream_handle(stream)))
+
+
+def varlen_metadata(cu_seqlens, seqlen, chunk_size, stream=None, with_seq_idx=True):
+    """Packed-sequence metadata on the chunk grid (ssd_varlen_metadata): returns the raw
+    status code and, on SSD_OK, device tensors seq_idx [seqlen] (or None), chunk_begin
+    [n_chunks + 1], segments [n_chunks + nseqs, 3] (the first chunk_begin[-1] rows are
+    valid) and the device status word [1]."""
+    dev = cu_seqlens.device
+    S = cu_seqlens.numel() - 1
+    nch = -(-int(seqlen) // int(chunk_size))
+    seq_idx = torch.full((max(int(seqlen), 1),), -1, dtype=torch.int32, device=dev) if with_seq_idx else None
+    begin = torch.full((nch + 1,), -1, dtype=torch.int32, device=dev)
+    segs = torch.full((nch + S, 3), -1, dtype=torch.int32, device=dev)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    code = int(load().ssd_varlen_metadata(ctypes.c_void_p(cu_seqlens.data_ptr()), S, int(seqlen), int(chunk_size),
+                                          None if seq_idx is None else ctypes.c_void_p(seq_idx.data_ptr()),
+                                          ctypes.c_void_p(begin.data_ptr()), ctypes.c_void_p(segs.data_ptr()),
+                                          ctypes.c_void_p(status.data_ptr()), _stream_handle(stream)))
+    return code, seq_idx, begin, segs, status
 
 
 def selftest_bounded_wait(workspace, wait_ms, stream=None):

@@ -11,6 +11,8 @@ cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int
                               SeqInfo *seqs, ChunkInfo *chunks, UnitInfo *units, int32_t *last_unit,
                               uint32_t *zero_words, int64_t n_zero, cudaStream_t st);
 cudaError_t launch_wait_probe(int32_t *hdr, int wait_ms, cudaStream_t st);
+cudaError_t launch_varlen_metadata(const int32_t *cu, int S, int L, int Q, int32_t *status, int32_t *chunk_begin,
+                                   int32_t *segments, int32_t *seq_idx, cudaStream_t st);
 cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr, const float *init,
                                    float *final_, cudaStream_t st);
 // simt_fwd.cu
@@ -232,13 +234,22 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
                 if (t->stride[i] % 8 != 0) aligned = false;
         }
     }
+    // The chunk length is the caller's, never replaced: the tensor-core path computes
+    // 128-token chunks (one M = 128 tcgen05 tile per chunk), the SIMT path 64-token chunks.
+    bool fused = false;
     if (p->algo == SSD_ALGO_FUSED) {
-        if (!tc_ok) return SSD_ERR_UNSUPPORTED;
+        if (!tc_ok || p->chunk_size != kTcQ) return SSD_ERR_UNSUPPORTED;
         if (!aligned) return SSD_ERR_MISALIGNED;
+        fused = true;
+    } else if (p->algo == SSD_ALGO_STAGED) {
+        if (p->chunk_size != kSimtQ) return SSD_ERR_UNSUPPORTED;
+    } else if (p->chunk_size == kTcQ && tc_ok) {
+        if (!aligned) return SSD_ERR_MISALIGNED;
+        fused = true;
+    } else if (p->chunk_size != kSimtQ) {
+        return SSD_ERR_UNSUPPORTED;
     }
-    pl.algo = (p->algo == SSD_ALGO_FUSED || (p->algo == SSD_ALGO_AUTO && tc_ok && aligned)) ? SSD_ALGO_FUSED
-                                                                                           : SSD_ALGO_STAGED;
-    const bool fused = pl.algo == SSD_ALGO_FUSED;
+    pl.algo = fused ? SSD_ALGO_FUSED : SSD_ALGO_STAGED;
     if (a->chunk_states != nullptr) {   // kept chunk states: the tensor-core path's tile format only
         if (!fused) return SSD_ERR_UNSUPPORTED;
         if (((uintptr_t)a->chunk_states) % 16 != 0) return SSD_ERR_MISALIGNED;
@@ -623,6 +634,19 @@ ssd_status ssd_selftest_bounded_wait(void *ws, size_t ws_bytes, int32_t wait_ms,
     if (ws == nullptr || ws_bytes < HDR_WORDS * sizeof(int32_t) || wait_ms < 1 || wait_ms > 2000)
         return SSD_ERR_INVALID_ARGUMENT;
     if (launch_wait_probe(static_cast<int32_t *>(ws), wait_ms, (cudaStream_t)stream) != cudaSuccess) return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+ssd_status ssd_varlen_metadata(const int32_t *cu_seqlens, int64_t nseqs, int64_t seqlen, int64_t chunk_size,
+                               int32_t *seq_idx, int32_t *chunk_begin, int32_t *segments, int32_t *status,
+                               void *stream) {
+    if (cu_seqlens == nullptr || chunk_begin == nullptr || segments == nullptr || status == nullptr)
+        return SSD_ERR_INVALID_ARGUMENT;
+    if (nseqs < 1 || seqlen < 0 || chunk_size < 1) return SSD_ERR_INVALID_ARGUMENT;
+    if (nseqs > (int64_t)1 << 24 || seqlen > (int64_t)1 << 30 || chunk_size > 65536) return SSD_ERR_UNSUPPORTED;
+    if (launch_varlen_metadata(cu_seqlens, (int)nseqs, (int)seqlen, (int)chunk_size, status, chunk_begin, segments,
+                               seq_idx, (cudaStream_t)stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
     return SSD_OK;
 }
 

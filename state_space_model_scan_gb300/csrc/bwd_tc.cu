@@ -159,26 +159,33 @@ __device__ __forceinline__ float block_scan256(float v, float *wsum, float *tota
     return x + off;
 }
 
-// Inclusive block scan of v with the block total (*total), plus the block sum of u
-// (*usum), in one pass; fixed order.  wsum holds 16 floats.
-__device__ __forceinline__ float block_scan_sum(float v, float u, float *wsum, float *total, float *usum) {
+// In one pass over the block (fixed order): *vrev = the sum of v over this position and all
+// later ones (reverse inclusive scan), *uexcl = the sum of u over all earlier positions
+// (exclusive scan).  Both are formed directly, never as a total minus a prefix, so a large
+// term never has to cancel against itself.  wsum holds 16 floats.
+__device__ __forceinline__ void block_rev_excl_scan(float v, float u, float *wsum, float *vrev, float *uexcl) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const float x = warp_incl_sum(v);
-    const float us = warp_sum(u);
-    if (lane == 31) wsum[w] = x;
-    if (lane == 0) wsum[8 + w] = us;
+    float x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_down_sync(0xffffffffu, x, o);
+        if (lane + o < 32) x += t;
+    }
+    const float y = warp_incl_sum(u);
+    float ye = __shfl_up_sync(0xffffffffu, y, 1);
+    if (lane == 0) ye = 0.f;
+    if (lane == 0) wsum[w] = x;          // warp total of v
+    if (lane == 31) wsum[8 + w] = y;     // warp total of u
     __syncthreads();
-    float off = 0.f, tot = 0.f, ut = 0.f;
+    float offv = 0.f, offu = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        if (i < w) off += wsum[i];
-        tot += wsum[i];
-        ut += wsum[8 + i];
+        if (i > w) offv += wsum[i];
+        if (i < w) offu += wsum[8 + i];
     }
-    *total = tot;
-    *usum = ut;
     __syncthreads();
-    return x + off;
+    *vrev = x + offv;
+    *uexcl = ye + offu;
 }
 
 // ------------------------------------------------------------------ dstates
@@ -220,7 +227,7 @@ k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         stage_head(h0);
     }
     auto load_dtv = [&](int h) -> float {
-        return tid < ci.len ? p.dt_raw[(int64_t)ci.b * p.sdb + (int64_t)(ci.t0 + tid) * p.sdl + h] +
+        return (tid >= ci.lo && tid < ci.len) ? p.dt_raw[(int64_t)ci.b * p.sdb + (int64_t)(ci.t0 + tid) * p.sdl + h] +
                                   (p.bias ? p.bias[h] : 0.f)
                             : 0.f;
     };
@@ -237,7 +244,7 @@ k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         const int h = h0 + hi;
         const float vcur = dt_next, Ah = A_next;
         {   // dt and the in-chunk cumulative log-decay (cs2 = cs log2 e); chunk total -> chunk_lam
-            const float dt = tid < ci.len ? softplus_f(vcur) : 0.f;
+            const float dt = (tid >= ci.lo && tid < ci.len) ? softplus_f(vcur) : 0.f;
             float tot;
             const float cs = block_scan256(tid < QT ? dt * Ah : 0.f, wsum, &tot);
             if (tid < QT) {
@@ -252,7 +259,7 @@ k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         {   // (e o dyp) row `row`, half hf -> swizzled [l][p] tile
             float v[32];
             load_row32_swz(sm + DS_OFF_ST + row * 128, row, hf, v);
-            const float el = row < ci.len ? ex2(cs2[row]) : 0.f;
+            const float el = (row >= ci.lo && row < ci.len) ? ex2(cs2[row]) : 0.f;
             if (has_z) {
                 float zz[32];
                 load_row32_swz(sm + DS_OFF_ST + X_BYTES + row * 128, row, hf, zz);
@@ -321,7 +328,7 @@ constexpr uint32_t O_SD = O_WX + X_BYTES;          // dS     [p][n]   16 KB }   
 constexpr uint32_t O_MISC = O_SD + S_BYTES;
 // misc floats
 constexpr int F_ROWT1 = 0, F_ROWXU = 256, F_ROWT2 = 512, F_ROWD = 768, F_COLP = 1024, F_RED = 1536,
-              F_WSUM = 1552, F_PB = 1568, F_TSUM = 1576, F_TAB = 1584, F_END = 3120;
+              F_WSUM = 1552, F_PB = 1568, F_TSUM = 1576, F_TAB = 1584, F_DIAG = 3120, F_END = 3248;
 // Per-head position tables, two sets (the next head's is built while this head runs):
 // T_CS2 cs log2 e, T_DT dt, T_W w = dt exp(cs[Q-1] - cs), T_GD {exp(cs[a] - cs[s]), dt[s]}
 // with a the last position of s's 32-block, T_VR dt_raw + dt_bias.
@@ -456,16 +463,16 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     // dt_raw + bias at position tid - 128 (warps 4..7; 0 past the chunk's end)
     auto load_dtv = [&](const ChunkInfo &c, int h) -> float {
         const int pos = tid - 128;
-        return pos < c.len ? p.dt_raw[(int64_t)c.b * p.sdb + (int64_t)(c.t0 + pos) * p.sdl + h] +
+        return (pos >= c.lo && pos < c.len) ? p.dt_raw[(int64_t)c.b * p.sdb + (int64_t)(c.t0 + pos) * p.sdl + h] +
                                  (p.bias ? p.bias[h] : 0.f)
                            : 0.f;
     };
     // Warps 4..7 (position tid - 128): a head's tables into set `set` (dt, the in-chunk cumulative
     // log-decay by a fixed-order scan over the four warps' partial sums, w, the block factors)
-    auto build_tables = [&](int set, float vraw, float Aval, int clen) {
+    auto build_tables = [&](int set, float vraw, float Aval, int clo, int clen) {
         const int pos = tid - 128, wl = warp - 4;
         float *T = fm + F_TAB + set * TAB_STRIDE;
-        const float dt = pos < clen ? softplus_f(vraw) : 0.f;
+        const float dt = (pos >= clo && pos < clen) ? softplus_f(vraw) : 0.f;
         const float x = warp_incl_sum(dt * Aval);
         if (lane == 31) fm[F_TSUM + wl] = x;
         asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -494,7 +501,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         issue_first(cur);
         A_next = p.A[cur.h0];
         D_next = p.D ? p.D[cur.h0] : 0.f;
-        if (tid >= 128) build_tables(0, load_dtv(cur.ci, cur.h0), A_next, cur.ci.len);
+        if (tid >= 128) build_tables(0, load_dtv(cur.ci, cur.h0), A_next, cur.ci.lo, cur.ci.len);
     }
     __syncthreads();
 
@@ -505,7 +512,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     Item nxt;
     bool have_next = false;
     const int64_t tok = (int64_t)ci.t0 + row;
-    const bool live = row < ci.len;
+    const bool live = row >= ci.lo && row < ci.len;
 
     for (int hi = 0; hi < HS; ++hi) {
         const int h = h0 + hi;
@@ -529,12 +536,12 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         // the next head (this item's, or the first of the item taken at this head's start): its
         // dt (warps 4..7), A and D are read now; warps 4..7 build its tables during group 2
         bool nh_has = false;
-        int nh = 0, nh_len = 0;
+        int nh = 0, nh_lo = 0, nh_len = 0;
         if (hi + 1 < HS) {
-            nh_has = true; nh = h + 1; nh_len = ci.len;
+            nh_has = true; nh = h + 1; nh_lo = ci.lo; nh_len = ci.len;
         } else if (s_item[0] < p.n_items) {
             decode(s_item[0], nxt);
-            nh_has = true; nh = nxt.h0; nh_len = nxt.ci.len;
+            nh_has = true; nh = nxt.h0; nh_lo = nxt.ci.lo; nh_len = nxt.ci.len;
         }
         float v_next = 0.f;
         if (nh_has) {
@@ -636,7 +643,10 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         // ---- M = E dt_s CB and E' = E dt_s dM (bf16) rows; row sums of M o dM; column sums of
         // E CB dM (fixed order).  Blocks of 32 columns below the diagonal take
         // E = exp(cs[l] - cs[a]) exp(cs[a] - cs[s]) (a = the block's last column; both factors
-        // <= 1), the diagonal block exp per element.
+        // <= 1), the diagonal block exp per element.  The diagonal (s = l, E = 1) does not
+        // depend on cs: it stays out of both sums (in exact arithmetic its row and column terms
+        // cancel in dcs; in fp32, with dt large, they would leave rounding of their own size)
+        // and is kept apart for the direct dt term.
         {
             float rowt1 = 0.f;
             const int l = row;
@@ -688,13 +698,17 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         for (int jj = 0; jj < 2; ++jj) {
                             const int s = sb * 32 + i + jj;
                             float m = 0.f, e = 0.f, t = 0.f;
-                            if (s <= l) {
+                            if (s < l) {
                                 const float E = ex2(c2l - cs2[s]);
                                 const float ec = E * cb[i + jj], ed = E * dtc[s];
                                 m = ed * cb[i + jj];
                                 e = ed * dm[i + jj];
                                 t = ec * dm[i + jj];
                                 rowt1 = fmaf(m, dm[i + jj], rowt1);
+                            } else if (s == l) {
+                                m = dtc[s] * cb[i + jj];
+                                e = dtc[s] * dm[i + jj];
+                                fm[F_DIAG + l] = cb[i + jj] * dm[i + jj];
                             }
                             mv[jj] = m;
                             ev[jj] = e;
@@ -729,7 +743,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                           kk > 0);
             umma_commit(&bar[2]);
         }
-        if (nh_has && tid >= 128) build_tables(tb ^ 1, v_next, A_next, nh_len);   // while group 2 runs
+        if (nh_has && tid >= 128) build_tables(tb ^ 1, v_next, A_next, nh_lo, nh_len);   // while group 2 runs
         wait_mma();
         {   // dx = dx_diag + w o u + D dyp; x.u row sums; then e o dyp over the dyp tile
             float dxd[32], u[32], xv[32], dyp[32];
@@ -833,26 +847,27 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 const int sb = i >> 5, jj = i & 31;
                 const int hsel = (sb == 0 || sb == 3) ? 0 : 1;
                 const int bi = (sb == 0 || sb == 1) ? 0 : 1;
-                float colTm = 0.f;   // sum_l (E CB dM)[l][i], rows in quads >= sb, in quad order
+                float colTm = 0.f;   // sum_{l > i} (E CB dM)[l][i], rows in quads >= sb, in quad order
                 for (int q = sb; q < 4; ++q) colTm += fm[F_COLP + (hsel * 4 + q) * 64 + bi * 32 + jj];
                 const float xu = fm[F_ROWXU + i] + fm[F_ROWXU + 128 + i];
                 const float r1 = fm[F_ROWT1 + i] + fm[F_ROWT1 + 128 + i];
                 const float r2 = fm[F_ROWT2 + i] + fm[F_ROWT2 + 128 + i];
                 t4 = wst[i] * xu;
-                ddir = colTm + ex2(cl2 - cs2[i]) * xu;
-                dcs = r1 - dtc[i] * colTm + r2 - t4;
+                ddir = colTm + fm[F_DIAG + i] + ex2(cl2 - cs2[i]) * xu;
+                dcs = r1 - dtc[i] * colTm + r2;
             }
             float T3 = 0.f;
 #pragma unroll
             for (int w = 0; w < 8; ++w) T3 += fm[F_RED + w];
             T3 *= ex2(cl2);
-            // da[u] = sum_{i>=u} dcs[i] + T3 + sum_s T4[s]: one pass gives the scan of dcs and the sum of T4
-            float dtot, t4tot;
-            const float inc = block_scan_sum(dcs, t4, fm + F_WSUM, &dtot, &t4tot);
+            // da[u] = sum_{i>=u} dcs[i] + T3 + sum_{s<u} T4[s]  (T4[s] enters dcs at the chunk's
+            // last position with + and at s with -: their net share of da[u] is the prefix below u)
+            float drev, t4ex;
+            block_rev_excl_scan(dcs, t4, fm + F_WSUM, &drev, &t4ex);
             float pa = 0.f, pb = 0.f, pd = 0.f;
             if (i < QT) {
-                const float da = dtot - inc + dcs + T3 + t4tot;
-                if (i < ci.len) {
+                const float da = drev + T3 + t4ex;
+                if (i >= ci.lo && i < ci.len) {
                     const float gv = (ddir + Ah * da) * sigmoid_f(vrt[i]);
                     p.ddt[(int64_t)ci.b * p.sddb + (int64_t)(ci.t0 + i) * p.sddl + h] = gv;
                     pa = dtc[i] * da;
@@ -984,7 +999,7 @@ k_bwd_finish(const BwdParams p, int tail_blocks) {
     if (p.hdr[HDR_STATUS] != 0 || k >= p.hdr[HDR_NCHUNKS]) return;
     const ChunkInfo ci = p.chunks[k];
     const int l = l0 + (threadIdx.x >> 4), n0 = (threadIdx.x & 15) * 8;
-    if (l >= ci.len) return;
+    if (l < ci.lo || l >= ci.len) return;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < p.nsub_tail; ++j) {
         const float4 *src = reinterpret_cast<const float4 *>(

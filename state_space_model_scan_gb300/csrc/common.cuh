@@ -23,18 +23,34 @@ enum HeaderWord {
     HDR_WORDS = 64
 };
 
-// One sequence: tokens [t0, t0 + len) of batch row b; its chunks start at chunk0.
+// The chunk grid runs over each batch row's token axis: physical chunk c of a row holds
+// tokens [cQ, (c+1)Q).  With packed sequences (cu_seqlens) a chunk may hold parts of
+// several sequences; each part (a segment) is processed as one chunk tile: the Q rows
+// from the chunk's first token, of which rows [lo, len) belong to the segment.  Rows
+// outside get dt := 0 (decay 1, no input) and are never written, which is the
+// sequence mask seq_idx[l] == seq_idx[s] of the intra-chunk matrix.
+
+// One sequence: tokens [t0, t0 + len) of batch row b; its chunk tiles start at chunk0.
 struct SeqInfo {
     int32_t b, t0, len, chunk0;
 };
-// One chunk of one sequence: tokens [t0, t0 + len) of batch row b, len <= Q.
+// Number of chunk tiles of a sequence: the physical chunks its tokens touch.
+__host__ __device__ __forceinline__ int seq_nchunks(int t0, int len, int Q) {
+    return len > 0 ? (t0 + len + Q - 1) / Q - t0 / Q : 0;
+}
+// One chunk tile: the segment of one sequence in the physical chunk starting at token t0
+// of batch row b; rows [lo, len) of the tile belong to it (0 <= lo < len <= Q).
 struct ChunkInfo {
     int32_t seq, b, t0, len;
+    int32_t lo, pad0, pad1, pad2;
 };
-// One work unit of the fused forward: segment j (`nchunk` consecutive chunks) of one sequence.
+// One work unit of the fused forward: segment j (`nchunk` consecutive chunk tiles) of one
+// sequence; t0 = first token of its first tile's physical chunk, rows [lo, len) from t0
+// belong to the sequence (lo > 0 only for a sequence starting inside its first chunk).
 struct UnitInfo {
-    int32_t seq, b, t0, len;          // token range [t0, t0+len) of row b
+    int32_t seq, b, t0, len;          // rows [lo, len) from token t0 of row b
     int32_t nchunk, prev, last, j;    // prev: index of unit (seq, j-1) or -1; last: j is the final segment
+    int32_t lo, pad0, pad1, pad2;
 };
 
 // Shape of one call, as the kernels see it.

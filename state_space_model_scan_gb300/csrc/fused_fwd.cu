@@ -287,7 +287,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int pos = c * QT + 4 * lane + i;
-                if (pos < un.len)
+                if (pos >= un.lo && pos < un.len)
                     cp_async4(dtn + pos, p.dt_raw + (int64_t)un.b * p.sdb + (int64_t)(un.t0 + pos) * p.sdl + hn);
             }
         }
@@ -336,7 +336,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int pos = c * QT + 4 * lane + i;
-                    dt4[r][i] = (wact && pos < ui.len) ? softplus_f(dtn[pos] + bias) : 0.f;
+                    dt4[r][i] = (wact && pos >= ui.lo && pos < ui.len) ? softplus_f(dtn[pos] + bias) : 0.f;
                     run += dt4[r][i] * Ah;
                     loc[i] = run;
                 }
@@ -514,7 +514,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         // ---- phase 2, states-only mode: the carried state entering every chunk, from the chunk
         // states kept in TMEM (no loads, no MMAs)
         if (!full) {
-            const int64_t kfirst = (int64_t)p.seqs[ui.seq].chunk0 + (ui.t0 - p.seqs[ui.seq].t0) / QT;
+            const int64_t kfirst = (int64_t)p.seqs[ui.seq].chunk0 + ui.t0 / QT - p.seqs[ui.seq].t0 / QT;
             for (int c = 0; c < ui.nchunk; ++c) {
                 uint8_t *dst = state_tile_row(p.states_out, kfirst + c, sh.H, h, row);
 #pragma unroll
@@ -538,10 +538,11 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         }
         // ---- phase 2: outputs
         const float Dh = p.D ? p.D[h] : 0.f;
-        const int64_t kfirst = (int64_t)p.seqs[ui.seq].chunk0 + (ui.t0 - p.seqs[ui.seq].t0) / QT;
+        const int64_t kfirst = (int64_t)p.seqs[ui.seq].chunk0 + ui.t0 / QT - p.seqs[ui.seq].t0 / QT;
         for (int c = 0; c < ui.nchunk; ++c) {
             const int tc0 = ui.t0 + c * QT;
             const int clen = min(QT, ui.len - c * QT);
+            const int clo = c == 0 ? ui.lo : 0;   // rows [clo, clen) are this sequence's
             const bool more = c + 1 < ui.nchunk;
             const int64_t tok = (int64_t)tc0 + row;
             const bool has_z = p.z != nullptr;
@@ -673,9 +674,9 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             if (more) load_x(h, tc0 + QT, ui.b);
             if (has_z) wait_bar(BAR_Z);
             // full chunks: y rows go into W (in place of the gate rows just read) and leave as
-            // one TMA store; a ragged chunk stores its rows directly (rows past it may belong
-            // to the next packed sequence)
-            const bool tile_out = clen == QT;
+            // one TMA store; a chunk shared with another packed sequence stores its own rows
+            // directly
+            const bool tile_out = clen == QT && clo == 0;
             {   // epilogue: row l
                 const int l = row;
                 const float el = ex2(cs2[l]);
@@ -687,7 +688,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     tmem_ld32(tmem + lane_base + TM_YD + 32 * half, yd);
                     tmem_ld32(tmem + lane_base + TM_YO + 32 * half, yo);
                     tmem_wait_ld();
-                    if (l < clen) {
+                    if (l >= clo && l < clen) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             uint4 zq = make_uint4(0u, 0u, 0u, 0u);

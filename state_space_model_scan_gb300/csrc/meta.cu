@@ -1,16 +1,18 @@
-// meta.cu -- chunk and work-unit lists for fixed-length batches and packed
-// variable-length sequences (cu_seqlens).
+// meta.cu -- chunk-tile and work-unit lists for fixed-length batches and packed
+// variable-length sequences (cu_seqlens), and the packed-sequence metadata entry
+// point (sequence index of every token, segments of every physical chunk).
 //
-// Each sequence is cut into Q-token chunks from its own first token (the last
-// chunk ragged), so no chunk ever holds two sequences; the carried state is
-// reset to the sequence's initial state at its first chunk.  Chunks are listed
-// sequence by sequence.  Work units of the fused forward group consecutive
-// chunks of one sequence (segment j of the sequence): a sequence of n chunks has
-// m = max(ceil(n / R), min(n, ceil(n * num / den))) segments of floor(n/m) or
-// ceil(n/m) chunks, the larger ones first (the planner raises m above ceil(n/R)
-// so that the units fill whole rounds of the resident CTAs); segments are grouped in
-// blocks of KB.  Units are listed by (block, sequence, segment), so a unit only
-// ever depends on units listed before it and the units of one sequence inside
+// The chunk grid runs over the token axis of each batch row: physical chunk c holds
+// tokens [cQ, (c+1)Q).  With packed sequences a chunk may hold parts of several
+// sequences, so chunk boundaries need not meet sequence starts; each part (segment) is
+// one chunk tile (see ChunkInfo), and the carried state is reset to a sequence's initial
+// state at its first tile.  A sequence's tiles are listed in order, sequences in order.
+// Work units of the fused forward group consecutive tiles of one sequence (segment j of
+// the sequence): a sequence of n tiles has m = max(ceil(n / R), min(n, ceil(n * num /
+// den))) units of floor(n/m) or ceil(n/m) tiles, the larger ones first (the planner
+// raises m above ceil(n/R) so that the units fill whole rounds of the resident CTAs);
+// units are grouped in blocks of KB.  Units are listed by (block, sequence, segment), so
+// a unit only ever depends on units listed before it and the units of one sequence inside
 // one block are consecutive in the list.
 #include <algorithm>
 
@@ -103,7 +105,7 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
             if (cu) { t0 = cu[s]; len = cu[s + 1] - t0; }
             else { b = s; len = L; }
         }
-        int nch = (len + Q - 1) / Q;
+        int nch = seq_nchunks(t0, len, Q);
         int tot;
         int off = block_excl_scan(s < S ? nch : 0, &tot, sm);
         if (s < S) {
@@ -132,7 +134,10 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
         const SeqInfo si = seqs[lo];
         const int j = c - si.chunk0;
         ChunkInfo ci;
-        ci.seq = lo; ci.b = si.b; ci.t0 = si.t0 + j * Q; ci.len = min(Q, si.len - j * Q);
+        ci.seq = lo; ci.b = si.b; ci.t0 = (si.t0 / Q + j) * Q;
+        ci.lo = max(si.t0 - ci.t0, 0);
+        ci.len = min(Q, si.t0 + si.len - ci.t0);
+        ci.pad0 = ci.pad1 = ci.pad2 = 0;
         chunks[c] = ci;
     }
     // pass 3: work units ordered by (block of KB segments, sequence, segment)
@@ -146,7 +151,7 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
                 SeqInfo si;
                 if (s < S) {
                     si = seqs[s];
-                    nch = (si.len + Q - 1) / Q;
+                    nch = seq_nchunks(si.t0, si.len, Q);
                     nseg = seg_count(nch, R, num, den);
                     cnt = max(0, min(KB, nseg - blk * KB));
                 }
@@ -160,12 +165,14 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
                         ui.seq = s; ui.b = si.b;
                         const int base = nch / nseg, rem = nch % nseg;
                         const int c0 = j * base + min(j, rem);
-                        ui.t0 = si.t0 + c0 * Q;
+                        ui.t0 = (si.t0 / Q + c0) * Q;
                         ui.nchunk = base + (j < rem ? 1 : 0);
-                        ui.len = min(ui.nchunk * Q, si.len - c0 * Q);
+                        ui.len = min(ui.nchunk * Q, si.t0 + si.len - ui.t0);
+                        ui.lo = c0 == 0 ? si.t0 - ui.t0 : 0;
                         ui.prev = (j == 0) ? -1 : (i > 0 ? u - 1 : last_unit[s]);
                         ui.last = (j == nseg - 1) ? 1 : 0;
                         ui.j = j;
+                        ui.pad0 = ui.pad1 = ui.pad2 = 0;
                         units[u] = ui;
                         if (i == cnt - 1) last_unit[s] = u;
                     }
@@ -218,6 +225,7 @@ k_build_meta_fixed(int B, int L, int Q, int R, int num, int den, int KB, int kma
         const int s = (int)(c / nch), j = (int)(c % nch);
         ChunkInfo ci;
         ci.seq = s; ci.b = s; ci.t0 = j * Q; ci.len = min(Q, L - j * Q);
+        ci.lo = 0; ci.pad0 = ci.pad1 = ci.pad2 = 0;
         chunks[c] = ci;
     }
     const int base = nseg > 0 ? nch / nseg : 0, rem = nseg > 0 ? nch % nseg : 0;
@@ -236,6 +244,7 @@ k_build_meta_fixed(int B, int L, int Q, int R, int num, int den, int KB, int kma
         ui.prev = j == 0 ? -1 : (i > 0 ? (int)u - 1 : (int)((blk - 1) * B * KB + (int64_t)s * KB + KB - 1));
         ui.last = j == nseg - 1 ? 1 : 0;
         ui.j = j;
+        ui.lo = 0; ui.pad0 = ui.pad1 = ui.pad2 = 0;
         units[u] = ui;
     }
 }
@@ -268,7 +277,89 @@ __global__ void k_wait_probe(int32_t *hdr, uint64_t limit_ns) {
     set_status(hdr, SSD_ERR_DEVICE_TIMEOUT);
 }
 
+// ---------------------------------------------------------------- packed-sequence metadata
+// Largest s in [0, S] with cu[s] <= t (cu validated: cu[0] = 0 <= t, non-decreasing).
+__device__ __forceinline__ int seq_of(const int32_t *cu, int S, int t) {
+    int lo = 0, hi = S;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Walks the segments of physical chunk c (tokens [cQ, min((c+1)Q, L))): the sequence
+// holding the current token runs to min(its end, the chunk's end), then the next token's
+// sequence takes over.  Writes them at seg (when not null); returns their number.
+__device__ int chunk_segments(const int32_t *cu, int S, int L, int Q, int c, int32_t *seg) {
+    const int end = min((c + 1) * Q, L);
+    int a = c * Q, n = 0;
+    while (a < end) {
+        const int s = seq_of(cu, S, a);
+        const int e = min(cu[s + 1], end);
+        if (seg != nullptr) {
+            seg[3 * n] = s;
+            seg[3 * n + 1] = a;
+            seg[3 * n + 2] = e;
+        }
+        ++n;
+        a = e;
+    }
+    return n;
+}
+
+// One block: validates cu (status), then the segment count of every physical chunk, their
+// exclusive scan (chunk_begin) and the segments themselves.
+__global__ void __launch_bounds__(kMetaThreads)
+k_varlen_segments(const int32_t *__restrict__ cu, int S, int L, int Q, int32_t *status, int32_t *chunk_begin,
+                  int32_t *segments) {
+    __shared__ int sm[32];
+    __shared__ int bad;
+    const int tid = threadIdx.x;
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    for (int s = tid; s <= S; s += blockDim.x) {
+        const int c = cu[s];
+        if ((s == 0 && c != 0) || (s == S && c != L) || (s < S && cu[s + 1] < c)) bad = 1;
+    }
+    __syncthreads();
+    if (tid == 0) *status = bad ? SSD_ERR_INVALID_ARGUMENT : SSD_OK;
+    if (bad) return;
+    const int nch = (L + Q - 1) / Q;
+    int carry = 0;
+    for (int base = 0; base < nch; base += blockDim.x) {
+        const int c = base + tid;
+        const int n = c < nch ? chunk_segments(cu, S, L, Q, c, nullptr) : 0;
+        int tot;
+        const int off = block_excl_scan(n, &tot, sm);
+        if (c < nch) {
+            chunk_begin[c] = carry + off;
+            chunk_segments(cu, S, L, Q, c, segments + 3 * (int64_t)(carry + off));
+        }
+        carry += tot;
+    }
+    if (tid == 0) chunk_begin[nch] = carry;
+}
+
+// seq_idx[t] for every token (after k_varlen_segments has validated cu).
+__global__ void k_varlen_seq_idx(const int32_t *__restrict__ cu, int S, int L, const int32_t *status,
+                                 int32_t *seq_idx) {
+    if (*status != SSD_OK) return;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < L; t += (int64_t)gridDim.x * blockDim.x)
+        seq_idx[t] = seq_of(cu, S, (int)t);
+}
+
 }  // namespace
+
+cudaError_t launch_varlen_metadata(const int32_t *cu, int S, int L, int Q, int32_t *status, int32_t *chunk_begin,
+                                   int32_t *segments, int32_t *seq_idx, cudaStream_t st) {
+    k_varlen_segments<<<1, kMetaThreads, 0, st>>>(cu, S, L, Q, status, chunk_begin, segments);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || seq_idx == nullptr || L == 0) return e;
+    const int blocks = (int)std::min<int64_t>(((int64_t)L + 255) / 256, 4096);
+    k_varlen_seq_idx<<<blocks, 256, 0, st>>>(cu, S, L, status, seq_idx);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_wait_probe(int32_t *hdr, int wait_ms, cudaStream_t st) {
     k_wait_probe<<<1, 32, 0, st>>>(hdr, (uint64_t)wait_ms * 1000000ull);

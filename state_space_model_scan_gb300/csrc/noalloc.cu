@@ -10,7 +10,12 @@
 //
 // The array lives in this translation unit's module, so it occupies device
 // memory only on devices where this entry point is used (the module is loaded
-// on first use) and stays allocated until the process exits.
+// on first use) and stays allocated until the process exits.  In host code its
+// name is only a host-side stand-in: the device address is looked up with
+// cudaGetSymbolAddress, with the device current, once per device and context (a
+// context that was torn down and rebuilt, e.g. after cudaDeviceReset, gets a new
+// lookup), and that address is what the kernels receive.
+#include <cuda.h>
 #include <mutex>
 
 #include "common.cuh"
@@ -18,24 +23,58 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;   // SSD_NOALLOC_SCRATCH_BYTES
+constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void *g_addr[64] = {nullptr};   // device address of g_noalloc_scratch, per device ordinal
+typedef CUresult (*PfnCtxGetCurrent)(CUcontext *);
+typedef CUresult (*PfnCtxGetId)(CUcontext, unsigned long long *);
 
-// Device address of the scratch array on the current device (looked up once per
-// device, with that device current).  nullptr on failure.
+struct Slot {
+    void *addr = nullptr;
+    unsigned long long ctx_id = 0;
+};
+std::mutex g_mu;
+Slot g_slot[kMaxDevices];   // per device ordinal: the scratch address and the context it belongs to
+
+// Unique id of the current context (0 if there is none yet or the query is unavailable).
+unsigned long long current_ctx_id() {
+    static PfnCtxGetCurrent get_cur = nullptr;
+    static PfnCtxGetId get_id = nullptr;
+    static bool looked = false;
+    if (!looked) {
+        void *p1 = nullptr, *p2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p1, 4000, cudaEnableDefault, &q1) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PfnCtxGetCurrent>(p1);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q2 == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PfnCtxGetId>(p2);
+        looked = true;
+    }
+    if (get_cur == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_noalloc_scratch on the current device; nullptr on failure (an
+// ordinal beyond kMaxDevices included: the cache has one slot per ordinal).
 void *scratch_address() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_addr[dev] == nullptr) {
+    Slot &sl = g_slot[dev];
+    const unsigned long long id = current_ctx_id();
+    if (sl.addr == nullptr || id == 0 || id != sl.ctx_id) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        g_addr[dev] = ptr;
+        sl.addr = ptr;
+        sl.ctx_id = current_ctx_id();   // the lookup made the device's context current
     }
-    return g_addr[dev];
+    return sl.addr;
 }
 
 }  // namespace
@@ -48,4 +87,10 @@ extern "C" ssd_status ssd_fwd_noalloc(const ssd_problem *prob, const ssd_fwd_arg
     void *ws = scratch_address();
     if (ws == nullptr) return SSD_ERR_CUDA;
     return ssd_fwd(prob, args, ws, kNoAllocScratchBytes, stream);
+}
+
+extern "C" ssd_status ssd_noalloc_query_status(void *stream) {
+    void *ws = scratch_address();
+    if (ws == nullptr) return SSD_ERR_CUDA;
+    return ssd_query_status(ws, stream);
 }

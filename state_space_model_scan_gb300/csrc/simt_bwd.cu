@@ -14,9 +14,13 @@
 //       dB[s]   = sum_l E dt_s dM[l][s] C[l]      + w_s x[s]^T dS_out
 //       dC[l]   = sum_s E dt_s dM[l][s] B[s]      + exp(cs[l]) dyp[l]^T S_in
 //       ddt[s] (direct) = sum_l E CB dM[l][s]     + exp(cs[Q-1]-cs[s]) x[s].u[s]
-//       dcs[i]  = sum_s T1[i][s] - sum_l T1[l][i] + T2[i] - T4[i] + [i = Q-1](T3 + sum_s T4[s])
+//       dcs[i]  = sum_{s<i} T1[i][s] - sum_{l>i} T1[l][i] + T2[i] - T4[i] + [i = Q-1](T3 + sum_s T4[s])
 //         T1 = M o dM, T2[l] = dyp[l].Y_off[l], T4[s] = w_s x[s].u[s], T3 = exp(cs[Q-1]) <S_in, dS_out>
-//       da[u] = sum_{i>=u} dcs[i];  ddt = ddt_direct + A da;  dA += sum dt da
+//         (the diagonal s = l of T1 does not depend on cs: its row and column terms cancel exactly
+//         and are left out of both sums)
+//       da[u] = sum_{i>=u} dcs[i] = sum_{i>=u} (dcs[i] without T4) + T3 + sum_{s<u} T4[s], formed
+//         that way (a reverse scan and a forward exclusive scan), so no large term cancels against
+//         itself;  ddt = ddt_direct + A da;  dA += sum dt da
 //       ddt_raw = ddt * sigmoid(dt_raw + dt_bias);  dz = dy ypre silu'(z)
 //   reductions       : dB/dC over the heads of a group, dA/dD/ddt_bias over chunks, in a
 //                      fixed order (bitwise reproducible; no atomics).
@@ -63,7 +67,7 @@ k_bwd_dstates(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__rest
         for (int i = tid; i < LT * P; i += 256) {
             int r = i / P, c = i % P, l = l0 + r;
             float v = 0.f;
-            if (l < ci.len) {
+            if (l >= ci.lo && l < ci.len) {
                 int64_t tok = ci.t0 + l;
                 v = to_f(dyb[tok * dy.s1 + c]);
                 if (zb) { float zz = to_f(zb[tok * z.s1 + c]); v *= zz * sigmoid_f(zz); }
@@ -73,7 +77,7 @@ k_bwd_dstates(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__rest
         }
         for (int i = tid; i < LT * N; i += 256) {
             int r = i / N, c = i % N, l = l0 + r;
-            cs_[r][c] = (l < ci.len) ? to_f(cb[(int64_t)(ci.t0 + l) * Cm.s1 + c]) : 0.f;
+            cs_[r][c] = (l >= ci.lo && l < ci.len) ? to_f(cb[(int64_t)(ci.t0 + l) * Cm.s1 + c]) : 0.f;
         }
         __syncthreads();
 #pragma unroll 4
@@ -134,7 +138,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     for (int i = tid; i < QS * P; i += 256) {
         int r = i / P, c = i % P;
         float xv = 0.f, dv = 0.f;
-        if (r < ci.len) {
+        if (r >= ci.lo && r < ci.len) {
             int64_t tok = ci.t0 + r;
             xv = to_f(xb[tok * x.s1 + c]);
             dv = to_f(dyb[tok * dy.s1 + c]);
@@ -145,7 +149,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     }
     for (int i = tid; i < QS * N; i += 256) {
         int r = i / N, c = i % N;
-        bool in = r < ci.len;
+        bool in = r >= ci.lo && r < ci.len;
         Bs[r * N1 + c] = in ? to_f(bb[(int64_t)(ci.t0 + r) * Bm.s1 + c]) : 0.f;
         Cs[r * N1 + c] = in ? to_f(cb[(int64_t)(ci.t0 + r) * Cm.s1 + c]) : 0.f;
     }
@@ -169,7 +173,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     const float *dso = dstates + ((int64_t)k * sh.H + h) * P * N;
     const float *sin = states + ((int64_t)k * sh.H + h) * P * N;
     const float Dh = D ? D[h] : 0.f;
-    const bool live = r < ci.len;
+    const bool live = r >= ci.lo && r < ci.len;
     const int64_t tok = (int64_t)ci.t0 + r;
     // dx[r][p] and x.u row sums
     {
@@ -252,24 +256,17 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
         for (int w = 0; w < 8; ++w) T3 += red[w];
         T3 *= expf(clast);
         float dcs[2], t4[2], ddir[2];
-        float t4sum_part = 0.f;
         for (int q = 0; q < 2; ++q) {
             const int i = tid + 32 * q;
-            float rowT1 = 0.f, colT1 = 0.f, colTm = 0.f;
-            for (int s = 0; s <= i; ++s) rowT1 += dt[s] * Tm[i * Q1 + s];
-            for (int l = i; l < QS; ++l) { colTm += Tm[l * Q1 + i]; }
-            colT1 = dt[i] * colTm;
+            float rowT1 = 0.f, colTm = 0.f;
+            for (int s = 0; s < i; ++s) rowT1 += dt[s] * Tm[i * Q1 + s];
+            for (int l = i + 1; l < QS; ++l) colTm += Tm[l * Q1 + i];
             t4[q] = wst[i] * rowXU[i];
-            ddir[q] = colTm + expf(clast - cs[i]) * rowXU[i];
-            dcs[q] = rowT1 - colT1 + rowT2[i] - t4[q];
-            t4sum_part += t4[q];
+            ddir[q] = colTm + Tm[i * Q1 + i] + expf(clast - cs[i]) * rowXU[i];
+            dcs[q] = rowT1 - dt[i] * colTm + rowT2[i];
         }
-        const float t4sum = warp_sum(t4sum_part);
-        if (tid == 31) dcs[1] += T3 + t4sum;        // position QS-1
-        // da[u] = sum_{i >= u} dcs[i]: reverse inclusive scan over 64 positions
-        float hi = dcs[1], lo = dcs[0];
-        // suffix sums within each half via reversed warp scan
-        float hs = hi, ls = lo;
+        // sum_{i >= u} dcs[i]: reverse inclusive scans within each half of the 64 positions
+        float hs = dcs[1], ls = dcs[0];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             float th = __shfl_down_sync(0xffffffffu, hs, o);
@@ -277,12 +274,23 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
             if (tid + o < 32) { hs += th; ls += tl; }
         }
         const float hi_total = __shfl_sync(0xffffffffu, hs, 0);
-        const float da[2] = {ls + hi_total, hs};
+        // sum_{s < u} T4[s]: exclusive forward scans within each half
+        float p0 = t4[0], p1 = t4[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            float t0 = __shfl_up_sync(0xffffffffu, p0, o);
+            float t1 = __shfl_up_sync(0xffffffffu, p1, o);
+            if (tid >= o) { p0 += t0; p1 += t1; }
+        }
+        const float lo_total = __shfl_sync(0xffffffffu, p0, 31);
+        float e0 = __shfl_up_sync(0xffffffffu, p0, 1), e1 = __shfl_up_sync(0xffffffffu, p1, 1);
+        if (tid == 0) { e0 = 0.f; e1 = 0.f; }
+        const float da[2] = {ls + hi_total + T3 + e0, hs + T3 + lo_total + e1};
         const float Ah = A[h];
         float pa = 0.f, pb = 0.f;
         for (int q = 0; q < 2; ++q) {
             const int i = tid + 32 * q;
-            if (i < ci.len) {
+            if (i >= ci.lo && i < ci.len) {
                 const float v = dt_raw[(int64_t)ci.b * sdb + (int64_t)(ci.t0 + i) * sdl + h] + (bias ? bias[h] : 0.f);
                 const float g_ = (ddir[q] + Ah * da[q]) * sigmoid_f(v);
                 ddt[(int64_t)ci.b * sddb + (int64_t)(ci.t0 + i) * sddl + h] = g_;
@@ -319,6 +327,7 @@ __global__ void k_reduce_group(Shape sh, const int32_t *__restrict__ hdr, const 
     const int rows = min(16, ci.len - l0);
     for (int i = threadIdx.x; i < rows * N; i += blockDim.x) {
         const int l = l0 + i / N, n = i % N;
+        if (l < ci.lo) continue;   // rows of another sequence sharing the chunk
         float a = 0.f;
         const float *s = src + (((int64_t)k * sh.H + (int64_t)g * sh.hpg) * sh.Q + l) * N + n;
         for (int j = 0; j < sh.hpg; ++j) a += s[(int64_t)j * sh.Q * N];

@@ -13,7 +13,8 @@
 //                          + exp(cs[l]) C_l . S_in + D x) * silu(z)
 //                      ("Readout, real cast, slice-back": Y_diag + Y_off)
 // Arithmetic is fp32 throughout (fp32 inputs are never rounded to tf32/bf16).
-// Positions past a chunk's length get dt := 0 (decay 1, no input).
+// Rows of a chunk tile outside its segment [lo, len) get dt := 0 (decay 1, no input) and
+// are not written.
 #include "common.cuh"
 
 namespace ssd {
@@ -31,7 +32,7 @@ __global__ void k_chunk_cumsum(Shape sh, const int32_t *__restrict__ hdr, const 
     if (k >= hdr[HDR_NCHUNKS]) return;
     const ChunkInfo ci = chunks[k];
     float dt = 0.f;
-    if (l < ci.len) {
+    if (l >= ci.lo && l < ci.len) {
         float v = dt_raw[(int64_t)ci.b * sdb + (int64_t)(ci.t0 + l) * sdl + h] + (bias ? bias[h] : 0.f);
         dt = softplus_f(v);
     }
@@ -126,7 +127,7 @@ k_state_passing(Shape sh, const int32_t *__restrict__ hdr, const SeqInfo *__rest
     const int e = (blockIdx.y * 256 + threadIdx.x) * 4, lane = threadIdx.x & 31;
     if ((blockIdx.y * 256 + (threadIdx.x & ~31)) * 4 >= PN) return;   // whole warp past the end
     const SeqInfo si = seqs[s];
-    const int nch = (si.len + sh.Q - 1) / sh.Q;
+    const int nch = seq_nchunks(si.t0, si.len, sh.Q);
     const int64_t sbase = ((int64_t)s * sh.H + h) * PN;
     const bool act = e < PN;
     float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -239,7 +240,7 @@ k_chunk_scan(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restr
     for (int j = 0; j < 16; ++j) {
         if (j >= J) continue;
         const int r = lr + pr * j, l = r0 + r;
-        if (l >= ci.len) continue;
+        if (l < ci.lo || l >= ci.len) continue;
         float yo = 0.f;
         for (int n = 0; n < N; ++n) yo += Cs[r * (N + 1) + n] * sin[n];
         const int64_t tok = (int64_t)(ci.t0 + l);

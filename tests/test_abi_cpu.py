@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.abi_version() == 3
+    assert lib.abi_version() == 4
     for code, name in lib.STATUS_NAMES.items():
         assert lib.status_string(code) == name
     assert lib.status_string(99) == "SSD_ERR_UNKNOWN"
@@ -113,6 +113,52 @@ def test_validation_codes(lib, mutate, code):
     rc2 = m.load().ssd_fwd(ctypes.byref(p), ctypes.byref(a), ctypes.c_void_p(0x100000), ctypes.c_size_t(1 << 40),
                            None)
     assert rc2 == code
+
+
+@pytest.mark.parametrize("P,N,bf16,Q,algo,aligned,code,qi", [
+    (16, 16, True, 64, "auto", True, 0, 64),        # SIMT computes 64-token chunks
+    (16, 16, True, 128, "auto", True, 2, None),     # ... and nothing else
+    (16, 16, False, 32, "auto", True, 2, None),
+    (64, 128, True, 128, "auto", True, 0, 128),     # tensor-core tile set: 128-token chunks
+    (64, 128, True, 64, "auto", True, 0, 64),       # same shape at 64: the SIMT path, honoured
+    (64, 128, True, 256, "auto", True, 2, None),    # not computed by either path: no silent re-chunking
+    (64, 128, True, 128, "fused", True, 0, 128),
+    (64, 128, True, 64, "fused", True, 2, None),
+    (64, 128, True, 128, "staged", True, 2, None),
+    (64, 128, True, 128, "auto", False, 3, None),   # tensor-core chunk length, strides break the TMA rule
+    (64, 128, False, 128, "auto", True, 2, None),   # fp32 inputs run SIMT only
+])
+def test_chunk_size_is_honoured(lib, P, N, bf16, Q, algo, aligned, code, qi):
+    """Each chunk_size outcome: the path that computes exactly that chunk length, or
+    SSD_ERR_UNSUPPORTED / SSD_ERR_MISALIGNED; the debug layout reports the chunk used."""
+    m = lib_mod()
+    p, a = good_case(P=P, N=N, bf16=bf16)
+    p.chunk_size = Q
+    p.algo = m.ALGO[algo]
+    if not aligned:
+        a.x.stride[2] = P + 4
+        a.x.stride[1] = 4 * (P + 4)
+    rc, _ = ws_size(p, a)
+    assert rc == code
+    if code == 0:
+        lay = m.DebugLayout()
+        assert m.load().ssd_fwd_debug_layout(ctypes.byref(p), ctypes.byref(a), ctypes.byref(lay)) == 0
+        assert lay.qi == qi
+
+
+def test_varlen_metadata_validates_on_host(lib):
+    """Argument checks of ssd_varlen_metadata happen before any launch."""
+    m = lib_mod().load()
+    d = ctypes.c_void_p(0x100000)
+    assert m.ssd_varlen_metadata(None, 2, 10, 4, d, d, d, d, None) == 1
+    assert m.ssd_varlen_metadata(d, 2, 10, 4, d, None, d, d, None) == 1
+    assert m.ssd_varlen_metadata(d, 2, 10, 4, d, d, None, d, None) == 1
+    assert m.ssd_varlen_metadata(d, 2, 10, 4, d, d, d, None, None) == 1
+    assert m.ssd_varlen_metadata(d, 0, 10, 4, d, d, d, d, None) == 1
+    assert m.ssd_varlen_metadata(d, 2, -1, 4, d, d, d, d, None) == 1
+    assert m.ssd_varlen_metadata(d, 2, 10, 0, d, d, d, d, None) == 1
+    assert m.ssd_varlen_metadata(d, 2, 10, 1 << 17, d, d, d, d, None) == 2
+    assert m.ssd_varlen_metadata(d, (1 << 24) + 1, 10, 4, d, d, d, d, None) == 2
 
 
 def test_workspace_checks(lib):
@@ -197,6 +243,7 @@ def _tc_case(Bsz=2, L=1000, H=8, G=2, cu=None):
     """A problem on the tensor-core path (bf16, headdim 64, dstate 128), fake 16-byte-aligned pointers."""
     m = lib_mod()
     p, a = good_case(Bsz=Bsz, L=L, H=H, P=64, G=G, N=128)
+    p.chunk_size = 128
     if cu is not None:
         p.batch = 1
         p.nseqs = cu

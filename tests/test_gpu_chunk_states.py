@@ -33,27 +33,32 @@ def decode_tiles(buf, n_tiles):
 
 
 def oracle_chunk_states(w, inp):
-    """{(global chunk index, head): state entering the chunk}, from prefix runs of the oracle."""
-    from oracle import sequential
+    """{(tile index, head): state entering the tile}, from prefix runs of the oracle.  The tiles
+    are the segments of the chunk grid (oracle.varlen_meta), listed sequence by sequence; the
+    state entering a tile is the final state of its sequence's prefix that ends where the tile's
+    rows of that sequence begin."""
+    from oracle import sequential, varlen_meta
     o = I.to_oracle(inp, w)
-    cu = o["cu"]
+    cu = [int(c) for c in o["cu"]]
     H, P, N = w.nheads, w.headdim, w.dstate
-    out, k = {}, 0
-    for s in range(len(cu) - 1):
-        t0, n = int(cu[s]), int(cu[s + 1] - cu[s])
+    if inp["cu_seqlens"] is not None:
+        tiles = [(s, a) for (s, a, _) in varlen_meta.segments(cu, Q)[0]]
+    else:
+        tiles = [(b, cu[b] + c * Q) for b in range(w.batch) for c in range(-(-w.seqlen // Q))]
+    out = {}
+    for k, (s, a) in enumerate(tiles):
+        t0 = cu[s]
         init = o["init"][s] if o["init"] is not None else np.zeros((H, P, N))
-        for c in range(-(-n // Q)):
-            if c == 0:
-                st = init
-            else:
-                sl = slice(t0, t0 + c * Q)
-                _, fin = sequential.forward(o["x"][sl], o["dt_raw"][sl], o["A"], o["B"][sl], o["C"][sl], D=o["D"],
-                                            z=None if o["z"] is None else o["z"][sl], dt_bias=o["dt_bias"],
-                                            init=init[None], cu=np.array([0, c * Q]))
-                st = fin[0]
-            for h in range(H):
-                out[(k, h)] = st[h]
-            k += 1
+        if a == t0:
+            st = init
+        else:
+            sl = slice(t0, a)
+            _, fin = sequential.forward(o["x"][sl], o["dt_raw"][sl], o["A"], o["B"][sl], o["C"][sl], D=o["D"],
+                                        z=None if o["z"] is None else o["z"][sl], dt_bias=o["dt_bias"],
+                                        init=init[None], cu=np.array([0, a - t0]))
+            st = fin[0]
+        for h in range(H):
+            out[(k, h)] = st[h]
     return out
 
 

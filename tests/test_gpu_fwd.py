@@ -19,8 +19,20 @@ ALGOS = ["staged"]
 BF16_ALGOS = ["staged", "fused"]
 
 
-def W(name="t", B=1, L=256, H=4, P=16, G=1, N=16, Q=64, dtype="f32", **kw):
+def W(name="t", B=1, L=256, H=4, P=16, G=1, N=16, Q=None, dtype="f32", **kw):
+    """A workload; the chunk length defaults to the one its path computes (128 for the
+    tensor-core tile set, 64 for SIMT)."""
+    if Q is None:
+        Q = 128 if (dtype == "bf16" and P == 64 and N == 128) else 64
     return I.Workload(name, B, L, H, P, G, N, Q, dtype, **kw)
+
+
+def for_algo(case, algo):
+    """The SIMT path computes 64-token chunks: a staged run of a tensor-core case uses 64."""
+    case = dict(case)
+    if algo == "staged":
+        case["Q"] = 64
+    return case
 
 
 def check_fwd(w, algo="auto", heads=None, tol=None, **kw):
@@ -48,7 +60,7 @@ def test_tiny_fp32_workload(algo):
 
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("case", [
-    dict(L=1), dict(L=63), dict(L=65), dict(L=200, Q=16), dict(L=300, Q=256),
+    dict(L=1), dict(L=63), dict(L=65), dict(L=200), dict(L=300),
     dict(B=3, L=130, H=6, G=2),                    # 3 heads per group, ragged tail
     dict(H=6, G=3, P=32, N=64, has_z=True),
     dict(P=128, N=128, L=150, H=2),                # largest compiled tile
@@ -68,7 +80,18 @@ def test_fp32_cases(algo, case):
     dict(B=3, L=129, H=3, P=64, G=3, N=128, Q=128, has_D=False, has_dt_bias=False),
 ])
 def test_bf16_cases(algo, case):
-    check_fwd(W(dtype="bf16", **case), algo=algo)
+    check_fwd(W(dtype="bf16", **for_algo(case, algo)), algo=algo)
+
+
+@pytest.mark.parametrize("Q", [16, 32, 256])
+def test_chunk_lengths_no_path_computes_are_refused(Q):
+    """No silent re-chunking: a chunk length that neither path computes is refused."""
+    for dtype, P, N in (("f32", 16, 16), ("bf16", 64, 128)):
+        w = W(L=300, P=P, N=N, Q=Q, dtype=dtype)
+        inp = I.make_inputs(w)
+        with pytest.raises(_lib.SSDError) as e:
+            gpu_forward(w, inp)
+        assert e.value.code == 2
 
 
 @pytest.mark.parametrize("seg", [1, 2, 3, 4, 5])
@@ -83,7 +106,7 @@ def test_fused_matches_staged_closely():
     w = W(L=700, H=4, P=64, G=1, N=128, Q=128, dtype="bf16", has_z=True, has_init=True)
     inp = I.make_inputs(w)
     y1, f1 = gpu_forward(w, inp, algo="fused")
-    y2, f2 = gpu_forward(w, inp, algo="staged")
+    y2, f2 = gpu_forward(dataclasses.replace(w, chunk_size=64), inp, algo="staged")
     assert rel_l2(y1.double().cpu(), y2.double().cpu()) < 1e-2
     assert rel_l2(f1.double().cpu(), f2.double().cpu()) < 1e-2
 
@@ -172,9 +195,10 @@ def test_strided_views_of_packed_buffer(P, N, dtype):
     assert not xs.is_contiguous()
     d = to_dev(inp)
     from state_space_model_scan_gb300.api import ssd_forward
-    y1, f1 = ssd_forward(xs, d["dt_raw"], d["A"], Bs, Cs, D=d["D"], z=d["z"], dt_bias=d["dt_bias"], chunk_size=64)
+    y1, f1 = ssd_forward(xs, d["dt_raw"], d["A"], Bs, Cs, D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                         chunk_size=w.chunk_size)
     y2, f2 = ssd_forward(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
-                         chunk_size=64)
+                         chunk_size=w.chunk_size)
     assert torch.equal(y1, y2) and torch.equal(f1, f2)
 
 
@@ -189,7 +213,7 @@ def test_deterministic_and_every_output_written(P, N):
         y = torch.full_like(d["x"], float("nan"))
         f = torch.full((1, 4, P, N), float("nan"), device="cuda")
         ssd_forward(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
-                    initial_states=d["initial_states"], chunk_size=64, y=y, final_states=f, seg_chunks=1)
+                    initial_states=d["initial_states"], chunk_size=w.chunk_size, y=y, final_states=f, seg_chunks=1)
         torch.cuda.synchronize()
         assert torch.isfinite(y.float()).all() and torch.isfinite(f).all()
         outs.append((y, f))
