@@ -1,16 +1,22 @@
 """Benchmark of the SSD scan hot path on GB300.
 
-One step, on the Nemotron-Nano-shaped workload (batch 1, L=8192, 64 heads x 64,
-8 groups, dstate 128, chunk 128, z gate and D skip, bf16 x/B/C/z, fp32
-dt/A/D/states), each call replayed from a CUDA graph:
-  L2 flush (256 MB write), inference forward (metadata + fused tensor-core forward),
-  L2 flush, training step = forward that also keeps the carried chunk states +
-  backward that reads them (no states recompute).
-`value` is inference-forward tokens/s from CUDA events around that forward;
-`ms_per_step` is the training step's device time (forward + backward); `e2e` is
-forward tokens/s with every step's inputs copied from pinned host memory and its y
-copied back inside the timed region, two independent steps in flight (copy-in,
-compute and copy-out streams).  Prints ONE JSON line.
+One step, each call replayed from a CUDA graph with the L2 flushed (256 MB write)
+before it:
+  * the Nemotron-Nano-shaped workload (batch 1, L=8192, 64 heads x 64, 8 groups,
+    dstate 128, chunk 128, z gate and D skip, bf16 x/B/C/z, fp32 dt/A/D/states):
+    inference forward (metadata + fused tensor-core forward), then a training step =
+    forward that also keeps the carried chunk states + backward that reads them;
+  * the other forward workloads, one forward each: the long-sequence sweep (128 heads
+    x 64, 1 group, dstate 128, initial states, L = 1k .. 32k) and the packed varlen
+    workload (16 sequences of U{512..8192} tokens, 80 heads x 64, own initial states).
+`value` is the inference forward's tokens/s at the Nemotron-Nano shape (median over
+the steps of its CUDA-event time); `ms_per_step` is the training step's median device
+time (forward + backward); `sweep` holds the other workloads' median forward times,
+tokens/s and HBM roofline fractions; `e2e` is forward tokens/s with every step's inputs
+copied from pinned host memory and its y copied back inside the timed region, two
+independent steps in flight (copy-in, compute and copy-out streams).  Clocks and
+throttle reasons are sampled through NVML every millisecond during the timed steps.
+Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -139,6 +145,82 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class NvmlSampler:
+    """Clock, power and throttle-reason samples of one GPU through NVML (ctypes), every
+    `interval` seconds on a background thread; None from start() when NVML is absent."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid, interval=0.001):
+        import ctypes
+        self.ct = ctypes
+        self.interval = interval
+        self.samples = []
+        self.stop = threading.Event()
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        if lib.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for " + key)
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))   # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+
+    def _run(self):
+        ct, lib = self.ct, self.lib
+        clk, pw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        while not self.stop.is_set():
+            a = lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk))
+            b = lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+            c = self.reasons_fn(self.h, ct.byref(rs))
+            if a == 0 and c == 0:
+                self.samples.append((float(clk.value), pw.value / 1000.0 if b == 0 else None, int(rs.value)))
+            time.sleep(self.interval)
+
+    def __enter__(self):
+        self.t = threading.Thread(target=self._run, daemon=True)
+        self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self.stop.set()
+        self.t.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"], "source": "nvml"}
+        sm = sorted(v[0] for v in self.samples)
+        pw = sorted(v[1] for v in self.samples if v[1] is not None)
+        reasons = set()
+        for _, _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(sm), "sm_mhz_min": sm[0], "power_w_median": pw[len(pw) // 2] if pw else None,
+                "source": "nvml, 1 ms"}
+
+
+def clock_sampler(dev_index):
+    """NVML sampler of the CUDA device (by UUID), else the nvidia-smi one."""
+    import torch
+    try:
+        return NvmlSampler(str(torch.cuda.get_device_properties(dev_index).uuid))
+    except (OSError, AttributeError, TypeError):
+        return ClockSampler(dev_index)
+
+
+def median(v):
+    v = sorted(v)
+    n = len(v)
+    return v[n // 2] if n % 2 else 0.5 * (v[n // 2 - 1] + v[n // 2])
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -234,6 +316,12 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def sweep_bytes(w):
+    """Algorithmic HBM bytes of one forward of workload w (inputs read once, y and the
+    states written once, initial states read once)."""
+    return algorithmic_bytes(w, fwd=True)
+
+
 def run_gpu(args):
     import torch
     world, rank, local = dist_env()
@@ -244,7 +332,6 @@ def run_gpu(args):
     dev = torch.device("cuda", torch.cuda.current_device() if world == 1 else local)
     from state_space_model_scan_gb300 import inputs as I
     from state_space_model_scan_gb300 import _lib
-    from state_space_model_scan_gb300.api import Workspace
     w = I.named(WORKLOAD)
     inp = I.make_inputs(w, with_grad_inputs=True)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
@@ -288,7 +375,31 @@ def run_gpu(args):
     # (tail pairs' dB/dC, per-head dA/dD/ddt_bias) (the ncu launch list in profiles/ shows the same set)
     launches_fwd, launches_bwd = 2, 5
 
-    def step(ev=None):
+    # the other forward workloads: the long-sequence sweep and the packed varlen batch
+    sweep = []
+    if not args.no_sweep:
+        for sw in [I.named("long_seq", L=n) for n in (1024, 2048, 4096, 8192, 16384, 32768)] + [I.named("varlen")]:
+            si = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in I.make_inputs(sw).items()}
+            S = sw.nseqs
+            sy = torch.empty_like(si["x"])
+            sfin = torch.empty(S, sw.nheads, sw.headdim, sw.dstate, device=dev)
+            sprob = _lib.problem(sw.batch, sw.seqlen, sw.nheads, sw.headdim, sw.ngroups, sw.dstate, sw.chunk_size,
+                                 S if si["cu_seqlens"] is not None else 0)
+            sargs = _lib.fwd_args(si["x"], si["dt_raw"], si["A"], si["B"], si["C"], sy, D=si["D"], z=si["z"],
+                                  dt_bias=si["dt_bias"], initial_states=si["initial_states"], final_states=sfin,
+                                  cu_seqlens=si["cu_seqlens"])
+            sws = torch.empty(_lib.fwd_workspace_size(sprob, sargs), dtype=torch.uint8, device=dev)
+            with torch.cuda.stream(s):
+                _lib.check(_lib.ssd_fwd(sprob, sargs, sws, s), "ssd_fwd")
+            s.synchronize()
+            sg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(sg, stream=s):
+                _lib.check(_lib.ssd_fwd(sprob, sargs, sws, torch.cuda.current_stream()), "ssd_fwd")
+            # metadata + fused forward, + the empty-sequence final states of a packed batch
+            sweep.append(dict(w=sw, graph=sg, keep=(si, sy, sfin, sws, sargs),
+                              launches=3 if si["cu_seqlens"] is not None else 2))
+
+    def step(ev=None, sev=None):
         with torch.cuda.stream(s):
             flush.fill_(float(rank + 1))
             if ev is not None:
@@ -305,32 +416,41 @@ def run_gpu(args):
             gb.replay()                    # ... and the backward
             if ev is not None:
                 ev[4].record(s)
+            for j, c in enumerate(sweep):  # the other forward workloads
+                flush.fill_(float(rank + 3 + j))
+                if sev is not None:
+                    sev[j][0].record(s)
+                c["graph"].replay()
+                if sev is not None:
+                    sev[j][1].record(s)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sevs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in sweep] for _ in range(args.steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+    with clock_sampler(dev.index if dev.index is not None else 0) as clk:
         wall0 = time.perf_counter()
         for i in range(args.steps):
-            step(evs[i])
+            step(evs[i], sevs[i])
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    fwdt_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    bwd_ms = [e[3].elapsed_time(e[4]) for e in evs]
-    fwd_mean = sum(fwd_ms) / len(fwd_ms)
-    fwdt_mean = sum(fwdt_ms) / len(fwdt_ms)
-    step_mean = sum(f + b for f, b in zip(fwdt_ms, bwd_ms)) / len(fwdt_ms)
-    fwd_mean, fwdt_mean, step_mean = max_over_ranks([fwd_mean, fwdt_mean, step_mean], device=dev)
+    fwd_ms = median([e[0].elapsed_time(e[1]) for e in evs])
+    fwdt_ms = median([e[2].elapsed_time(e[3]) for e in evs])
+    bwd_ms = median([e[3].elapsed_time(e[4]) for e in evs])
+    step_ms = median([e[2].elapsed_time(e[4]) for e in evs])
+    sweep_ms = [median([sevs[i][j][0].elapsed_time(sevs[i][j][1]) for i in range(args.steps)])
+                for j in range(len(sweep))]
+    red = max_over_ranks([fwd_ms, fwdt_ms, bwd_ms, step_ms] + sweep_ms, device=dev)
+    fwd_ms, fwdt_ms, bwd_ms, step_ms, sweep_ms = red[0], red[1], red[2], red[3], red[4:]
     toks = w.batch * w.seqlen
-    value = world * toks / (fwd_mean * 1e-3)
+    value = world * toks / (fwd_ms * 1e-3)
 
     # End to end through the C ABI with host buffers: every step copies its own inputs from
     # pinned host memory, runs ssd_fwd and copies its y back.  Steps are independent, so two are
@@ -395,30 +515,41 @@ def run_gpu(args):
         return
     peak, peak_kind = measured_peaks()
     alg = algorithmic_bytes(w, fwd=True)
-    achieved = alg / (fwd_mean * 1e-3) / 1e9
+    achieved = alg / (fwd_ms * 1e-3) / 1e9
     traffic = profile_traffic(os.path.join(ROOT, "state_space_model_scan_gb300", "csrc", "fused_fwd.cu"))
+    sweep_out = []
+    for c, ms in zip(sweep, sweep_ms):
+        sw = c["w"]
+        b = sweep_bytes(sw)
+        sweep_out.append({"workload": sw.name, "seqlen": sw.seqlen, "nseqs": sw.nseqs, "nheads": sw.nheads,
+                          "chunk_size": sw.chunk_size, "fwd_ms": ms, "tokens_per_s": sw.batch * sw.seqlen / (ms * 1e-3),
+                          "algorithmic_bytes": b, "achieved_gbs": b / (ms * 1e-3) / 1e9,
+                          "roofline_frac": b / (ms * 1e-3) / 1e9 / peak})
+    n_launch_step = 2 * launches_fwd + launches_bwd + sum(c["launches"] for c in sweep)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_mean, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "global_batch": w.batch * world, "seq_len": w.seqlen,
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "flushed before every step (256 MB write)", "timing": "CUDA graph replay, CUDA events"},
-        "fwd_ms": fwd_mean, "fwd_bwd_ms": step_mean, "fwd_train_ms": fwdt_mean, "bwd_ms": step_mean - fwdt_mean,
+                   "chunk_size": w.chunk_size, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed before every timed call (256 MB write)",
+                   "timing": "CUDA graph replay, CUDA events, median over the steps"},
+        "fwd_ms": fwd_ms, "fwd_bwd_ms": step_ms, "fwd_train_ms": fwdt_ms, "bwd_ms": bwd_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "ssd_fwd (metadata + fused tensor-core forward)",
                      "algorithmic_bytes_per_launch": alg, "peak_source": peak_kind},
-        "bwd_roofline": {"bound": "hbm", "achieved": algorithmic_bytes(w, fwd=False) / ((step_mean - fwdt_mean) * 1e-3)
-                         / 1e9, "peak": peak, "unit": "GB/s",
+        "bwd_roofline": {"bound": "hbm", "achieved": algorithmic_bytes(w, fwd=False) / (bwd_ms * 1e-3) / 1e9,
+                         "peak": peak, "unit": "GB/s",
+                         "frac": algorithmic_bytes(w, fwd=False) / (bwd_ms * 1e-3) / 1e9 / peak,
                          "algorithmic_bytes_per_launch": algorithmic_bytes(w, fwd=False)},
+        "sweep": sweep_out,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         # library kernels in the two timed regions: the step loop and the end-to-end loop
-        "gpu_launches": args.steps * (2 * launches_fwd + launches_bwd) + args.steps * launches_fwd,
+        "gpu_launches": args.steps * n_launch_step + args.steps * launches_fwd,
         "clocks": clk.summary(),
         "wall_s": wall,
     }
-    line["roofline"]["frac"] = achieved / peak
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(w)
     print(json.dumps(line))
@@ -451,54 +582,6 @@ def run_fwd_only(args):
                       "tokens_per_s": w.batch * w.seqlen / (sum(times) / len(times) * 1e-3)}))
 
 
-def run_sweep(args):
-    """Forward throughput of the other forward workloads (long-sequence sweep, packed varlen):
-    CUDA graph replay, L2 flushed before each run, median of --steps runs; one JSON line each."""
-    import torch
-    from state_space_model_scan_gb300 import inputs as I
-    from state_space_model_scan_gb300 import _lib
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    cases = [I.named("long_seq", L=L) for L in (1024, 2048, 4096, 8192, 16384, 32768)] + [I.named("varlen")]
-    for w in cases:
-        inp = I.make_inputs(w)
-        d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-        S = w.nseqs
-        y = torch.empty_like(d["x"])
-        fin = torch.empty(S, w.nheads, w.headdim, w.dstate, device="cuda")
-        prob = _lib.problem(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk_size,
-                            S if d["cu_seqlens"] is not None else 0)
-        args_ = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], z=d["z"],
-                              dt_bias=d["dt_bias"], initial_states=d["initial_states"], final_states=fin,
-                              cu_seqlens=d["cu_seqlens"])
-        ws = torch.empty(_lib.fwd_workspace_size(prob, args_), dtype=torch.uint8, device="cuda")
-        s = torch.cuda.Stream()
-        with torch.cuda.stream(s):
-            _lib.check(_lib.ssd_fwd(prob, args_, ws, s), "ssd_fwd")
-        s.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            _lib.check(_lib.ssd_fwd(prob, args_, ws, torch.cuda.current_stream()), "ssd_fwd")
-        ts = []
-        for i in range(args.warmup + args.steps):
-            with torch.cuda.stream(s):
-                flush.fill_(1.0)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(s)
-                g.replay()
-                e1.record(s)
-            s.synchronize()
-            if i >= args.warmup:
-                ts.append(e0.elapsed_time(e1))
-        ts.sort()
-        ms = ts[len(ts) // 2]
-        toks = w.batch * w.seqlen
-        per_tok = 2 * w.nheads * w.headdim * (3 if w.has_z else 2) + 2 * 2 * w.ngroups * w.dstate + 4 * w.nheads
-        alg = toks * per_tok + 4 * w.nheads * w.headdim * w.dstate * S * (2 if w.has_init else 1)
-        print(json.dumps({"mode": "sweep", "workload": w.name, "seqlen": w.seqlen, "nseqs": S, "nheads": w.nheads,
-                          "fwd_ms_median": ms, "tokens_per_s": toks / (ms * 1e-3),
-                          "algorithmic_bytes": alg, "algorithmic_gbs": alg / (ms * 1e-3) / 1e9}))
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -506,15 +589,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="bench", choices=["bench", "fwd", "sweep"])
+    ap.add_argument("--mode", default="bench", choices=["bench", "fwd"])
+    ap.add_argument("--no-sweep", action="store_true", help="time the Nemotron-Nano workload only")
     ap.add_argument("--seg-chunks", type=int, default=0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.mode == "fwd":
         run_fwd_only(args)
-    elif args.mode == "sweep":
-        run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -286,18 +286,18 @@ int32_t ssd_abi_version(void);
  * Byte offsets, inside an ssd_fwd workspace, of the intermediates the STAGED
  * forward leaves behind after it completes (for stage-by-stage checks):
  *   meta_counts : int32[4]  {n_chunks, n_units, n_seqs, status}
- *   chunk_info  : int32[n_chunks][8] {seq, batch row, first token t0 of the physical
- *                 chunk in the row, end - t0, first - t0, 0, 0, 0}: one chunk tile per
- *                 segment of a physical chunk; tile rows [first - t0, end - t0) are the
- *                 sequence's
+ *   chunk_info  : 16-byte records {int32 seq, int32 batch row, int32 first token t0 of
+ *                 the physical chunk in the row, int16 end - t0, int16 first - t0}: one
+ *                 chunk tile per segment of a physical chunk; tile rows [first - t0,
+ *                 end - t0) are the sequence's
  *   dt          : f32[n_chunks][nheads][qi]   softplus(dt_raw + dt_bias), 0 past the chunk's length
  *   cs          : f32[n_chunks][nheads][qi]   inclusive in-chunk cumulative sum of dt*A
  *   states      : f32[n_chunks][nheads][headdim][dstate]  carry-in state of each chunk
- *   units       : int32[n_units][12] (fused path) {seq, batch row, t0 of its first tile,
- *                 end of the sequence's rows from t0 (capped at its tiles), tile count,
- *                 index of the sequence's previous unit or -1, 1 if last unit of its
- *                 sequence, unit index j within the sequence, first row of its first tile,
- *                 0, 0, 0}; units are grouped in blocks of 4 and listed by (block,
+ *   units       : 32-byte records (fused path) {int32 seq, batch row, t0 of its first
+ *                 tile, end of the sequence's rows from t0 (capped at its tiles), tile
+ *                 count, index of the sequence's previous unit or -1, unit index j within
+ *                 the sequence; int16 1 if last unit of its sequence, int16 first row of
+ *                 its first tile}; units are grouped in blocks of 4 and listed by (block,
  *                 sequence, j)
  * where qi is the chunk length (chunk_size) written to *qi.  Tiles are listed sequence
  * by sequence, in order (the same order as chunk by chunk).  Offsets of -1 mean "not

@@ -691,6 +691,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         pe[i >> 1] = pack_bf16(ev[0], ev[1]);
                     }
                 } else {
+                    float dg = 0.f;   // the diagonal's E CB dM (E = 1)
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
                         float mv[2], ev[2];
@@ -698,17 +699,16 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         for (int jj = 0; jj < 2; ++jj) {
                             const int s = sb * 32 + i + jj;
                             float m = 0.f, e = 0.f, t = 0.f;
-                            if (s < l) {
+                            if (s <= l) {
                                 const float E = ex2(c2l - cs2[s]);
                                 const float ec = E * cb[i + jj], ed = E * dtc[s];
                                 m = ed * cb[i + jj];
                                 e = ed * dm[i + jj];
                                 t = ec * dm[i + jj];
-                                rowt1 = fmaf(m, dm[i + jj], rowt1);
-                            } else if (s == l) {
-                                m = dtc[s] * cb[i + jj];
-                                e = dtc[s] * dm[i + jj];
-                                fm[F_DIAG + l] = cb[i + jj] * dm[i + jj];
+                                const bool dia = s == l;
+                                rowt1 = fmaf(dia ? 0.f : m, dm[i + jj], rowt1);
+                                dg = dia ? t : dg;
+                                t = dia ? 0.f : t;
                             }
                             mv[jj] = m;
                             ev[jj] = e;
@@ -717,6 +717,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                         pm[i >> 1] = pack_bf16(mv[0], mv[1]);
                         pe[i >> 1] = pack_bf16(ev[0], ev[1]);
                     }
+                    fm[F_DIAG + l] = dg;
                 }
                 colp[warp * 64 + bi * 32 + lane] = colsum32(cb);
 #pragma unroll

@@ -30,27 +30,29 @@ enum HeaderWord {
 // outside get dt := 0 (decay 1, no input) and are never written, which is the
 // sequence mask seq_idx[l] == seq_idx[s] of the intra-chunk matrix.
 
-// One sequence: tokens [t0, t0 + len) of batch row b; its chunk tiles start at chunk0.
+// One sequence: tokens [t0, t0 + len) of batch row b; its nch chunk tiles start at chunk0.
 struct SeqInfo {
     int32_t b, t0, len, chunk0;
+    int32_t nch, pad0, pad1, pad2;
 };
 // Number of chunk tiles of a sequence: the physical chunks its tokens touch.
 __host__ __device__ __forceinline__ int seq_nchunks(int t0, int len, int Q) {
     return len > 0 ? (t0 + len + Q - 1) / Q - t0 / Q : 0;
 }
 // One chunk tile: the segment of one sequence in the physical chunk starting at token t0
-// of batch row b; rows [lo, len) of the tile belong to it (0 <= lo < len <= Q).
+// of batch row b; rows [lo, len) of the tile belong to it (0 <= lo < len <= Q).  16 bytes
+// (the gradient kernel keeps two of these live at its register limit).
 struct ChunkInfo {
-    int32_t seq, b, t0, len;
-    int32_t lo, pad0, pad1, pad2;
+    int32_t seq, b, t0;
+    int16_t len, lo;
 };
 // One work unit of the fused forward: segment j (`nchunk` consecutive chunk tiles) of one
 // sequence; t0 = first token of its first tile's physical chunk, rows [lo, len) from t0
 // belong to the sequence (lo > 0 only for a sequence starting inside its first chunk).
 struct UnitInfo {
     int32_t seq, b, t0, len;          // rows [lo, len) from token t0 of row b
-    int32_t nchunk, prev, last, j;    // prev: index of unit (seq, j-1) or -1; last: j is the final segment
-    int32_t lo, pad0, pad1, pad2;
+    int32_t nchunk, prev, j;          // prev: index of unit (seq, j-1) or -1
+    int16_t last, lo;                 // last: j is the sequence's final unit
 };
 
 // Shape of one call, as the kernels see it.

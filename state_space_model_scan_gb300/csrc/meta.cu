@@ -111,6 +111,7 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
         if (s < S) {
             SeqInfo si;
             si.b = b; si.t0 = t0; si.len = len; si.chunk0 = carry + off;
+            si.nch = nch; si.pad0 = si.pad1 = si.pad2 = 0;
             seqs[s] = si;
         }
         int nseg = seg_count(nch, R, num, den);
@@ -135,9 +136,8 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
         const int j = c - si.chunk0;
         ChunkInfo ci;
         ci.seq = lo; ci.b = si.b; ci.t0 = (si.t0 / Q + j) * Q;
-        ci.lo = max(si.t0 - ci.t0, 0);
-        ci.len = min(Q, si.t0 + si.len - ci.t0);
-        ci.pad0 = ci.pad1 = ci.pad2 = 0;
+        ci.lo = (int16_t)max(si.t0 - ci.t0, 0);
+        ci.len = (int16_t)min(Q, si.t0 + si.len - ci.t0);
         chunks[c] = ci;
     }
     // pass 3: work units ordered by (block of KB segments, sequence, segment)
@@ -151,7 +151,7 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
                 SeqInfo si;
                 if (s < S) {
                     si = seqs[s];
-                    nch = seq_nchunks(si.t0, si.len, Q);
+                    nch = si.nch;
                     nseg = seg_count(nch, R, num, den);
                     cnt = max(0, min(KB, nseg - blk * KB));
                 }
@@ -168,11 +168,10 @@ k_build_meta(const int32_t *__restrict__ cu, int B, int L, int S, int Q, int R, 
                         ui.t0 = (si.t0 / Q + c0) * Q;
                         ui.nchunk = base + (j < rem ? 1 : 0);
                         ui.len = min(ui.nchunk * Q, si.t0 + si.len - ui.t0);
-                        ui.lo = c0 == 0 ? si.t0 - ui.t0 : 0;
+                        ui.lo = (int16_t)(c0 == 0 ? si.t0 - ui.t0 : 0);
                         ui.prev = (j == 0) ? -1 : (i > 0 ? u - 1 : last_unit[s]);
                         ui.last = (j == nseg - 1) ? 1 : 0;
                         ui.j = j;
-                        ui.pad0 = ui.pad1 = ui.pad2 = 0;
                         units[u] = ui;
                         if (i == cnt - 1) last_unit[s] = u;
                     }
@@ -219,13 +218,14 @@ k_build_meta_fixed(int B, int L, int Q, int R, int num, int den, int KB, int kma
     for (int64_t s = t0; s < B; s += stride) {
         SeqInfo si;
         si.b = (int)s; si.t0 = 0; si.len = L; si.chunk0 = (int)(s * nch);
+        si.nch = nch; si.pad0 = si.pad1 = si.pad2 = 0;
         seqs[s] = si;
     }
     for (int64_t c = t0; c < nchunks; c += stride) {
         const int s = (int)(c / nch), j = (int)(c % nch);
         ChunkInfo ci;
-        ci.seq = s; ci.b = s; ci.t0 = j * Q; ci.len = min(Q, L - j * Q);
-        ci.lo = 0; ci.pad0 = ci.pad1 = ci.pad2 = 0;
+        ci.seq = s; ci.b = s; ci.t0 = j * Q; ci.len = (int16_t)min(Q, L - j * Q);
+        ci.lo = 0;
         chunks[c] = ci;
     }
     const int base = nseg > 0 ? nch / nseg : 0, rem = nseg > 0 ? nch % nseg : 0;
@@ -244,7 +244,7 @@ k_build_meta_fixed(int B, int L, int Q, int R, int num, int den, int KB, int kma
         ui.prev = j == 0 ? -1 : (i > 0 ? (int)u - 1 : (int)((blk - 1) * B * KB + (int64_t)s * KB + KB - 1));
         ui.last = j == nseg - 1 ? 1 : 0;
         ui.j = j;
-        ui.lo = 0; ui.pad0 = ui.pad1 = ui.pad2 = 0;
+        ui.lo = 0;
         units[u] = ui;
     }
 }

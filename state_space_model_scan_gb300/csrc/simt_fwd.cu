@@ -127,7 +127,7 @@ k_state_passing(Shape sh, const int32_t *__restrict__ hdr, const SeqInfo *__rest
     const int e = (blockIdx.y * 256 + threadIdx.x) * 4, lane = threadIdx.x & 31;
     if ((blockIdx.y * 256 + (threadIdx.x & ~31)) * 4 >= PN) return;   // whole warp past the end
     const SeqInfo si = seqs[s];
-    const int nch = seq_nchunks(si.t0, si.len, sh.Q);
+    const int nch = si.nch;   // (a division by the runtime chunk length here measurably slowed the scan)
     const int64_t sbase = ((int64_t)s * sh.H + h) * PN;
     const bool act = e < PN;
     float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);

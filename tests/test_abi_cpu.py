@@ -202,12 +202,12 @@ def test_unit_schedule_restatement():
     assert [u[:5] for u in m["units"]] == [(0, 0, 0, 5, 1), (2, 0, 0, 128, 2), (2, 0, 128, 128, 2),
                                            (2, 0, 256, 44, 1)]
     assert [u[5] for u in m["units"]] == [-1, -1, 1, 2]
-    assert [u[6] for u in m["units"]] == [1, 0, 0, 1]
-    assert [u[7] for u in m["units"]] == [0, 0, 1, 2]
+    assert [u[6] for u in m["units"]] == [0, 0, 1, 2]
+    assert [u[7] for u in m["units"]] == [1, 0, 0, 1]
     assert [u[8] for u in m["units"]] == [0, 5, 0, 0]
     # blocks of two units; sequence 1 starts inside physical chunk 4 and has 6 tiles
     m = meta.build(cu=[0, 300, 600], Q=64, R=1, KB=2)
-    assert [(u[0], u[7]) for u in m["units"]] == [(0, 0), (0, 1), (1, 0), (1, 1), (0, 2), (0, 3), (1, 2), (1, 3),
+    assert [(u[0], u[6]) for u in m["units"]] == [(0, 0), (0, 1), (1, 0), (1, 1), (0, 2), (0, 3), (1, 2), (1, 3),
                                                   (0, 4), (1, 4), (1, 5)]
     assert [u[5] for u in m["units"]] == [-1, 0, -1, 2, 1, 4, 3, 6, 5, 7, 9]
     assert [(u[2], u[3], u[8]) for u in m["units"] if u[0] == 1][:2] == [(256, 64, 44), (320, 64, 0)]
@@ -223,7 +223,7 @@ def test_unit_schedule_balanced_units():
     sizes = [u[4] for u in m["units"]]
     assert sizes == [4] * 7 + [3] * 12
     pos = 0
-    for u in sorted(m["units"], key=lambda r: r[7]):
+    for u in sorted(m["units"], key=lambda r: r[6]):
         assert u[2] == pos and u[3] == min(u[4] * 128, 128 * 64 - 5 - pos)
         pos += u[3]
     assert pos == 128 * 64 - 5

@@ -88,10 +88,9 @@ def test_chunk_tiles_are_the_segments(algo):
     raw, lay, counts, _ = run_meta(w, I.make_inputs(w), algo)
     Q = lay.qi
     segs, _ = varlen_meta.segments(cu_of(lens), Q)
-    ref = [(s, 0, (a // Q) * Q, e - (a // Q) * Q, a - (a // Q) * Q, 0, 0, 0) for (s, a, e) in segs]
+    ref = [(s, 0, (a // Q) * Q, e - (a // Q) * Q, a - (a // Q) * Q) for (s, a, e) in segs]
     assert counts[0] == len(ref) and counts[3] == 0
-    got = raw[lay.chunk_info:lay.chunk_info + 32 * counts[0]].view(np.int32).reshape(-1, 8)
-    assert [tuple(r) for r in got.tolist()] == ref
+    assert unit_schedule.decode_chunks(raw[lay.chunk_info:], counts[0]) == ref
 
 
 def test_fused_unit_list_matches_the_scheduler_restatement():
@@ -102,8 +101,7 @@ def test_fused_unit_list_matches_the_scheduler_restatement():
     raw, lay, counts, _ = run_meta(w, I.make_inputs(w), "fused", seg=2)
     ref = unit_schedule.build(cu=cu_of(lens), Q=128, R=2, KB=4)
     assert lay.units >= 0 and counts[1] == len(ref["units"]) and counts[3] == 0
-    got = raw[lay.units:lay.units + 48 * counts[1]].view(np.int32).reshape(-1, 12)
-    assert [tuple(r) for r in got.tolist()] == ref["units"]
+    assert unit_schedule.decode_units(raw[lay.units:], counts[1]) == ref["units"]
 
 
 @pytest.mark.parametrize("dtype,P,N,algo", [("f32", 16, 16, "staged"), ("bf16", 16, 16, "staged"),
@@ -212,14 +210,12 @@ def test_fixed_batch_metadata_bit_exact(B, L, seg, algo):
     raw = ws.cpu().numpy()
     counts = raw[lay.meta_counts:lay.meta_counts + 16].view(np.int32)
     if fused:
-        got = raw[lay.units:lay.units + 48 * counts[1]].view(np.int32).reshape(-1, 12)
-        R = int(prob.seg_chunks) or int(got[0][4])   # the library's own unit size when seg = 0
+        got = unit_schedule.decode_units(raw[lay.units:], counts[1])
+        R = int(prob.seg_chunks) or got[0][4]   # the library's own unit size when seg = 0
         ref = unit_schedule.build(batch=B, seqlen=L, Q=128, R=R, KB=4)
         assert counts[1] == len(ref["units"]) and counts[3] == 0
-        assert [tuple(r) for r in got.tolist()] == ref["units"]
+        assert got == ref["units"]
     else:
         ref = unit_schedule.build(batch=B, seqlen=L, Q=lay.qi)
     assert counts[0] == len(ref["chunks"]) and counts[3] == 0
-    got_c = raw[lay.chunk_info:lay.chunk_info + 32 * counts[0]].view(np.int32).reshape(-1, 8)
-    assert [tuple(r[:5]) for r in got_c.tolist()] == ref["chunks"]
-    assert (got_c[:, 5:] == 0).all()
+    assert unit_schedule.decode_chunks(raw[lay.chunk_info:], counts[0]) == ref["chunks"]

@@ -17,9 +17,25 @@ m = max(ceil(n/R), min(n, ceil(n num/den))) units (num/den = 1/R unless given),
 unit j holding floor(n/m) tiles plus one more for j < n mod m; units are grouped
 in blocks of KB and listed by (block, sequence, j) -> rows (seq, batch row, t0 of
 its first tile, end of the sequence's tokens - t0 capped at its tiles, tile count,
-index of unit (s, j-1) or -1, 1 if last unit of s, j, leading rows lo of its first
-tile, 0, 0, 0).
+index of unit (s, j-1) or -1, j, 1 if last unit of s, leading rows lo of its first
+tile).
+
+decode_chunks / decode_units turn the library's raw records (16 and 32 bytes: the
+last int32 word of each holds two int16 fields, low half first) into those tuples.
 """
+import numpy as np
+
+
+def decode_chunks(raw_bytes, n):
+    a = np.frombuffer(raw_bytes[:16 * n].tobytes(), dtype=np.int32).reshape(n, 4)
+    h = np.frombuffer(raw_bytes[:16 * n].tobytes(), dtype=np.int16).reshape(n, 8)
+    return [(int(r[0]), int(r[1]), int(r[2]), int(q[6]), int(q[7])) for r, q in zip(a, h)]
+
+
+def decode_units(raw_bytes, n):
+    a = np.frombuffer(raw_bytes[:32 * n].tobytes(), dtype=np.int32).reshape(n, 8)
+    h = np.frombuffer(raw_bytes[:32 * n].tobytes(), dtype=np.int16).reshape(n, 16)
+    return [tuple(int(v) for v in r[:7]) + (int(q[14]), int(q[15])) for r, q in zip(a, h)]
 from oracle import varlen_meta
 
 
@@ -63,7 +79,6 @@ def build(cu=None, batch=1, seqlen=0, Q=64, R=1, KB=8, num=None, den=None):
                 first = chunks[chunk0[s] + c0]
                 ut0 = first[2]
                 units.append((s, b, ut0, min(nc * Q, t0 + n - ut0), nc,
-                              last.get(s, -1) if j > 0 else -1, 1 if j == nseg[s] - 1 else 0, j,
-                              first[4], 0, 0, 0))
+                              last.get(s, -1) if j > 0 else -1, j, 1 if j == nseg[s] - 1 else 0, first[4]))
                 last[s] = len(units) - 1
     return dict(seqs=[(b, t0, n, chunk0[s]) for s, (b, t0, n) in enumerate(seqs)], chunks=chunks, units=units)
