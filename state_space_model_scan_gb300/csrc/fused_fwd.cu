@@ -48,7 +48,7 @@ constexpr int NT = 128;   // state dim
 constexpr int RMAX = 5;   // max chunks per unit (states-only mode: 4, one 64-column TMEM slice each)
 constexpr int RMAX_STATES = 4;
 constexpr int KB = 4;     // segments per block of the carry-in fold
-constexpr int NTHR = 128; // one thread per tile row / TMEM lane
+constexpr int NTHR = 256; // two threads per tile row / TMEM lane: half hf holds head-dim columns [32 hf, 32 hf + 32)
 
 constexpr uint32_t X_BYTES = QT * PT * 2;    // 16 KB
 constexpr uint32_t BC_BYTES = QT * NT * 2;   // 32 KB
@@ -134,6 +134,9 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// TMEM column (from TM_M) of M's 32-column block sb (see the M build in phase 2).
+__device__ __forceinline__ uint32_t mcol(int sb) { return sb == 0 ? 0u : sb == 1 ? 32u : sb == 2 ? 48u : 16u; }
+
 // Row n of the carried-state tile of (chunk k, head h) in FusedParams::states_out.
 __device__ __forceinline__ uint8_t *state_tile_row(__nv_bfloat16 *base, int64_t k, int H, int h, int n) {
     return reinterpret_cast<uint8_t *>(base) + ((k * H + h) * (int64_t)(PT * NT) + (int64_t)n * PT) * 2;
@@ -148,14 +151,15 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k) {
     return sdesc(base + (uint32_t)k * 2048u, 16384u, 1024u);
 }
 
-// dst row = src row * w (a full 128-byte row; the 16-byte chunks are visited in
-// swizzled order so eight consecutive rows hit eight different bank groups).
-__device__ __forceinline__ void scale_row(const uint8_t *src_row, uint8_t *dst_row, int row, float wl) {
+// dst row = src row * w, half hf of the row's eight 16-byte pieces (the two halves of a
+// row are disjoint; visited in swizzled order so eight consecutive rows hit eight
+// different bank groups).
+__device__ __forceinline__ void scale_half(const uint8_t *src_row, uint8_t *dst_row, int row, int hf, float wl) {
     const uint4 *src = reinterpret_cast<const uint4 *>(src_row);
     uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
 #pragma unroll
-    for (int qq = 0; qq < 8; ++qq) {
-        const int q = qq ^ (row & 7);
+    for (int qq = 0; qq < 4; ++qq) {
+        const int q = (4 * hf + qq) ^ (row & 7);
         uint4 v = src[q];
         __nv_bfloat162 *e = reinterpret_cast<__nv_bfloat162 *>(&v);
 #pragma unroll
@@ -167,17 +171,27 @@ __device__ __forceinline__ void scale_row(const uint8_t *src_row, uint8_t *dst_r
     }
 }
 
-// acc[i] += sc * src[i * NT] for the 64 state columns p (a [P][N] state: for each
-// column p the warp reads one contiguous 128-byte line).
-__device__ __forceinline__ void fma_col64(float *acc, const float *src, float sc) {
+// acc[i] += sc * src[i * NT] for 32 state columns p (a [P][N] state: for each column p
+// the warp reads one contiguous 128-byte line).
+__device__ __forceinline__ void fma_col32(float *acc, const float *src, float sc) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float v[32];
+    for (int j = 0; j < 32; j += 8) {
+        float v[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __ldcg(src + (int64_t)(32 * h + i) * NT);
+        for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + (int64_t)(j + i) * NT);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[32 * h + i] += sc * v[i];
+        for (int i = 0; i < 8; ++i) acc[j + i] += sc * v[i];
     }
+}
+
+// Row n of a carried-state tile (bf16, 128-byte swizzled [n][p]), half hf: the four
+// 16-byte pieces of columns p = 32 hf .. 32 hf + 31, from the thread's 32 values.
+__device__ __forceinline__ void store_state_half(uint8_t *rowp, int row, int hf, const float *v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(rowp + (((4 * hf + q) ^ (row & 7)) << 4)) =
+            make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                       pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
 }
 
 // kStatesOnly: the states-only mode (only FusedParams::states_out is written), compiled
@@ -190,7 +204,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int row = tid;
+    const int row = tid & 127, hf = tid >> 7, quad = warp & 3;
     Misc *ms = reinterpret_cast<Misc *>(sm + OFF_MISC);
     float *dtu = reinterpret_cast<float *>(sm + OFF_DTU);
     float *wu = reinterpret_cast<float *>(sm + OFF_WU);
@@ -215,13 +229,13 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ms->tmem_base;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
-    // Completed-phase counters, kept identically by every thread (all issue
-    // decisions are uniform), and the count of issued-but-unwaited operations per
-    // barrier for the drain after an early stop.
-    uint32_t done[NBAR] = {0, 0, 0, 0, 0};
-    uint32_t issued[NBAR] = {0, 0, 0, 0, 0};
+    // Per barrier, kept identically by every thread (all issue decisions are uniform):
+    // the parity of its completed phases (bit b of par) and the count of issued-but-
+    // unwaited operations (4-bit field b of pend, at most 2) for the drain after an
+    // early stop.
+    uint32_t par = 0u, pend = 0u;
     const int total = (p.hdr[HDR_STATUS] != 0) ? 0 : p.hdr[HDR_NUNITS] * sh.H;
 
     auto fail = [&]() {
@@ -229,8 +243,9 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
     };
     auto wait_bar = [&](int b) {
-        if (!mbar_wait(&ms->bar[b], done[b] & 1)) fail();
-        ++done[b];
+        if (!mbar_wait(&ms->bar[b], (par >> b) & 1u)) fail();
+        par ^= 1u << b;
+        pend -= 1u << (4 * b);
         if (b == BAR_MMA) tc_fence_after();
     };
     // TMA issue helpers (one thread issues; every thread counts)
@@ -242,14 +257,14 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             tma_load_4d(bd, &tmB, bar, 0, g, t, bb);
             tma_load_4d(bd + BC_BYTES / 2, &tmB, bar, 64, g, t, bb);
         }
-        ++issued[b_];
+        pend += 1u << (4 * b_);
     };
     auto load_x = [&](int h, int t, int bb) {
         if (tid == 0) {
             mbar_expect_tx(&ms->bar[BAR_X], X_BYTES);
             tma_load_4d(Xs, &tmX, &ms->bar[BAR_X], 0, h, t, bb);
         }
-        ++issued[BAR_X];
+        pend += 1u << (4 * BAR_X);
     };
     auto load_bc = [&](int b_, const CUtensorMap *map, uint8_t *dst, int g, int t, int bb) {
         if (tid == 0) {
@@ -257,18 +272,18 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             tma_load_4d(dst, map, &ms->bar[b_], 0, g, t, bb);
             tma_load_4d(dst + BC_BYTES / 2, map, &ms->bar[b_], 64, g, t, bb);
         }
-        ++issued[b_];
+        pend += 1u << (4 * b_);
     };
     auto load_z = [&](int h, int t, int bb) {
         if (tid == 0) {
             mbar_expect_tx(&ms->bar[BAR_Z], X_BYTES);
             tma_load_4d(Ws, &tmZ, &ms->bar[BAR_Z], 0, h, t, bb);
         }
-        ++issued[BAR_Z];
+        pend += 1u << (4 * BAR_Z);
     };
     auto commit = [&]() {
         if (tid == 0) umma_commit(&ms->bar[BAR_MMA]);
-        ++issued[BAR_MMA];
+        pend += 1u << (4 * BAR_MMA);
     };
 
     const uint32_t idesc_cb = idesc_bf16(128, 128, 0, 0);
@@ -385,7 +400,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             wait_bar(st ? BAR_C : BAR_X);
             const float wl = full ? wu[c * QT + row]
                                   : dtu[c * QT + row] * ex2(cs2u[c * QT + QT - 1] - cs2u[c * QT + row]);
-            scale_row(xs + row * 128, xs + row * 128, row, wl);   // x -> w o x in place
+            scale_half(xs + row * 128, xs + row * 128, row, hf, wl);   // x -> w o x in place
             fence_proxy_async_smem();
             __syncthreads();
             if (ms->abort_) break;
@@ -404,36 +419,28 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 load_xb(st ? BAR_C : BAR_X, xs, st ? Cs : Bs, h, g, ui.t0 + (c + 2) * QT, ui.b);
         }
         if (ms->abort_) break;
-        float s_run[64];   // row n = tid: aggregate, then carried state, columns p
+        float s_run[32];   // row n, columns p = 32 hf + i: aggregate, then carried state
         if (full) {
-            float t32[32];
-            tmem_ld32(tmem + lane_base + TM_SC, t32);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s_run[i] = t32[i];
-            tmem_ld32(tmem + lane_base + TM_SC + 32, t32);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s_run[32 + i] = t32[i];
+            tmem_ld32(tmem + lane_base + TM_SC + 32 * hf, s_run);
             tmem_wait_ld();
         } else {   // aggregate = (..(S_0 a_1 + S_1) a_2 + ..) + S_last, a_c = the chunk's decay
 #pragma unroll
-            for (int i = 0; i < 64; ++i) s_run[i] = 0.f;
+            for (int i = 0; i < 32; ++i) s_run[i] = 0.f;
             for (int c = 0; c < ui.nchunk; ++c) {
                 const float a_c = ex2(cs2u[c * QT + QT - 1]);
+                float t32[32];
+                tmem_ld32(tmem + lane_base + 64u * (uint32_t)c + 32 * hf, t32);
+                tmem_wait_ld();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float t32[32];
-                    tmem_ld32(tmem + lane_base + 64u * (uint32_t)c + 32 * hh, t32);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s_run[32 * hh + i] = fmaf(a_c, s_run[32 * hh + i], t32[i]);
-                }
+                for (int i = 0; i < 32; ++i) s_run[i] = fmaf(a_c, s_run[i], t32[i]);
             }
         }
         const int64_t my = (int64_t)u * sh.H + h;
+        const int64_t col0 = (int64_t)(32 * hf) * NT;   // this thread's first column p of a [P][N] state
         {   // aggregate^T row n -> agg[p][n]
-            float *dst = p.agg + my * unit_stride + row;
+            float *dst = p.agg + my * unit_stride + col0 + row;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) __stcg(dst + (int64_t)i * NT, s_run[i]);
+            for (int i = 0; i < 32; ++i) __stcg(dst + (int64_t)i * NT, s_run[i]);
             if (tid == 0) __stcg(p.lam + my, lam_u);
         }
         __threadfence();
@@ -459,9 +466,9 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         // ---- carry-in state of the unit (row n, all 64 columns p)
         // P_j = sum_{i=b0}^{j-1} exp(lam_{i+1} + .. + lam_{j-1}) agg_i + exp(lam_{b0} + .. + lam_{j-1}) E,
         // E = end state of unit b0-1 (published by it) or the initial state when b0 = 0.
-        float agg_keep[64];
+        float agg_keep[32];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) { agg_keep[i] = s_run[i]; s_run[i] = 0.f; }
+        for (int i = 0; i < 32; ++i) { agg_keep[i] = s_run[i]; s_run[i] = 0.f; }
         const int b0 = ui.j - (ui.j % KB);
         const int nfold = ui.j - b0;     // in-block predecessors: units u-1 .. u-nfold
         const int uprev_blk = (b0 > 0) ? (nfold > 0 ? p.units[u - nfold].prev : ui.prev) : -1;
@@ -489,23 +496,23 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         for (int i = 1; i <= nfold; ++i) {   // units u-1, u-2, .. in that order
             const int64_t pi = (int64_t)(u - i) * sh.H + h;
             const float lam_i = __ldcg(p.lam + pi);
-            fma_col64(s_run, p.agg + pi * unit_stride + row, ex2(logm * LOG2E));
+            fma_col32(s_run, p.agg + pi * unit_stride + col0 + row, ex2(logm * LOG2E));
             logm += lam_i;
         }
         if (uprev_blk >= 0) {
             const int64_t pi = (int64_t)uprev_blk * sh.H + h;
-            fma_col64(s_run, p.incl + pi * unit_stride + row, ex2(logm * LOG2E));
+            fma_col32(s_run, p.incl + pi * unit_stride + col0 + row, ex2(logm * LOG2E));
         } else if (p.init) {
             const float sc = ex2(logm * LOG2E);
-            const float *src = p.init + ((int64_t)ui.seq * sh.H + h) * PT * NT + row;
+            const float *src = p.init + ((int64_t)ui.seq * sh.H + h) * PT * NT + col0 + row;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) s_run[i] += sc * src[(int64_t)i * NT];
+            for (int i = 0; i < 32; ++i) s_run[i] += sc * src[(int64_t)i * NT];
         }
         if ((ui.j % KB) == KB - 1 && !ui.last) {   // block end: publish the unit's end state
             const float dec = ex2(lam_u * LOG2E);
-            float *dst = p.incl + my * unit_stride + row;
+            float *dst = p.incl + my * unit_stride + col0 + row;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) __stcg(dst + (int64_t)i * NT, agg_keep[i] + dec * s_run[i]);
+            for (int i = 0; i < 32; ++i) __stcg(dst + (int64_t)i * NT, agg_keep[i] + dec * s_run[i]);
             __threadfence();
             __syncthreads();
             if (tid == 0) st_release_u32(p.flags + my, 2u);
@@ -516,21 +523,13 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         if (!full) {
             const int64_t kfirst = (int64_t)p.seqs[ui.seq].chunk0 + ui.t0 / QT - p.seqs[ui.seq].t0 / QT;
             for (int c = 0; c < ui.nchunk; ++c) {
-                uint8_t *dst = state_tile_row(p.states_out, kfirst + c, sh.H, h, row);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<uint4 *>(dst + ((q ^ (row & 7)) << 4)) =
-                        make_uint4(pack_bf16(s_run[8 * q], s_run[8 * q + 1]), pack_bf16(s_run[8 * q + 2], s_run[8 * q + 3]),
-                                   pack_bf16(s_run[8 * q + 4], s_run[8 * q + 5]), pack_bf16(s_run[8 * q + 6], s_run[8 * q + 7]));
+                store_state_half(state_tile_row(p.states_out, kfirst + c, sh.H, h, row), row, hf, s_run);
                 const float a_c = ex2(cs2u[c * QT + QT - 1]);
+                float t32[32];
+                tmem_ld32(tmem + lane_base + 64u * (uint32_t)c + 32 * hf, t32);
+                tmem_wait_ld();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float t32[32];
-                    tmem_ld32(tmem + lane_base + 64u * (uint32_t)c + 32 * hh, t32);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s_run[32 * hh + i] = fmaf(a_c, s_run[32 * hh + i], t32[i]);
-                }
+                for (int i = 0; i < 32; ++i) s_run[i] = fmaf(a_c, s_run[i], t32[i]);
             }
             tc_fence_before();
             __syncthreads();   // TMEM read: the next unit's phase 1 may overwrite it
@@ -568,7 +567,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 y_inflight = false;
             }
             // W = w o x, w[l] = dt[l] exp(cs[Q-1] - cs[l])
-            scale_row(Xs + row * 128, Ws + row * 128, row, dtc[row] * ex2(cs2[QT - 1] - cs2[row]));
+            scale_half(Xs + row * 128, Ws + row * 128, row, hf, dtc[row] * ex2(cs2[QT - 1] - cs2[row]));
             fence_proxy_async_smem();
             __syncthreads();
             if (ms->abort_) {
@@ -591,12 +590,13 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                     uint8_t *rowp = Ws + row * 128;
                     uint8_t *grow = p.states_out ? state_tile_row(p.states_out, kfirst + c, sh.H, h, row) : nullptr;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < 4; ++q) {
                         const uint4 v =
                             make_uint4(pack_bf16(s_run[8 * q], s_run[8 * q + 1]), pack_bf16(s_run[8 * q + 2], s_run[8 * q + 3]),
                                        pack_bf16(s_run[8 * q + 4], s_run[8 * q + 5]), pack_bf16(s_run[8 * q + 6], s_run[8 * q + 7]));
-                        *reinterpret_cast<uint4 *>(rowp + ((q ^ (row & 7)) << 4)) = v;
-                        if (grow) *reinterpret_cast<uint4 *>(grow + ((q ^ (row & 7)) << 4)) = v;
+                        const int pos = ((4 * hf + q) ^ (row & 7)) << 4;
+                        *reinterpret_cast<uint4 *>(rowp + pos) = v;
+                        if (grow) *reinterpret_cast<uint4 *>(grow + pos) = v;
                     }
                 }
                 fence_proxy_async_smem();
@@ -608,13 +608,20 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                         umma_bf16(tmem + TM_YO, kmaj(sC, k, BC_BYTES / 2), mnmaj(sW, k), idesc_yo, k > 0);
                 }
                 commit();
-                // M (bf16, K-major [l][s], D on the diagonal) into the B buffer while Y_off runs
+                // M (bf16, [l][s], D on the diagonal) into TMEM while Y_off runs.  The two threads
+                // of row l take two of its four 32-column blocks each (hf 0: blocks 0 and 3, hf 1:
+                // blocks 1 and 2, so the causal work is split evenly).  M lives in CB's first 64
+                // columns; each thread stores its two M blocks (16 columns each) over the CB block
+                // it read first (hf 0 over CB block 0, hf 1 over CB block 1), which no other thread
+                // reads, so no thread overwrites CB that another still needs.  M block sb thus sits
+                // at column mcol(sb) = {0, 32, 48, 16}[sb]; Y_diag's K steps follow that order.
                 const int l = row;
                 const float cl = cs2[l];
 #pragma unroll
-                for (int sb = 0; sb < 4; ++sb) {
+                for (int bi = 0; bi < 2; ++bi) {
+                    const int sb = hf == 0 ? (bi == 0 ? 0 : 3) : (bi == 0 ? 1 : 2);
                     uint32_t pk[16];
-                    if (sb < warp) {
+                    if (sb < quad) {
                         // strictly below the diagonal: exp(cs[l]-cs[s]) = exp(cs[l]-cs[e]) exp(cs[e]-cs[s]),
                         // e = last token of the block; both factors <= 1, so neither overflows
                         float cb[32];
@@ -624,7 +631,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                         for (int i = 0; i < 32; i += 2)
                             pk[i >> 1] = pack_bf16(cb[i] * rl * cf[sb * 32 + i], cb[i + 1] * rl * cf[sb * 32 + i + 1]);
-                    } else if (sb == warp) {   // diagonal block: causal mask, D on the diagonal
+                    } else if (sb == quad) {   // diagonal block: causal mask, D on the diagonal
                         float cb[32];
                         tmem_ld32(tmem + lane_base + TM_CB + sb * 32, cb);
                         tmem_wait_ld();
@@ -641,21 +648,17 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
 #pragma unroll
                         for (int i = 0; i < 16; ++i) pk[i] = 0u;
                     }
-                    // row l of M, columns [32 sb, 32 sb + 32): 16 packed pairs into this lane's TMEM
-                    // (a thread only ever touches its own lane, and this block's CB is already read)
-                    tmem_st16(tmem + lane_base + TM_M + 16 * sb, pk);
+                    // row l of M block sb: 16 packed pairs into this lane's TMEM, over CB columns
+                    // this thread has already read
+                    tmem_st16(tmem + lane_base + TM_M + mcol(sb), pk);
                 }
             }
-            {   // carried state update: S_in[c+1] = a_c S_in[c] + S_c (row n)
+            {   // carried state update: S_in[c+1] = a_c S_in[c] + S_c (row n, this half's columns)
                 float sc[32];
-                tmem_ld32(tmem + lane_base + TM_SC, sc);
+                tmem_ld32(tmem + lane_base + TM_SC + 32 * hf, sc);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s_run[i] = a_c * s_run[i] + sc[i];
-                tmem_ld32(tmem + lane_base + TM_SC + 32, sc);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s_run[32 + i] = a_c * s_run[32 + i] + sc[i];
             }
             wait_bar(BAR_MMA);   // Y_off done: C and W free
             if (has_z) load_z(h, tc0, ui.b);
@@ -667,7 +670,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < QT / 16; ++k)   // Y_diag + D x = M x (K = source tokens), M from TMEM
-                    umma_bf16_ta(tmem + TM_YD, tmem + TM_M + 8 * k, mnmaj(sX, k), idesc_yd, k > 0);
+                    umma_bf16_ta(tmem + TM_YD, tmem + TM_M + mcol(k >> 1) + 8 * (k & 1), mnmaj(sX, k), idesc_yd, k > 0);
             }
             commit();
             wait_bar(BAR_MMA);   // x free: next chunk's x
@@ -677,27 +680,29 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
             // one TMA store; a chunk shared with another packed sequence stores its own rows
             // directly
             const bool tile_out = clen == QT && clo == 0;
-            {   // epilogue: row l
+            {   // epilogue: row l, this thread's half of the columns
                 const int l = row;
                 const float el = ex2(cs2[l]);
                 __nv_bfloat16 *yrow = p.y + (int64_t)ui.b * p.syb + tok * p.syl + (int64_t)h * p.syh;
                 const uint8_t *zrow = Ws + l * 128;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float yd[32], yo[32];
-                    tmem_ld32(tmem + lane_base + TM_YD + 32 * half, yd);
-                    tmem_ld32(tmem + lane_base + TM_YO + 32 * half, yo);
+                for (int qq = 0; qq < 4; qq += 2) {   // two passes of 16 columns
+                    const int q0 = 4 * hf + qq;       // first 16-byte piece (8 columns) of the pass
+                    float yd[16], yo[16];
+                    tmem_ld16(tmem + lane_base + TM_YD + 8 * q0, yd);
+                    tmem_ld16(tmem + lane_base + TM_YO + 8 * q0, yo);
                     tmem_wait_ld();
                     if (l >= clo && l < clen) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
+                        for (int qi = 0; qi < 2; ++qi) {
+                            const int q = q0 + qi;
                             uint4 zq = make_uint4(0u, 0u, 0u, 0u);
-                            if (has_z) zq = *reinterpret_cast<const uint4 *>(zrow + (((half * 4 + q) ^ (l & 7)) << 4));
+                            if (has_z) zq = *reinterpret_cast<const uint4 *>(zrow + ((q ^ (l & 7)) << 4));
                             const __nv_bfloat162 *ze = reinterpret_cast<const __nv_bfloat162 *>(&zq);
                             uint32_t o[4];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                const int j = q * 8 + 2 * i;
+                                const int j = qi * 8 + 2 * i;
                                 float v0 = yd[j] + el * yo[j];
                                 float v1 = yd[j + 1] + el * yo[j + 1];
                                 if (has_z) {
@@ -709,9 +714,9 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
                             }
                             const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
                             if (tile_out)
-                                *reinterpret_cast<uint4 *>(Ws + l * 128 + (((half * 4 + q) ^ (l & 7)) << 4)) = ov;
+                                *reinterpret_cast<uint4 *>(Ws + l * 128 + ((q ^ (l & 7)) << 4)) = ov;
                             else
-                                *reinterpret_cast<uint4 *>(yrow + half * 32 + q * 8) = ov;
+                                *reinterpret_cast<uint4 *>(yrow + q * 8) = ov;
                         }
                     }
                 }
@@ -729,9 +734,9 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         }
         if (ms->abort_) break;
         if (ui.last && p.final_) {
-            float *dst = p.final_ + ((int64_t)ui.seq * sh.H + h) * PT * NT + row;
+            float *dst = p.final_ + ((int64_t)ui.seq * sh.H + h) * PT * NT + col0 + row;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) dst[(int64_t)i * NT] = s_run[i];
+            for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = s_run[i];
         }
     }
     // Drain (only non-empty after an early stop): bounded waits for loads and
@@ -739,7 +744,7 @@ k_fused_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     cp_async_wait_all();
     if (tid == 0) bulk_wait0();   // y stores
     for (int b_ = 0; b_ < NBAR; ++b_)
-        for (uint32_t q = done[b_]; q < issued[b_]; ++q) mbar_wait(&ms->bar[b_], q & 1);
+        for (uint32_t q = 0; q < ((pend >> (4 * b_)) & 15u); ++q) mbar_wait(&ms->bar[b_], ((par >> b_) ^ q) & 1u);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
