@@ -83,7 +83,8 @@ typedef enum {
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
-/* Which forward/backward pipeline to run.  AUTO takes the tensor-core path when
+/* Which forward/backward pipeline to run.  AUTO takes the tensor-core path (its single-pass
+ * forward) when
  * chunk_size == 128 and the inputs are bf16 with headdim == 64, dstate == 128 (the
  * compiled tile set; tensors that break its 16-byte rule then return
  * SSD_ERR_MISALIGNED), and the SIMT path when chunk_size == 64 (f32 inputs always
@@ -92,7 +93,10 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 typedef enum {
     SSD_ALGO_AUTO = 0,
     SSD_ALGO_STAGED = 1,   /* SIMT, one kernel per step: cumsum, chunk_state, state_passing, chunk_scan */
-    SSD_ALGO_FUSED = 2     /* tcgen05/TMA single-pass forward; tcgen05 backward */
+    SSD_ALGO_FUSED = 2,    /* tcgen05/TMA single-pass forward (one persistent kernel); tcgen05 backward */
+    SSD_ALGO_SPLIT = 3     /* tcgen05/TMA forward in three launches (chunk states, state passing,
+                              outputs; no waits between CTAs); tcgen05 backward whose state
+                              recompute (when the forward kept none) uses the first two */
 } ssd_algo;
 
 typedef struct {

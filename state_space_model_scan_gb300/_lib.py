@@ -17,7 +17,7 @@ SSD_OK = 0
 STATUS_NAMES = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARGUMENT", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_MISALIGNED",
                 4: "SSD_ERR_WORKSPACE_TOO_SMALL", 5: "SSD_ERR_CUDA", 6: "SSD_ERR_DEVICE_TIMEOUT"}
 SSD_F32, SSD_BF16 = 0, 1
-ALGO = {"auto": 0, "staged": 1, "fused": 2}
+ALGO = {"auto": 0, "staged": 1, "fused": 2, "split": 3}
 
 # Every symbol include/ssd.h declares.
 EXPORTS = ["ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",

@@ -55,6 +55,17 @@ cudaError_t launch_bwd_dstates_tc(const Shape &sh, const int32_t *hdr, const Chu
                                   cudaStream_t st);
 cudaError_t launch_bwd_chunk_tc(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const BwdTcArgs &a,
                                 cudaStream_t st);
+// split_fwd.cu
+cudaError_t launch_split_states(const Shape &sh, int32_t *hdr, const ChunkInfo *chunks, const SeqInfo *seqs,
+                                const void *x, const int64_t *sx, const void *Bp, const int64_t *sb,
+                                const float *dt_raw, int64_t sdb, int64_t sdl, const float *A, const float *bias,
+                                const float *init, float *final_, __nv_bfloat16 *states, float *lam, int sms,
+                                cudaStream_t st);
+cudaError_t launch_split_out(const Shape &sh, int32_t *hdr, const ChunkInfo *chunks, const void *x, const int64_t *sx,
+                             const void *Bp, const int64_t *sb, const void *Cp, const int64_t *sc, const float *dt_raw,
+                             int64_t sdb, int64_t sdl, const float *A, const float *D, const float *bias,
+                             const void *z, const int64_t *sz, void *y, const int64_t *sy,
+                             __nv_bfloat16 *states, int sms, cudaStream_t st);
 cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *units, const void *x, const int64_t *sx,
                              const void *Bp, const int64_t *sb, const void *Cp, const int64_t *sc, const float *dt_raw,
                              int64_t sdb, int64_t sdl, const float *A, const float *D, const float *bias,
@@ -184,7 +195,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     if (L > (int64_t)1 << 30 || B > (int64_t)1 << 20 || H > 65535) return SSD_ERR_UNSUPPORTED;
     if (!pow2_in(p->chunk_size, 16, 256)) return SSD_ERR_UNSUPPORTED;
     if (!pow2_in(P, 16, 128) || !pow2_in(N, 16, 128)) return SSD_ERR_UNSUPPORTED;
-    if (p->algo < SSD_ALGO_AUTO || p->algo > SSD_ALGO_FUSED) return SSD_ERR_INVALID_ARGUMENT;
+    if (p->algo < SSD_ALGO_AUTO || p->algo > SSD_ALGO_SPLIT) return SSD_ERR_INVALID_ARGUMENT;
     if (p->seg_chunks < 0 || p->seg_chunks > 8) return SSD_ERR_INVALID_ARGUMENT;
     if (p->bwd_heads < 0 || p->bwd_heads > 32 || p->reserved0 != 0) return SSD_ERR_INVALID_ARGUMENT;
     const bool varlen = a->cu_seqlens != nullptr;
@@ -236,8 +247,8 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     }
     // The chunk length is the caller's, never replaced: the tensor-core path computes
     // 128-token chunks (one M = 128 tcgen05 tile per chunk), the SIMT path 64-token chunks.
-    bool fused = false;
-    if (p->algo == SSD_ALGO_FUSED) {
+    bool fused = false;   // the tensor-core path (single-pass or split forward)
+    if (p->algo == SSD_ALGO_FUSED || p->algo == SSD_ALGO_SPLIT) {
         if (!tc_ok || p->chunk_size != kTcQ) return SSD_ERR_UNSUPPORTED;
         if (!aligned) return SSD_ERR_MISALIGNED;
         fused = true;
@@ -249,7 +260,10 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     } else if (p->chunk_size != kSimtQ) {
         return SSD_ERR_UNSUPPORTED;
     }
-    pl.algo = fused ? SSD_ALGO_FUSED : SSD_ALGO_STAGED;
+    // AUTO takes the single-pass forward on the tensor-core path (measured faster than the
+    // split forward at every benchmarked shape); SSD_ALGO_SPLIT selects the three-launch one.
+    const bool split = fused && p->algo == SSD_ALGO_SPLIT;
+    pl.algo = split ? SSD_ALGO_SPLIT : fused ? SSD_ALGO_FUSED : SSD_ALGO_STAGED;
     if (a->chunk_states != nullptr) {   // kept chunk states: the tensor-core path's tile format only
         if (!fused) return SSD_ERR_UNSUPPORTED;
         if (((uintptr_t)a->chunk_states) % 16 != 0) return SSD_ERR_MISALIGNED;
@@ -260,7 +274,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     if (kmax > (int64_t)1 << 30) return SSD_ERR_UNSUPPORTED;
     int R = 1, num = 1, den = 1;
     int64_t umax = 0;
-    if (fused) {
+    if (fused && !split) {
         R = p->seg_chunks;
         const int rmax = bwd ? fused_rmax_states() : fused_rmax();
         if (R == 0) {
@@ -299,12 +313,17 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     pl.off_lastunit = lay.take(sizeof(int32_t) * (size_t)S);
     const size_t kh = (size_t)kmax * (size_t)H;
     if (fused) {
-        const size_t uh = (size_t)umax * (size_t)H;
-        pl.off_units = lay.take(sizeof(UnitInfo) * (size_t)umax);
-        pl.off_agg = lay.take(sizeof(float) * uh * (size_t)(P * N));
-        pl.off_incl = lay.take(sizeof(float) * uh * (size_t)(P * N));
-        pl.off_lam = lay.take(sizeof(float) * uh);
-        pl.off_flags = lay.take(sizeof(uint32_t) * uh);
+        if (!split) {   // the single-pass forward's work units and their exchange buffers
+            const size_t uh = (size_t)umax * (size_t)H;
+            pl.off_units = lay.take(sizeof(UnitInfo) * (size_t)umax);
+            pl.off_agg = lay.take(sizeof(float) * uh * (size_t)(P * N));
+            pl.off_incl = lay.take(sizeof(float) * uh * (size_t)(P * N));
+            pl.off_lam = lay.take(sizeof(float) * uh);
+            pl.off_flags = lay.take(sizeof(uint32_t) * uh);
+        } else if (!bwd) {   // the split forward: carried-state tiles (unless kept) and tile log-decays
+            if (a->chunk_states == nullptr) pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * N));
+            pl.off_cs = lay.take(sizeof(float) * kh);
+        }
         if (bwd) {
             pl.hs = p->bwd_heads > 0 ? p->bwd_heads : bwd_heads_per_cta(kmax, H, sh.hpg);
             if (sh.hpg % pl.hs != 0) return SSD_ERR_INVALID_ARGUMENT;
@@ -455,7 +474,7 @@ ssd_status ssd_fwd_debug_layout(const ssd_problem *prob, const ssd_fwd_args *arg
     out->dt = staged ? (int64_t)pl.off_dt : -1;
     out->cs = staged ? (int64_t)pl.off_cs : -1;
     out->states = staged ? (int64_t)pl.off_states : -1;
-    out->units = staged ? -1 : (int64_t)pl.off_units;
+    out->units = pl.algo == SSD_ALGO_FUSED ? (int64_t)pl.off_units : -1;
     out->qi = pl.sh.Q;
     return SSD_OK;
 }
@@ -468,6 +487,30 @@ ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, siz
     cudaStream_t st = (cudaStream_t)stream;
     const Shape &sh = pl.sh;
     float *final_ = (float *)a->final_states.ptr;
+    if (pl.algo == SSD_ALGO_SPLIT) {
+        int32_t *hdr = at<int32_t>(ws, pl.off_hdr);
+        SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
+        ChunkInfo *chunks = at<ChunkInfo>(ws, pl.off_chunks);
+        __nv_bfloat16 *states = a->chunk_states ? static_cast<__nv_bfloat16 *>(a->chunk_states)
+                                                : at<__nv_bfloat16>(ws, pl.off_states);
+        float *lam = at<float>(ws, pl.off_cs);
+        SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, 1, 1, 1, 1, sh.kmax, 0, hdr, seqs, chunks,
+                                   nullptr, at<int32_t>(ws, pl.off_lastunit), nullptr, 0, st));
+        SSD_CUDA(launch_split_states(sh, hdr, chunks, seqs, a->x.ptr, a->x.stride, a->B.ptr, a->B.stride,
+                                     (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1], (const float *)a->A.ptr,
+                                     (const float *)a->dt_bias.ptr, (const float *)a->initial_states.ptr, final_, states,
+                                     lam, num_sms(), st));
+        if (sh.kmax > 0)
+            SSD_CUDA(launch_split_out(sh, hdr, chunks, a->x.ptr, a->x.stride, a->B.ptr, a->B.stride, a->C.ptr,
+                                      a->C.stride, (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1],
+                                      (const float *)a->A.ptr, (const float *)a->D.ptr, (const float *)a->dt_bias.ptr,
+                                      a->z.ptr, a->z.ptr ? a->z.stride : nullptr, a->y.ptr, a->y.stride, states,
+                                      num_sms(), st));
+        if (final_ != nullptr && (pl.varlen || sh.L == 0))
+            SSD_CUDA(launch_empty_seq_final(sh.S, sh.H, sh.P * sh.N, seqs, hdr,
+                                            (const float *)a->initial_states.ptr, final_, st));
+        return SSD_OK;
+    }
     if (pl.algo == SSD_ALGO_FUSED) {
         int32_t *hdr = at<int32_t>(ws, pl.off_hdr);
         SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
@@ -513,7 +556,7 @@ ssd_status ssd_chunk_states_size(const ssd_problem *prob, const ssd_fwd_args *ar
     if (bytes == nullptr) return SSD_ERR_INVALID_ARGUMENT;
     Plan pl;
     SSD_TRY(plan_common(prob, args, false, &pl));
-    if (pl.algo != SSD_ALGO_FUSED) return SSD_ERR_UNSUPPORTED;
+    if (pl.algo == SSD_ALGO_STAGED) return SSD_ERR_UNSUPPORTED;
     *bytes = pl.chunk_state_bytes;
     return SSD_OK;
 }
@@ -534,12 +577,13 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
     cudaStream_t st = (cudaStream_t)stream;
     const Shape &sh = pl.sh;
     const ssd_fwd_args *a = &b->fwd;
-    if (pl.algo == SSD_ALGO_FUSED) {
+    if (pl.algo == SSD_ALGO_FUSED || pl.algo == SSD_ALGO_SPLIT) {
+        const bool split = pl.algo == SSD_ALGO_SPLIT;
         int32_t *hdr = at<int32_t>(ws, pl.off_hdr);
         SeqInfo *seqs = at<SeqInfo>(ws, pl.off_seqs);
         ChunkInfo *chunks = at<ChunkInfo>(ws, pl.off_chunks);
-        UnitInfo *units = at<UnitInfo>(ws, pl.off_units);
-        uint32_t *flags = at<uint32_t>(ws, pl.off_flags);
+        UnitInfo *units = split ? nullptr : at<UnitInfo>(ws, pl.off_units);
+        uint32_t *flags = split ? nullptr : at<uint32_t>(ws, pl.off_flags);
         const bool kept = a->chunk_states != nullptr;   // the forward's chunk states, else recomputed
         __nv_bfloat16 *states = kept ? static_cast<__nv_bfloat16 *>(a->chunk_states) : at<__nv_bfloat16>(ws, pl.off_states);
         float *dS = at<float>(ws, pl.off_dstates), *clam = at<float>(ws, pl.off_cs);
@@ -549,7 +593,12 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
                                    fused_block_units(), sh.kmax, sh.umax, hdr, seqs, chunks, units,
                                    at<int32_t>(ws, pl.off_lastunit), flags, n_zero, st));
         const int64_t tickets = (int64_t)sh.umax * sh.H;
-        if (tickets > 0 && !kept) {
+        if (split && !kept) {   // carried state entering every chunk tile: the split forward's first two launches
+            SSD_CUDA(launch_split_states(sh, hdr, chunks, seqs, a->x.ptr, a->x.stride, a->B.ptr, a->B.stride,
+                                         (const float *)a->dt.ptr, a->dt.stride[0], a->dt.stride[1],
+                                         (const float *)a->A.ptr, (const float *)a->dt_bias.ptr,
+                                         (const float *)a->initial_states.ptr, nullptr, states, clam, num_sms(), st));
+        } else if (tickets > 0 && !kept) {
             // carried state entering every chunk (forward recomputed in states-only mode)
             const int64_t slots = 2LL * num_sms();   // two CTAs per SM
             const int grid = (int)(tickets < slots ? tickets : slots);
