@@ -279,6 +279,46 @@ ssd_status ssd_varlen_metadata(const int32_t *cu_seqlens, int64_t nseqs, int64_t
                                int32_t *seq_idx, int32_t *chunk_begin, int32_t *segments, int32_t *status,
                                void *stream);
 
+/*
+ * Gated RMS normalisation over feature groups -- the normalisation that follows the scan
+ * in a Mamba-2 block (the gated-LayerNorm whose backward the Helion pull request for the
+ * Mamba-2 SSD path times as layer_norm_bwd, "Summary" and "Measurements"; read as RMS
+ * normalisation with the gate applied before it):
+ *
+ *   v[t,i]    = y[t,i] * silu(z[t,i])          (v = y when z is NULL)
+ *   rstd[t,g] = 1 / sqrt(mean_{i in group g} v[t,i]^2 + eps),  group g = features
+ *               [g * group_size, (g+1) * group_size)
+ *   out[t,i]  = v[t,i] * rstd[t, i / group_size] * weight[i]
+ *
+ * Feed it the scan's ungated output (ssd_fwd with z absent) and z; a Mamba-2 block uses
+ * group_size = nheads * headdim / ngroups, so a group is the heads of one B/C group.
+ * Tensors y, z, out, dout, dy, dz: `rows` rows of `width` contiguous features at an element
+ * row stride, all of `dtype` (bf16 or f32), 16-byte aligned with strides a multiple of 8
+ * (else SSD_ERR_MISALIGNED).  weight, dweight: f32 [width]; rstd: f32 [rows][width /
+ * group_size], written by the forward and read by the backward.  group_size must divide
+ * width (else SSD_ERR_INVALID_ARGUMENT) and be a multiple of 8 no larger than 6144 (else
+ * SSD_ERR_UNSUPPORTED).  Buffers are the caller's, device memory; work is enqueued on
+ * `stream`; the weight gradient is summed in a fixed order (bitwise reproducible).
+ */
+typedef struct {
+    int64_t rows, width, group_size;
+    float eps;
+    int32_t dtype;      /* ssd_dtype of y, z, out, dout, dy, dz */
+    int32_t reserved;   /* must be 0 */
+} ssd_norm_problem;
+
+ssd_status ssd_gated_norm_fwd(const ssd_norm_problem *prob, const void *y, int64_t y_stride, const void *z,
+                              int64_t z_stride, const float *weight, void *out, int64_t out_stride, float *rstd,
+                              void *stream);
+/* Gradients of sum(dout * out): dy, dz (when z is given) and dweight; `workspace` (at least
+ * ssd_gated_norm_bwd_workspace_size bytes, 16-byte aligned) holds the weight gradient's
+ * per-row-chunk shares. */
+ssd_status ssd_gated_norm_bwd_workspace_size(const ssd_norm_problem *prob, size_t *bytes);
+ssd_status ssd_gated_norm_bwd(const ssd_norm_problem *prob, const void *y, int64_t y_stride, const void *z,
+                              int64_t z_stride, const float *weight, const float *rstd, const void *dout,
+                              int64_t dout_stride, void *dy, int64_t dy_stride, void *dz, int64_t dz_stride,
+                              float *dweight, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *ssd_status_string(ssd_status status);
 

@@ -22,7 +22,8 @@ ALGO = {"auto": 0, "staged": 1, "fused": 2, "split": 3}
 # Every symbol include/ssd.h declares.
 EXPORTS = ["ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
            "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout", "ssd_fwd_noalloc",
-           "ssd_selftest_bounded_wait", "ssd_chunk_states_size", "ssd_noalloc_query_status", "ssd_varlen_metadata"]
+           "ssd_selftest_bounded_wait", "ssd_chunk_states_size", "ssd_noalloc_query_status", "ssd_varlen_metadata",
+           "ssd_gated_norm_fwd", "ssd_gated_norm_bwd_workspace_size", "ssd_gated_norm_bwd"]
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -56,6 +57,11 @@ _BWD_FIELDS = ["dy", "dfinal_states", "dx", "ddt", "dA", "dB", "dC", "dD", "dz",
 
 class BwdArgs(ctypes.Structure):
     _fields_ = [("fwd", FwdArgs)] + [(n, Tensor) for n in _BWD_FIELDS]
+
+
+class NormProblem(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("width", ctypes.c_int64), ("group_size", ctypes.c_int64),
+                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class DebugLayout(ctypes.Structure):
@@ -92,9 +98,15 @@ def load(path: str = LIB_PATH):
     lib.ssd_varlen_metadata.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p]
+    V, I64 = ctypes.c_void_p, ctypes.c_int64
+    lib.ssd_gated_norm_fwd.argtypes = [P(NormProblem), V, I64, V, I64, V, V, I64, V, V]
+    lib.ssd_gated_norm_bwd_workspace_size.argtypes = [P(NormProblem), P(ctypes.c_size_t)]
+    lib.ssd_gated_norm_bwd.argtypes = [P(NormProblem), V, I64, V, I64, V, V, V, I64, V, I64, V, I64, V, V,
+                                       ctypes.c_size_t, V]
     for f in ("ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
               "ssd_fwd_debug_layout", "ssd_fwd_noalloc", "ssd_selftest_bounded_wait", "ssd_chunk_states_size",
-              "ssd_noalloc_query_status", "ssd_varlen_metadata"):
+              "ssd_noalloc_query_status", "ssd_varlen_metadata", "ssd_gated_norm_fwd",
+              "ssd_gated_norm_bwd_workspace_size", "ssd_gated_norm_bwd"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -243,3 +255,39 @@ def status_string(code):
 
 def abi_version():
     return int(load().ssd_abi_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _rowstride(t):
+    return 0 if t is None else int(t.stride(-2)) if t.dim() >= 2 else int(t.shape[-1])
+
+
+def norm_problem(rows, width, group_size, eps, dtype):
+    return NormProblem(rows, width, group_size, eps, SSD_BF16 if dtype == torch.bfloat16 else SSD_F32, 0)
+
+
+def gated_norm_fwd(prob, y, z, weight, out, rstd, stream=None):
+    """Raw call on 2-D [rows, width] views (row stride = stride(0)); returns the status code."""
+    return int(load().ssd_gated_norm_fwd(ctypes.byref(prob), _ptr(y), _rowstride(y), _ptr(z), _rowstride(z),
+                                         _ptr(weight), _ptr(out), _rowstride(out), _ptr(rstd),
+                                         _stream_handle(stream)))
+
+
+def gated_norm_bwd_workspace_size(prob):
+    n = ctypes.c_size_t(0)
+    check(load().ssd_gated_norm_bwd_workspace_size(ctypes.byref(prob), ctypes.byref(n)),
+          "ssd_gated_norm_bwd_workspace_size")
+    return int(n.value)
+
+
+def gated_norm_bwd(prob, y, z, weight, rstd, dout, dy, dz, dweight, workspace, stream=None):
+    return int(load().ssd_gated_norm_bwd(ctypes.byref(prob), _ptr(y), _rowstride(y), _ptr(z), _rowstride(z),
+                                         _ptr(weight), _ptr(rstd), _ptr(dout), _rowstride(dout), _ptr(dy),
+                                         _rowstride(dy), _ptr(dz), _rowstride(dz), _ptr(dweight),
+                                         _ptr(workspace),
+                                         ctypes.c_size_t(0 if workspace is None else workspace.numel() *
+                                                         workspace.element_size()),
+                                         _stream_handle(stream)))

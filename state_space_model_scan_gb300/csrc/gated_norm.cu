@@ -1,0 +1,314 @@
+// gated_norm.cu -- gated RMS normalisation over feature groups, forward and backward: the
+// normalisation that follows the SSD scan in a Mamba-2 block (the gated-LayerNorm whose
+// backward the Helion pull request for the Mamba-2 SSD path times as layer_norm_bwd,
+// "Measurements"), read as RMS normalisation with the gate applied first:
+//
+//   v = y silu(z)  (v = y without a gate),  rstd[t,g] = 1/sqrt(mean_{i in g} v[t,i]^2 + eps),
+//   out[t,i] = v[t,i] rstd[t,g(i)] w[i]
+//
+// and its exact derivative.  Memory-bound: one warp per (row, group) item, each lane eight
+// consecutive features per 16-byte (bf16) or 32-byte (fp32) access; the backward's weight
+// gradient is summed in a fixed order (per-warp shared-memory rows, then row chunks), so
+// every result is bitwise reproducible.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr int NW = 8;                 // warps per block
+constexpr int64_t kMaxGroup = 6144;   // features per group at most (backward: NW rows of it in shared memory)
+
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float *v) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const __nv_bfloat162 *e = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(e[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void load8(const float *p, float *v) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float *v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void store8(float *p, const float *v) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+struct NormArgs {
+    int64_t rows, width, G;   // G = features per group
+    int ng;                   // groups per row
+    float eps;
+    const void *y, *z, *dout;
+    int64_t sy, sz, sdout;
+    const float *w, *rstd_in;
+    void *out, *dy, *dz;
+    int64_t sout, sdy, sdz;
+    float *rstd;
+    float *partials;          // [row chunk][width] (backward)
+    int64_t rows_per_chunk;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(NW * 32)
+k_norm_fwd(const NormArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t items = a.rows * a.ng, nw = (int64_t)gridDim.x * NW;
+    const int pieces = (int)(a.G / 8);
+    for (int64_t it = (int64_t)blockIdx.x * NW + (threadIdx.x >> 5); it < items; it += nw) {
+        const int64_t r = it / a.ng;
+        const int g = (int)(it - r * a.ng);
+        const T *yr = static_cast<const T *>(a.y) + r * a.sy + (int64_t)g * a.G;
+        const T *zr = a.z ? static_cast<const T *>(a.z) + r * a.sz + (int64_t)g * a.G : nullptr;
+        float ss = 0.f;
+        for (int j = lane; j < pieces; j += 32) {
+            float v[8];
+            load8(yr + 8 * j, v);
+            if (zr) {
+                float zz[8];
+                load8(zr + 8 * j, zz);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sigmoid_f(zz[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+        }
+        ss = warp_sum(ss);
+        const float rs = 1.f / sqrtf(ss / (float)a.G + a.eps);
+        if (lane == 0) a.rstd[r * a.ng + g] = rs;
+        T *orow = static_cast<T *>(a.out) + r * a.sout + (int64_t)g * a.G;
+        const float *wr = a.w + (int64_t)g * a.G;
+        for (int j = lane; j < pieces; j += 32) {   // the warp just read these lines: cache hits
+            float v[8], wv[8];
+            load8(yr + 8 * j, v);
+            if (zr) {
+                float zz[8];
+                load8(zr + 8 * j, zz);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sigmoid_f(zz[e]);
+            }
+            load8(wr + 8 * j, wv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = v[e] * rs * wv[e];
+            store8(orow + 8 * j, v);
+        }
+    }
+}
+
+// grid (row chunks, groups), NW warps: warp w takes rows chunk_start + w, + NW, ...; its share
+// of dw for the group's columns accumulates in its own shared-memory row, the rows are summed
+// in warp order at the end, and k_norm_dw sums the row chunks in order.
+template <typename T>
+__global__ void __launch_bounds__(NW * 32)
+k_norm_bwd(const NormArgs a) {
+    extern __shared__ float acc[];   // [NW][G]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = blockIdx.y;
+    const int pieces = (int)(a.G / 8);
+    float *mine = acc + (int64_t)warp * a.G;
+    for (int64_t i = lane; i < a.G; i += 32) mine[i] = 0.f;
+    const int64_t r0 = (int64_t)blockIdx.x * a.rows_per_chunk, r1 = std::min(a.rows, r0 + a.rows_per_chunk);
+    const float *wr = a.w + (int64_t)g * a.G;
+    for (int64_t r = r0 + warp; r < r1; r += NW) {
+        const T *yr = static_cast<const T *>(a.y) + r * a.sy + (int64_t)g * a.G;
+        const T *zr = a.z ? static_cast<const T *>(a.z) + r * a.sz + (int64_t)g * a.G : nullptr;
+        const T *dr = static_cast<const T *>(a.dout) + r * a.sdout + (int64_t)g * a.G;
+        const float rs = a.rstd_in[r * a.ng + g];
+        float dot = 0.f;   // sum_i (dout w)_i vhat_i
+        for (int j = lane; j < pieces; j += 32) {
+            float v[8], d[8], wv[8];
+            load8(yr + 8 * j, v);
+            if (zr) {
+                float zz[8];
+                load8(zr + 8 * j, zz);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sigmoid_f(zz[e]);
+            }
+            load8(dr + 8 * j, d);
+            load8(wr + 8 * j, wv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dot = fmaf(d[e] * wv[e], v[e] * rs, dot);
+        }
+        dot = warp_sum(dot) / (float)a.G;
+        T *dyr = static_cast<T *>(a.dy) + r * a.sdy + (int64_t)g * a.G;
+        T *dzr = a.z ? static_cast<T *>(a.dz) + r * a.sdz + (int64_t)g * a.G : nullptr;
+        for (int j = lane; j < pieces; j += 32) {
+            float y8[8], d[8], wv[8], z8[8], sg[8], s[8];
+            load8(yr + 8 * j, y8);
+            if (zr) {
+                load8(zr + 8 * j, z8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    sg[e] = sigmoid_f(z8[e]);
+                    s[e] = z8[e] * sg[e];
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[e] = 1.f;
+            }
+            load8(dr + 8 * j, d);
+            load8(wr + 8 * j, wv);
+            float o1[8], o2[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float vhat = y8[e] * s[e] * rs;
+                const float dv = rs * (d[e] * wv[e] - vhat * dot);
+                o1[e] = dv * s[e];                                                       // dy
+                if (zr) o2[e] = dv * y8[e] * sg[e] * (1.f + z8[e] * (1.f - sg[e]));     // dz
+                mine[8 * j + e] += d[e] * vhat;                                          // dw share
+            }
+            store8(dyr + 8 * j, o1);
+            if (zr) store8(dzr + 8 * j, o2);
+        }
+    }
+    __syncthreads();
+    float *dst = a.partials + (int64_t)blockIdx.x * a.width + (int64_t)g * a.G;
+    for (int64_t i = threadIdx.x; i < a.G; i += blockDim.x) {
+        float s = 0.f;
+        for (int w = 0; w < NW; ++w) s += acc[(int64_t)w * a.G + i];
+        dst[i] = s;
+    }
+}
+
+__global__ void k_norm_dw(const float *partials, int64_t chunks, int64_t width, float *dw) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < width; i += (int64_t)gridDim.x * blockDim.x) {
+        float s = 0.f;
+        for (int64_t c = 0; c < chunks; ++c) s += partials[c * width + i];
+        dw[i] = s;
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p) % 16 == 0; }
+
+// Shared checks of both directions; *chunks = the backward's row chunks.
+ssd_status check_norm(const ssd_norm_problem *p, int64_t *chunks) {
+    if (p == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    if (p->rows < 0 || p->width < 1 || p->group_size < 1 || p->width % p->group_size != 0)
+        return SSD_ERR_INVALID_ARGUMENT;
+    if (!(p->eps >= 0.f) || p->dtype < SSD_F32 || p->dtype > SSD_BF16 || p->reserved != 0)
+        return SSD_ERR_INVALID_ARGUMENT;
+    if (p->group_size % 8 != 0 || p->group_size > kMaxGroup || p->rows > ((int64_t)1 << 31) ||
+        p->width > ((int64_t)1 << 24))
+        return SSD_ERR_UNSUPPORTED;
+    const int64_t ng = p->width / p->group_size;
+    const int64_t want = std::max<int64_t>(1, (4 * (int64_t)sm_count() + ng - 1) / ng);
+    *chunks = std::max<int64_t>(1, std::min<int64_t>(p->rows, want));
+    return SSD_OK;
+}
+
+// A row-major [rows, width] tensor with element row stride `stride`.
+ssd_status check_rows(const ssd_norm_problem *p, const void *t, int64_t stride, bool required) {
+    if (t == nullptr) return required && p->rows > 0 ? SSD_ERR_INVALID_ARGUMENT : SSD_OK;
+    if (p->rows > 1 && stride < p->width) return SSD_ERR_INVALID_ARGUMENT;
+    if (!aligned16(t) || stride % 8 != 0) return SSD_ERR_MISALIGNED;
+    return SSD_OK;
+}
+
+#define NORM_TRY(expr)                 \
+    do {                               \
+        ssd_status _s = (expr);        \
+        if (_s != SSD_OK) return _s;   \
+    } while (0)
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+ssd_status ssd_gated_norm_fwd(const ssd_norm_problem *p, const void *y, int64_t y_stride, const void *z,
+                              int64_t z_stride, const float *weight, void *out, int64_t out_stride, float *rstd,
+                              void *stream) {
+    int64_t chunks = 0;
+    NORM_TRY(check_norm(p, &chunks));
+    NORM_TRY(check_rows(p, y, y_stride, true));
+    NORM_TRY(check_rows(p, z, z_stride, false));
+    NORM_TRY(check_rows(p, out, out_stride, true));
+    if (p->rows > 0 && (weight == nullptr || rstd == nullptr)) return SSD_ERR_INVALID_ARGUMENT;
+    if (weight != nullptr && !aligned16(weight)) return SSD_ERR_MISALIGNED;
+    if (p->rows == 0) return SSD_OK;
+    NormArgs a{};
+    a.rows = p->rows; a.width = p->width; a.G = p->group_size; a.ng = (int)(p->width / p->group_size);
+    a.eps = p->eps; a.y = y; a.z = z; a.sy = y_stride; a.sz = z_stride; a.w = weight; a.out = out;
+    a.sout = out_stride; a.rstd = rstd;
+    const int64_t items = p->rows * a.ng;
+    const int blocks = (int)std::min<int64_t>((items + NW - 1) / NW, 8LL * sm_count());
+    cudaStream_t st = (cudaStream_t)stream;
+    if (p->dtype == SSD_BF16)
+        k_norm_fwd<__nv_bfloat16><<<blocks, NW * 32, 0, st>>>(a);
+    else
+        k_norm_fwd<float><<<blocks, NW * 32, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status ssd_gated_norm_bwd_workspace_size(const ssd_norm_problem *p, size_t *bytes) {
+    if (bytes == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    int64_t chunks = 0;
+    NORM_TRY(check_norm(p, &chunks));
+    *bytes = (size_t)chunks * (size_t)p->width * sizeof(float);
+    return SSD_OK;
+}
+
+ssd_status ssd_gated_norm_bwd(const ssd_norm_problem *p, const void *y, int64_t y_stride, const void *z,
+                              int64_t z_stride, const float *weight, const float *rstd, const void *dout,
+                              int64_t dout_stride, void *dy, int64_t dy_stride, void *dz, int64_t dz_stride,
+                              float *dweight, void *workspace, size_t workspace_bytes, void *stream) {
+    int64_t chunks = 0;
+    NORM_TRY(check_norm(p, &chunks));
+    NORM_TRY(check_rows(p, y, y_stride, true));
+    NORM_TRY(check_rows(p, z, z_stride, false));
+    NORM_TRY(check_rows(p, dout, dout_stride, true));
+    NORM_TRY(check_rows(p, dy, dy_stride, true));
+    NORM_TRY(check_rows(p, dz, dz_stride, z != nullptr));
+    if (weight == nullptr || dweight == nullptr || (p->rows > 0 && rstd == nullptr)) return SSD_ERR_INVALID_ARGUMENT;
+    if (!aligned16(weight)) return SSD_ERR_MISALIGNED;
+    const size_t need = (size_t)chunks * (size_t)p->width * sizeof(float);
+    if (workspace == nullptr || workspace_bytes < need) return SSD_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = (cudaStream_t)stream;
+    NormArgs a{};
+    a.rows = p->rows; a.width = p->width; a.G = p->group_size; a.ng = (int)(p->width / p->group_size);
+    a.eps = p->eps; a.y = y; a.z = z; a.dout = dout; a.sy = y_stride; a.sz = z_stride; a.sdout = dout_stride;
+    a.w = weight; a.rstd_in = rstd; a.dy = dy; a.dz = dz; a.sdy = dy_stride; a.sdz = dz_stride;
+    a.partials = static_cast<float *>(workspace);
+    a.rows_per_chunk = p->rows > 0 ? (p->rows + chunks - 1) / chunks : 1;
+    const size_t smem = (size_t)NW * (size_t)p->group_size * sizeof(float);
+    const dim3 grid((unsigned)chunks, (unsigned)a.ng);
+    cudaError_t e;
+    if (p->dtype == SSD_BF16) {
+        static int attr[64] = {0};
+        e = ensure_smem_attr(k_norm_bwd<__nv_bfloat16>, (int)smem, attr);
+        if (e == cudaSuccess) k_norm_bwd<__nv_bfloat16><<<grid, NW * 32, smem, st>>>(a);
+    } else {
+        static int attr[64] = {0};
+        e = ensure_smem_attr(k_norm_bwd<float>, (int)smem, attr);
+        if (e == cudaSuccess) k_norm_bwd<float><<<grid, NW * 32, smem, st>>>(a);
+    }
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
+    const int blocks = (int)std::min<int64_t>((p->width + 255) / 256, 1024);
+    k_norm_dw<<<blocks, 256, 0, st>>>(a.partials, chunks, p->width, dweight);
+    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // extern "C"

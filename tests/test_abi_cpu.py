@@ -346,3 +346,37 @@ def test_fwd_accepts_five_chunk_units(lib):
     assert ws_size(p, a)[0] == 0
     p.seg_chunks = 6
     assert ws_size(p, a)[0] == 2
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("width", 0, 1), ("group_size", 0, 1), ("group_size", 7, 1),     # 7 does not divide 4096
+    ("group_size", 12, 2),                                           # not a multiple of 8 (divides 4092? no: width 48 below)
+    ("group_size", 8192, 2), ("eps", -1.0, 1), ("dtype", 5, 1), ("reserved", 1, 1), ("rows", -1, 1),
+])
+def test_gated_norm_validation(lib, field, value, code):
+    """Host-side checks of the gated normalisation entry points (nothing reaches the device)."""
+    m = lib_mod()
+    p = m.NormProblem(16, 48 if field == "group_size" and value == 12 else 4096, 512, 1e-5, m.SSD_BF16, 0)
+    if field == "group_size" and value == 8192:
+        p.width = 8192
+    setattr(p, field, value)
+    n = ctypes.c_size_t(0)
+    assert m.load().ssd_gated_norm_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == code
+    d = ctypes.c_void_p(0x100000)
+    assert m.load().ssd_gated_norm_fwd(ctypes.byref(p), d, 4096, None, 0, d, d, 4096, d, None) == code
+
+
+def test_gated_norm_pointer_checks(lib):
+    m = lib_mod()
+    p = m.NormProblem(16, 4096, 512, 1e-5, m.SSD_BF16, 0)
+    d = ctypes.c_void_p(0x100000)
+    f = m.load().ssd_gated_norm_fwd
+    assert f(ctypes.byref(p), None, 4096, None, 0, d, d, 4096, d, None) == 1               # y required
+    assert f(ctypes.byref(p), ctypes.c_void_p(0x100008), 4096, None, 0, d, d, 4096, d, None) == 3   # 16-byte rule
+    assert f(ctypes.byref(p), d, 4100, None, 0, d, d, 4096, d, None) == 3                  # stride % 8
+    assert f(ctypes.byref(p), d, 100, None, 0, d, d, 4096, d, None) == 1                   # stride < width
+    n = ctypes.c_size_t(0)
+    assert m.load().ssd_gated_norm_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0 and n.value > 0
+    b = m.load().ssd_gated_norm_bwd
+    assert b(ctypes.byref(p), d, 4096, None, 0, d, d, d, 4096, d, 4096, None, 0, d, d, ctypes.c_size_t(n.value - 4),
+             None) == 4                                                                    # workspace too small
