@@ -319,6 +319,45 @@ ssd_status ssd_gated_norm_bwd(const ssd_norm_problem *prob, const void *y, int64
                               int64_t dout_stride, void *dy, int64_t dy_stride, void *dz, int64_t dz_stride,
                               float *dweight, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Causal depthwise convolution over the sequence axis with an optional SiLU -- the step
+ * before the scan in a Mamba-2 block, run on the packed xBC = [x | B | C] channels (the
+ * Helion pull request for the Mamba-2 SSD path, "Summary": mamba_split_conv1d_scan_combined;
+ * "Testing": x, B and C are views of one packed buffer):
+ *
+ *   pre[t,c] = bias[c] + sum_{k<width} weight[c][k] * u[t - (width-1) + k][c]
+ *   out[t,c] = silu(pre[t,c])   (activation 1)   or   pre[t,c]   (activation 0)
+ *
+ * with u := 0 before the start of t's sequence (a batch row, or with cu_seqlens -- int32
+ * [nseqs + 1], device, batch 1 -- a packed sequence): a window never reaches into another
+ * sequence.  The scan then reads x, B and C as strided views of out (ssd_tensor strides), so
+ * the split costs no copy.  Token tensors u, out, dout, du: [batch][seqlen][channels], channels
+ * contiguous, at element strides (per batch row, per token), of `dtype` (bf16 or f32),
+ * 16-byte aligned with strides a multiple of 8 (else SSD_ERR_MISALIGNED); weight, dweight: f32
+ * [channels][width]; bias, dbias: f32 [channels] (optional).  width 1..8 and channels a
+ * multiple of 8 (else SSD_ERR_UNSUPPORTED).  cu_seqlens contents are not validated here
+ * (ssd_varlen_metadata reports bad ones); bad ones give unspecified values, yet every access
+ * stays inside the tensors described above.  The backward gives du, dweight and dbias (sums over
+ * tokens in a fixed order: bitwise reproducible) and needs `workspace` of
+ * ssd_conv1d_bwd_workspace_size bytes, 16-byte aligned.
+ */
+typedef struct {
+    int64_t batch, seqlen, channels, width, nseqs;   /* nseqs: packed sequences (cu_seqlens), else 0 */
+    int32_t dtype, activation;                       /* ssd_dtype; 0 none, 1 silu */
+    int32_t reserved, pad;                           /* reserved must be 0 */
+} ssd_conv_problem;
+
+ssd_status ssd_conv1d_fwd(const ssd_conv_problem *prob, const void *u, int64_t u_batch_stride,
+                          int64_t u_token_stride, const float *weight, const float *bias,
+                          const int32_t *cu_seqlens, void *out, int64_t out_batch_stride,
+                          int64_t out_token_stride, void *stream);
+ssd_status ssd_conv1d_bwd_workspace_size(const ssd_conv_problem *prob, size_t *bytes);
+ssd_status ssd_conv1d_bwd(const ssd_conv_problem *prob, const void *u, int64_t u_batch_stride,
+                          int64_t u_token_stride, const float *weight, const float *bias,
+                          const int32_t *cu_seqlens, const void *dout, int64_t dout_batch_stride,
+                          int64_t dout_token_stride, void *du, int64_t du_batch_stride, int64_t du_token_stride,
+                          float *dweight, float *dbias, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *ssd_status_string(ssd_status status);
 

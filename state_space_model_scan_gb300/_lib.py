@@ -23,7 +23,8 @@ ALGO = {"auto": 0, "staged": 1, "fused": 2, "split": 3}
 EXPORTS = ["ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
            "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout", "ssd_fwd_noalloc",
            "ssd_selftest_bounded_wait", "ssd_chunk_states_size", "ssd_noalloc_query_status", "ssd_varlen_metadata",
-           "ssd_gated_norm_fwd", "ssd_gated_norm_bwd_workspace_size", "ssd_gated_norm_bwd"]
+           "ssd_gated_norm_fwd", "ssd_gated_norm_bwd_workspace_size", "ssd_gated_norm_bwd",
+           "ssd_conv1d_fwd", "ssd_conv1d_bwd_workspace_size", "ssd_conv1d_bwd"]
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -62,6 +63,12 @@ class BwdArgs(ctypes.Structure):
 class NormProblem(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int64), ("width", ctypes.c_int64), ("group_size", ctypes.c_int64),
                 ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class ConvProblem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("channels", ctypes.c_int64),
+                ("width", ctypes.c_int64), ("nseqs", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("activation", ctypes.c_int32), ("reserved", ctypes.c_int32), ("pad", ctypes.c_int32)]
 
 
 class DebugLayout(ctypes.Structure):
@@ -103,10 +110,15 @@ def load(path: str = LIB_PATH):
     lib.ssd_gated_norm_bwd_workspace_size.argtypes = [P(NormProblem), P(ctypes.c_size_t)]
     lib.ssd_gated_norm_bwd.argtypes = [P(NormProblem), V, I64, V, I64, V, V, V, I64, V, I64, V, I64, V, V,
                                        ctypes.c_size_t, V]
+    lib.ssd_conv1d_fwd.argtypes = [P(ConvProblem), V, I64, I64, V, V, V, V, I64, I64, V]
+    lib.ssd_conv1d_bwd_workspace_size.argtypes = [P(ConvProblem), P(ctypes.c_size_t)]
+    lib.ssd_conv1d_bwd.argtypes = [P(ConvProblem), V, I64, I64, V, V, V, V, I64, I64, V, I64, I64, V, V, V,
+                                   ctypes.c_size_t, V]
     for f in ("ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
               "ssd_fwd_debug_layout", "ssd_fwd_noalloc", "ssd_selftest_bounded_wait", "ssd_chunk_states_size",
               "ssd_noalloc_query_status", "ssd_varlen_metadata", "ssd_gated_norm_fwd",
-              "ssd_gated_norm_bwd_workspace_size", "ssd_gated_norm_bwd"):
+              "ssd_gated_norm_bwd_workspace_size", "ssd_gated_norm_bwd", "ssd_conv1d_fwd",
+              "ssd_conv1d_bwd_workspace_size", "ssd_conv1d_bwd"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -291,3 +303,33 @@ def gated_norm_bwd(prob, y, z, weight, rstd, dout, dy, dz, dweight, workspace, s
                                          ctypes.c_size_t(0 if workspace is None else workspace.numel() *
                                                          workspace.element_size()),
                                          _stream_handle(stream)))
+
+
+def conv_problem(batch, seqlen, channels, width, nseqs, dtype, silu):
+    return ConvProblem(batch, seqlen, channels, width, nseqs, SSD_BF16 if dtype == torch.bfloat16 else SSD_F32,
+                       1 if silu else 0, 0, 0)
+
+
+def _bl(t):
+    """(batch stride, token stride) of a [batch, seqlen, channels] tensor."""
+    return (0, 0) if t is None else (int(t.stride(0)), int(t.stride(1)))
+
+
+def conv1d_fwd(prob, u, weight, bias, cu_seqlens, out, stream=None):
+    """Raw call on [batch, seqlen, channels] tensors; returns the status code."""
+    return int(load().ssd_conv1d_fwd(ctypes.byref(prob), _ptr(u), *_bl(u), _ptr(weight), _ptr(bias),
+                                     _ptr(cu_seqlens), _ptr(out), *_bl(out), _stream_handle(stream)))
+
+
+def conv1d_bwd_workspace_size(prob):
+    n = ctypes.c_size_t(0)
+    check(load().ssd_conv1d_bwd_workspace_size(ctypes.byref(prob), ctypes.byref(n)), "ssd_conv1d_bwd_workspace_size")
+    return int(n.value)
+
+
+def conv1d_bwd(prob, u, weight, bias, cu_seqlens, dout, du, dweight, dbias, workspace, stream=None):
+    return int(load().ssd_conv1d_bwd(ctypes.byref(prob), _ptr(u), *_bl(u), _ptr(weight), _ptr(bias),
+                                     _ptr(cu_seqlens), _ptr(dout), *_bl(dout), _ptr(du), *_bl(du), _ptr(dweight),
+                                     _ptr(dbias), _ptr(workspace),
+                                     ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                     _stream_handle(stream)))

@@ -134,6 +134,42 @@ def gated_norm_backward(y, weight, rstd, dout, group_size, z=None, eps=1e-5, str
     return dy.reshape(y.shape), (dz.reshape(z.shape) if dz is not None else None), dw
 
 
+def conv1d_forward(xbc, weight, bias=None, cu_seqlens=None, silu=True, stream=None):
+    """Causal depthwise conv1d (+ SiLU) over the sequence axis of xbc [batch, seqlen, channels]
+    (see include/ssd.h, ssd_conv1d_fwd); packed sequences (cu_seqlens, batch 1) never mix."""
+    Bsz, L, Cn = xbc.shape
+    out = torch.empty(Bsz, L, Cn, dtype=xbc.dtype, device=xbc.device)
+    prob = _lib.conv_problem(Bsz, L, Cn, weight.shape[1], 0 if cu_seqlens is None else cu_seqlens.numel() - 1,
+                             xbc.dtype, silu)
+    _lib.check(_lib.conv1d_fwd(prob, xbc, weight, bias, cu_seqlens, out, stream), "ssd_conv1d_fwd")
+    return out
+
+
+def conv1d_backward(xbc, weight, dout, bias=None, cu_seqlens=None, silu=True, stream=None):
+    """dxbc, dweight, dbias (None without bias): gradients of sum(dout * conv1d_forward(...))."""
+    Bsz, L, Cn = xbc.shape
+    du = torch.empty(Bsz, L, Cn, dtype=xbc.dtype, device=xbc.device)
+    dw = torch.empty_like(weight)
+    db = torch.empty_like(bias) if bias is not None else None
+    prob = _lib.conv_problem(Bsz, L, Cn, weight.shape[1], 0 if cu_seqlens is None else cu_seqlens.numel() - 1,
+                             xbc.dtype, silu)
+    ws = torch.empty(max(_lib.conv1d_bwd_workspace_size(prob), 16), dtype=torch.uint8, device=xbc.device)
+    _lib.check(_lib.conv1d_bwd(prob, xbc, weight, bias, cu_seqlens, dout, du, dw, db, ws, stream), "ssd_conv1d_bwd")
+    return du, dw, db
+
+
+def split_xbc(xbc, nheads, headdim, ngroups, dstate):
+    """x [B, L, H, P], B and C [B, L, G, N] as views of the packed xbc [B, L, H P + 2 G N] (no copy);
+    the scan takes them as they are (strided tensors)."""
+    Bsz, L, Cn = xbc.shape
+    hp, gn = nheads * headdim, ngroups * dstate
+    assert Cn == hp + 2 * gn
+    x = xbc[..., :hp].unflatten(-1, (nheads, headdim))
+    Bm = xbc[..., hp:hp + gn].unflatten(-1, (ngroups, dstate))
+    Cm = xbc[..., hp + gn:].unflatten(-1, (ngroups, dstate))
+    return x, Bm, Cm
+
+
 class SSDFunction(torch.autograd.Function):
     """Autograd wrapper: forward and backward both run in libssd.so.  On the tensor-core
     path the forward keeps its carried chunk states for the backward."""

@@ -380,3 +380,51 @@ def test_gated_norm_pointer_checks(lib):
     b = m.load().ssd_gated_norm_bwd
     assert b(ctypes.byref(p), d, 4096, None, 0, d, d, d, 4096, d, 4096, None, 0, d, d, ctypes.c_size_t(n.value - 4),
              None) == 4                                                                    # workspace too small
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("batch", 0, 1), ("seqlen", -1, 1), ("channels", 0, 1), ("width", 0, 1), ("reserved", 1, 1),
+    ("dtype", 7, 1), ("activation", 2, 1), ("nseqs", 3, 1),       # nseqs without cu_seqlens
+    ("width", 9, 2), ("channels", 20, 2),                          # width 1..8, channels % 8
+])
+def test_conv1d_validation(lib, field, value, code):
+    """Host-side checks of the conv1d entry points (nothing reaches the device)."""
+    m = lib_mod()
+    p = m.ConvProblem(2, 64, 64, 4, 0, m.SSD_BF16, 1, 0, 0)
+    setattr(p, field, value)
+    n = ctypes.c_size_t(0)
+    assert m.load().ssd_conv1d_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == code
+    d = ctypes.c_void_p(0x100000)
+    assert m.load().ssd_conv1d_fwd(ctypes.byref(p), d, 64 * 64, 64, d, None, None, d, 64 * 64, 64, None) == code
+
+
+def test_conv1d_pointer_and_layout_checks(lib):
+    m = lib_mod()
+    p = m.ConvProblem(2, 64, 64, 4, 0, m.SSD_BF16, 1, 0, 0)
+    d = ctypes.c_void_p(0x100000)
+    f = m.load().ssd_conv1d_fwd
+    assert f(ctypes.byref(p), None, 4096, 64, d, None, None, d, 4096, 64, None) == 1        # u required
+    assert f(ctypes.byref(p), d, 4096, 64, None, None, None, d, 4096, 64, None) == 1        # weight required
+    assert f(ctypes.byref(p), ctypes.c_void_p(0x100008), 4096, 64, d, None, None, d, 4096, 64, None) == 3
+    assert f(ctypes.byref(p), d, 4096, 60, d, None, None, d, 4096, 64, None) == 1           # token stride < channels
+    assert f(ctypes.byref(p), d, 4096, 72 + 4, d, None, None, d, 4096, 64, None) == 1       # rows overlap
+    assert f(ctypes.byref(p), d, 64 * 76, 76, d, None, None, d, 4096, 64, None) == 3        # stride % 8
+    # packed sequences: batch 1 and nseqs >= 1
+    p2 = m.ConvProblem(2, 64, 64, 4, 2, m.SSD_BF16, 1, 0, 0)
+    assert f(ctypes.byref(p2), d, 4096, 64, d, None, d, d, 4096, 64, None) == 1
+    p2.batch, p2.nseqs = 1, 0
+    assert f(ctypes.byref(p2), d, 4096, 64, d, None, d, d, 4096, 64, None) == 1
+    # empty sequence: nothing to check or launch
+    p3 = m.ConvProblem(1, 0, 64, 4, 0, m.SSD_F32, 0, 0, 0)
+    assert f(ctypes.byref(p3), None, 0, 0, d, None, None, None, 0, 0, None) == 0
+    n = ctypes.c_size_t(0)
+    assert m.load().ssd_conv1d_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    assert n.value == 2 * 1 * 64 * 5 * 4                     # 2 rows x 1 tile of 64 tokens x channels x (width+1) f32
+    b = m.load().ssd_conv1d_bwd
+    args = lambda ws, nb, dw=d, db=None, bias=None: (ctypes.byref(p), d, 4096, 64, d, bias, None, d, 4096, 64,
+                                                     d, 4096, 64, dw, db, ws, ctypes.c_size_t(nb), None)
+    assert b(*args(d, n.value - 4)) == 4                     # workspace too small
+    assert b(*args(None, n.value)) == 4
+    assert b(*args(ctypes.c_void_p(0x100004), n.value)) == 3
+    assert b(*args(d, n.value, dw=None)) == 1                # dweight required
+    assert b(*args(d, n.value, bias=d)) == 1                 # bias given, dbias missing
