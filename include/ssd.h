@@ -364,6 +364,44 @@ const char *ssd_status_string(ssd_status status);
 /* SSD_ABI_VERSION of the built library. */
 int32_t ssd_abi_version(void);
 
+/* ------------------------------------------------------------------------------------------
+ * Complex-A SSD scan, forward (the Mamba-3-Lite variant: Mamba-3-Lite "SSD Reference --
+ * complex scan API & kernel contract", sections "Math: the recurrence both functions
+ * implement", "ssd_naive_complex", "ssd_complex_chunkwise" and its shape table).
+ *
+ * Per batch row b and head h, with abar_t = exp(softplus(dt[b,t,h]) * A[h]) (A complex, dt
+ * real, no bias) and a complex state h_t [headdim][dstate]:
+ *
+ *   h_t = abar_t h_{t-1} + x_t (outer) B_t,   y_t[d] = sum_n C_t[n] h_t[d][n]
+ *
+ * from h_{-1} = initial_states[b,h] (zero when NULL).  No dt factor on the input and no
+ * conjugation (C and B enter bilinearly).  y_real = Re y, y_imag = Im y (optional: NULL skips
+ * it), final_states = h_{T-1} (optional).  One exact function: the chunking (chunk_size
+ * positions per tile) changes only rounding order.
+ *
+ * Layouts (all contiguous, element offsets; complex = interleaved (re, im) fp32 pairs, the
+ * layout of a complex64 tensor): x [batch][seqlen][nheads][headdim] complex; B, C
+ * [batch][seqlen][nheads][dstate] complex (one projection per head); dt [batch][seqlen]
+ * [nheads] f32; A [nheads] complex; initial/final_states [batch][nheads][headdim][dstate]
+ * complex; y_real, y_imag [batch][seqlen][nheads][headdim] f32.  x, B, C, y_*, the states
+ * and the workspace 16-byte aligned (else SSD_ERR_MISALIGNED).
+ *
+ * Compiled set: headdim = dstate = chunk_size = 64 (the 434M Mamba-3-Lite configuration of
+ * the page), else SSD_ERR_UNSUPPORTED.  The contractions run on the tensor cores in tf32
+ * (10-bit mantissa operands, fp32 accumulation), the decays, the carried state and the
+ * outputs in fp32.  `workspace` (>= ssd_complex_fwd_workspace_size bytes, caller-owned)
+ * holds the status header that ssd_query_status reads; stream-ordered, no allocation.
+ */
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, dstate, chunk_size;
+} ssd_complex_problem;
+
+ssd_status ssd_complex_fwd_workspace_size(const ssd_complex_problem *prob, size_t *bytes);
+ssd_status ssd_complex_fwd(const ssd_complex_problem *prob, const void *x, const float *dt, const void *A,
+                           const void *B, const void *C, const void *initial_states, float *y_real,
+                           float *y_imag, void *final_states, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
 /*
  * ssd_fwd_debug_layout
  * Byte offsets, inside an ssd_fwd workspace, of the intermediates the STAGED

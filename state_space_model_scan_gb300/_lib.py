@@ -24,7 +24,8 @@ EXPORTS = ["ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_b
            "ssd_status_string", "ssd_abi_version", "ssd_fwd_debug_layout", "ssd_fwd_noalloc",
            "ssd_selftest_bounded_wait", "ssd_chunk_states_size", "ssd_noalloc_query_status", "ssd_varlen_metadata",
            "ssd_gated_norm_fwd", "ssd_gated_norm_bwd_workspace_size", "ssd_gated_norm_bwd",
-           "ssd_conv1d_fwd", "ssd_conv1d_bwd_workspace_size", "ssd_conv1d_bwd"]
+           "ssd_conv1d_fwd", "ssd_conv1d_bwd_workspace_size", "ssd_conv1d_bwd",
+           "ssd_complex_fwd_workspace_size", "ssd_complex_fwd"]
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -71,6 +72,11 @@ class ConvProblem(ctypes.Structure):
                 ("activation", ctypes.c_int32), ("reserved", ctypes.c_int32), ("pad", ctypes.c_int32)]
 
 
+class ComplexProblem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("chunk_size", ctypes.c_int64)]
+
+
 class DebugLayout(ctypes.Structure):
     _fields_ = [("meta_counts", ctypes.c_int64), ("chunk_info", ctypes.c_int64), ("dt", ctypes.c_int64),
                 ("cs", ctypes.c_int64), ("states", ctypes.c_int64), ("units", ctypes.c_int64),
@@ -114,11 +120,14 @@ def load(path: str = LIB_PATH):
     lib.ssd_conv1d_bwd_workspace_size.argtypes = [P(ConvProblem), P(ctypes.c_size_t)]
     lib.ssd_conv1d_bwd.argtypes = [P(ConvProblem), V, I64, I64, V, V, V, V, I64, I64, V, I64, I64, V, V, V,
                                    ctypes.c_size_t, V]
+    lib.ssd_complex_fwd_workspace_size.argtypes = [P(ComplexProblem), P(ctypes.c_size_t)]
+    lib.ssd_complex_fwd.argtypes = [P(ComplexProblem), V, V, V, V, V, V, V, V, V, V, ctypes.c_size_t, V]
     for f in ("ssd_fwd_workspace_size", "ssd_fwd", "ssd_bwd_workspace_size", "ssd_bwd", "ssd_query_status",
               "ssd_fwd_debug_layout", "ssd_fwd_noalloc", "ssd_selftest_bounded_wait", "ssd_chunk_states_size",
               "ssd_noalloc_query_status", "ssd_varlen_metadata", "ssd_gated_norm_fwd",
               "ssd_gated_norm_bwd_workspace_size", "ssd_gated_norm_bwd", "ssd_conv1d_fwd",
-              "ssd_conv1d_bwd_workspace_size", "ssd_conv1d_bwd"):
+              "ssd_conv1d_bwd_workspace_size", "ssd_conv1d_bwd", "ssd_complex_fwd_workspace_size",
+              "ssd_complex_fwd"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -333,3 +342,17 @@ def conv1d_bwd(prob, u, weight, bias, cu_seqlens, dout, du, dweight, dbias, work
                                      _ptr(dbias), _ptr(workspace),
                                      ctypes.c_size_t(workspace.numel() * workspace.element_size()),
                                      _stream_handle(stream)))
+
+
+def complex_fwd_workspace_size(prob):
+    n = ctypes.c_size_t(0)
+    check(load().ssd_complex_fwd_workspace_size(ctypes.byref(prob), ctypes.byref(n)), "ssd_complex_fwd_workspace_size")
+    return int(n.value)
+
+
+def complex_fwd(prob, x, dt, A, B, C, init, y_re, y_im, final, workspace, stream=None):
+    """Raw call (complex tensors are complex64, contiguous); returns the status code."""
+    return int(load().ssd_complex_fwd(ctypes.byref(prob), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(init),
+                                      _ptr(y_re), _ptr(y_im), _ptr(final), _ptr(workspace),
+                                      ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                      _stream_handle(stream)))

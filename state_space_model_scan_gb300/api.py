@@ -198,3 +198,33 @@ class SSDFunction(torch.autograd.Function):
                          chunk_size=ctx.chunk_size, chunk_states=ctx.chunk_states)
         return (g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], g.get("dD"), g.get("dz"), g.get("ddt_bias"),
                 g.get("dinitial_states"), None, None)
+
+
+def complex_ssd_forward(x, A, B, C, dt, initial_states=None, chunk_size=64, return_imag=False,
+                        return_final=False, stream=None):
+    """Complex-A SSD scan (Mamba-3-Lite): h_t = exp(softplus(dt_t) A) h_{t-1} + x_t (outer) B_t,
+    y_t = sum_n C_t[n] h_t[:, n].  x [batch, seqlen, nheads, headdim], B/C [batch, seqlen, nheads,
+    dstate] and A [nheads] complex64; dt [batch, seqlen, nheads] float32; initial_states
+    [batch, nheads, headdim, dstate] complex64.  Returns Re y (float32), then Im y and the final
+    state when asked for."""
+    Bt, T, H, Dh = x.shape
+    N = B.shape[-1]
+    dev = x.device
+    for t in (x, B, C, A) + ((initial_states,) if initial_states is not None else ()):
+        if t.dtype != torch.complex64 or not t.is_contiguous():
+            raise ValueError("complex tensors must be contiguous complex64")
+    if dt.dtype != torch.float32 or not dt.is_contiguous():
+        raise ValueError("dt must be contiguous float32")
+    prob = _lib.ComplexProblem(Bt, T, H, Dh, N, chunk_size)
+    y_re = torch.empty(Bt, T, H, Dh, dtype=torch.float32, device=dev)
+    y_im = torch.empty_like(y_re) if return_imag else None
+    final = torch.empty(Bt, H, Dh, N, dtype=torch.complex64, device=dev) if return_final else None
+    ws = torch.empty(_lib.complex_fwd_workspace_size(prob), dtype=torch.uint8, device=dev)
+    _lib.check(_lib.complex_fwd(prob, x, dt, A, B, C, initial_states, y_re, y_im, final, ws, stream),
+               "ssd_complex_fwd")
+    out = (y_re,)
+    if return_imag:
+        out += (y_im,)
+    if return_final:
+        out += (final,)
+    return out[0] if len(out) == 1 else out

@@ -1,0 +1,512 @@
+// complex_fwd.cu -- forward of the complex-A SSD scan (the Mamba-3-Lite variant), on the
+// tensor cores in tf32 with fp32 accumulation.
+//
+// What it computes (Mamba-3-Lite "SSD Reference -- complex scan API & kernel contract",
+// section "Math: the recurrence both functions implement"; section "ssd_complex_chunkwise"
+// for the chunked evaluation and its inter-chunk contract): per (batch row, head), with
+// abar_t = exp(softplus(dt_t) A_h) (A complex, dt real) and a complex state h_t [D, N],
+//     h_t = abar_t h_{t-1} + x_t (outer) B_t ,   y_t[d] = sum_n C_t[n] h_t[d, n]
+// from h_{-1} = initial_states (or 0); y_real = Re y, y_imag = Im y, final = h_{T-1}.
+//
+// Design.  One CTA per (batch row, head) walks its chunks of 64 positions in order and
+// carries the state in shared memory (fp32), so no state ever goes to HBM between chunks.
+// Complex products run as real tf32 MMAs over interleaved (re, im) K: with u, v complex
+// K-vectors stored as [re, im] pairs, sum u v = [u_re, u_im] . [v_re, -v_im]  (real part)
+// and [u_re, u_im] . [v_im, v_re]  (imaginary part), so the as-loaded interleaved operand
+// pairs with a "conjugated" and a "swapped" copy of the other one; equally
+// [u_im, -u_re] . [v_re, -v_im] is the imaginary part.  Both parts of every complex result
+// land in the same TMEM lane (two column blocks).  Per chunk:
+//   Cb    = C B^T                      A = C, C' = (Im C, -Re C),   B = conj(B tile)
+//   Yraw  = C S^T    (carry-in state)  A = C, C',                   B = conj(S)
+//   Ydiag = (L o Cb) X                 A = [Mr, Mi](l, s),          B = {conj, swap}(X^T)
+//   Sloc  = (w o B)^T X                A = [(wB)r, (wB)i](n, l),    B = {conj, swap}(X^T)
+//   y = Ydiag + exp(cs_l) Yraw ;  S <- exp(cs_63) S + Sloc
+// with cs the in-chunk inclusive cumulative sum of softplus(dt) A, L[l, s] = exp(cs_l - cs_s)
+// for l >= s and w_l = exp(cs_63 - cs_l).  The MMAs are M = 64 (rows 16q..16q+15 in TMEM
+// lanes 32q..32q+15), N = 64, K = 128 (16 instructions of K = 8).  Positions past the end of
+// the sequence read as zero (TMA bounds fill) and carry no decay.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace ssd {
+namespace {
+
+using namespace tc;
+
+constexpr int CQ = 64;                      // chunk length
+constexpr int CD = 64;                      // head dimension (P)
+constexpr int CN = 64;                      // state dimension
+constexpr int CX_THREADS = 512;             // 16 warps: four per TMEM lane quadrant
+constexpr uint32_t SLOT = 32768;            // one operand: 64 rows x 128 fp32, 4 K-atoms of 8 KB
+constexpr uint32_t ATOM = 8192;
+constexpr uint32_t OFF_P0 = 0, OFF_P1 = SLOT, OFF_P2 = 2 * SLOT, OFF_P3 = 3 * SLOT, OFF_P4 = 4 * SLOT;
+constexpr uint32_t OFF_S0 = 5 * SLOT;                      // carried state, conjugated
+constexpr uint32_t OFF_MISC = 6 * SLOT;
+constexpr uint32_t MISC_CS = 0, MISC_E = 512, MISC_W = 1024, MISC_ROT = 1536, MISC_BAR = 2048, MISC_TMEM = 2112,
+                   MISC_ABORT = 2116;
+constexpr uint32_t CX_SMEM = OFF_MISC + 2560 + 1024;       // + alignment slack
+constexpr uint32_t TX_BYTES = 3 * SLOT;                    // C, B and X tiles of one chunk
+
+// TMEM columns: four accumulators of 128 columns (real part block, imaginary part block).
+constexpr uint32_t TC_CB = 0, TC_YR = 128, TC_YD = 256, TC_SL = 384;
+
+enum { BAR_IN = 0, BAR_M1 = 1, BAR_M2 = 2 };
+
+struct CxParams {
+    int64_t Bt, T, H;
+    const float *dt;        // [Bt][T][H]
+    const float *A;         // [H] complex (re, im)
+    const float *init;      // [Bt][H][D][N] complex or null
+    float *y_re, *y_im;     // [Bt][T][H][D]; y_im may be null
+    float *final_;          // [Bt][H][D][N] complex or null
+    int32_t *hdr;           // status header
+};
+
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// K step k (8 fp32 = 32 bytes) of a 64-row operand slot.
+__device__ __forceinline__ uint64_t opdesc(uint32_t slot, int k) {
+    return sdesc(slot + (uint32_t)(k >> 2) * ATOM + (uint32_t)(k & 3) * 32u, 16u, 1024u);
+}
+// Byte offset of fp32 element (row r, k) inside a slot (128-byte swizzle, K-major).
+__device__ __forceinline__ uint32_t elem_off(int r, int k) {
+    return (uint32_t)(k >> 5) * ATOM + (uint32_t)r * 128u + ((uint32_t)(((k & 31) >> 2) ^ (r & 7)) << 4) +
+           (uint32_t)(k & 3) * 4u;
+}
+__device__ __forceinline__ float tf32r(float v) {   // round to the tf32 grid (nearest, ties away)
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+    return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
+}
+__device__ __forceinline__ float2 cexp(float2 a) {
+    float s, c;
+    sincosf(a.y, &s, &c);
+    const float m = __expf(a.x);
+    return make_float2(m * c, m * s);
+}
+__device__ __forceinline__ float softplus_f(float v) {
+    return v > 20.f ? v : log1pf(__expf(v));
+}
+__device__ __forceinline__ void st_pair(uint8_t *slot, int r, int k, float a, float b) {
+    *reinterpret_cast<float2 *>(slot + elem_off(r, k)) = make_float2(a, b);
+}
+__device__ __forceinline__ float2 ld_pair(const uint8_t *slot, int r, int k) {
+    return *reinterpret_cast<const float2 *>(slot + elem_off(r, k));
+}
+
+__global__ void __launch_bounds__(CX_THREADS, 1)
+k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const CxParams p) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *P0 = sm + OFF_P0, *P1 = sm + OFF_P1, *P2 = sm + OFF_P2, *P3 = sm + OFF_P3, *P4 = sm + OFF_P4;
+    uint8_t *S0 = sm + OFF_S0;
+    float2 *cs = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_CS);
+    float2 *ecs = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_E);
+    float2 *wv = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_W);
+    float2 *rot = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_ROT);   // exp(i Im cs_l)
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_MISC + MISC_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + MISC_TMEM);
+    volatile int *abort_ = reinterpret_cast<volatile int *>(sm + OFF_MISC + MISC_ABORT);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t item = blockIdx.x;
+    const int64_t b = item / p.H, h = item % p.H;
+    const int nc = (int)((p.T + CQ - 1) / CQ);
+    const float2 Ah = make_float2(p.A[2 * h], p.A[2 * h + 1]);
+    // TMEM-phase mapping (M = 64 accumulators): lanes 0..15 of each warp hold rows
+    // quad*16 + lane; the four warps of a quadrant take 16 columns each.
+    const int quad = warp & 3, sub = warp >> 2;
+    const bool trow = lane < 16;
+    const int row = quad * 16 + (lane & 15);
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+        *abort_ = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, 512);
+    // carried state from initial_states (or zero), kept as conj(S): rows d, K = 2n + part, (Sr, -Si)
+    for (int i = tid; i < CD * CN; i += CX_THREADS) {
+        const int d = i / CN, n = i % CN;
+        float2 v = make_float2(0.f, 0.f);
+        if (p.init != nullptr) v = reinterpret_cast<const float2 *>(p.init)[((b * p.H + h) * CD + d) * CN + n];
+        st_pair(S0, d, 2 * n, v.x, -v.y);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sP0 = smem_u32(P0), sP1 = smem_u32(P1), sP3 = smem_u32(P3), sP4 = smem_u32(P4);
+    const uint32_t sS0 = smem_u32(S0);
+    const uint32_t id64 = idesc_tf32(64, 64);
+
+    // One BAR_IN phase per chunk, armed for all three tiles when the X tile is issued; the C
+    // and B tiles follow later into the same phase.
+    auto load_x = [&](int c) {
+        mbar_expect_tx(&bar[BAR_IN], TX_BYTES);
+        for (int a = 0; a < 4; ++a) tma_load_4d(P2 + a * ATOM, &tmX, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);
+    };
+    auto load_cb = [&](int c) {
+        for (int a = 0; a < 4; ++a) {
+            tma_load_4d(P0 + a * ATOM, &tmC, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);
+            tma_load_4d(P1 + a * ATOM, &tmB, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);
+        }
+    };
+    // thread 0's record of what may still be in flight when a bounded wait gives up
+    bool in_pending = false, m1_pending = false, m2_pending = false;
+    uint32_t in_par = 0, m_par = 0;
+    if (tid == 0 && nc > 0) {
+        load_x(0);
+        load_cb(0);
+        in_pending = true;
+    }
+    // warp 0 reads dt one chunk ahead (the load's latency hides behind a whole chunk)
+    float dtn[2] = {0.f, 0.f};
+    auto fetch_dt = [&](int c) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t t = (int64_t)c * CQ + 2 * lane + j;
+            dtn[j] = t < p.T ? p.dt[(b * p.T + t) * p.H + h] : 0.f;
+        }
+    };
+    if (warp == 0 && nc > 0) fetch_dt(0);
+
+    for (int c = 0; c < nc; ++c) {
+        const uint32_t par = (uint32_t)(c & 1);
+        const int64_t t0 = (int64_t)c * CQ;
+        // ---- in-chunk cumulative log-decay (warp 0: two positions per lane)
+        if (warp == 0) {
+            float2 a2[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float sp = (t0 + 2 * lane + j < p.T) ? softplus_f(dtn[j]) : 0.f;
+                a2[j] = make_float2(sp * Ah.x, sp * Ah.y);
+            }
+            if (c + 1 < nc) fetch_dt(c + 1);
+            float2 s = make_float2(a2[0].x + a2[1].x, a2[0].y + a2[1].y);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float ux = __shfl_up_sync(0xffffffffu, s.x, o), uy = __shfl_up_sync(0xffffffffu, s.y, o);
+                if (lane >= o) { s.x += ux; s.y += uy; }
+            }
+            float2 ex = make_float2(__shfl_up_sync(0xffffffffu, s.x, 1), __shfl_up_sync(0xffffffffu, s.y, 1));
+            if (lane == 0) ex = make_float2(0.f, 0.f);
+            cs[2 * lane] = make_float2(ex.x + a2[0].x, ex.y + a2[0].y);
+            cs[2 * lane + 1] = s;
+        }
+        __syncthreads();
+        if (tid < CQ) {
+            const float2 cl = cs[tid], last = cs[CQ - 1];
+            ecs[tid] = cexp(cl);
+            wv[tid] = cexp(make_float2(last.x - cl.x, last.y - cl.y));
+            float sn, cn;
+            sincosf(cl.y, &sn, &cn);
+            rot[tid] = make_float2(cn, sn);
+        }
+        // ---- chunk inputs
+        if (tid == 0) {
+            in_par = par;
+            if (!mbar_wait_abort(&bar[BAR_IN], par, abort_)) set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+            else in_pending = false;
+        }
+        __syncthreads();
+        if (*abort_) break;
+        // C rounded in place (P0) and C' = (Im C, -Re C) into P3; conj(B) in place (P1)
+        for (int i = tid; i < (int)(SLOT / 16); i += CX_THREADS) {
+            float4 *cp = reinterpret_cast<float4 *>(P0) + i;
+            const float4 cv = *cp;
+            *cp = make_float4(tf32r(cv.x), tf32r(cv.y), tf32r(cv.z), tf32r(cv.w));
+            reinterpret_cast<float4 *>(P3)[i] = make_float4(tf32r(cv.y), tf32r(-cv.x), tf32r(cv.w), tf32r(-cv.z));
+            float4 *bp = reinterpret_cast<float4 *>(P1) + i;
+            const float4 bv = *bp;
+            *bp = make_float4(tf32r(bv.x), tf32r(-bv.y), tf32r(bv.z), tf32r(-bv.w));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- batch 1: Cb = C B^T and Yraw = C S^T, real parts with C, imaginary parts with C'
+        if (tid == 0) {
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_CB, opdesc(sP0, k), opdesc(sP1, k), id64, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_CB + 64, opdesc(sP3, k), opdesc(sP1, k), id64, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YR, opdesc(sP0, k), opdesc(sS0, k), id64, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YR + 64, opdesc(sP3, k), opdesc(sS0, k), id64, k > 0);
+            umma_commit(&bar[BAR_M1]);
+            m_par = par;
+            m1_pending = true;
+        }
+        // ---- meanwhile conj(X^T) into P4 (rows d, K = 2s + part: Xr, -Xi).  A warp reads one
+        // 16-byte piece (two complex columns d) of 32 consecutive rows s and writes a contiguous
+        // 256-byte run of rows d and d+1.
+        {
+            const int s = lane + 32 * (warp & 1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int d0 = 2 * ((warp >> 1) + 8 * i);
+                const float4 v = *reinterpret_cast<const float4 *>(P2 + elem_off(s, 2 * d0));
+                st_pair(P4, d0, 2 * s, tf32r(v.x), tf32r(-v.y));
+                st_pair(P4, d0 + 1, 2 * s, tf32r(v.z), tf32r(-v.w));
+            }
+        }
+        if (tid == 0) {
+            if (!mbar_wait_abort(&bar[BAR_M1], par, abort_)) set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+            else m1_pending = false;
+        }
+        __syncthreads();
+        tc_fence_after();
+        if (*abort_) break;
+        // ---- swap(X^T) into P3 (Xi, Xr) and (w o B)^T into P0 (rows n, K = 2l + part) from conj(B)
+        {
+            const int s = lane + 32 * (warp & 1);
+            const float2 ws = wv[s];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int d0 = 2 * ((warp >> 1) + 8 * i);
+                const float4 v = *reinterpret_cast<const float4 *>(P2 + elem_off(s, 2 * d0));
+                st_pair(P3, d0, 2 * s, tf32r(v.y), tf32r(v.x));
+                st_pair(P3, d0 + 1, 2 * s, tf32r(v.w), tf32r(v.z));
+                const float4 cb = *reinterpret_cast<const float4 *>(P1 + elem_off(s, 2 * d0));
+                const float2 v0 = cmul(ws, make_float2(cb.x, -cb.y)), v1 = cmul(ws, make_float2(cb.z, -cb.w));
+                st_pair(P0, d0, 2 * s, tf32r(v0.x), tf32r(v0.y));
+                st_pair(P0, d0 + 1, 2 * s, tf32r(v1.x), tf32r(v1.y));
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0 && c + 1 < nc) {   // the X tile of the next chunk into the freed slot
+            load_x(c + 1);
+            in_pending = true;
+        }
+        // ---- M = L o Cb into P1 (rows l, K = 2s + part): lanes 0..15 of each warp, 16 columns
+        {
+            float re[16], im[16];
+            tmem_ld16(tmem + lane_base + TC_CB + 16 * sub, re);
+            tmem_ld16(tmem + lane_base + TC_CB + 64 + 16 * sub, im);
+            tmem_wait_ld();
+            if (trow) {
+                // L[l, s] = exp(Re(cs_l - cs_s)) rot_l conj(rot_s): the phase factors have modulus one,
+                // so splitting them costs no range; the magnitude stays a difference
+                const float lre = cs[row].x * 1.4426950408889634f;
+                const float2 rl = rot[row];
+                float out[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int s = 16 * sub + j;
+                    float2 m = make_float2(0.f, 0.f);
+                    if (s <= row) {
+                        const float2 rs = rot[s];
+                        const float mag = ex2(lre - cs[s].x * 1.4426950408889634f);
+                        const float2 ph = make_float2(rl.x * rs.x + rl.y * rs.y, rl.y * rs.x - rl.x * rs.y);
+                        m = cmul(make_float2(mag * ph.x, mag * ph.y), make_float2(re[j], im[j]));
+                    }
+                    out[2 * j] = tf32r(m.x);
+                    out[2 * j + 1] = tf32r(m.y);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4 *>(P1 + elem_off(row, 32 * sub + 4 * j)) =
+                        make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // ---- batch 2: Ydiag = M X and Sloc = (w o B)^T X (real parts with conj(X^T), imaginary with swap)
+        if (tid == 0) {
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YD, opdesc(sP1, k), opdesc(sP4, k), id64, k > 0);
+            if (p.y_im != nullptr)
+                for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YD + 64, opdesc(sP1, k), opdesc(sP3, k), id64, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_SL, opdesc(sP0, k), opdesc(sP4, k), id64, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_SL + 64, opdesc(sP0, k), opdesc(sP3, k), id64, k > 0);
+            umma_commit(&bar[BAR_M2]);
+            m2_pending = true;
+            if (!mbar_wait_abort(&bar[BAR_M2], par, abort_)) {
+                set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+            } else {
+                m2_pending = false;
+                if (c + 1 < nc) load_cb(c + 1);   // C and B slots are free again: overlaps the epilogue
+            }
+        }
+        __syncthreads();
+        tc_fence_after();
+        if (*abort_) break;
+        // ---- outputs: y = Ydiag + exp(cs_l) Yraw
+        {
+            float yr[16], yi[16], dr[16], di[16];
+            tmem_ld16(tmem + lane_base + TC_YR + 16 * sub, yr);
+            tmem_ld16(tmem + lane_base + TC_YR + 64 + 16 * sub, yi);
+            tmem_ld16(tmem + lane_base + TC_YD + 16 * sub, dr);
+            if (p.y_im != nullptr) tmem_ld16(tmem + lane_base + TC_YD + 64 + 16 * sub, di);
+            tmem_wait_ld();
+            const int64_t t = t0 + row;
+            if (trow && t < p.T) {
+                const float2 e = ecs[row];
+                const int64_t off = ((b * p.T + t) * p.H + h) * CD + 16 * sub;
+                float o[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) o[j] = dr[j] + e.x * yr[j] - e.y * yi[j];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    reinterpret_cast<float4 *>(p.y_re + off)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2],
+                                                                              o[4 * j + 3]);
+                if (p.y_im != nullptr) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o[j] = di[j] + e.x * yi[j] + e.y * yr[j];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        reinterpret_cast<float4 *>(p.y_im + off)[j] =
+                            make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                }
+            }
+        }
+        // ---- state: S <- exp(cs_63) S + Sloc (row n, columns d); each (d, n) has one owner
+        {
+            float sr[16], si[16];
+            tmem_ld16(tmem + lane_base + TC_SL + 16 * sub, sr);
+            tmem_ld16(tmem + lane_base + TC_SL + 64 + 16 * sub, si);
+            tmem_wait_ld();
+            if (trow) {
+                const float2 e = ecs[CQ - 1];
+                const int n = row;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int d = 16 * sub + j;
+                    const float2 o = ld_pair(S0, d, 2 * n);   // (Sr, -Si)
+                    const float nr = e.x * o.x + e.y * o.y + sr[j];
+                    const float ni = e.x * (-o.y) + e.y * o.x + si[j];
+                    st_pair(S0, d, 2 * n, nr, -ni);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (*abort_) {
+        // let copies and MMAs still in flight finish (bounded) before shared memory and
+        // tensor memory are released
+        if (tid == 0) {
+            if (in_pending) mbar_wait(&bar[BAR_IN], in_par);
+            if (m1_pending) mbar_wait(&bar[BAR_M1], m_par);
+            if (m2_pending) mbar_wait(&bar[BAR_M2], m_par);
+        }
+    } else if (p.final_ != nullptr) {
+        for (int i = tid; i < CD * CN; i += CX_THREADS) {
+            const int d = i / CN, n = i % CN;
+            const float2 v = ld_pair(S0, d, 2 * n);
+            reinterpret_cast<float2 *>(p.final_)[((b * p.H + h) * CD + d) * CN + n] = make_float2(v.x, -v.y);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_cx() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// fp32 map over a contiguous [Bt][T][H][128 floats] tensor, box {32, 1, 64, 1}, 128-byte swizzle.
+bool map_cx(CUtensorMap *m, const void *ptr, int64_t Bt, int64_t T, int64_t H) {
+    auto fn = encode_fn_cx();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)Bt};
+    cuuint64_t strides[3] = {512, (cuuint64_t)(H * 512), (cuuint64_t)(T * H * 512)};
+    cuuint32_t box[4] = {32, 1, (cuuint32_t)CQ, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+ssd_status ssd_complex_fwd_workspace_size(const ssd_complex_problem *p, size_t *bytes) {
+    if (p == nullptr || bytes == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    *bytes = HDR_WORDS * sizeof(int32_t);
+    return SSD_OK;
+}
+
+ssd_status ssd_complex_fwd(const ssd_complex_problem *p, const void *x, const float *dt, const void *A,
+                          const void *B, const void *C, const void *initial_states, float *y_real, float *y_imag,
+                          void *final_states, void *workspace, size_t workspace_bytes, void *stream) {
+    if (p == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    if (p->batch < 1 || p->seqlen < 0 || p->nheads < 1 || p->headdim < 1 || p->dstate < 1 || p->chunk_size < 1)
+        return SSD_ERR_INVALID_ARGUMENT;
+    if (p->headdim != CD || p->dstate != CN || p->chunk_size != CQ) return SSD_ERR_UNSUPPORTED;
+    if (p->seqlen > ((int64_t)1 << 30) || p->nheads > ((int64_t)1 << 20) || p->batch * p->nheads > ((int64_t)1 << 30))
+        return SSD_ERR_UNSUPPORTED;
+    if (A == nullptr) return SSD_ERR_INVALID_ARGUMENT;
+    if (p->seqlen > 0 && (x == nullptr || dt == nullptr || B == nullptr || C == nullptr || y_real == nullptr))
+        return SSD_ERR_INVALID_ARGUMENT;
+    if (workspace == nullptr || workspace_bytes < HDR_WORDS * sizeof(int32_t)) return SSD_ERR_WORKSPACE_TOO_SMALL;
+    auto al16 = [](const void *q) { return ((uintptr_t)q & 15u) == 0; };
+    for (const void *q : {x, (const void *)B, (const void *)C, (const void *)y_real, (const void *)y_imag,
+                          initial_states, (const void *)final_states, (const void *)workspace})
+        if (q != nullptr && !al16(q)) return SSD_ERR_MISALIGNED;
+    if (((uintptr_t)A & 7u) != 0 || ((uintptr_t)dt & 3u) != 0) return SSD_ERR_MISALIGNED;
+    if (p->seqlen == 0 && final_states == nullptr) return SSD_OK;   // nothing to compute
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(workspace, 0, HDR_WORDS * sizeof(int32_t), st) != cudaSuccess) return SSD_ERR_CUDA;
+    CUtensorMap mx{}, mb{}, mc{};
+    if (p->seqlen > 0) {
+        if (!map_cx(&mx, x, p->batch, p->seqlen, p->nheads) || !map_cx(&mb, B, p->batch, p->seqlen, p->nheads) ||
+            !map_cx(&mc, C, p->batch, p->seqlen, p->nheads))
+            return SSD_ERR_CUDA;
+    } else {
+        // no tokens: maps are never read; the kernel only copies the initial state out
+        if (!map_cx(&mx, final_states, 1, 1, 1)) return SSD_ERR_CUDA;
+        mb = mx;
+        mc = mx;
+    }
+    CxParams q{};
+    q.Bt = p->batch; q.T = p->seqlen; q.H = p->nheads;
+    q.dt = dt; q.A = static_cast<const float *>(A); q.init = static_cast<const float *>(initial_states);
+    q.y_re = y_real; q.y_im = y_imag; q.final_ = static_cast<float *>(final_states);
+    q.hdr = static_cast<int32_t *>(workspace);
+    static int attr[64] = {0};
+    if (ensure_smem_attr(k_complex_fwd, (int)CX_SMEM, attr) != cudaSuccess) return SSD_ERR_CUDA;
+    k_complex_fwd<<<(unsigned)(p->batch * p->nheads), CX_THREADS, CX_SMEM, st>>>(mx, mb, mc, q);
+    return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -158,3 +158,35 @@ def to_oracle(inp: dict, w: Workload) -> dict:
         o["dy"] = f(inp["dy"], (T, H, P))
         o["dfinal"] = f(inp["dfinal_states"])
     return o
+
+
+def complex_inputs(batch: int, seqlen: int, nheads: int, headdim: int = 64, dstate: int = 64, seed: int = 0,
+                   with_init: bool = True) -> dict:
+    """CPU tensors for the complex-A scan (the Mamba-3-Lite variant).
+
+    * Re A = -exp(U[ln 0.1, ln 1]), Im A = U[-pi, pi]      (A [H] complex64)
+    * dt ~ N(0, 1) before softplus                          (dt [B, L, H] float32)
+    * x, B, C: complex normal, real and imaginary parts N(0, 1/2) each (unit variance)
+    * initial_states: 0.1 x complex normal                   ([B, H, headdim, dstate])
+    Each tensor draws from its own generator; values drawn in float64, rounded once.
+    """
+    d = torch.float64
+    g = lambda k: torch.Generator().manual_seed(seed * 1000 + 500 + k)
+
+    def cn(k, *shape):
+        gen = g(k)
+        re = torch.randn(*shape, generator=gen, dtype=d)
+        im = torch.randn(*shape, generator=gen, dtype=d)
+        return (torch.complex(re, im) / math.sqrt(2.0)).to(torch.complex64)
+
+    u = torch.rand(nheads, generator=g(0), dtype=d)
+    ph = torch.rand(nheads, generator=g(1), dtype=d)
+    A = torch.complex(-torch.exp(math.log(0.1) + u * (0.0 - math.log(0.1))), (2 * ph - 1) * math.pi)
+    out = dict(A=A.to(torch.complex64),
+               dt=torch.randn(batch, seqlen, nheads, generator=g(2), dtype=d).to(torch.float32),
+               x=cn(3, batch, seqlen, nheads, headdim),
+               B=cn(4, batch, seqlen, nheads, dstate),
+               C=cn(5, batch, seqlen, nheads, dstate))
+    out["initial_states"] = (0.1 * cn(6, batch, nheads, headdim, dstate).to(torch.complex128)).to(
+        torch.complex64) if with_init else None
+    return out

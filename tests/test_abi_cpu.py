@@ -428,3 +428,38 @@ def test_conv1d_pointer_and_layout_checks(lib):
     assert b(*args(ctypes.c_void_p(0x100004), n.value)) == 3
     assert b(*args(d, n.value, dw=None)) == 1                # dweight required
     assert b(*args(d, n.value, bias=d)) == 1                 # bias given, dbias missing
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("batch", 0, 1), ("seqlen", -1, 1), ("nheads", 0, 1), ("chunk_size", 0, 1),
+    ("headdim", 32, 2), ("dstate", 128, 2), ("chunk_size", 128, 2),   # compiled set: 64 / 64 / 64
+])
+def test_complex_validation(lib, field, value, code):
+    """Host-side checks of the complex-A scan entry point (nothing reaches the device)."""
+    m = lib_mod()
+    p = m.ComplexProblem(2, 128, 4, 64, 64, 64)
+    setattr(p, field, value)
+    d = ctypes.c_void_p(0x100000)
+    ws = ctypes.c_size_t(256)
+    f = m.load().ssd_complex_fwd
+    assert f(ctypes.byref(p), d, d, d, d, d, None, d, None, None, d, ws, None) == code
+
+
+def test_complex_pointer_checks(lib):
+    m = lib_mod()
+    p = m.ComplexProblem(2, 128, 4, 64, 64, 64)
+    n = ctypes.c_size_t(0)
+    assert m.load().ssd_complex_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0 and n.value == 256
+    d, odd = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x100008)
+    f = m.load().ssd_complex_fwd
+    ws = ctypes.c_size_t(n.value)
+    assert f(ctypes.byref(p), None, d, d, d, d, None, d, None, None, d, ws, None) == 1      # x required
+    assert f(ctypes.byref(p), d, d, None, d, d, None, d, None, None, d, ws, None) == 1      # A required
+    assert f(ctypes.byref(p), d, d, d, d, d, None, None, None, None, d, ws, None) == 1      # y_real required
+    assert f(ctypes.byref(p), d, d, d, d, d, None, d, None, None, d, ctypes.c_size_t(8), None) == 4
+    assert f(ctypes.byref(p), d, d, d, d, d, None, d, None, None, None, ws, None) == 4
+    assert f(ctypes.byref(p), odd, d, d, d, d, None, d, None, None, d, ws, None) == 3      # 16-byte rule
+    assert f(ctypes.byref(p), d, d, d, d, d, odd, d, None, None, d, ws, None) == 3
+    # no tokens and no final state asked for: nothing to do
+    p0 = m.ComplexProblem(2, 0, 4, 64, 64, 64)
+    assert f(ctypes.byref(p0), None, None, d, None, None, None, None, None, None, d, ws, None) == 0
