@@ -8,12 +8,17 @@ before it:
     forward that also keeps the carried chunk states + backward that reads them;
   * the other forward workloads, one forward each: the long-sequence sweep (128 heads
     x 64, 1 group, dstate 128, initial states, L = 1k .. 32k) and the packed varlen
-    workload (16 sequences of U{512..8192} tokens, 80 heads x 64, own initial states).
+    workload (16 sequences of U{512..8192} tokens, 80 heads x 64, own initial states);
+  * the kernels around the scan, forward and backward at the Nemotron-Nano widths (8192
+    tokens, bf16): the gated RMS normalisation of y over 8 groups of 512 features and the
+    causal conv1d (width 4, SiLU) over the packed xBC (6144 channels); and the complex-A
+    scan of the Mamba-3-Lite variant at its 434M configuration (8 x 2048 tokens, 16 heads,
+    headdim = dstate = chunk = 64).
 `value` is the inference forward's tokens/s at the Nemotron-Nano shape (median over
 the steps of its CUDA-event time); `ms_per_step` is the training step's median device
 time (forward + backward); `sweep` holds the other workloads' median forward times,
-tokens/s and HBM roofline fractions; `e2e` is forward tokens/s with every step's inputs
-copied from pinned host memory and its y copied back inside the timed region, two
+tokens/s and HBM roofline fractions, `extras` the same for the kernels around the
+scan; `e2e` is forward tokens/s with every step's inputs copied from pinned host memory and its y copied back inside the timed region, two
 independent steps in flight (copy-in, compute and copy-out streams).  Clocks and
 throttle reasons are sampled through NVML every millisecond during the timed steps.
 Prints ONE JSON line.
@@ -322,6 +327,67 @@ def sweep_bytes(w):
     return algorithmic_bytes(w, fwd=True)
 
 
+def build_extras(dev, s, w):
+    """Graph-captured calls of the other kernels, each with its algorithmic bytes per launch."""
+    import torch
+    from state_space_model_scan_gb300 import inputs as I
+    from state_space_model_scan_gb300 import _lib
+    out = []
+    g = torch.Generator().manual_seed(7)
+    T = w.batch * w.seqlen
+    width, gsize = w.nheads * w.headdim, w.headdim * w.nheads // w.ngroups
+    bf = torch.bfloat16
+
+    def capture(name, fn, nbytes, launches, tokens, keep):
+        with torch.cuda.stream(s):
+            _lib.check(fn(s), name)
+        s.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            _lib.check(fn(torch.cuda.current_stream()), name)
+        out.append(dict(name=name, graph=gr, bytes=nbytes, launches=launches, tokens=tokens, keep=keep))
+
+    # gated RMS normalisation over the scan output: rows = tokens, width = H*P, groups of H*P/G
+    y = torch.randn(T, width, generator=g).to(bf).to(dev)
+    z = torch.randn(T, width, generator=g).to(bf).to(dev)
+    nw = (1.0 + 0.1 * torch.randn(width, generator=g)).to(dev)
+    nout, dout = torch.empty_like(y), torch.randn(T, width, generator=g).to(bf).to(dev)
+    rstd = torch.empty(T, width // gsize, dtype=torch.float32, device=dev)
+    ndy, ndz, ndw = torch.empty_like(y), torch.empty_like(z), torch.empty(width, device=dev)
+    nprob = _lib.norm_problem(T, width, gsize, 1e-5, bf)
+    nws = torch.empty(max(_lib.gated_norm_bwd_workspace_size(nprob), 16), dtype=torch.uint8, device=dev)
+    el = T * width * 2
+    capture("gated_norm_fwd", lambda st: _lib.gated_norm_fwd(nprob, y, z, nw, nout, rstd, st),
+            3 * el + rstd.numel() * 4 + width * 4, 1, T, (y, z, nw, nout, rstd))
+    capture("gated_norm_bwd", lambda st: _lib.gated_norm_bwd(nprob, y, z, nw, rstd, dout, ndy, ndz, ndw, nws, st),
+            5 * el + rstd.numel() * 4 + 2 * width * 4, 2, T, (dout, ndy, ndz, ndw, nws))
+    # causal depthwise conv1d + SiLU over the packed xBC: channels H*P + 2*G*N, width 4
+    Cn = width + 2 * w.ngroups * w.dstate
+    u = torch.randn(1, T, Cn, generator=g).to(bf).to(dev)
+    cw = (0.5 * torch.randn(Cn, 4, generator=g)).to(dev)
+    cb = (0.1 * torch.randn(Cn, generator=g)).to(dev)
+    cout, cdo = torch.empty_like(u), torch.randn(1, T, Cn, generator=g).to(bf).to(dev)
+    cdu, cdw, cdb = torch.empty_like(u), torch.empty_like(cw), torch.empty_like(cb)
+    cprob = _lib.conv_problem(1, T, Cn, 4, 0, bf, True)
+    cws = torch.empty(_lib.conv1d_bwd_workspace_size(cprob), dtype=torch.uint8, device=dev)
+    ue = T * Cn * 2
+    capture("conv1d_fwd", lambda st: _lib.conv1d_fwd(cprob, u, cw, cb, None, cout, st), 2 * ue, 1, T,
+            (u, cw, cb, cout))
+    capture("conv1d_bwd", lambda st: _lib.conv1d_bwd(cprob, u, cw, cb, None, cdo, cdu, cdw, cdb, cws, st),
+            3 * ue, 2, T, (cdo, cdu, cdw, cdb, cws))
+    # complex-A scan, 8 x 2048 tokens, 16 heads, headdim = dstate = chunk = 64
+    ci = {k: (v.to(dev) if v is not None else None) for k, v in I.complex_inputs(8, 2048, 16, seed=434).items()}
+    xp = _lib.ComplexProblem(8, 2048, 16, 64, 64, 64)
+    yr = torch.empty(8, 2048, 16, 64, dtype=torch.float32, device=dev)
+    cfin = torch.empty(8, 16, 64, 64, dtype=torch.complex64, device=dev)
+    xws = torch.empty(_lib.complex_fwd_workspace_size(xp), dtype=torch.uint8, device=dev)
+    cbytes = 3 * ci["x"].numel() * 8 + ci["dt"].numel() * 4 + yr.numel() * 4 + 2 * cfin.numel() * 8
+    capture("complex_fwd_434m", lambda st: _lib.complex_fwd(xp, ci["x"], ci["dt"], ci["A"], ci["B"], ci["C"],
+                                                            ci["initial_states"], yr, None, cfin, xws, st),
+            cbytes, 1, 8 * 2048, (ci, yr, cfin, xws))
+    return out
+
+
 def run_gpu(args):
     import torch
     world, rank, local = dist_env()
@@ -399,6 +465,13 @@ def run_gpu(args):
             sweep.append(dict(w=sw, graph=sg, keep=(si, sy, sfin, sws, sargs),
                               launches=3 if si["cu_seqlens"] is not None else 2))
 
+    # the steps next to the scan: the gated RMS normalisation after it and the conv1d over the
+    # packed xBC before it (Nemotron-Nano widths, 8192 tokens, bf16), and the complex-A scan of
+    # the Mamba-3-Lite variant (its 434M configuration); forward and backward where both exist
+    extras = []
+    if not args.no_sweep:
+        extras = build_extras(dev, s, w)
+
     def step(ev=None, sev=None):
         with torch.cuda.stream(s):
             flush.fill_(float(rank + 1))
@@ -416,7 +489,7 @@ def run_gpu(args):
             gb.replay()                    # ... and the backward
             if ev is not None:
                 ev[4].record(s)
-            for j, c in enumerate(sweep):  # the other forward workloads
+            for j, c in enumerate(sweep + extras):  # the other workloads
                 flush.fill_(float(rank + 3 + j))
                 if sev is not None:
                     sev[j][0].record(s)
@@ -428,7 +501,8 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    sevs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in sweep] for _ in range(args.steps)]
+    sevs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in sweep + extras]
+            for _ in range(args.steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -446,9 +520,11 @@ def run_gpu(args):
     bwd_ms = median([e[3].elapsed_time(e[4]) for e in evs])
     step_ms = median([e[2].elapsed_time(e[4]) for e in evs])
     sweep_ms = [median([sevs[i][j][0].elapsed_time(sevs[i][j][1]) for i in range(args.steps)])
-                for j in range(len(sweep))]
+                for j in range(len(sweep) + len(extras))]
     red = max_over_ranks([fwd_ms, fwdt_ms, bwd_ms, step_ms] + sweep_ms, device=dev)
     fwd_ms, fwdt_ms, bwd_ms, step_ms, sweep_ms = red[0], red[1], red[2], red[3], red[4:]
+    extra_ms = sweep_ms[len(sweep):]
+    sweep_ms = sweep_ms[:len(sweep)]
     toks = w.batch * w.seqlen
     value = world * toks / (fwd_ms * 1e-3)
 
@@ -525,7 +601,14 @@ def run_gpu(args):
                           "chunk_size": sw.chunk_size, "fwd_ms": ms, "tokens_per_s": sw.batch * sw.seqlen / (ms * 1e-3),
                           "algorithmic_bytes": b, "achieved_gbs": b / (ms * 1e-3) / 1e9,
                           "roofline_frac": b / (ms * 1e-3) / 1e9 / peak})
-    n_launch_step = 2 * launches_fwd + launches_bwd + sum(c["launches"] for c in sweep)
+    extras_out = []
+    for c, ms in zip(extras, extra_ms):
+        gbs = c["bytes"] / (ms * 1e-3) / 1e9
+        extras_out.append({"workload": c["name"], "ms": ms, "tokens_per_s": c["tokens"] / (ms * 1e-3),
+                           "algorithmic_bytes": c["bytes"], "achieved_gbs": gbs, "roofline_frac": gbs / peak,
+                           "launches": c["launches"]})
+    n_launch_step = (2 * launches_fwd + launches_bwd + sum(c["launches"] for c in sweep) +
+                     sum(c["launches"] for c in extras))
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -544,6 +627,7 @@ def run_gpu(args):
                          "frac": algorithmic_bytes(w, fwd=False) / (bwd_ms * 1e-3) / 1e9 / peak,
                          "algorithmic_bytes_per_launch": algorithmic_bytes(w, fwd=False)},
         "sweep": sweep_out,
+        "extras": extras_out,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         # library kernels in the two timed regions: the step loop and the end-to-end loop
         "gpu_launches": args.steps * n_launch_step + args.steps * launches_fwd,

@@ -184,12 +184,163 @@ k_norm_bwd(const NormArgs a) {
     }
 }
 
+// Register-resident variants for groups of at most 32 * PPL * 8 features: a lane keeps its PPL
+// pieces of y (and z, dout) in registers, so every load of a row is issued at once and nothing is
+// read twice; in the backward the lane's slice of w and of the dw sums stay in registers too.
+template <typename T, int PPL>
+__global__ void __launch_bounds__(NW * 32)
+k_norm_fwd_reg(const NormArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t items = a.rows * a.ng, nw = (int64_t)gridDim.x * NW;
+    const int pieces = (int)(a.G / 8);
+    for (int64_t it = (int64_t)blockIdx.x * NW + (threadIdx.x >> 5); it < items; it += nw) {
+        const int64_t r = it / a.ng;
+        const int g = (int)(it - r * a.ng);
+        const T *yr = static_cast<const T *>(a.y) + r * a.sy + (int64_t)g * a.G;
+        const T *zr = a.z ? static_cast<const T *>(a.z) + r * a.sz + (int64_t)g * a.G : nullptr;
+        float v[PPL][8], zz[PPL][8];
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            const int j = lane + 32 * k;
+            if (j < pieces) {
+                load8(yr + 8 * j, v[k]);
+                if (zr) load8(zr + 8 * j, zz[k]);
+            }
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            if (lane + 32 * k < pieces) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (zr) v[k][e] *= zz[k][e] * sigmoid_f(zz[k][e]);
+                    ss = fmaf(v[k][e], v[k][e], ss);
+                }
+            }
+        }
+        ss = warp_sum(ss);
+        const float rs = 1.f / sqrtf(ss / (float)a.G + a.eps);
+        if (lane == 0) a.rstd[r * a.ng + g] = rs;
+        T *orow = static_cast<T *>(a.out) + r * a.sout + (int64_t)g * a.G;
+        const float *wr = a.w + (int64_t)g * a.G;
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            const int j = lane + 32 * k;
+            if (j < pieces) {
+                float wv[8];
+                load8(wr + 8 * j, wv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[k][e] = v[k][e] * rs * wv[e];
+                store8(orow + 8 * j, v[k]);
+            }
+        }
+    }
+}
+
+template <typename T, int PPL>
+__global__ void __launch_bounds__(NW * 32, PPL <= 2 ? 2 : 1)
+k_norm_bwd_reg(const NormArgs a) {
+    extern __shared__ float acc[];   // [NW][G]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = blockIdx.y;
+    const int pieces = (int)(a.G / 8);
+    const int64_t r0 = (int64_t)blockIdx.x * a.rows_per_chunk, r1 = std::min(a.rows, r0 + a.rows_per_chunk);
+    const float *wr = a.w + (int64_t)g * a.G;
+    float wv[PPL][8], dw[PPL][8];
+#pragma unroll
+    for (int k = 0; k < PPL; ++k) {
+        const int j = lane + 32 * k;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { dw[k][e] = 0.f; wv[k][e] = 0.f; }
+        if (j < pieces) load8(wr + 8 * j, wv[k]);
+    }
+    for (int64_t r = r0 + warp; r < r1; r += NW) {
+        const T *yr = static_cast<const T *>(a.y) + r * a.sy + (int64_t)g * a.G;
+        const T *zr = a.z ? static_cast<const T *>(a.z) + r * a.sz + (int64_t)g * a.G : nullptr;
+        const T *dr = static_cast<const T *>(a.dout) + r * a.sdout + (int64_t)g * a.G;
+        float y8[PPL][8], z8[PPL][8], d[PPL][8];
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            const int j = lane + 32 * k;
+            if (j < pieces) {
+                load8(yr + 8 * j, y8[k]);
+                if (zr) load8(zr + 8 * j, z8[k]);
+                load8(dr + 8 * j, d[k]);
+            }
+        }
+        const float rs = a.rstd_in[r * a.ng + g];
+        float dot = 0.f;   // sum_i (dout w)_i vhat_i
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            if (lane + 32 * k < pieces) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float sgate = zr ? z8[k][e] * sigmoid_f(z8[k][e]) : 1.f;
+                    dot = fmaf(d[k][e] * wv[k][e], y8[k][e] * sgate * rs, dot);
+                }
+            }
+        }
+        dot = warp_sum(dot) / (float)a.G;
+        T *dyr = static_cast<T *>(a.dy) + r * a.sdy + (int64_t)g * a.G;
+        T *dzr = a.z ? static_cast<T *>(a.dz) + r * a.sdz + (int64_t)g * a.G : nullptr;
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            const int j = lane + 32 * k;
+            if (j < pieces) {
+                float o1[8], o2[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float sg = zr ? sigmoid_f(z8[k][e]) : 0.f;
+                    const float sgate = zr ? z8[k][e] * sg : 1.f;
+                    const float vhat = y8[k][e] * sgate * rs;
+                    const float dv = rs * (d[k][e] * wv[k][e] - vhat * dot);
+                    o1[e] = dv * sgate;                                                          // dy
+                    o2[e] = zr ? dv * y8[k][e] * sg * (1.f + z8[k][e] * (1.f - sg)) : 0.f;      // dz
+                    dw[k][e] = fmaf(d[k][e], vhat, dw[k][e]);                                   // dw share
+                }
+                store8(dyr + 8 * j, o1);
+                if (zr) store8(dzr + 8 * j, o2);
+            }
+        }
+    }
+    float *mine = acc + (int64_t)warp * a.G;
+#pragma unroll
+    for (int k = 0; k < PPL; ++k) {
+        const int j = lane + 32 * k;
+        if (j < pieces)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mine[8 * j + e] = dw[k][e];
+    }
+    __syncthreads();
+    float *dst = a.partials + (int64_t)blockIdx.x * a.width + (int64_t)g * a.G;
+    for (int64_t i = threadIdx.x; i < a.G; i += blockDim.x) {
+        float s = 0.f;
+        for (int w = 0; w < NW; ++w) s += acc[(int64_t)w * a.G + i];
+        dst[i] = s;
+    }
+}
+
 __global__ void k_norm_dw(const float *partials, int64_t chunks, int64_t width, float *dw) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < width; i += (int64_t)gridDim.x * blockDim.x) {
         float s = 0.f;
         for (int64_t c = 0; c < chunks; ++c) s += partials[c * width + i];
         dw[i] = s;
     }
+}
+
+template <typename K>
+cudaError_t launch_one(K kernel, const NormArgs &a, dim3 grid, size_t smem, cudaStream_t st, int *attr) {
+    cudaError_t e = ensure_smem_attr(kernel, (int)smem, attr);
+    if (e == cudaSuccess) kernel<<<grid, NW * 32, smem, st>>>(a);
+    return e;
+}
+template <typename T>
+cudaError_t launch_norm_bwd(const NormArgs &a, int64_t ppl, dim3 grid, size_t smem, cudaStream_t st) {
+    static int attr[4][64] = {};
+    if (ppl <= 1) return launch_one(k_norm_bwd_reg<T, 1>, a, grid, smem, st, attr[0]);
+    if (ppl <= 2) return launch_one(k_norm_bwd_reg<T, 2>, a, grid, smem, st, attr[1]);
+    if (ppl <= 4) return launch_one(k_norm_bwd_reg<T, 4>, a, grid, smem, st, attr[2]);
+    return launch_one(k_norm_bwd<T>, a, grid, smem, st, attr[3]);
 }
 
 int sm_count() {
@@ -256,10 +407,18 @@ ssd_status ssd_gated_norm_fwd(const ssd_norm_problem *p, const void *y, int64_t 
     const int64_t items = p->rows * a.ng;
     const int blocks = (int)std::min<int64_t>((items + NW - 1) / NW, 8LL * sm_count());
     cudaStream_t st = (cudaStream_t)stream;
-    if (p->dtype == SSD_BF16)
-        k_norm_fwd<__nv_bfloat16><<<blocks, NW * 32, 0, st>>>(a);
-    else
-        k_norm_fwd<float><<<blocks, NW * 32, 0, st>>>(a);
+    const int64_t ppl = (p->group_size / 8 + 31) / 32;   // pieces per lane
+    if (p->dtype == SSD_BF16) {
+        if (ppl <= 1) k_norm_fwd_reg<__nv_bfloat16, 1><<<blocks, NW * 32, 0, st>>>(a);
+        else if (ppl <= 2) k_norm_fwd_reg<__nv_bfloat16, 2><<<blocks, NW * 32, 0, st>>>(a);
+        else if (ppl <= 4) k_norm_fwd_reg<__nv_bfloat16, 4><<<blocks, NW * 32, 0, st>>>(a);
+        else k_norm_fwd<__nv_bfloat16><<<blocks, NW * 32, 0, st>>>(a);
+    } else {
+        if (ppl <= 1) k_norm_fwd_reg<float, 1><<<blocks, NW * 32, 0, st>>>(a);
+        else if (ppl <= 2) k_norm_fwd_reg<float, 2><<<blocks, NW * 32, 0, st>>>(a);
+        else if (ppl <= 4) k_norm_fwd_reg<float, 4><<<blocks, NW * 32, 0, st>>>(a);
+        else k_norm_fwd<float><<<blocks, NW * 32, 0, st>>>(a);
+    }
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
@@ -295,16 +454,12 @@ ssd_status ssd_gated_norm_bwd(const ssd_norm_problem *p, const void *y, int64_t 
     a.rows_per_chunk = p->rows > 0 ? (p->rows + chunks - 1) / chunks : 1;
     const size_t smem = (size_t)NW * (size_t)p->group_size * sizeof(float);
     const dim3 grid((unsigned)chunks, (unsigned)a.ng);
+    const int64_t ppl = (p->group_size / 8 + 31) / 32;   // pieces per lane
     cudaError_t e;
-    if (p->dtype == SSD_BF16) {
-        static int attr[64] = {0};
-        e = ensure_smem_attr(k_norm_bwd<__nv_bfloat16>, (int)smem, attr);
-        if (e == cudaSuccess) k_norm_bwd<__nv_bfloat16><<<grid, NW * 32, smem, st>>>(a);
-    } else {
-        static int attr[64] = {0};
-        e = ensure_smem_attr(k_norm_bwd<float>, (int)smem, attr);
-        if (e == cudaSuccess) k_norm_bwd<float><<<grid, NW * 32, smem, st>>>(a);
-    }
+    if (p->dtype == SSD_BF16)
+        e = launch_norm_bwd<__nv_bfloat16>(a, ppl, grid, smem, st);
+    else
+        e = launch_norm_bwd<float>(a, ppl, grid, smem, st);
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
     const int blocks = (int)std::min<int64_t>((p->width + 255) / 256, 1024);
     k_norm_dw<<<blocks, 256, 0, st>>>(a.partials, chunks, p->width, dweight);
