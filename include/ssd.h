@@ -50,8 +50,14 @@
  *   dt, ddt             : [batch, seqlen, nheads]                 f32
  *   A, D, dt_bias, dA, dD, ddt_bias : [nheads], contiguous        f32
  *   initial_states, final_states, dfinal_states, dinitial_states :
- *                         [nstate, nheads, headdim, dstate], contiguous, f32
- *                         (nstate = batch, or nseqs with cu_seqlens)
+ *                         [nstate, nheads, headdim, dstate], contiguous, f32 or
+ *                         bf16, each independently (nstate = batch, or nseqs with
+ *                         cu_seqlens).  bf16 is a storage dtype only (the state
+ *                         cache of a serving stack, whose speed the vLLM pull request
+ *                         for the fused Mamba2 SSD kernel reports "depending on state
+ *                         dtype", "Purpose"): the scan widens bf16 inputs and carries
+ *                         and accumulates every state in f32, then rounds a bf16
+ *                         output to nearest even.  The fp32 copies live in the workspace.
  *   cu_seqlens          : int32 [nseqs + 1] device array, batch must be 1;
  *                         cu[0] = 0, non-decreasing, cu[nseqs] = seqlen.
  *                         Sequence s is tokens [cu[s], cu[s+1]) of row 0; its

@@ -29,11 +29,14 @@ def _nseqs(x, cu_seqlens):
 
 def ssd_forward(x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_states=None, cu_seqlens=None,
                 chunk_size=128, return_final_states=True, algo="auto", seg_chunks=0, workspace=None,
-                y=None, final_states=None, stream=None, keep_chunk_states=False, chunk_states=None):
+                y=None, final_states=None, stream=None, keep_chunk_states=False, chunk_states=None,
+                state_dtype=None):
     """y, final_states = SSD scan (see include/ssd.h for the definition and layouts).
 
     x, z: [B, L, H, P]; dt: [B, L, H] fp32; A, D, dt_bias: [H] fp32; B, C: [B, L, G, N];
-    initial_states: [S, H, P, N] fp32; cu_seqlens: int32 [S+1] (batch 1).
+    initial_states: [S, H, P, N] fp32 or bf16; cu_seqlens: int32 [S+1] (batch 1).
+    state_dtype: storage dtype of the returned final states (default: that of initial_states,
+    else fp32); the scan itself carries its state in fp32 either way.
     keep_chunk_states: also return the carried chunk states (a uint8 device buffer, tensor-core
     path only; raises SSDError(SSD_ERR_UNSUPPORTED) otherwise) for ssd_backward(chunk_states=...),
     which then skips their recompute.  chunk_states: a caller-owned buffer to fill instead.
@@ -44,7 +47,8 @@ def ssd_forward(x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_states=Non
     if y is None:
         y = torch.empty(x.shape, dtype=x.dtype, device=x.device)
     if final_states is None and return_final_states:
-        final_states = torch.empty(S, H, P, N, dtype=torch.float32, device=x.device)
+        sdt = state_dtype or (initial_states.dtype if initial_states is not None else torch.float32)
+        final_states = torch.empty(S, H, P, N, dtype=sdt, device=x.device)
     prob = _lib.problem(Bsz, L, H, P, G, N, chunk_size, S if cu_seqlens is not None else 0, algo, seg_chunks)
     args = _lib.fwd_args(x, dt, A, B, C, y, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
                          final_states=final_states, cu_seqlens=cu_seqlens)
@@ -86,8 +90,8 @@ def ssd_backward(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, initial_state
         g["dz"] = torch.empty(z.shape, dtype=z.dtype, device=dev)
     if dt_bias is not None:
         g["ddt_bias"] = torch.empty(H, dtype=torch.float32, device=dev)
-    if initial_states is not None:
-        g["dinitial_states"] = torch.empty(S, H, P, N, dtype=torch.float32, device=dev)
+    if initial_states is not None:   # in the initial states' storage dtype
+        g["dinitial_states"] = torch.empty(S, H, P, N, dtype=initial_states.dtype, device=dev)
     prob = _lib.problem(Bsz, L, H, P, G, N, chunk_size, S if cu_seqlens is not None else 0, algo, seg_chunks,
                         bwd_heads)
     fa = _lib.fwd_args(x, dt, A, B, C, None, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,

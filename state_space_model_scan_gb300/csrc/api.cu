@@ -13,6 +13,7 @@ cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int
 cudaError_t launch_wait_probe(int32_t *hdr, int wait_ms, cudaStream_t st);
 cudaError_t launch_varlen_metadata(const int32_t *cu, int S, int L, int Q, int32_t *status, int32_t *chunk_begin,
                                    int32_t *segments, int32_t *seq_idx, cudaStream_t st);
+cudaError_t launch_states_cvt(const void *src, void *dst, int64_t n, bool to_f32, cudaStream_t st);
 cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr, const float *init,
                                    float *final_, cudaStream_t st);
 // simt_fwd.cu
@@ -105,6 +106,9 @@ struct Plan {
     size_t off_dt = 0, off_cs = 0, off_states = 0, off_dstates = 0, off_dBh = 0, off_dCh = 0, off_part = 0;
     size_t off_agg = 0, off_incl = 0, off_lam = 0, off_flags = 0;
     size_t chunk_state_bytes = 0;   // tensor-core path: one bf16 [P][N] tile per (chunk, head)
+    // fp32 copies of state tensors the caller stores in bf16: initial, final, dfinal, dinitial
+    size_t off_st32[4] = {0, 0, 0, 0};
+    bool st_bf16[4] = {false, false, false, false};
     size_t total = 0;
 };
 
@@ -165,10 +169,10 @@ ssd_status check_tensor(const ssd_tensor &t, int rank, int dtype_req, bool requi
     return SSD_OK;
 }
 
-// Contiguous [S, H, P, N] state tensors.
+// Contiguous [S, H, P, N] state tensors, fp32 or bf16.
 ssd_status check_state(const ssd_tensor &t, int64_t H, int64_t P, int64_t N) {
     if (t.ptr == nullptr) return SSD_OK;
-    if (t.dtype != SSD_F32) return SSD_ERR_INVALID_ARGUMENT;
+    if (t.dtype != SSD_F32 && t.dtype != SSD_BF16) return SSD_ERR_INVALID_ARGUMENT;
     if (t.stride[3] != 1 || t.stride[2] != N || t.stride[1] != P * N || t.stride[0] != H * P * N)
         return SSD_ERR_INVALID_ARGUMENT;
     return SSD_OK;
@@ -370,6 +374,14 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         pl.off_part = lay.take(sizeof(float) * kh * 4);
     }
     if (fused) pl.chunk_state_bytes = sizeof(__nv_bfloat16) * kh * (size_t)(P * N);
+    const size_t st_bytes = sizeof(float) * (size_t)S * (size_t)H * (size_t)(P * N);
+    const ssd_tensor *sts[4] = {&a->initial_states, bwd ? nullptr : &a->final_states,
+                                b != nullptr ? &b->dfinal_states : nullptr, b != nullptr ? &b->dinitial_states : nullptr};
+    for (int i = 0; i < 4; ++i)
+        if (sts[i] != nullptr && sts[i]->ptr != nullptr && sts[i]->dtype == SSD_BF16) {
+            pl.st_bf16[i] = true;
+            pl.off_st32[i] = lay.take(st_bytes);
+        }
     pl.total = lay.cur;
     *out = pl;
     return SSD_OK;
@@ -479,12 +491,19 @@ ssd_status ssd_fwd_debug_layout(const ssd_problem *prob, const ssd_fwd_args *arg
     return SSD_OK;
 }
 
-ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, size_t ws_bytes, void *stream) {
-    Plan pl;
-    SSD_TRY(plan_common(prob, a, false, &pl));
-    if (ws == nullptr || ws_bytes < pl.total) return SSD_ERR_WORKSPACE_TOO_SMALL;
-    if (((uintptr_t)ws) % kAlign != 0) return SSD_ERR_MISALIGNED;
-    cudaStream_t st = (cudaStream_t)stream;
+// A state tensor as the kernels take it: the caller's fp32 tensor, or the workspace's fp32
+// copy of a bf16 one.
+static ssd_tensor state32(const Plan &pl, int i, const ssd_tensor &t, void *ws) {
+    ssd_tensor r = t;
+    if (pl.st_bf16[i]) {
+        r.ptr = at<float>(ws, pl.off_st32[i]);
+        r.dtype = SSD_F32;
+    }
+    return r;
+}
+static int64_t state_elems(const Plan &pl) { return (int64_t)pl.sh.S * pl.sh.H * pl.sh.P * pl.sh.N; }
+
+static ssd_status fwd_impl(const Plan &pl, const ssd_fwd_args *a, void *ws, cudaStream_t st) {
     const Shape &sh = pl.sh;
     float *final_ = (float *)a->final_states.ptr;
     if (pl.algo == SSD_ALGO_SPLIT) {
@@ -569,12 +588,7 @@ ssd_status ssd_bwd_workspace_size(const ssd_problem *prob, const ssd_bwd_args *a
     return SSD_OK;
 }
 
-ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, size_t ws_bytes, void *stream) {
-    Plan pl;
-    SSD_TRY(plan_bwd(prob, b, &pl));
-    if (ws == nullptr || ws_bytes < pl.total) return SSD_ERR_WORKSPACE_TOO_SMALL;
-    if (((uintptr_t)ws) % kAlign != 0) return SSD_ERR_MISALIGNED;
-    cudaStream_t st = (cudaStream_t)stream;
+static ssd_status bwd_impl(const Plan &pl, const ssd_bwd_args *b, void *ws, cudaStream_t st) {
     const Shape &sh = pl.sh;
     const ssd_fwd_args *a = &b->fwd;
     if (pl.algo == SSD_ALGO_FUSED || pl.algo == SSD_ALGO_SPLIT) {
@@ -676,6 +690,40 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
         }
     }
     SSD_CUDA(launch_reduce_heads(sh, hdr, part, (float *)b->dA.ptr, (float *)b->dD.ptr, (float *)b->ddt_bias.ptr, st));
+    return SSD_OK;
+}
+
+ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, size_t ws_bytes, void *stream) {
+    Plan pl;
+    SSD_TRY(plan_common(prob, a, false, &pl));
+    if (ws == nullptr || ws_bytes < pl.total) return SSD_ERR_WORKSPACE_TOO_SMALL;
+    if (((uintptr_t)ws) % kAlign != 0) return SSD_ERR_MISALIGNED;
+    cudaStream_t st = (cudaStream_t)stream;
+    ssd_fwd_args a32 = *a;
+    a32.initial_states = state32(pl, 0, a->initial_states, ws);
+    a32.final_states = state32(pl, 1, a->final_states, ws);
+    const int64_t n = state_elems(pl);
+    if (pl.st_bf16[0]) SSD_CUDA(launch_states_cvt(a->initial_states.ptr, a32.initial_states.ptr, n, true, st));
+    SSD_TRY(fwd_impl(pl, &a32, ws, st));
+    if (pl.st_bf16[1]) SSD_CUDA(launch_states_cvt(a32.final_states.ptr, a->final_states.ptr, n, false, st));
+    return SSD_OK;
+}
+
+ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, size_t ws_bytes, void *stream) {
+    Plan pl;
+    SSD_TRY(plan_bwd(prob, b, &pl));
+    if (ws == nullptr || ws_bytes < pl.total) return SSD_ERR_WORKSPACE_TOO_SMALL;
+    if (((uintptr_t)ws) % kAlign != 0) return SSD_ERR_MISALIGNED;
+    cudaStream_t st = (cudaStream_t)stream;
+    ssd_bwd_args b32 = *b;
+    b32.fwd.initial_states = state32(pl, 0, b->fwd.initial_states, ws);
+    b32.dfinal_states = state32(pl, 2, b->dfinal_states, ws);
+    b32.dinitial_states = state32(pl, 3, b->dinitial_states, ws);
+    const int64_t n = state_elems(pl);
+    if (pl.st_bf16[0]) SSD_CUDA(launch_states_cvt(b->fwd.initial_states.ptr, b32.fwd.initial_states.ptr, n, true, st));
+    if (pl.st_bf16[2]) SSD_CUDA(launch_states_cvt(b->dfinal_states.ptr, b32.dfinal_states.ptr, n, true, st));
+    SSD_TRY(bwd_impl(pl, &b32, ws, st));
+    if (pl.st_bf16[3]) SSD_CUDA(launch_states_cvt(b32.dinitial_states.ptr, b->dinitial_states.ptr, n, false, st));
     return SSD_OK;
 }
 

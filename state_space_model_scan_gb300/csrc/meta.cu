@@ -388,4 +388,24 @@ cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, co
     return cudaGetLastError();
 }
 
+// State tensors stored in bf16 at the boundary: widened to fp32 before the scan reads them,
+// and the fp32 results rounded (nearest even) into the caller's bf16 tensor afterwards.
+__global__ void k_states_to_f32(const __nv_bfloat16 *src, float *dst, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = __bfloat162float(src[i]);
+}
+__global__ void k_states_to_bf16(const float *src, __nv_bfloat16 *dst, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = __float2bfloat16_rn(src[i]);
+}
+cudaError_t launch_states_cvt(const void *src, void *dst, int64_t n, bool to_f32, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
+    if (to_f32)
+        k_states_to_f32<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(src), static_cast<float *>(dst), n);
+    else
+        k_states_to_bf16<<<blocks, 256, 0, st>>>(static_cast<const float *>(src), static_cast<__nv_bfloat16 *>(dst), n);
+    return cudaGetLastError();
+}
+
 }  // namespace ssd
