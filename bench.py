@@ -666,6 +666,30 @@ def run_fwd_only(args):
                       "tokens_per_s": w.batch * w.seqlen / (sum(times) / len(times) * 1e-3)}))
 
 
+def run_extras_only(args):
+    """The kernels around the scan only (graph replays, L2 flushed before each): the command the
+    ncu captures of those kernels run."""
+    import torch
+    from state_space_model_scan_gb300 import inputs as I
+    dev = torch.device("cuda", torch.cuda.current_device())
+    s = torch.cuda.Stream(device=dev)
+    extras = build_extras(dev, s, I.named(WORKLOAD))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    times = {c["name"]: [] for c in extras}
+    for i in range(args.warmup + args.steps):
+        for c in extras:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                flush.fill_(float(i))
+                e0.record(s)
+                c["graph"].replay()
+                e1.record(s)
+            s.synchronize()
+            if i >= args.warmup:
+                times[c["name"]].append(e0.elapsed_time(e1))
+    print(json.dumps({"mode": "extras", "ms": {k: median(v) for k, v in times.items()}}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -673,7 +697,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="bench", choices=["bench", "fwd"])
+    ap.add_argument("--mode", default="bench", choices=["bench", "fwd", "extras"])
     ap.add_argument("--no-sweep", action="store_true", help="time the Nemotron-Nano workload only")
     ap.add_argument("--seg-chunks", type=int, default=0)
     args = ap.parse_args()
@@ -681,6 +705,8 @@ def main():
         args.warmup = 3
     if args.mode == "fwd":
         run_fwd_only(args)
+    elif args.mode == "extras":
+        run_extras_only(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
