@@ -97,173 +97,258 @@ struct SeqCursor {
     }
 };
 
-template <typename T, int K>
-__global__ void __launch_bounds__(CT)
-k_conv_fwd(const ConvArgs a) {
-    const int64_t c0 = ((int64_t)blockIdx.y * CT + threadIdx.x) * 8;
-    if (c0 >= a.Cn) return;
-    const int64_t b = blockIdx.x / a.tiles_per_row, t0 = (blockIdx.x % a.tiles_per_row) * TT;
-    const int64_t t1 = std::min(a.L, t0 + TT);
-    const T *u = static_cast<const T *>(a.u) + b * a.su_b + c0;
-    T *o = static_cast<T *>(a.out) + b * a.so_b + c0;
-    float w[K][8], bias[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        bias[e] = a.bias ? a.bias[c0 + e] : 0.f;
-#pragma unroll
-        for (int k = 0; k < K; ++k) w[k][e] = a.w[(c0 + e) * K + k];
-    }
-    SeqCursor cur;
-    cur.init(a, t0);
-    float ring[K][8];   // ring[k] = u[t - (K-1) + k] for the current t (k < K-1 filled before t)
-#pragma unroll
-    for (int k = 0; k < K - 1; ++k) {
-        const int64_t tp = t0 - (K - 1) + k;
-        if (tp >= cur.start) ld8(u + tp * a.su_l, ring[k]);
-        else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ring[k][e] = 0.f;
+// ---- staged sweeps.  A block covers TT tokens x CB channels (32 pieces of 8); its threads
+// first copy the tile (plus the K-1 rows before it, and for the backward after it) into
+// shared memory with cp.async -- a whole tile of loads in flight at once -- and then thread
+// (piece j, token group g) sweeps its 8 channels over TG = 8 tokens (forward, 256 threads) or
+// TGB = 16 tokens (backward, 128 threads: its larger per-thread state allows two blocks per
+// SM only at that size) from shared memory.
+constexpr int CB = 256;              // channels per block (32 pieces of 8)
+constexpr int TG = TT / (CT / 32);   // tokens per thread: 8
+constexpr int CTB = 128;             // backward: threads per block (two blocks per SM) ...
+constexpr int TGB = TT / (CTB / 32); // ... and tokens per thread: 16
+#define TAPS_BYTES(K) ((size_t)((K) + 1) * CB * sizeof(float))   // staged taps and bias
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+// Copies rows [tb, tb + nrows) of a [L][channels] token matrix (row stride sl elements),
+// channels [cbase, cbase + CB), into `dst` (row r at r * 32 pieces); rows outside [0, L) and
+// channels past Cn are not copied (never read unmasked).
+template <typename T>
+__device__ __forceinline__ void stage_rows(const T *src, int64_t sl, int64_t tb, int nrows, int64_t L, int64_t cbase,
+                                           int64_t Cn, T *dst) {
+    for (int i = threadIdx.x; i < nrows * 32; i += blockDim.x) {
+        const int r = i >> 5, j = i & 31;
+        const int64_t t = tb + r, c = cbase + 8 * j;
+        if (t >= 0 && t < L && c < Cn) {
+            const T *g = src + t * sl + c;
+            T *d = dst + (int64_t)r * (32 * 8) + 8 * j;
+            if (sizeof(T) == 2) {
+                cp_async16(d, g);
+            } else {
+                cp_async16(d, g);
+                cp_async16(d + 4, g + 4);
+            }
         }
     }
-    for (int64_t t = t0; t < t1; ++t) {
-        if (cur.advance(a, t)) {   // a new sequence: nothing before it counts
+    cp_async_commit_wait();
+}
+
+template <typename T>
+__device__ __forceinline__ void lds8(const T *p, float *v) { ld8(p, v); }
+
+// logistic function with the fast exponential and divide (relative error ~1e-6; 1/inf = 0
+// gives the right limit for very negative arguments)
+__device__ __forceinline__ float sig_fast(float v) { return __fdividef(1.f, 1.f + __expf(-v)); }
+
+// The block's taps and biases, staged once in shared memory as [k][channel] (then [K][c] =
+// the bias): weight [Cn][K] holds channels cbase .. cbase+255 as 256K contiguous floats, read
+// with consecutive threads on consecutive floats; a thread then reads its 8 channels of tap k
+// as two 16-byte pieces.
+template <int K>
+__device__ __forceinline__ void stage_taps(const float *w, const float *bias, int64_t cbase, int64_t Cn, float *ws) {
+    const int64_t nch = std::min<int64_t>(CB, Cn - cbase);
+    for (int i = threadIdx.x; i < CB * K; i += blockDim.x) {
+        const int c = i / K, k = i % K;
+        ws[k * CB + c] = c < nch ? w[cbase * K + i] : 0.f;
+    }
+    for (int c = threadIdx.x; c < CB; c += blockDim.x)
+        ws[K * CB + c] = (bias != nullptr && c < nch) ? bias[cbase + c] : 0.f;
+}
+template <int K>
+__device__ __forceinline__ void read_taps(const float *ws, int j, float (&wt)[K][8], float (&bs)[8]) {
 #pragma unroll
-            for (int k = 0; k < K - 1; ++k)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ring[k][e] = 0.f;
-        }
-        ld8(u + t * a.su_l, ring[K - 1]);
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float acc = bias[e];
-#pragma unroll
-            for (int k = 0; k < K; ++k) acc = fmaf(w[k][e], ring[k][e], acc);
-            v[e] = a.silu ? acc * sigmoid_f(acc) : acc;
-        }
-        st8(o + t * a.so_l, v);
-#pragma unroll
-        for (int k = 0; k < K - 1; ++k)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ring[k][e] = ring[k + 1][e];
+    for (int k = 0; k <= K; ++k) {
+        const float4 lo = reinterpret_cast<const float4 *>(ws + k * CB + 8 * j)[0];
+        const float4 hi = reinterpret_cast<const float4 *>(ws + k * CB + 8 * j)[1];
+        float *dst = k < K ? wt[k < K ? k : 0] : bs;
+        dst[0] = lo.x; dst[1] = lo.y; dst[2] = lo.z; dst[3] = lo.w;
+        dst[4] = hi.x; dst[5] = hi.y; dst[6] = hi.z; dst[7] = hi.w;
     }
 }
 
-// Backward over the tile [t0, t1): the sweep runs t from t0 to t1 + K - 2 computing
-// g[t] = dout[t] act'(pre[t]); g[t] reaches du[t - (K-1) + k] (same sequence) for every k;
-// du[t'] is complete once t passes t' + K - 1 and leaves then.  dw and dbias take the tile's
-// tokens t in [t0, t1).
 template <typename T, int K>
 __global__ void __launch_bounds__(CT)
-k_conv_bwd(const ConvArgs a) {
-    const int64_t c0 = ((int64_t)blockIdx.y * CT + threadIdx.x) * 8;
-    if (c0 >= a.Cn) return;
+k_conv_fwd(const ConvArgs a) {
+    extern __shared__ __align__(16) uint8_t conv_sm[];
+    float *ws = reinterpret_cast<float *>(conv_sm);                  // taps [K][CB], bias [CB]
+    T *tile = reinterpret_cast<T *>(conv_sm + TAPS_BYTES(K));        // rows t0-(K-1) .. t0+TT-1
+    const int j = threadIdx.x & 31, grp = threadIdx.x >> 5;
+    const int64_t cbase = (int64_t)blockIdx.y * CB, c0 = cbase + 8 * j;
     const int64_t b = blockIdx.x / a.tiles_per_row, t0 = (blockIdx.x % a.tiles_per_row) * TT;
-    const int64_t t1 = std::min(a.L, t0 + TT);
-    const T *u = static_cast<const T *>(a.u) + b * a.su_b + c0;
-    const T *d = static_cast<const T *>(a.dout) + b * a.sd_b + c0;
-    T *du = static_cast<T *>(a.du) + b * a.sdu_b + c0;
+    const int64_t tb = t0 - (K - 1);
+    stage_taps<K>(a.w, a.bias, cbase, a.Cn, ws);
+    stage_rows(static_cast<const T *>(a.u) + b * a.su_b, a.su_l, tb, TT + K - 1, a.L, cbase, a.Cn, tile);
+    __syncthreads();
+    if (c0 >= a.Cn) return;
+    const int64_t s0 = t0 + (int64_t)grp * TG, s1 = std::min(a.L, s0 + TG);   // this thread's tokens
+    if (s0 >= s1) return;
+    T *o = static_cast<T *>(a.out) + b * a.so_b + c0;
     float w[K][8], bias[8];
+    read_taps<K>(ws, j, w, bias);
+    SeqCursor cur;
+    cur.init(a, s0);
+    const T *col = tile + 8 * j;   // row t at (t - tb) * 256 (offsets below fit 32 bits)
+    for (int64_t t = s0; t < s1; ++t) {
+        cur.advance(a, t);
+        float acc[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        bias[e] = a.bias ? a.bias[c0 + e] : 0.f;
+        for (int e = 0; e < 8; ++e) acc[e] = bias[e];
 #pragma unroll
-        for (int k = 0; k < K; ++k) w[k][e] = a.w[(c0 + e) * K + k];
+        for (int k = 0; k < K; ++k) {
+            const int64_t tp = t - (K - 1) + k;   // u[tp] feeds pre[t] when in t's sequence
+            if (tp >= cur.start) {
+                float v[8];
+                lds8(col + (int)(tp - tb) * 256, v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(w[k][e], v[e], acc[e]);
+            }
+        }
+        if (a.silu) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] *= sig_fast(acc[e]);
+        }
+        st8(o + t * a.so_l, acc);
     }
-    float dw[K][8], db[8];
+}
+
+// Backward over the thread's tokens [s0, s1): the sweep runs t from s0 to s1 + K - 2 computing
+// g[t] = dout[t] act'(pre[t]); g[t] reaches du[t - (K-1) + k] (same sequence) for every k;
+// du[t'] is complete once t passes t' + K - 1 and leaves then.  dw and dbias take the thread's
+// tokens t in [s0, s1); the eight token groups' shares are summed in order in shared memory.
+template <typename T, int K>
+__global__ void __launch_bounds__(CTB)
+k_conv_bwd(const ConvArgs a) {
+    extern __shared__ __align__(16) uint8_t conv_sm[];
+    constexpr int RU = TT + 2 * (K - 1), RD = TT + K - 1;
+    float *ws = reinterpret_cast<float *>(conv_sm);                    // taps [K][CB], bias [CB]
+    T *tu = reinterpret_cast<T *>(conv_sm + TAPS_BYTES(K));            // u rows t0-(K-1) .. t0+TT+K-2
+    T *td = tu + RU * 256;                                             // dout rows t0 .. t0+TT+K-2
+    float *red = reinterpret_cast<float *>(conv_sm + TAPS_BYTES(K));   // after the sweep: [group][K+1][256]
+    const int j = threadIdx.x & 31, grp = threadIdx.x >> 5;
+    const int64_t cbase = (int64_t)blockIdx.y * CB, c0 = cbase + 8 * j;
+    const int64_t b = blockIdx.x / a.tiles_per_row, t0 = (blockIdx.x % a.tiles_per_row) * TT;
+    const int64_t tb = t0 - (K - 1);
+    stage_taps<K>(a.w, a.bias, cbase, a.Cn, ws);
+    stage_rows(static_cast<const T *>(a.u) + b * a.su_b, a.su_l, tb, RU, a.L, cbase, a.Cn, tu);
+    stage_rows(static_cast<const T *>(a.dout) + b * a.sd_b, a.sd_l, t0, RD, a.L, cbase, a.Cn, td);
+    __syncthreads();
+    const bool live = c0 < a.Cn;
+    const int64_t s0 = t0 + (int64_t)grp * TGB, s1 = std::min(a.L, s0 + TGB);
+    float w[K][8], bias[8], dw[K][8], db[8];
+    read_taps<K>(ws, j, w, bias);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         db[e] = 0.f;
 #pragma unroll
         for (int k = 0; k < K; ++k) dw[k][e] = 0.f;
     }
-    SeqCursor cur;
-    cur.init(a, t0);
-    float ring[K][8];   // inputs u[t - (K-1) + k]
-    float acc[K][8];    // du[t - (K-1) + k] being summed
+    if (live && s0 < s1) {
+        T *du = static_cast<T *>(a.du) + b * a.sdu_b + c0;
+        const T *ucol = tu + 8 * j, *dcol = td + 8 * j;
+        SeqCursor cur;
+        cur.init(a, s0);
+        float ring[K][8];   // inputs u[t - (K-1) + k]
+        float acc[K][8];    // du[t - (K-1) + k] being summed
 #pragma unroll
-    for (int k = 0; k < K; ++k)
+        for (int k = 0; k < K; ++k)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
+            for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
 #pragma unroll
-    for (int k = 0; k < K - 1; ++k) {
-        const int64_t tp = t0 - (K - 1) + k;
-        if (tp >= cur.start) ld8(u + tp * a.su_l, ring[k]);
-        else {
+        for (int k = 0; k < K - 1; ++k) {
+            const int64_t tp = s0 - (K - 1) + k;
+            if (tp >= cur.start) lds8(ucol + (int)(tp - tb) * 256, ring[k]);
+            else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ring[k][e] = 0.f;
+                for (int e = 0; e < 8; ++e) ring[k][e] = 0.f;
+            }
         }
-    }
-    const int64_t tend = std::min(a.L, t1 + K - 1);
-    for (int64_t t = t0; t < tend; ++t) {
-        if (cur.advance(a, t)) {
+        const int64_t tend = std::min(a.L, s1 + K - 1);
+        for (int64_t t = s0; t < tend; ++t) {
+            if (cur.advance(a, t)) {
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ring[k][e] = 0.f;
+            }
+            lds8(ucol + (int)(t - tb) * 256, ring[K - 1]);
+            float dv[8];
+            lds8(dcol + (int)(t - t0) * 256, dv);
+            float g[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float pre = bias[e];
+#pragma unroll
+                for (int k = 0; k < K; ++k) pre = fmaf(w[k][e], ring[k][e], pre);
+                if (a.silu) {
+                    const float sg = sig_fast(pre);
+                    g[e] = dv[e] * sg * (1.f + pre * (1.f - sg));
+                } else {
+                    g[e] = dv[e];
+                }
+            }
+            const bool own = t < s1;   // this thread's token: its dw / dbias shares
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int64_t tp = t - (K - 1) + k;
+                if (tp >= cur.start) {   // u[tp] fed pre[t] (same sequence)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        acc[k][e] = fmaf(w[k][e], g[e], acc[k][e]);
+                        if (own) dw[k][e] = fmaf(g[e], ring[k][e], dw[k][e]);
+                    }
+                }
+            }
+            if (own) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) db[e] += g[e];
+            }
+            const int64_t tdone = t - (K - 1);   // du[tdone] has all its contributions now
+            if (tdone >= s0 && tdone < s1) st8(du + tdone * a.sdu_l, acc[0]);
 #pragma unroll
             for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ring[k][e] = 0.f;
-        }
-        ld8(u + t * a.su_l, ring[K - 1]);
-        float dv[8];
-        ld8(d + t * a.sd_l, dv);
-        float g[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float pre = bias[e];
-#pragma unroll
-            for (int k = 0; k < K; ++k) pre = fmaf(w[k][e], ring[k][e], pre);
-            if (a.silu) {
-                const float sg = sigmoid_f(pre);
-                g[e] = dv[e] * sg * (1.f + pre * (1.f - sg));
-            } else {
-                g[e] = dv[e];
-            }
-        }
-        const bool own = t < t1;   // this tile's token: its dw / dbias shares
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-            const int64_t tp = t - (K - 1) + k;
-            if (tp >= cur.start) {   // u[tp] fed pre[t] (same sequence)
-#pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    acc[k][e] = fmaf(w[k][e], g[e], acc[k][e]);
-                    if (own) dw[k][e] = fmaf(g[e], ring[k][e], dw[k][e]);
+                    ring[k][e] = ring[k + 1][e];
+                    acc[k][e] = acc[k + 1][e];
                 }
-            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[K - 1][e] = 0.f;
         }
-        if (own) {
+        // the last rows, whose windows would run past the end of the row: acc[0] now holds
+        // du[tend - (K-1)]; rows before s0 are skipped over
+        for (int64_t tdone = tend - (K - 1); tdone < s1; ++tdone) {
+            if (tdone >= s0) st8(du + tdone * a.sdu_l, acc[0]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) db[e] += g[e];
+            for (int k = 0; k < K - 1; ++k)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[k][e] = acc[k + 1][e];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[K - 1][e] = 0.f;
         }
-        // du[t - (K-1)] has all its contributions now
-        const int64_t tdone = t - (K - 1);
-        if (tdone >= t0 && tdone < t1) st8(du + tdone * a.sdu_l, acc[0]);
-#pragma unroll
-        for (int k = 0; k < K - 1; ++k)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                ring[k][e] = ring[k + 1][e];
-                acc[k][e] = acc[k + 1][e];
-            }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[K - 1][e] = 0.f;
     }
-    // the tile's last rows, whose windows would run past the end of the row: acc[0] now holds
-    // du[tend - (K-1)]; rows before t0 are skipped over
-    for (int64_t tdone = tend - (K - 1); tdone < t1; ++tdone) {
-        if (tdone >= t0) st8(du + tdone * a.sdu_l, acc[0]);
-#pragma unroll
-        for (int k = 0; k < K - 1; ++k)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[k][e] = acc[k + 1][e];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[K - 1][e] = 0.f;
-    }
-    float *pp = a.partials + (int64_t)blockIdx.x * a.Cn * (K + 1);
+    __syncthreads();   // the staged tiles are no longer read: reuse them for the group sums
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
 #pragma unroll
-        for (int k = 0; k < K; ++k) pp[(c0 + e) * (K + 1) + k] = dw[k][e];
-        pp[(c0 + e) * (K + 1) + K] = db[e];
+        for (int k = 0; k < K; ++k) red[((grp * (K + 1)) + k) * 256 + 8 * j + e] = dw[k][e];
+        red[((grp * (K + 1)) + K) * 256 + 8 * j + e] = db[e];
+    }
+    __syncthreads();
+    float *pp = a.partials + (int64_t)blockIdx.x * a.Cn * (K + 1);
+    for (int i = threadIdx.x; i < 256 * (K + 1); i += CTB) {
+        const int c = i / (K + 1), k = i % (K + 1);   // channel within the block, tap (K: bias)
+        if (cbase + c >= a.Cn) continue;
+        float sum = 0.f;
+        for (int q = 0; q < CTB / 32; ++q) sum += red[(q * (K + 1) + k) * 256 + c];
+        pp[(cbase + c) * (K + 1) + k] = sum;
     }
 }
 
@@ -279,33 +364,58 @@ __global__ void k_conv_dw(const float *partials, int64_t tiles, int64_t Cn, int 
     }
 }
 
+template <typename T, int K>
+size_t fwd_smem() { return TAPS_BYTES(K) + (size_t)(TT + K - 1) * 256 * sizeof(T); }
+template <typename T, int K>
+size_t bwd_smem() {
+    const size_t stage = (size_t)(2 * TT + 3 * (K - 1)) * 256 * sizeof(T);
+    const size_t red = (size_t)(CTB / 32) * (K + 1) * 256 * sizeof(float);
+    return TAPS_BYTES(K) + (stage > red ? stage : red);
+}
+template <typename T, int K>
+cudaError_t launch_fwd_k(const ConvArgs &a, dim3 grid, cudaStream_t st) {
+    static int attr[64] = {0};
+    const size_t sm = fwd_smem<T, K>();
+    cudaError_t e = ensure_smem_attr(k_conv_fwd<T, K>, (int)sm, attr);
+    if (e != cudaSuccess) return e;
+    k_conv_fwd<T, K><<<grid, CT, sm, st>>>(a);
+    return cudaGetLastError();
+}
+template <typename T, int K>
+cudaError_t launch_bwd_k(const ConvArgs &a, dim3 grid, cudaStream_t st) {
+    static int attr[64] = {0};
+    const size_t sm = bwd_smem<T, K>();
+    cudaError_t e = ensure_smem_attr(k_conv_bwd<T, K>, (int)sm, attr);
+    if (e != cudaSuccess) return e;
+    k_conv_bwd<T, K><<<grid, CTB, sm, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_fwd(const ConvArgs &a, dim3 grid, cudaStream_t st) {
     switch (a.K) {
-        case 1: k_conv_fwd<T, 1><<<grid, CT, 0, st>>>(a); break;
-        case 2: k_conv_fwd<T, 2><<<grid, CT, 0, st>>>(a); break;
-        case 3: k_conv_fwd<T, 3><<<grid, CT, 0, st>>>(a); break;
-        case 4: k_conv_fwd<T, 4><<<grid, CT, 0, st>>>(a); break;
-        case 5: k_conv_fwd<T, 5><<<grid, CT, 0, st>>>(a); break;
-        case 6: k_conv_fwd<T, 6><<<grid, CT, 0, st>>>(a); break;
-        case 7: k_conv_fwd<T, 7><<<grid, CT, 0, st>>>(a); break;
-        default: k_conv_fwd<T, 8><<<grid, CT, 0, st>>>(a); break;
+        case 1: return launch_fwd_k<T, 1>(a, grid, st);
+        case 2: return launch_fwd_k<T, 2>(a, grid, st);
+        case 3: return launch_fwd_k<T, 3>(a, grid, st);
+        case 4: return launch_fwd_k<T, 4>(a, grid, st);
+        case 5: return launch_fwd_k<T, 5>(a, grid, st);
+        case 6: return launch_fwd_k<T, 6>(a, grid, st);
+        case 7: return launch_fwd_k<T, 7>(a, grid, st);
+        default: return launch_fwd_k<T, 8>(a, grid, st);
     }
-    return cudaGetLastError();
 }
 template <typename T>
 cudaError_t launch_bwd(const ConvArgs &a, dim3 grid, cudaStream_t st) {
     switch (a.K) {
-        case 1: k_conv_bwd<T, 1><<<grid, CT, 0, st>>>(a); break;
-        case 2: k_conv_bwd<T, 2><<<grid, CT, 0, st>>>(a); break;
-        case 3: k_conv_bwd<T, 3><<<grid, CT, 0, st>>>(a); break;
-        case 4: k_conv_bwd<T, 4><<<grid, CT, 0, st>>>(a); break;
-        case 5: k_conv_bwd<T, 5><<<grid, CT, 0, st>>>(a); break;
-        case 6: k_conv_bwd<T, 6><<<grid, CT, 0, st>>>(a); break;
-        case 7: k_conv_bwd<T, 7><<<grid, CT, 0, st>>>(a); break;
-        default: k_conv_bwd<T, 8><<<grid, CT, 0, st>>>(a); break;
+        case 1: return launch_bwd_k<T, 1>(a, grid, st);
+        case 2: return launch_bwd_k<T, 2>(a, grid, st);
+        case 3: return launch_bwd_k<T, 3>(a, grid, st);
+        case 4: return launch_bwd_k<T, 4>(a, grid, st);
+        case 5: return launch_bwd_k<T, 5>(a, grid, st);
+        case 6: return launch_bwd_k<T, 6>(a, grid, st);
+        case 7: return launch_bwd_k<T, 7>(a, grid, st);
+        default: return launch_bwd_k<T, 8>(a, grid, st);
     }
-    return cudaGetLastError();
 }
 
 bool al16(const void *p) { return ((uintptr_t)p) % 16 == 0; }
@@ -364,7 +474,7 @@ ssd_status ssd_conv1d_fwd(const ssd_conv_problem *p, const void *x, int64_t x_sb
     if (p->seqlen == 0) return SSD_OK;
     ConvArgs a = make_args(p, weight, bias, cu_seqlens);
     a.u = x; a.su_b = x_sb; a.su_l = x_sl; a.out = out; a.so_b = out_sb; a.so_l = out_sl;
-    const dim3 grid((unsigned)(a.B * a.tiles_per_row), (unsigned)((a.Cn / 8 + CT - 1) / CT));
+    const dim3 grid((unsigned)(a.B * a.tiles_per_row), (unsigned)((a.Cn + CB - 1) / CB));
     cudaStream_t st = (cudaStream_t)stream;
     const cudaError_t e = p->dtype == SSD_BF16 ? launch_fwd<__nv_bfloat16>(a, grid, st) : launch_fwd<float>(a, grid, st);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
@@ -396,7 +506,7 @@ ssd_status ssd_conv1d_bwd(const ssd_conv_problem *p, const void *x, int64_t x_sb
     a.u = x; a.su_b = x_sb; a.su_l = x_sl; a.dout = dout; a.sd_b = dout_sb; a.sd_l = dout_sl;
     a.du = dx; a.sdu_b = dx_sb; a.sdu_l = dx_sl; a.partials = static_cast<float *>(workspace);
     if (tiles > 0) {
-        const dim3 grid((unsigned)tiles, (unsigned)((a.Cn / 8 + CT - 1) / CT));
+        const dim3 grid((unsigned)tiles, (unsigned)((a.Cn + CB - 1) / CB));
         const cudaError_t e =
             p->dtype == SSD_BF16 ? launch_bwd<__nv_bfloat16>(a, grid, st) : launch_bwd<float>(a, grid, st);
         if (e != cudaSuccess) return SSD_ERR_CUDA;
