@@ -55,13 +55,14 @@ def workload_desc(w):
                                                   w.chunk_size))
 
 
-def algorithmic_bytes(w, fwd=True):
-    """Compulsory HBM bytes of one forward (or backward) of workload w."""
+def algorithmic_bytes(w, fwd=True, state_bytes=4):
+    """Compulsory HBM bytes of one forward (or backward) of workload w (states stored in
+    `state_bytes` per element)."""
     b_x = 2 if w.dtype == "bf16" else 4
     T = w.batch * w.seqlen
     per_tok_heads = w.nheads * w.headdim * b_x
     bc = 2 * w.ngroups * w.dstate * b_x
-    st = w.nseqs * w.nheads * w.headdim * w.dstate * 4
+    st = w.nseqs * w.nheads * w.headdim * w.dstate * state_bytes
     if fwd:
         n = T * ((3 if w.has_z else 2) * per_tok_heads + bc + 4 * w.nheads) + st   # x, z, y, B, C, dt, final
         if w.has_init:
@@ -321,10 +322,10 @@ def run_reference(args):
     print(json.dumps(line))
 
 
-def sweep_bytes(w):
+def sweep_bytes(w, state_bytes=4):
     """Algorithmic HBM bytes of one forward of workload w (inputs read once, y and the
     states written once, initial states read once)."""
-    return algorithmic_bytes(w, fwd=True)
+    return algorithmic_bytes(w, fwd=True, state_bytes=state_bytes)
 
 
 def build_extras(dev, s, w):
@@ -444,11 +445,20 @@ def run_gpu(args):
     # the other forward workloads: the long-sequence sweep and the packed varlen batch
     sweep = []
     if not args.no_sweep:
-        for sw in [I.named("long_seq", L=n) for n in (1024, 2048, 4096, 8192, 16384, 32768)] + [I.named("varlen")]:
+        import dataclasses
+        variants = ([(I.named("long_seq", L=n), torch.float32) for n in (1024, 2048, 4096, 8192, 16384, 32768)] +
+                    [(I.named("varlen"), torch.float32),
+                     # the variants: dstate 64 on the tensor-core path, and bf16 state storage
+                     (dataclasses.replace(w, name="nemotron_nano_dstate64", dstate=64), torch.float32),
+                     (dataclasses.replace(I.named("long_seq", L=8192), name="long_seq_L8192_bf16_states"),
+                      torch.bfloat16)])
+        for sw, sdt in variants:
             si = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in I.make_inputs(sw).items()}
+            if si["initial_states"] is not None:
+                si["initial_states"] = si["initial_states"].to(sdt)
             S = sw.nseqs
             sy = torch.empty_like(si["x"])
-            sfin = torch.empty(S, sw.nheads, sw.headdim, sw.dstate, device=dev)
+            sfin = torch.empty(S, sw.nheads, sw.headdim, sw.dstate, dtype=sdt, device=dev)
             sprob = _lib.problem(sw.batch, sw.seqlen, sw.nheads, sw.headdim, sw.ngroups, sw.dstate, sw.chunk_size,
                                  S if si["cu_seqlens"] is not None else 0)
             sargs = _lib.fwd_args(si["x"], si["dt_raw"], si["A"], si["B"], si["C"], sy, D=si["D"], z=si["z"],
@@ -461,9 +471,11 @@ def run_gpu(args):
             sg = torch.cuda.CUDAGraph()
             with torch.cuda.graph(sg, stream=s):
                 _lib.check(_lib.ssd_fwd(sprob, sargs, sws, torch.cuda.current_stream()), "ssd_fwd")
-            # metadata + fused forward, + the empty-sequence final states of a packed batch
-            sweep.append(dict(w=sw, graph=sg, keep=(si, sy, sfin, sws, sargs),
-                              launches=3 if si["cu_seqlens"] is not None else 2))
+            # metadata + forward (+ the empty-sequence final states of a packed batch, + the state
+            # conversions of bf16 or dstate-64 states)
+            conv = (1 if sdt == torch.bfloat16 or sw.dstate != 128 else 0) * (1 + (si["initial_states"] is not None))
+            sweep.append(dict(w=sw, graph=sg, keep=(si, sy, sfin, sws, sargs), state_bytes=2 if sdt == torch.bfloat16 else 4,
+                              launches=(3 if si["cu_seqlens"] is not None else 2) + conv))
 
     # the steps next to the scan: the gated RMS normalisation after it and the conv1d over the
     # packed xBC before it (Nemotron-Nano widths, 8192 tokens, bf16), and the complex-A scan of
@@ -596,8 +608,9 @@ def run_gpu(args):
     sweep_out = []
     for c, ms in zip(sweep, sweep_ms):
         sw = c["w"]
-        b = sweep_bytes(sw)
+        b = sweep_bytes(sw, c["state_bytes"])
         sweep_out.append({"workload": sw.name, "seqlen": sw.seqlen, "nseqs": sw.nseqs, "nheads": sw.nheads,
+                          "dstate": sw.dstate, "state_dtype": "bf16" if c["state_bytes"] == 2 else "f32",
                           "chunk_size": sw.chunk_size, "fwd_ms": ms, "tokens_per_s": sw.batch * sw.seqlen / (ms * 1e-3),
                           "algorithmic_bytes": b, "achieved_gbs": b / (ms * 1e-3) / 1e9,
                           "roofline_frac": b / (ms * 1e-3) / 1e9 / peak})

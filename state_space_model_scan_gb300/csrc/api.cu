@@ -13,7 +13,8 @@ cudaError_t launch_build_meta(const int32_t *cu, int B, int L, int S, int Q, int
 cudaError_t launch_wait_probe(int32_t *hdr, int wait_ms, cudaStream_t st);
 cudaError_t launch_varlen_metadata(const int32_t *cu, int S, int L, int Q, int32_t *status, int32_t *chunk_begin,
                                    int32_t *segments, int32_t *seq_idx, cudaStream_t st);
-cudaError_t launch_states_cvt(const void *src, void *dst, int64_t n, bool to_f32, cudaStream_t st);
+cudaError_t launch_states_cvt(const void *src, bool src_bf16, int src_n, void *dst, bool dst_bf16, int dst_n,
+                              int64_t rows, cudaStream_t st);
 cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, const int32_t *hdr, const float *init,
                                    float *final_, cudaStream_t st);
 // simt_fwd.cu
@@ -106,7 +107,8 @@ struct Plan {
     size_t off_dt = 0, off_cs = 0, off_states = 0, off_dstates = 0, off_dBh = 0, off_dCh = 0, off_part = 0;
     size_t off_agg = 0, off_incl = 0, off_lam = 0, off_flags = 0;
     size_t chunk_state_bytes = 0;   // tensor-core path: one bf16 [P][N] tile per (chunk, head)
-    // fp32 copies of state tensors the caller stores in bf16: initial, final, dfinal, dinitial
+    // fp32 [.., N] copies of state tensors stored otherwise (bf16, or dstate 64 on the tensor-core
+    // path): initial, final, dfinal, dinitial
     size_t off_st32[4] = {0, 0, 0, 0};
     bool st_bf16[4] = {false, false, false, false};
     size_t total = 0;
@@ -235,7 +237,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     // dstate 128 whose x/B/C/z/y obey the 16-byte rule of TMA and vector access;
     // everything else (fp32 inputs in particular) runs the SIMT pipeline.  The
     // backward follows the same choice, with dy/dx/dz/dB/dC under the same rule.
-    bool tc_ok = pl.bf16 && P == 64 && N == 128;
+    bool tc_ok = pl.bf16 && P == 64 && (N == 128 || N == 64);
     bool aligned = true;
     {
         const ssd_tensor *ts[10] = {&a->x, &a->B, &a->C, &a->z, bwd ? nullptr : &a->y, b ? &b->dy : nullptr,
@@ -273,6 +275,9 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         if (((uintptr_t)a->chunk_states) % 16 != 0) return SSD_ERR_MISALIGNED;
     }
     const int Q = fused ? kTcQ : kSimtQ;
+    // dstate the kernels compute: the tensor-core tiles are N = 128; dstate 64 runs as the zero-
+    // extended half (TMA fills the B/C columns past 64 with zeros; states are padded copies)
+    const int64_t Nk = fused ? 128 : N;
     if (fused && bwd && b == nullptr) return SSD_ERR_INVALID_ARGUMENT;
     int64_t kmax = varlen ? (L + Q - 1) / Q + S : B * ((L + Q - 1) / Q);
     if (kmax > (int64_t)1 << 30) return SSD_ERR_UNSUPPORTED;
@@ -307,7 +312,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         umax = per + S;
     }
     Shape sh;
-    sh.B = (int)B; sh.L = (int)L; sh.H = (int)H; sh.P = (int)P; sh.G = (int)G; sh.N = (int)N; sh.S = (int)S;
+    sh.B = (int)B; sh.L = (int)L; sh.H = (int)H; sh.P = (int)P; sh.G = (int)G; sh.N = (int)Nk; sh.Nio = (int)N; sh.S = (int)S;
     sh.Q = Q; sh.hpg = (int)(H / G); sh.kmax = (int)kmax; sh.umax = (int)umax; sh.R = R; sh.useg_num = num; sh.useg_den = den;
     pl.sh = sh;
     Layout lay;
@@ -320,12 +325,12 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         if (!split) {   // the single-pass forward's work units and their exchange buffers
             const size_t uh = (size_t)umax * (size_t)H;
             pl.off_units = lay.take(sizeof(UnitInfo) * (size_t)umax);
-            pl.off_agg = lay.take(sizeof(float) * uh * (size_t)(P * N));
-            pl.off_incl = lay.take(sizeof(float) * uh * (size_t)(P * N));
+            pl.off_agg = lay.take(sizeof(float) * uh * (size_t)(P * Nk));
+            pl.off_incl = lay.take(sizeof(float) * uh * (size_t)(P * Nk));
             pl.off_lam = lay.take(sizeof(float) * uh);
             pl.off_flags = lay.take(sizeof(uint32_t) * uh);
         } else if (!bwd) {   // the split forward: carried-state tiles (unless kept) and tile log-decays
-            if (a->chunk_states == nullptr) pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * N));
+            if (a->chunk_states == nullptr) pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * Nk));
             pl.off_cs = lay.take(sizeof(float) * kh);
         }
         if (bwd) {
@@ -351,34 +356,34 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
             }
             pl.n_items = pl.k_pairs * nsub_main + (int)(pairs - pl.k_pairs) * pl.nsub_tail;
             const int64_t tail_items = nsub_main == 1 && pl.nsub_tail > 1 ? (pairs - pl.k_pairs) * pl.nsub_tail : 0;
-            pl.off_tpart = lay.take(sizeof(float) * (size_t)tail_items * 2 * Q * (size_t)N);
+            pl.off_tpart = lay.take(sizeof(float) * (size_t)tail_items * 2 * Q * (size_t)Nk);
             // dB/dC shares of head subsets, only when a CTA covers part of a group
             const size_t ksub = pl.hs < sh.hpg ? (size_t)kmax * (size_t)(H / pl.hs) : 0;
             if (a->chunk_states == nullptr)   // carried states, bf16, unless the forward kept them
-                pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * N));
-            pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * N));
+                pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * Nk));
+            pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * Nk));
             pl.off_cs = lay.take(sizeof(float) * kh);                                // chunk total log-decay
-            pl.off_dBh = lay.take(sizeof(float) * ksub * Q * (size_t)N);
-            pl.off_dCh = lay.take(sizeof(float) * ksub * Q * (size_t)N);
+            pl.off_dBh = lay.take(sizeof(float) * ksub * Q * (size_t)Nk);
+            pl.off_dCh = lay.take(sizeof(float) * ksub * Q * (size_t)Nk);
             pl.off_part = lay.take(sizeof(float) * kh * 4);
         }
     } else {
         pl.off_dt = lay.take(sizeof(float) * kh * Q);
         pl.off_cs = lay.take(sizeof(float) * kh * Q);
-        pl.off_states = lay.take(sizeof(float) * kh * (size_t)(P * N));
+        pl.off_states = lay.take(sizeof(float) * kh * (size_t)(P * Nk));
     }
     if (bwd && !fused) {
-        pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * N));
-        pl.off_dBh = lay.take(sizeof(float) * kh * Q * (size_t)N);
-        pl.off_dCh = lay.take(sizeof(float) * kh * Q * (size_t)N);
+        pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * Nk));
+        pl.off_dBh = lay.take(sizeof(float) * kh * Q * (size_t)Nk);
+        pl.off_dCh = lay.take(sizeof(float) * kh * Q * (size_t)Nk);
         pl.off_part = lay.take(sizeof(float) * kh * 4);
     }
-    if (fused) pl.chunk_state_bytes = sizeof(__nv_bfloat16) * kh * (size_t)(P * N);
-    const size_t st_bytes = sizeof(float) * (size_t)S * (size_t)H * (size_t)(P * N);
+    if (fused) pl.chunk_state_bytes = sizeof(__nv_bfloat16) * kh * (size_t)(P * Nk);
+    const size_t st_bytes = sizeof(float) * (size_t)S * (size_t)H * (size_t)(P * Nk);
     const ssd_tensor *sts[4] = {&a->initial_states, bwd ? nullptr : &a->final_states,
                                 b != nullptr ? &b->dfinal_states : nullptr, b != nullptr ? &b->dinitial_states : nullptr};
     for (int i = 0; i < 4; ++i)
-        if (sts[i] != nullptr && sts[i]->ptr != nullptr && sts[i]->dtype == SSD_BF16) {
+        if (sts[i] != nullptr && sts[i]->ptr != nullptr && (sts[i]->dtype == SSD_BF16 || Nk != N)) {
             pl.st_bf16[i] = true;
             pl.off_st32[i] = lay.take(st_bytes);
         }
@@ -501,7 +506,14 @@ static ssd_tensor state32(const Plan &pl, int i, const ssd_tensor &t, void *ws) 
     }
     return r;
 }
-static int64_t state_elems(const Plan &pl) { return (int64_t)pl.sh.S * pl.sh.H * pl.sh.P * pl.sh.N; }
+static int64_t state_rows(const Plan &pl) { return (int64_t)pl.sh.S * pl.sh.H * pl.sh.P; }
+// caller's state tensor -> the kernels' fp32 rows of sh.N, and back
+static cudaError_t state_in(const Plan &pl, const ssd_tensor &user, void *f32, cudaStream_t st) {
+    return launch_states_cvt(user.ptr, user.dtype == SSD_BF16, pl.sh.Nio, f32, false, pl.sh.N, state_rows(pl), st);
+}
+static cudaError_t state_out(const Plan &pl, const void *f32, const ssd_tensor &user, cudaStream_t st) {
+    return launch_states_cvt(f32, false, pl.sh.N, user.ptr, user.dtype == SSD_BF16, pl.sh.Nio, state_rows(pl), st);
+}
 
 static ssd_status fwd_impl(const Plan &pl, const ssd_fwd_args *a, void *ws, cudaStream_t st) {
     const Shape &sh = pl.sh;
@@ -702,10 +714,9 @@ ssd_status ssd_fwd(const ssd_problem *prob, const ssd_fwd_args *a, void *ws, siz
     ssd_fwd_args a32 = *a;
     a32.initial_states = state32(pl, 0, a->initial_states, ws);
     a32.final_states = state32(pl, 1, a->final_states, ws);
-    const int64_t n = state_elems(pl);
-    if (pl.st_bf16[0]) SSD_CUDA(launch_states_cvt(a->initial_states.ptr, a32.initial_states.ptr, n, true, st));
+    if (pl.st_bf16[0]) SSD_CUDA(state_in(pl, a->initial_states, a32.initial_states.ptr, st));
     SSD_TRY(fwd_impl(pl, &a32, ws, st));
-    if (pl.st_bf16[1]) SSD_CUDA(launch_states_cvt(a32.final_states.ptr, a->final_states.ptr, n, false, st));
+    if (pl.st_bf16[1]) SSD_CUDA(state_out(pl, a32.final_states.ptr, a->final_states, st));
     return SSD_OK;
 }
 
@@ -719,11 +730,10 @@ ssd_status ssd_bwd(const ssd_problem *prob, const ssd_bwd_args *b, void *ws, siz
     b32.fwd.initial_states = state32(pl, 0, b->fwd.initial_states, ws);
     b32.dfinal_states = state32(pl, 2, b->dfinal_states, ws);
     b32.dinitial_states = state32(pl, 3, b->dinitial_states, ws);
-    const int64_t n = state_elems(pl);
-    if (pl.st_bf16[0]) SSD_CUDA(launch_states_cvt(b->fwd.initial_states.ptr, b32.fwd.initial_states.ptr, n, true, st));
-    if (pl.st_bf16[2]) SSD_CUDA(launch_states_cvt(b->dfinal_states.ptr, b32.dfinal_states.ptr, n, true, st));
+    if (pl.st_bf16[0]) SSD_CUDA(state_in(pl, b->fwd.initial_states, b32.fwd.initial_states.ptr, st));
+    if (pl.st_bf16[2]) SSD_CUDA(state_in(pl, b->dfinal_states, b32.dfinal_states.ptr, st));
     SSD_TRY(bwd_impl(pl, &b32, ws, st));
-    if (pl.st_bf16[3]) SSD_CUDA(launch_states_cvt(b32.dinitial_states.ptr, b->dinitial_states.ptr, n, false, st));
+    if (pl.st_bf16[3]) SSD_CUDA(state_out(pl, b32.dinitial_states.ptr, b->dinitial_states, st));
     return SSD_OK;
 }
 

@@ -912,7 +912,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
     {
         auto store_bf16 = [&](int which, const float *v) {
-            if (!live) return;
+            if (!live || 64 * hf >= p.sh.Nio) return;   // columns the caller's dB/dC hold
             __nv_bfloat16 *dst = (which == 0 ? p.dB : p.dC) + (int64_t)ci.b * (which == 0 ? p.sdBb : p.sdCb) +
                                  tok * (which == 0 ? p.sdBl : p.sdCl) + (int64_t)g * (which == 0 ? p.sdBg : p.sdCg) +
                                  64 * hf;
@@ -1000,7 +1000,7 @@ k_bwd_finish(const BwdParams p, int tail_blocks) {
     if (p.hdr[HDR_STATUS] != 0 || k >= p.hdr[HDR_NCHUNKS]) return;
     const ChunkInfo ci = p.chunks[k];
     const int l = l0 + (threadIdx.x >> 4), n0 = (threadIdx.x & 15) * 8;
-    if (l < ci.lo || l >= ci.len) return;
+    if (l < ci.lo || l >= ci.len || n0 >= p.sh.Nio) return;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < p.nsub_tail; ++j) {
         const float4 *src = reinterpret_cast<const float4 *>(
@@ -1074,7 +1074,7 @@ static BwdParams make_params(const Shape &sh, const int32_t *hdr, const ChunkInf
 cudaError_t launch_bwd_dstates_tc(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, const BwdTcArgs &a,
                                   cudaStream_t st) {
     CUtensorMap mc, mdy, mz;
-    if (!map4(&mc, a.Cp, NT, sh.G, sh.L, sh.B, a.sc[2], a.sc[1], a.sc[0], QT)) return cudaErrorInvalidValue;
+    if (!map4(&mc, a.Cp, sh.Nio, sh.G, sh.L, sh.B, a.sc[2], a.sc[1], a.sc[0], QT)) return cudaErrorInvalidValue;
     if (!map4(&mdy, a.dy, PT, sh.H, sh.L, sh.B, a.sdy[2], a.sdy[1], a.sdy[0], QT)) return cudaErrorInvalidValue;
     if (a.z != nullptr) {
         if (!map4(&mz, a.z, PT, sh.H, sh.L, sh.B, a.sz[2], a.sz[1], a.sz[0], QT)) return cudaErrorInvalidValue;
@@ -1099,8 +1099,8 @@ cudaError_t launch_bwd_chunk_tc(const Shape &sh, const int32_t *hdr, const Chunk
     } else {
         mz = mdy;   // not read
     }
-    if (!map4(&mb, a.Bp, NT, sh.G, sh.L, sh.B, a.sb[2], a.sb[1], a.sb[0], QT)) return cudaErrorInvalidValue;
-    if (!map4(&mc, a.Cp, NT, sh.G, sh.L, sh.B, a.sc[2], a.sc[1], a.sc[0], QT)) return cudaErrorInvalidValue;
+    if (!map4(&mb, a.Bp, sh.Nio, sh.G, sh.L, sh.B, a.sb[2], a.sb[1], a.sb[0], QT)) return cudaErrorInvalidValue;
+    if (!map4(&mc, a.Cp, sh.Nio, sh.G, sh.L, sh.B, a.sc[2], a.sc[1], a.sc[0], QT)) return cudaErrorInvalidValue;
     BwdParams p = make_params(sh, hdr, chunks, a);
     static int attr_done[64] = {0};
     cudaError_t e = ensure_smem_attr(k_bwd_chunk_tc, (int)BWD_SMEM, attr_done);

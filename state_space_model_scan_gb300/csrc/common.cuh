@@ -58,6 +58,8 @@ struct UnitInfo {
 // Shape of one call, as the kernels see it.
 struct Shape {
     int B, L, H, P, G, N, S;
+    int Nio;          // dstate of the caller's B, C, dB, dC (the tensor-core path computes N = 128
+                      // and reads a dstate-64 problem as its zero-extended half: TMA fills past Nio)
     int Q;            // internal chunk length
     int hpg;          // H / G
     int kmax;         // capacity of the chunk list

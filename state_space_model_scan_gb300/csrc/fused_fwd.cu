@@ -799,13 +799,13 @@ cudaError_t launch_fused_fwd(const Shape &sh, int32_t *hdr, const UnitInfo *unit
     } else {
         mz = mx;
     }
-    if (!make_map(&mb, Bp, NT, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
+    if (!make_map(&mb, Bp, sh.Nio, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
     if (y != nullptr) {
         if (!make_map(&my, y, PT, sh.H, sh.L, sh.B, sy[2], sy[1], sy[0])) return cudaErrorInvalidValue;
     } else {
         my = mx;   // not written (states-only mode)
     }
-    if (!make_map(&mc, Cp, NT, sh.G, sh.L, sh.B, sc[2], sc[1], sc[0])) return cudaErrorInvalidValue;
+    if (!make_map(&mc, Cp, sh.Nio, sh.G, sh.L, sh.B, sc[2], sc[1], sc[0])) return cudaErrorInvalidValue;
     FusedParams fp;
     fp.sh = sh; fp.hdr = hdr; fp.units = units; fp.dt_raw = dt_raw; fp.sdb = sdb; fp.sdl = sdl;
     fp.A = A; fp.D = D; fp.bias = bias;

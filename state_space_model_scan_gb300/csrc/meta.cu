@@ -388,23 +388,34 @@ cudaError_t launch_empty_seq_final(int S, int H, int PN, const SeqInfo *seqs, co
     return cudaGetLastError();
 }
 
-// State tensors stored in bf16 at the boundary: widened to fp32 before the scan reads them,
-// and the fp32 results rounded (nearest even) into the caller's bf16 tensor afterwards.
-__global__ void k_states_to_f32(const __nv_bfloat16 *src, float *dst, int64_t n) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        dst[i] = __bfloat162float(src[i]);
+// State tensors at the boundary whose storage differs from the kernels' fp32 [.., N] rows: bf16
+// storage, and/or dstate 64 on the tensor-core path (rows of 128, the upper half zero).  Copies
+// rows of `src_n` columns into rows of `dst_n` columns (zero-filled past src_n), widening bf16
+// or rounding to it (nearest even).
+template <typename S, typename D>
+__global__ void k_states_cvt(const S *src, int src_n, D *dst, int dst_n, int64_t rows) {
+    const int64_t n = rows * dst_n;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / dst_n;
+        const int c = (int)(i - r * dst_n);
+        const float v = c < src_n ? (float)src[r * src_n + c] : 0.f;
+        dst[i] = (D)v;
+    }
 }
-__global__ void k_states_to_bf16(const float *src, __nv_bfloat16 *dst, int64_t n) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        dst[i] = __float2bfloat16_rn(src[i]);
-}
-cudaError_t launch_states_cvt(const void *src, void *dst, int64_t n, bool to_f32, cudaStream_t st) {
-    if (n <= 0) return cudaSuccess;
-    const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
-    if (to_f32)
-        k_states_to_f32<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(src), static_cast<float *>(dst), n);
+cudaError_t launch_states_cvt(const void *src, bool src_bf16, int src_n, void *dst, bool dst_bf16, int dst_n,
+                              int64_t rows, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    const int blocks = (int)std::min<int64_t>((rows * dst_n + 255) / 256, 4096);
+    using bf = __nv_bfloat16;
+    if (src_bf16)   // widen into the fp32 copy
+        k_states_cvt<bf, float><<<blocks, 256, 0, st>>>(static_cast<const bf *>(src), src_n, static_cast<float *>(dst),
+                                                         dst_n, rows);
+    else if (dst_bf16)
+        k_states_cvt<float, bf><<<blocks, 256, 0, st>>>(static_cast<const float *>(src), src_n, static_cast<bf *>(dst),
+                                                         dst_n, rows);
     else
-        k_states_to_bf16<<<blocks, 256, 0, st>>>(static_cast<const float *>(src), static_cast<__nv_bfloat16 *>(dst), n);
+        k_states_cvt<float, float><<<blocks, 256, 0, st>>>(static_cast<const float *>(src), src_n,
+                                                            static_cast<float *>(dst), dst_n, rows);
     return cudaGetLastError();
 }
 

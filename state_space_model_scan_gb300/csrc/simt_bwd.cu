@@ -323,10 +323,10 @@ __global__ void k_reduce_group(Shape sh, const int32_t *__restrict__ hdr, const 
     const ChunkInfo ci = chunks[k];
     const float *src = which == 0 ? srcB : srcC;
     const MView3 dst = which == 0 ? dstB : dstC;
-    const int N = sh.N;
+    const int N = sh.N, No = sh.Nio;   // share row stride; columns the caller's tensors hold
     const int rows = min(16, ci.len - l0);
-    for (int i = threadIdx.x; i < rows * N; i += blockDim.x) {
-        const int l = l0 + i / N, n = i % N;
+    for (int i = threadIdx.x; i < rows * No; i += blockDim.x) {
+        const int l = l0 + i / No, n = i % No;
         if (l < ci.lo) continue;   // rows of another sequence sharing the chunk
         float a = 0.f;
         const float *s = src + (((int64_t)k * sh.H + (int64_t)g * sh.hpg) * sh.Q + l) * N + n;

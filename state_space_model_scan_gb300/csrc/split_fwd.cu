@@ -705,7 +705,7 @@ cudaError_t launch_split_states(const Shape &sh, int32_t *hdr, const ChunkInfo *
                                 cudaStream_t st) {
     CUtensorMap mx, mb;
     if (!map_s(&mx, x, PT, sh.H, sh.L, sh.B, sx[2], sx[1], sx[0])) return cudaErrorInvalidValue;
-    if (!map_s(&mb, Bp, NT, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
+    if (!map_s(&mb, Bp, sh.Nio, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
     SplitParams p{};
     p.sh = sh; p.hdr = hdr; p.chunks = chunks; p.seqs = seqs;
     p.hs = split_heads_per_item(sh.hpg);
@@ -736,8 +736,8 @@ cudaError_t launch_split_out(const Shape &sh, int32_t *hdr, const ChunkInfo *chu
                              __nv_bfloat16 *states, int sms, cudaStream_t st) {
     CUtensorMap mx, mb, mc, mz, my;
     if (!map_s(&mx, x, PT, sh.H, sh.L, sh.B, sx[2], sx[1], sx[0])) return cudaErrorInvalidValue;
-    if (!map_s(&mb, Bp, NT, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
-    if (!map_s(&mc, Cp, NT, sh.G, sh.L, sh.B, sc[2], sc[1], sc[0])) return cudaErrorInvalidValue;
+    if (!map_s(&mb, Bp, sh.Nio, sh.G, sh.L, sh.B, sb[2], sb[1], sb[0])) return cudaErrorInvalidValue;
+    if (!map_s(&mc, Cp, sh.Nio, sh.G, sh.L, sh.B, sc[2], sc[1], sc[0])) return cudaErrorInvalidValue;
     if (!map_s(&my, y, PT, sh.H, sh.L, sh.B, sy[2], sy[1], sy[0])) return cudaErrorInvalidValue;
     if (z != nullptr) {
         if (!map_s(&mz, z, PT, sh.H, sh.L, sh.B, sz[2], sz[1], sz[0])) return cudaErrorInvalidValue;
