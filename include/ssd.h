@@ -90,12 +90,12 @@ typedef enum {
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
 /* Which forward/backward pipeline to run.  AUTO takes the tensor-core path (its single-pass
- * forward) when
- * chunk_size == 128 and the inputs are bf16 with headdim == 64, dstate == 128 (the
- * compiled tile set; tensors that break its 16-byte rule then return
- * SSD_ERR_MISALIGNED), and the SIMT path when chunk_size == 64 (f32 inputs always
- * take SIMT: fp32 inputs are computed in fp32 FMA, never in tf32); any other
- * combination returns SSD_ERR_UNSUPPORTED. */
+ * forward) when chunk_size == 128 and the inputs are bf16 with headdim == 64 and dstate 128
+ * or 64 (the compiled tile set is dstate 128; dstate 64 runs as its zero-extended half, the
+ * cuDNN frontend Mamba-2 engine's headdim = dstate = 64 shape; tensors that break the
+ * 16-byte rule then return SSD_ERR_MISALIGNED), and the SIMT path when chunk_size == 64
+ * (f32 inputs always take SIMT: fp32 inputs are computed in fp32 FMA, never in tf32); any
+ * other combination returns SSD_ERR_UNSUPPORTED. */
 typedef enum {
     SSD_ALGO_AUTO = 0,
     SSD_ALGO_STAGED = 1,   /* SIMT, one kernel per step: cumsum, chunk_state, state_passing, chunk_scan */

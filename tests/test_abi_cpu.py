@@ -127,6 +127,10 @@ def test_validation_codes(lib, mutate, code):
     (64, 128, True, 128, "staged", True, 2, None),
     (64, 128, True, 128, "auto", False, 3, None),   # tensor-core chunk length, strides break the TMA rule
     (64, 128, False, 128, "auto", True, 2, None),   # fp32 inputs run SIMT only
+    (64, 64, True, 128, "auto", True, 0, 128),      # dstate 64: the tensor-core tiles' zero-extended half
+    (64, 64, True, 128, "split", True, 0, 128),
+    (64, 32, True, 128, "auto", True, 2, None),     # other dstates: SIMT only (64-token chunks)
+    (64, 32, True, 64, "auto", True, 0, 64),
 ])
 def test_chunk_size_is_honoured(lib, P, N, bf16, Q, algo, aligned, code, qi):
     """Each chunk_size outcome: the path that computes exactly that chunk length, or
