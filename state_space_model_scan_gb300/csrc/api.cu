@@ -27,6 +27,9 @@ cudaError_t launch_chunk_state(const Shape &sh, const int32_t *hdr, const ChunkI
 cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqInfo *seqs, const float *lamw,
                                  int lam_stride, float *states, const float *init, float *final_, int reverse,
                                  cudaStream_t st);
+cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqInfo *seqs, const float *lamw,
+                                 int lam_stride, __nv_bfloat16 *states, const float *init, float *final_, int reverse,
+                                 cudaStream_t st);
 template <typename T>
 cudaError_t launch_chunk_scan(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 x, View3 Bm,
                               View3 Cm, View3 z, const float *D, const float *dtw, const float *csw,
@@ -361,7 +364,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
             const size_t ksub = pl.hs < sh.hpg ? (size_t)kmax * (size_t)(H / pl.hs) : 0;
             if (a->chunk_states == nullptr)   // carried states, bf16, unless the forward kept them
                 pl.off_states = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * Nk));
-            pl.off_dstates = lay.take(sizeof(float) * kh * (size_t)(P * Nk));
+            pl.off_dstates = lay.take(sizeof(__nv_bfloat16) * kh * (size_t)(P * Nk));   // dS, bf16
             pl.off_cs = lay.take(sizeof(float) * kh);                                // chunk total log-decay
             pl.off_dBh = lay.take(sizeof(float) * ksub * Q * (size_t)Nk);
             pl.off_dCh = lay.take(sizeof(float) * ksub * Q * (size_t)Nk);
@@ -612,7 +615,8 @@ static ssd_status bwd_impl(const Plan &pl, const ssd_bwd_args *b, void *ws, cuda
         uint32_t *flags = split ? nullptr : at<uint32_t>(ws, pl.off_flags);
         const bool kept = a->chunk_states != nullptr;   // the forward's chunk states, else recomputed
         __nv_bfloat16 *states = kept ? static_cast<__nv_bfloat16 *>(a->chunk_states) : at<__nv_bfloat16>(ws, pl.off_states);
-        float *dS = at<float>(ws, pl.off_dstates), *clam = at<float>(ws, pl.off_cs);
+        __nv_bfloat16 *dS = at<__nv_bfloat16>(ws, pl.off_dstates);
+        float *clam = at<float>(ws, pl.off_cs);
         float *dBh = at<float>(ws, pl.off_dBh), *dCh = at<float>(ws, pl.off_dCh), *part = at<float>(ws, pl.off_part);
         const int64_t n_zero = (int64_t)sh.umax * sh.H;   // the unit flags
         SSD_CUDA(launch_build_meta(a->cu_seqlens, sh.B, sh.L, sh.S, sh.Q, sh.R, sh.useg_num, sh.useg_den,

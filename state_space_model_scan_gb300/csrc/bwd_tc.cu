@@ -55,9 +55,9 @@ struct BwdParams {
     int64_t sdxb, sdxl, sdxh, sdzb, sdzl, sdzh;
     float *ddt;
     int64_t sddb, sddl;
-    const float *dS;         // [chunk][H][P][N] fp32: gradient of the state leaving the chunk
+    const __nv_bfloat16 *dS; // [chunk][H][P][N] bf16: gradient of the state leaving the chunk
     const __nv_bfloat16 *states;   // 16 KB tile per (chunk, head): row n = S_in[0..63][n], 128-byte swizzle
-    float *dS_loc;           // [chunk][H][P][N] fp32 (dstates kernel output)
+    __nv_bfloat16 *dS_loc;   // [chunk][H][P][N] bf16 (dstates kernel output)
     float *chunk_lam;        // [chunk][H] total log-decay of the chunk (dstates kernel output)
     float *dBh, *dCh;        // [chunk][H/hs][Q][N] fp32 shares of head subsets (when hs < H/G)
     float *partials;         // [chunk][H][4]: dA, dD, ddt_bias shares
@@ -297,9 +297,9 @@ k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             float v[32];
             tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + 32 * hf, v);
             tmem_wait_ld();
-            float *dst = p.dS_loc + ((int64_t)k * p.sh.H + h) * (PT * NT) + (int64_t)(32 * hf) * NT + row;
+            __nv_bfloat16 *dst = p.dS_loc + ((int64_t)k * p.sh.H + h) * (PT * NT) + (int64_t)(32 * hf) * NT + row;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = v[i];
+            for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(v[i]);
         }
         tc_fence_before();
         __syncthreads();
@@ -323,8 +323,8 @@ constexpr uint32_t O_SI = O_C + BC_BYTES;          // S_in   [n][p]   16 KB (bul
 constexpr uint32_t O_DY = O_SI + S_BYTES;          // dyp, then e o dyp [l][p] 16 KB
 constexpr uint32_t O_M = O_DY + X_BYTES;           // M      [l][s]   32 KB
 constexpr uint32_t O_E = O_M + BC_BYTES;           // E'     [l][s]   32 KB; before: dy, z of the head (TMA)
-constexpr uint32_t O_WX = O_E + BC_BYTES;          // w o x  [s][p]   16 KB } before: dS of the head,
-constexpr uint32_t O_SD = O_WX + X_BYTES;          // dS     [p][n]   16 KB }   fp32 [p][n] (bulk copy)
+constexpr uint32_t O_WX = O_E + BC_BYTES;          // w o x  [s][p]   16 KB; before: dS of the head, bf16 [p][n] (bulk copy)
+constexpr uint32_t O_SD = O_WX + X_BYTES;          // dS     [p][n]   16 KB (swizzled MMA tile)
 constexpr uint32_t O_MISC = O_SD + S_BYTES;
 // misc floats
 constexpr int F_ROWT1 = 0, F_ROWXU = 256, F_ROWT2 = 512, F_ROWD = 768, F_COLP = 1024, F_RED = 1536,
@@ -437,13 +437,12 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         tma_load_4d(sm + O_X, &tmX, &bar[1], 0, h, w.ci.t0, w.ci.b);
         bulk_load(sm + O_SI, p.states + (int64_t)slab * (PT * NT), S_BYTES, &bar[1]);
     };
-    auto stage_head = [&](const Item &w, int h) {   // one thread: dy, z and fp32 dS
-        const float *src = p.dS + ((int64_t)w.k * H + h) * (PT * NT);
-        mbar_expect_tx(&bar[3], X_BYTES * (has_z ? 2u : 1u) + 2u * S_BYTES);   // dS fp32 = 2 x S_BYTES
+    auto stage_head = [&](const Item &w, int h) {   // one thread: dy, z and bf16 dS
+        const __nv_bfloat16 *src = p.dS + ((int64_t)w.k * H + h) * (PT * NT);
+        mbar_expect_tx(&bar[3], X_BYTES * (has_z ? 2u : 1u) + S_BYTES);
         tma_load_4d(sm + O_E, &tmDY, &bar[3], 0, h, w.ci.t0, w.ci.b);
         if (has_z) tma_load_4d(sm + O_E + X_BYTES, &tmZ, &bar[3], 0, h, w.ci.t0, w.ci.b);
         bulk_load(sm + O_WX, src, S_BYTES, &bar[3]);
-        bulk_load(sm + O_WX + S_BYTES, src + PT * NT / 2, S_BYTES, &bar[3]);
     };
     auto issue_first = [&](const Item &w) {   // B/C and the first head's inputs (one thread issues)
         if (tid == 0) {
@@ -602,16 +601,20 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             const float wl = wst[row];
 #pragma unroll
             for (int i = 0; i < 32; ++i) xv[i] *= wl;
-            // dS (fp32 [p][n], staged over the w o x and dS tiles): T3 partial and a bf16 copy.
+            // dS (bf16 [p][n], staged in the w o x tile): T3 partial and the swizzled MMA copy.
             // Thread: 4 runs of 8 consecutive n (run c = tid + 256 j: p = c / 16, n0 = 8 (c % 16)).
             float dsv[4][8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int c = tid + 256 * j, pp = c >> 4, nc = c & 15;
-                const float4 *s4 = reinterpret_cast<const float4 *>(sm + O_WX) + pp * (NT / 4) + nc * 2;
-                const float4 a = s4[0], b = s4[1];
-                dsv[j][0] = a.x; dsv[j][1] = a.y; dsv[j][2] = a.z; dsv[j][3] = a.w;
-                dsv[j][4] = b.x; dsv[j][5] = b.y; dsv[j][6] = b.z; dsv[j][7] = b.w;
+                const uint4 raw = *reinterpret_cast<const uint4 *>(sm + O_WX + (pp * NT + 8 * nc) * 2);
+                const __nv_bfloat162 *e2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(e2[i]);
+                    dsv[j][2 * i] = f.x;
+                    dsv[j][2 * i + 1] = f.y;
+                }
             }
             // <S_in, dS> partial: thread takes 8 consecutive p at one n (run r = tid + 256 j:
             // n = r % 128, p = 8 (r / 128) ..), one 16-byte piece of the S_in tile's row n
@@ -620,12 +623,12 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 const int r = tid + 256 * j, n = r & 127, q = r >> 7;
                 const uint4 si = *reinterpret_cast<const uint4 *>(sm + O_SI + n * 128 + ((q ^ (n & 7)) << 4));
                 const __nv_bfloat162 *e2 = reinterpret_cast<const __nv_bfloat162 *>(&si);
-                const float *dsn = reinterpret_cast<const float *>(sm + O_WX) + 8 * q * NT + n;
+                const __nv_bfloat16 *dsn = reinterpret_cast<const __nv_bfloat16 *>(sm + O_WX) + 8 * q * NT + n;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 sv = __bfloat1622float2(e2[i]);
-                    t3p = fmaf(sv.x, dsn[(2 * i) * NT], t3p);
-                    t3p = fmaf(sv.y, dsn[(2 * i + 1) * NT], t3p);
+                    t3p = fmaf(sv.x, __bfloat162float(dsn[(2 * i) * NT]), t3p);
+                    t3p = fmaf(sv.y, __bfloat162float(dsn[(2 * i + 1) * NT]), t3p);
                 }
             }
             __syncthreads();   // the staged dS is read: its space becomes the w o x and dS tiles

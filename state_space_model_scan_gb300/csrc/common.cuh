@@ -82,7 +82,9 @@ struct BwdTcArgs {
     float *ddt;
     int64_t sddb, sddl;
     const __nv_bfloat16 *states;   // carried state entering each chunk: 16 KB swizzled tile per (chunk, head)
-    float *dS, *chunk_lam, *dBh, *dCh, *partials;
+    __nv_bfloat16 *dS;    // [chunk][H][P][N] bf16: local dS from the dstates kernel, then (in place) the
+                          // gradient of the state leaving every chunk (carried in fp32 by the reverse scan)
+    float *chunk_lam, *dBh, *dCh, *partials;
     int hs;                         // heads per CTA of the gradient kernel (divides H/G)
     int hs_ds;                      // heads per CTA of the dstates kernel (divides H/G)
     // gradient kernel work items: pairs (chunk, group) below k_pairs in H/G/hs subsets of hs

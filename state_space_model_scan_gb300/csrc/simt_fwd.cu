@@ -115,10 +115,28 @@ k_chunk_state(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__rest
 // visited last to first: that is the backward recursion dS_out[c] = exp(cs_{c+1}[Q-1])
 // dS_out[c+1] + dS_loc[c+1] (same affine form, the chunk's own decay), with `init` =
 // dfinal and `final_` = dinit (caller tensors: read and written per element, since
-// their 16-byte alignment is not guaranteed).  P*N is a multiple of 256.
+// their 16-byte alignment is not guaranteed).  P*N is a multiple of 256.  The chunk tiles are
+// fp32, or bf16 (the tensor-core backward's dS: stored rounded, carried in fp32).
+__device__ __forceinline__ float4 ld_st4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld_st4(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st_st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void st_st4(__nv_bfloat16 *p, float4 v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&a);
+    u.y = *reinterpret_cast<const uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+template <typename T>
 __global__ void __launch_bounds__(256)
 k_state_passing(Shape sh, const int32_t *__restrict__ hdr, const SeqInfo *__restrict__ seqs,
-                const float *__restrict__ lamw, int lam_stride, float *__restrict__ states,
+                const float *__restrict__ lamw, int lam_stride, T *__restrict__ states,
                 const float *__restrict__ init, float *__restrict__ final_, int reverse) {
     constexpr int CB = 8;   // chunks per batch
     if (hdr[HDR_STATUS] != 0) return;
@@ -133,18 +151,18 @@ k_state_passing(Shape sh, const int32_t *__restrict__ hdr, const SeqInfo *__rest
     float4 carry = make_float4(0.f, 0.f, 0.f, 0.f);
     if (init != nullptr && act) carry = make_float4(init[sbase + e], init[sbase + e + 1], init[sbase + e + 2], init[sbase + e + 3]);
     auto chunk_of = [&](int pos) { return reverse ? si.chunk0 + nch - 1 - pos : si.chunk0 + pos; };
-    auto slot = [&](int pos) { return reinterpret_cast<float4 *>(states + ((int64_t)chunk_of(pos) * sh.H + h) * PN + e); };
+    auto slot = [&](int pos) { return states + ((int64_t)chunk_of(pos) * sh.H + h) * PN + e; };
     for (int c0 = 0; c0 < nch; c0 += CB) {
         const int nc = min(CB, nch - c0);
         const float mydec = lane < nc ? expf(lamw[((int64_t)chunk_of(c0 + lane) * sh.H + h) * lam_stride]) : 0.f;
         float4 v[CB];
 #pragma unroll
-        for (int j = 0; j < CB; ++j) v[j] = (act && j < nc) ? *slot(c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < CB; ++j) v[j] = (act && j < nc) ? ld_st4(slot(c0 + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < CB; ++j) {
             const float d = __shfl_sync(0xffffffffu, mydec, j);
             if (j < nc) {
-                if (act) *slot(c0 + j) = carry;   // carry entering the chunk
+                if (act) st_st4(slot(c0 + j), carry);   // carry entering the chunk
                 carry.x = fmaf(d, carry.x, v[j].x);
                 carry.y = fmaf(d, carry.y, v[j].y);
                 carry.z = fmaf(d, carry.z, v[j].z);
@@ -276,8 +294,18 @@ cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqI
     const int PN = sh.P * sh.N;
     if (sh.S * sh.H == 0) return cudaSuccess;
     if (PN % 256 != 0) return cudaErrorInvalidValue;   // float4 per thread, whole warps
-    k_state_passing<<<dim3(sh.S * sh.H, (PN + 1023) / 1024), 256, 0, st>>>(sh, hdr, seqs, lamw, lam_stride, states,
-                                                                           init, final_, reverse);
+    k_state_passing<float><<<dim3(sh.S * sh.H, (PN + 1023) / 1024), 256, 0, st>>>(sh, hdr, seqs, lamw, lam_stride,
+                                                                                  states, init, final_, reverse);
+    return cudaGetLastError();
+}
+cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqInfo *seqs, const float *lamw,
+                                 int lam_stride, __nv_bfloat16 *states, const float *init, float *final_, int reverse,
+                                 cudaStream_t st) {
+    const int PN = sh.P * sh.N;
+    if (sh.S * sh.H == 0) return cudaSuccess;
+    if (PN % 256 != 0) return cudaErrorInvalidValue;
+    k_state_passing<__nv_bfloat16><<<dim3(sh.S * sh.H, (PN + 1023) / 1024), 256, 0, st>>>(
+        sh, hdr, seqs, lamw, lam_stride, states, init, final_, reverse);
     return cudaGetLastError();
 }
 
