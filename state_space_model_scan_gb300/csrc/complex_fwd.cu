@@ -46,9 +46,10 @@ constexpr uint32_t ATOM = 8192;
 constexpr uint32_t OFF_P0 = 0, OFF_P1 = SLOT, OFF_P2 = 2 * SLOT, OFF_P3 = 3 * SLOT, OFF_P4 = 4 * SLOT;
 constexpr uint32_t OFF_S0 = 5 * SLOT;                      // carried state, conjugated
 constexpr uint32_t OFF_MISC = 6 * SLOT;
-constexpr uint32_t MISC_CS = 0, MISC_E = 512, MISC_W = 1024, MISC_ROT = 1536, MISC_BAR = 2048, MISC_TMEM = 2112,
-                   MISC_ABORT = 2116;
-constexpr uint32_t CX_SMEM = OFF_MISC + 2560 + 1024;       // + alignment slack
+// per-chunk tables, two sets (chunk c uses set c & 1; the next chunk's is built meanwhile)
+constexpr uint32_t MISC_CS = 0, MISC_E = 1024, MISC_W = 2048, MISC_ROT = 3072, MISC_BAR = 4096, MISC_TMEM = 4160,
+                   MISC_ABORT = 4164;
+constexpr uint32_t CX_SMEM = OFF_MISC + 4608 + 1024;       // + alignment slack
 constexpr uint32_t TX_BYTES = 3 * SLOT;                    // C, B and X tiles of one chunk
 
 // TMEM columns: four accumulators of 128 columns (real part block, imaginary part block).
@@ -117,10 +118,10 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
     uint8_t *P0 = sm + OFF_P0, *P1 = sm + OFF_P1, *P2 = sm + OFF_P2, *P3 = sm + OFF_P3, *P4 = sm + OFF_P4;
     uint8_t *S0 = sm + OFF_S0;
-    float2 *cs = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_CS);
-    float2 *ecs = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_E);
-    float2 *wv = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_W);
-    float2 *rot = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_ROT);   // exp(i Im cs_l)
+    float2 *cs_t = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_CS);    // [2][CQ] in-chunk cumsum
+    float2 *ecs_t = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_E);    // [2][CQ] exp(cs_l)
+    float2 *wv_t = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_W);     // [2][CQ] exp(cs_63 - cs_l)
+    float2 *rot_t = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_ROT);  // [2][CQ] exp(i Im cs_l)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_MISC + MISC_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC + MISC_TMEM);
     volatile int *abort_ = reinterpret_cast<volatile int *>(sm + OFF_MISC + MISC_ABORT);
@@ -182,7 +183,9 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         load_cb(0);
         in_pending = true;
     }
-    // warp 0 reads dt one chunk ahead (the load's latency hides behind a whole chunk)
+    // Warp 1 builds the per-chunk tables (one lane: two positions), the next chunk's while
+    // thread 0 issues and waits for the current chunk's second MMA batch; it reads dt one
+    // chunk ahead of that.
     float dtn[2] = {0.f, 0.f};
     auto fetch_dt = [&](int c) {
 #pragma unroll
@@ -191,40 +194,48 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             dtn[j] = t < p.T ? p.dt[(b * p.T + t) * p.H + h] : 0.f;
         }
     };
-    if (warp == 0 && nc > 0) fetch_dt(0);
+    auto build_tables = [&](int c) {   // warp 1; dtn holds chunk c's dt
+        const int set = c & 1;
+        const int64_t t0 = (int64_t)c * CQ;
+        float2 a2[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float sp = (t0 + 2 * lane + j < p.T) ? softplus_f(dtn[j]) : 0.f;
+            a2[j] = make_float2(sp * Ah.x, sp * Ah.y);
+        }
+        if (c + 1 < nc) fetch_dt(c + 1);
+        float2 s = make_float2(a2[0].x + a2[1].x, a2[0].y + a2[1].y);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float ux = __shfl_up_sync(0xffffffffu, s.x, o), uy = __shfl_up_sync(0xffffffffu, s.y, o);
+            if (lane >= o) { s.x += ux; s.y += uy; }
+        }
+        float2 ex = make_float2(__shfl_up_sync(0xffffffffu, s.x, 1), __shfl_up_sync(0xffffffffu, s.y, 1));
+        if (lane == 0) ex = make_float2(0.f, 0.f);
+        const float2 last = make_float2(__shfl_sync(0xffffffffu, s.x, 31), __shfl_sync(0xffffffffu, s.y, 31));
+        const float2 cl[2] = {make_float2(ex.x + a2[0].x, ex.y + a2[0].y), s};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int l = 2 * lane + j;
+            cs_t[set * CQ + l] = cl[j];
+            ecs_t[set * CQ + l] = cexp(cl[j]);
+            wv_t[set * CQ + l] = cexp(make_float2(last.x - cl[j].x, last.y - cl[j].y));
+            float sn, cn;
+            sincosf(cl[j].y, &sn, &cn);
+            rot_t[set * CQ + l] = make_float2(cn, sn);
+        }
+    };
+    if (warp == 1 && nc > 0) {
+        fetch_dt(0);
+        build_tables(0);
+    }
+    __syncthreads();
 
     for (int c = 0; c < nc; ++c) {
         const uint32_t par = (uint32_t)(c & 1);
         const int64_t t0 = (int64_t)c * CQ;
-        // ---- in-chunk cumulative log-decay (warp 0: two positions per lane)
-        if (warp == 0) {
-            float2 a2[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float sp = (t0 + 2 * lane + j < p.T) ? softplus_f(dtn[j]) : 0.f;
-                a2[j] = make_float2(sp * Ah.x, sp * Ah.y);
-            }
-            if (c + 1 < nc) fetch_dt(c + 1);
-            float2 s = make_float2(a2[0].x + a2[1].x, a2[0].y + a2[1].y);
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float ux = __shfl_up_sync(0xffffffffu, s.x, o), uy = __shfl_up_sync(0xffffffffu, s.y, o);
-                if (lane >= o) { s.x += ux; s.y += uy; }
-            }
-            float2 ex = make_float2(__shfl_up_sync(0xffffffffu, s.x, 1), __shfl_up_sync(0xffffffffu, s.y, 1));
-            if (lane == 0) ex = make_float2(0.f, 0.f);
-            cs[2 * lane] = make_float2(ex.x + a2[0].x, ex.y + a2[0].y);
-            cs[2 * lane + 1] = s;
-        }
-        __syncthreads();
-        if (tid < CQ) {
-            const float2 cl = cs[tid], last = cs[CQ - 1];
-            ecs[tid] = cexp(cl);
-            wv[tid] = cexp(make_float2(last.x - cl.x, last.y - cl.y));
-            float sn, cn;
-            sincosf(cl.y, &sn, &cn);
-            rot[tid] = make_float2(cn, sn);
-        }
+        const float2 *cs = cs_t + (c & 1) * CQ, *ecs = ecs_t + (c & 1) * CQ;
+        const float2 *wv = wv_t + (c & 1) * CQ, *rot = rot_t + (c & 1) * CQ;
         // ---- chunk inputs
         if (tid == 0) {
             in_par = par;
@@ -350,6 +361,7 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                 if (c + 1 < nc) load_cb(c + 1);   // C and B slots are free again: overlaps the epilogue
             }
         }
+        if (warp == 1 && c + 1 < nc) build_tables(c + 1);   // while thread 0 waits for batch 2
         __syncthreads();
         tc_fence_after();
         if (*abort_) break;
