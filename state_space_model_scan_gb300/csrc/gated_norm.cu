@@ -49,6 +49,10 @@ __device__ __forceinline__ void store8(float *p, const float *v) {
     reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// logistic function with the fast exponential and divide (relative error ~1e-6, far inside the
+// fp32 tolerance; 1/inf = 0 gives the right limit for very negative arguments)
+__device__ __forceinline__ float sig(float v) { return __fdividef(1.f, 1.f + __expf(-v)); }
+
 struct NormArgs {
     int64_t rows, width, G;   // G = features per group
     int ng;                   // groups per row
@@ -82,7 +86,7 @@ k_norm_fwd(const NormArgs a) {
                 float zz[8];
                 load8(zr + 8 * j, zz);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sigmoid_f(zz[e]);
+                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig(zz[e]);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
@@ -99,7 +103,7 @@ k_norm_fwd(const NormArgs a) {
                 float zz[8];
                 load8(zr + 8 * j, zz);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sigmoid_f(zz[e]);
+                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig(zz[e]);
             }
             load8(wr + 8 * j, wv);
 #pragma unroll
@@ -136,7 +140,7 @@ k_norm_bwd(const NormArgs a) {
                 float zz[8];
                 load8(zr + 8 * j, zz);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sigmoid_f(zz[e]);
+                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig(zz[e]);
             }
             load8(dr + 8 * j, d);
             load8(wr + 8 * j, wv);
@@ -153,7 +157,7 @@ k_norm_bwd(const NormArgs a) {
                 load8(zr + 8 * j, z8);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    sg[e] = sigmoid_f(z8[e]);
+                    sg[e] = sig(z8[e]);
                     s[e] = z8[e] * sg[e];
                 }
             } else {
@@ -213,7 +217,7 @@ k_norm_fwd_reg(const NormArgs a) {
             if (lane + 32 * k < pieces) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    if (zr) v[k][e] *= zz[k][e] * sigmoid_f(zz[k][e]);
+                    if (zr) v[k][e] *= zz[k][e] * sig(zz[k][e]);
                     ss = fmaf(v[k][e], v[k][e], ss);
                 }
             }
@@ -275,7 +279,7 @@ k_norm_bwd_reg(const NormArgs a) {
             if (lane + 32 * k < pieces) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float sgate = zr ? z8[k][e] * sigmoid_f(z8[k][e]) : 1.f;
+                    const float sgate = zr ? z8[k][e] * sig(z8[k][e]) : 1.f;
                     dot = fmaf(d[k][e] * wv[k][e], y8[k][e] * sgate * rs, dot);
                 }
             }
@@ -290,7 +294,7 @@ k_norm_bwd_reg(const NormArgs a) {
                 float o1[8], o2[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float sg = zr ? sigmoid_f(z8[k][e]) : 0.f;
+                    const float sg = zr ? sig(z8[k][e]) : 0.f;
                     const float sgate = zr ? z8[k][e] * sg : 1.f;
                     const float vhat = y8[k][e] * sgate * rs;
                     const float dv = rs * (d[k][e] * wv[k][e] - vhat * dot);
