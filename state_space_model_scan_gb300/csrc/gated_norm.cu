@@ -324,11 +324,144 @@ k_norm_bwd_reg(const NormArgs a) {
     }
 }
 
+// Backward with the rows staged in shared memory: a block takes its row chunk of one group in
+// batches of NW rows (one per warp); y, z and dout of the next batch are copied in by cp.async
+// (double-buffered) while the current batch is computed, so the loads in flight do not depend
+// on how many warps the registers allow.  A lane keeps its slice of w and of the dw sums in
+// registers; the block's dw rows are summed in warp order at the end, as in the kernels above.
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+template <typename T, int PPL>
+__global__ void __launch_bounds__(NW * 32)
+k_norm_bwd_staged(const NormArgs a) {
+    extern __shared__ __align__(16) uint8_t nsm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = blockIdx.y;
+    const int G = (int)a.G, pieces = G / 8;
+    const int cpr = G * (int)sizeof(T) / 16;                  // 16-byte pieces per row
+    const int ntens = a.z ? 3 : 2;                            // y, dout, z
+    T *stage = reinterpret_cast<T *>(nsm);                    // [2][ntens][NW][G]
+    const int64_t r0 = (int64_t)blockIdx.x * a.rows_per_chunk, r1 = std::min(a.rows, r0 + a.rows_per_chunk);
+    const float *wr = a.w + (int64_t)g * G;
+    float wv[PPL][8], dw[PPL][8];
+#pragma unroll
+    for (int k = 0; k < PPL; ++k) {
+        const int j = lane + 32 * k;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { dw[k][e] = 0.f; wv[k][e] = 0.f; }
+        if (j < pieces) load8(wr + 8 * j, wv[k]);
+    }
+    auto tile = [&](int buf, int t, int rw) { return stage + (((int64_t)buf * 3 + t) * NW + rw) * G; };
+    auto issue = [&](int64_t rb, int buf) {   // rows rb .. rb+NW-1 (those < r1) into buffer buf
+        for (int i = threadIdx.x; i < ntens * NW * cpr; i += NW * 32) {
+            const int t = i / (NW * cpr), rem = i % (NW * cpr), rw = rem / cpr, q = rem % cpr;
+            const int64_t r = rb + rw;
+            if (r >= r1) continue;
+            const T *src = t == 0 ? static_cast<const T *>(a.y) + r * a.sy
+                         : t == 1 ? static_cast<const T *>(a.dout) + r * a.sdout
+                                  : static_cast<const T *>(a.z) + r * a.sz;
+            cp16(reinterpret_cast<uint8_t *>(tile(buf, t, rw)) + 16 * q,
+                 reinterpret_cast<const uint8_t *>(src + (int64_t)g * G) + 16 * q);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int buf = 0;
+    if (r0 < r1) issue(r0, 0);
+    for (int64_t rb = r0; rb < r1; rb += NW, buf ^= 1) {
+        if (rb + NW < r1) {
+            issue(rb + NW, buf ^ 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        const int64_t r = rb + warp;
+        if (r < r1) {
+            const T *ys = tile(buf, 0, warp), *ds = tile(buf, 1, warp), *zs = a.z ? tile(buf, 2, warp) : nullptr;
+            float y8[PPL][8], z8[PPL][8], d[PPL][8];
+#pragma unroll
+            for (int k = 0; k < PPL; ++k) {
+                const int j = lane + 32 * k;
+                if (j < pieces) {
+                    load8(ys + 8 * j, y8[k]);
+                    load8(ds + 8 * j, d[k]);
+                    if (zs) load8(zs + 8 * j, z8[k]);
+                }
+            }
+            const float rs = a.rstd_in[r * a.ng + g];
+            float dot = 0.f;
+#pragma unroll
+            for (int k = 0; k < PPL; ++k) {
+                if (lane + 32 * k < pieces) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float sgate = zs ? z8[k][e] * sig(z8[k][e]) : 1.f;
+                        dot = fmaf(d[k][e] * wv[k][e], y8[k][e] * sgate * rs, dot);
+                    }
+                }
+            }
+            dot = warp_sum(dot) / (float)G;
+            T *dyr = static_cast<T *>(a.dy) + r * a.sdy + (int64_t)g * G;
+            T *dzr = a.z ? static_cast<T *>(a.dz) + r * a.sdz + (int64_t)g * G : nullptr;
+#pragma unroll
+            for (int k = 0; k < PPL; ++k) {
+                const int j = lane + 32 * k;
+                if (j < pieces) {
+                    float o1[8], o2[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float sg = zs ? sig(z8[k][e]) : 0.f;
+                        const float sgate = zs ? z8[k][e] * sg : 1.f;
+                        const float vhat = y8[k][e] * sgate * rs;
+                        const float dv = rs * (d[k][e] * wv[k][e] - vhat * dot);
+                        o1[e] = dv * sgate;
+                        o2[e] = zs ? dv * y8[k][e] * sg * (1.f + z8[k][e] * (1.f - sg)) : 0.f;
+                        dw[k][e] = fmaf(d[k][e], vhat, dw[k][e]);
+                    }
+                    store8(dyr + 8 * j, o1);
+                    if (zs) store8(dzr + 8 * j, o2);
+                }
+            }
+        }
+        __syncthreads();   // this buffer is refilled two batches on
+    }
+    float *acc = reinterpret_cast<float *>(nsm);   // [NW][G], over the (now idle) stage
+    float *mine = acc + (int64_t)warp * G;
+#pragma unroll
+    for (int k = 0; k < PPL; ++k) {
+        const int j = lane + 32 * k;
+        if (j < pieces)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mine[8 * j + e] = dw[k][e];
+    }
+    __syncthreads();
+    float *dst = a.partials + (int64_t)blockIdx.x * a.width + (int64_t)g * G;
+    for (int i = threadIdx.x; i < G; i += NW * 32) {
+        float sum = 0.f;
+        for (int q = 0; q < NW; ++q) sum += acc[(int64_t)q * G + i];
+        dst[i] = sum;
+    }
+}
+template <typename T>
+size_t staged_smem(int64_t G) {
+    const size_t stage = (size_t)2 * 3 * NW * (size_t)G * sizeof(T);
+    const size_t red = (size_t)NW * (size_t)G * sizeof(float);
+    return stage > red ? stage : red;
+}
+
 __global__ void k_norm_dw(const float *partials, int64_t chunks, int64_t width, float *dw) {
+    // four interleaved partial sums, then combined: a fixed order, so bitwise reproducible
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < width; i += (int64_t)gridDim.x * blockDim.x) {
-        float s = 0.f;
-        for (int64_t c = 0; c < chunks; ++c) s += partials[c * width + i];
-        dw[i] = s;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        int64_t c = 0;
+        for (; c + 4 <= chunks; c += 4)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) s4[q] += partials[(c + q) * width + i];
+        for (; c < chunks; ++c) s4[0] += partials[c * width + i];
+        dw[i] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     }
 }
 
@@ -341,9 +474,10 @@ cudaError_t launch_one(K kernel, const NormArgs &a, dim3 grid, size_t smem, cuda
 template <typename T>
 cudaError_t launch_norm_bwd(const NormArgs &a, int64_t ppl, dim3 grid, size_t smem, cudaStream_t st) {
     static int attr[4][64] = {};
-    if (ppl <= 1) return launch_one(k_norm_bwd_reg<T, 1>, a, grid, smem, st, attr[0]);
-    if (ppl <= 2) return launch_one(k_norm_bwd_reg<T, 2>, a, grid, smem, st, attr[1]);
-    if (ppl <= 4) return launch_one(k_norm_bwd_reg<T, 4>, a, grid, smem, st, attr[2]);
+    const size_t ssm = staged_smem<T>(a.G);
+    if (ppl <= 1) return launch_one(k_norm_bwd_staged<T, 1>, a, grid, ssm, st, attr[0]);
+    if (ppl <= 2) return launch_one(k_norm_bwd_staged<T, 2>, a, grid, ssm, st, attr[1]);
+    if (ppl <= 4) return launch_one(k_norm_bwd_staged<T, 4>, a, grid, ssm, st, attr[2]);
     return launch_one(k_norm_bwd<T>, a, grid, smem, st, attr[3]);
 }
 
@@ -465,8 +599,8 @@ ssd_status ssd_gated_norm_bwd(const ssd_norm_problem *p, const void *y, int64_t 
     else
         e = launch_norm_bwd<float>(a, ppl, grid, smem, st);
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
-    const int blocks = (int)std::min<int64_t>((p->width + 255) / 256, 1024);
-    k_norm_dw<<<blocks, 256, 0, st>>>(a.partials, chunks, p->width, dweight);
+    const int blocks = (int)std::min<int64_t>((p->width + 63) / 64, 4096);
+    k_norm_dw<<<blocks, 64, 0, st>>>(a.partials, chunks, p->width, dweight);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
