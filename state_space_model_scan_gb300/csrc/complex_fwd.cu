@@ -14,17 +14,21 @@
 // K-vectors stored as [re, im] pairs, sum u v = [u_re, u_im] . [v_re, -v_im]  (real part)
 // and [u_re, u_im] . [v_im, v_re]  (imaginary part), so the as-loaded interleaved operand
 // pairs with a "conjugated" and a "swapped" copy of the other one; equally
-// [u_im, -u_re] . [v_re, -v_im] is the imaginary part.  Both parts of every complex result
-// land in the same TMEM lane (two column blocks).  Per chunk:
-//   Cb    = C B^T                      A = C, C' = (Im C, -Re C),   B = conj(B tile)
-//   Yraw  = C S^T    (carry-in state)  A = C, C',                   B = conj(S)
-//   Ydiag = (L o Cb) X                 A = [Mr, Mi](l, s),          B = {conj, swap}(X^T)
-//   Sloc  = (w o B)^T X                A = [(wB)r, (wB)i](n, l),    B = {conj, swap}(X^T)
+// [u_im, -u_re] . [v_re, -v_im] is the imaginary part.  An M = 128 MMA costs the issuing
+// thread no more than an M = 64 one, so two 64-row A operands are stacked into one:
+//   batch 1  A = [C ; C'],  C' = (Im C, -Re C)        B = conj(B tile) -> [Re Cb ; Im Cb]
+//                                                     B = conj(S)      -> [Re Yraw ; Im Yraw]
+//   batch 2  A = [M ; (w o B)^T],  M = L o Cb          B = conj(X^T)   -> [Re Ydiag ; Re Sloc]
+//                                                     B = swap(X^T)   -> [Im Ydiag ; Im Sloc]
 //   y = Ydiag + exp(cs_l) Yraw ;  S <- exp(cs_63) S + Sloc
-// with cs the in-chunk inclusive cumulative sum of softplus(dt) A, L[l, s] = exp(cs_l - cs_s)
-// for l >= s and w_l = exp(cs_63 - cs_l).  The MMAs are M = 64 (rows 16q..16q+15 in TMEM
-// lanes 32q..32q+15), N = 64, K = 128 (16 instructions of K = 8).  Positions past the end of
-// the sequence read as zero (TMA bounds fill) and carry no decay.
+// (Cb = C B^T, Yraw = C S^T with S the carry-in state, Ydiag = M X, Sloc = (w o B)^T X) with
+// cs the in-chunk inclusive cumulative sum of softplus(dt) A, L[l, s] = exp(cs_l - cs_s) for
+// l >= s and w_l = exp(cs_63 - cs_l).  TMEM lanes 0..63 (the upper half of the CTA's warps)
+// hold rows l of Cb, Yraw and Ydiag; lanes 64..127 (the lower half) the imaginary parts of
+// Cb and Yraw, which they pass to the upper half through shared memory, and Sloc, whose rows n
+// they fold into the carried state.  MMAs: M = 128, N = 64, K = 128 (16 of K = 8 each),
+// 64 per chunk.  Positions past the end of the sequence read as zero (TMA bounds fill) and
+// carry no decay.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -41,19 +45,26 @@ constexpr int CQ = 64;                      // chunk length
 constexpr int CD = 64;                      // head dimension (P)
 constexpr int CN = 64;                      // state dimension
 constexpr int CX_THREADS = 512;             // 16 warps: four per TMEM lane quadrant
-constexpr uint32_t SLOT = 32768;            // one operand: 64 rows x 128 fp32, 4 K-atoms of 8 KB
+constexpr uint32_t SLOT = 32768;            // a 64-row operand: 64 rows x 128 fp32, 4 K-atoms of 8 KB
 constexpr uint32_t ATOM = 8192;
-constexpr uint32_t OFF_P0 = 0, OFF_P1 = SLOT, OFF_P2 = 2 * SLOT, OFF_P3 = 3 * SLOT, OFF_P4 = 4 * SLOT;
-constexpr uint32_t OFF_S0 = 5 * SLOT;                      // carried state, conjugated
-constexpr uint32_t OFF_MISC = 6 * SLOT;
+constexpr uint32_t ATOM128 = 16384;         // K-atom of a 128-row operand (rows 64.. at +8 KB)
+constexpr uint32_t OFF_CC = 0;              // 128-row: [C ; C'] (batch 1), then [M ; (w o B)^T] (batch 2)
+constexpr uint32_t OFF_BB = 2 * SLOT;       // conj(B tile), then swap(X^T)
+constexpr uint32_t OFF_SS = 3 * SLOT;       // carried state, conjugated
+constexpr uint32_t OFF_X = 4 * SLOT;        // X tile as loaded
+constexpr uint32_t OFF_XC = 5 * SLOT;       // conj(X^T)
+constexpr uint32_t OFF_E = 6 * SLOT;        // exchange: imaginary parts of Cb, then of Yraw, [64][65] fp32
+constexpr uint32_t E_STRIDE = 65;
+constexpr uint32_t OFF_MISC = OFF_E + 64 * E_STRIDE * 4 + 256;
 // per-chunk tables, two sets (chunk c uses set c & 1; the next chunk's is built meanwhile)
 constexpr uint32_t MISC_CS = 0, MISC_E = 1024, MISC_W = 2048, MISC_ROT = 3072, MISC_BAR = 4096, MISC_TMEM = 4160,
                    MISC_ABORT = 4164;
 constexpr uint32_t CX_SMEM = OFF_MISC + 4608 + 1024;       // + alignment slack
 constexpr uint32_t TX_BYTES = 3 * SLOT;                    // C, B and X tiles of one chunk
 
-// TMEM columns: four accumulators of 128 columns (real part block, imaginary part block).
-constexpr uint32_t TC_CB = 0, TC_YR = 128, TC_YD = 256, TC_SL = 384;
+// TMEM columns: [Re Cb ; Im Cb] 64, [Re Yraw ; Im Yraw] 64, [Ydiag ; Sloc] real parts 64 and
+// imaginary parts 64 (lanes 0..63 / 64..127 in each).
+constexpr uint32_t TC_CB = 0, TC_YR = 64, TC_Y2 = 128, TM_COLS = 256;
 
 enum { BAR_IN = 0, BAR_M1 = 1, BAR_M2 = 2 };
 
@@ -82,9 +93,18 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a, uint64_t 
 __device__ __forceinline__ uint64_t opdesc(uint32_t slot, int k) {
     return sdesc(slot + (uint32_t)(k >> 2) * ATOM + (uint32_t)(k & 3) * 32u, 16u, 1024u);
 }
-// Byte offset of fp32 element (row r, k) inside a slot (128-byte swizzle, K-major).
+// K step k of a 128-row operand.
+__device__ __forceinline__ uint64_t opdesc128(uint32_t slot, int k) {
+    return sdesc(slot + (uint32_t)(k >> 2) * ATOM128 + (uint32_t)(k & 3) * 32u, 16u, 1024u);
+}
+// Byte offset of fp32 element (row r, k) inside a 64-row slot (128-byte swizzle, K-major) ...
 __device__ __forceinline__ uint32_t elem_off(int r, int k) {
     return (uint32_t)(k >> 5) * ATOM + (uint32_t)r * 128u + ((uint32_t)(((k & 31) >> 2) ^ (r & 7)) << 4) +
+           (uint32_t)(k & 3) * 4u;
+}
+// ... and inside a 128-row operand
+__device__ __forceinline__ uint32_t elem_off128(int r, int k) {
+    return (uint32_t)(k >> 5) * ATOM128 + (uint32_t)r * 128u + ((uint32_t)(((k & 31) >> 2) ^ (r & 7)) << 4) +
            (uint32_t)(k & 3) * 4u;
 }
 __device__ __forceinline__ float tf32r(float v) {   // round to the tf32 grid (nearest, ties away)
@@ -116,8 +136,8 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
               const __grid_constant__ CUtensorMap tmC, const CxParams p) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *P0 = sm + OFF_P0, *P1 = sm + OFF_P1, *P2 = sm + OFF_P2, *P3 = sm + OFF_P3, *P4 = sm + OFF_P4;
-    uint8_t *S0 = sm + OFF_S0;
+    uint8_t *CC = sm + OFF_CC, *BB = sm + OFF_BB, *SS = sm + OFF_SS, *XT = sm + OFF_X, *XC = sm + OFF_XC;
+    float *E = reinterpret_cast<float *>(sm + OFF_E);
     float2 *cs_t = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_CS);    // [2][CQ] in-chunk cumsum
     float2 *ecs_t = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_E);    // [2][CQ] exp(cs_l)
     float2 *wv_t = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_W);     // [2][CQ] exp(cs_63 - cs_l)
@@ -131,11 +151,12 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
     const int64_t b = item / p.H, h = item % p.H;
     const int nc = (int)((p.T + CQ - 1) / CQ);
     const float2 Ah = make_float2(p.A[2 * h], p.A[2 * h + 1]);
-    // TMEM-phase mapping (M = 64 accumulators): lanes 0..15 of each warp hold rows
-    // quad*16 + lane; the four warps of a quadrant take 16 columns each.
+    // TMEM-phase mapping (M = 128 accumulators): warp w reads lanes 32 (w & 3) .. + 31, i.e.
+    // accumulator row r = 32 (w & 3) + lane; the four warps of a lane quadrant take 16 columns
+    // each.  Upper half (rows 0..63): row l = r; lower half: l or n = r - 64.
     const int quad = warp & 3, sub = warp >> 2;
-    const bool trow = lane < 16;
-    const int row = quad * 16 + (lane & 15);
+    const bool upper = quad < 2;
+    const int r64 = 32 * (quad & 1) + lane;   // l (upper) or the lower half's row - 64
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
     if (tid == 0) {
@@ -146,33 +167,32 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmC);
     }
-    if (warp == 0) tmem_alloc(tmem_slot, 512);
+    if (warp == 0) tmem_alloc(tmem_slot, TM_COLS);
     // carried state from initial_states (or zero), kept as conj(S): rows d, K = 2n + part, (Sr, -Si)
     for (int i = tid; i < CD * CN; i += CX_THREADS) {
         const int d = i / CN, n = i % CN;
         float2 v = make_float2(0.f, 0.f);
         if (p.init != nullptr) v = reinterpret_cast<const float2 *>(p.init)[((b * p.H + h) * CD + d) * CN + n];
-        st_pair(S0, d, 2 * n, v.x, -v.y);
+        st_pair(SS, d, 2 * n, v.x, -v.y);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t sP0 = smem_u32(P0), sP1 = smem_u32(P1), sP3 = smem_u32(P3), sP4 = smem_u32(P4);
-    const uint32_t sS0 = smem_u32(S0);
-    const uint32_t id64 = idesc_tf32(64, 64);
+    const uint32_t sCC = smem_u32(CC), sBB = smem_u32(BB), sSS = smem_u32(SS), sXC = smem_u32(XC);
+    const uint32_t id128 = idesc_tf32(128, 64);
 
     // One BAR_IN phase per chunk, armed for all three tiles when the X tile is issued; the C
     // and B tiles follow later into the same phase.
     auto load_x = [&](int c) {
         mbar_expect_tx(&bar[BAR_IN], TX_BYTES);
-        for (int a = 0; a < 4; ++a) tma_load_4d(P2 + a * ATOM, &tmX, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);
+        for (int a = 0; a < 4; ++a) tma_load_4d(XT + a * ATOM, &tmX, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);
     };
     auto load_cb = [&](int c) {
         for (int a = 0; a < 4; ++a) {
-            tma_load_4d(P0 + a * ATOM, &tmC, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);
-            tma_load_4d(P1 + a * ATOM, &tmB, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);
+            tma_load_4d(CC + a * ATOM128, &tmC, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);   // rows 0..63
+            tma_load_4d(BB + a * ATOM, &tmB, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);
         }
     };
     // thread 0's record of what may still be in flight when a bounded wait gives up
@@ -244,13 +264,14 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         }
         __syncthreads();
         if (*abort_) break;
-        // C rounded in place (P0) and C' = (Im C, -Re C) into P3; conj(B) in place (P1)
+        // C rounded in place (rows 0..63 of CC) and C' = (Im C, -Re C) below it (rows 64..127, the
+        // same swizzled position 8 KB on); conj(B) in place
         for (int i = tid; i < (int)(SLOT / 16); i += CX_THREADS) {
-            float4 *cp = reinterpret_cast<float4 *>(P0) + i;
+            float4 *cp = reinterpret_cast<float4 *>(CC + (i >> 9) * ATOM128) + (i & 511);
             const float4 cv = *cp;
             *cp = make_float4(tf32r(cv.x), tf32r(cv.y), tf32r(cv.z), tf32r(cv.w));
-            reinterpret_cast<float4 *>(P3)[i] = make_float4(tf32r(cv.y), tf32r(-cv.x), tf32r(cv.w), tf32r(-cv.z));
-            float4 *bp = reinterpret_cast<float4 *>(P1) + i;
+            cp[ATOM / 16] = make_float4(tf32r(cv.y), tf32r(-cv.x), tf32r(cv.w), tf32r(-cv.z));
+            float4 *bp = reinterpret_cast<float4 *>(BB) + i;
             const float4 bv = *bp;
             *bp = make_float4(tf32r(bv.x), tf32r(-bv.y), tf32r(bv.z), tf32r(-bv.w));
         }
@@ -258,17 +279,15 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // ---- batch 1: Cb = C B^T and Yraw = C S^T, real parts with C, imaginary parts with C'
+        // ---- batch 1: [Re Cb ; Im Cb] and [Re Yraw ; Im Yraw]
         if (tid == 0) {
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_CB, opdesc(sP0, k), opdesc(sP1, k), id64, k > 0);
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_CB + 64, opdesc(sP3, k), opdesc(sP1, k), id64, k > 0);
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YR, opdesc(sP0, k), opdesc(sS0, k), id64, k > 0);
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YR + 64, opdesc(sP3, k), opdesc(sS0, k), id64, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_CB, opdesc128(sCC, k), opdesc(sBB, k), id128, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YR, opdesc128(sCC, k), opdesc(sSS, k), id128, k > 0);
             umma_commit(&bar[BAR_M1]);
             m_par = par;
             m1_pending = true;
         }
-        // ---- meanwhile conj(X^T) into P4 (rows d, K = 2s + part: Xr, -Xi).  A warp reads one
+        // ---- meanwhile conj(X^T) into XC (rows d, K = 2s + part: Xr, -Xi).  A warp reads one
         // 16-byte piece (two complex columns d) of 32 consecutive rows s and writes a contiguous
         // 256-byte run of rows d and d+1.
         {
@@ -276,9 +295,9 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int d0 = 2 * ((warp >> 1) + 8 * i);
-                const float4 v = *reinterpret_cast<const float4 *>(P2 + elem_off(s, 2 * d0));
-                st_pair(P4, d0, 2 * s, tf32r(v.x), tf32r(-v.y));
-                st_pair(P4, d0 + 1, 2 * s, tf32r(v.z), tf32r(-v.w));
+                const float4 v = *reinterpret_cast<const float4 *>(XT + elem_off(s, 2 * d0));
+                st_pair(XC, d0, 2 * s, tf32r(v.x), tf32r(-v.y));
+                st_pair(XC, d0 + 1, 2 * s, tf32r(v.z), tf32r(-v.w));
             }
         }
         if (tid == 0) {
@@ -288,70 +307,78 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         __syncthreads();
         tc_fence_after();
         if (*abort_) break;
-        // ---- swap(X^T) into P3 (Xi, Xr) and (w o B)^T into P0 (rows n, K = 2l + part) from conj(B)
-        {
-            const int s = lane + 32 * (warp & 1);
-            const float2 ws = wv[s];
+        // ---- lower half: Im Cb rows into E; upper half: (w o B)^T into rows 64..127 of CC (rows n,
+        // K = 2l + part) from conj(B)
+        if (!upper) {
+            float im[16];
+            tmem_ld16(tmem + lane_base + TC_CB + 16 * sub, im);
+            tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int d0 = 2 * ((warp >> 1) + 8 * i);
-                const float4 v = *reinterpret_cast<const float4 *>(P2 + elem_off(s, 2 * d0));
-                st_pair(P3, d0, 2 * s, tf32r(v.y), tf32r(v.x));
-                st_pair(P3, d0 + 1, 2 * s, tf32r(v.w), tf32r(v.z));
-                const float4 cb = *reinterpret_cast<const float4 *>(P1 + elem_off(s, 2 * d0));
-                const float2 v0 = cmul(ws, make_float2(cb.x, -cb.y)), v1 = cmul(ws, make_float2(cb.z, -cb.w));
-                st_pair(P0, d0, 2 * s, tf32r(v0.x), tf32r(v0.y));
-                st_pair(P0, d0 + 1, 2 * s, tf32r(v1.x), tf32r(v1.y));
+            for (int j = 0; j < 16; ++j) E[r64 * E_STRIDE + 16 * sub + j] = im[j];
+        } else {
+            const int l = r64;
+            const float2 wl = wv[l];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int n0 = 2 * (sub + 4 * i);
+                const float4 cb = *reinterpret_cast<const float4 *>(BB + elem_off(l, 2 * n0));
+                const float2 v0 = cmul(wl, make_float2(cb.x, -cb.y)), v1 = cmul(wl, make_float2(cb.z, -cb.w));
+                *reinterpret_cast<float2 *>(CC + elem_off128(64 + n0, 2 * l)) = make_float2(tf32r(v0.x), tf32r(v0.y));
+                *reinterpret_cast<float2 *>(CC + elem_off128(65 + n0, 2 * l)) = make_float2(tf32r(v1.x), tf32r(v1.y));
             }
         }
-        fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0 && c + 1 < nc) {   // the X tile of the next chunk into the freed slot
-            load_x(c + 1);
-            in_pending = true;
-        }
-        // ---- M = L o Cb into P1 (rows l, K = 2s + part): lanes 0..15 of each warp, 16 columns
-        {
-            float re[16], im[16];
+        // ---- upper half: M = L o Cb into rows 0..63 of CC (rows l, K = 2s + part), 16 columns a
+        // thread; lower half: swap(X^T) into BB (Xi, Xr)
+        if (upper) {
+            const int l = r64;
+            float re[16];
             tmem_ld16(tmem + lane_base + TC_CB + 16 * sub, re);
-            tmem_ld16(tmem + lane_base + TC_CB + 64 + 16 * sub, im);
             tmem_wait_ld();
-            if (trow) {
-                // L[l, s] = exp(Re(cs_l - cs_s)) rot_l conj(rot_s): the phase factors have modulus one,
-                // so splitting them costs no range; the magnitude stays a difference
-                const float lre = cs[row].x * 1.4426950408889634f;
-                const float2 rl = rot[row];
-                float out[32];
+            // L[l, s] = exp(Re(cs_l - cs_s)) rot_l conj(rot_s): the phase factors have modulus one,
+            // so splitting them costs no range; the magnitude stays a difference
+            const float lre = cs[l].x * 1.4426950408889634f;
+            const float2 rl = rot[l];
+            float out[32];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int s = 16 * sub + j;
-                    float2 m = make_float2(0.f, 0.f);
-                    if (s <= row) {
-                        const float2 rs = rot[s];
-                        const float mag = ex2(lre - cs[s].x * 1.4426950408889634f);
-                        const float2 ph = make_float2(rl.x * rs.x + rl.y * rs.y, rl.y * rs.x - rl.x * rs.y);
-                        m = cmul(make_float2(mag * ph.x, mag * ph.y), make_float2(re[j], im[j]));
-                    }
-                    out[2 * j] = tf32r(m.x);
-                    out[2 * j + 1] = tf32r(m.y);
+            for (int j = 0; j < 16; ++j) {
+                const int s = 16 * sub + j;
+                float2 m = make_float2(0.f, 0.f);
+                if (s <= l) {
+                    const float2 rs = rot[s];
+                    const float mag = ex2(lre - cs[s].x * 1.4426950408889634f);
+                    const float2 ph = make_float2(rl.x * rs.x + rl.y * rs.y, rl.y * rs.x - rl.x * rs.y);
+                    m = cmul(make_float2(mag * ph.x, mag * ph.y), make_float2(re[j], E[l * E_STRIDE + s]));
                 }
+                out[2 * j] = tf32r(m.x);
+                out[2 * j + 1] = tf32r(m.y);
+            }
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<float4 *>(P1 + elem_off(row, 32 * sub + 4 * j)) =
-                        make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4 *>(CC + elem_off128(l, 32 * sub + 4 * j)) =
+                    make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+        } else {
+            const int s = r64;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d0 = 2 * (sub + 4 * i);
+                const float4 v = *reinterpret_cast<const float4 *>(XT + elem_off(s, 2 * d0));
+                st_pair(BB, d0, 2 * s, tf32r(v.y), tf32r(v.x));
+                st_pair(BB, d0 + 1, 2 * s, tf32r(v.w), tf32r(v.z));
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // ---- batch 2: Ydiag = M X and Sloc = (w o B)^T X (real parts with conj(X^T), imaginary with swap)
+        // ---- batch 2: [Re Ydiag ; Re Sloc] and [Im Ydiag ; Im Sloc]
         if (tid == 0) {
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YD, opdesc(sP1, k), opdesc(sP4, k), id64, k > 0);
-            if (p.y_im != nullptr)
-                for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YD + 64, opdesc(sP1, k), opdesc(sP3, k), id64, k > 0);
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_SL, opdesc(sP0, k), opdesc(sP4, k), id64, k > 0);
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_SL + 64, opdesc(sP0, k), opdesc(sP3, k), id64, k > 0);
+            if (c + 1 < nc) {   // the X tile of the next chunk into its freed slot
+                load_x(c + 1);
+                in_pending = true;
+            }
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_Y2, opdesc128(sCC, k), opdesc(sXC, k), id128, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_Y2 + 64, opdesc128(sCC, k), opdesc(sBB, k), id128, k > 0);
             umma_commit(&bar[BAR_M2]);
             m2_pending = true;
             if (!mbar_wait_abort(&bar[BAR_M2], par, abort_)) {
@@ -361,21 +388,28 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                 if (c + 1 < nc) load_cb(c + 1);   // C and B slots are free again: overlaps the epilogue
             }
         }
-        if (warp == 1 && c + 1 < nc) build_tables(c + 1);   // while thread 0 waits for batch 2
+        if (!upper) {   // meanwhile the lower half passes Im Yraw to the upper half
+            float yi[16];
+            tmem_ld16(tmem + lane_base + TC_YR + 16 * sub, yi);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) E[r64 * E_STRIDE + 16 * sub + j] = yi[j];
+        }
+        if (warp == 1 && c + 1 < nc) build_tables(c + 1);   // ... and warp 1 the next tables
         __syncthreads();
         tc_fence_after();
         if (*abort_) break;
-        // ---- outputs: y = Ydiag + exp(cs_l) Yraw
-        {
-            float yr[16], yi[16], dr[16], di[16];
+        if (upper) {   // ---- outputs of rows l: y = Ydiag + exp(cs_l) Yraw
+            const int l = r64;
+            float yr[16], dr[16], di[16];
             tmem_ld16(tmem + lane_base + TC_YR + 16 * sub, yr);
-            tmem_ld16(tmem + lane_base + TC_YR + 64 + 16 * sub, yi);
-            tmem_ld16(tmem + lane_base + TC_YD + 16 * sub, dr);
-            if (p.y_im != nullptr) tmem_ld16(tmem + lane_base + TC_YD + 64 + 16 * sub, di);
+            tmem_ld16(tmem + lane_base + TC_Y2 + 16 * sub, dr);
+            tmem_ld16(tmem + lane_base + TC_Y2 + 64 + 16 * sub, di);
             tmem_wait_ld();
-            const int64_t t = t0 + row;
-            if (trow && t < p.T) {
-                const float2 e = ecs[row];
+            const int64_t t = t0 + l;
+            if (t < p.T) {
+                const float2 e = ecs[l];
+                const float *yi = E + l * E_STRIDE + 16 * sub;
                 const int64_t off = ((b * p.T + t) * p.H + h) * CD + 16 * sub;
                 float o[16];
 #pragma unroll
@@ -393,24 +427,20 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                             make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
                 }
             }
-        }
-        // ---- state: S <- exp(cs_63) S + Sloc (row n, columns d); each (d, n) has one owner
-        {
+        } else {   // ---- state of rows n: S <- exp(cs_63) S + Sloc (columns d); each (d, n) has one owner
+            const int n = r64;
             float sr[16], si[16];
-            tmem_ld16(tmem + lane_base + TC_SL + 16 * sub, sr);
-            tmem_ld16(tmem + lane_base + TC_SL + 64 + 16 * sub, si);
+            tmem_ld16(tmem + lane_base + TC_Y2 + 16 * sub, sr);
+            tmem_ld16(tmem + lane_base + TC_Y2 + 64 + 16 * sub, si);
             tmem_wait_ld();
-            if (trow) {
-                const float2 e = ecs[CQ - 1];
-                const int n = row;
+            const float2 e = ecs[CQ - 1];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int d = 16 * sub + j;
-                    const float2 o = ld_pair(S0, d, 2 * n);   // (Sr, -Si)
-                    const float nr = e.x * o.x + e.y * o.y + sr[j];
-                    const float ni = e.x * (-o.y) + e.y * o.x + si[j];
-                    st_pair(S0, d, 2 * n, nr, -ni);
-                }
+            for (int j = 0; j < 16; ++j) {
+                const int d = 16 * sub + j;
+                const float2 o = ld_pair(SS, d, 2 * n);   // (Sr, -Si)
+                const float nr = e.x * o.x + e.y * o.y + sr[j];
+                const float ni = e.x * (-o.y) + e.y * o.x + si[j];
+                st_pair(SS, d, 2 * n, nr, -ni);
             }
         }
         fence_proxy_async_smem();
@@ -429,14 +459,14 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
     } else if (p.final_ != nullptr) {
         for (int i = tid; i < CD * CN; i += CX_THREADS) {
             const int d = i / CN, n = i % CN;
-            const float2 v = ld_pair(S0, d, 2 * n);
+            const float2 v = ld_pair(SS, d, 2 * n);
             reinterpret_cast<float2 *>(p.final_)[((b * p.H + h) * CD + d) * CN + n] = make_float2(v.x, -v.y);
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_cx() {
