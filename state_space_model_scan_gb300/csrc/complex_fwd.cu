@@ -14,20 +14,21 @@
 // K-vectors stored as [re, im] pairs, sum u v = [u_re, u_im] . [v_re, -v_im]  (real part)
 // and [u_re, u_im] . [v_im, v_re]  (imaginary part), so the as-loaded interleaved operand
 // pairs with a "conjugated" and a "swapped" copy of the other one; equally
-// [u_im, -u_re] . [v_re, -v_im] is the imaginary part.  An M = 128 MMA costs the issuing
-// thread no more than an M = 64 one, so two 64-row A operands are stacked into one:
-//   batch 1  A = [C ; C'],  C' = (Im C, -Re C)        B = conj(B tile) -> [Re Cb ; Im Cb]
-//                                                     B = conj(S)      -> [Re Yraw ; Im Yraw]
-//   batch 2  A = [M ; (w o B)^T],  M = L o Cb          B = conj(X^T)   -> [Re Ydiag ; Re Sloc]
-//                                                     B = swap(X^T)   -> [Im Ydiag ; Im Sloc]
+// [u_re, -u_im] . [v_re, v_im] and [u_im, u_re] . [v_re, v_im] are the real and imaginary parts.
+// An M = 128 MMA costs the issuing thread no more than an M = 64 one, and an N = 128 one about
+// 1.4 times an N = 64 one, so operands are stacked on both sides:
+//   batch 1  A = [conj(C) ; swap(C)]    B = [B tile ; S]  -> [Re Cb | Re Yraw ; Im Cb | Im Yraw]
+//   batch 2  A = [M ; (w o B)^T],  M = L o Cb
+//                                       B = conj(X^T)    -> [Re Ydiag ; Re Sloc]
+//                                       B = swap(X^T)    -> [Im Ydiag ; Im Sloc]
 //   y = Ydiag + exp(cs_l) Yraw ;  S <- exp(cs_63) S + Sloc
 // (Cb = C B^T, Yraw = C S^T with S the carry-in state, Ydiag = M X, Sloc = (w o B)^T X) with
 // cs the in-chunk inclusive cumulative sum of softplus(dt) A, L[l, s] = exp(cs_l - cs_s) for
 // l >= s and w_l = exp(cs_63 - cs_l).  TMEM lanes 0..63 (the upper half of the CTA's warps)
 // hold rows l of Cb, Yraw and Ydiag; lanes 64..127 (the lower half) the imaginary parts of
 // Cb and Yraw, which they pass to the upper half through shared memory, and Sloc, whose rows n
-// they fold into the carried state.  MMAs: M = 128, N = 64, K = 128 (16 of K = 8 each),
-// 64 per chunk.  Positions past the end of the sequence read as zero (TMA bounds fill) and
+// they fold into the carried state.  MMAs (K = 128: 16 of K = 8 each): 16 of M = 128,
+// N = 128 and 32 of M = 128, N = 64 per chunk.  Positions past the end of the sequence read as zero (TMA bounds fill) and
 // carry no decay.
 #include <cudaTypedefs.h>
 
@@ -48,9 +49,8 @@ constexpr int CX_THREADS = 512;             // 16 warps: four per TMEM lane quad
 constexpr uint32_t SLOT = 32768;            // a 64-row operand: 64 rows x 128 fp32, 4 K-atoms of 8 KB
 constexpr uint32_t ATOM = 8192;
 constexpr uint32_t ATOM128 = 16384;         // K-atom of a 128-row operand (rows 64.. at +8 KB)
-constexpr uint32_t OFF_CC = 0;              // 128-row: [C ; C'] (batch 1), then [M ; (w o B)^T] (batch 2)
-constexpr uint32_t OFF_BB = 2 * SLOT;       // conj(B tile), then swap(X^T)
-constexpr uint32_t OFF_SS = 3 * SLOT;       // carried state, conjugated
+constexpr uint32_t OFF_CC = 0;              // 128-row: [conj(C) ; swap(C)] (batch 1), then [M ; (w o B)^T]
+constexpr uint32_t OFF_BS = 2 * SLOT;       // 128-row: [B tile (then swap(X^T)) ; carried state S]
 constexpr uint32_t OFF_X = 4 * SLOT;        // X tile as loaded
 constexpr uint32_t OFF_XC = 5 * SLOT;       // conj(X^T)
 constexpr uint32_t OFF_E = 6 * SLOT;        // exchange: imaginary parts of Cb, then of Yraw, [64][65] fp32
@@ -62,8 +62,8 @@ constexpr uint32_t MISC_CS = 0, MISC_E = 1024, MISC_W = 2048, MISC_ROT = 3072, M
 constexpr uint32_t CX_SMEM = OFF_MISC + 4608 + 1024;       // + alignment slack
 constexpr uint32_t TX_BYTES = 3 * SLOT;                    // C, B and X tiles of one chunk
 
-// TMEM columns: [Re Cb ; Im Cb] 64, [Re Yraw ; Im Yraw] 64, [Ydiag ; Sloc] real parts 64 and
-// imaginary parts 64 (lanes 0..63 / 64..127 in each).
+// TMEM columns: batch 1 [Cb | Yraw] 128 (real parts in lanes 0..63, imaginary in 64..127);
+// batch 2 [Ydiag ; Sloc] real parts 64, imaginary parts 64.
 constexpr uint32_t TC_CB = 0, TC_YR = 64, TC_Y2 = 128, TM_COLS = 256;
 
 enum { BAR_IN = 0, BAR_M1 = 1, BAR_M2 = 2 };
@@ -127,16 +127,13 @@ __device__ __forceinline__ float softplus_f(float v) {
 __device__ __forceinline__ void st_pair(uint8_t *slot, int r, int k, float a, float b) {
     *reinterpret_cast<float2 *>(slot + elem_off(r, k)) = make_float2(a, b);
 }
-__device__ __forceinline__ float2 ld_pair(const uint8_t *slot, int r, int k) {
-    return *reinterpret_cast<const float2 *>(slot + elem_off(r, k));
-}
 
 __global__ void __launch_bounds__(CX_THREADS, 1)
 k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const CxParams p) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *CC = sm + OFF_CC, *BB = sm + OFF_BB, *SS = sm + OFF_SS, *XT = sm + OFF_X, *XC = sm + OFF_XC;
+    uint8_t *CC = sm + OFF_CC, *BS = sm + OFF_BS, *XT = sm + OFF_X, *XC = sm + OFF_XC;
     float *E = reinterpret_cast<float *>(sm + OFF_E);
     float2 *cs_t = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_CS);    // [2][CQ] in-chunk cumsum
     float2 *ecs_t = reinterpret_cast<float2 *>(sm + OFF_MISC + MISC_E);    // [2][CQ] exp(cs_l)
@@ -168,20 +165,20 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         prefetch_tmap(&tmC);
     }
     if (warp == 0) tmem_alloc(tmem_slot, TM_COLS);
-    // carried state from initial_states (or zero), kept as conj(S): rows d, K = 2n + part, (Sr, -Si)
+    // carried state from initial_states (or zero): rows 64 + d of BS, K = 2n + part, (Sr, Si)
     for (int i = tid; i < CD * CN; i += CX_THREADS) {
         const int d = i / CN, n = i % CN;
         float2 v = make_float2(0.f, 0.f);
         if (p.init != nullptr) v = reinterpret_cast<const float2 *>(p.init)[((b * p.H + h) * CD + d) * CN + n];
-        st_pair(SS, d, 2 * n, v.x, -v.y);
+        *reinterpret_cast<float2 *>(BS + elem_off128(64 + d, 2 * n)) = v;
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t sCC = smem_u32(CC), sBB = smem_u32(BB), sSS = smem_u32(SS), sXC = smem_u32(XC);
-    const uint32_t id128 = idesc_tf32(128, 64);
+    const uint32_t sCC = smem_u32(CC), sBS = smem_u32(BS), sXC = smem_u32(XC);
+    const uint32_t id128 = idesc_tf32(128, 64), id128n = idesc_tf32(128, 128);
 
     // One BAR_IN phase per chunk, armed for all three tiles when the X tile is issued; the C
     // and B tiles follow later into the same phase.
@@ -192,7 +189,7 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
     auto load_cb = [&](int c) {
         for (int a = 0; a < 4; ++a) {
             tma_load_4d(CC + a * ATOM128, &tmC, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);   // rows 0..63
-            tma_load_4d(BB + a * ATOM, &tmB, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);
+            tma_load_4d(BS + a * ATOM128, &tmB, &bar[BAR_IN], 32 * a, (int)h, c * CQ, (int)b);   // rows 0..63
         }
     };
     // thread 0's record of what may still be in flight when a bounded wait gives up
@@ -264,25 +261,21 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         }
         __syncthreads();
         if (*abort_) break;
-        // C rounded in place (rows 0..63 of CC) and C' = (Im C, -Re C) below it (rows 64..127, the
-        // same swizzled position 8 KB on); conj(B) in place
+        // conj(C) in place (rows 0..63 of CC) and swap(C) below it (rows 64..127, the same
+        // swizzled position 8 KB on); B and S are used as they are
         for (int i = tid; i < (int)(SLOT / 16); i += CX_THREADS) {
             float4 *cp = reinterpret_cast<float4 *>(CC + (i >> 9) * ATOM128) + (i & 511);
             const float4 cv = *cp;
-            *cp = make_float4(tf32r(cv.x), tf32r(cv.y), tf32r(cv.z), tf32r(cv.w));
-            cp[ATOM / 16] = make_float4(tf32r(cv.y), tf32r(-cv.x), tf32r(cv.w), tf32r(-cv.z));
-            float4 *bp = reinterpret_cast<float4 *>(BB) + i;
-            const float4 bv = *bp;
-            *bp = make_float4(tf32r(bv.x), tf32r(-bv.y), tf32r(bv.z), tf32r(-bv.w));
+            *cp = make_float4(tf32r(cv.x), tf32r(-cv.y), tf32r(cv.z), tf32r(-cv.w));
+            cp[ATOM / 16] = make_float4(tf32r(cv.y), tf32r(cv.x), tf32r(cv.w), tf32r(cv.z));
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // ---- batch 1: [Re Cb ; Im Cb] and [Re Yraw ; Im Yraw]
+        // ---- batch 1: [Re Cb | Re Yraw ; Im Cb | Im Yraw] (B tile and state stacked, N = 128)
         if (tid == 0) {
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_CB, opdesc128(sCC, k), opdesc(sBB, k), id128, k > 0);
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_YR, opdesc128(sCC, k), opdesc(sSS, k), id128, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_CB, opdesc128(sCC, k), opdesc128(sBS, k), id128n, k > 0);
             umma_commit(&bar[BAR_M1]);
             m_par = par;
             m1_pending = true;
@@ -308,7 +301,7 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         tc_fence_after();
         if (*abort_) break;
         // ---- lower half: Im Cb rows into E; upper half: (w o B)^T into rows 64..127 of CC (rows n,
-        // K = 2l + part) from conj(B)
+        // K = 2l + part) from the B tile
         if (!upper) {
             float im[16];
             tmem_ld16(tmem + lane_base + TC_CB + 16 * sub, im);
@@ -321,15 +314,15 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int n0 = 2 * (sub + 4 * i);
-                const float4 cb = *reinterpret_cast<const float4 *>(BB + elem_off(l, 2 * n0));
-                const float2 v0 = cmul(wl, make_float2(cb.x, -cb.y)), v1 = cmul(wl, make_float2(cb.z, -cb.w));
+                const float4 bv = *reinterpret_cast<const float4 *>(BS + elem_off128(l, 2 * n0));
+                const float2 v0 = cmul(wl, make_float2(bv.x, bv.y)), v1 = cmul(wl, make_float2(bv.z, bv.w));
                 *reinterpret_cast<float2 *>(CC + elem_off128(64 + n0, 2 * l)) = make_float2(tf32r(v0.x), tf32r(v0.y));
                 *reinterpret_cast<float2 *>(CC + elem_off128(65 + n0, 2 * l)) = make_float2(tf32r(v1.x), tf32r(v1.y));
             }
         }
         __syncthreads();
         // ---- upper half: M = L o Cb into rows 0..63 of CC (rows l, K = 2s + part), 16 columns a
-        // thread; lower half: swap(X^T) into BB (Xi, Xr)
+        // thread; lower half: swap(X^T) into the B-tile rows of BS (Xi, Xr)
         if (upper) {
             const int l = r64;
             float re[16];
@@ -363,8 +356,8 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             for (int i = 0; i < 8; ++i) {
                 const int d0 = 2 * (sub + 4 * i);
                 const float4 v = *reinterpret_cast<const float4 *>(XT + elem_off(s, 2 * d0));
-                st_pair(BB, d0, 2 * s, tf32r(v.y), tf32r(v.x));
-                st_pair(BB, d0 + 1, 2 * s, tf32r(v.w), tf32r(v.z));
+                *reinterpret_cast<float2 *>(BS + elem_off128(d0, 2 * s)) = make_float2(tf32r(v.y), tf32r(v.x));
+                *reinterpret_cast<float2 *>(BS + elem_off128(d0 + 1, 2 * s)) = make_float2(tf32r(v.w), tf32r(v.z));
             }
         }
         fence_proxy_async_smem();
@@ -378,7 +371,7 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                 in_pending = true;
             }
             for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_Y2, opdesc128(sCC, k), opdesc(sXC, k), id128, k > 0);
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_Y2 + 64, opdesc128(sCC, k), opdesc(sBB, k), id128, k > 0);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_Y2 + 64, opdesc128(sCC, k), opdesc128(sBS, k), id128, k > 0);
             umma_commit(&bar[BAR_M2]);
             m2_pending = true;
             if (!mbar_wait_abort(&bar[BAR_M2], par, abort_)) {
@@ -437,10 +430,9 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int d = 16 * sub + j;
-                const float2 o = ld_pair(SS, d, 2 * n);   // (Sr, -Si)
-                const float nr = e.x * o.x + e.y * o.y + sr[j];
-                const float ni = e.x * (-o.y) + e.y * o.x + si[j];
-                st_pair(SS, d, 2 * n, nr, -ni);
+                float2 *sp = reinterpret_cast<float2 *>(BS + elem_off128(64 + d, 2 * n));
+                const float2 o = *sp;   // (Sr, Si)
+                *sp = make_float2(e.x * o.x - e.y * o.y + sr[j], e.x * o.y + e.y * o.x + si[j]);
             }
         }
         fence_proxy_async_smem();
@@ -459,8 +451,8 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
     } else if (p.final_ != nullptr) {
         for (int i = tid; i < CD * CN; i += CX_THREADS) {
             const int d = i / CN, n = i % CN;
-            const float2 v = ld_pair(SS, d, 2 * n);
-            reinterpret_cast<float2 *>(p.final_)[((b * p.H + h) * CD + d) * CN + n] = make_float2(v.x, -v.y);
+            reinterpret_cast<float2 *>(p.final_)[((b * p.H + h) * CD + d) * CN + n] =
+                *reinterpret_cast<const float2 *>(BS + elem_off128(64 + d, 2 * n));
         }
     }
     tc_fence_before();
