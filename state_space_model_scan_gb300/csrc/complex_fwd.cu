@@ -300,19 +300,29 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         __syncthreads();
         tc_fence_after();
         if (*abort_) break;
-        // ---- lower half: Im Cb rows into E; upper half: (w o B)^T into rows 64..127 of CC (rows n,
-        // K = 2l + part) from the B tile
-        if (!upper) {
-            float im[16];
-            tmem_ld16(tmem + lane_base + TC_CB + 16 * sub, im);
+        // ---- M = L o Cb is built by both halves, in 8-column groups g of row l: the upper half (Re Cb
+        // in its lanes) takes the even groups, the lower half (Im Cb) the odd ones, so the causal
+        // work splits evenly.  Each half passes the other the component of the other's groups
+        // through E, keeping its own; both halves share the (w o B)^T and swap(X^T) builds.
+        float own[8];
+        {
+            float v[16];
+            tmem_ld16(tmem + lane_base + TC_CB + 16 * sub, v);
             tmem_wait_ld();
+            // the upper half keeps group 2 sub and passes group 2 sub + 1; the lower half the reverse
+            float *ex = E + r64 * E_STRIDE + 16 * sub + (upper ? 8 : 0);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) E[r64 * E_STRIDE + 16 * sub + j] = im[j];
-        } else {
+            for (int j = 0; j < 8; ++j) {
+                own[j] = upper ? v[j] : v[8 + j];
+                ex[j] = upper ? v[8 + j] : v[j];
+            }
+        }
+        {   // (w o B)^T into rows 64..127 of CC (rows n, K = 2l + part) from the B tile
             const int l = r64;
             const float2 wl = wv[l];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i0 = 0; i0 < 4; ++i0) {
+                const int i = upper ? i0 : i0 + 4;
                 const int n0 = 2 * (sub + 4 * i);
                 const float4 bv = *reinterpret_cast<const float4 *>(BS + elem_off128(l, 2 * n0));
                 const float2 v0 = cmul(wl, make_float2(bv.x, bv.y)), v1 = cmul(wl, make_float2(bv.z, bv.w));
@@ -321,39 +331,39 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             }
         }
         __syncthreads();
-        // ---- upper half: M = L o Cb into rows 0..63 of CC (rows l, K = 2s + part), 16 columns a
-        // thread; lower half: swap(X^T) into the B-tile rows of BS (Xi, Xr)
-        if (upper) {
+        {   // ---- M rows l, group g, into rows 0..63 of CC (K = 2s + part)
             const int l = r64;
-            float re[16];
-            tmem_ld16(tmem + lane_base + TC_CB + 16 * sub, re);
-            tmem_wait_ld();
+            const int g = 2 * sub + (upper ? 0 : 1);
             // L[l, s] = exp(Re(cs_l - cs_s)) rot_l conj(rot_s): the phase factors have modulus one,
             // so splitting them costs no range; the magnitude stays a difference
             const float lre = cs[l].x * 1.4426950408889634f;
             const float2 rl = rot[l];
-            float out[32];
+            float out[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int s = 16 * sub + j;
+            for (int j = 0; j < 8; ++j) {
+                const int s = 8 * g + j;
+                const float other = E[l * E_STRIDE + s];
+                const float2 cb = upper ? make_float2(own[j], other) : make_float2(other, own[j]);
                 float2 m = make_float2(0.f, 0.f);
                 if (s <= l) {
                     const float2 rs = rot[s];
                     const float mag = ex2(lre - cs[s].x * 1.4426950408889634f);
                     const float2 ph = make_float2(rl.x * rs.x + rl.y * rs.y, rl.y * rs.x - rl.x * rs.y);
-                    m = cmul(make_float2(mag * ph.x, mag * ph.y), make_float2(re[j], E[l * E_STRIDE + s]));
+                    m = cmul(make_float2(mag * ph.x, mag * ph.y), cb);
                 }
                 out[2 * j] = tf32r(m.x);
                 out[2 * j + 1] = tf32r(m.y);
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<float4 *>(CC + elem_off128(l, 32 * sub + 4 * j)) =
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<float4 *>(CC + elem_off128(l, 16 * g + 4 * j)) =
                     make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-        } else {
+        }
+        {   // swap(X^T) into the B-tile rows of BS (Xi, Xr)
             const int s = r64;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i0 = 0; i0 < 4; ++i0) {
+                const int i = upper ? i0 : i0 + 4;
                 const int d0 = 2 * (sub + 4 * i);
                 const float4 v = *reinterpret_cast<const float4 *>(XT + elem_off(s, 2 * d0));
                 *reinterpret_cast<float2 *>(BS + elem_off128(d0, 2 * s)) = make_float2(tf32r(v.y), tf32r(v.x));
