@@ -66,7 +66,7 @@ constexpr uint32_t TX_BYTES = 3 * SLOT;                    // C, B and X tiles o
 // batch 2 [Ydiag ; Sloc] real parts 64, imaginary parts 64.
 constexpr uint32_t TC_CB = 0, TC_YR = 64, TC_Y2 = 128, TM_COLS = 256;
 
-enum { BAR_IN = 0, BAR_M1 = 1, BAR_M2 = 2 };
+enum { BAR_IN = 0, BAR_M1 = 1, BAR_M2 = 2, BAR_M3 = 3 };
 
 struct CxParams {
     int64_t Bt, T, H;
@@ -124,6 +124,9 @@ __device__ __forceinline__ float2 cexp(float2 a) {
 __device__ __forceinline__ float softplus_f(float v) {
     return v > 20.f ? v : log1pf(__expf(v));
 }
+// Named barrier 1 over the whole CTA: one half arrives (no wait), the other waits for it.
+__device__ __forceinline__ void halves_arrive() { asm volatile("barrier.arrive 1, %0;" ::"n"(CX_THREADS) : "memory"); }
+__device__ __forceinline__ void halves_sync() { asm volatile("barrier.sync 1, %0;" ::"n"(CX_THREADS) : "memory"); }
 __device__ __forceinline__ void st_pair(uint8_t *slot, int r, int k, float a, float b) {
     *reinterpret_cast<float2 *>(slot + elem_off(r, k)) = make_float2(a, b);
 }
@@ -157,7 +160,7 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
 
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
         *abort_ = 0;
         fence_mbar_init();
         prefetch_tmap(&tmX);
@@ -200,9 +203,8 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         load_cb(0);
         in_pending = true;
     }
-    // Warp 1 builds the per-chunk tables (one lane: two positions), the next chunk's while
-    // thread 0 issues and waits for the current chunk's second MMA batch; it reads dt one
-    // chunk ahead of that.
+    // Warp 2 builds the per-chunk tables (one lane: two positions), the next chunk's while the
+    // current chunk's second MMA batch runs; it reads dt one chunk ahead of that.
     float dtn[2] = {0.f, 0.f};
     auto fetch_dt = [&](int c) {
 #pragma unroll
@@ -211,7 +213,7 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             dtn[j] = t < p.T ? p.dt[(b * p.T + t) * p.H + h] : 0.f;
         }
     };
-    auto build_tables = [&](int c) {   // warp 1; dtn holds chunk c's dt
+    auto build_tables = [&](int c) {   // warp 2; dtn holds chunk c's dt
         const int set = c & 1;
         const int64_t t0 = (int64_t)c * CQ;
         float2 a2[2];
@@ -242,7 +244,7 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             rot_t[set * CQ + l] = make_float2(cn, sn);
         }
     };
-    if (warp == 1 && nc > 0) {
+    if (warp == 2 && nc > 0) {
         fetch_dt(0);
         build_tables(0);
     }
@@ -374,81 +376,112 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // ---- batch 2: [Re Ydiag ; Re Sloc] and [Im Ydiag ; Im Sloc]
+        // ---- batch 2: chain 1 [Re Ydiag ; Re Sloc] (B = conj(X^T)) and chain 2 [Im Ydiag ; Im Sloc]
+        // (B = swap(X^T)), committed separately, so the upper half writes the real outputs while
+        // chain 2 runs; the lower half (the state update) waits for both.
         if (tid == 0) {
             if (c + 1 < nc) {   // the X tile of the next chunk into its freed slot
                 load_x(c + 1);
                 in_pending = true;
             }
             for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_Y2, opdesc128(sCC, k), opdesc(sXC, k), id128, k > 0);
-            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_Y2 + 64, opdesc128(sCC, k), opdesc128(sBS, k), id128, k > 0);
             umma_commit(&bar[BAR_M2]);
+            for (int k = 0; k < 16; ++k) umma_tf32(tmem + TC_Y2 + 64, opdesc128(sCC, k), opdesc128(sBS, k), id128, k > 0);
+            umma_commit(&bar[BAR_M3]);
+            m_par = par;
             m2_pending = true;
-            if (!mbar_wait_abort(&bar[BAR_M2], par, abort_)) {
-                set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
-            } else {
-                m2_pending = false;
-                if (c + 1 < nc) load_cb(c + 1);   // C and B slots are free again: overlaps the epilogue
+        }
+        // Every thread of a half waits on the chain barrier itself; the outcome is made uniform per
+        // warp before any warp-collective TMEM access.
+        if (!upper) {
+            {   // Im Yraw to the upper half
+                float yi[16];
+                tmem_ld16(tmem + lane_base + TC_YR + 16 * sub, yi);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) E[r64 * E_STRIDE + 16 * sub + j] = yi[j];
             }
-        }
-        if (!upper) {   // meanwhile the lower half passes Im Yraw to the upper half
-            float yi[16];
-            tmem_ld16(tmem + lane_base + TC_YR + 16 * sub, yi);
-            tmem_wait_ld();
+            __syncwarp();
+            halves_arrive();
+            if (warp == 2 && c + 1 < nc) build_tables(c + 1);   // the next chunk's tables meanwhile
+            bool ok = mbar_wait_abort(&bar[BAR_M3], par, abort_);
+            if (!ok) set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+            if (ok) {
+                // C and B slots are free again: the next chunk's tiles overlap the state update
+                if (tid == 64 && c + 1 < nc) load_cb(c + 1);
+                __syncwarp();
+                // ---- state of rows n: S <- exp(cs_63) S + Sloc (columns d); each (d, n) has one owner
+                const int n = r64;
+                float sr[16], si[16];
+                tmem_ld16(tmem + lane_base + TC_Y2 + 16 * sub, sr);
+                tmem_ld16(tmem + lane_base + TC_Y2 + 64 + 16 * sub, si);
+                tmem_wait_ld();
+                const float2 e = ecs[CQ - 1];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) E[r64 * E_STRIDE + 16 * sub + j] = yi[j];
-        }
-        if (warp == 1 && c + 1 < nc) build_tables(c + 1);   // ... and warp 1 the next tables
-        __syncthreads();
-        tc_fence_after();
-        if (*abort_) break;
-        if (upper) {   // ---- outputs of rows l: y = Ydiag + exp(cs_l) Yraw
+                for (int j = 0; j < 16; ++j) {
+                    const int d = 16 * sub + j;
+                    float2 *sp = reinterpret_cast<float2 *>(BS + elem_off128(64 + d, 2 * n));
+                    const float2 o = *sp;   // (Sr, Si)
+                    *sp = make_float2(e.x * o.x - e.y * o.y + sr[j], e.x * o.y + e.y * o.x + si[j]);
+                }
+            }
+        } else {
+            __syncwarp();
+            halves_sync();   // E holds Im Yraw
+            bool ok = mbar_wait_abort(&bar[BAR_M2], par, abort_);
+            if (!ok) set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
             const int l = r64;
-            float yr[16], dr[16], di[16];
-            tmem_ld16(tmem + lane_base + TC_YR + 16 * sub, yr);
-            tmem_ld16(tmem + lane_base + TC_Y2 + 16 * sub, dr);
-            tmem_ld16(tmem + lane_base + TC_Y2 + 64 + 16 * sub, di);
-            tmem_wait_ld();
             const int64_t t = t0 + l;
-            if (t < p.T) {
-                const float2 e = ecs[l];
-                const float *yi = E + l * E_STRIDE + 16 * sub;
-                const int64_t off = ((b * p.T + t) * p.H + h) * CD + 16 * sub;
-                float o[16];
+            const float2 e = ecs[l];
+            const float *yi = E + l * E_STRIDE + 16 * sub;
+            const int64_t off = ((b * p.T + t) * p.H + h) * CD + 16 * sub;
+            float yr[16];
+            if (ok) {   // ---- outputs of rows l: y = Ydiag + exp(cs_l) Yraw
+                float dr[16];
+                tmem_ld16(tmem + lane_base + TC_YR + 16 * sub, yr);
+                tmem_ld16(tmem + lane_base + TC_Y2 + 16 * sub, dr);
+                tmem_wait_ld();
+                if (t < p.T) {
+                    float o[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) o[j] = dr[j] + e.x * yr[j] - e.y * yi[j];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    reinterpret_cast<float4 *>(p.y_re + off)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2],
-                                                                              o[4 * j + 3]);
-                if (p.y_im != nullptr) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) o[j] = di[j] + e.x * yi[j] + e.y * yr[j];
+                    for (int j = 0; j < 16; ++j) o[j] = dr[j] + e.x * yr[j] - e.y * yi[j];
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        reinterpret_cast<float4 *>(p.y_im + off)[j] =
+                        reinterpret_cast<float4 *>(p.y_re + off)[j] =
                             make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
                 }
             }
-        } else {   // ---- state of rows n: S <- exp(cs_63) S + Sloc (columns d); each (d, n) has one owner
-            const int n = r64;
-            float sr[16], si[16];
-            tmem_ld16(tmem + lane_base + TC_Y2 + 16 * sub, sr);
-            tmem_ld16(tmem + lane_base + TC_Y2 + 64 + 16 * sub, si);
-            tmem_wait_ld();
-            const float2 e = ecs[CQ - 1];
+            if (ok && p.y_im != nullptr) {
+                ok = mbar_wait_abort(&bar[BAR_M3], par, abort_);
+                if (!ok) set_status(p.hdr, SSD_ERR_DEVICE_TIMEOUT);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+                if (ok) {
+                    float di[16];
+                    tmem_ld16(tmem + lane_base + TC_Y2 + 64 + 16 * sub, di);
+                    tmem_wait_ld();
+                    if (t < p.T) {
+                        float o[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int d = 16 * sub + j;
-                float2 *sp = reinterpret_cast<float2 *>(BS + elem_off128(64 + d, 2 * n));
-                const float2 o = *sp;   // (Sr, Si)
-                *sp = make_float2(e.x * o.x - e.y * o.y + sr[j], e.x * o.y + e.y * o.x + si[j]);
+                        for (int j = 0; j < 16; ++j) o[j] = di[j] + e.x * yi[j] + e.y * yr[j];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            reinterpret_cast<float4 *>(p.y_im + off)[j] =
+                                make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                    }
+                }
             }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        if (*abort_) break;
+        if (tid == 0) m2_pending = false;   // both chains were waited for
     }
     if (*abort_) {
         // let copies and MMAs still in flight finish (bounded) before shared memory and
@@ -456,7 +489,10 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         if (tid == 0) {
             if (in_pending) mbar_wait(&bar[BAR_IN], in_par);
             if (m1_pending) mbar_wait(&bar[BAR_M1], m_par);
-            if (m2_pending) mbar_wait(&bar[BAR_M2], m_par);
+            if (m2_pending) {
+                mbar_wait(&bar[BAR_M2], m_par);
+                mbar_wait(&bar[BAR_M3], m_par);
+            }
         }
     } else if (p.final_ != nullptr) {
         for (int i = tid; i < CD * CN; i += CX_THREADS) {
