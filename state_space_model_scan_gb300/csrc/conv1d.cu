@@ -147,6 +147,15 @@ __device__ __forceinline__ void lds8(const T *p, float *v) { ld8(p, v); }
 // logistic function with the fast exponential and divide (relative error ~1e-6; 1/inf = 0
 // gives the right limit for very negative arguments)
 __device__ __forceinline__ float sig_fast(float v) { return __fdividef(1.f, 1.f + __expf(-v)); }
+// the same through one tanh.approx (relative error ~2^-11): (1 + tanh(v/2)) / 2, for bf16 data,
+// whose own rounding is 2^-9
+__device__ __forceinline__ float sig_tanh(float v) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * v));
+    return fmaf(0.5f, t, 0.5f);
+}
+template <typename T>
+__device__ __forceinline__ float sig_t(float v) { return sizeof(T) == 2 ? sig_tanh(v) : sig_fast(v); }
 
 // The block's taps and biases, staged once in shared memory as [k][channel] (then [K][c] =
 // the bias): weight [Cn][K] holds channels cbase .. cbase+255 as 256K contiguous floats, read
@@ -213,7 +222,7 @@ k_conv_fwd(const ConvArgs a) {
         }
         if (a.silu) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] *= sig_fast(acc[e]);
+            for (int e = 0; e < 8; ++e) acc[e] *= sig_t<T>(acc[e]);
         }
         st8(o + t * a.so_l, acc);
     }
@@ -288,7 +297,7 @@ k_conv_bwd(const ConvArgs a) {
 #pragma unroll
                 for (int k = 0; k < K; ++k) pre = fmaf(w[k][e], ring[k][e], pre);
                 if (a.silu) {
-                    const float sg = sig_fast(pre);
+                    const float sg = sig_t<T>(pre);
                     g[e] = dv[e] * sg * (1.f + pre * (1.f - sg));
                 } else {
                     g[e] = dv[e];
