@@ -78,8 +78,14 @@ __device__ __forceinline__ uint64_t kmaj(uint32_t base, int k, uint32_t col_byte
 __device__ __forceinline__ uint64_t mnmaj(uint32_t base, int k, uint32_t mn_atom) {
     return sdesc(base + (uint32_t)k * 2048u, mn_atom, 1024u);
 }
-__device__ __forceinline__ float silu_f(float z) { return z * rcp(1.f + ex2(-z * LOG2E)); }
-__device__ __forceinline__ float sig_f(float z) { return rcp(1.f + ex2(-z * LOG2E)); }
+// logistic (1 + tanh(z/2)) / 2 through one tanh.approx (relative error ~2^-11, below the bf16
+// rounding of the data it gates)
+__device__ __forceinline__ float sig_f(float z) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+    return fmaf(0.5f, t, 0.5f);
+}
+__device__ __forceinline__ float silu_f(float z) { return z * sig_f(z); }
 
 // 32 floats as bf16 to 64 contiguous bytes of global memory: two 256-bit stores when the
 // address is 32-byte aligned (`st32`, checked on the host for base and strides), else four

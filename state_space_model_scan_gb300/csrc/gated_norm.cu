@@ -52,6 +52,17 @@ __device__ __forceinline__ void store8(float *p, const float *v) {
 // logistic function with the fast exponential and divide (relative error ~1e-6, far inside the
 // fp32 tolerance; 1/inf = 0 gives the right limit for very negative arguments)
 __device__ __forceinline__ float sig(float v) { return __fdividef(1.f, 1.f + __expf(-v)); }
+// for bf16 data, whose own rounding is 2^-9: (1 + tanh(v/2)) / 2 through one tanh.approx
+// (relative error ~2^-11) instead of an exponential and a reciprocal
+template <typename T>
+__device__ __forceinline__ float sig_t(float v) {
+    if (sizeof(T) == 2) {
+        float t;
+        asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * v));
+        return fmaf(0.5f, t, 0.5f);
+    }
+    return sig(v);
+}
 
 struct NormArgs {
     int64_t rows, width, G;   // G = features per group
@@ -86,7 +97,7 @@ k_norm_fwd(const NormArgs a) {
                 float zz[8];
                 load8(zr + 8 * j, zz);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig(zz[e]);
+                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig_t<T>(zz[e]);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
@@ -103,7 +114,7 @@ k_norm_fwd(const NormArgs a) {
                 float zz[8];
                 load8(zr + 8 * j, zz);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig(zz[e]);
+                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig_t<T>(zz[e]);
             }
             load8(wr + 8 * j, wv);
 #pragma unroll
@@ -140,7 +151,7 @@ k_norm_bwd(const NormArgs a) {
                 float zz[8];
                 load8(zr + 8 * j, zz);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig(zz[e]);
+                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig_t<T>(zz[e]);
             }
             load8(dr + 8 * j, d);
             load8(wr + 8 * j, wv);
@@ -157,7 +168,7 @@ k_norm_bwd(const NormArgs a) {
                 load8(zr + 8 * j, z8);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    sg[e] = sig(z8[e]);
+                    sg[e] = sig_t<T>(z8[e]);
                     s[e] = z8[e] * sg[e];
                 }
             } else {
@@ -217,7 +228,7 @@ k_norm_fwd_reg(const NormArgs a) {
             if (lane + 32 * k < pieces) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    if (zr) v[k][e] *= zz[k][e] * sig(zz[k][e]);
+                    if (zr) v[k][e] *= zz[k][e] * sig_t<T>(zz[k][e]);
                     ss = fmaf(v[k][e], v[k][e], ss);
                 }
             }
@@ -279,7 +290,7 @@ k_norm_bwd_reg(const NormArgs a) {
             if (lane + 32 * k < pieces) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float sgate = zr ? z8[k][e] * sig(z8[k][e]) : 1.f;
+                    const float sgate = zr ? z8[k][e] * sig_t<T>(z8[k][e]) : 1.f;
                     dot = fmaf(d[k][e] * wv[k][e], y8[k][e] * sgate * rs, dot);
                 }
             }
@@ -294,7 +305,7 @@ k_norm_bwd_reg(const NormArgs a) {
                 float o1[8], o2[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float sg = zr ? sig(z8[k][e]) : 0.f;
+                    const float sg = zr ? sig_t<T>(z8[k][e]) : 0.f;
                     const float sgate = zr ? z8[k][e] * sg : 1.f;
                     const float vhat = y8[k][e] * sgate * rs;
                     const float dv = rs * (d[k][e] * wv[k][e] - vhat * dot);
@@ -398,7 +409,7 @@ k_norm_bwd_staged(const NormArgs a) {
                 if (lane + 32 * k < pieces) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float sgate = zs ? z8[k][e] * sig(z8[k][e]) : 1.f;
+                        const float sgate = zs ? z8[k][e] * sig_t<T>(z8[k][e]) : 1.f;
                         dot = fmaf(d[k][e] * wv[k][e], y8[k][e] * sgate * rs, dot);
                     }
                 }
@@ -413,7 +424,7 @@ k_norm_bwd_staged(const NormArgs a) {
                     float o1[8], o2[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float sg = zs ? sig(z8[k][e]) : 0.f;
+                        const float sg = zs ? sig_t<T>(z8[k][e]) : 0.f;
                         const float sgate = zs ? z8[k][e] * sg : 1.f;
                         const float vhat = y8[k][e] * sgate * rs;
                         const float dv = rs * (d[k][e] * wv[k][e] - vhat * dot);
