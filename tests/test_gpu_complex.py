@@ -104,3 +104,74 @@ def test_complex_deterministic():
     r2 = run(inp)
     for a, b in zip(r1, r2):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("T", [63, 65, 127, 129])
+def test_complex_chunk_boundaries(T):
+    """One token short of / past a chunk edge (the last chunk's rows past T are never stored)."""
+    inp = I.complex_inputs(1, T, 2, seed=T)
+    y_re, y_im, fin = run(inp)
+    y, f = oracle(inp)
+    assert rel(y_re.double().numpy(), y.real) <= TOL
+    assert rel(y_im.double().numpy(), y.imag) <= TOL
+    assert rel(npc(fin), f) <= TOL
+
+
+@pytest.mark.parametrize("want_final", [True, False])
+def test_complex_real_output_only(want_final):
+    """Re y alone (the second MMA chain is then waited for by the state update only), with and
+    without the final state."""
+    inp = I.complex_inputs(2, 200, 2, seed=21)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    out = complex_ssd_forward(d["x"], d["A"], d["B"], d["C"], d["dt"], initial_states=d["initial_states"],
+                              return_imag=False, return_final=want_final)
+    torch.cuda.synchronize()
+    y_re = out[0] if isinstance(out, (tuple, list)) else out
+    y, f = oracle(inp)
+    assert rel(y_re.cpu().double().numpy(), y.real) <= TOL
+    if want_final:
+        assert rel(npc(out[-1].cpu()), f) <= TOL
+
+
+@pytest.mark.parametrize("regime", ["strong_decay", "weak_decay", "fast_rotation", "softplus_switch", "far_negative"])
+def test_complex_decay_regimes(regime):
+    """Decay and timestep regimes: Re A = -16 with dt near 3 (abar ~ e^-48 per step: every
+    chunk forgets its past), Re A = -1e-4 (the state keeps everything), |Im A| = 3 pi (the
+    phase turns by more than a half-turn per step), raw dt straddling softplus's switch at 20
+    and raw dt near -30 (dt underflows towards 0)."""
+    H, T = 3, 200
+    inp = I.complex_inputs(1, T, H, seed=31)
+    g = torch.Generator().manual_seed(77)
+    A = inp["A"]
+    dt = inp["dt"]
+    if regime == "strong_decay":
+        A = torch.complex(torch.full((H,), -16.0), A.imag)
+        dt = 3.0 + 0.1 * torch.randn(1, T, H, generator=g)
+    elif regime == "weak_decay":
+        A = torch.complex(torch.full((H,), -1e-4), A.imag)
+    elif regime == "fast_rotation":
+        A = torch.complex(A.real, torch.tensor([3 * np.pi, -3 * np.pi, 2.5 * np.pi]))
+    elif regime == "softplus_switch":
+        vals = torch.tensor([19.9, 20.0, 20.1, 40.0])
+        dt = vals[torch.randint(0, 4, (1, T, H), generator=g)]
+        A = torch.complex(torch.full((H,), -0.05), A.imag)
+    else:
+        dt = -30.0 + torch.randn(1, T, H, generator=g)
+    inp["A"] = A.to(torch.complex64)
+    inp["dt"] = dt.to(torch.float32)
+    y_re, y_im, fin = run(inp)
+    y, f = oracle(inp)
+    assert np.isfinite(y_re.numpy()).all() and np.isfinite(y_im.numpy()).all()
+    assert rel(y_re.double().numpy(), y.real) <= TOL
+    assert rel(y_im.double().numpy(), y.imag) <= TOL
+    assert rel(npc(fin), f) <= TOL
+
+
+def test_complex_more_rows_than_sms():
+    """3 x 70 (batch row, head) pairs: more CTAs than SMs, each still one walk."""
+    inp = I.complex_inputs(3, 70, 70, seed=41)
+    y_re, y_im, fin = run(inp)
+    y, f = oracle(inp)
+    assert rel(y_re.double().numpy(), y.real) <= TOL
+    assert rel(y_im.double().numpy(), y.imag) <= TOL
+    assert rel(npc(fin), f) <= TOL
