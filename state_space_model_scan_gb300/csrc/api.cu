@@ -83,7 +83,7 @@ using namespace ssd;
 
 namespace {
 
-constexpr int kSimtQ = 64;
+constexpr int kSimtQmin = 32, kSimtQmax = 256, kSimtQbwd = 64;   // SIMT chunk lengths (powers of two)
 constexpr int kTcQ = 128;
 constexpr size_t kAlign = 256;
 
@@ -255,18 +255,21 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         }
     }
     // The chunk length is the caller's, never replaced: the tensor-core path computes
-    // 128-token chunks (one M = 128 tcgen05 tile per chunk), the SIMT path 64-token chunks.
+    // 128-token chunks (one M = 128 tcgen05 tile per chunk); the SIMT path computes chunks of
+    // 32, 64, 128 or 256 tokens in the forward and of 32 or 64 in the backward (whose per-chunk
+    // tiles, Q x Q and Q x (P, N), live in shared memory).
+    const bool simt_q = p->chunk_size >= kSimtQmin && p->chunk_size <= (bwd ? kSimtQbwd : kSimtQmax);
     bool fused = false;   // the tensor-core path (single-pass or split forward)
     if (p->algo == SSD_ALGO_FUSED || p->algo == SSD_ALGO_SPLIT) {
         if (!tc_ok || p->chunk_size != kTcQ) return SSD_ERR_UNSUPPORTED;
         if (!aligned) return SSD_ERR_MISALIGNED;
         fused = true;
     } else if (p->algo == SSD_ALGO_STAGED) {
-        if (p->chunk_size != kSimtQ) return SSD_ERR_UNSUPPORTED;
+        if (!simt_q) return SSD_ERR_UNSUPPORTED;
     } else if (p->chunk_size == kTcQ && tc_ok) {
         if (!aligned) return SSD_ERR_MISALIGNED;
         fused = true;
-    } else if (p->chunk_size != kSimtQ) {
+    } else if (!simt_q) {
         return SSD_ERR_UNSUPPORTED;
     }
     // AUTO takes the single-pass forward on the tensor-core path (measured faster than the
@@ -277,7 +280,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         if (!fused) return SSD_ERR_UNSUPPORTED;
         if (((uintptr_t)a->chunk_states) % 16 != 0) return SSD_ERR_MISALIGNED;
     }
-    const int Q = fused ? kTcQ : kSimtQ;
+    const int Q = fused ? kTcQ : (int)p->chunk_size;
     // dstate the kernels compute: the tensor-core tiles are N = 128; dstate 64 runs as the zero-
     // extended half (TMA fills the B/C columns past 64 with zeros; states are padded copies)
     const int64_t Nk = fused ? 128 : N;

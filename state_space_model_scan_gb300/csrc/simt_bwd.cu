@@ -24,24 +24,24 @@
 //       ddt_raw = ddt * sigmoid(dt_raw + dt_bias);  dz = dy ypre silu'(z)
 //   reductions       : dB/dC over the heads of a group, dA/dD/ddt_bias over chunks, in a
 //                      fixed order (bitwise reproducible; no atomics).
-// SIMT internal chunk length is 64: one chunk row per 4 threads.
+// Chunk lengths QS = 32 or 64 (a template argument): one chunk row per 256 / QS threads.
 #include "common.cuh"
 
 namespace ssd {
 
 namespace {
 
-constexpr int QS = 64;   // SIMT chunk length
-
-__device__ __forceinline__ float sum4(float v) {
-    v += __shfl_xor_sync(0xffffffffu, v, 1);
-    v += __shfl_xor_sync(0xffffffffu, v, 2);
+// sum over the NP consecutive lanes that share a chunk row (fixed order)
+template <int NP>
+__device__ __forceinline__ float sum_parts(float v) {
+#pragma unroll
+    for (int o = 1; o < NP; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
 
 // ------------------------------------------------------------------ bwd_dstates
 // grid (kmax, H), block 256; mapping as the forward chunk_state kernel.
-template <typename T>
+template <typename T, int QS>
 __global__ void __launch_bounds__(256)
 k_bwd_dstates(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restrict__ chunks,
               View3 dy, View3 z, View3 Cm, const float *__restrict__ csw, float *__restrict__ dstates) {
@@ -96,8 +96,8 @@ k_bwd_dstates(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__rest
 }
 
 // ------------------------------------------------------------------ bwd_chunk
-// grid (kmax, H), block 256 = 64 rows x 4 threads.  Dynamic shared memory.
-template <typename T>
+// grid (kmax, H), block 256 = QS rows x NP threads.  Dynamic shared memory.
+template <typename T, int QS>
 __global__ void __launch_bounds__(256)
 k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restrict__ chunks,
             View3 x, View3 Bm, View3 Cm, View3 z, View3 dy, const float *__restrict__ dt_raw, int64_t sdb,
@@ -105,6 +105,8 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
             const float *__restrict__ dtw, const float *__restrict__ csw, const float *__restrict__ states,
             const float *__restrict__ dstates, MView3 dx, MView3 dz, float *__restrict__ ddt, int64_t sddb,
             int64_t sddl, float *__restrict__ dBh, float *__restrict__ dCh, float *__restrict__ partials) {
+    constexpr int NP = 256 / QS;   // threads per chunk row
+    constexpr int NQ = QS / 32;    // 32-position blocks of the per-position scalars
     extern __shared__ float sm[];
     const int k = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     if (k >= hdr[HDR_NCHUNKS] || hdr[HDR_STATUS] != 0) return;
@@ -169,7 +171,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     }
     __syncthreads();
 
-    const int r = tid >> 2, part = tid & 3;     // row r, quarter `part`
+    const int r = tid / NP, part = tid % NP;     // row r, part `part` of its columns
     const float *dso = dstates + ((int64_t)k * sh.H + h) * P * N;
     const float *sin = states + ((int64_t)k * sh.H + h) * P * N;
     const float Dh = D ? D[h] : 0.f;
@@ -178,7 +180,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     // dx[r][p] and x.u row sums
     {
         float xu = 0.f;
-        for (int p = part; p < P; p += 4) {
+        for (int p = part; p < P; p += NP) {
             float a = 0.f;
             for (int l = r; l < QS; ++l) a += Mm[l * Q1 + r] * dys[l * P1 + p];
             float u = 0.f;
@@ -190,13 +192,13 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
                 o[p] = from_f<T>(a + wst[r] * u + Dh * dys[r * P1 + p]);
             }
         }
-        xu = sum4(xu);
+        xu = sum_parts<NP>(xu);
         if (part == 0) rowXU[r] = xu;
     }
     // dB (this head) [r][n]
     {
         float *o = dBh + (((int64_t)k * sh.H + h) * QS + r) * N;
-        for (int n = part; n < N; n += 4) {
+        for (int n = part; n < N; n += NP) {
             float a = 0.f;
             for (int l = r; l < QS; ++l) a += Em[l * Q1 + r] * Cs[l * N1 + n];
             float b = 0.f;
@@ -208,7 +210,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     {
         float *o = dCh + (((int64_t)k * sh.H + h) * QS + r) * N;
         const float er = expf(cs[r]);
-        for (int n = part; n < N; n += 4) {
+        for (int n = part; n < N; n += NP) {
             float a = 0.f;
             for (int s = 0; s <= r; ++s) a += Em[r * Q1 + s] * Bs[s * N1 + n];
             float b = 0.f;
@@ -220,7 +222,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     {
         const float er = expf(cs[r]);
         float t2 = 0.f, dd = 0.f;
-        for (int p = part; p < P; p += 4) {
+        for (int p = part; p < P; p += NP) {
             float yd = 0.f;
             for (int s = 0; s <= r; ++s) yd += Mm[r * Q1 + s] * xs[s * P1 + p];
             float yb = 0.f;
@@ -238,8 +240,8 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
                 o[p] = from_f<T>(dyv * ypre * sg * (1.f + zz * (1.f - sg)));
             }
         }
-        t2 = sum4(t2);
-        dd = sum4(dd);
+        t2 = sum_parts<NP>(t2);
+        dd = sum_parts<NP>(dd);
         if (part == 0) { rowT2[r] = t2; rowD[r] = dd; }
     }
     __syncthreads();
@@ -251,12 +253,13 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     if ((tid & 31) == 0) red[tid >> 5] = t3p;
     __syncthreads();
     if (tid < 32) {
-        // per-position scalars: thread i handles positions i and i + 32
+        // per-position scalars: thread i handles positions i + 32 q (q < NQ)
         float T3 = 0.f;
         for (int w = 0; w < 8; ++w) T3 += red[w];
         T3 *= expf(clast);
-        float dcs[2], t4[2], ddir[2];
-        for (int q = 0; q < 2; ++q) {
+        float dcs[NQ], t4[NQ], ddir[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
             const int i = tid + 32 * q;
             float rowT1 = 0.f, colTm = 0.f;
             for (int s = 0; s < i; ++s) rowT1 += dt[s] * Tm[i * Q1 + s];
@@ -265,30 +268,44 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
             ddir[q] = colTm + Tm[i * Q1 + i] + expf(clast - cs[i]) * rowXU[i];
             dcs[q] = rowT1 - dt[i] * colTm + rowT2[i];
         }
-        // sum_{i >= u} dcs[i]: reverse inclusive scans within each half of the 64 positions
-        float hs = dcs[1], ls = dcs[0];
+        // sum_{i >= u} dcs[i]: reverse inclusive scans within each block of 32 positions;
+        // sum_{s < u} T4[s]: exclusive forward scans within each block; then the other
+        // blocks' totals
+        float rs[NQ], ps[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) { rs[q] = dcs[q]; ps[q] = t4[q]; }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            float th = __shfl_down_sync(0xffffffffu, hs, o);
-            float tl = __shfl_down_sync(0xffffffffu, ls, o);
-            if (tid + o < 32) { hs += th; ls += tl; }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float t = __shfl_down_sync(0xffffffffu, rs[q], o);
+                if (tid + o < 32) rs[q] += t;
+            }
         }
-        const float hi_total = __shfl_sync(0xffffffffu, hs, 0);
-        // sum_{s < u} T4[s]: exclusive forward scans within each half
-        float p0 = t4[0], p1 = t4[1];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            float t0 = __shfl_up_sync(0xffffffffu, p0, o);
-            float t1 = __shfl_up_sync(0xffffffffu, p1, o);
-            if (tid >= o) { p0 += t0; p1 += t1; }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float t = __shfl_up_sync(0xffffffffu, ps[q], o);
+                if (tid >= o) ps[q] += t;
+            }
         }
-        const float lo_total = __shfl_sync(0xffffffffu, p0, 31);
-        float e0 = __shfl_up_sync(0xffffffffu, p0, 1), e1 = __shfl_up_sync(0xffffffffu, p1, 1);
-        if (tid == 0) { e0 = 0.f; e1 = 0.f; }
-        const float da[2] = {ls + hi_total + T3 + e0, hs + T3 + lo_total + e1};
+        float da[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            float later = 0.f, earlier = 0.f;   // later blocks' dcs totals, earlier blocks' T4 totals
+#pragma unroll
+            for (int q2 = q + 1; q2 < NQ; ++q2) later += __shfl_sync(0xffffffffu, rs[q2], 0);
+#pragma unroll
+            for (int q2 = 0; q2 < q; ++q2) earlier += __shfl_sync(0xffffffffu, ps[q2], 31);
+            float ex = __shfl_up_sync(0xffffffffu, ps[q], 1);
+            if (tid == 0) ex = 0.f;
+            da[q] = rs[q] + later + T3 + earlier + ex;
+        }
         const float Ah = A[h];
         float pa = 0.f, pb = 0.f;
-        for (int q = 0; q < 2; ++q) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
             const int i = tid + 32 * q;
             if (i >= ci.lo && i < ci.len) {
                 const float v = dt_raw[(int64_t)ci.b * sdb + (int64_t)(ci.t0 + i) * sdl + h] + (bias ? bias[h] : 0.f);
@@ -300,7 +317,9 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
         }
         pa = warp_sum(pa);
         pb = warp_sum(pb);
-        float pd = rowD[tid] + rowD[tid + 32];
+        float pd = 0.f;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) pd += rowD[tid + 32 * q];
         pd = warp_sum(pd);
         if (tid == 0) {
             float *pp = partials + ((int64_t)k * sh.H + h) * 4;
@@ -362,14 +381,19 @@ __global__ void k_reduce_heads(Shape sh, const int32_t *__restrict__ hdr, const 
 }  // namespace
 
 size_t bwd_chunk_smem(const Shape &sh) {
-    const int P1 = sh.P + 1, N1 = sh.N + 1, Q1 = QS + 1;
+    const int QS = sh.Q, P1 = sh.P + 1, N1 = sh.N + 1, Q1 = QS + 1;
     return sizeof(float) * (size_t)(11 * QS + 2 * QS * P1 + 2 * QS * N1 + 3 * QS * Q1);
 }
 
 template <typename T>
 cudaError_t launch_bwd_dstates(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 dy, View3 z,
                                View3 Cm, const float *csw, float *dstates, cudaStream_t st) {
-    k_bwd_dstates<T><<<dim3(sh.kmax, sh.H), 256, 0, st>>>(sh, hdr, chunks, dy, z, Cm, csw, dstates);
+    if (sh.Q == 32)
+        k_bwd_dstates<T, 32><<<dim3(sh.kmax, sh.H), 256, 0, st>>>(sh, hdr, chunks, dy, z, Cm, csw, dstates);
+    else if (sh.Q == 64)
+        k_bwd_dstates<T, 64><<<dim3(sh.kmax, sh.H), 256, 0, st>>>(sh, hdr, chunks, dy, z, Cm, csw, dstates);
+    else
+        return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 
@@ -380,12 +404,23 @@ cudaError_t launch_bwd_chunk(const Shape &sh, const int32_t *hdr, const ChunkInf
                              const float *states, const float *dstates, MView3 dx, MView3 dz, float *ddt,
                              int64_t sddb, int64_t sddl, float *dBh, float *dCh, float *partials, cudaStream_t st) {
     const size_t smem = bwd_chunk_smem(sh);
-    static int attr_done[64] = {0};
-    cudaError_t e = ensure_smem_attr(k_bwd_chunk<T>, (int)smem, attr_done);
-    if (e != cudaSuccess) return e;
-    k_bwd_chunk<T><<<dim3(sh.kmax, sh.H), 256, smem, st>>>(sh, hdr, chunks, x, Bm, Cm, z, dy, dt_raw, sdb, sdl, A, D,
-                                                           bias, dtw, csw, states, dstates, dx, dz, ddt, sddb, sddl,
-                                                           dBh, dCh, partials);
+    if (sh.Q == 32) {
+        static int attr_done[64] = {0};
+        cudaError_t e = ensure_smem_attr(k_bwd_chunk<T, 32>, (int)smem, attr_done);
+        if (e != cudaSuccess) return e;
+        k_bwd_chunk<T, 32><<<dim3(sh.kmax, sh.H), 256, smem, st>>>(sh, hdr, chunks, x, Bm, Cm, z, dy, dt_raw, sdb, sdl,
+                                                                   A, D, bias, dtw, csw, states, dstates, dx, dz, ddt,
+                                                                   sddb, sddl, dBh, dCh, partials);
+    } else if (sh.Q == 64) {
+        static int attr_done[64] = {0};
+        cudaError_t e = ensure_smem_attr(k_bwd_chunk<T, 64>, (int)smem, attr_done);
+        if (e != cudaSuccess) return e;
+        k_bwd_chunk<T, 64><<<dim3(sh.kmax, sh.H), 256, smem, st>>>(sh, hdr, chunks, x, Bm, Cm, z, dy, dt_raw, sdb, sdl,
+                                                                   A, D, bias, dtw, csw, states, dstates, dx, dz, ddt,
+                                                                   sddb, sddl, dBh, dCh, partials);
+    } else {
+        return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

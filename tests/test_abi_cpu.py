@@ -116,25 +116,28 @@ def test_validation_codes(lib, mutate, code):
 
 
 @pytest.mark.parametrize("P,N,bf16,Q,algo,aligned,code,qi", [
-    (16, 16, True, 64, "auto", True, 0, 64),        # SIMT computes 64-token chunks
-    (16, 16, True, 128, "auto", True, 2, None),     # ... and nothing else
-    (16, 16, False, 32, "auto", True, 2, None),
+    (16, 16, True, 64, "auto", True, 0, 64),        # SIMT computes 32-, 64-, 128- and 256-token chunks
+    (16, 16, True, 32, "auto", True, 0, 32),
+    (16, 16, True, 128, "auto", True, 0, 128),
+    (16, 16, False, 256, "auto", True, 0, 256),
+    (16, 16, True, 16, "auto", True, 2, None),      # ... and nothing shorter
     (64, 128, True, 128, "auto", True, 0, 128),     # tensor-core tile set: 128-token chunks
     (64, 128, True, 64, "auto", True, 0, 64),       # same shape at 64: the SIMT path, honoured
-    (64, 128, True, 256, "auto", True, 2, None),    # not computed by either path: no silent re-chunking
+    (64, 128, True, 256, "auto", True, 0, 256),     # ... and at 256: SIMT, never re-chunked
     (64, 128, True, 128, "fused", True, 0, 128),
-    (64, 128, True, 64, "fused", True, 2, None),
-    (64, 128, True, 128, "staged", True, 2, None),
+    (64, 128, True, 64, "fused", True, 2, None),    # the tensor-core path computes 128 only
+    (64, 128, True, 256, "split", True, 2, None),
+    (64, 128, True, 128, "staged", True, 0, 128),   # an explicit SIMT run at 128
     (64, 128, True, 128, "auto", False, 3, None),   # tensor-core chunk length, strides break the TMA rule
-    (64, 128, False, 128, "auto", True, 2, None),   # fp32 inputs run SIMT only
+    (64, 128, False, 128, "auto", True, 0, 128),    # fp32 inputs run SIMT (here at 128)
     (64, 64, True, 128, "auto", True, 0, 128),      # dstate 64: the tensor-core tiles' zero-extended half
     (64, 64, True, 128, "split", True, 0, 128),
-    (64, 32, True, 128, "auto", True, 2, None),     # other dstates: SIMT only (64-token chunks)
+    (64, 32, True, 128, "auto", True, 0, 128),      # other dstates: SIMT
     (64, 32, True, 64, "auto", True, 0, 64),
 ])
 def test_chunk_size_is_honoured(lib, P, N, bf16, Q, algo, aligned, code, qi):
-    """Each chunk_size outcome: the path that computes exactly that chunk length, or
-    SSD_ERR_UNSUPPORTED / SSD_ERR_MISALIGNED; the debug layout reports the chunk used."""
+    """Each chunk_size outcome of the forward: the path that computes exactly that chunk
+    length, or SSD_ERR_UNSUPPORTED / SSD_ERR_MISALIGNED; the debug layout reports the chunk used."""
     m = lib_mod()
     p, a = good_case(P=P, N=N, bf16=bf16)
     p.chunk_size = Q
@@ -148,6 +151,24 @@ def test_chunk_size_is_honoured(lib, P, N, bf16, Q, algo, aligned, code, qi):
         lay = m.DebugLayout()
         assert m.load().ssd_fwd_debug_layout(ctypes.byref(p), ctypes.byref(a), ctypes.byref(lay)) == 0
         assert lay.qi == qi
+
+
+@pytest.mark.parametrize("P,N,bf16,Q,code", [
+    (16, 16, True, 32, 0),      # the SIMT backward: 32- and 64-token chunks
+    (16, 16, False, 64, 0),
+    (16, 16, True, 128, 2),     # its per-chunk tiles at 128 or 256 exceed shared memory
+    (16, 16, True, 256, 2),
+    (64, 128, True, 128, 0),    # the tensor-core backward: 128
+    (64, 128, False, 128, 2),   # fp32 inputs at 128: no backward computes it
+])
+def test_bwd_chunk_size_is_honoured(lib, P, N, bf16, Q, code):
+    """Each chunk_size outcome of the backward (never re-chunked)."""
+    m = lib_mod()
+    p, a = good_case(P=P, N=N, bf16=bf16)
+    p.chunk_size = Q
+    b = _tc_bwd_args(p, a)
+    n = ctypes.c_size_t(0)
+    assert m.load().ssd_bwd_workspace_size(ctypes.byref(p), ctypes.byref(b), ctypes.byref(n)) == code
 
 
 def test_varlen_metadata_validates_on_host(lib):

@@ -66,6 +66,29 @@ def test_bwd_fp32(case):
     check_bwd(W(**case))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", [
+    dict(L=200, H=4, P=16, G=2, N=16, has_z=True, has_init=True),
+    dict(B=2, L=45, H=3, P=32, G=3, N=64, has_z=True),
+    dict(L=150, H=2, P=128, N=128, has_init=True),
+])
+def test_bwd_chunk32(case, dtype):
+    """The SIMT backward at 32-token chunks (eight threads per chunk row)."""
+    check_bwd(W(Q=32, dtype=dtype, **case), algo="staged")
+
+
+def test_bwd_long_simt_chunks_refused():
+    """The SIMT backward computes 32- and 64-token chunks only: 128 (fp32) and 256 are refused."""
+    import pytest as _pt
+    from state_space_model_scan_gb300 import _lib
+    for Q in (128, 256):
+        w = W(L=300, Q=Q)
+        inp = I.make_inputs(w, with_grad_inputs=True)
+        with _pt.raises(_lib.SSDError) as e:
+            gpu_backward(w, inp, algo="staged")
+        assert e.value.code == 2
+
+
 @pytest.mark.parametrize("algo", ["staged", "fused"])
 @pytest.mark.parametrize("case", [
     dict(L=600, H=8, P=64, G=2, N=128, Q=128, has_z=True, has_init=True),

@@ -83,9 +83,22 @@ def test_bf16_cases(algo, case):
     check_fwd(W(dtype="bf16", **for_algo(case, algo)), algo=algo)
 
 
-@pytest.mark.parametrize("Q", [16, 32, 256])
+@pytest.mark.parametrize("Q", [32, 128, 256])
+@pytest.mark.parametrize("case", [
+    dict(L=300, H=4, P=16, G=2, N=16, has_z=True, has_init=True),   # ragged tail, several chunks
+    dict(B=2, L=97, H=3, P=32, G=1, N=64),                          # shorter than a 128/256 chunk
+    dict(L=513, H=2, P=64, G=1, N=128, has_init=True),              # the tensor-core shape, on SIMT
+])
+def test_simt_chunk_lengths(Q, case):
+    """The SIMT forward at chunk lengths 32, 128 and 256 (the same exact function; only the
+    chunking, and so the rounding order, differs), fp32 and bf16 inputs."""
+    check_fwd(W(Q=Q, **case), algo="staged")
+    check_fwd(W(Q=Q, dtype="bf16", **case), algo="staged")
+
+
+@pytest.mark.parametrize("Q", [16, 512])
 def test_chunk_lengths_no_path_computes_are_refused(Q):
-    """No silent re-chunking: a chunk length that neither path computes is refused."""
+    """No silent re-chunking: a chunk length that no path computes is refused."""
     for dtype, P, N in (("f32", 16, 16), ("bf16", 64, 128)):
         w = W(L=300, P=P, N=N, Q=Q, dtype=dtype)
         inp = I.make_inputs(w)
