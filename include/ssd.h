@@ -93,9 +93,11 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
  * forward) when chunk_size == 128 and the inputs are bf16 with headdim == 64 and dstate 128
  * or 64 (the compiled tile set is dstate 128; dstate 64 runs as its zero-extended half, the
  * cuDNN frontend Mamba-2 engine's headdim = dstate = 64 shape; tensors that break the
- * 16-byte rule then return SSD_ERR_MISALIGNED), and the SIMT path when chunk_size == 64
- * (f32 inputs always take SIMT: fp32 inputs are computed in fp32 FMA, never in tf32); any
- * other combination returns SSD_ERR_UNSUPPORTED. */
+ * 16-byte rule then return SSD_ERR_MISALIGNED), and the SIMT path otherwise (f32 inputs
+ * always take SIMT: fp32 inputs are computed in fp32 FMA, never in tf32).  The chunk length
+ * is never replaced: the SIMT forward computes chunk_size 32, 64, 128 or 256, the SIMT
+ * backward 32 or 64 (its per-chunk Q x Q tiles live in shared memory), the tensor-core path
+ * 128; any other combination returns SSD_ERR_UNSUPPORTED.  STAGED forces the SIMT path. */
 typedef enum {
     SSD_ALGO_AUTO = 0,
     SSD_ALGO_STAGED = 1,   /* SIMT, one kernel per step: cumsum, chunk_state, state_passing, chunk_scan */

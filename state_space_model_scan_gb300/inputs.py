@@ -71,7 +71,8 @@ def named(name: str, L: Optional[int] = None) -> Workload:
     if name == "varlen":         # 16 packed sequences, lengths U{512..8192}, 80 heads x 64, 1 group
         # The continuous-batching workload is quoted with 256-token chunks; the tensor-core
         # tile set computes 128-token chunks (the scan's result does not depend on the chunk
-        # length), so it runs at 128, on a chunk grid over the packed axis.
+        # length), so it is timed at 128, on a chunk grid over the packed axis; the SIMT path
+        # computes it at 256 as well (a parity case).
         lens = varlen_lengths(16, 512, 8192, 0)
         return Workload(name, 1, sum(lens), 80, 64, 1, 128, 128, "bf16", has_z=False, has_D=True,
                         has_init=True, seqlens=lens)

@@ -2,6 +2,8 @@
 configuration bench.py times (AUTO path, default work units).  The float64
 oracle computes a sample of heads (heads are independent, so each sampled head
 is an exact reference for that head's outputs and final state)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -39,6 +41,12 @@ def test_long_sequence_fwd_full_size(L):
 def test_varlen_fwd_full_size():
     """16 packed sequences, lengths U{512..8192}, 80 heads x 64, 1 group, own initial states."""
     check_sampled(I.named("varlen"), [0, 41, 79])
+
+
+def test_varlen_fwd_full_size_chunk256():
+    """The same packed workload at the 256-token chunks it is quoted with (the SIMT path; the
+    chunk grid over the packed axis, chunks holding up to three sequences)."""
+    check_sampled(dataclasses.replace(I.named("varlen"), chunk_size=256), [0, 41, 79])
 
 
 @pytest.mark.parametrize("kept", [False, True])
