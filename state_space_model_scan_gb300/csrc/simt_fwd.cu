@@ -199,6 +199,7 @@ k_chunk_scan(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restr
     float *Bs = Cs + RT * (N + 1);    // RT x (N+1)
     float *Ms = Bs + RT * (N + 1);    // RT x Q
     float *xs = Ms + RT * Q;          // RT x (P+1)
+    float *Ss = xs + RT * (P + 1);    // P x (N+1): the carried state entering the chunk
     const float *dtk = dtw + ((int64_t)k * sh.H + h) * Q;
     const float *csk = csw + ((int64_t)k * sh.H + h) * Q;
     for (int l = tid; l < Q; l += 256) { cs[l] = csk[l]; dt[l] = dtk[l]; }
@@ -208,6 +209,10 @@ k_chunk_scan(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restr
     for (int i = tid; i < RT * N; i += 256) {
         int r = i / N, c = i % N, l = r0 + r;
         Cs[r * (N + 1) + c] = (l < ci.len) ? to_f(cb[(int64_t)(ci.t0 + l) * Cm.s1 + c]) : 0.f;
+    }
+    {   // S_in staged once (coalesced), so the Y_off dot products read shared memory
+        const float *sk = states + ((int64_t)k * sh.H + h) * P * N;
+        for (int i = tid; i < P * N; i += 256) Ss[(i / N) * (N + 1) + i % N] = sk[i];
     }
     __syncthreads();
     // M[l][s] = (C_l . B_s) exp(cs[l] - cs[s]) dt[s] for s <= l, over s-tiles up to this row tile
@@ -250,7 +255,7 @@ k_chunk_scan(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restr
         __syncthreads();
     }
     // Y_off[l][p] = exp(cs[l]) sum_n C[l][n] S_in[p][n]; then D skip, gate, store
-    const float *sin = states + ((int64_t)k * sh.H + h) * P * N + (int64_t)p * N;
+    const float *sin = Ss + p * (N + 1);
     const float Dh = D ? D[h] : 0.f;
     T *yb = (T *)y.p + (int64_t)ci.b * y.s0 + (int64_t)h * y.s2;
     const T *zb = z.p ? (const T *)z.p + (int64_t)ci.b * z.s0 + (int64_t)h * z.s2 : nullptr;
@@ -310,7 +315,8 @@ cudaError_t launch_state_passing(const Shape &sh, const int32_t *hdr, const SeqI
 }
 
 size_t chunk_scan_smem(const Shape &sh) {
-    return sizeof(float) * (size_t)(2 * sh.Q + 2 * 32 * (sh.N + 1) + 32 * sh.Q + 32 * (sh.P + 1));
+    return sizeof(float) * (size_t)(2 * sh.Q + 2 * 32 * (sh.N + 1) + 32 * sh.Q + 32 * (sh.P + 1) +
+                                    sh.P * (sh.N + 1));
 }
 
 template <typename T>
