@@ -104,7 +104,8 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
             int64_t sdl, const float *__restrict__ A, const float *__restrict__ D, const float *__restrict__ bias,
             const float *__restrict__ dtw, const float *__restrict__ csw, const float *__restrict__ states,
             const float *__restrict__ dstates, MView3 dx, MView3 dz, float *__restrict__ ddt, int64_t sddb,
-            int64_t sddl, float *__restrict__ dBh, float *__restrict__ dCh, float *__restrict__ partials) {
+            int64_t sddl, float *__restrict__ dBh, float *__restrict__ dCh, float *__restrict__ partials,
+            int stage_states) {
     constexpr int NP = 256 / QS;   // threads per chunk row
     constexpr int NQ = QS / 32;    // 32-position blocks of the per-position scalars
     extern __shared__ float sm[];
@@ -124,6 +125,8 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     float *Mm = Cs + QS * N1;        // QS x Q1  CB, then M
     float *Em = Mm + QS * Q1;        // QS x Q1  dM, then E dt dM
     float *Tm = Em + QS * Q1;        // QS x Q1  E CB dM
+    float *Dso = Tm + QS * Q1;       // P x N1   dS_out, S_in (when stage_states: the per-row dot
+    float *Sis = Dso + P * N1;       //          products then read shared memory, not global)
     float *rowXU = vec, *rowT2 = vec + QS, *rowD = vec + 2 * QS;
 
     const float *dtk = dtw + ((int64_t)k * sh.H + h) * QS;
@@ -155,6 +158,14 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
         Bs[r * N1 + c] = in ? to_f(bb[(int64_t)(ci.t0 + r) * Bm.s1 + c]) : 0.f;
         Cs[r * N1 + c] = in ? to_f(cb[(int64_t)(ci.t0 + r) * Cm.s1 + c]) : 0.f;
     }
+    const float *dsg = dstates + ((int64_t)k * sh.H + h) * P * N;
+    const float *sig = states + ((int64_t)k * sh.H + h) * P * N;
+    if (stage_states) {
+        for (int i = tid; i < P * N; i += 256) {
+            Dso[(i / N) * N1 + i % N] = dsg[i];
+            Sis[(i / N) * N1 + i % N] = sig[i];
+        }
+    }
     __syncthreads();
     // CB[l][s], dM[l][s]
     for (int i = tid; i < QS * QS; i += 256) {
@@ -172,8 +183,9 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     __syncthreads();
 
     const int r = tid / NP, part = tid % NP;     // row r, part `part` of its columns
-    const float *dso = dstates + ((int64_t)k * sh.H + h) * P * N;
-    const float *sin = states + ((int64_t)k * sh.H + h) * P * N;
+    const float *dso = stage_states ? Dso : dsg;
+    const float *sin = stage_states ? Sis : sig;
+    const int ld = stage_states ? N1 : N;   // row stride of dso / sin
     const float Dh = D ? D[h] : 0.f;
     const bool live = r >= ci.lo && r < ci.len;
     const int64_t tok = (int64_t)ci.t0 + r;
@@ -184,7 +196,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
             float a = 0.f;
             for (int l = r; l < QS; ++l) a += Mm[l * Q1 + r] * dys[l * P1 + p];
             float u = 0.f;
-            const float *drow = dso + (int64_t)p * N;
+            const float *drow = dso + p * ld;
             for (int n = 0; n < N; ++n) u += Bs[r * N1 + n] * drow[n];
             xu += xs[r * P1 + p] * u;
             if (live) {
@@ -202,7 +214,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
             float a = 0.f;
             for (int l = r; l < QS; ++l) a += Em[l * Q1 + r] * Cs[l * N1 + n];
             float b = 0.f;
-            for (int p = 0; p < P; ++p) b += xs[r * P1 + p] * dso[(int64_t)p * N + n];
+            for (int p = 0; p < P; ++p) b += xs[r * P1 + p] * dso[p * ld + n];
             o[n] = a + wst[r] * b;
         }
     }
@@ -214,7 +226,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
             float a = 0.f;
             for (int s = 0; s <= r; ++s) a += Em[r * Q1 + s] * Bs[s * N1 + n];
             float b = 0.f;
-            for (int p = 0; p < P; ++p) b += dys[r * P1 + p] * sin[(int64_t)p * N + n];
+            for (int p = 0; p < P; ++p) b += dys[r * P1 + p] * sin[p * ld + n];
             o[n] = a + er * b;
         }
     }
@@ -226,7 +238,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
             float yd = 0.f;
             for (int s = 0; s <= r; ++s) yd += Mm[r * Q1 + s] * xs[s * P1 + p];
             float yb = 0.f;
-            const float *srow = sin + (int64_t)p * N;
+            const float *srow = sin + p * ld;
             for (int n = 0; n < N; ++n) yb += Cs[r * N1 + n] * srow[n];
             const float yo = er * yb;
             t2 += dys[r * P1 + p] * yo;
@@ -247,7 +259,7 @@ k_bwd_chunk(Shape sh, const int32_t *__restrict__ hdr, const ChunkInfo *__restri
     __syncthreads();
     // T3 = exp(cs[Q-1]) <S_in, dS_out>: fixed-order block reduction
     float t3p = 0.f;
-    for (int i = tid; i < P * N; i += 256) t3p += sin[i] * dso[i];
+    for (int i = tid; i < P * N; i += 256) t3p += sin[(i / N) * ld + i % N] * dso[(i / N) * ld + i % N];
     t3p = warp_sum(t3p);
     float *red = vec + 3 * QS;    // 8 warp partials
     if ((tid & 31) == 0) red[tid >> 5] = t3p;
@@ -384,6 +396,9 @@ size_t bwd_chunk_smem(const Shape &sh) {
     const int QS = sh.Q, P1 = sh.P + 1, N1 = sh.N + 1, Q1 = QS + 1;
     return sizeof(float) * (size_t)(11 * QS + 2 * QS * P1 + 2 * QS * N1 + 3 * QS * Q1);
 }
+// dS_out and S_in of the chunk staged in shared memory too, where they fit (227 KB per block)
+static size_t bwd_chunk_stage_bytes(const Shape &sh) { return sizeof(float) * 2 * (size_t)sh.P * (sh.N + 1); }
+static bool bwd_chunk_stages(const Shape &sh) { return bwd_chunk_smem(sh) + bwd_chunk_stage_bytes(sh) <= 227 * 1024; }
 
 template <typename T>
 cudaError_t launch_bwd_dstates(const Shape &sh, const int32_t *hdr, const ChunkInfo *chunks, View3 dy, View3 z,
@@ -403,21 +418,22 @@ cudaError_t launch_bwd_chunk(const Shape &sh, const int32_t *hdr, const ChunkInf
                              const float *A, const float *D, const float *bias, const float *dtw, const float *csw,
                              const float *states, const float *dstates, MView3 dx, MView3 dz, float *ddt,
                              int64_t sddb, int64_t sddl, float *dBh, float *dCh, float *partials, cudaStream_t st) {
-    const size_t smem = bwd_chunk_smem(sh);
+    const int stage = bwd_chunk_stages(sh) ? 1 : 0;
+    const size_t smem = bwd_chunk_smem(sh) + (stage ? bwd_chunk_stage_bytes(sh) : 0);
     if (sh.Q == 32) {
         static int attr_done[64] = {0};
         cudaError_t e = ensure_smem_attr(k_bwd_chunk<T, 32>, (int)smem, attr_done);
         if (e != cudaSuccess) return e;
         k_bwd_chunk<T, 32><<<dim3(sh.kmax, sh.H), 256, smem, st>>>(sh, hdr, chunks, x, Bm, Cm, z, dy, dt_raw, sdb, sdl,
                                                                    A, D, bias, dtw, csw, states, dstates, dx, dz, ddt,
-                                                                   sddb, sddl, dBh, dCh, partials);
+                                                                   sddb, sddl, dBh, dCh, partials, stage);
     } else if (sh.Q == 64) {
         static int attr_done[64] = {0};
         cudaError_t e = ensure_smem_attr(k_bwd_chunk<T, 64>, (int)smem, attr_done);
         if (e != cudaSuccess) return e;
         k_bwd_chunk<T, 64><<<dim3(sh.kmax, sh.H), 256, smem, st>>>(sh, hdr, chunks, x, Bm, Cm, z, dy, dt_raw, sdb, sdl,
                                                                    A, D, bias, dtw, csw, states, dstates, dx, dz, ddt,
-                                                                   sddb, sddl, dBh, dCh, partials);
+                                                                   sddb, sddl, dBh, dCh, partials, stage);
     } else {
         return cudaErrorInvalidValue;
     }
