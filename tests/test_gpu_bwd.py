@@ -115,8 +115,9 @@ def test_bwd_fused_multi_unit(seg):
         assert rel_l2(a.reshape(o[on].shape), o[on]) <= TOL["bf16"], gn
 
 
-def test_bwd_varlen():
-    w = I.Workload("v", 1, 241, 4, 16, 2, 16, 64, "f32", has_z=True, has_init=True, seqlens=[40, 0, 130, 1, 70])
+@pytest.mark.parametrize("Q", [32, 64])
+def test_bwd_varlen(Q):
+    w = I.Workload("v", 1, 241, 4, 16, 2, 16, Q, "f32", has_z=True, has_init=True, seqlens=[40, 0, 130, 1, 70])
     check_bwd(w)
 
 

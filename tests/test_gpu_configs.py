@@ -45,7 +45,7 @@ def test_varlen_fwd_full_size():
 
 def test_varlen_fwd_full_size_chunk256():
     """The same packed workload at the 256-token chunks it is quoted with (the SIMT path; the
-    chunk grid over the packed axis, chunks holding up to three sequences)."""
+    chunk grid over the packed axis, so chunks that straddle two sequences)."""
     check_sampled(dataclasses.replace(I.named("varlen"), chunk_size=256), [0, 41, 79])
 
 

@@ -118,6 +118,20 @@ def test_varlen_matches_oracle(dtype, P, N, algo):
     assert rel_l2(fin.double().cpu().numpy(), fo) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("Q", [32, 256])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_varlen_simt_chunk_lengths(Q, dtype):
+    """Packed sequences at chunk lengths 32 and 256 (SIMT path): at 256 the first chunk holds
+    six sequences (40, 0, 130, 1, 70 tokens and the head of the 64-token one), at 32 most
+    sequences span several chunks."""
+    w = VW([40, 0, 130, 1, 70, 64, 129, 300], dtype=dtype, has_z=True, Q=Q)
+    inp = I.make_inputs(w)
+    y, fin = gpu_forward(w, inp, algo="staged")
+    yo, fo = oracle_forward(w, inp)
+    assert rel_l2(flat(y, w.seqlen), yo) <= TOL[dtype]
+    assert rel_l2(fin.double().cpu().numpy(), fo) <= TOL[dtype]
+
+
 @pytest.mark.parametrize("seg", [1, 2, 5])
 def test_varlen_fused_units_across_shared_chunks(seg):
     """Many short and long sequences on the tensor-core path with several units per
