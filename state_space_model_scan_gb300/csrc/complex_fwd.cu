@@ -25,11 +25,14 @@
 // (Cb = C B^T, Yraw = C S^T with S the carry-in state, Ydiag = M X, Sloc = (w o B)^T X) with
 // cs the in-chunk inclusive cumulative sum of softplus(dt) A, L[l, s] = exp(cs_l - cs_s) for
 // l >= s and w_l = exp(cs_63 - cs_l).  TMEM lanes 0..63 (the upper half of the CTA's warps)
-// hold rows l of Cb, Yraw and Ydiag; lanes 64..127 (the lower half) the imaginary parts of
-// Cb and Yraw, which they pass to the upper half through shared memory, and Sloc, whose rows n
-// they fold into the carried state.  MMAs (K = 128: 16 of K = 8 each): 16 of M = 128,
-// N = 128 and 32 of M = 128, N = 64 per chunk.  Positions past the end of the sequence read as zero (TMA bounds fill) and
-// carry no decay.
+// hold the real parts of rows l of Cb, Yraw and Ydiag; lanes 64..127 (the lower half) the
+// imaginary parts of Cb and Yraw, and Sloc, whose rows n they fold into the carried state.
+// Both halves build M, in alternating 8-column groups, passing each other the component of
+// the other's groups through shared memory; the lower half passes Im Yraw to the upper half,
+// which writes y.  Batch 2's two chains are committed separately, so the real outputs are
+// written while the imaginary chain runs.  MMAs (K = 128: 16 of K = 8 each): 16 of M = 128,
+// N = 128 and 32 of M = 128, N = 64 per chunk.  Positions past the end of the sequence read
+// as zero (TMA bounds fill) and carry no decay.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -53,7 +56,7 @@ constexpr uint32_t OFF_CC = 0;              // 128-row: [conj(C) ; swap(C)] (bat
 constexpr uint32_t OFF_BS = 2 * SLOT;       // 128-row: [B tile (then swap(X^T)) ; carried state S]
 constexpr uint32_t OFF_X = 4 * SLOT;        // X tile as loaded
 constexpr uint32_t OFF_XC = 5 * SLOT;       // conj(X^T)
-constexpr uint32_t OFF_E = 6 * SLOT;        // exchange: imaginary parts of Cb, then of Yraw, [64][65] fp32
+constexpr uint32_t OFF_E = 6 * SLOT;        // exchange, [64][65] fp32: Cb parts for the M build, then Im Yraw
 constexpr uint32_t E_STRIDE = 65;
 constexpr uint32_t OFF_MISC = OFF_E + 64 * E_STRIDE * 4 + 256;
 // per-chunk tables, two sets (chunk c uses set c & 1; the next chunk's is built meanwhile)
