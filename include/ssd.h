@@ -75,7 +75,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 4
+#define SSD_ABI_VERSION 5
 
 typedef enum {
     SSD_OK = 0,
@@ -288,31 +288,36 @@ ssd_status ssd_varlen_metadata(const int32_t *cu_seqlens, int64_t nseqs, int64_t
                                void *stream);
 
 /*
- * Gated RMS normalisation over feature groups -- the normalisation that follows the scan
- * in a Mamba-2 block (the gated-LayerNorm whose backward the Helion pull request for the
- * Mamba-2 SSD path times as layer_norm_bwd, "Summary" and "Measurements"; read as RMS
- * normalisation with the gate applied before it):
+ * Gated normalisation over feature groups -- the normalisation that follows the scan in a
+ * Mamba-2 block (the gated LayerNorm / RMSNorm whose backward the Helion pull request for the
+ * Mamba-2 SSD path times as layer_norm_bwd, "Summary" and "Measurements").  Per row t and
+ * group g = features [g * group_size, (g+1) * group_size), with s = silu(z) (s = 1 when z is
+ * NULL):
  *
- *   v[t,i]    = y[t,i] * silu(z[t,i])          (v = y when z is NULL)
- *   rstd[t,g] = 1 / sqrt(mean_{i in group g} v[t,i]^2 + eps),  group g = features
- *               [g * group_size, (g+1) * group_size)
- *   out[t,i]  = v[t,i] * rstd[t, i / group_size] * weight[i]
+ *   u[t,i]    = y[t,i] * s[t,i]       (default: the gate first)
+ *             = y[t,i]                (flags & SSD_NORM_GATE_AFTER)
+ *   mu[t,g]   = 0                     (default: RMS normalisation)
+ *             = mean_{i in g} u[t,i]  (flags & SSD_NORM_LAYER: LayerNorm, no bias)
+ *   rstd[t,g] = 1 / sqrt(mean_{i in g} (u[t,i] - mu[t,g])^2 + eps)
+ *   out[t,i]  = (u[t,i] - mu[t,g]) * rstd[t,g] * weight[i]    (times s[t,i] when the gate comes after)
  *
  * Feed it the scan's ungated output (ssd_fwd with z absent) and z; a Mamba-2 block uses
  * group_size = nheads * headdim / ngroups, so a group is the heads of one B/C group.
  * Tensors y, z, out, dout, dy, dz: `rows` rows of `width` contiguous features at an element
  * row stride, all of `dtype` (bf16 or f32), 16-byte aligned with strides a multiple of 8
  * (else SSD_ERR_MISALIGNED).  weight, dweight: f32 [width]; rstd: f32 [rows][width /
- * group_size], written by the forward and read by the backward.  group_size must divide
- * width (else SSD_ERR_INVALID_ARGUMENT) and be a multiple of 8 no larger than 6144 (else
- * SSD_ERR_UNSUPPORTED).  Buffers are the caller's, device memory; work is enqueued on
+ * group_size], written by the forward and read by the backward (which recomputes mu).
+ * group_size must divide width (else SSD_ERR_INVALID_ARGUMENT) and be a multiple of 8 no
+ * larger than 6144 (else SSD_ERR_UNSUPPORTED); flags other than the two below are
+ * SSD_ERR_INVALID_ARGUMENT.  Buffers are the caller's, device memory; work is enqueued on
  * `stream`; the weight gradient is summed in a fixed order (bitwise reproducible).
  */
+enum { SSD_NORM_LAYER = 1, SSD_NORM_GATE_AFTER = 2 };
 typedef struct {
     int64_t rows, width, group_size;
     float eps;
     int32_t dtype;      /* ssd_dtype of y, z, out, dout, dy, dz */
-    int32_t reserved;   /* must be 0 */
+    int32_t flags;      /* SSD_NORM_LAYER | SSD_NORM_GATE_AFTER, or 0 (gated RMS normalisation) */
 } ssd_norm_problem;
 
 ssd_status ssd_gated_norm_fwd(const ssd_norm_problem *prob, const void *y, int64_t y_stride, const void *z,

@@ -63,7 +63,7 @@ class BwdArgs(ctypes.Structure):
 
 class NormProblem(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int64), ("width", ctypes.c_int64), ("group_size", ctypes.c_int64),
-                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("eps", ctypes.c_float), ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class ConvProblem(ctypes.Structure):
@@ -286,8 +286,12 @@ def _rowstride(t):
     return 0 if t is None else int(t.stride(-2)) if t.dim() >= 2 else int(t.shape[-1])
 
 
-def norm_problem(rows, width, group_size, eps, dtype):
-    return NormProblem(rows, width, group_size, eps, SSD_BF16 if dtype == torch.bfloat16 else SSD_F32, 0)
+SSD_NORM_LAYER, SSD_NORM_GATE_AFTER = 1, 2
+
+
+def norm_problem(rows, width, group_size, eps, dtype, layer_norm=False, gate_after=False):
+    flags = (SSD_NORM_LAYER if layer_norm else 0) | (SSD_NORM_GATE_AFTER if gate_after else 0)
+    return NormProblem(rows, width, group_size, eps, SSD_BF16 if dtype == torch.bfloat16 else SSD_F32, flags)
 
 
 def gated_norm_fwd(prob, y, z, weight, out, rstd, stream=None):

@@ -111,28 +111,31 @@ def _rows(t, width):
     return t.reshape(-1, width)
 
 
-def gated_norm_forward(y, weight, group_size, z=None, eps=1e-5, stream=None):
-    """out, rstd = the gated RMS normalisation of y (see include/ssd.h, ssd_gated_norm_fwd):
-    out = y silu(z) / rms over each group of `group_size` features * weight.  y, z: [..., width]."""
+def gated_norm_forward(y, weight, group_size, z=None, eps=1e-5, layer_norm=False, gate_after=False, stream=None):
+    """out, rstd = the gated normalisation of y over groups of `group_size` features (see
+    include/ssd.h, ssd_gated_norm_fwd): RMS (default) or LayerNorm (layer_norm=True, no bias)
+    of u = y silu(z), times weight; with gate_after=True, of u = y, times weight and silu(z).
+    y, z: [..., width]."""
     width = y.shape[-1]
     y2 = _rows(y, width)
     z2 = _rows(z, width) if z is not None else None
     out = torch.empty_like(y2)
     rstd = torch.empty(y2.shape[0], width // group_size, dtype=torch.float32, device=y.device)
-    prob = _lib.norm_problem(y2.shape[0], width, group_size, eps, y.dtype)
+    prob = _lib.norm_problem(y2.shape[0], width, group_size, eps, y.dtype, layer_norm, gate_after)
     _lib.check(_lib.gated_norm_fwd(prob, y2, z2, weight, out, rstd, stream), "ssd_gated_norm_fwd")
     return out.reshape(y.shape), rstd
 
 
-def gated_norm_backward(y, weight, rstd, dout, group_size, z=None, eps=1e-5, stream=None):
-    """dy, dz (None without z), dweight: gradients of sum(dout * out)."""
+def gated_norm_backward(y, weight, rstd, dout, group_size, z=None, eps=1e-5, layer_norm=False, gate_after=False,
+                        stream=None):
+    """dy, dz (None without z), dweight: gradients of sum(dout * out) (same options as the forward)."""
     width = y.shape[-1]
     y2, d2 = _rows(y, width), _rows(dout, width)
     z2 = _rows(z, width) if z is not None else None
     dy = torch.empty_like(y2)
     dz = torch.empty_like(z2) if z is not None else None
     dw = torch.empty(width, dtype=torch.float32, device=y.device)
-    prob = _lib.norm_problem(y2.shape[0], width, group_size, eps, y.dtype)
+    prob = _lib.norm_problem(y2.shape[0], width, group_size, eps, y.dtype, layer_norm, gate_after)
     ws = torch.empty(max(_lib.gated_norm_bwd_workspace_size(prob), 16), dtype=torch.uint8, device=y.device)
     _lib.check(_lib.gated_norm_bwd(prob, y2, z2, weight, rstd, d2, dy, dz, dw, ws, stream), "ssd_gated_norm_bwd")
     return dy.reshape(y.shape), (dz.reshape(z.shape) if dz is not None else None), dw

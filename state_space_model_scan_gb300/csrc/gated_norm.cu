@@ -1,10 +1,11 @@
-// gated_norm.cu -- gated RMS normalisation over feature groups, forward and backward: the
-// normalisation that follows the SSD scan in a Mamba-2 block (the gated-LayerNorm whose
-// backward the Helion pull request for the Mamba-2 SSD path times as layer_norm_bwd,
-// "Measurements"), read as RMS normalisation with the gate applied first:
+// gated_norm.cu -- gated normalisation over feature groups, forward and backward: the
+// normalisation that follows the SSD scan in a Mamba-2 block (the gated LayerNorm / RMSNorm
+// whose backward the Helion pull request for the Mamba-2 SSD path times as layer_norm_bwd,
+// "Measurements").  Per row t and group g of features i, with s = silu(z) (s = 1 without z):
 //
-//   v = y silu(z)  (v = y without a gate),  rstd[t,g] = 1/sqrt(mean_{i in g} v[t,i]^2 + eps),
-//   out[t,i] = v[t,i] rstd[t,g(i)] w[i]
+//   u = y s (gate first, the default) or u = y (normalise, then gate),
+//   mu = mean_{i in g} u (LayerNorm) or 0 (RMS),  rstd[t,g] = 1/sqrt(mean_{i in g} (u-mu)^2 + eps),
+//   out[t,i] = (u - mu) rstd w[i]  (times s when the gate comes after)
 //
 // and its exact derivative.  Memory-bound: one warp per (row, group) item, each lane eight
 // consecutive features per 16-byte (bf16) or 32-byte (fp32) access; the backward's weight
@@ -76,6 +77,7 @@ struct NormArgs {
     float *rstd;
     float *partials;          // [row chunk][width] (backward)
     int64_t rows_per_chunk;
+    int ln, bg;               // LayerNorm (subtract the group mean); gate applied after the norm
 };
 
 template <typename T>
@@ -89,37 +91,55 @@ k_norm_fwd(const NormArgs a) {
         const int g = (int)(it - r * a.ng);
         const T *yr = static_cast<const T *>(a.y) + r * a.sy + (int64_t)g * a.G;
         const T *zr = a.z ? static_cast<const T *>(a.z) + r * a.sz + (int64_t)g * a.G : nullptr;
-        float ss = 0.f;
-        for (int j = lane; j < pieces; j += 32) {
-            float v[8];
-            load8(yr + 8 * j, v);
-            if (zr) {
+        // u of piece j (each pass re-reads the lines the warp just read: cache hits)
+        auto load_u = [&](int j, float (&u)[8]) {
+            load8(yr + 8 * j, u);
+            if (zr && !a.bg) {
                 float zz[8];
                 load8(zr + 8 * j, zz);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig_t<T>(zz[e]);
+                for (int e = 0; e < 8; ++e) u[e] *= zz[e] * sig_t<T>(zz[e]);
             }
+        };
+        float mu = 0.f;
+        if (a.ln) {
+            float ls = 0.f;
+            for (int j = lane; j < pieces; j += 32) {
+                float u[8];
+                load_u(j, u);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+                for (int e = 0; e < 8; ++e) ls += u[e];
+            }
+            mu = warp_sum(ls) / (float)a.G;
+        }
+        float ss = 0.f;
+        for (int j = lane; j < pieces; j += 32) {
+            float u[8];
+            load_u(j, u);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float c = u[e] - mu;
+                ss = fmaf(c, c, ss);
+            }
         }
         ss = warp_sum(ss);
         const float rs = 1.f / sqrtf(ss / (float)a.G + a.eps);
         if (lane == 0) a.rstd[r * a.ng + g] = rs;
         T *orow = static_cast<T *>(a.out) + r * a.sout + (int64_t)g * a.G;
         const float *wr = a.w + (int64_t)g * a.G;
-        for (int j = lane; j < pieces; j += 32) {   // the warp just read these lines: cache hits
-            float v[8], wv[8];
-            load8(yr + 8 * j, v);
-            if (zr) {
+        for (int j = lane; j < pieces; j += 32) {
+            float u[8], wv[8];
+            load_u(j, u);
+            load8(wr + 8 * j, wv);
+            if (zr && a.bg) {
                 float zz[8];
                 load8(zr + 8 * j, zz);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig_t<T>(zz[e]);
+                for (int e = 0; e < 8; ++e) wv[e] *= zz[e] * sig_t<T>(zz[e]);
             }
-            load8(wr + 8 * j, wv);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = v[e] * rs * wv[e];
-            store8(orow + 8 * j, v);
+            for (int e = 0; e < 8; ++e) u[e] = (u[e] - mu) * rs * wv[e];
+            store8(orow + 8 * j, u);
         }
     }
 }
@@ -143,48 +163,65 @@ k_norm_bwd(const NormArgs a) {
         const T *zr = a.z ? static_cast<const T *>(a.z) + r * a.sz + (int64_t)g * a.G : nullptr;
         const T *dr = static_cast<const T *>(a.dout) + r * a.sdout + (int64_t)g * a.G;
         const float rs = a.rstd_in[r * a.ng + g];
-        float dot = 0.f;   // sum_i (dout w)_i vhat_i
-        for (int j = lane; j < pieces; j += 32) {
-            float v[8], d[8], wv[8];
-            load8(yr + 8 * j, v);
-            if (zr) {
-                float zz[8];
-                load8(zr + 8 * j, zz);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= zz[e] * sig_t<T>(zz[e]);
-            }
-            load8(dr + 8 * j, d);
-            load8(wr + 8 * j, wv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dot = fmaf(d[e] * wv[e], v[e] * rs, dot);
-        }
-        dot = warp_sum(dot) / (float)a.G;
-        T *dyr = static_cast<T *>(a.dy) + r * a.sdy + (int64_t)g * a.G;
-        T *dzr = a.z ? static_cast<T *>(a.dz) + r * a.sdz + (int64_t)g * a.G : nullptr;
-        for (int j = lane; j < pieces; j += 32) {
-            float y8[8], d[8], wv[8], z8[8], sg[8], s[8];
+        // piece j: y, the gate s = silu(z) and sigma(z), dout, w (re-read by each pass: cache hits)
+        auto load_piece = [&](int j, float (&y8)[8], float (&sg)[8], float (&sgate)[8], float (&z8)[8]) {
             load8(yr + 8 * j, y8);
             if (zr) {
                 load8(zr + 8 * j, z8);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     sg[e] = sig_t<T>(z8[e]);
-                    s[e] = z8[e] * sg[e];
+                    sgate[e] = z8[e] * sg[e];
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s[e] = 1.f;
+                for (int e = 0; e < 8; ++e) { sg[e] = 0.f; sgate[e] = 1.f; z8[e] = 0.f; }
             }
+        };
+        float mu = 0.f;
+        if (a.ln) {
+            float ls = 0.f;
+            for (int j = lane; j < pieces; j += 32) {
+                float y8[8], sg[8], sgate[8], z8[8];
+                load_piece(j, y8, sg, sgate, z8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ls += a.bg ? y8[e] : y8[e] * sgate[e];
+            }
+            mu = warp_sum(ls) / (float)a.G;
+        }
+        float dot = 0.f, gs = 0.f;   // sums over the group of g x_hat and of g, g = d out / d x_hat
+        for (int j = lane; j < pieces; j += 32) {
+            float y8[8], sg[8], sgate[8], z8[8], d[8], wv[8];
+            load_piece(j, y8, sg, sgate, z8);
+            load8(dr + 8 * j, d);
+            load8(wr + 8 * j, wv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float xh = ((a.bg ? y8[e] : y8[e] * sgate[e]) - mu) * rs;
+                const float gw = a.bg ? d[e] * wv[e] * sgate[e] : d[e] * wv[e];
+                dot = fmaf(gw, xh, dot);
+                gs += gw;
+            }
+        }
+        dot = warp_sum(dot) / (float)a.G;
+        gs = a.ln ? warp_sum(gs) / (float)a.G : 0.f;
+        T *dyr = static_cast<T *>(a.dy) + r * a.sdy + (int64_t)g * a.G;
+        T *dzr = a.z ? static_cast<T *>(a.dz) + r * a.sdz + (int64_t)g * a.G : nullptr;
+        for (int j = lane; j < pieces; j += 32) {
+            float y8[8], sg[8], sgate[8], z8[8], d[8], wv[8];
+            load_piece(j, y8, sg, sgate, z8);
             load8(dr + 8 * j, d);
             load8(wr + 8 * j, wv);
             float o1[8], o2[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float vhat = y8[e] * s[e] * rs;
-                const float dv = rs * (d[e] * wv[e] - vhat * dot);
-                o1[e] = dv * s[e];                                                       // dy
-                if (zr) o2[e] = dv * y8[e] * sg[e] * (1.f + z8[e] * (1.f - sg[e]));     // dz
-                mine[8 * j + e] += d[e] * vhat;                                          // dw share
+                const float xh = ((a.bg ? y8[e] : y8[e] * sgate[e]) - mu) * rs;
+                const float gw = a.bg ? d[e] * wv[e] * sgate[e] : d[e] * wv[e];
+                const float du = rs * (gw - gs - xh * dot);                  // d out / d u
+                const float dsilu = sg[e] * (1.f + z8[e] * (1.f - sg[e]));    // silu'(z)
+                o1[e] = a.bg ? du : du * sgate[e];                                          // dy
+                o2[e] = a.bg ? d[e] * wv[e] * xh * dsilu : du * y8[e] * dsilu;              // dz
+                mine[8 * j + e] += d[e] * (a.bg ? xh * sgate[e] : xh);                      // dw share
             }
             store8(dyr + 8 * j, o1);
             if (zr) store8(dzr + 8 * j, o2);
@@ -202,9 +239,11 @@ k_norm_bwd(const NormArgs a) {
 // Register-resident variants for groups of at most 32 * PPL * 8 features: a lane keeps its PPL
 // pieces of y (and z, dout) in registers, so every load of a row is issued at once and nothing is
 // read twice; in the backward the lane's slice of w and of the dw sums stay in registers too.
-template <typename T, int PPL>
+// GEN = false compiles the default mode only (RMS, the gate first); true reads a.ln and a.bg.
+template <typename T, int PPL, bool GEN>
 __global__ void __launch_bounds__(NW * 32)
 k_norm_fwd_reg(const NormArgs a) {
+    const bool ln = GEN && a.ln, bg = GEN && a.bg;
     const int lane = threadIdx.x & 31;
     const int64_t items = a.rows * a.ng, nw = (int64_t)gridDim.x * NW;
     const int pieces = (int)(a.G / 8);
@@ -222,14 +261,32 @@ k_norm_fwd_reg(const NormArgs a) {
                 if (zr) load8(zr + 8 * j, zz[k]);
             }
         }
+        // u in place: the gate multiplies now unless it comes after the norm
+        if (zr && !bg) {
+#pragma unroll
+            for (int k = 0; k < PPL; ++k)
+                if (lane + 32 * k < pieces)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[k][e] *= zz[k][e] * sig_t<T>(zz[k][e]);
+        }
+        float mu = 0.f;
+        if (ln) {
+            float ls = 0.f;
+#pragma unroll
+            for (int k = 0; k < PPL; ++k)
+                if (lane + 32 * k < pieces)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ls += v[k][e];
+            mu = warp_sum(ls) / (float)a.G;
+        }
         float ss = 0.f;
 #pragma unroll
         for (int k = 0; k < PPL; ++k) {
             if (lane + 32 * k < pieces) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    if (zr) v[k][e] *= zz[k][e] * sig_t<T>(zz[k][e]);
-                    ss = fmaf(v[k][e], v[k][e], ss);
+                    const float c = v[k][e] - mu;
+                    ss = fmaf(c, c, ss);
                 }
             }
         }
@@ -244,94 +301,72 @@ k_norm_fwd_reg(const NormArgs a) {
             if (j < pieces) {
                 float wv[8];
                 load8(wr + 8 * j, wv);
+                if (zr && bg)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[k][e] = v[k][e] * rs * wv[e];
+                    for (int e = 0; e < 8; ++e) wv[e] *= zz[k][e] * sig_t<T>(zz[k][e]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[k][e] = (v[k][e] - mu) * rs * wv[e];
                 store8(orow + 8 * j, v[k]);
             }
         }
     }
 }
 
-template <typename T, int PPL>
-__global__ void __launch_bounds__(NW * 32, PPL <= 2 ? 2 : 1)
-k_norm_bwd_reg(const NormArgs a) {
-    extern __shared__ float acc[];   // [NW][G]
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = blockIdx.y;
-    const int pieces = (int)(a.G / 8);
-    const int64_t r0 = (int64_t)blockIdx.x * a.rows_per_chunk, r1 = std::min(a.rows, r0 + a.rows_per_chunk);
-    const float *wr = a.w + (int64_t)g * a.G;
-    float wv[PPL][8], dw[PPL][8];
+// The backward of one (row, group) from a lane's PPL pieces of y, z, dout and w held in
+// registers (the warp holds the row): dy, dz stored, the dw shares accumulated.
+template <typename T, int PPL, bool GEN>
+__device__ __forceinline__ void bwd_row(const NormArgs &a, int lane, int pieces, bool hasz, float rs,
+                                        const float (&y8)[PPL][8], const float (&z8)[PPL][8],
+                                        const float (&d)[PPL][8], const float (&wv)[PPL][8], float (&dw)[PPL][8],
+                                        T *dyr, T *dzr) {
+    const bool ln = GEN && a.ln, bg = GEN && a.bg;
+    float mu = 0.f;
+    if (ln) {
+        float ls = 0.f;
+#pragma unroll
+        for (int k = 0; k < PPL; ++k)
+            if (lane + 32 * k < pieces)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ls += (hasz && !bg) ? y8[k][e] * (z8[k][e] * sig_t<T>(z8[k][e])) : y8[k][e];
+        mu = warp_sum(ls) / (float)a.G;
+    }
+    float dot = 0.f, gs = 0.f;   // sums over the group of g x_hat and of g, g = d out / d x_hat
+#pragma unroll
+    for (int k = 0; k < PPL; ++k) {
+        if (lane + 32 * k < pieces) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float sgate = hasz ? z8[k][e] * sig_t<T>(z8[k][e]) : 1.f;
+                const float xh = ((bg ? y8[k][e] : y8[k][e] * sgate) - mu) * rs;
+                const float gw = bg ? d[k][e] * wv[k][e] * sgate : d[k][e] * wv[k][e];
+                dot = fmaf(gw, xh, dot);
+                if (ln) gs += gw;
+            }
+        }
+    }
+    dot = warp_sum(dot) / (float)a.G;
+    gs = ln ? warp_sum(gs) / (float)a.G : 0.f;
 #pragma unroll
     for (int k = 0; k < PPL; ++k) {
         const int j = lane + 32 * k;
+        if (j < pieces) {
+            float o1[8], o2[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) { dw[k][e] = 0.f; wv[k][e] = 0.f; }
-        if (j < pieces) load8(wr + 8 * j, wv[k]);
-    }
-    for (int64_t r = r0 + warp; r < r1; r += NW) {
-        const T *yr = static_cast<const T *>(a.y) + r * a.sy + (int64_t)g * a.G;
-        const T *zr = a.z ? static_cast<const T *>(a.z) + r * a.sz + (int64_t)g * a.G : nullptr;
-        const T *dr = static_cast<const T *>(a.dout) + r * a.sdout + (int64_t)g * a.G;
-        float y8[PPL][8], z8[PPL][8], d[PPL][8];
-#pragma unroll
-        for (int k = 0; k < PPL; ++k) {
-            const int j = lane + 32 * k;
-            if (j < pieces) {
-                load8(yr + 8 * j, y8[k]);
-                if (zr) load8(zr + 8 * j, z8[k]);
-                load8(dr + 8 * j, d[k]);
+            for (int e = 0; e < 8; ++e) {
+                const float sg = hasz ? sig_t<T>(z8[k][e]) : 0.f;
+                const float sgate = hasz ? z8[k][e] * sg : 1.f;
+                const float xh = ((bg ? y8[k][e] : y8[k][e] * sgate) - mu) * rs;
+                const float gw = bg ? d[k][e] * wv[k][e] * sgate : d[k][e] * wv[k][e];
+                const float du = rs * (gw - gs - xh * dot);                     // d out / d u
+                const float dsilu = sg * (1.f + z8[k][e] * (1.f - sg));         // silu'(z)
+                o1[e] = bg ? du : du * sgate;                                                    // dy
+                o2[e] = hasz ? (bg ? d[k][e] * wv[k][e] * xh * dsilu : du * y8[k][e] * dsilu) : 0.f;  // dz
+                dw[k][e] = fmaf(d[k][e], bg ? xh * sgate : xh, dw[k][e]);                       // dw share
             }
+            store8(dyr + 8 * j, o1);
+            if (hasz) store8(dzr + 8 * j, o2);
         }
-        const float rs = a.rstd_in[r * a.ng + g];
-        float dot = 0.f;   // sum_i (dout w)_i vhat_i
-#pragma unroll
-        for (int k = 0; k < PPL; ++k) {
-            if (lane + 32 * k < pieces) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float sgate = zr ? z8[k][e] * sig_t<T>(z8[k][e]) : 1.f;
-                    dot = fmaf(d[k][e] * wv[k][e], y8[k][e] * sgate * rs, dot);
-                }
-            }
-        }
-        dot = warp_sum(dot) / (float)a.G;
-        T *dyr = static_cast<T *>(a.dy) + r * a.sdy + (int64_t)g * a.G;
-        T *dzr = a.z ? static_cast<T *>(a.dz) + r * a.sdz + (int64_t)g * a.G : nullptr;
-#pragma unroll
-        for (int k = 0; k < PPL; ++k) {
-            const int j = lane + 32 * k;
-            if (j < pieces) {
-                float o1[8], o2[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float sg = zr ? sig_t<T>(z8[k][e]) : 0.f;
-                    const float sgate = zr ? z8[k][e] * sg : 1.f;
-                    const float vhat = y8[k][e] * sgate * rs;
-                    const float dv = rs * (d[k][e] * wv[k][e] - vhat * dot);
-                    o1[e] = dv * sgate;                                                          // dy
-                    o2[e] = zr ? dv * y8[k][e] * sg * (1.f + z8[k][e] * (1.f - sg)) : 0.f;      // dz
-                    dw[k][e] = fmaf(d[k][e], vhat, dw[k][e]);                                   // dw share
-                }
-                store8(dyr + 8 * j, o1);
-                if (zr) store8(dzr + 8 * j, o2);
-            }
-        }
-    }
-    float *mine = acc + (int64_t)warp * a.G;
-#pragma unroll
-    for (int k = 0; k < PPL; ++k) {
-        const int j = lane + 32 * k;
-        if (j < pieces)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mine[8 * j + e] = dw[k][e];
-    }
-    __syncthreads();
-    float *dst = a.partials + (int64_t)blockIdx.x * a.width + (int64_t)g * a.G;
-    for (int64_t i = threadIdx.x; i < a.G; i += blockDim.x) {
-        float s = 0.f;
-        for (int w = 0; w < NW; ++w) s += acc[(int64_t)w * a.G + i];
-        dst[i] = s;
     }
 }
 
@@ -345,7 +380,7 @@ __device__ __forceinline__ void cp16(void *dst, const void *src) {
                  "l"(src)
                  : "memory");
 }
-template <typename T, int PPL>
+template <typename T, int PPL, bool GEN>
 __global__ void __launch_bounds__(NW * 32)
 k_norm_bwd_staged(const NormArgs a) {
     extern __shared__ __align__(16) uint8_t nsm[];
@@ -392,7 +427,7 @@ k_norm_bwd_staged(const NormArgs a) {
         const int64_t r = rb + warp;
         if (r < r1) {
             const T *ys = tile(buf, 0, warp), *ds = tile(buf, 1, warp), *zs = a.z ? tile(buf, 2, warp) : nullptr;
-            float y8[PPL][8], z8[PPL][8], d[PPL][8];
+            float y8[PPL][8], z8[PPL][8] = {}, d[PPL][8];
 #pragma unroll
             for (int k = 0; k < PPL; ++k) {
                 const int j = lane + 32 * k;
@@ -403,39 +438,9 @@ k_norm_bwd_staged(const NormArgs a) {
                 }
             }
             const float rs = a.rstd_in[r * a.ng + g];
-            float dot = 0.f;
-#pragma unroll
-            for (int k = 0; k < PPL; ++k) {
-                if (lane + 32 * k < pieces) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float sgate = zs ? z8[k][e] * sig_t<T>(z8[k][e]) : 1.f;
-                        dot = fmaf(d[k][e] * wv[k][e], y8[k][e] * sgate * rs, dot);
-                    }
-                }
-            }
-            dot = warp_sum(dot) / (float)G;
             T *dyr = static_cast<T *>(a.dy) + r * a.sdy + (int64_t)g * G;
             T *dzr = a.z ? static_cast<T *>(a.dz) + r * a.sdz + (int64_t)g * G : nullptr;
-#pragma unroll
-            for (int k = 0; k < PPL; ++k) {
-                const int j = lane + 32 * k;
-                if (j < pieces) {
-                    float o1[8], o2[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float sg = zs ? sig_t<T>(z8[k][e]) : 0.f;
-                        const float sgate = zs ? z8[k][e] * sg : 1.f;
-                        const float vhat = y8[k][e] * sgate * rs;
-                        const float dv = rs * (d[k][e] * wv[k][e] - vhat * dot);
-                        o1[e] = dv * sgate;
-                        o2[e] = zs ? dv * y8[k][e] * sg * (1.f + z8[k][e] * (1.f - sg)) : 0.f;
-                        dw[k][e] = fmaf(d[k][e], vhat, dw[k][e]);
-                    }
-                    store8(dyr + 8 * j, o1);
-                    if (zs) store8(dzr + 8 * j, o2);
-                }
-            }
+            bwd_row<T, PPL, GEN>(a, lane, pieces, zs != nullptr, rs, y8, z8, d, wv, dw, dyr, dzr);
         }
         __syncthreads();   // this buffer is refilled two batches on
     }
@@ -482,14 +487,31 @@ cudaError_t launch_one(K kernel, const NormArgs &a, dim3 grid, size_t smem, cuda
     if (e == cudaSuccess) kernel<<<grid, NW * 32, smem, st>>>(a);
     return e;
 }
-template <typename T>
-cudaError_t launch_norm_bwd(const NormArgs &a, int64_t ppl, dim3 grid, size_t smem, cudaStream_t st) {
+template <typename T, bool GEN>
+cudaError_t launch_norm_bwd_g(const NormArgs &a, int64_t ppl, dim3 grid, size_t smem, cudaStream_t st) {
     static int attr[4][64] = {};
     const size_t ssm = staged_smem<T>(a.G);
-    if (ppl <= 1) return launch_one(k_norm_bwd_staged<T, 1>, a, grid, ssm, st, attr[0]);
-    if (ppl <= 2) return launch_one(k_norm_bwd_staged<T, 2>, a, grid, ssm, st, attr[1]);
-    if (ppl <= 4) return launch_one(k_norm_bwd_staged<T, 4>, a, grid, ssm, st, attr[2]);
+    if (ppl <= 1) return launch_one(k_norm_bwd_staged<T, 1, GEN>, a, grid, ssm, st, attr[0]);
+    if (ppl <= 2) return launch_one(k_norm_bwd_staged<T, 2, GEN>, a, grid, ssm, st, attr[1]);
+    if (ppl <= 4) return launch_one(k_norm_bwd_staged<T, 4, GEN>, a, grid, ssm, st, attr[2]);
     return launch_one(k_norm_bwd<T>, a, grid, smem, st, attr[3]);
+}
+template <typename T>
+cudaError_t launch_norm_bwd(const NormArgs &a, int64_t ppl, dim3 grid, size_t smem, cudaStream_t st) {
+    return (a.ln || a.bg) ? launch_norm_bwd_g<T, true>(a, ppl, grid, smem, st)
+                          : launch_norm_bwd_g<T, false>(a, ppl, grid, smem, st);
+}
+template <typename T, bool GEN>
+void launch_norm_fwd_g(const NormArgs &a, int64_t ppl, int blocks, cudaStream_t st) {
+    if (ppl <= 1) k_norm_fwd_reg<T, 1, GEN><<<blocks, NW * 32, 0, st>>>(a);
+    else if (ppl <= 2) k_norm_fwd_reg<T, 2, GEN><<<blocks, NW * 32, 0, st>>>(a);
+    else if (ppl <= 4) k_norm_fwd_reg<T, 4, GEN><<<blocks, NW * 32, 0, st>>>(a);
+    else k_norm_fwd<T><<<blocks, NW * 32, 0, st>>>(a);
+}
+template <typename T>
+void launch_norm_fwd(const NormArgs &a, int64_t ppl, int blocks, cudaStream_t st) {
+    if (a.ln || a.bg) launch_norm_fwd_g<T, true>(a, ppl, blocks, st);
+    else launch_norm_fwd_g<T, false>(a, ppl, blocks, st);
 }
 
 int sm_count() {
@@ -506,7 +528,8 @@ ssd_status check_norm(const ssd_norm_problem *p, int64_t *chunks) {
     if (p == nullptr) return SSD_ERR_INVALID_ARGUMENT;
     if (p->rows < 0 || p->width < 1 || p->group_size < 1 || p->width % p->group_size != 0)
         return SSD_ERR_INVALID_ARGUMENT;
-    if (!(p->eps >= 0.f) || p->dtype < SSD_F32 || p->dtype > SSD_BF16 || p->reserved != 0)
+    if (!(p->eps >= 0.f) || p->dtype < SSD_F32 || p->dtype > SSD_BF16 ||
+        (p->flags & ~(SSD_NORM_LAYER | SSD_NORM_GATE_AFTER)) != 0)
         return SSD_ERR_INVALID_ARGUMENT;
     if (p->group_size % 8 != 0 || p->group_size > kMaxGroup || p->rows > ((int64_t)1 << 31) ||
         p->width > ((int64_t)1 << 24))
@@ -553,21 +576,13 @@ ssd_status ssd_gated_norm_fwd(const ssd_norm_problem *p, const void *y, int64_t 
     a.rows = p->rows; a.width = p->width; a.G = p->group_size; a.ng = (int)(p->width / p->group_size);
     a.eps = p->eps; a.y = y; a.z = z; a.sy = y_stride; a.sz = z_stride; a.w = weight; a.out = out;
     a.sout = out_stride; a.rstd = rstd;
+    a.ln = (p->flags & SSD_NORM_LAYER) != 0; a.bg = (p->flags & SSD_NORM_GATE_AFTER) != 0;
     const int64_t items = p->rows * a.ng;
     const int blocks = (int)std::min<int64_t>((items + NW - 1) / NW, 8LL * sm_count());
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t ppl = (p->group_size / 8 + 31) / 32;   // pieces per lane
-    if (p->dtype == SSD_BF16) {
-        if (ppl <= 1) k_norm_fwd_reg<__nv_bfloat16, 1><<<blocks, NW * 32, 0, st>>>(a);
-        else if (ppl <= 2) k_norm_fwd_reg<__nv_bfloat16, 2><<<blocks, NW * 32, 0, st>>>(a);
-        else if (ppl <= 4) k_norm_fwd_reg<__nv_bfloat16, 4><<<blocks, NW * 32, 0, st>>>(a);
-        else k_norm_fwd<__nv_bfloat16><<<blocks, NW * 32, 0, st>>>(a);
-    } else {
-        if (ppl <= 1) k_norm_fwd_reg<float, 1><<<blocks, NW * 32, 0, st>>>(a);
-        else if (ppl <= 2) k_norm_fwd_reg<float, 2><<<blocks, NW * 32, 0, st>>>(a);
-        else if (ppl <= 4) k_norm_fwd_reg<float, 4><<<blocks, NW * 32, 0, st>>>(a);
-        else k_norm_fwd<float><<<blocks, NW * 32, 0, st>>>(a);
-    }
+    if (p->dtype == SSD_BF16) launch_norm_fwd<__nv_bfloat16>(a, ppl, blocks, st);
+    else launch_norm_fwd<float>(a, ppl, blocks, st);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
@@ -600,6 +615,7 @@ ssd_status ssd_gated_norm_bwd(const ssd_norm_problem *p, const void *y, int64_t 
     a.eps = p->eps; a.y = y; a.z = z; a.dout = dout; a.sy = y_stride; a.sz = z_stride; a.sdout = dout_stride;
     a.w = weight; a.rstd_in = rstd; a.dy = dy; a.dz = dz; a.sdy = dy_stride; a.sdz = dz_stride;
     a.partials = static_cast<float *>(workspace);
+    a.ln = (p->flags & SSD_NORM_LAYER) != 0; a.bg = (p->flags & SSD_NORM_GATE_AFTER) != 0;
     a.rows_per_chunk = p->rows > 0 ? (p->rows + chunks - 1) / chunks : 1;
     const size_t smem = (size_t)NW * (size_t)p->group_size * sizeof(float);
     const dim3 grid((unsigned)chunks, (unsigned)a.ng);

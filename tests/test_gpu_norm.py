@@ -1,6 +1,7 @@
-"""Gated RMS normalisation over feature groups on the GPU (forward and backward) against
-the float64 oracle: dtypes, with and without the gate, group sizes, strided rows, the full
-Nemotron-Nano width, determinism, and the composition scan -> gated norm of a Mamba-2
+"""Gated normalisation over feature groups on the GPU (forward and backward) against the
+float64 oracle: RMS and LayerNorm, the gate before or after the norm, dtypes, with and
+without the gate, group sizes (register, staged and two-pass kernels), strided rows, the
+full Nemotron-Nano width, determinism, and the composition scan -> gated norm of a Mamba-2
 block."""
 import numpy as np
 import pytest
@@ -42,6 +43,31 @@ def test_gated_norm_matches_oracle(dtype, gate, rows, width, group):
     torch.cuda.synchronize()
     oo, orstd = gn.forward(host(y), host(w), group, z=host(z))
     ody, odz, odw = gn.backward(host(y), host(w), host(dout), group, z=host(z))
+    tol = TOL[dtype]
+    assert rel_l2(host(out), oo) <= tol
+    assert rel_l2(host(rstd), orstd) <= tol
+    assert rel_l2(host(dy), ody) <= tol
+    assert rel_l2(host(dw), odw) <= tol
+    if gate:
+        assert rel_l2(host(dz), odz) <= tol
+
+
+@pytest.mark.parametrize("mode", [dict(layer_norm=True), dict(gate_after=True),
+                                  dict(layer_norm=True, gate_after=True)])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("gate", [True, False])
+@pytest.mark.parametrize("rows,width,group", [(37, 256, 64), (64, 1536, 512), (33, 6144, 6144)])
+def test_gated_norm_modes_match_oracle(mode, dtype, gate, rows, width, group):
+    """LayerNorm and/or the gate after the norm, through every kernel size class; the inputs
+    carry a per-row offset so the LayerNorm mean matters."""
+    y, z, w, dout = tensors(rows, width, dtype, gate, seed=9)
+    y = (y.double() + torch.linspace(-2.0, 3.0, rows, dtype=torch.float64)[:, None]).to(y.dtype)
+    yd, zd, wd, dd = (None if t is None else t.cuda() for t in (y, z, w, dout))
+    out, rstd = gated_norm_forward(yd, wd, group, z=zd, **mode)
+    dy, dz, dw = gated_norm_backward(yd, wd, rstd, dd, group, z=zd, **mode)
+    torch.cuda.synchronize()
+    oo, orstd = gn.forward(host(y), host(w), group, z=host(z), **mode)
+    ody, odz, odw = gn.backward(host(y), host(w), host(dout), group, z=host(z), **mode)
     tol = TOL[dtype]
     assert rel_l2(host(out), oo) <= tol
     assert rel_l2(host(rstd), orstd) <= tol
