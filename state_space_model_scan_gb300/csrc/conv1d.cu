@@ -108,6 +108,9 @@ constexpr int TG = TT / (CT / 32);   // tokens per thread: 8
 constexpr int CTB = 128;             // backward: threads per block (two blocks per SM) ...
 constexpr int TGB = TT / (CTB / 32); // ... and tokens per thread: 16
 #define TAPS_BYTES(K) ((size_t)((K) + 1) * CB * sizeof(float))   // staged taps and bias
+#ifndef CONV_BWD_W
+#define CONV_BWD_W 4
+#endif
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
@@ -143,6 +146,48 @@ __device__ __forceinline__ void stage_rows(const T *src, int64_t sl, int64_t tb,
 
 template <typename T>
 __device__ __forceinline__ void lds8(const T *p, float *v) { ld8(p, v); }
+// 4 channels: 8 bytes (bf16) or 16 bytes (fp32)
+__device__ __forceinline__ void ld4(const __nv_bfloat16 *p, float *v) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+__device__ __forceinline__ void ld4(const float *p, float *v) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void st4(__nv_bfloat16 *p, const float *v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&a);
+    u.y = *reinterpret_cast<const uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+__device__ __forceinline__ void st4(float *p, const float *v) {
+    *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+// 2 channels: 4 bytes (bf16) or 8 bytes (fp32)
+__device__ __forceinline__ void ld2(const __nv_bfloat16 *p, float *v) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+    v[0] = a.x; v[1] = a.y;
+}
+__device__ __forceinline__ void ld2(const float *p, float *v) {
+    const float2 a = *reinterpret_cast<const float2 *>(p);
+    v[0] = a.x; v[1] = a.y;
+}
+__device__ __forceinline__ void st2(__nv_bfloat16 *p, const float *v) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(v[0], v[1]);
+}
+__device__ __forceinline__ void st2(float *p, const float *v) { *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]); }
+template <int W, typename T>
+__device__ __forceinline__ void ldw(const T *p, float *v) {
+    if (W == 8) ld8(p, v); else if (W == 4) ld4(p, v); else ld2(p, v);
+}
+template <int W, typename T>
+__device__ __forceinline__ void stw(T *p, const float *v) {
+    if (W == 8) st8(p, v); else if (W == 4) st4(p, v); else st2(p, v);
+}
 
 // logistic function with the fast exponential and divide (relative error ~1e-6; 1/inf = 0
 // gives the right limit for very negative arguments)
@@ -232,17 +277,19 @@ k_conv_fwd(const ConvArgs a) {
 // g[t] = dout[t] act'(pre[t]); g[t] reaches du[t - (K-1) + k] (same sequence) for every k;
 // du[t'] is complete once t passes t' + K - 1 and leaves then.  dw and dbias take the thread's
 // tokens t in [s0, s1); the eight token groups' shares are summed in order in shared memory.
-template <typename T, int K>
-__global__ void __launch_bounds__(CTB)
+template <typename T, int K, int W>   // W channels per thread (8: 128 threads, 4: 256 threads)
+__global__ void __launch_bounds__(CTB * 8 / W)
 k_conv_bwd(const ConvArgs a) {
+    constexpr int NPC = CB / W;        // channel pieces per row
+    constexpr int NT = NPC * (TT / TGB);
     extern __shared__ __align__(16) uint8_t conv_sm[];
     constexpr int RU = TT + 2 * (K - 1), RD = TT + K - 1;
     float *ws = reinterpret_cast<float *>(conv_sm);                    // taps [K][CB], bias [CB]
     T *tu = reinterpret_cast<T *>(conv_sm + TAPS_BYTES(K));            // u rows t0-(K-1) .. t0+TT+K-2
     T *td = tu + RU * 256;                                             // dout rows t0 .. t0+TT+K-2
     float *red = reinterpret_cast<float *>(conv_sm + TAPS_BYTES(K));   // after the sweep: [group][K+1][256]
-    const int j = threadIdx.x & 31, grp = threadIdx.x >> 5;
-    const int64_t cbase = (int64_t)blockIdx.y * CB, c0 = cbase + 8 * j;
+    const int j = threadIdx.x % NPC, grp = threadIdx.x / NPC;
+    const int64_t cbase = (int64_t)blockIdx.y * CB, c0 = cbase + W * j;
     const int64_t b = blockIdx.x / a.tiles_per_row, t0 = (blockIdx.x % a.tiles_per_row) * TT;
     const int64_t tb = t0 - (K - 1);
     stage_taps<K>(a.w, a.bias, cbase, a.Cn, ws);
@@ -251,32 +298,37 @@ k_conv_bwd(const ConvArgs a) {
     __syncthreads();
     const bool live = c0 < a.Cn;
     const int64_t s0 = t0 + (int64_t)grp * TGB, s1 = std::min(a.L, s0 + TGB);
-    float w[K][8], bias[8], dw[K][8], db[8];
-    read_taps<K>(ws, j, w, bias);
+    float w[K][W], bias[W], dw[K][W], db[W];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int k = 0; k <= K; ++k) {   // the thread's W channels of tap k (k = K: the bias)
+        float *dst = k < K ? w[k < K ? k : 0] : bias;
+#pragma unroll
+        for (int e = 0; e < W; ++e) dst[e] = ws[k * CB + W * j + e];
+    }
+#pragma unroll
+    for (int e = 0; e < W; ++e) {
         db[e] = 0.f;
 #pragma unroll
         for (int k = 0; k < K; ++k) dw[k][e] = 0.f;
     }
     if (live && s0 < s1) {
         T *du = static_cast<T *>(a.du) + b * a.sdu_b + c0;
-        const T *ucol = tu + 8 * j, *dcol = td + 8 * j;
+        const T *ucol = tu + W * j, *dcol = td + W * j;
         SeqCursor cur;
         cur.init(a, s0);
-        float ring[K][8];   // inputs u[t - (K-1) + k]
-        float acc[K][8];    // du[t - (K-1) + k] being summed
+        float ring[K][W];   // inputs u[t - (K-1) + k]
+        float acc[K][W];    // du[t - (K-1) + k] being summed
 #pragma unroll
         for (int k = 0; k < K; ++k)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
+            for (int e = 0; e < W; ++e) acc[k][e] = 0.f;
 #pragma unroll
         for (int k = 0; k < K - 1; ++k) {
             const int64_t tp = s0 - (K - 1) + k;
-            if (tp >= cur.start) lds8(ucol + (int)(tp - tb) * 256, ring[k]);
+            if (tp >= cur.start) ldw<W>(ucol + (int)(tp - tb) * 256, ring[k]);
             else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ring[k][e] = 0.f;
+                for (int e = 0; e < W; ++e) ring[k][e] = 0.f;
             }
         }
         const int64_t tend = std::min(a.L, s1 + K - 1);
@@ -285,14 +337,14 @@ k_conv_bwd(const ConvArgs a) {
 #pragma unroll
                 for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) ring[k][e] = 0.f;
+                    for (int e = 0; e < W; ++e) ring[k][e] = 0.f;
             }
-            lds8(ucol + (int)(t - tb) * 256, ring[K - 1]);
-            float dv[8];
-            lds8(dcol + (int)(t - t0) * 256, dv);
-            float g[8];
+            ldw<W>(ucol + (int)(t - tb) * 256, ring[K - 1]);
+            float dv[W];
+            ldw<W>(dcol + (int)(t - t0) * 256, dv);
+            float g[W];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+            for (int e = 0; e < W; ++e) {
                 float pre = bias[e];
 #pragma unroll
                 for (int k = 0; k < K; ++k) pre = fmaf(w[k][e], ring[k][e], pre);
@@ -309,7 +361,7 @@ k_conv_bwd(const ConvArgs a) {
                 const int64_t tp = t - (K - 1) + k;
                 if (tp >= cur.start) {   // u[tp] fed pre[t] (same sequence)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
+                    for (int e = 0; e < W; ++e) {
                         acc[k][e] = fmaf(w[k][e], g[e], acc[k][e]);
                         if (own) dw[k][e] = fmaf(g[e], ring[k][e], dw[k][e]);
                     }
@@ -317,46 +369,46 @@ k_conv_bwd(const ConvArgs a) {
             }
             if (own) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) db[e] += g[e];
+                for (int e = 0; e < W; ++e) db[e] += g[e];
             }
             const int64_t tdone = t - (K - 1);   // du[tdone] has all its contributions now
-            if (tdone >= s0 && tdone < s1) st8(du + tdone * a.sdu_l, acc[0]);
+            if (tdone >= s0 && tdone < s1) stw<W>(du + tdone * a.sdu_l, acc[0]);
 #pragma unroll
             for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < W; ++e) {
                     ring[k][e] = ring[k + 1][e];
                     acc[k][e] = acc[k + 1][e];
                 }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[K - 1][e] = 0.f;
+            for (int e = 0; e < W; ++e) acc[K - 1][e] = 0.f;
         }
         // the last rows, whose windows would run past the end of the row: acc[0] now holds
         // du[tend - (K-1)]; rows before s0 are skipped over
         for (int64_t tdone = tend - (K - 1); tdone < s1; ++tdone) {
-            if (tdone >= s0) st8(du + tdone * a.sdu_l, acc[0]);
+            if (tdone >= s0) stw<W>(du + tdone * a.sdu_l, acc[0]);
 #pragma unroll
             for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[k][e] = acc[k + 1][e];
+                for (int e = 0; e < W; ++e) acc[k][e] = acc[k + 1][e];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[K - 1][e] = 0.f;
+            for (int e = 0; e < W; ++e) acc[K - 1][e] = 0.f;
         }
     }
     __syncthreads();   // the staged tiles are no longer read: reuse them for the group sums
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+    for (int e = 0; e < W; ++e) {
 #pragma unroll
-        for (int k = 0; k < K; ++k) red[((grp * (K + 1)) + k) * 256 + 8 * j + e] = dw[k][e];
-        red[((grp * (K + 1)) + K) * 256 + 8 * j + e] = db[e];
+        for (int k = 0; k < K; ++k) red[((grp * (K + 1)) + k) * 256 + W * j + e] = dw[k][e];
+        red[((grp * (K + 1)) + K) * 256 + W * j + e] = db[e];
     }
     __syncthreads();
     float *pp = a.partials + (int64_t)blockIdx.x * a.Cn * (K + 1);
-    for (int i = threadIdx.x; i < 256 * (K + 1); i += CTB) {
+    for (int i = threadIdx.x; i < 256 * (K + 1); i += NT) {
         const int c = i / (K + 1), k = i % (K + 1);   // channel within the block, tap (K: bias)
         if (cbase + c >= a.Cn) continue;
         float sum = 0.f;
-        for (int q = 0; q < CTB / 32; ++q) sum += red[(q * (K + 1) + k) * 256 + c];
+        for (int q = 0; q < TT / TGB; ++q) sum += red[(q * (K + 1) + k) * 256 + c];
         pp[(cbase + c) * (K + 1) + k] = sum;
     }
 }
@@ -378,7 +430,7 @@ size_t fwd_smem() { return TAPS_BYTES(K) + (size_t)(TT + K - 1) * 256 * sizeof(T
 template <typename T, int K>
 size_t bwd_smem() {
     const size_t stage = (size_t)(2 * TT + 3 * (K - 1)) * 256 * sizeof(T);
-    const size_t red = (size_t)(CTB / 32) * (K + 1) * 256 * sizeof(float);
+    const size_t red = (size_t)(TT / TGB) * (K + 1) * 256 * sizeof(float);
     return TAPS_BYTES(K) + (stage > red ? stage : red);
 }
 template <typename T, int K>
@@ -390,13 +442,14 @@ cudaError_t launch_fwd_k(const ConvArgs &a, dim3 grid, cudaStream_t st) {
     k_conv_fwd<T, K><<<grid, CT, sm, st>>>(a);
     return cudaGetLastError();
 }
+constexpr int kBwdW = CONV_BWD_W;   // channels per thread of the backward sweep
 template <typename T, int K>
 cudaError_t launch_bwd_k(const ConvArgs &a, dim3 grid, cudaStream_t st) {
     static int attr[64] = {0};
     const size_t sm = bwd_smem<T, K>();
-    cudaError_t e = ensure_smem_attr(k_conv_bwd<T, K>, (int)sm, attr);
+    cudaError_t e = ensure_smem_attr(k_conv_bwd<T, K, kBwdW>, (int)sm, attr);
     if (e != cudaSuccess) return e;
-    k_conv_bwd<T, K><<<grid, CTB, sm, st>>>(a);
+    k_conv_bwd<T, K, kBwdW><<<grid, CTB * 8 / kBwdW, sm, st>>>(a);
     return cudaGetLastError();
 }
 
