@@ -97,12 +97,12 @@ struct SeqCursor {
     }
 };
 
-// ---- staged sweeps.  A block covers TT tokens x CB channels (32 pieces of 8); its threads
-// first copy the tile (plus the K-1 rows before it, and for the backward after it) into
-// shared memory with cp.async -- a whole tile of loads in flight at once -- and then thread
-// (piece j, token group g) sweeps its 8 channels over TG = 8 tokens (forward, 256 threads) or
-// TGB = 16 tokens (backward, 128 threads: its larger per-thread state allows two blocks per
-// SM only at that size) from shared memory.
+// ---- staged sweeps.  A block covers TT tokens x CB channels; its threads first copy the tile
+// (plus the K-1 rows before it, and for the backward after it) into shared memory with
+// cp.async -- a whole tile of loads in flight at once -- and then thread (piece j, token group
+// g) sweeps its W channels over TG = 8 tokens (forward: W = 8, 256 threads) or TGB = 16 tokens
+// (backward: W = 4, 256 threads, about 110 registers, two blocks per SM) from shared memory.
+// (Measured: a forward with W = 4 is a third slower; a backward with W = 8 or 2 a tenth.)
 constexpr int CB = 256;              // channels per block (32 pieces of 8)
 constexpr int TG = TT / (CT / 32);   // tokens per thread: 8
 constexpr int CTB = 128;             // backward: threads per block (two blocks per SM) ...
@@ -110,6 +110,9 @@ constexpr int TGB = TT / (CTB / 32); // ... and tokens per thread: 16
 #define TAPS_BYTES(K) ((size_t)((K) + 1) * CB * sizeof(float))   // staged taps and bias
 #ifndef CONV_BWD_W
 #define CONV_BWD_W 4
+#endif
+#ifndef CONV_FWD_W
+#define CONV_FWD_W 8
 #endif
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
@@ -216,26 +219,16 @@ __device__ __forceinline__ void stage_taps(const float *w, const float *bias, in
     for (int c = threadIdx.x; c < CB; c += blockDim.x)
         ws[K * CB + c] = (bias != nullptr && c < nch) ? bias[cbase + c] : 0.f;
 }
-template <int K>
-__device__ __forceinline__ void read_taps(const float *ws, int j, float (&wt)[K][8], float (&bs)[8]) {
-#pragma unroll
-    for (int k = 0; k <= K; ++k) {
-        const float4 lo = reinterpret_cast<const float4 *>(ws + k * CB + 8 * j)[0];
-        const float4 hi = reinterpret_cast<const float4 *>(ws + k * CB + 8 * j)[1];
-        float *dst = k < K ? wt[k < K ? k : 0] : bs;
-        dst[0] = lo.x; dst[1] = lo.y; dst[2] = lo.z; dst[3] = lo.w;
-        dst[4] = hi.x; dst[5] = hi.y; dst[6] = hi.z; dst[7] = hi.w;
-    }
-}
 
-template <typename T, int K>
-__global__ void __launch_bounds__(CT)
+template <typename T, int K, int W>   // W channels per thread (8: 256 threads, 4: 512 threads)
+__global__ void __launch_bounds__(CT * 8 / W)
 k_conv_fwd(const ConvArgs a) {
+    constexpr int NPC = CB / W;        // channel pieces per row
     extern __shared__ __align__(16) uint8_t conv_sm[];
     float *ws = reinterpret_cast<float *>(conv_sm);                  // taps [K][CB], bias [CB]
     T *tile = reinterpret_cast<T *>(conv_sm + TAPS_BYTES(K));        // rows t0-(K-1) .. t0+TT-1
-    const int j = threadIdx.x & 31, grp = threadIdx.x >> 5;
-    const int64_t cbase = (int64_t)blockIdx.y * CB, c0 = cbase + 8 * j;
+    const int j = threadIdx.x % NPC, grp = threadIdx.x / NPC;
+    const int64_t cbase = (int64_t)blockIdx.y * CB, c0 = cbase + W * j;
     const int64_t b = blockIdx.x / a.tiles_per_row, t0 = (blockIdx.x % a.tiles_per_row) * TT;
     const int64_t tb = t0 - (K - 1);
     stage_taps<K>(a.w, a.bias, cbase, a.Cn, ws);
@@ -245,31 +238,36 @@ k_conv_fwd(const ConvArgs a) {
     const int64_t s0 = t0 + (int64_t)grp * TG, s1 = std::min(a.L, s0 + TG);   // this thread's tokens
     if (s0 >= s1) return;
     T *o = static_cast<T *>(a.out) + b * a.so_b + c0;
-    float w[K][8], bias[8];
-    read_taps<K>(ws, j, w, bias);
+    float w[K][W], bias[W];
+#pragma unroll
+    for (int k = 0; k <= K; ++k) {   // the thread's W channels of tap k (k = K: the bias)
+        float *dst = k < K ? w[k < K ? k : 0] : bias;
+#pragma unroll
+        for (int e = 0; e < W; ++e) dst[e] = ws[k * CB + W * j + e];
+    }
     SeqCursor cur;
     cur.init(a, s0);
-    const T *col = tile + 8 * j;   // row t at (t - tb) * 256 (offsets below fit 32 bits)
+    const T *col = tile + W * j;   // row t at (t - tb) * 256 (offsets below fit 32 bits)
     for (int64_t t = s0; t < s1; ++t) {
         cur.advance(a, t);
-        float acc[8];
+        float acc[W];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = bias[e];
+        for (int e = 0; e < W; ++e) acc[e] = bias[e];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const int64_t tp = t - (K - 1) + k;   // u[tp] feeds pre[t] when in t's sequence
             if (tp >= cur.start) {
-                float v[8];
-                lds8(col + (int)(tp - tb) * 256, v);
+                float v[W];
+                ldw<W>(col + (int)(tp - tb) * 256, v);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaf(w[k][e], v[e], acc[e]);
+                for (int e = 0; e < W; ++e) acc[e] = fmaf(w[k][e], v[e], acc[e]);
             }
         }
         if (a.silu) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] *= sig_t<T>(acc[e]);
+            for (int e = 0; e < W; ++e) acc[e] *= sig_t<T>(acc[e]);
         }
-        st8(o + t * a.so_l, acc);
+        stw<W>(o + t * a.so_l, acc);
     }
 }
 
@@ -433,13 +431,14 @@ size_t bwd_smem() {
     const size_t red = (size_t)(TT / TGB) * (K + 1) * 256 * sizeof(float);
     return TAPS_BYTES(K) + (stage > red ? stage : red);
 }
+constexpr int kFwdW = CONV_FWD_W;   // channels per thread of the forward sweep
 template <typename T, int K>
 cudaError_t launch_fwd_k(const ConvArgs &a, dim3 grid, cudaStream_t st) {
     static int attr[64] = {0};
     const size_t sm = fwd_smem<T, K>();
-    cudaError_t e = ensure_smem_attr(k_conv_fwd<T, K>, (int)sm, attr);
+    cudaError_t e = ensure_smem_attr(k_conv_fwd<T, K, kFwdW>, (int)sm, attr);
     if (e != cudaSuccess) return e;
-    k_conv_fwd<T, K><<<grid, CT, sm, st>>>(a);
+    k_conv_fwd<T, K, kFwdW><<<grid, CT * 8 / kFwdW, sm, st>>>(a);
     return cudaGetLastError();
 }
 constexpr int kBwdW = CONV_BWD_W;   // channels per thread of the backward sweep
