@@ -90,9 +90,10 @@ typedef enum {
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
 /* Which forward/backward pipeline to run.  AUTO takes the tensor-core path (its single-pass
- * forward) when chunk_size == 128 and the inputs are bf16 with headdim == 64 and dstate 128
- * or 64 (the compiled tile set is dstate 128; dstate 64 runs as its zero-extended half, the
- * cuDNN frontend Mamba-2 engine's headdim = dstate = 64 shape; tensors that break the
+ * forward) when chunk_size == 128 and the inputs are bf16 with headdim == 64 and dstate 128,
+ * 64, 32 or 16 (the compiled tile set is dstate 128; a smaller dstate runs as its
+ * zero-extended part -- dstate 64 is the cuDNN frontend Mamba-2 engine's headdim = dstate =
+ * 64 shape; tensors that break the
  * 16-byte rule then return SSD_ERR_MISALIGNED), and the SIMT path otherwise (f32 inputs
  * always take SIMT: fp32 inputs are computed in fp32 FMA, never in tf32).  The chunk length
  * is never replaced: the SIMT forward computes chunk_size 32, 64, 128 or 256, the SIMT

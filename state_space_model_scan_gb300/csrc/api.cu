@@ -240,7 +240,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     // dstate 128 whose x/B/C/z/y obey the 16-byte rule of TMA and vector access;
     // everything else (fp32 inputs in particular) runs the SIMT pipeline.  The
     // backward follows the same choice, with dy/dx/dz/dB/dC under the same rule.
-    bool tc_ok = pl.bf16 && P == 64 && (N == 128 || N == 64);
+    bool tc_ok = pl.bf16 && P == 64 && N <= 128;   // N < 128: the zero-extended tiles (below)
     bool aligned = true;
     {
         const ssd_tensor *ts[10] = {&a->x, &a->B, &a->C, &a->z, bwd ? nullptr : &a->y, b ? &b->dy : nullptr,
@@ -281,8 +281,8 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
         if (((uintptr_t)a->chunk_states) % 16 != 0) return SSD_ERR_MISALIGNED;
     }
     const int Q = fused ? kTcQ : (int)p->chunk_size;
-    // dstate the kernels compute: the tensor-core tiles are N = 128; dstate 64 runs as the zero-
-    // extended half (TMA fills the B/C columns past 64 with zeros; states are padded copies)
+    // dstate the kernels compute: the tensor-core tiles are N = 128; a smaller dstate runs as the
+    // zero-extended tile (TMA fills the B/C columns past it with zeros; states are padded copies)
     const int64_t Nk = fused ? 128 : N;
     if (fused && bwd && b == nullptr) return SSD_ERR_INVALID_ARGUMENT;
     int64_t kmax = varlen ? (L + Q - 1) / Q + S : B * ((L + Q - 1) / Q);

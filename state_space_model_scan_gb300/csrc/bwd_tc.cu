@@ -921,15 +921,17 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
     {
         auto store_bf16 = [&](int which, const float *v) {
-            if (!live || 64 * hf >= p.sh.Nio) return;   // columns the caller's dB/dC hold
+            const int ncols = p.sh.Nio - 64 * hf;   // of this half's 64 columns, those the caller's dB/dC hold
+            if (!live || ncols <= 0) return;
             __nv_bfloat16 *dst = (which == 0 ? p.dB : p.dC) + (int64_t)ci.b * (which == 0 ? p.sdBb : p.sdCb) +
                                  tok * (which == 0 ? p.sdBl : p.sdCl) + (int64_t)g * (which == 0 ? p.sdBg : p.sdCg) +
                                  64 * hf;
             uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-                d4[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
-                                   pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+                if (8 * q < ncols)
+                    d4[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                                       pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
         };
 #pragma unroll
         for (int which = 0; which < 2; ++which) {

@@ -132,7 +132,7 @@ def test_validation_codes(lib, mutate, code):
     (64, 128, False, 128, "auto", True, 0, 128),    # fp32 inputs run SIMT (here at 128)
     (64, 64, True, 128, "auto", True, 0, 128),      # dstate 64: the tensor-core tiles' zero-extended half
     (64, 64, True, 128, "split", True, 0, 128),
-    (64, 32, True, 128, "auto", True, 0, 128),      # other dstates: SIMT
+    (64, 32, True, 128, "auto", True, 0, 128),      # dstate 32: the zero-extended tensor-core tiles too
     (64, 32, True, 64, "auto", True, 0, 64),
 ])
 def test_chunk_size_is_honoured(lib, P, N, bf16, Q, algo, aligned, code, qi):

@@ -1,6 +1,7 @@
-"""dstate 64 (headdim 64, bf16) on the tensor-core path: the N = 128 tiles compute it as their
-zero-extended half (TMA fills B/C past column 64 with zeros; the states are padded copies), so
-the results are those of the N = 64 problem.  Forward (single-pass and split), packed
+"""dstate 64, 32 and 16 (headdim 64, bf16) on the tensor-core path: the N = 128 tiles compute
+them as their zero-extended part (TMA fills B/C past the caller's dstate with zeros; the states
+are padded copies; dB/dC stores are clipped to the caller's columns), so the results are those
+of the smaller problem.  Forward (single-pass and split), packed
 sequences, kept chunk states, backward (whole-group items and head subsets), bf16 states,
 against the float64 oracle."""
 import pytest
@@ -14,14 +15,14 @@ from helpers import TOL, rel_l2, gpu_forward, gpu_backward, oracle_forward, orac
 pytestmark = pytest.mark.gpu
 
 
-def W(B=1, L=700, H=8, G=2, **kw):
+def W(B=1, L=700, H=8, G=2, N=64, **kw):
     kw.setdefault("has_init", True)
-    return I.Workload("n64", B, L, H, 64, G, 64, 128, "bf16", **kw)
+    return I.Workload("n%d" % N, B, L, H, 64, G, N, 128, "bf16", **kw)
 
 
 def on_tensor_cores(w, inp):
     d = to_dev(inp)
-    prob = _lib.problem(w.batch, w.seqlen, w.nheads, 64, w.ngroups, 64, 128,
+    prob = _lib.problem(w.batch, w.seqlen, w.nheads, 64, w.ngroups, w.dstate, 128,
                         w.nseqs if d["cu_seqlens"] is not None else 0)
     y = torch.empty_like(d["x"])
     args = _lib.fwd_args(d["x"], d["dt_raw"], d["A"], d["B"], d["C"], y, D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
@@ -29,10 +30,11 @@ def on_tensor_cores(w, inp):
     return _lib.chunk_states_size(prob, args) > 0   # the tensor-core path's kept-state format only
 
 
+@pytest.mark.parametrize("N", [64, 32, 16])
 @pytest.mark.parametrize("algo", ["auto", "split"])
 @pytest.mark.parametrize("B,L,lens", [(2, 700, None), (1, 0, [130, 0, 300, 1, 269])])
-def test_n64_forward(algo, B, L, lens):
-    w = W(B=B, L=sum(lens) if lens else L, seqlens=lens)
+def test_n64_forward(algo, B, L, lens, N):
+    w = W(B=B, L=sum(lens) if lens else L, seqlens=lens, N=N)
     inp = I.make_inputs(w)
     assert on_tensor_cores(w, inp)
     y, fin = gpu_forward(w, inp, algo=algo)
@@ -41,10 +43,11 @@ def test_n64_forward(algo, B, L, lens):
     assert rel_l2(fin.double().cpu().numpy(), fo) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("N", [64, 32, 16])
 @pytest.mark.parametrize("H,G", [(8, 2), (16, 1)])   # 4 heads per group; 16 (head subsets + reduction)
 @pytest.mark.parametrize("kept", [False, True])
-def test_n64_backward(H, G, kept):
-    w = W(B=1, L=520, H=H, G=G, has_z=True)
+def test_n64_backward(H, G, kept, N):
+    w = W(B=1, L=520, H=H, G=G, has_z=True, N=N)
     inp = I.make_inputs(w, with_grad_inputs=True, with_dfinal=True)
     kw = {}
     if kept:
