@@ -31,8 +31,9 @@
 // the other's groups through shared memory; the lower half passes Im Yraw to the upper half,
 // which writes y.  Batch 2's two chains are committed separately, so the real outputs are
 // written while the imaginary chain runs.  MMAs (K = 128: 16 of K = 8 each): 16 of M = 128,
-// N = 128 and 32 of M = 128, N = 64 per chunk.  Positions past the end of the sequence read
-// as zero (TMA bounds fill) and carry no decay.
+// N = 128 and 32 of M = 128, N = 64 per chunk.  Operands are written as fp32; the tensor cores
+// read their tf32 part (10 mantissa bits, truncated).  Positions past the end of the sequence
+// read as zero (TMA bounds fill) and carry no decay.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -109,11 +110,6 @@ __device__ __forceinline__ uint32_t elem_off(int r, int k) {
 __device__ __forceinline__ uint32_t elem_off128(int r, int k) {
     return (uint32_t)(k >> 5) * ATOM128 + (uint32_t)r * 128u + ((uint32_t)(((k & 31) >> 2) ^ (r & 7)) << 4) +
            (uint32_t)(k & 3) * 4u;
-}
-__device__ __forceinline__ float tf32r(float v) {   // round to the tf32 grid (nearest, ties away)
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-    return __uint_as_float(r);
 }
 __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
     return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
@@ -271,8 +267,8 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
         for (int i = tid; i < (int)(SLOT / 16); i += CX_THREADS) {
             float4 *cp = reinterpret_cast<float4 *>(CC + (i >> 9) * ATOM128) + (i & 511);
             const float4 cv = *cp;
-            *cp = make_float4(tf32r(cv.x), tf32r(-cv.y), tf32r(cv.z), tf32r(-cv.w));
-            cp[ATOM / 16] = make_float4(tf32r(cv.y), tf32r(cv.x), tf32r(cv.w), tf32r(cv.z));
+            *cp = make_float4(cv.x, -cv.y, cv.z, -cv.w);
+            cp[ATOM / 16] = make_float4(cv.y, cv.x, cv.w, cv.z);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -294,8 +290,8 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
             for (int i = 0; i < 4; ++i) {
                 const int d0 = 2 * ((warp >> 1) + 8 * i);
                 const float4 v = *reinterpret_cast<const float4 *>(XT + elem_off(s, 2 * d0));
-                st_pair(XC, d0, 2 * s, tf32r(v.x), tf32r(-v.y));
-                st_pair(XC, d0 + 1, 2 * s, tf32r(v.z), tf32r(-v.w));
+                st_pair(XC, d0, 2 * s, v.x, -v.y);
+                st_pair(XC, d0 + 1, 2 * s, v.z, -v.w);
             }
         }
         if (tid == 0) {
@@ -331,8 +327,8 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                 const int n0 = 2 * (sub + 4 * i);
                 const float4 bv = *reinterpret_cast<const float4 *>(BS + elem_off128(l, 2 * n0));
                 const float2 v0 = cmul(wl, make_float2(bv.x, bv.y)), v1 = cmul(wl, make_float2(bv.z, bv.w));
-                *reinterpret_cast<float2 *>(CC + elem_off128(64 + n0, 2 * l)) = make_float2(tf32r(v0.x), tf32r(v0.y));
-                *reinterpret_cast<float2 *>(CC + elem_off128(65 + n0, 2 * l)) = make_float2(tf32r(v1.x), tf32r(v1.y));
+                *reinterpret_cast<float2 *>(CC + elem_off128(64 + n0, 2 * l)) = make_float2(v0.x, v0.y);
+                *reinterpret_cast<float2 *>(CC + elem_off128(65 + n0, 2 * l)) = make_float2(v1.x, v1.y);
             }
         }
         __syncthreads();
@@ -356,8 +352,8 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                     const float2 ph = make_float2(rl.x * rs.x + rl.y * rs.y, rl.y * rs.x - rl.x * rs.y);
                     m = cmul(make_float2(mag * ph.x, mag * ph.y), cb);
                 }
-                out[2 * j] = tf32r(m.x);
-                out[2 * j + 1] = tf32r(m.y);
+                out[2 * j] = m.x;
+                out[2 * j + 1] = m.y;
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -371,8 +367,8 @@ k_complex_fwd(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ C
                 const int i = upper ? i0 : i0 + 4;
                 const int d0 = 2 * (sub + 4 * i);
                 const float4 v = *reinterpret_cast<const float4 *>(XT + elem_off(s, 2 * d0));
-                *reinterpret_cast<float2 *>(BS + elem_off128(d0, 2 * s)) = make_float2(tf32r(v.y), tf32r(v.x));
-                *reinterpret_cast<float2 *>(BS + elem_off128(d0 + 1, 2 * s)) = make_float2(tf32r(v.w), tf32r(v.z));
+                *reinterpret_cast<float2 *>(BS + elem_off128(d0, 2 * s)) = make_float2(v.y, v.x);
+                *reinterpret_cast<float2 *>(BS + elem_off128(d0 + 1, 2 * s)) = make_float2(v.w, v.z);
             }
         }
         fence_proxy_async_smem();

@@ -1,10 +1,10 @@
 """Complex-A SSD forward (tensor cores, tf32) against the complex128 oracle walk.
 
 Tolerance: rel-L2 <= 5e-3 per output.  The contractions take tf32 operands (10-bit
-mantissa: 2^-11 relative rounding for the rounded operands, 2^-10 for the as-loaded C
-tile), three chained contractions (C B^T, then (L o Cb) X, and C S^T through the carried
-state) give a few times 2^-10 ~ 1e-3 in the worst direction; the carried state, the decays
-and the accumulation are fp32."""
+mantissa, truncated: up to 2^-10 relative per operand, biased towards zero), three chained
+contractions (C B^T, then (L o Cb) X, and C S^T through the carried state) give a few times
+2^-10 ~ 1e-3 in the worst direction (measured 1.5e-3); the carried state, the decays and the
+accumulation are fp32."""
 import numpy as np
 import pytest
 import torch
