@@ -165,11 +165,12 @@ __device__ __forceinline__ float block_scan256(float v, float *wsum, float *tota
     return x + off;
 }
 
-// In one pass over the block (fixed order): *vrev = the sum of v over this position and all
-// later ones (reverse inclusive scan), *uexcl = the sum of u over all earlier positions
-// (exclusive scan).  Both are formed directly, never as a total minus a prefix, so a large
-// term never has to cancel against itself.  wsum holds 16 floats.
-__device__ __forceinline__ void block_rev_excl_scan(float v, float u, float *wsum, float *vrev, float *uexcl) {
+// Over threads 0..127 (four warps, named barrier 2), in one pass and a fixed order: *vrev =
+// the sum of v over this position and all later ones (reverse inclusive scan), *uexcl = the
+// sum of u over all earlier positions (exclusive scan).  Both are formed directly, never as a
+// total minus a prefix, so a large term never has to cancel against itself.  wsum holds 8
+// floats and must not be rewritten before every participant has read it.
+__device__ __forceinline__ void rev_excl_scan128(float v, float u, float *wsum, float *vrev, float *uexcl) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     float x = v;
 #pragma unroll
@@ -181,15 +182,14 @@ __device__ __forceinline__ void block_rev_excl_scan(float v, float u, float *wsu
     float ye = __shfl_up_sync(0xffffffffu, y, 1);
     if (lane == 0) ye = 0.f;
     if (lane == 0) wsum[w] = x;          // warp total of v
-    if (lane == 31) wsum[8 + w] = y;     // warp total of u
-    __syncthreads();
+    if (lane == 31) wsum[4 + w] = y;     // warp total of u
+    asm volatile("bar.sync 2, 128;" ::: "memory");
     float offv = 0.f, offu = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
         if (i > w) offv += wsum[i];
-        if (i < w) offu += wsum[8 + i];
+        if (i < w) offu += wsum[4 + i];
     }
-    __syncthreads();
     *vrev = x + offv;
     *uexcl = ye + offu;
 }
@@ -450,16 +450,17 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         if (has_z) tma_load_4d(sm + O_E + X_BYTES, &tmZ, &bar[3], 0, h, w.ci.t0, w.ci.b);
         bulk_load(sm + O_WX, src, S_BYTES, &bar[3]);
     };
-    auto issue_first = [&](const Item &w) {   // B/C and the first head's inputs (one thread issues)
-        if (tid == 0) {
-            mbar_expect_tx(&bar[0], 2 * BC_BYTES);
-            tma_load_4d(sm + O_B, &tmB, &bar[0], 0, w.g, w.ci.t0, w.ci.b);
-            tma_load_4d(sm + O_B + BC_BYTES / 2, &tmB, &bar[0], 64, w.g, w.ci.t0, w.ci.b);
-            tma_load_4d(sm + O_C, &tmC, &bar[0], 0, w.g, w.ci.t0, w.ci.b);
-            tma_load_4d(sm + O_C + BC_BYTES / 2, &tmC, &bar[0], 64, w.g, w.ci.t0, w.ci.b);
-            stage_head(w, w.h0);
-            load_head(w, w.h0);
-        }
+    auto load_first = [&](const Item &w) {   // one thread: B/C and the first head's inputs of an item
+        mbar_expect_tx(&bar[0], 2 * BC_BYTES);
+        tma_load_4d(sm + O_B, &tmB, &bar[0], 0, w.g, w.ci.t0, w.ci.b);
+        tma_load_4d(sm + O_B + BC_BYTES / 2, &tmB, &bar[0], 64, w.g, w.ci.t0, w.ci.b);
+        tma_load_4d(sm + O_C, &tmC, &bar[0], 0, w.g, w.ci.t0, w.ci.b);
+        tma_load_4d(sm + O_C + BC_BYTES / 2, &tmC, &bar[0], 64, w.g, w.ci.t0, w.ci.b);
+        stage_head(w, w.h0);
+        load_head(w, w.h0);
+    };
+    auto issue_first = [&](const Item &w) {   // the same, issued by thread 0, counted by all
+        if (tid == 0) load_first(w);
         ++bc_issued;
         ++st_issued;
         ++ld_issued;
@@ -835,25 +836,33 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             const float w = warp_sum(t3p);
             if (lane == 0) fm[F_RED + warp] = w;
         }
-        wait_mma2();   // the dB/dC chains are done: no MMA reads smem now
-        __syncthreads();
-        // B, C, E', w o x, dS, x and S_in are free: fetch the next head's inputs (or the next
-        // item's B/C and first-head inputs)
+        __syncthreads();   // the row sums and T3 shares are visible; every thread has read x and e o dyp
+        // Thread 128 waits for the dB/dC chains (the last MMAs reading shared memory) and at once
+        // fetches the next head's inputs (or the next item's B/C and first-head inputs, nxt having
+        // been decoded during this head) into the freed tiles, while threads 0..127 compute the
+        // per-position scalars.
         if (hi + 1 < HS) {
-            if (tid == 0) {
+            if (tid == 128) {
+                if (!mbar_wait(&bar[4], mma2_phase & 1)) fail();
                 stage_head(cur, h + 1);
                 load_head(cur, h + 1);
             }
             ++st_issued;
             ++ld_issued;
-        } else if (s_item[0] < p.n_items) {   // nxt was decoded, its tables built, during this head
+        } else if (s_item[0] < p.n_items) {
             have_next = true;
-            issue_first(nxt);
+            if (tid == 128) {
+                if (!mbar_wait(&bar[4], mma2_phase & 1)) fail();
+                load_first(nxt);
+            }
+            ++bc_issued;
+            ++st_issued;
+            ++ld_issued;
         }
-        {   // ---- per-position scalars (threads 0..127 = position i)
+        if (tid < QT) {   // ---- per-position scalars (threads 0..127 = position i; named barrier 2)
             const int i = tid;
-            float dcs = 0.f, ddir = 0.f, t4 = 0.f;
-            if (i < QT) {
+            float dcs, ddir, t4;
+            {
                 const int sb = i >> 5, jj = i & 31;
                 const int hsel = (sb == 0 || sb == 3) ? 0 : 1;
                 const int bi = (sb == 0 || sb == 1) ? 0 : 1;
@@ -873,19 +882,18 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             // da[u] = sum_{i>=u} dcs[i] + T3 + sum_{s<u} T4[s]  (T4[s] enters dcs at the chunk's
             // last position with + and at s with -: their net share of da[u] is the prefix below u)
             float drev, t4ex;
-            block_rev_excl_scan(dcs, t4, fm + F_WSUM, &drev, &t4ex);
-            float pa = 0.f, pb = 0.f, pd = 0.f;
-            if (i < QT) {
-                const float da = drev + T3 + t4ex;
-                if (i >= ci.lo && i < ci.len) {
-                    const float gv = (ddir + Ah * da) * sigmoid_f(vrt[i]);
-                    p.ddt[(int64_t)ci.b * p.sddb + (int64_t)(ci.t0 + i) * p.sddl + h] = gv;
-                    pa = dtc[i] * da;
-                    pb = gv;
-                }
-                pd = fm[F_ROWD + i] + fm[F_ROWD + 128 + i];
+            rev_excl_scan128(dcs, t4, fm + F_WSUM, &drev, &t4ex);
+            float pa = 0.f, pb = 0.f;
+            const float da = drev + T3 + t4ex;
+            if (i >= ci.lo && i < ci.len) {
+                const float gv = (ddir + Ah * da) * sigmoid_f(vrt[i]);
+                p.ddt[(int64_t)ci.b * p.sddb + (int64_t)(ci.t0 + i) * p.sddl + h] = gv;
+                pa = dtc[i] * da;
+                pb = gv;
             }
-            // dA, ddt_bias, dD shares: fixed-order block sums of pa, pb, pd
+            float pd = fm[F_ROWD + i] + fm[F_ROWD + 128 + i];
+            // dA, ddt_bias, dD shares: fixed-order sums of pa, pb, pd over the four warps (the
+            // T3 slots were read by every participant before the scan's barrier)
             pa = warp_sum(pa);
             pb = warp_sum(pb);
             pd = warp_sum(pd);
@@ -894,11 +902,11 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 fm[F_PB + warp] = pb;
                 fm[F_RED + 8 + warp] = pd;
             }
-            __syncthreads();
+            asm volatile("bar.sync 2, 128;" ::: "memory");
             if (tid == 0) {
                 float ta = 0.f, tb = 0.f, td = 0.f;
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
+                for (int w = 0; w < 4; ++w) {
                     ta += fm[F_RED + w];
                     tb += fm[F_PB + w];
                     td += fm[F_RED + 8 + w];
@@ -907,6 +915,7 @@ k_bwd_chunk_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 pp[0] = ta; pp[1] = td; pp[2] = tb; pp[3] = 0.f;
             }
         }
+        wait_mma2();   // every thread: the dB/dC chains are done (thread 128 has seen it already)
         tb ^= 1;
         tc_fence_before();
         __syncthreads();
