@@ -320,6 +320,70 @@ k_conv_bwd(const ConvArgs a) {
         for (int k = 0; k < K; ++k)
 #pragma unroll
             for (int e = 0; e < W; ++e) acc[k][e] = 0.f;
+        const int64_t tend_all = std::min(a.L, s1 + K - 1);
+        if (s0 - (K - 1) >= cur.start && tend_all <= cur.next) {
+            // The thread's whole window (its tokens, the K-1 before and after) lies in one
+            // sequence: no sequence starts to test, 32-bit counters, pointers that step a row.
+            const T *up = ucol + (int)(s0 - t0) * 256, *dp = dcol + (int)(s0 - t0) * 256;
+#pragma unroll
+            for (int k = 0; k < K - 1; ++k) ldw<W>(up + k * 256, ring[k]);
+            up += (K - 1) * 256;
+            T *dup = du + (s0 - (K - 1)) * a.sdu_l;   // du[t - (K-1)] of the current t
+            const int nown = (int)(s1 - s0), ntot = (int)(tend_all - s0);
+            for (int i = 0; i < ntot; ++i) {
+                ldw<W>(up, ring[K - 1]);
+                up += 256;
+                float dv[W];
+                ldw<W>(dp, dv);
+                dp += 256;
+                float g[W];
+#pragma unroll
+                for (int e = 0; e < W; ++e) {
+                    float pre = bias[e];
+#pragma unroll
+                    for (int k = 0; k < K; ++k) pre = fmaf(w[k][e], ring[k][e], pre);
+                    if (a.silu) {
+                        const float sg = sig_t<T>(pre);
+                        g[e] = dv[e] * sg * (1.f + pre * (1.f - sg));
+                    } else {
+                        g[e] = dv[e];
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < K; ++k)
+#pragma unroll
+                    for (int e = 0; e < W; ++e) acc[k][e] = fmaf(w[k][e], g[e], acc[k][e]);
+                if (i < nown) {   // this thread's token: its dw / dbias shares
+#pragma unroll
+                    for (int e = 0; e < W; ++e) {
+#pragma unroll
+                        for (int k = 0; k < K; ++k) dw[k][e] = fmaf(g[e], ring[k][e], dw[k][e]);
+                        db[e] += g[e];
+                    }
+                }
+                if (i >= K - 1) stw<W>(dup, acc[0]);   // du[s0 + i - (K-1)] is complete
+                dup += a.sdu_l;
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k)
+#pragma unroll
+                    for (int e = 0; e < W; ++e) {
+                        ring[k][e] = ring[k + 1][e];
+                        acc[k][e] = acc[k + 1][e];
+                    }
+#pragma unroll
+                for (int e = 0; e < W; ++e) acc[K - 1][e] = 0.f;
+            }
+            // rows whose windows would run past the end of the row (tend_all clamped to L)
+            for (int64_t tdone = tend_all - (K - 1); tdone < s1; ++tdone) {
+                if (tdone >= s0) stw<W>(du + tdone * a.sdu_l, acc[0]);
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k)
+#pragma unroll
+                    for (int e = 0; e < W; ++e) acc[k][e] = acc[k + 1][e];
+#pragma unroll
+                for (int e = 0; e < W; ++e) acc[K - 1][e] = 0.f;
+            }
+        } else {
 #pragma unroll
         for (int k = 0; k < K - 1; ++k) {
             const int64_t tp = s0 - (K - 1) + k;
@@ -392,6 +456,7 @@ k_conv_bwd(const ConvArgs a) {
 #pragma unroll
             for (int e = 0; e < W; ++e) acc[K - 1][e] = 0.f;
         }
+        }   // general path
     }
     __syncthreads();   // the staged tiles are no longer read: reuse them for the group sums
 #pragma unroll
