@@ -248,6 +248,33 @@ k_conv_fwd(const ConvArgs a) {
     SeqCursor cur;
     cur.init(a, s0);
     const T *col = tile + W * j;   // row t at (t - tb) * 256 (offsets below fit 32 bits)
+    if (s0 - (K - 1) >= cur.start && s1 <= cur.next) {
+        // The thread's tokens and the K-1 before them lie in one sequence: no sequence starts
+        // to test, a 32-bit counter, pointers that step a row.
+        const T *rp = col + (int)(s0 - t0) * 256;   // row t - (K-1) of the current t
+        T *op = o + s0 * a.so_l;
+        const int n = (int)(s1 - s0);
+        for (int i = 0; i < n; ++i) {
+            float acc[W];
+#pragma unroll
+            for (int e = 0; e < W; ++e) acc[e] = bias[e];
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                float v[W];
+                ldw<W>(rp + k * 256, v);
+#pragma unroll
+                for (int e = 0; e < W; ++e) acc[e] = fmaf(w[k][e], v[e], acc[e]);
+            }
+            if (a.silu) {
+#pragma unroll
+                for (int e = 0; e < W; ++e) acc[e] *= sig_t<T>(acc[e]);
+            }
+            stw<W>(op, acc);
+            rp += 256;
+            op += a.so_l;
+        }
+        return;
+    }
     for (int64_t t = s0; t < s1; ++t) {
         cur.advance(a, t);
         float acc[W];
