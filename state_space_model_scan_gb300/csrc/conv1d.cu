@@ -503,15 +503,37 @@ k_conv_bwd(const ConvArgs a) {
     }
 }
 
-__global__ void k_conv_dw(const float *partials, int64_t tiles, int64_t Cn, int K, float *dw, float *db) {
-    const int64_t n = Cn * (K + 1);
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        float s = 0.f;
-        for (int64_t t = 0; t < tiles; ++t) s += partials[t * n + i];
+// dw / dbias: the column sums of the per-tile shares [tiles][Cn (K+1)] in a fixed order.  A
+// block takes 32 columns; warp w sums tiles w, w + 8, ... in ascending order (four loads in
+// flight), and the eight warp sums are added in warp order.
+__global__ void __launch_bounds__(256) k_conv_dw(const float *partials, int64_t tiles, int64_t Cn, int K, float *dw,
+                                                 float *db) {
+    __shared__ float red[8][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t n = Cn * (K + 1), i = (int64_t)blockIdx.x * 32 + lane;
+    float s = 0.f;
+    if (i < n) {
+        const float *col = partials + i;
+        int64_t t = w;
+        for (; t + 24 < tiles; t += 32) {
+            const float a0 = col[t * n], a1 = col[(t + 8) * n], a2 = col[(t + 16) * n], a3 = col[(t + 24) * n];
+            s += a0;
+            s += a1;
+            s += a2;
+            s += a3;
+        }
+        for (; t < tiles; t += 8) s += col[t * n];
+    }
+    red[w][lane] = s;
+    __syncthreads();
+    if (w == 0 && i < n) {
+        float tot = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tot += red[q][lane];
         const int64_t c = i / (K + 1);
         const int k = (int)(i - c * (K + 1));
-        if (k < K) dw[c * K + k] = s;
-        else if (db) db[c] = s;
+        if (k < K) dw[c * K + k] = tot;
+        else if (db) db[c] = tot;
     }
 }
 
@@ -667,7 +689,7 @@ ssd_status ssd_conv1d_bwd(const ssd_conv_problem *p, const void *x, int64_t x_sb
         if (cudaMemsetAsync(workspace, 0, need, st) != cudaSuccess) return SSD_ERR_CUDA;
     }
     const int64_t n = p->channels * (p->width + 1);
-    k_conv_dw<<<(unsigned)std::min<int64_t>((n + 255) / 256, 1024), 256, 0, st>>>(
+    k_conv_dw<<<(unsigned)((n + 31) / 32), 256, 0, st>>>(
         a.partials, std::max<int64_t>(tiles, 1), p->channels, (int)p->width, dweight, dbias);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

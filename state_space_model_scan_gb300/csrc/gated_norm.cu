@@ -146,7 +146,7 @@ k_norm_fwd(const NormArgs a) {
 
 // grid (row chunks, groups), NW warps: warp w takes rows chunk_start + w, + NW, ...; its share
 // of dw for the group's columns accumulates in its own shared-memory row, the rows are summed
-// in warp order at the end, and k_norm_dw sums the row chunks in order.
+// in warp order at the end, and k_norm_dw sums the row chunks in a fixed order.
 template <typename T>
 __global__ void __launch_bounds__(NW * 32)
 k_norm_bwd(const NormArgs a) {
@@ -468,16 +468,34 @@ size_t staged_smem(int64_t G) {
     return stage > red ? stage : red;
 }
 
-__global__ void k_norm_dw(const float *partials, int64_t chunks, int64_t width, float *dw) {
-    // four interleaved partial sums, then combined: a fixed order, so bitwise reproducible
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < width; i += (int64_t)gridDim.x * blockDim.x) {
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-        int64_t c = 0;
-        for (; c + 4 <= chunks; c += 4)
+// dw: the column sums of the per-chunk shares [chunks][width] in a fixed order.  A block takes
+// 32 columns; warp w sums chunks w, w + 8, ... in ascending order (four loads in flight), and the
+// eight warp sums are added in warp order, so the result is bitwise reproducible.
+__global__ void __launch_bounds__(256) k_norm_dw(const float *partials, int64_t chunks, int64_t width, float *dw) {
+    __shared__ float red[8][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t i = (int64_t)blockIdx.x * 32 + lane;
+    float s = 0.f;
+    if (i < width) {
+        const float *col = partials + i;
+        int64_t c = w;
+        for (; c + 24 < chunks; c += 32) {
+            const float a0 = col[c * width], a1 = col[(c + 8) * width], a2 = col[(c + 16) * width],
+                        a3 = col[(c + 24) * width];
+            s += a0;
+            s += a1;
+            s += a2;
+            s += a3;
+        }
+        for (; c < chunks; c += 8) s += col[c * width];
+    }
+    red[w][lane] = s;
+    __syncthreads();
+    if (w == 0 && i < width) {
+        float tot = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) s4[q] += partials[(c + q) * width + i];
-        for (; c < chunks; ++c) s4[0] += partials[c * width + i];
-        dw[i] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        for (int q = 0; q < 8; ++q) tot += red[q][lane];
+        dw[i] = tot;
     }
 }
 
@@ -626,8 +644,7 @@ ssd_status ssd_gated_norm_bwd(const ssd_norm_problem *p, const void *y, int64_t 
     else
         e = launch_norm_bwd<float>(a, ppl, grid, smem, st);
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SSD_ERR_CUDA;
-    const int blocks = (int)std::min<int64_t>((p->width + 63) / 64, 4096);
-    k_norm_dw<<<blocks, 64, 0, st>>>(a.partials, chunks, p->width, dweight);
+    k_norm_dw<<<(unsigned)((p->width + 31) / 32), 256, 0, st>>>(a.partials, chunks, p->width, dweight);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
