@@ -36,6 +36,29 @@ __device__ __forceinline__ void load8(const float *p, float *v) {
     const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
+// 8 elements as loaded (raw bits), converted later: lets a warp keep the next item's loads in flight
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> { uint4 u; };
+template <> struct Raw8<float> { float4 a, b; };
+__device__ __forceinline__ void ldraw(const __nv_bfloat16 *p, Raw8<__nv_bfloat16> &r) {
+    r.u = *reinterpret_cast<const uint4 *>(p);
+}
+__device__ __forceinline__ void ldraw(const float *p, Raw8<float> &r) {
+    r.a = reinterpret_cast<const float4 *>(p)[0];
+    r.b = reinterpret_cast<const float4 *>(p)[1];
+}
+__device__ __forceinline__ void cvt8(const Raw8<__nv_bfloat16> &r, float *v) {
+    const __nv_bfloat162 *e = reinterpret_cast<const __nv_bfloat162 *>(&r.u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(e[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void cvt8(const Raw8<float> &r, float *v) {
+    v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w; v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
+}
 __device__ __forceinline__ void store8(__nv_bfloat16 *p, const float *v) {
     uint32_t w[4];
 #pragma unroll
@@ -247,22 +270,40 @@ k_norm_fwd_reg(const NormArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t items = a.rows * a.ng, nw = (int64_t)gridDim.x * NW;
     const int pieces = (int)(a.G / 8);
-    for (int64_t it = (int64_t)blockIdx.x * NW + (threadIdx.x >> 5); it < items; it += nw) {
-        const int64_t r = it / a.ng;
-        const int g = (int)(it - r * a.ng);
-        const T *yr = static_cast<const T *>(a.y) + r * a.sy + (int64_t)g * a.G;
-        const T *zr = a.z ? static_cast<const T *>(a.z) + r * a.sz + (int64_t)g * a.G : nullptr;
-        float v[PPL][8], zz[PPL][8];
+    const bool hasz = a.z != nullptr;
+    // y and z of an item are loaded one item ahead (raw bits), so a warp's loads stay in flight
+    // while it normalises the current item
+    Raw8<T> ry[PPL], rz[PPL];
+    auto fetch = [&](int64_t it2) {
+        const int64_t r2 = it2 / a.ng;
+        const int g2 = (int)(it2 - r2 * a.ng);
+        const T *y2 = static_cast<const T *>(a.y) + r2 * a.sy + (int64_t)g2 * a.G;
+        const T *z2 = hasz ? static_cast<const T *>(a.z) + r2 * a.sz + (int64_t)g2 * a.G : nullptr;
 #pragma unroll
         for (int k = 0; k < PPL; ++k) {
             const int j = lane + 32 * k;
             if (j < pieces) {
-                load8(yr + 8 * j, v[k]);
-                if (zr) load8(zr + 8 * j, zz[k]);
+                ldraw(y2 + 8 * j, ry[k]);
+                if (hasz) ldraw(z2 + 8 * j, rz[k]);
             }
         }
+    };
+    const int64_t first = (int64_t)blockIdx.x * NW + (threadIdx.x >> 5);
+    if (first < items) fetch(first);
+    for (int64_t it = first; it < items; it += nw) {
+        const int64_t r = it / a.ng;
+        const int g = (int)(it - r * a.ng);
+        float v[PPL][8], zz[PPL][8];
+#pragma unroll
+        for (int k = 0; k < PPL; ++k) {
+            if (lane + 32 * k < pieces) {
+                cvt8(ry[k], v[k]);
+                if (hasz) cvt8(rz[k], zz[k]);
+            }
+        }
+        if (it + nw < items) fetch(it + nw);
         // u in place: the gate multiplies now unless it comes after the norm
-        if (zr && !bg) {
+        if (hasz && !bg) {
 #pragma unroll
             for (int k = 0; k < PPL; ++k)
                 if (lane + 32 * k < pieces)
@@ -301,7 +342,7 @@ k_norm_fwd_reg(const NormArgs a) {
             if (j < pieces) {
                 float wv[8];
                 load8(wr + 8 * j, wv);
-                if (zr && bg)
+                if (hasz && bg)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) wv[e] *= zz[k][e] * sig_t<T>(zz[k][e]);
 #pragma unroll
