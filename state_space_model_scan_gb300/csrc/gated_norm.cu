@@ -412,9 +412,9 @@ __device__ __forceinline__ void bwd_row(const NormArgs &a, int lane, int pieces,
 }
 
 // Backward with the rows staged in shared memory: a block takes its row chunk of one group in
-// batches of NW rows (one per warp); y, z and dout of the next batch are copied in by cp.async
-// (double-buffered) while the current batch is computed, so the loads in flight do not depend
-// on how many warps the registers allow.  A lane keeps its slice of w and of the dw sums in
+// batches of NW rows (one per warp); each warp copies y, z and dout of its row of the next batch
+// by cp.async (double-buffered) while it computes the current one, so the loads in flight do
+// not depend on how many warps the registers allow.  A lane keeps its slice of w and of the dw sums in
 // registers; the block's dw rows are summed in warp order at the end, as in the kernels above.
 __device__ __forceinline__ void cp16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
@@ -442,16 +442,19 @@ k_norm_bwd_staged(const NormArgs a) {
         if (j < pieces) load8(wr + 8 * j, wv[k]);
     }
     auto tile = [&](int buf, int t, int rw) { return stage + (((int64_t)buf * 3 + t) * NW + rw) * G; };
-    auto issue = [&](int64_t rb, int buf) {   // rows rb .. rb+NW-1 (those < r1) into buffer buf
-        for (int i = threadIdx.x; i < ntens * NW * cpr; i += NW * 32) {
-            const int t = i / (NW * cpr), rem = i % (NW * cpr), rw = rem / cpr, q = rem % cpr;
-            const int64_t r = rb + rw;
-            if (r >= r1) continue;
-            const T *src = t == 0 ? static_cast<const T *>(a.y) + r * a.sy
-                         : t == 1 ? static_cast<const T *>(a.dout) + r * a.sdout
-                                  : static_cast<const T *>(a.z) + r * a.sz;
-            cp16(reinterpret_cast<uint8_t *>(tile(buf, t, rw)) + 16 * q,
-                 reinterpret_cast<const uint8_t *>(src + (int64_t)g * G) + 16 * q);
+    // Each warp stages the row it computes (y, dout, z of row rb + warp): the copies and the
+    // reads of a row stay within one warp, so a warp barrier orders them.
+    auto issue = [&](int64_t rb, int buf) {
+        const int64_t r = rb + warp;
+        if (r < r1) {
+            const T *src[3] = {static_cast<const T *>(a.y) + r * a.sy + (int64_t)g * G,
+                               static_cast<const T *>(a.dout) + r * a.sdout + (int64_t)g * G,
+                               a.z ? static_cast<const T *>(a.z) + r * a.sz + (int64_t)g * G : nullptr};
+            for (int t = 0; t < ntens; ++t) {
+                uint8_t *dst = reinterpret_cast<uint8_t *>(tile(buf, t, warp));
+                const uint8_t *sp = reinterpret_cast<const uint8_t *>(src[t]);
+                for (int q = lane; q < cpr; q += 32) cp16(dst + 16 * q, sp + 16 * q);
+            }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
@@ -464,7 +467,7 @@ k_norm_bwd_staged(const NormArgs a) {
         } else {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
-        __syncthreads();
+        __syncwarp();
         const int64_t r = rb + warp;
         if (r < r1) {
             const T *ys = tile(buf, 0, warp), *ds = tile(buf, 1, warp), *zs = a.z ? tile(buf, 2, warp) : nullptr;
@@ -483,8 +486,9 @@ k_norm_bwd_staged(const NormArgs a) {
             T *dzr = a.z ? static_cast<T *>(a.dz) + r * a.sdz + (int64_t)g * G : nullptr;
             bwd_row<T, PPL, GEN>(a, lane, pieces, zs != nullptr, rs, y8, z8, d, wv, dw, dyr, dzr);
         }
-        __syncthreads();   // this buffer is refilled two batches on
+        __syncwarp();   // this warp's reads of the buffer precede its refill at the next step
     }
+    __syncthreads();   // every warp is done with the stage before it becomes the dw rows
     float *acc = reinterpret_cast<float *>(nsm);   // [NW][G], over the (now idle) stage
     float *mine = acc + (int64_t)warp * G;
 #pragma unroll
