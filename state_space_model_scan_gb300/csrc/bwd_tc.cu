@@ -132,6 +132,30 @@ __device__ __forceinline__ void load_row32_swz(const uint8_t *row_base, int row,
         }
     }
 }
+// 16 floats as bf16 into the 16-byte chunks 2 qt, 2 qt + 1 of a 128-byte swizzled row, and back.
+__device__ __forceinline__ void store_row16_swz(uint8_t *row_base, int row, int qt, const float *v) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int c = (2 * qt + q) ^ (row & 7);
+        *reinterpret_cast<uint4 *>(row_base + c * 16) =
+            make_uint4(pack_bf16(v[q * 8], v[q * 8 + 1]), pack_bf16(v[q * 8 + 2], v[q * 8 + 3]),
+                       pack_bf16(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
+    }
+}
+__device__ __forceinline__ void load_row16_swz(const uint8_t *row_base, int row, int qt, float *v) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int c = (2 * qt + q) ^ (row & 7);
+        uint4 u = *reinterpret_cast<const uint4 *>(row_base + c * 16);
+        const __nv_bfloat162 *e = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(e[i]);
+            v[q * 8 + 2 * i] = f.x;
+            v[q * 8 + 2 * i + 1] = f.y;
+        }
+    }
+}
 // Column sums of a 32x32 block held one row per lane (v[i] = column i): after the
 // call lane j holds the sum over the warp's 32 rows of column j (fixed order).
 __device__ __forceinline__ float colsum32(float (&v)[32]) {
@@ -195,15 +219,17 @@ __device__ __forceinline__ void rev_excl_scan128(float v, float u, float *wsum, 
 }
 
 // ------------------------------------------------------------------ dstates
-// grid (kmax, H / hs_ds), 256 threads, two CTAs per SM: one chunk and hs_ds heads of one
+// grid (kmax, H / hs_ds), 256 threads, three CTAs per SM: one chunk and hs_ds heads of one
 // group per CTA.  Per head, dS_loc^T[n][p] = sum_l C[l][n] (e o dyp)[l][p] on the tensor
-// cores (A = C^T, M-major; B = e o dyp, N-major), written as fp32 [p][n].  C is loaded
-// once; each head's dy and z tiles arrive by TMA while the previous head computes.
-constexpr uint32_t DS_OFF_C = 0, DS_OFF_ST = BC_BYTES, DS_OFF_Y = BC_BYTES + 2 * X_BYTES,
-                   DS_OFF_MISC = DS_OFF_Y + X_BYTES;
+// cores (A = C^T, M-major; B = e o dyp, N-major), written as bf16 [p][n].  C is loaded
+// once; e o dyp is formed in place over the dy tile (each thread rewrites the bytes it read),
+// so the next head's z travels as soon as this head's e o dyp is formed and its dy once the
+// MMA has read the tile.
+constexpr uint32_t DS_OFF_C = 0, DS_OFF_ST = BC_BYTES, DS_OFF_Y = BC_BYTES,
+                   DS_OFF_MISC = DS_OFF_ST + 2 * X_BYTES;
 constexpr uint32_t DS_SMEM = DS_OFF_MISC + 2048 + 1024;
 
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, 3)
 k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmDY,
                  const __grid_constant__ CUtensorMap tmZ, const BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -217,20 +243,24 @@ k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
     float *dtc = reinterpret_cast<float *>(sm + DS_OFF_MISC);
     float *cs2 = dtc + QT;
     float *wsum = cs2 + QT;                                        // 16
-    uint64_t *bar = reinterpret_cast<uint64_t *>(wsum + 16);       // 0: C, 1: dy/z, 2: MMA
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 3);
-    auto stage_head = [&](int h) {   // one thread
-        mbar_expect_tx(&bar[1], X_BYTES * (has_z ? 2u : 1u));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(wsum + 16);       // 0: C, 1: dy, 2: MMA, 3: z
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
+    auto stage_dy = [&](int h) {   // one thread
+        mbar_expect_tx(&bar[1], X_BYTES);
         tma_load_4d(sm + DS_OFF_ST, &tmDY, &bar[1], 0, h, ci.t0, ci.b);
-        if (has_z) tma_load_4d(sm + DS_OFF_ST + X_BYTES, &tmZ, &bar[1], 0, h, ci.t0, ci.b);
+    };
+    auto stage_z = [&](int h) {   // one thread
+        mbar_expect_tx(&bar[3], X_BYTES);
+        tma_load_4d(sm + DS_OFF_ST + X_BYTES, &tmZ, &bar[3], 0, h, ci.t0, ci.b);
     };
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
         mbar_expect_tx(&bar[0], BC_BYTES);
         tma_load_4d(sm + DS_OFF_C, &tmC, &bar[0], 0, g, ci.t0, ci.b);
         tma_load_4d(sm + DS_OFF_C + BC_BYTES / 2, &tmC, &bar[0], 64, g, ci.t0, ci.b);
-        stage_head(h0);
+        stage_dy(h0);
+        if (has_z) stage_z(h0);
     }
     auto load_dtv = [&](int h) -> float {
         return (tid >= ci.lo && tid < ci.len) ? p.dt_raw[(int64_t)ci.b * p.sdb + (int64_t)(ci.t0 + tid) * p.sdl + h] +
@@ -260,27 +290,33 @@ k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             if (tid == 0) p.chunk_lam[(int64_t)k * p.sh.H + h] = tot;
             __syncthreads();
         }
-        if (!mbar_wait(&bar[1], st_done & 1)) bad = 1;
+        if (!mbar_wait(&bar[1], st_done & 1)) bad = 1;   // dy (and z) of this head
+        if (has_z && !mbar_wait(&bar[3], st_done & 1)) bad = 1;
         ++st_done;
-        {   // (e o dyp) row `row`, half hf -> swizzled [l][p] tile
-            float v[32];
-            load_row32_swz(sm + DS_OFF_ST + row * 128, row, hf, v);
+        {   // (e o dyp) row `row`, half hf, in place over the dy tile (two 16-column pieces)
             const float el = (row >= ci.lo && row < ci.len) ? ex2(cs2[row]) : 0.f;
-            if (has_z) {
-                float zz[32];
-                load_row32_swz(sm + DS_OFF_ST + X_BYTES + row * 128, row, hf, zz);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= silu_f(zz[i]) * el;
-            } else {
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint8_t *yrow = sm + DS_OFF_ST + row * 128;
+                const int qt = 2 * hf + q2;   // 16-column piece of the row
+                float v[16];
+                load_row16_swz(yrow, row, qt, v);
+                if (has_z) {
+                    float zz[16];
+                    load_row16_swz(sm + DS_OFF_ST + X_BYTES + row * 128, row, qt, zz);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= el;
+                    for (int i = 0; i < 16; ++i) v[i] *= silu_f(zz[i]) * el;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] *= el;
+                }
+                store_row16_swz(yrow, row, qt, v);
             }
-            store_row32_swz(sm + DS_OFF_Y + row * 128, row, hf, v);
         }
         fence_proxy_async_smem();
         if (__syncthreads_or(bad)) break;
         if (tid == 0) {
-            if (hi + 1 < HS) stage_head(h + 1);   // the staged tiles are read
+            if (hi + 1 < HS && has_z) stage_z(h + 1);   // the z tile is read
             if (hi == 0) {
                 if (!mbar_wait(&bar[0], 0)) bad = 1;
                 ++c_done;
@@ -299,20 +335,26 @@ k_bwd_dstates_tc(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         if (!mbar_wait(&bar[2], mma_phase & 1)) bad = 1;
         ++mma_phase;
         tc_fence_after();
-        {
-            float v[32];
-            tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + 32 * hf, v);
-            tmem_wait_ld();
-            __nv_bfloat16 *dst = p.dS_loc + ((int64_t)k * p.sh.H + h) * (PT * NT) + (int64_t)(32 * hf) * NT + row;
+        if (tid == 0 && hi + 1 < HS) stage_dy(h + 1);   // the MMA has read the e o dyp tile
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(v[i]);
+        for (int q2 = 0; q2 < 2; ++q2) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + 32 * hf + 16 * q2, v);
+            tmem_wait_ld();
+            __nv_bfloat16 *dst =
+                p.dS_loc + ((int64_t)k * p.sh.H + h) * (PT * NT) + (int64_t)(32 * hf + 16 * q2) * NT + row;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dst[(int64_t)i * NT] = __float2bfloat16_rn(v[i]);
         }
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
     }
     if (bad) set_status(const_cast<int32_t *>(p.hdr), SSD_ERR_DEVICE_TIMEOUT);
-    for (uint32_t q = st_done; q < st_issued; ++q) mbar_wait(&bar[1], q & 1);
+    for (uint32_t q = st_done; q < st_issued; ++q) {
+        mbar_wait(&bar[1], q & 1);
+        if (has_z) mbar_wait(&bar[3], q & 1);
+    }
     if (tid == 0 && c_done == 0) mbar_wait(&bar[0], 0);
     tc_fence_before();
     __syncthreads();
