@@ -357,6 +357,7 @@ k_conv_bwd(const ConvArgs a) {
             up += (K - 1) * 256;
             T *dup = du + (s0 - (K - 1)) * a.sdu_l;   // du[t - (K-1)] of the current t
             const int nown = (int)(s1 - s0), ntot = (int)(tend_all - s0);
+#pragma unroll 4   // the ring and accumulator rotation becomes register renaming
             for (int i = 0; i < ntot; ++i) {
                 ldw<W>(up, ring[K - 1]);
                 up += 256;
