@@ -292,27 +292,52 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
     if (fused && !split) {
         R = p->seg_chunks;
         const int rmax = bwd ? fused_rmax_states() : fused_rmax();
+        num = 1;   // units per chunk: 1/R, or the larger ratio num/den chosen below
+        den = R;
         if (R == 0) {
-            // Chunks per unit from a model of the persistent kernel: rounds of resident CTAs
-            // (two per SM) times one unit's time, R chunks plus a fixed part (unit prologue and
+            // Work units from a model of the persistent kernel: rounds of resident CTAs (two
+            // per SM) times one unit's time, its chunks plus a fixed part (unit prologue and
             // carry-in fold).  Per-chunk cost: full forward about 9.3 us, states-only (the
             // backward's recompute) about 2.3 us; fixed part about 8 us.
             const int64_t slots = 2LL * num_sms();
             const double c_chunk = bwd ? 2.3 : 9.3, c_unit = 8.0;
             double best = 1e300;
-            for (int r = 1; r <= rmax; ++r) {
-                const int64_t units = varlen ? (kmax + r - 1) / r + S : B * (((L + Q - 1) / Q + r - 1) / r);
-                const int64_t rounds = (units * H + slots - 1) / slots;
-                const double cost = (double)rounds * (r * c_chunk + c_unit);
-                if (cost < best) {
-                    best = cost;
-                    R = r;
+            const int64_t n = (L + Q - 1) / Q;   // chunks per sequence of a fixed-length batch
+            if (!varlen && n > 0) {
+                // The number of units per sequence, U, is chosen rather than their length, so
+                // that the units of the last round fill it: units of n/U chunks on average
+                // (floor or ceil), B U H of them.  Units stay between rmax - 1 and rmax chunks
+                // long: shorter ones measured slower (more carry-in folds and block ends in
+                // the serial chain of a sequence).
+                const int64_t U0 = (n + rmax - 1) / rmax;
+                const int64_t U1 = rmax > 1 ? (n + rmax - 2) / (rmax - 1) : n;
+                int64_t bestU = U0;
+                for (int64_t U = U0; U <= U1 && U <= n; ++U) {
+                    const int64_t rounds = (B * U * H + slots - 1) / slots;
+                    const double cost = (double)rounds * ((double)n / (double)U * c_chunk + c_unit);
+                    if (cost < best) {
+                        best = cost;
+                        bestU = U;
+                    }
                 }
+                R = (int)((n + bestU - 1) / bestU);
+                num = (int)bestU;
+                den = (int)n;
+            } else {
+                for (int r = 1; r <= rmax; ++r) {
+                    const int64_t units = varlen ? (kmax + r - 1) / r + S : B * ((n + r - 1) / r);
+                    const int64_t rounds = (units * H + slots - 1) / slots;
+                    const double cost = (double)rounds * (r * c_chunk + c_unit);
+                    if (cost < best) {
+                        best = cost;
+                        R = r;
+                    }
+                }
+                num = 1;
+                den = R;
             }
         }
         if (R > rmax) return SSD_ERR_UNSUPPORTED;
-        num = 1;   // units per chunk: 1/R (the metadata kernel also accepts a larger ratio)
-        den = R;
         // units: sum over sequences of max(ceil(n/R), ceil(n num/den)) <= kmax max(1/R, num/den) + S
         const int64_t per = (int64_t)num * R > den ? (kmax * num + den - 1) / den : (kmax + R - 1) / R;
         umax = per + S;

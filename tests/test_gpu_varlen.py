@@ -225,8 +225,12 @@ def test_fixed_batch_metadata_bit_exact(B, L, seg, algo):
     counts = raw[lay.meta_counts:lay.meta_counts + 16].view(np.int32)
     if fused:
         got = unit_schedule.decode_units(raw[lay.units:], counts[1])
-        R = int(prob.seg_chunks) or got[0][4]   # the library's own unit size when seg = 0
-        ref = unit_schedule.build(batch=B, seqlen=L, Q=128, R=R, KB=4)
+        n = -(-L // 128)
+        if prob.seg_chunks:   # units of seg_chunks tiles
+            ref = unit_schedule.build(batch=B, seqlen=L, Q=128, R=int(prob.seg_chunks), KB=4)
+        else:   # the library's own choice: U units per row (the unit count tells U), n/U tiles each
+            U = max(1, int(counts[1]) // B)
+            ref = unit_schedule.build(batch=B, seqlen=L, Q=128, R=-(-n // U), KB=4, num=U, den=max(n, 1))
         assert counts[1] == len(ref["units"]) and counts[3] == 0
         assert got == ref["units"]
     else:
