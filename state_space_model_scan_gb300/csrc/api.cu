@@ -144,12 +144,13 @@ int bwd_heads_per_cta(int64_t kmax, int64_t H, int hpg) {
     return best;
 }
 
-// Heads per CTA of the tensor-core dstates kernel (two CTAs per SM): the largest
-// divisor of H/G up to 8 that still gives two full waves of CTAs, else 1.
+// Heads per CTA of the tensor-core dstates kernel (three CTAs per SM): the largest
+// divisor of H/G up to 8 that still gives four full waves of CTAs (short CTAs keep the last
+// wave's idle time small), else 1.
 int dstates_heads_per_cta(int64_t kmax, int64_t H, int hpg) {
-    const int64_t slots = 3LL * num_sms();   // the dstates kernel runs three CTAs per SM
+    const int64_t slots = 3LL * num_sms();
     for (int d = 8; d > 1; --d)
-        if (hpg % d == 0 && kmax * (H / d) >= 2 * slots) return d;
+        if (hpg % d == 0 && kmax * (H / d) >= 4 * slots) return d;
     return 1;
 }
 
