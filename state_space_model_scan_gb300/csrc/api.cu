@@ -370,7 +370,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
             if (sh.hpg % pl.hs != 0) return SSD_ERR_INVALID_ARGUMENT;
             // Work items of the persistent gradient kernel (one CTA per SM).  With whole-group
             // items, the pairs (chunk, group) that would form a last partial wave are split into
-            // subsets of >= 2 heads, so the last wave is filled with small items; their dB/dC
+            // subsets of >= 2 heads, so the last wave is filled with smaller items; their dB/dC
             // shares are summed, in subset order, by a small kernel afterwards.
             const int64_t pairs = kmax * G;
             const int nsub_main = sh.hpg / pl.hs;
@@ -378,9 +378,12 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
             pl.nsub_tail = nsub_main;
             if (p->bwd_heads == 0 && nsub_main == 1) {
                 const int64_t sms = num_sms(), r = pairs % sms;
+                // the fewest subsets (of at least 2 heads): halves measured faster than quarters
+                // or single heads, whose per-item overhead (B/C loads, C B^T, dB/dC shares)
+                // outweighs the finer fill of the last wave
                 int f = 1;
-                for (int d = 4; d >= 2; --d)
-                    if (pl.hs % d == 0 && pl.hs / d >= 2) { f = d; break; }
+                for (int d = 2; d <= pl.hs / 2; ++d)
+                    if (pl.hs % d == 0) { f = d; break; }
                 if (r > 0 && f > 1 && pairs > sms) {
                     pl.k_pairs = (int)(pairs - r);
                     pl.nsub_tail = f;
