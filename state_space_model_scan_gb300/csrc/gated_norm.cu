@@ -564,17 +564,26 @@ cudaError_t launch_norm_bwd(const NormArgs &a, int64_t ppl, dim3 grid, size_t sm
     return (a.ln || a.bg) ? launch_norm_bwd_g<T, true>(a, ppl, grid, smem, st)
                           : launch_norm_bwd_g<T, false>(a, ppl, grid, smem, st);
 }
+// The grid-stride kernels run one wave: at most the blocks that are resident at once (the
+// occupancy of the instantiation at hand times the SMs), so no block waits for a free SM.
+template <typename K>
+void launch_wave(K kernel, const NormArgs &a, int blocks, int sms, cudaStream_t st) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, NW * 32, 0) == cudaSuccess && per_sm > 0)
+        blocks = std::min(blocks, per_sm * sms);
+    kernel<<<blocks, NW * 32, 0, st>>>(a);
+}
 template <typename T, bool GEN>
-void launch_norm_fwd_g(const NormArgs &a, int64_t ppl, int blocks, cudaStream_t st) {
-    if (ppl <= 1) k_norm_fwd_reg<T, 1, GEN><<<blocks, NW * 32, 0, st>>>(a);
-    else if (ppl <= 2) k_norm_fwd_reg<T, 2, GEN><<<blocks, NW * 32, 0, st>>>(a);
-    else if (ppl <= 4) k_norm_fwd_reg<T, 4, GEN><<<blocks, NW * 32, 0, st>>>(a);
-    else k_norm_fwd<T><<<blocks, NW * 32, 0, st>>>(a);
+void launch_norm_fwd_g(const NormArgs &a, int64_t ppl, int blocks, int sms, cudaStream_t st) {
+    if (ppl <= 1) launch_wave(k_norm_fwd_reg<T, 1, GEN>, a, blocks, sms, st);
+    else if (ppl <= 2) launch_wave(k_norm_fwd_reg<T, 2, GEN>, a, blocks, sms, st);
+    else if (ppl <= 4) launch_wave(k_norm_fwd_reg<T, 4, GEN>, a, blocks, sms, st);
+    else launch_wave(k_norm_fwd<T>, a, blocks, sms, st);
 }
 template <typename T>
-void launch_norm_fwd(const NormArgs &a, int64_t ppl, int blocks, cudaStream_t st) {
-    if (a.ln || a.bg) launch_norm_fwd_g<T, true>(a, ppl, blocks, st);
-    else launch_norm_fwd_g<T, false>(a, ppl, blocks, st);
+void launch_norm_fwd(const NormArgs &a, int64_t ppl, int blocks, int sms, cudaStream_t st) {
+    if (a.ln || a.bg) launch_norm_fwd_g<T, true>(a, ppl, blocks, sms, st);
+    else launch_norm_fwd_g<T, false>(a, ppl, blocks, sms, st);
 }
 
 int sm_count() {
@@ -641,11 +650,12 @@ ssd_status ssd_gated_norm_fwd(const ssd_norm_problem *p, const void *y, int64_t 
     a.sout = out_stride; a.rstd = rstd;
     a.ln = (p->flags & SSD_NORM_LAYER) != 0; a.bg = (p->flags & SSD_NORM_GATE_AFTER) != 0;
     const int64_t items = p->rows * a.ng;
-    const int blocks = (int)std::min<int64_t>((items + NW - 1) / NW, 8LL * sm_count());
+    const int sms = sm_count();
+    const int blocks = (int)std::min<int64_t>((items + NW - 1) / NW, 8LL * sms);
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t ppl = (p->group_size / 8 + 31) / 32;   // pieces per lane
-    if (p->dtype == SSD_BF16) launch_norm_fwd<__nv_bfloat16>(a, ppl, blocks, st);
-    else launch_norm_fwd<float>(a, ppl, blocks, st);
+    if (p->dtype == SSD_BF16) launch_norm_fwd<__nv_bfloat16>(a, ppl, blocks, sms, st);
+    else launch_norm_fwd<float>(a, ppl, blocks, sms, st);
     return cudaGetLastError() == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
