@@ -595,7 +595,8 @@ int sm_count() {
 
 bool aligned16(const void *p) { return ((uintptr_t)p) % 16 == 0; }
 
-// Shared checks of both directions; *chunks = the backward's row chunks.
+// Shared checks of both directions; *chunks = the backward's row chunks: two blocks per SM
+// over all groups (one resident wave of the staged backward, about 120 registers a thread).
 ssd_status check_norm(const ssd_norm_problem *p, int64_t *chunks) {
     if (p == nullptr) return SSD_ERR_INVALID_ARGUMENT;
     if (p->rows < 0 || p->width < 1 || p->group_size < 1 || p->width % p->group_size != 0)
@@ -607,7 +608,7 @@ ssd_status check_norm(const ssd_norm_problem *p, int64_t *chunks) {
         p->width > ((int64_t)1 << 24))
         return SSD_ERR_UNSUPPORTED;
     const int64_t ng = p->width / p->group_size;
-    const int64_t want = std::max<int64_t>(1, (4 * (int64_t)sm_count() + ng - 1) / ng);
+    const int64_t want = std::max<int64_t>(1, (2 * (int64_t)sm_count() + ng - 1) / ng);
     *chunks = std::max<int64_t>(1, std::min<int64_t>(p->rows, want));
     return SSD_OK;
 }
