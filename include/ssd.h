@@ -118,12 +118,14 @@ typedef struct {
 typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseqs;
     int32_t algo;        /* ssd_algo */
-    int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice, else 1..5
-                            (1..4 for the backward) */
+    int32_t seg_chunks;  /* fused path: chunks per work unit, 0 = library choice (for
+                            fixed-length batches a number of units per sequence that fills the
+                            last round of resident CTAs, units of 4-5 chunks, 3-4 for the
+                            backward's recompute), else 1..5 (1..4 for the backward) */
     int32_t bwd_heads;   /* tensor-core backward: heads per work item of the gradient kernel,
-                            0 = library choice (whole groups of up to 8 heads, with the last
-                            partial wave split into 2-head items), else a divisor of
-                            nheads/ngroups no larger than 32 (no split) */
+                            0 = library choice (whole groups of up to 8 heads, with the pairs of
+                            the last partial wave split into halves of a group), else a divisor
+                            of nheads/ngroups no larger than 32 (no split) */
     int32_t reserved0;   /* must be 0 */
 } ssd_problem;
 
