@@ -184,8 +184,8 @@ def test_bwd_rejects_five_chunk_units():
 @pytest.mark.parametrize("lens", [None, [1000, 3000, 1120]])
 def test_bwd_tail_split(lens):
     """More (chunk, group) pairs than SMs: the gradient kernel's last partial wave is split into
-    2-head items whose dB/dC shares are summed afterwards; packed sequences also leave work items
-    past the real chunk count, which are skipped."""
+    items of half a group whose dB/dC shares are summed afterwards; packed sequences also leave
+    work items past the real chunk count, which are skipped."""
     if lens is None:
         w = W(L=128 * 40, H=32, P=64, G=4, N=128, Q=128, dtype="bf16", has_z=True, has_init=True)
     else:
