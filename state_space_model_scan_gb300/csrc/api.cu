@@ -311,7 +311,7 @@ ssd_status plan_common(const ssd_problem *p, const ssd_fwd_args *a, bool bwd, Pl
                 // long: shorter ones measured slower (more carry-in folds and block ends in
                 // the serial chain of a sequence).
                 const int64_t U0 = (n + rmax - 1) / rmax;
-                const int64_t U1 = rmax > 1 ? (n + rmax - 2) / (rmax - 1) : n;
+                const int64_t U1 = rmax > 1 ? n / (rmax - 1) : n;   // n / U >= rmax - 1
                 int64_t bestU = U0;
                 for (int64_t U = U0; U <= U1 && U <= n; ++U) {
                     const int64_t rounds = (B * U * H + slots - 1) / slots;
