@@ -221,7 +221,7 @@ __device__ __forceinline__ void stage_taps(const float *w, const float *bias, in
 }
 
 template <typename T, int K, int W>   // W channels per thread (8: 256 threads, 4: 512 threads)
-__global__ void __launch_bounds__(CT * 8 / W)
+__global__ void __launch_bounds__(CT * 8 / W, 4)   // four blocks per SM (64 registers) measured 2-3% faster than three
 k_conv_fwd(const ConvArgs a) {
     constexpr int NPC = CB / W;        // channel pieces per row
     extern __shared__ __align__(16) uint8_t conv_sm[];
