@@ -252,6 +252,9 @@ def test_unit_schedule_balanced_units():
         assert u[2] == pos and u[3] == min(u[4] * 128, 128 * 64 - 5 - pos)
         pos += u[3]
     assert pos == 128 * 64 - 5
+    # the library's choice at 64 chunks and 64 heads on 152 SMs: 14 units of 5 or 4 tiles
+    m = meta.build(batch=1, seqlen=128 * 64, Q=128, R=5, KB=4, num=14, den=64)
+    assert [u[4] for u in sorted(m["units"], key=lambda r: r[6])] == [5] * 8 + [4] * 6
     # never fewer units than ceil(n/R), never more than n
     assert len(meta.build(batch=1, seqlen=640, Q=64, R=4, num=1, den=100)["units"]) == 3
     assert len(meta.build(batch=1, seqlen=640, Q=64, R=4, num=5, den=1)["units"]) == 10
